@@ -1,0 +1,70 @@
+"""Seeded synthetic inputs for the decode step.
+
+`synth.h` defines one counter-based generator (splitmix64 + an Irwin-Hall sum,
+rounded to BF16).  `libsynth.so` evaluates it on the host (for the oracle and
+the tests) or fills device buffers with it (for the GPU path).  The module holds
+no arithmetic of the decode step.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from .workloads import (MODELS, WORKLOADS, ModelShape, Workload, StepInputs, make_inputs,  # noqa: F401
+                        step_kv_bytes, seq_lens_for, block_tables_for, tokens_for,
+                        zipf_router_bias)
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libsynth.so")
+
+EMB, WQKV, WO, WR, WG, WU, WD, WLM, KPOOL, VPOOL = range(1, 11)
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            from .build import build
+            build()
+        L = ctypes.CDLL(LIB_PATH)
+        u64, u32 = ctypes.c_uint64, ctypes.c_uint32
+        L.synth_fill_device.restype = ctypes.c_int
+        L.synth_fill_device.argtypes = [ctypes.c_void_p, u64, u64, u64, u32, u32, u32, ctypes.c_int,
+                                        ctypes.c_double, ctypes.c_void_p]
+        L.synth_fill_host.restype = None
+        L.synth_fill_host.argtypes = [ctypes.c_void_p, u64, u64, u64, u32, u32, u32, ctypes.c_int,
+                                      ctypes.c_double]
+        L.synth_raw.restype = u64
+        L.synth_raw.argtypes = [u64, u64]
+        _lib = L
+    return _lib
+
+
+def fill_host(n_streams: int, per_stream: int, seed: int, kind: int, layer0: int = 0,
+              expert0: int = 0, vary_layer: bool = False, sigma: float = 0.02) -> np.ndarray:
+    """uint16 BF16 bit patterns, shape [n_streams, per_stream]."""
+    out = np.empty((n_streams, per_stream), dtype=np.uint16)
+    lib().synth_fill_host(out.ctypes.data, n_streams, per_stream, seed, kind, layer0, expert0,
+                          int(vary_layer), sigma)
+    return out
+
+
+def fill_device(ptr: int, n_streams: int, per_stream: int, seed: int, kind: int, layer0: int = 0,
+                expert0: int = 0, vary_layer: bool = False, sigma: float = 0.02,
+                stream: int = 0) -> None:
+    rc = lib().synth_fill_device(ptr, n_streams, per_stream, seed, kind, layer0, expert0,
+                                 int(vary_layer), sigma, stream)
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_device failed with CUDA error {rc}")
+
+
+def raw(key: int, idx: int) -> int:
+    return int(lib().synth_raw(key, idx))
+
+
+def bf16_bits_to_f32(a: np.ndarray) -> np.ndarray:
+    return (a.astype(np.uint32) << 16).view(np.float32)

@@ -1,0 +1,116 @@
+/*
+ * synth.h -- seeded, counter-based generator for the synthetic inputs of a
+ * decode step (random-init BF16 weights and a random BF16 KV cache).
+ *
+ * This header is the one piece of code that both the CPU oracle and the GPU
+ * input-fill kernel compile.  It holds no arithmetic of the decode step
+ * itself: it only maps (seed, stream, index) to a BF16 bit pattern, so that
+ * either side can regenerate any element of any tensor on demand.
+ *
+ * Definition (everything below is exact integer arithmetic plus one IEEE-754
+ * binary32 multiply, so host and device produce identical bits):
+ *
+ *   mix(z)       = splitmix64 output function (Steele, Lea, Flood,
+ *                  "Fast splittable pseudorandom number generators",
+ *                  OOPSLA 2014): z ^= z>>30; z *= 0xbf58476d1ce4e5b9;
+ *                  z ^= z>>27; z *= 0x94d049bb133111eb; z ^= z>>31.
+ *   key(seed,s)  = mix(seed * G + mix(s + 0x632be59bd9b4e019)),
+ *                  G = 0x9e3779b97f4a7c15 (the splitmix64 increment).
+ *   draw(key,i)  = mix(key + (i+1)*G), i.e. the (i+1)-th splitmix64 output
+ *                  of a generator whose state starts at key.
+ *   ih4(r)       = sum of the four 16-bit fields of r minus 131070: an
+ *                  Irwin-Hall sum of four discrete uniforms, mean 0,
+ *                  standard deviation sqrt((65536^2-1)/3) = 37837.2265...
+ *   value        = bf16_rne( (float)ih4(draw(key,i)) * scale ),
+ *                  scale = (float)(sigma / 37837.2265...) rounded once.
+ *
+ * The values are bounded by +-3.46 sigma and have the first two moments of
+ * N(0, sigma^2); the decode step's inputs only need "random BF16 of scale
+ * sigma", not exact Gaussian tails.
+ */
+#ifndef SYNTH_H
+#define SYNTH_H
+
+#include <stdint.h>
+#include <string.h>
+
+#if defined(__CUDACC__)
+#define SYNTH_FN static __host__ __device__ __forceinline__
+#else
+#define SYNTH_FN static inline
+#endif
+
+#define SYNTH_GOLDEN 0x9e3779b97f4a7c15ULL
+#define SYNTH_IH4_STD 37837.22651061575 /* sqrt((65536^2 - 1) / 3) */
+
+/* Tensor kinds: the stream id of a tensor is (kind, layer, expert). */
+enum {
+  SYNTH_EMB = 1,   /* token embedding [V][H]                    */
+  SYNTH_WQKV = 2,  /* fused q|k|v projection [(nq+2nkv)d][H]     */
+  SYNTH_WO = 3,    /* output projection [H][nq d]               */
+  SYNTH_WR = 4,    /* router [E][H]                             */
+  SYNTH_WG = 5,    /* expert gate [I][H]                        */
+  SYNTH_WU = 6,    /* expert up [I][H]                          */
+  SYNTH_WD = 7,    /* expert down [H][I]                        */
+  SYNTH_WLM = 8,   /* LM head [V][H]                            */
+  SYNTH_KPOOL = 9, /* K pool of one layer [pages][nkv][P][d]    */
+  SYNTH_VPOOL = 10 /* V pool of one layer [pages][nkv][P][d]    */
+};
+
+SYNTH_FN uint64_t synth_mix64(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ULL;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebULL;
+  return z ^ (z >> 31);
+}
+
+SYNTH_FN uint64_t synth_stream(uint32_t kind, uint32_t layer, uint32_t expert) {
+  return ((uint64_t)kind << 48) | ((uint64_t)(layer & 0xffffffu) << 24) | (uint64_t)(expert & 0xffffffu);
+}
+
+SYNTH_FN uint64_t synth_key(uint64_t seed, uint64_t stream) {
+  return synth_mix64(seed * SYNTH_GOLDEN + synth_mix64(stream + 0x632be59bd9b4e019ULL));
+}
+
+SYNTH_FN uint64_t synth_draw(uint64_t key, uint64_t idx) {
+  return synth_mix64(key + (idx + 1) * SYNTH_GOLDEN);
+}
+
+SYNTH_FN int32_t synth_ih4(uint64_t r) {
+  return (int32_t)(r & 0xffffu) + (int32_t)((r >> 16) & 0xffffu) +
+         (int32_t)((r >> 32) & 0xffffu) + (int32_t)((r >> 48) & 0xffffu) - 131070;
+}
+
+SYNTH_FN uint16_t synth_f32_to_bf16_rne(float f) {
+  uint32_t u;
+#if defined(__CUDA_ARCH__)
+  u = __float_as_uint(f);
+#else
+  memcpy(&u, &f, sizeof u);
+#endif
+  /* no NaN or Inf can reach here: |f| <= 131070 * scale */
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+/* One element: the bf16 bit pattern of element idx of stream key. */
+SYNTH_FN uint16_t synth_bf16(uint64_t key, uint64_t idx, float scale) {
+  float v = (float)synth_ih4(synth_draw(key, idx)) * scale;
+  return synth_f32_to_bf16_rne(v);
+}
+
+/* The one rounding of sigma into the per-tensor scale (IEEE double divide,
+ * then round-to-nearest-even to binary32), identical on every host. */
+SYNTH_FN float synth_scale(double sigma) { return (float)(sigma / SYNTH_IH4_STD); }
+
+SYNTH_FN float synth_bf16_to_f32(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+#if defined(__CUDA_ARCH__)
+  f = __uint_as_float(u);
+#else
+  memcpy(&f, &u, sizeof f);
+#endif
+  return f;
+}
+
+#endif /* SYNTH_H */
