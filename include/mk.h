@@ -1,0 +1,188 @@
+/*
+ * mk.h -- C ABI of the GB300 (sm_103a) decode megakernel.
+ *
+ * One decode step of a parallel-attention / MoE transformer runs as a single
+ * persistent kernel: one CTA per SM walks a host-built list of fixed-size
+ * task descriptors, synchronises with other SMs only through counters in
+ * global memory, and pulls runtime-sized work (full-attention KV slices, MoE
+ * expert tiles) from shared work queues.  This follows "Cohere: a decode
+ * megakernel for North Mini Code" (sections "What is a Megakernel?", "The
+ * task descriptor", "Barriers", "Task scheduler"), re-designed for GB300.
+ *
+ * Conventions for every entry point:
+ *  - All device memory is allocated by the caller and passed as plain
+ *    pointers; the library never allocates device memory.  Host handles
+ *    (mk_model, mk_sched) are allocated by the library and freed with
+ *    mk_free_model / mk_free_sched.
+ *  - Functions return MK_OK (0) or a negative MK_ERR_* code; mk_last_error()
+ *    then returns a message (thread-local, valid until the next call).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - BF16 tensors are raw uint16 bit patterns of bfloat16.
+ *  - There is no CPU fallback: without a GB300 the compute entry points return
+ *    MK_ERR_CUDA.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MK_OK 0
+#define MK_ERR_ARG (-1)         /* a bad argument; nothing was launched */
+#define MK_ERR_CUDA (-2)        /* a CUDA runtime call failed */
+#define MK_ERR_TIMEOUT (-3)     /* a device-side wait gave up (watchdog) */
+#define MK_ERR_UNSUPPORTED (-4) /* no compiled kernel for this model shape */
+#define MK_ERR_DEVICE (-5)      /* a device-side check failed (e.g. page id out of range) */
+
+/* Model shape.  Layer l attends to its whole context iff window == 0 or
+ * (l + 1) % full_period == 0; otherwise to the last `window` positions.
+ * The compiled kernels cover three shapes (hidden, n_q, n_kv, head_dim,
+ * n_experts, top_k, inter, page_size): (256,4,2,64,16,4,128,16),
+ * (1024,16,2,64,32,4,512,64) and (2048,32,4,128,128,8,768,64); n_layers,
+ * vocab, window and full_period are free. */
+typedef struct {
+  int32_t n_layers, hidden, n_q, n_kv, head_dim, n_experts, top_k, inter, vocab;
+  int32_t page_size, window, full_period;
+  float rope_base, eps;
+} mk_config;
+
+/* Device pointers to the weights, row-major with the output dimension first
+ * ([out][in], the layout of a linear layer's weight).  Stacked over layers
+ * (and experts) with no padding.  The library keeps the pointers; the
+ * caller keeps the memory alive and unchanged while the model is in use. */
+typedef struct {
+  const void* embedding;   /* bf16 [vocab][hidden] */
+  const void* w_qkv;       /* bf16 [L][(n_q + 2 n_kv) head_dim][hidden]: q heads, k heads, v heads */
+  const void* w_o;         /* bf16 [L][hidden][n_q head_dim] */
+  const void* w_router;    /* bf16 [L][n_experts][hidden] */
+  const float* router_bias;/* fp32 [n_experts] added to every layer's router logits, or NULL */
+  const void* w_gate;      /* bf16 [L][n_experts][inter][hidden] */
+  const void* w_up;        /* bf16 [L][n_experts][inter][hidden] */
+  const void* w_down;      /* bf16 [L][n_experts][hidden][inter] */
+  const float* norm_gamma; /* fp32 [L][hidden] input RMSNorm gain of each layer */
+  const float* final_gamma;/* fp32 [hidden] final RMSNorm gain */
+  const void* w_lm;        /* bf16 [vocab][hidden] */
+} mk_weights;
+
+typedef struct mk_model mk_model;
+typedef struct mk_sched mk_sched;
+
+/* Validates the shape against the compiled kernels and records the weight
+ * pointers (the [out][in] layout is already tile-contiguous for the row
+ * tiles the kernel streams, so nothing is repacked).  Host only. */
+int mk_load_model(const mk_config* cfg, const mk_weights* w, mk_model** out);
+void mk_free_model(mk_model* m);
+
+/* Wave orders of one layer ("Task scheduler: mapping tasks to SMs"):
+ * DEFAULT     qkv, router, top-k, route setup, gather, attention (+combine),
+ *             MoE up/down, O-proj, RMSNorm;
+ * INTERLEAVED attention, MoE up/down, attention combine, MoE combine,
+ *             O-proj, RMSNorm;
+ * ATTN_FIRST  attention, attention combine, O-proj, MoE up/down, MoE
+ *             combine, RMSNorm. */
+#define MK_WAVES_DEFAULT 0
+#define MK_WAVES_INTERLEAVED 1
+#define MK_WAVES_ATTN_FIRST 2
+
+typedef struct {
+  int32_t num_sms;          /* SMs to schedule for; 0 = the current device's count */
+  int32_t wave_order;       /* MK_WAVES_* */
+  int32_t attn_split_pages; /* KV pages per attention task; 0 = choose from the context */
+  int32_t attn_claimers;    /* ATTN_DRAIN claimers per full-attention layer; 0 = auto */
+  int32_t moe_claimers;     /* claimers per MoE drain per layer; 0 = auto */
+  int32_t qkv_tile_rows;    /* output rows per QKV task; 0 = auto */
+  int32_t o_tile_rows;      /* output rows per O-proj task (per KV group); 0 = auto */
+  int32_t lm_tile_rows;     /* vocab rows per LM-head task; 0 = auto */
+  int32_t fuse_finalize;    /* 1: the (single) top-k task also builds the MoE queue */
+  int32_t fuse_moe_combine; /* 1: the residual RMSNorm also does the MoE combine */
+  int32_t explicit_gather;  /* 1: MOE_GATHER materialises expert-ordered rows */
+  int32_t trace_hidden;     /* 1: keep the residual entering every layer in the workspace */
+  int32_t watchdog_ms;      /* device-side wait limit; 0 = 2000 ms */
+} mk_sched_opts;
+
+/* Fills opts with the defaults (all zero except fuse_* = 1). */
+void mk_default_sched_opts(mk_sched_opts* opts);
+
+/* Builds and validates the per-SM task lists for steps with batch <=
+ * max_batch and every seq_len <= max_ctx ("Task scheduler": the list is
+ * built on the host once and reused by every step).  Host only; no device
+ * call unless opts->num_sms == 0.  max_batch <= 64. */
+int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx,
+                   const mk_sched_opts* opts, mk_sched** out);
+void mk_free_sched(mk_sched* s);
+
+/* Bytes of the device copy of the task lists, and the upload into a
+ * caller-allocated buffer of that size (16-byte aligned). */
+size_t mk_sched_bytes(const mk_sched* s);
+int mk_sched_upload(mk_sched* s, void* sched_dev, size_t bytes, void* stream);
+
+/* Bytes of device scratch one step needs (barriers, activations, queues). */
+size_t mk_workspace_bytes(const mk_sched* s);
+
+/* One decode step ("What is a Megakernel?": one launch per step).
+ *  last_tokens   device int32 [batch]: the token decoded at this step
+ *  seq_lens      device int32 [batch]: sequence length including that token,
+ *                1 <= seq_len <= max_ctx; the new K/V go to position seq_len-1
+ *  block_tables  device int32 [batch][max_pages]: physical page of logical
+ *                page j of row b; pages for positions < seq_len must exist
+ *  k_pool,v_pool device bf16 [n_layers][num_pages][n_kv][page_size][head_dim];
+ *                the step writes the new token's K and V into them
+ *  workspace     device, mk_workspace_bytes(s) bytes, 256-byte aligned
+ *  logits        device fp32 [batch][vocab]
+ * Asynchronous on `stream` (one memset and one cooperative launch; the host
+ * never waits).  MK_ERR_ARG for a bad shape or pointer (nothing launched).
+ * Values are checked on the device: a seq_len, token or page id out of
+ * range, or a watchdog timeout, is reported by mk_check_step. */
+int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens,
+                   const int32_t* seq_lens, const int32_t* block_tables, int32_t batch,
+                   int32_t max_pages, void* k_pool, void* v_pool, int64_t num_pages,
+                   void* workspace, size_t workspace_bytes, float* logits, void* stream);
+
+/* Waits for `stream`, then reads the step's device error record: MK_OK,
+ * MK_ERR_TIMEOUT or MK_ERR_DEVICE (details in mk_last_error()). */
+int mk_check_step(const mk_sched* s, const void* workspace, void* stream);
+
+const char* mk_last_error(void);
+
+/* ---- inspection (tests, tracing) ---- */
+
+/* Byte offsets of named regions inside the workspace (-1 if absent):
+ * "topk_ids" int32 [L][B][k], "topk_w" fp32 [L][B][k], "router_logits"
+ * fp32 [L][B][E], "expert_count" int32 [L][E], "moe_queue" int32 entries
+ * (last layer), "moe_down_queue" int32, "moe_queue_len" int32 [2] (up, down),
+ * "perm" int32 [B*k] (last layer), "hidden_trace" fp32 [L+1][B][H],
+ * "error" uint32 [8], "barriers" uint32, and the activations "h", "x", "q",
+ * "kvnew", "attn_out", "opart", "u", "y", "moe_out" of the last layer. */
+int64_t mk_workspace_offset(const mk_sched* s, const char* name);
+
+/* Task list access for tests: counts, a copy of one descriptor (32 int32),
+ * and replacement of one descriptor (host copy only; re-upload after). */
+int32_t mk_sched_num_sms(const mk_sched* s);
+int32_t mk_sched_num_tasks(const mk_sched* s, int32_t sm);
+int mk_sched_get_task(const mk_sched* s, int32_t sm, int32_t idx, int32_t desc[32]);
+int mk_sched_set_task(mk_sched* s, int32_t sm, int32_t idx, const int32_t desc[32]);
+int32_t mk_sched_num_barriers(const mk_sched* s);
+
+/* Static validation of the lists: every waited-on barrier is signalled by
+ * enough tasks that come earlier in the global order, static barriers
+ * receive exactly their target, claimers precede what waits on them.
+ * Returns MK_OK or MK_ERR_ARG with the first violation in mk_last_error(). */
+int mk_sched_validate(const mk_sched* s);
+
+/* Host simulation of the lists as the device runs them (in order per SM,
+ * waits on counters, claimers draining queues) for a given batch, host
+ * seq_lens and routing (int32 [L][batch][k], or NULL for a seeded uniform
+ * routing).  Returns MK_OK if every task finishes and every barrier ends at
+ * exactly its target, MK_ERR_ARG (deadlock or miscount, described in
+ * mk_last_error()) otherwise. */
+int mk_sched_simulate(const mk_sched* s, int32_t batch, const int32_t* seq_lens,
+                      const int32_t* routing, uint64_t seed);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H */

@@ -1,0 +1,234 @@
+// mk_api.cpp -- the C ABI: model and schedule handles, upload, the decode
+// step launch and its error check.
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <string>
+
+#include "mk_host.h"
+
+namespace mk {
+
+namespace {
+thread_local std::string g_error;
+}
+
+void set_error(const std::string& msg) { g_error = msg; }
+
+int fail(int code, const std::string& msg) {
+  g_error = msg;
+  return code;
+}
+
+int query_num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  return n;
+}
+
+int launch_tiny(const Params& p, int grid, cudaStream_t s);
+int launch_small(const Params& p, int grid, cudaStream_t s);
+int launch_full(const Params& p, int grid, cudaStream_t s);
+
+namespace {
+
+struct CompiledShape {
+  ShapeDims dims;
+  int (*launch)(const Params&, int, cudaStream_t);
+};
+
+const CompiledShape kShapes[] = {
+    {{256, 4, 2, 64, 16, 4, 128, 16}, launch_tiny},
+    {{1024, 16, 2, 64, 32, 4, 512, 64}, launch_small},
+    {{2048, 32, 4, 128, 128, 8, 768, 64}, launch_full},
+};
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(MK_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+}  // namespace
+}  // namespace mk
+
+using namespace mk;
+
+extern "C" {
+
+const char* mk_last_error(void) { return g_error.c_str(); }
+
+int mk_load_model(const mk_config* cfg, const mk_weights* w, mk_model** out) {
+  if (!cfg || !w || !out) return fail(MK_ERR_ARG, "null argument");
+  *out = nullptr;
+  const mk_config& c = *cfg;
+  if (c.n_layers < 1 || c.vocab < 1 || c.window < 0 || c.full_period < 1 || !(c.rope_base > 0.f) ||
+      !(c.eps >= 0.f))
+    return fail(MK_ERR_ARG, "invalid config (layers, vocab, window, full_period, rope_base or eps)");
+  int id = -1;
+  for (int i = 0; i < (int)(sizeof(kShapes) / sizeof(kShapes[0])); ++i) {
+    const ShapeDims& d = kShapes[i].dims;
+    if (d.H == c.hidden && d.NQ == c.n_q && d.NKV == c.n_kv && d.D == c.head_dim && d.E == c.n_experts &&
+        d.K == c.top_k && d.I == c.inter && d.P == c.page_size)
+      id = i;
+  }
+  if (id < 0) return fail(MK_ERR_UNSUPPORTED, "no compiled kernel for this model shape");
+  if (!w->embedding || !w->w_qkv || !w->w_o || !w->w_router || !w->w_gate || !w->w_up || !w->w_down ||
+      !w->norm_gamma || !w->final_gamma || !w->w_lm)
+    return fail(MK_ERR_ARG, "a weight pointer is null");
+  mk_model* m = new mk_model();
+  m->cfg = c;
+  m->w = *w;
+  m->shape_id = id;
+  m->dims = kShapes[id].dims;
+  m->plan = moe_plan(m->dims);
+  *out = m;
+  return MK_OK;
+}
+
+void mk_free_model(mk_model* m) { delete m; }
+
+int mk_sched_upload(mk_sched* s, void* dev, size_t bytes, void* stream) {
+  if (!s || !dev) return fail(MK_ERR_ARG, "null argument");
+  if (bytes < mk_sched_bytes(s)) return fail(MK_ERR_ARG, "sched buffer too small");
+  if (reinterpret_cast<uintptr_t>(dev) & 127u) return fail(MK_ERR_ARG, "sched buffer must be 128-byte aligned");
+  // [num_sms][2] (offset, count) header, then each SM's descriptors
+  const int nsm = s->num_sms;
+  size_t off = ((size_t)2 * nsm + 31) / 32 * 32;
+  s->upload.assign(off + 32 * s->tasks.size(), 0);
+  for (int sm = 0; sm < nsm; ++sm) {
+    s->upload[2 * sm] = (int32_t)off;
+    s->upload[2 * sm + 1] = (int32_t)s->per_sm[sm].size();
+    for (int t : s->per_sm[sm]) {
+      std::memcpy(&s->upload[off], s->tasks[t].data(), sizeof(int32_t) * 32);
+      off += 32;
+    }
+  }
+  cudaError_t e = cudaMemcpyAsync(dev, s->upload.data(), sizeof(int32_t) * s->upload.size(),
+                                  cudaMemcpyHostToDevice, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "upload of the task lists");
+  s->sched_dev = dev;
+  return MK_OK;
+}
+
+int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const int32_t* seq_lens,
+                   const int32_t* block_tables, int32_t batch, int32_t max_pages, void* k_pool,
+                   void* v_pool, int64_t num_pages, void* workspace, size_t workspace_bytes,
+                   float* logits, void* stream) {
+  if (!m || !s) return fail(MK_ERR_ARG, "null model or schedule");
+  if (!s->sched_dev) return fail(MK_ERR_ARG, "schedule not uploaded");
+  if (std::memcmp(&m->cfg, &s->cfg, sizeof(mk_config)) != 0)
+    return fail(MK_ERR_ARG, "schedule was built for another model");
+  if (batch < 1 || batch > s->max_batch) return fail(MK_ERR_ARG, "batch outside [1, max_batch]");
+  if (!last_tokens || !seq_lens || !block_tables || !k_pool || !v_pool || !workspace || !logits)
+    return fail(MK_ERR_ARG, "null device pointer");
+  if (max_pages < 1 || num_pages < 1) return fail(MK_ERR_ARG, "max_pages and num_pages must be positive");
+  if (workspace_bytes < s->ws.total) return fail(MK_ERR_ARG, "workspace too small");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(MK_ERR_ARG, "workspace must be 256-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool)) & 15u)
+    return fail(MK_ERR_ARG, "KV pools must be 16-byte aligned");
+
+  const ShapeDims& D = s->dims;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto at = [&](const char* name) -> uint8_t* {
+    const size_t o = s->ws.off(name);
+    return o == (size_t)-1 ? nullptr : ws + o;
+  };
+  Params p{};
+  const mk_weights& w = m->w;
+  p.emb = static_cast<const uint16_t*>(w.embedding);
+  p.wqkv = static_cast<const uint16_t*>(w.w_qkv);
+  p.wo = static_cast<const uint16_t*>(w.w_o);
+  p.wr = static_cast<const uint16_t*>(w.w_router);
+  p.rbias = w.router_bias;
+  p.wg = static_cast<const uint16_t*>(w.w_gate);
+  p.wu = static_cast<const uint16_t*>(w.w_up);
+  p.wd = static_cast<const uint16_t*>(w.w_down);
+  p.gamma = w.norm_gamma;
+  p.gamma_f = w.final_gamma;
+  p.wlm = static_cast<const uint16_t*>(w.w_lm);
+  p.L = m->cfg.n_layers;
+  p.V = m->cfg.vocab;
+  p.window = m->cfg.window;
+  p.full_period = m->cfg.full_period;
+  p.rope_base = m->cfg.rope_base;
+  p.eps = m->cfg.eps;
+  p.B = batch;
+  p.MB = s->max_batch;
+  p.tokens = last_tokens;
+  p.block_tables = block_tables;
+  p.max_pages = max_pages;
+  p.kpool = static_cast<uint16_t*>(k_pool);
+  p.vpool = static_cast<uint16_t*>(v_pool);
+  p.num_pages = num_pages;
+  p.logits = logits;
+  p.sched = static_cast<const int32_t*>(s->sched_dev);
+  p.bars = reinterpret_cast<uint32_t*>(at("barriers"));
+  p.err = reinterpret_cast<uint32_t*>(at("error"));
+  p.seq_lens = seq_lens;
+  p.max_ctx = s->max_ctx;
+  p.h = reinterpret_cast<float*>(at("h"));
+  p.x = reinterpret_cast<uint16_t*>(at("x"));
+  p.q = reinterpret_cast<float*>(at("q"));
+  p.kvnew = reinterpret_cast<uint16_t*>(at("kvnew"));
+  p.part_o = reinterpret_cast<float*>(at("part_o"));
+  p.part_ml = reinterpret_cast<float*>(at("part_ml"));
+  p.attn_out = reinterpret_cast<uint16_t*>(at("attn_out"));
+  p.opart = reinterpret_cast<float*>(at("opart"));
+  p.rlog = reinterpret_cast<float*>(at("router_logits"));
+  p.topk_ids = reinterpret_cast<int32_t*>(at("topk_ids"));
+  p.topk_w = reinterpret_cast<float*>(at("topk_w"));
+  p.ecount = reinterpret_cast<int32_t*>(at("expert_count"));
+  p.eoff = reinterpret_cast<int32_t*>(at("expert_offset"));
+  p.perm = reinterpret_cast<int32_t*>(at("perm"));
+  p.inv = reinterpret_cast<int32_t*>(at("inv"));
+  p.upq = reinterpret_cast<int32_t*>(at("moe_queue"));
+  p.dnq = reinterpret_cast<int32_t*>(at("moe_down_queue"));
+  p.qlen = reinterpret_cast<int32_t*>(at("moe_queue_len"));
+  p.xg = reinterpret_cast<uint16_t*>(at("xg"));
+  p.u = reinterpret_cast<uint16_t*>(at("u"));
+  p.y = reinterpret_cast<float*>(at("y"));
+  p.moe_out = reinterpret_cast<float*>(at("moe_out"));
+  p.htrace = reinterpret_cast<float*>(at("hidden_trace"));
+  p.split_len = s->split_len;
+  p.n_static = s->n_static;
+  p.max_slots = s->max_slots;
+  p.explicit_gather = s->opts.explicit_gather;
+  p.watchdog_ns = s->watchdog_ns;
+  (void)D;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // "Barriers": the counters are zeroed before each step (with the error record)
+  const size_t zero_bytes = s->ws.off("error") + sizeof(uint32_t) * 8;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, zero_bytes, st);
+  if (e != cudaSuccess) return cuda_fail(e, "barrier reset");
+  const int rc = kShapes[m->shape_id].launch(p, s->num_sms, st);
+  if (rc != 0) return cuda_fail((cudaError_t)rc, "megakernel launch");
+  return MK_OK;
+}
+
+int mk_check_step(const mk_sched* s, const void* workspace, void* stream) {
+  if (!s || !workspace) return fail(MK_ERR_ARG, "null argument");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t rec[8];
+  cudaError_t e = cudaMemcpyAsync(rec, static_cast<const uint8_t*>(workspace) + s->ws.off("error"), sizeof rec,
+                                  cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "step");
+  if (rec[0] == 0) return MK_OK;
+  const std::string where = " (sm " + std::to_string(rec[1]) + ", task " + std::to_string((int32_t)rec[2]) +
+                            ", op " + std::to_string((int32_t)rec[6]) + ", layer " +
+                            std::to_string((int32_t)rec[7]) + ", index " + std::to_string((int32_t)rec[3]) +
+                            ", value " + std::to_string((int32_t)rec[4]) + ", limit " +
+                            std::to_string((int32_t)rec[5]) + ")";
+  if (rec[0] == 1) return fail(MK_ERR_TIMEOUT, "device wait timed out" + where);
+  if (rec[0] == 2) return fail(MK_ERR_DEVICE, "page id out of range" + where);
+  return fail(MK_ERR_DEVICE, "index out of range" + where);
+}
+
+}  // extern "C"

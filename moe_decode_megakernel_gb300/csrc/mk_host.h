@@ -1,0 +1,79 @@
+// mk_host.h -- host-side objects behind the C ABI handles.
+#pragma once
+
+#include <array>
+#include <string>
+#include <vector>
+
+#include "../../include/mk.h"
+#include "mk_internal.h"
+
+struct mk_model {
+  mk_config cfg;
+  mk_weights w;
+  int shape_id;  // index into the compiled shapes
+  mk::ShapeDims dims;
+  mk::MoePlan plan;
+};
+
+namespace mk {
+
+using Desc = std::array<int32_t, 32>;
+
+// What a barrier counts, for validation and simulation.
+enum BarKind : int8_t {
+  BK_STATIC = 0,   // +1 per signalling task; waited on with a fixed count
+  BK_UP_EXPERT,    // +1 per up/gate tile of one expert (count fixed per expert)
+  BK_ATTN_COUNT,   // +1 per KV slice of one (row, group)
+  BK_CLAIM,        // a claim counter (atomicAdd), never waited on
+};
+
+struct WsLayout {
+  size_t total = 0;
+  std::vector<std::pair<std::string, size_t>> regions;  // name -> byte offset
+  size_t off(const char* name) const;
+  size_t add(const char* name, size_t bytes);
+};
+
+// Barrier indices of one layer (or -1 where absent).
+struct LayerBars {
+  int norm = -1, router = -1, topk = -1, fin = -1, gather = -1, o = -1, mcomb = -1;
+  int upd = -1, dnd = -1, attn_done = -1;
+  int claim_attn = -1, claim_up = -1, claim_dn = -1;
+  int qkv = -1;    // base, n_kv entries
+  int acomb = -1;  // base, n_kv entries
+  int cnt = -1;    // base, MB * n_kv entries
+  int up = -1;     // base, n_experts entries
+  // task counts behind the static targets
+  int n_norm = 0, n_router = 0, n_topk = 0, n_gather = 0, n_o = 0, n_mcomb = 0;
+  int n_up_claim = 0, n_dn_claim = 0, n_attn_claim = 0;
+  std::vector<int> n_qkv_g, n_acomb_g;
+};
+
+}  // namespace mk
+
+struct mk_sched {
+  mk_config cfg;
+  mk::ShapeDims dims;
+  mk::MoePlan plan;
+  mk_sched_opts opts;
+  int num_sms = 0, max_batch = 0, max_ctx = 0;
+  int split_len = 0, n_static = 0, max_slots = 0, max_attn_entries = 0;
+  int lm_bar = -1;
+  std::vector<mk::Desc> tasks;              // global order
+  std::vector<std::vector<int>> per_sm;     // task indices in execution order
+  std::vector<int8_t> bar_kind;
+  std::vector<mk::LayerBars> lb;            // [L + 1]
+  mk::WsLayout ws;
+  std::vector<int32_t> upload;              // host image of the device task lists
+  const void* sched_dev = nullptr;          // uploaded lists
+  int64_t watchdog_ns = 0;
+};
+
+namespace mk {
+void set_error(const std::string& msg);
+int fail(int code, const std::string& msg);
+int attn_slices(const mk_sched* s, int seq_len);  // KV slices of a full-attention row
+int query_num_sms();                              // SMs of the current device, -1 without one
+bool is_full_layer(const mk_config& c, int l);
+}  // namespace mk

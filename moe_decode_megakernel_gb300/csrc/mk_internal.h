@@ -1,0 +1,184 @@
+// mk_internal.h -- definitions shared by the host scheduler and the device
+// kernel: opcodes, the 32 x int32 task descriptor, stage geometry, and the
+// kernel's parameter block.
+#pragma once
+
+#include <stdint.h>
+
+namespace mk {
+
+// ---------------------------------------------------------------- opcodes
+// The sixteen operations of one decode step ("Cohere: a decode megakernel
+// for North Mini Code", section "Tasks"), plus the no-op.
+enum Op : int32_t {
+  OP_NOP = 0,
+  OP_RESID_NORM = 1,        // residual add (+ MoE combine) + RMSNorm; embedding at layer 0
+  OP_QKV_PROJ = 2,          // one row tile of x W_qkv, RoPE + KV append in the epilogue
+  OP_O_PROJ = 3,            // one row tile of attn W_o over one KV group's columns (split-K)
+  OP_FFN_UPGATE_ACT = 4,    // dense SwiGLU up/gate (dense-layer models; reserved)
+  OP_FFN_DOWN = 5,          // dense down projection (reserved)
+  OP_LM_HEAD = 6,           // one vocab tile of the LM head
+  OP_ATTN_DECODE = 7,       // one static KV slice of one (row, KV group)
+  OP_ATTN_COMBINE = 8,      // merge of the slice partials of one (row, KV group)
+  OP_ATTN_DRAIN = 9,        // claimer over the full-attention queue
+  OP_ROUTER_GEMM = 10,      // router logits for a tile of experts
+  OP_ROUTER_TOPK = 11,      // top-k experts and weights of a range of rows
+  OP_ROUTE_FINALIZE = 12,   // per-expert counts, offsets, row order and the MoE queues
+  OP_MOE_GATHER = 13,       // expert-ordered copy of the routed rows
+  OP_MOE_UPGATE_ACT_DRAIN = 14,  // claimer over the up/gate tile queue
+  OP_MOE_DOWN_DRAIN = 15,   // claimer over the down tile queue
+  OP_MOE_COMBINE = 16,      // weighted sum of each row's expert outputs
+  OP_COUNT = 17,
+  // work items made by the producer warp from claimer tasks (never in a list)
+  W_ATTN = 32,      // one KV slice (from ATTN_DECODE or ATTN_DRAIN)
+  W_UP_TILE = 33,   // one claimed up/gate tile
+  W_DOWN_TILE = 34, // one claimed down tile
+  W_CLAIM_END = 35, // a claimer found its queue empty: signal completion
+  W_EXIT = 36,      // end of this SM's list
+};
+
+// ------------------------------------------------------ task descriptor
+// "The task descriptor": 32 int32, field 0 the opcode, then the layer, the
+// barriers to wait on with their counts, the barriers to signal, and the
+// op-specific fields.
+enum Field : int {
+  F_OP = 0,
+  F_LAYER = 1,
+  F_WAIT0 = 2,  // barrier index or -1
+  F_TGT0 = 3,   // count to wait for (TGT_DYN_SPLITS: the row's number of KV slices)
+  F_WAIT1 = 4,
+  F_TGT1 = 5,
+  F_SIG0 = 6,   // barrier incremented when the task (or tile) is done, or -1
+  F_SIG1 = 7,
+  F_A0 = 8,     // op-specific arguments F_A0 .. F_A0 + 15
+  F_TASK = 24,  // global index of the task (error reports, tracing)
+  F_NSTAGE = 25,  // work items: shared-memory stages that belong to the item
+  F_DESC_INTS = 32,
+};
+constexpr int32_t TGT_DYN_SPLITS = -2;
+
+// op-specific argument slots
+// RESID_NORM:   A0 b0, A1 b1 (row range), A2 final (1 = final norm before the LM head)
+//               A3 fused MoE combine of the previous layer
+// dense GEMV:   A0 row0, A1 n_rows, A2 KV group (O_PROJ split-K slice)
+// ATTN_DECODE:  A0 b, A1 g, A2 slice index within the window, A3 counter base
+// ATTN_DRAIN:   A0 claim counter, A1 counter base, A2 QKV barrier base, A3 QKV target
+// ATTN_COMBINE: A0 b, A1 g, A2 counter base
+// ROUTER_TOPK:  A0 b0, A1 b1, A2 1 = also finalize (single top-k task)
+// MOE_GATHER:   A0 row0, A1 n_rows
+// MOE_*_DRAIN:  A0 claim counter, A1 up barrier base (per expert), A2 explicit-gather barrier
+//               (or -1), A3 its target
+// MOE_COMBINE:  A0 b0, A1 b1
+// W_ATTN:       A0 b, A1 g, A2 t0, A3 t1, A4 first page, A5 partial slot
+// W_UP_TILE / W_DOWN_TILE: A0 expert, A1 tile index, A2 row0, A3 n_rows
+
+// ------------------------------------------------------- stage geometry
+constexpr int kStageBytes = 32768;   // one shared-memory stage
+constexpr int kStages = 6;           // stage ring depth (192 KB)
+constexpr int kDescRing = 4;         // descriptor ring (controller -> producer)
+constexpr int kWorkRing = 8;         // work-item ring (producer -> consumers)
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (2 + kConsumerWarps);  // controller, producer, consumers
+constexpr int kTB = 4;               // activation rows per GEMV pass
+constexpr int kMaxStageRows = 64;
+constexpr int kMaxBatch = 64;
+
+// Rows of a [rows][k] bf16 matrix that fit one stage, a multiple of 8, at most 64.
+constexpr int stage_rows(int k) {
+  int r = kStageBytes / (2 * k);
+  r = r > kMaxStageRows ? kMaxStageRows : r;
+  return r >= 8 ? (r / 8) * 8 : r;
+}
+
+struct ShapeDims {
+  int H, NQ, NKV, D, E, K, I, P;
+};
+
+// Stage plan of the MoE tiles: an up/gate stage holds `up_half` gate rows
+// and as many up rows; a tile is `up_stages` stages.  A down stage holds
+// `dn_rows` rows of W_down[e] ([H][I]); a tile is `dn_stages` stages.
+struct MoePlan {
+  int up_half, up_stages, up_tile, up_tiles;  // up_tile outputs per tile, tiles per expert
+  int dn_rows, dn_stages, dn_tile, dn_tiles;
+};
+
+constexpr MoePlan moe_plan(ShapeDims s) {
+  MoePlan p{};
+  p.up_half = stage_rows(s.H) / 2;
+  p.up_stages = (s.I % (2 * p.up_half) == 0) ? 2 : 1;
+  p.up_tile = p.up_half * p.up_stages;
+  p.up_tiles = s.I / p.up_tile;
+  p.dn_rows = stage_rows(s.I);
+  p.dn_stages = (s.H % (2 * p.dn_rows) == 0) ? 2 : 1;
+  p.dn_tile = p.dn_rows * p.dn_stages;
+  p.dn_tiles = s.H / p.dn_tile;
+  return p;
+}
+
+// ------------------------------------------------------ kernel parameters
+struct Params {
+  // weights ([out][in] row-major BF16 unless noted)
+  const uint16_t* emb;
+  const uint16_t* wqkv;
+  const uint16_t* wo;
+  const uint16_t* wr;
+  const float* rbias;
+  const uint16_t* wg;
+  const uint16_t* wu;
+  const uint16_t* wd;
+  const float* gamma;
+  const float* gamma_f;
+  const uint16_t* wlm;
+  int L, V, window, full_period;
+  float rope_base, eps;
+
+  // step inputs and outputs
+  int B, MB;  // batch, schedule's max batch (buffer stride)
+  const int32_t* tokens;
+  const int32_t* block_tables;
+  int max_pages;
+  uint16_t* kpool;
+  uint16_t* vpool;
+  int64_t num_pages;
+  float* logits;
+
+  // task lists: [num_sms][2] (offset in int32, count) then descriptors
+  const int32_t* sched;
+
+  // workspace regions
+  uint32_t* bars;
+  uint32_t* err;        // [8]: code, sm, task, barrier, observed, target, op, layer
+  const int32_t* seq_lens;  // [B] device, length including the decoded token
+  int max_ctx;
+  float* h;             // [MB][H] residual stream
+  uint16_t* x;          // [MB][H] normalised layer input (bf16)
+  float* q;             // [MB][NQ][D] RoPE'd queries
+  uint16_t* kvnew;      // [MB][2][NKV][D] the new token's K and V (bf16, as stored)
+  float* part_o;        // [MB][NKV][max_slots][G][D] unnormalised slice outputs
+  float* part_ml;       // [MB][NKV][max_slots][G][2] slice max (log2 domain) and sum
+  uint16_t* attn_out;   // [MB][NQ D]
+  float* opart;         // [NKV][MB][H] O-proj split-K partials
+  float* rlog;          // [L][MB][E] router logits
+  int32_t* topk_ids;    // [L][MB][K]
+  float* topk_w;        // [L][MB][K]
+  int32_t* ecount;      // [L][E]
+  int32_t* eoff;        // [E + 1] row offset of each expert (current layer)
+  int32_t* perm;        // [MB K] expert-ordered row -> b * K + j
+  int32_t* inv;         // [MB K] b * K + j -> expert-ordered row
+  int32_t* upq;         // up tile queue: (e << 16) | tile
+  int32_t* dnq;         // down tile queue
+  int32_t* qlen;        // [2] queue lengths (up, down)
+  uint16_t* xg;         // [MB K][H] gathered rows (explicit gather)
+  uint16_t* u;          // [MB K][I] SwiGLU activations (bf16)
+  float* y;             // [MB K][H] expert outputs
+  float* moe_out;       // [MB][H]
+  float* htrace;        // [L + 1][MB][H] or null
+
+  int split_len;        // tokens per KV slice
+  int n_static;         // static slices per (row, group) of a sliding layer
+  int max_slots;
+  int explicit_gather;
+  int64_t watchdog_ns;
+};
+
+}  // namespace mk

@@ -1,0 +1,1299 @@
+// mk_kernel.cuh -- the persistent decode megakernel for sm_103a.
+//
+// One CTA per SM, resident for the whole decode step ("Cohere: a decode
+// megakernel for North Mini Code", section "What is a Megakernel?").  The
+// CTA has three roles, fixed per warp:
+//   warp 0      controller: copies the SM's task descriptors from global
+//               memory into a small shared-memory ring ("The task
+//               descriptor": the controller stays ahead of the workers);
+//   warp 1      producer: turns each task into work items and streams the
+//               task's weight rows / KV pages into a ring of 32 KB shared-
+//               memory stages with bulk async copies (cp.async.bulk +
+//               mbarrier complete_tx).  Weights never depend on the step's
+//               activations, so the producer runs ahead across task
+//               boundaries without waiting on any cross-SM barrier ("3.
+//               Weight prefetch"); only the MoE claimers wait, for the
+//               routing that decides which expert rows to stream;
+//   warps 2-9   consumers: wait on the task's cross-SM counters, compute
+//               from the staged rows, write the outputs and signal.
+// There is no storer warp: decode outputs are a few hundred bytes per task,
+// so consumers store them directly and publish them with a release add.
+//
+// Cross-SM synchronisation is a counter per dependency in global memory,
+// zeroed before each step ("Barriers"): a producer task adds 1 with release
+// semantics after its outputs are written; a waiting task spins with
+// acquire loads until the count is reached.  Every wait has a time limit: on
+// expiry the kernel records the failing barrier, every role drains its
+// in-flight copies and returns, and the host sees MK_ERR_TIMEOUT.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mk_internal.h"
+
+namespace mk {
+namespace dev {
+
+constexpr uint32_t ERR_TIMEOUT = 1, ERR_PAGE = 2, ERR_INDEX = 3;
+constexpr uint32_t FULL = 0xffffffffu;
+constexpr int kBarConsumers = 1;  // named barrier id of the consumer warps
+constexpr int kConsumerThreads = 32 * kConsumerWarps;
+
+// --------------------------------------------------------------- PTX glue
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ int64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return static_cast<int64_t>(t);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity), "r"(200000u)
+      : "memory");
+  return ok != 0;
+}
+// 1-D bulk copy global -> this CTA's shared memory, completing on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* b) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(b))
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_volatile(const uint32_t* p) {
+  return *reinterpret_cast<const volatile uint32_t*>(p);
+}
+__device__ __forceinline__ void bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// Named barrier with an OR over the threads' predicates: a uniform decision.
+__device__ __forceinline__ bool bar_or(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+      " barrier.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void consumers_sync() { bar_sync(kBarConsumers, kConsumerThreads); }
+
+// ------------------------------------------------------------ numerics
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+__device__ __forceinline__ float bf16_f(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
+__device__ __forceinline__ uint16_t f_bf16(float f) {  // round to nearest even (finite inputs)
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7f800000u) == 0x7f800000u) return (uint16_t)((u >> 16) | ((u & 0xffffu) ? 0x40u : 0u));
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+__device__ __forceinline__ float dot8(uint4 w, uint4 x, float acc) {
+  acc = fmaf(bf16_lo(w.x), bf16_lo(x.x), acc);
+  acc = fmaf(bf16_hi(w.x), bf16_hi(x.x), acc);
+  acc = fmaf(bf16_lo(w.y), bf16_lo(x.y), acc);
+  acc = fmaf(bf16_hi(w.y), bf16_hi(x.y), acc);
+  acc = fmaf(bf16_lo(w.z), bf16_lo(x.z), acc);
+  acc = fmaf(bf16_hi(w.z), bf16_hi(x.z), acc);
+  acc = fmaf(bf16_lo(w.w), bf16_lo(x.w), acc);
+  acc = fmaf(bf16_hi(w.w), bf16_hi(x.w), acc);
+  return acc;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(FULL, v, m);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, m));
+  return v;
+}
+// Sums N per-lane values over the warp and leaves lane l holding the total of
+// value l / (32 / N) ("transpose reduction": N-1 + log2(32/N) shuffles instead
+// of 5N).
+template <int N>
+__device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
+  static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "power of two");
+#pragma unroll
+  for (int n = N, m = 16; n > 1; n >>= 1, m >>= 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = up ? v[i] : v[i + n / 2];
+      const float keep = up ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(FULL, send, m);
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int m = 16 / N; m >= 1; m >>= 1) r += __shfl_xor_sync(FULL, r, m);
+  return r;
+}
+
+// ----------------------------------------------------- shared memory map
+struct Hdr {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t dfull[kDescRing], dempty[kDescRing];
+  uint64_t wfull[kWorkRing], wempty[kWorkRing];
+  int32_t desc[kDescRing][32];
+  int32_t work[kWorkRing][32];
+  volatile int32_t abort;
+  int32_t pad[31];
+};
+
+template <class S>
+struct Scratch {
+  uint16_t xs[kTB * S::H];                  // activation rows of one GEMV pass
+  float out[2][kTB * kMaxStageRows];        // dot products of one stage (double buffer)
+  float sc[S::G * S::P];                    // attention scores of one page
+  float pr[S::G * S::P];                    // attention probabilities of one page
+  float am[S::G], al[S::G], aa[S::G];       // running max, sum, rescale per head
+  float red[kConsumerWarps * 2];
+  unsigned long long mask[S::E];            // rows routed to each expert (bit b)
+  int32_t cnt[S::E], off[S::E + 1], act[S::E + 1];
+};
+
+template <class S>
+constexpr size_t smem_bytes() {
+  return (size_t)kStages * kStageBytes + sizeof(Hdr) + sizeof(Scratch<S>);
+}
+
+// ---------------------------------------------------------------- shapes
+template <int H_, int NQ_, int NKV_, int D_, int E_, int K_, int I_, int P_>
+struct Shape {
+  static constexpr int H = H_, NQ = NQ_, NKV = NKV_, D = D_, E = E_, K = K_, I = I_, P = P_;
+  static constexpr int G = NQ / NKV;
+  static constexpr int QKV = (NQ + 2 * NKV) * D;
+  static constexpr ShapeDims dims{H, NQ, NKV, D, E, K, I, P};
+  static constexpr MoePlan mp = moe_plan(dims);
+  static constexpr int SR_H = stage_rows(H), SR_O = stage_rows(G * D), SR_I = stage_rows(I);
+  static_assert(H % 256 == 0 && (G * D) % 8 == 0 && I % 8 == 0, "row chunks");
+  static_assert(D % 32 == 0 && 32 % G == 0 && (G * D) % 4 == 0, "attention lane maps");
+  static_assert((G * D / 4) <= kConsumerThreads, "PV threads");
+  static_assert(2 * P * D * 2 <= kStageBytes, "one KV page per stage");
+  static_assert(E <= 256 && K <= 32, "routing scratch");
+};
+
+struct Ctx {
+  Hdr* hdr;
+  uint8_t* stages;
+  int sm;
+  uint32_t st;  // stages issued (producer) / consumed (consumers)
+  uint32_t wk;  // work items pushed / popped
+};
+
+// ----------------------------------------------------------- errors/waits
+static __device__ __noinline__ void record_error(const Params& p, uint32_t code, int sm, const int32_t* d, int bar,
+                             uint32_t seen, uint32_t tgt) {
+  if (atomicCAS(p.err, 0u, code) == 0u) {
+    p.err[1] = (uint32_t)sm;
+    p.err[2] = d ? (uint32_t)d[F_TASK] : 0xffffffffu;
+    p.err[3] = (uint32_t)bar;
+    p.err[4] = seen;
+    p.err[5] = tgt;
+    p.err[6] = d ? (uint32_t)d[F_OP] : 0xffffffffu;
+    p.err[7] = d ? (uint32_t)d[F_LAYER] : 0xffffffffu;
+    __threadfence();
+  }
+}
+
+static __device__ __forceinline__ bool aborted(const Ctx& c) { return c.hdr->abort != 0; }
+
+// Waits for an mbarrier phase; false if the CTA is aborting or the watchdog fired.
+static __device__ bool mbar_wait(const Params& p, Ctx& c, uint64_t* b, uint32_t parity) {
+  if (mbar_try_wait(b, parity)) return true;
+  const int64_t t0 = gtimer();
+  for (;;) {
+    if (mbar_try_wait(b, parity)) return true;
+    if (aborted(c)) return false;
+    if (gtimer() - t0 > p.watchdog_ns) {
+      record_error(p, ERR_TIMEOUT, c.sm, nullptr, -1, 0, 0);
+      c.hdr->abort = 1;
+      return false;
+    }
+  }
+}
+
+// Waits until counter `bar` reaches `tgt` (one thread).  "Barriers": spin with
+// a short sleep; here with acquire loads and a time limit.
+static __device__ bool wait_counter(const Params& p, Ctx& c, int bar, uint32_t tgt, const int32_t* d) {
+  if (bar < 0 || tgt == 0) return true;
+  const uint32_t* a = p.bars + bar;
+  if (ld_acquire(a) >= tgt) return true;
+  const int64_t t0 = gtimer();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(20);
+    if (ld_acquire(a) >= tgt) return true;
+    if ((it & 31u) == 0) {
+      if (aborted(c)) return false;
+      if (ld_volatile(p.err) != 0) {
+        c.hdr->abort = 1;
+        return false;
+      }
+      if (gtimer() - t0 > p.watchdog_ns) {
+        record_error(p, ERR_TIMEOUT, c.sm, d, bar, ld_volatile(a), tgt);
+        c.hdr->abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+static __device__ __forceinline__ int slices_of(const Params& p, int seq) {
+  return (seq + p.split_len - 1) / p.split_len;
+}
+
+// ======================================================================
+// controller
+// ======================================================================
+static __device__ void controller(const Params& p, Ctx& c) {
+  if ((threadIdx.x & 31) != 0) return;
+  const int off = p.sched[2 * c.sm], n = p.sched[2 * c.sm + 1];
+  Hdr* H = c.hdr;
+  int i = 0;
+  for (; i < n; ++i) {
+    const int slot = i % kDescRing;
+    if (i >= kDescRing && !mbar_wait(p, c, &H->dempty[slot], ((i / kDescRing) - 1) & 1)) break;
+    mbar_expect_tx(&H->dfull[slot], 128);
+    bulk_g2s(H->desc[slot], p.sched + off + 32 * i, 128, &H->dfull[slot]);
+  }
+  if (i < n) {  // aborted: let the copies already issued land before returning
+    for (int j = (i > kDescRing ? i - kDescRing : 0); j < i; ++j) {
+      const int64_t t0 = gtimer();
+      while (!mbar_try_wait(&H->dfull[j % kDescRing], (j / kDescRing) & 1) && gtimer() - t0 < p.watchdog_ns) {
+      }
+    }
+  }
+}
+
+// ======================================================================
+// producer
+// ======================================================================
+template <class S>
+struct Producer {
+  const Params& p;
+  Ctx& c;
+
+  __device__ bool acquire_stage(int& slot) {
+    slot = c.st % kStages;
+    if (c.st >= (uint32_t)kStages)
+      return mbar_wait(p, c, &c.hdr->empty[slot], ((c.st / kStages) - 1) & 1);
+    return true;
+  }
+  __device__ uint8_t* stage(int slot) { return c.stages + (size_t)slot * kStageBytes; }
+
+  __device__ bool push(const int32_t* item) {
+    const int slot = c.wk % kWorkRing;
+    if (c.wk >= (uint32_t)kWorkRing && !mbar_wait(p, c, &c.hdr->wempty[slot], ((c.wk / kWorkRing) - 1) & 1))
+      return false;
+    int32_t* dst = c.hdr->work[slot];
+    for (int i = 0; i < 32; ++i) dst[i] = item[i];
+    mbar_arrive(&c.hdr->wfull[slot]);
+    ++c.wk;
+    return true;
+  }
+
+  // rows [row0, row0+nrows) of a [rows][K] matrix (row stride `ld` elements),
+  // SR rows per stage
+  __device__ bool load_rows(const uint16_t* base, int64_t ld, int K, int row0, int nrows, int SR) {
+    for (int s0 = 0; s0 < nrows; s0 += SR) {
+      const int rs = min(SR, nrows - s0);
+      int slot;
+      if (!acquire_stage(slot)) return false;
+      uint64_t* fb = &c.hdr->full[slot];
+      uint8_t* dst = stage(slot);
+      const uint32_t bytes = (uint32_t)rs * K * 2;
+      mbar_expect_tx(fb, bytes);
+      if (ld == K) {
+        bulk_g2s(dst, base + (int64_t)(row0 + s0) * K, bytes, fb);
+      } else {
+        for (int r = 0; r < rs; ++r) bulk_g2s(dst + (size_t)r * K * 2, base + (int64_t)(row0 + s0 + r) * ld, K * 2, fb);
+      }
+      ++c.st;
+    }
+    return true;
+  }
+
+  __device__ int dense_stages(int rows, int SR) { return (rows + SR - 1) / SR; }
+
+  __device__ bool dense(const int32_t* d) {
+    int32_t it[32];
+    for (int i = 0; i < 32; ++i) it[i] = d[i];
+    const int op = d[F_OP], l = d[F_LAYER], row0 = d[F_A0], rows = d[F_A0 + 1];
+    const uint16_t* base;
+    int64_t ld;
+    int K, SR;
+    switch (op) {
+      case OP_QKV_PROJ: base = p.wqkv + (int64_t)l * S::QKV * S::H; ld = S::H; K = S::H; SR = S::SR_H; break;
+      case OP_ROUTER_GEMM: base = p.wr + (int64_t)l * S::E * S::H; ld = S::H; K = S::H; SR = S::SR_H; break;
+      case OP_LM_HEAD: base = p.wlm; ld = S::H; K = S::H; SR = S::SR_H; break;
+      default:  // OP_O_PROJ: the columns of KV group g
+        base = p.wo + (int64_t)l * S::H * S::NQ * S::D + (int64_t)d[F_A0 + 2] * S::G * S::D;
+        ld = S::NQ * S::D; K = S::G * S::D; SR = S::SR_O; break;
+    }
+    it[F_NSTAGE] = dense_stages(rows, SR);
+    if (!push(it)) return false;
+    return load_rows(base, ld, K, row0, rows, SR);
+  }
+
+  __device__ bool attn_pages(int l, int b, int g, int pf, int np) {
+    const int64_t page_elems = (int64_t)S::P * S::D;
+    for (int k = 0; k < np; ++k) {
+      int slot;
+      if (!acquire_stage(slot)) return false;
+      uint64_t* fb = &c.hdr->full[slot];
+      uint8_t* dst = stage(slot);
+      int page = -1;
+      const int lp = pf + k;
+      if (lp < p.max_pages) page = __ldg(p.block_tables + (int64_t)b * p.max_pages + lp);
+      if (page < 0 || page >= p.num_pages) {
+        record_error(p, ERR_PAGE, c.sm, nullptr, lp, (uint32_t)page, (uint32_t)p.num_pages);
+        mbar_arrive(&c.hdr->full[slot]);  // complete the stage without data
+      } else {
+        const int64_t off = (((int64_t)l * p.num_pages + page) * S::NKV + g) * page_elems;
+        mbar_expect_tx(fb, (uint32_t)(2 * page_elems * 2));
+        bulk_g2s(dst, p.kpool + off, (uint32_t)(page_elems * 2), fb);
+        bulk_g2s(dst + page_elems * 2, p.vpool + off, (uint32_t)(page_elems * 2), fb);
+      }
+      ++c.st;
+    }
+    return true;
+  }
+
+  // one KV slice [t0, t1) of (b, g) as a work item plus its pages
+  __device__ bool attn_item(const int32_t* d, int l, int b, int g, int t0, int t1, int slot_idx, int wait_bar,
+                            int wait_tgt, int sig) {
+    int32_t it[32];
+    for (int i = 0; i < 32; ++i) it[i] = d[i];
+    it[F_OP] = W_ATTN;
+    it[F_LAYER] = l;
+    it[F_WAIT0] = wait_bar;
+    it[F_TGT0] = wait_tgt;
+    it[F_WAIT1] = -1;
+    it[F_SIG0] = sig;
+    it[F_SIG1] = -1;
+    const int pf = t0 / S::P;
+    const int np = t1 > t0 ? (t1 - 1) / S::P - pf + 1 : 0;
+    it[F_A0] = b;
+    it[F_A0 + 1] = g;
+    it[F_A0 + 2] = t0;
+    it[F_A0 + 3] = t1;
+    it[F_A0 + 4] = pf;
+    it[F_A0 + 5] = slot_idx;
+    it[F_NSTAGE] = np;
+    if (!push(it)) return false;
+    return attn_pages(l, b, g, pf, np);
+  }
+
+  __device__ bool attn_decode(const int32_t* d) {
+    const int l = d[F_LAYER], b = d[F_A0], g = d[F_A0 + 1], j = d[F_A0 + 2];
+    int t0 = 0, t1 = 0;
+    if (b < p.B) {
+      const int s = __ldg(p.seq_lens + b);
+      const bool full = p.window == 0 || (l + 1) % p.full_period == 0;
+      const int lo = full ? 0 : max(0, s - p.window);
+      const int jj = lo / p.split_len + j;
+      t0 = max(lo, jj * p.split_len);
+      t1 = min(s, (jj + 1) * p.split_len);
+      if (t1 < t0) t1 = t0;
+    }
+    return attn_item(d, l, b, g, t0, t1, j, d[F_WAIT0], d[F_TGT0], d[F_SIG0]);
+  }
+
+  // Claimer over the full-attention queue ("Task scheduler": ATTN_DRAIN
+  // claims the next entry until the queue is empty).  The queue holds one
+  // entry per (row b, KV group g, slice j), ordered (b, g, j); entry i is
+  // located from the rows' slice counts, so the queue needs no storage.
+  __device__ bool attn_drain(const int32_t* d) {
+    const int l = d[F_LAYER];
+    uint32_t* claim = p.bars + d[F_A0];
+    for (;;) {
+      if (aborted(c)) return false;
+      const uint32_t i = atomicAdd(claim, 1u);
+      uint32_t acc = 0;
+      int b = 0, n = 0, s = 0;
+      for (; b < p.B; ++b) {
+        s = __ldg(p.seq_lens + b);
+        n = slices_of(p, s) * S::NKV;
+        if (i < acc + (uint32_t)n) break;
+        acc += (uint32_t)n;
+      }
+      if (b >= p.B) break;  // queue exhausted
+      const int r = (int)(i - acc), per = n / S::NKV;
+      const int g = r / per, j = r - g * per;
+      if (j >= p.max_slots) {
+        record_error(p, ERR_INDEX, c.sm, d, d[F_A0], (uint32_t)s, (uint32_t)p.max_ctx);
+        c.hdr->abort = 1;
+        return false;
+      }
+      const int t0 = j * p.split_len, t1 = min(s, t0 + p.split_len);
+      if (!attn_item(d, l, b, g, t0, t1, j, d[F_A0 + 2] + g, d[F_A0 + 3], d[F_A0 + 1] + b * S::NKV + g))
+        return false;
+    }
+    return claim_end(d);
+  }
+
+  __device__ bool claim_end(const int32_t* d) {
+    int32_t it[32];
+    for (int i = 0; i < 32; ++i) it[i] = d[i];
+    it[F_OP] = W_CLAIM_END;
+    it[F_WAIT0] = it[F_WAIT1] = -1;
+    it[F_NSTAGE] = 0;
+    return push(it);
+  }
+
+  __device__ bool moe_drain(const int32_t* d, bool up) {
+    const int l = d[F_LAYER];
+    // the routing decides which expert rows to stream: wait for the queue
+    if (!wait_counter(p, c, d[F_WAIT0], (uint32_t)d[F_TGT0], d)) return false;
+    const int qlen = min(__ldcg(p.qlen + (up ? 0 : 1)), S::E * (up ? S::mp.up_tiles : S::mp.dn_tiles));
+    const int32_t* q = up ? p.upq : p.dnq;
+    uint32_t* claim = p.bars + d[F_A0];
+    constexpr MoePlan mp = S::mp;
+    for (;;) {
+      if (aborted(c)) return false;
+      const uint32_t i = atomicAdd(claim, 1u);
+      if (i >= (uint32_t)qlen) break;
+      const int32_t ent = __ldcg(q + i);
+      const int e = ent >> 16, t = ent & 0xffff;
+      const bool e_ok = e >= 0 && e < S::E && t < (up ? mp.up_tiles : mp.dn_tiles);
+      const int row0 = e_ok ? __ldcg(p.eoff + e) : -1;
+      const int nrows = e_ok ? __ldcg(p.ecount + l * S::E + e) : 0;
+      if (!e_ok || row0 < 0 || nrows < 1 || row0 + nrows > p.B * S::K) {
+        record_error(p, ERR_INDEX, c.sm, d, d[F_A0], (uint32_t)ent, (uint32_t)qlen);
+        c.hdr->abort = 1;
+        return false;
+      }
+      int32_t it[32];
+      for (int k = 0; k < 32; ++k) it[k] = d[k];
+      it[F_A0] = e;
+      it[F_A0 + 1] = t;
+      it[F_A0 + 2] = row0;
+      it[F_A0 + 3] = nrows;
+      it[F_WAIT1] = -1;
+      it[F_SIG1] = -1;
+      if (up) {
+        it[F_OP] = W_UP_TILE;
+        it[F_WAIT0] = d[F_A0 + 2];  // explicit gather barrier (or -1)
+        it[F_TGT0] = d[F_A0 + 3];
+        it[F_SIG0] = d[F_A0 + 1] + e;
+        it[F_NSTAGE] = mp.up_stages;
+      } else {
+        it[F_OP] = W_DOWN_TILE;
+        it[F_WAIT0] = d[F_A0 + 1] + e;  // every up tile of expert e
+        it[F_TGT0] = mp.up_tiles;
+        it[F_SIG0] = -1;
+        it[F_NSTAGE] = mp.dn_stages;
+      }
+      if (!push(it)) return false;
+      const int64_t le = (int64_t)l * S::E + e;
+      if (up) {
+        for (int s = 0; s < mp.up_stages; ++s) {
+          int slot;
+          if (!acquire_stage(slot)) return false;
+          uint64_t* fb = &c.hdr->full[slot];
+          uint8_t* dst = stage(slot);
+          const int r0 = t * mp.up_tile + s * mp.up_half;
+          const uint32_t half = (uint32_t)mp.up_half * S::H * 2;
+          mbar_expect_tx(fb, 2 * half);
+          bulk_g2s(dst, p.wg + (le * S::I + r0) * S::H, half, fb);
+          bulk_g2s(dst + half, p.wu + (le * S::I + r0) * S::H, half, fb);
+          ++c.st;
+        }
+      } else {
+        if (!load_rows(p.wd + le * S::H * S::I, S::I, S::I, t * mp.dn_tile, mp.dn_tile, mp.dn_rows)) return false;
+      }
+    }
+    return claim_end(d);
+  }
+
+  __device__ bool passthrough(const int32_t* d) {
+    int32_t it[32];
+    for (int i = 0; i < 32; ++i) it[i] = d[i];
+    it[F_NSTAGE] = 0;
+    return push(it);
+  }
+
+  __device__ void run() {
+    if ((threadIdx.x & 31) != 0) return;
+    const int n = p.sched[2 * c.sm + 1];
+    Hdr* H = c.hdr;
+    bool ok = true;
+    for (int i = 0; i < n && ok; ++i) {
+      const int slot = i % kDescRing;
+      if (!mbar_wait(p, c, &H->dfull[slot], (i / kDescRing) & 1)) {
+        ok = false;
+        break;
+      }
+      int32_t d[32];
+      for (int k = 0; k < 32; ++k) d[k] = H->desc[slot][k];
+      mbar_arrive(&H->dempty[slot]);
+      switch (d[F_OP]) {
+        case OP_QKV_PROJ:
+        case OP_O_PROJ:
+        case OP_ROUTER_GEMM:
+        case OP_LM_HEAD: ok = dense(d); break;
+        case OP_ATTN_DECODE: ok = attn_decode(d); break;
+        case OP_ATTN_DRAIN: ok = attn_drain(d); break;
+        case OP_MOE_UPGATE_ACT_DRAIN: ok = moe_drain(d, true); break;
+        case OP_MOE_DOWN_DRAIN: ok = moe_drain(d, false); break;
+        default: ok = passthrough(d); break;
+      }
+    }
+    if (ok) {
+      int32_t ex[32];
+      for (int k = 0; k < 32; ++k) ex[k] = 0;
+      ex[F_OP] = W_EXIT;
+      ex[F_WAIT0] = ex[F_WAIT1] = ex[F_SIG0] = ex[F_SIG1] = -1;
+      push(ex);
+      return;
+    }
+    // aborting: wait (bounded) for the copies already issued into the stage ring
+    const uint32_t first = c.st > (uint32_t)kStages ? c.st - kStages : 0;
+    for (uint32_t s = first; s < c.st; ++s) {
+      const int64_t t0 = gtimer();
+      while (!mbar_try_wait(&H->full[s % kStages], (s / kStages) & 1) && gtimer() - t0 < p.watchdog_ns) {
+      }
+    }
+  }
+};
+
+// ======================================================================
+// consumers
+// ======================================================================
+template <class S>
+struct Consumer {
+  const Params& p;
+  Ctx& c;
+  Scratch<S>& sm;
+  int ct, cw, lane;
+
+  // --- the stage ring
+  __device__ bool stage_wait(int& slot) {
+    slot = c.st % kStages;
+    return mbar_wait(p, c, &c.hdr->full[slot], (c.st / kStages) & 1);
+  }
+  __device__ void stage_release(int slot) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&c.hdr->empty[slot]);
+    ++c.st;
+  }
+  __device__ const uint8_t* stage(int slot) const { return c.stages + (size_t)slot * kStageBytes; }
+
+  // ---------------------------------------------------------- GEMV core
+  // out[t][r] = W[r][:] . xs[t][:] for the rows of one stage (warp per row).
+  template <int K>
+  __device__ void gemv_rows(const uint16_t* W, int rows, int tb, float* out) {
+    constexpr int C = K / 8;
+    constexpr int CPL = (C + 31) / 32;
+    const uint4* xs4 = reinterpret_cast<const uint4*>(sm.xs);
+    for (int r = cw; r < rows; r += kConsumerWarps) {
+      float acc[kTB];
+#pragma unroll
+      for (int t = 0; t < kTB; ++t) acc[t] = 0.f;
+      const uint4* wr = reinterpret_cast<const uint4*>(W + (size_t)r * K);
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) {
+        const int cc = lane + 32 * j;
+        if (C % 32 == 0 || cc < C) {
+          const uint4 w = wr[cc];
+#pragma unroll
+          for (int t = 0; t < kTB; ++t)
+            if (t < tb) acc[t] = dot8(w, xs4[t * C + cc], acc[t]);
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kTB; ++t)
+        if (t < tb) acc[t] = warp_sum(acc[t]);
+      if (lane == 0)
+#pragma unroll
+        for (int t = 0; t < kTB; ++t)
+          if (t < tb) out[t * kMaxStageRows + r] = acc[t];
+    }
+  }
+
+  // activation rows [4*chunk, 4*chunk + tb) of the item into sm.xs
+  template <int K>
+  __device__ void load_x(int op, const int32_t* w, int chunk, int tb) {
+    constexpr int C = K / 8;
+    uint4* xs4 = reinterpret_cast<uint4*>(sm.xs);
+    for (int i = ct; i < tb * C; i += kConsumerThreads) {
+      const int t = i / C, cc = i - t * C;
+      const int tok = kTB * chunk + t;
+      const uint4* src;
+      switch (op) {
+        case OP_O_PROJ:
+          src = reinterpret_cast<const uint4*>(p.attn_out + (int64_t)tok * S::NQ * S::D +
+                                               (int64_t)w[F_A0 + 2] * S::G * S::D);
+          break;
+        case W_UP_TILE: {
+          const int row = w[F_A0 + 2] + tok;
+          if (p.explicit_gather) {
+            src = reinterpret_cast<const uint4*>(p.xg + (int64_t)row * S::H);
+          } else {
+            int pr = __ldcg(p.perm + row);
+            int b = pr / S::K;
+            if (pr < 0 || b >= p.B) b = 0;  // only after a failed step
+            src = reinterpret_cast<const uint4*>(p.x + (int64_t)b * S::H);
+          }
+          break;
+        }
+        case W_DOWN_TILE:
+          src = reinterpret_cast<const uint4*>(p.u + (int64_t)(w[F_A0 + 2] + tok) * S::I);
+          break;
+        default:
+          src = reinterpret_cast<const uint4*>(p.x + (int64_t)tok * S::H);
+          break;
+      }
+      xs4[i] = __ldcg(src + cc);
+    }
+  }
+
+  // epilogue of one stage: rows [r_first, r_first + rows) of the item's output,
+  // activation rows [4*chunk, 4*chunk + tb)
+  __device__ void epilogue(int op, const int32_t* w, int s, int rows, int chunk, int tb, const float* out) {
+    const int l = w[F_LAYER];
+    switch (op) {
+      case OP_QKV_PROJ: {
+        // RoPE in the epilogue, then the new K/V into the pool ("Tasks":
+        // QKV_PROJ applies RoPE in-register before writing back)
+        const int half = rows / 2;
+        for (int i = ct; i < tb * half; i += kConsumerThreads) {
+          const int t = i / half, r = 2 * (i - t * half);
+          const int row = w[F_A0] + s * S::SR_H + r;
+          const int b = kTB * chunk + t;
+          float v0 = out[t * kMaxStageRows + r], v1 = out[t * kMaxStageRows + r + 1];
+          const int head = row / S::D, dd = row - head * S::D;
+          const int pos = __ldg(p.seq_lens + b) - 1;
+          if (head < S::NQ + S::NKV) {  // rotate q and k: pair (dd, dd+1) by pos * base^(-dd/D)
+            const double theta = pow((double)p.rope_base, -(double)dd / (double)S::D);
+            double sn, cs;
+            sincos((double)pos * theta, &sn, &cs);
+            const float c0 = (float)cs, s0 = (float)sn;
+            const float a = v0 * c0 - v1 * s0, bb = v0 * s0 + v1 * c0;
+            v0 = a;
+            v1 = bb;
+          }
+          if (head < S::NQ) {
+            float* qd = p.q + ((int64_t)b * S::NQ + head) * S::D + dd;
+            qd[0] = v0;
+            qd[1] = v1;
+          } else if (pos >= 0) {
+            const bool is_v = head >= S::NQ + S::NKV;
+            const int g = head - S::NQ - (is_v ? S::NKV : 0);
+            const uint32_t packed = (uint32_t)f_bf16(v0) | ((uint32_t)f_bf16(v1) << 16);
+            *reinterpret_cast<uint32_t*>(p.kvnew + (((int64_t)b * 2 + (is_v ? 1 : 0)) * S::NKV + g) * S::D + dd) = packed;
+            const int lp = pos / S::P;
+            int page = lp < p.max_pages ? __ldg(p.block_tables + (int64_t)b * p.max_pages + lp) : -1;
+            if (page < 0 || page >= p.num_pages) {
+              record_error(p, ERR_PAGE, c.sm, w, lp, (uint32_t)page, (uint32_t)p.num_pages);
+            } else {
+              uint16_t* pool = is_v ? p.vpool : p.kpool;
+              const int64_t o = ((((int64_t)l * p.num_pages + page) * S::NKV + g) * S::P + pos % S::P) * S::D + dd;
+              *reinterpret_cast<uint32_t*>(pool + o) = packed;
+            }
+          }
+        }
+        break;
+      }
+      case OP_ROUTER_GEMM:
+        for (int i = ct; i < tb * rows; i += kConsumerThreads) {
+          const int t = i / rows, r = i - t * rows;
+          const int e = w[F_A0] + s * S::SR_H + r, b = kTB * chunk + t;
+          p.rlog[((int64_t)l * p.MB + b) * S::E + e] = out[t * kMaxStageRows + r] + (p.rbias ? p.rbias[e] : 0.f);
+        }
+        break;
+      case OP_LM_HEAD:
+        for (int i = ct; i < tb * rows; i += kConsumerThreads) {
+          const int t = i / rows, r = i - t * rows;
+          const int v = w[F_A0] + s * S::SR_H + r, b = kTB * chunk + t;
+          p.logits[(int64_t)b * p.V + v] = out[t * kMaxStageRows + r];
+        }
+        break;
+      case OP_O_PROJ:
+        for (int i = ct; i < tb * rows; i += kConsumerThreads) {
+          const int t = i / rows, r = i - t * rows;
+          const int n = w[F_A0] + s * S::SR_O + r, b = kTB * chunk + t;
+          p.opart[((int64_t)w[F_A0 + 2] * p.MB + b) * S::H + n] = out[t * kMaxStageRows + r];
+        }
+        break;
+      case W_UP_TILE: {
+        // SiLU(gate) * up in the epilogue ("Tasks": the SiLU-and-multiply)
+        constexpr int hu = S::mp.up_half;
+        for (int i = ct; i < tb * hu; i += kConsumerThreads) {
+          const int t = i / hu, r = i - t * hu;
+          const float gte = out[t * kMaxStageRows + r], upv = out[t * kMaxStageRows + hu + r];
+          const float act = gte / (1.f + expf(-gte)) * upv;
+          const int row = w[F_A0 + 2] + kTB * chunk + t;
+          const int col = w[F_A0 + 1] * S::mp.up_tile + s * hu + r;
+          p.u[(int64_t)row * S::I + col] = f_bf16(act);
+        }
+        break;
+      }
+      case W_DOWN_TILE:
+        for (int i = ct; i < tb * rows; i += kConsumerThreads) {
+          const int t = i / rows, r = i - t * rows;
+          const int row = w[F_A0 + 2] + kTB * chunk + t;
+          const int n = w[F_A0 + 1] * S::mp.dn_tile + s * S::mp.dn_rows + r;
+          p.y[(int64_t)row * S::H + n] = out[t * kMaxStageRows + r];
+        }
+        break;
+      default: break;
+    }
+  }
+
+  // A GEMV item: stages of full weight rows, activation rows in passes of kTB.
+  template <int K>
+  __device__ void gemv_item(const int32_t* w, int SR, int total_rows, int ntok) {
+    const int op = w[F_OP];
+    const int nst = w[F_NSTAGE];
+    const int nchunk = (ntok + kTB - 1) / kTB;
+    int buf = 0;
+    for (int s = 0; s < nst; ++s) {
+      int slot;
+      const bool ok = stage_wait(slot);
+      const int rows = min(SR, total_rows - s * SR);
+      const uint16_t* W = reinterpret_cast<const uint16_t*>(stage(slot));
+      for (int chunk = 0; chunk < nchunk; ++chunk) {
+        const int tb = min(kTB, ntok - kTB * chunk);
+        if (s == 0 || nchunk > 1) {
+          if (!aborted(c)) load_x<K>(op, w, chunk, tb);
+          consumers_sync();
+        }
+        if (__all_sync(FULL, ok && !aborted(c))) gemv_rows<K>(W, rows, tb, sm.out[buf]);
+        consumers_sync();
+        if (!aborted(c)) epilogue(op, w, s, rows, chunk, tb, sm.out[buf]);
+        buf ^= 1;
+      }
+      stage_release(slot);
+    }
+  }
+
+  // --------------------------------------------------------- attention
+  // One KV slice of one (row b, KV group g): its G query heads against the
+  // keys in [t0, t1), as an unnormalised partial (running max in the log2
+  // domain, sum, weighted values) -- "Tasks": ATTN_DECODE on a partial slice.
+  __device__ void attn(const int32_t* w) {
+    constexpr int G = S::G, D = S::D, P = S::P, DPL = D / 32;
+    const int l = w[F_LAYER], b = w[F_A0], g = w[F_A0 + 1], t0 = w[F_A0 + 2], t1 = w[F_A0 + 3];
+    const int pf = w[F_A0 + 4], slot_idx = w[F_A0 + 5], np = w[F_NSTAGE];
+    (void)l;
+    const int s = b < p.B ? __ldg(p.seq_lens + b) : 0;
+    const int pos = s - 1;
+    const float scale = 1.4426950408889634f / sqrtf((float)D);
+    float qr[G][DPL];
+    if (np > 0) {
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int i = 0; i < DPL; ++i)
+          qr[h][i] = __ldcg(p.q + ((int64_t)b * S::NQ + g * G + h) * D + lane * DPL + i) * scale;
+    }
+    // PV thread map: head h = ct % G, dims [4 c4, 4 c4 + 4) with c4 = ct / G
+    const bool pv_thread = ct < G * D / 4;
+    const int ph = ct % G, pc = ct / G;
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    if (ct < G) {
+      sm.am[ct] = -INFINITY;
+      sm.al[ct] = 0.f;
+    }
+    for (int k = 0; k < np; ++k) {
+      int slot;
+      const bool ok = __all_sync(FULL, stage_wait(slot) && !aborted(c));
+      uint16_t* Kp = reinterpret_cast<uint16_t*>(c.stages + (size_t)slot * kStageBytes);
+      uint16_t* Vp = Kp + P * D;
+      const int page_t0 = (pf + k) * P;
+      // the new token's K/V replace its slot: the pool page may predate the write
+      if (pos >= page_t0 && pos < page_t0 + P && pos >= t0 && pos < t1) {
+        const int sl = pos - page_t0;
+        if (ok && ct < 2 * D / 8) {
+          const int which = ct / (D / 8), cc = ct % (D / 8);
+          const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p.kvnew + (((int64_t)b * 2 + which) * S::NKV + g) * D) + cc);
+          reinterpret_cast<uint4*>((which ? Vp : Kp) + sl * D)[cc] = v;
+          fence_proxy_async_smem();
+        }
+        consumers_sync();
+      }
+      // scores: warp per token, lane per DPL dims, transpose-reduced over heads
+      if (ok) {
+        for (int tt = cw; tt < P; tt += kConsumerWarps) {
+          const int tok = page_t0 + tt;
+          float part[G];
+          const uint16_t* kr = Kp + tt * D + lane * DPL;
+          float kv[DPL];
+          if (DPL == 4) {
+            const uint2 u = *reinterpret_cast<const uint2*>(kr);
+            kv[0] = bf16_lo(u.x); kv[1] = bf16_hi(u.x); kv[2] = bf16_lo(u.y); kv[3] = bf16_hi(u.y);
+          } else {
+            const uint32_t u = *reinterpret_cast<const uint32_t*>(kr);
+            kv[0] = bf16_lo(u); kv[1] = bf16_hi(u);
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            float a = 0.f;
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) a = fmaf(qr[h][i], kv[i], a);
+            part[h] = a;
+          }
+          const float sc = reduce_scatter<G>(part, lane);
+          if ((lane & (32 / G - 1)) == 0) {
+            const int h = lane / (32 / G);
+            sm.sc[h * P + tt] = (tok >= t0 && tok < t1) ? sc : -INFINITY;
+          }
+        }
+      }
+      consumers_sync();
+      // online softmax update: warp h owns head h
+      if (ok && cw < G) {
+        const int h = cw;
+        float mx = -INFINITY;
+        for (int tt = lane; tt < P; tt += 32) mx = fmaxf(mx, sm.sc[h * P + tt]);
+        mx = warp_max(mx);
+        const float m_old = sm.am[h];
+        const float m_new = fmaxf(m_old, mx);
+        float sum = 0.f;
+        for (int tt = lane; tt < P; tt += 32) {
+          const float sv = sm.sc[h * P + tt];
+          const float pv = (m_new == -INFINITY || sv == -INFINITY) ? 0.f : exp2f(sv - m_new);
+          sm.pr[h * P + tt] = pv;
+          sum += pv;
+        }
+        sum = warp_sum(sum);
+        if (lane == 0) {
+          const float alpha = (m_old == -INFINITY) ? 0.f : exp2f(m_old - m_new);
+          sm.aa[h] = alpha;
+          sm.al[h] = sm.al[h] * alpha + sum;
+          sm.am[h] = m_new;
+        }
+      }
+      consumers_sync();
+      if (ok && pv_thread) {
+        const float alpha = sm.aa[ph];
+        o[0] *= alpha; o[1] *= alpha; o[2] *= alpha; o[3] *= alpha;
+        const uint16_t* vc = Vp + pc * 4;
+#pragma unroll 4
+        for (int tt = 0; tt < P; ++tt) {
+          const float pv = sm.pr[ph * P + tt];
+          const uint2 u = *reinterpret_cast<const uint2*>(vc + tt * D);
+          o[0] = fmaf(pv, bf16_lo(u.x), o[0]);
+          o[1] = fmaf(pv, bf16_hi(u.x), o[1]);
+          o[2] = fmaf(pv, bf16_lo(u.y), o[2]);
+          o[3] = fmaf(pv, bf16_hi(u.y), o[3]);
+        }
+      }
+      stage_release(slot);
+    }
+    consumers_sync();
+    if (aborted(c)) return;
+    const int64_t base = ((int64_t)b * S::NKV + g) * p.max_slots + slot_idx;
+    if (pv_thread)
+      *reinterpret_cast<float4*>(p.part_o + (base * G + ph) * D + 4 * pc) = make_float4(o[0], o[1], o[2], o[3]);
+    if (ct < G) {
+      p.part_ml[(base * G + ct) * 2 + 0] = np > 0 ? sm.am[ct] : -INFINITY;
+      p.part_ml[(base * G + ct) * 2 + 1] = np > 0 ? sm.al[ct] : 0.f;
+    }
+  }
+
+  // Merge of the slice partials of (b, g): warp per head ("Tasks": ATTN_COMBINE).
+  __device__ void attn_combine(const int32_t* w) {
+    constexpr int G = S::G, D = S::D, DPL = D / 32;
+    const int l = w[F_LAYER], b = w[F_A0], g = w[F_A0 + 1];
+    if (b >= p.B || cw >= G) return;
+    const bool full = p.window == 0 || (l + 1) % p.full_period == 0;
+    const int n = min(full ? slices_of(p, __ldg(p.seq_lens + b)) : p.n_static, p.max_slots);
+    const int h = cw;
+    const int64_t base = ((int64_t)b * S::NKV + g) * p.max_slots;
+    float M = -INFINITY;
+    for (int j = lane; j < n; j += 32) {
+      const float lj = __ldcg(p.part_ml + ((base + j) * G + h) * 2 + 1);
+      if (lj > 0.f) M = fmaxf(M, __ldcg(p.part_ml + ((base + j) * G + h) * 2));
+    }
+    M = warp_max(M);
+    float z = 0.f, acc[DPL];
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+    for (int j = 0; j < n; ++j) {
+      const float mj = __ldcg(p.part_ml + ((base + j) * G + h) * 2);
+      const float lj = __ldcg(p.part_ml + ((base + j) * G + h) * 2 + 1);
+      if (!(lj > 0.f)) continue;
+      const float cj = exp2f(mj - M);
+      z = fmaf(cj, lj, z);
+      const float* oj = p.part_o + ((base + j) * G + h) * D + lane * DPL;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) acc[i] = fmaf(cj, __ldcg(oj + i), acc[i]);
+    }
+    const float inv = 1.f / z;
+    uint16_t* dst = p.attn_out + (int64_t)b * S::NQ * D + (int64_t)(g * G + h) * D + lane * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) dst[i] = f_bf16(acc[i] * inv);
+  }
+
+  // ------------------------------------------------------------- norm
+  // Residual add + RMSNorm ("1. Reduce wave quantization": attention and MoE
+  // rejoin only at the fused residual add + RMSNorm at the end of the layer).
+  // Layer 0 starts from the embedding row; with the combine fused, the MoE
+  // output of the previous layer is summed here from the expert rows.
+  __device__ void norm(const int32_t* w) {
+    constexpr int PER = S::H / kConsumerThreads;
+    const int l = w[F_LAYER], b1 = min(w[F_A0 + 1], p.B);
+    const bool final_norm = w[F_A0 + 2] != 0, fused = w[F_A0 + 3] != 0;
+    for (int b = w[F_A0]; b < b1; ++b) {
+      float v[PER];
+      if (l == 0) {
+        const int sl = __ldg(p.seq_lens + b);
+        if ((sl < 1 || sl > p.max_ctx) && ct == 0) record_error(p, ERR_INDEX, c.sm, w, -1, (uint32_t)sl, (uint32_t)p.max_ctx);
+        int tok = __ldg(p.tokens + b);
+        if (tok < 0 || tok >= p.V) {
+          if (ct == 0) record_error(p, ERR_INDEX, c.sm, w, -1, (uint32_t)tok, (uint32_t)p.V);
+          tok = 0;
+        }
+#pragma unroll
+        for (int k = 0; k < PER; ++k) v[k] = bf16_f(__ldg(p.emb + (int64_t)tok * S::H + ct + k * kConsumerThreads));
+      } else {
+        int rows[S::K];
+        float wts[S::K];
+        if (fused) {
+#pragma unroll
+          for (int j = 0; j < S::K; ++j) {
+            int r = __ldcg(p.inv + b * S::K + j);
+            rows[j] = (r >= 0 && r < p.B * S::K) ? r : 0;
+            wts[j] = __ldcg(p.topk_w + ((int64_t)(l - 1) * p.MB + b) * S::K + j);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+          const int i = ct + k * kConsumerThreads;
+          float a = __ldcg(p.h + (int64_t)b * S::H + i);
+#pragma unroll
+          for (int g = 0; g < S::NKV; ++g) a += __ldcg(p.opart + ((int64_t)g * p.MB + b) * S::H + i);
+          if (fused) {
+            float m = 0.f;
+#pragma unroll
+            for (int j = 0; j < S::K; ++j) m = fmaf(wts[j], __ldcg(p.y + (int64_t)rows[j] * S::H + i), m);
+            a += m;
+          } else {
+            a += __ldcg(p.moe_out + (int64_t)b * S::H + i);
+          }
+          v[k] = a;
+        }
+      }
+      float ss = 0.f;
+#pragma unroll
+      for (int k = 0; k < PER; ++k) ss = fmaf(v[k], v[k], ss);
+      ss = warp_sum(ss);
+      if (lane == 0) sm.red[cw] = ss;
+      consumers_sync();
+      float tot = 0.f;
+#pragma unroll
+      for (int i = 0; i < kConsumerWarps; ++i) tot += sm.red[i];
+      const float inv_rms = 1.f / sqrtf(tot / (float)S::H + p.eps);
+      const float* gam = final_norm ? p.gamma_f : p.gamma + (int64_t)l * S::H;
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int i = ct + k * kConsumerThreads;
+        p.x[(int64_t)b * S::H + i] = f_bf16(v[k] * inv_rms * __ldg(gam + i));
+        p.h[(int64_t)b * S::H + i] = v[k];
+        if (p.htrace) p.htrace[((int64_t)l * p.MB + b) * S::H + i] = v[k];
+      }
+      consumers_sync();
+    }
+  }
+
+  // ------------------------------------------------------------ routing
+  // Top-k of each row's router logits (higher logit first, lower expert id on
+  // ties) and softmax weights over the selected logits ("Tasks": ROUTER_TOPK).
+  __device__ void topk(const int32_t* w) {
+    constexpr int E = S::E, K = S::K, PL = (E + 31) / 32;
+    const int l = w[F_LAYER], b1 = min(w[F_A0 + 1], p.B);
+    for (int b = w[F_A0] + cw; b < b1; b += kConsumerWarps) {
+      float v[PL];
+#pragma unroll
+      for (int k = 0; k < PL; ++k) {
+        const int e = lane + 32 * k;
+        v[k] = e < E ? __ldcg(p.rlog + ((int64_t)l * p.MB + b) * E + e) : -INFINITY;
+      }
+      int ids[K];
+      float vals[K];
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int k = 0; k < PL; ++k) {
+          const int e = lane + 32 * k;
+          if (e < E && (v[k] > bv || (v[k] == bv && e < bi))) {
+            bv = v[k];
+            bi = e;
+          }
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) {
+          const float ov = __shfl_xor_sync(FULL, bv, m);
+          const int oi = __shfl_xor_sync(FULL, bi, m);
+          if (ov > bv || (ov == bv && oi < bi)) {
+            bv = ov;
+            bi = oi;
+          }
+        }
+        ids[j] = bi;
+        vals[j] = bv;
+#pragma unroll
+        for (int k = 0; k < PL; ++k)
+          if (lane + 32 * k == bi) v[k] = -INFINITY;
+      }
+      if (lane == 0) {
+        float z = 0.f, e_[K];
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+          e_[j] = expf(vals[j] - vals[0]);
+          z += e_[j];
+        }
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+          p.topk_ids[((int64_t)l * p.MB + b) * K + j] = ids[j];
+          p.topk_w[((int64_t)l * p.MB + b) * K + j] = e_[j] / z;
+        }
+      }
+    }
+    if (w[F_A0 + 2]) {
+      consumers_sync();
+      finalize(l);
+    }
+  }
+
+  // Per-expert counts and offsets, the expert-ordered row list (rows of an
+  // expert by row b ascending) and the tile queues of the up/gate and down
+  // drains, experts ascending ("Tasks": ROUTE_FINALIZE generates the MoE GEMM
+  // work queue).  Deterministic: no order depends on atomics.
+  __device__ void finalize(int l) {
+    constexpr int E = S::E, K = S::K;
+    constexpr MoePlan mp = S::mp;
+    const int B = p.B;
+    for (int e = ct; e < E; e += kConsumerThreads) sm.mask[e] = 0ull;
+    consumers_sync();
+    for (int i = ct; i < B * K; i += kConsumerThreads) {
+      const int b = i / K;
+      int e = __ldcg(p.topk_ids + ((int64_t)l * p.MB + b) * K + (i - b * K));
+      if (e < 0 || e >= E) {
+        record_error(p, ERR_INDEX, c.sm, nullptr, -1, (uint32_t)e, E);
+        e = 0;
+      }
+      atomicOr(&sm.mask[e], 1ull << b);
+    }
+    consumers_sync();
+    if (cw == 0) {
+      constexpr int PL = (E + 31) / 32;
+      int cnt[PL], a[PL];
+      int rs = 0, as = 0;
+#pragma unroll
+      for (int k = 0; k < PL; ++k) {
+        const int e = lane * PL + k;
+        cnt[k] = e < E ? __popcll(sm.mask[e]) : 0;
+        a[k] = cnt[k] > 0;
+        rs += cnt[k];
+        as += a[k];
+      }
+      int ri = rs, ai = as;  // inclusive scans over lanes
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const int r2 = __shfl_up_sync(FULL, ri, m), a2 = __shfl_up_sync(FULL, ai, m);
+        if (lane >= m) {
+          ri += r2;
+          ai += a2;
+        }
+      }
+      int ro = ri - rs, ao = ai - as;
+#pragma unroll
+      for (int k = 0; k < PL; ++k) {
+        const int e = lane * PL + k;
+        if (e < E) {
+          sm.cnt[e] = cnt[k];
+          sm.off[e] = ro;
+          sm.act[e] = ao;
+        }
+        ro += cnt[k];
+        ao += a[k];
+      }
+      if (lane == 31) {
+        sm.off[E] = ri;
+        sm.act[E] = ai;
+      }
+    }
+    consumers_sync();
+    for (int i = ct; i < B * K; i += kConsumerThreads) {
+      const int b = i / K;
+      int e = __ldcg(p.topk_ids + ((int64_t)l * p.MB + b) * K + (i - b * K));
+      if (e < 0 || e >= E) e = 0;
+      const int rank = __popcll(sm.mask[e] & ((1ull << b) - 1ull));
+      const int row = sm.off[e] + rank;
+      p.perm[row] = i;
+      p.inv[i] = row;
+    }
+    for (int e = ct; e < E; e += kConsumerThreads) {
+      const int n = sm.cnt[e];
+      p.ecount[(int64_t)l * E + e] = n;
+      p.eoff[e] = sm.off[e];
+      if (n > 0) {
+        const int a = sm.act[e];
+        for (int t = 0; t < mp.up_tiles; ++t) p.upq[a * mp.up_tiles + t] = (e << 16) | t;
+        for (int t = 0; t < mp.dn_tiles; ++t) p.dnq[a * mp.dn_tiles + t] = (e << 16) | t;
+      }
+    }
+    if (ct == 0) {
+      p.eoff[E] = sm.off[E];
+      p.qlen[0] = sm.act[E] * mp.up_tiles;
+      p.qlen[1] = sm.act[E] * mp.dn_tiles;
+    }
+  }
+
+  // expert-ordered copy of the routed rows ("Tasks": MOE_GATHER)
+  __device__ void gather(const int32_t* w) {
+    constexpr int C = S::H / 8;
+    const int r0 = w[F_A0], r1 = min(r0 + w[F_A0 + 1], p.B * S::K);
+    for (int i = ct; i < (r1 - r0) * C; i += kConsumerThreads) {
+      const int r = r0 + i / C, cc = i % C;
+      int pr = __ldcg(p.perm + r);
+      int b = pr / S::K;
+      if (pr < 0 || b >= p.B) b = 0;
+      reinterpret_cast<uint4*>(p.xg + (int64_t)r * S::H)[cc] =
+          __ldcg(reinterpret_cast<const uint4*>(p.x + (int64_t)b * S::H) + cc);
+    }
+  }
+
+  // weighted sum of each row's expert outputs ("Tasks": MOE_COMBINE)
+  __device__ void moe_combine(const int32_t* w) {
+    const int l = w[F_LAYER], b1 = min(w[F_A0 + 1], p.B);
+    for (int b = w[F_A0]; b < b1; ++b) {
+      int rows[S::K];
+      float wts[S::K];
+#pragma unroll
+      for (int j = 0; j < S::K; ++j) {
+        const int r = __ldcg(p.inv + b * S::K + j);
+        rows[j] = (r >= 0 && r < p.B * S::K) ? r : 0;
+        wts[j] = __ldcg(p.topk_w + ((int64_t)l * p.MB + b) * S::K + j);
+      }
+      for (int i = ct; i < S::H; i += kConsumerThreads) {
+        float m = 0.f;
+#pragma unroll
+        for (int j = 0; j < S::K; ++j) m = fmaf(wts[j], __ldcg(p.y + (int64_t)rows[j] * S::H + i), m);
+        p.moe_out[(int64_t)b * S::H + i] = m;
+      }
+    }
+  }
+
+  __device__ void execute(const int32_t* w) {
+    switch (w[F_OP]) {
+      case OP_QKV_PROJ:
+      case OP_ROUTER_GEMM:
+      case OP_LM_HEAD: gemv_item<S::H>(w, S::SR_H, w[F_A0 + 1], p.B); break;
+      case OP_O_PROJ: gemv_item<S::G * S::D>(w, S::SR_O, w[F_A0 + 1], p.B); break;
+      case W_UP_TILE: gemv_item<S::H>(w, 2 * S::mp.up_half, 2 * S::mp.up_half * S::mp.up_stages, w[F_A0 + 3]); break;
+      case W_DOWN_TILE: gemv_item<S::I>(w, S::mp.dn_rows, S::mp.dn_tile, w[F_A0 + 3]); break;
+      case W_ATTN: attn(w); break;
+      case OP_ATTN_COMBINE: attn_combine(w); break;
+      case OP_RESID_NORM: norm(w); break;
+      case OP_ROUTER_TOPK: topk(w); break;
+      case OP_ROUTE_FINALIZE: finalize(w[F_LAYER]); break;
+      case OP_MOE_GATHER: gather(w); break;
+      case OP_MOE_COMBINE: moe_combine(w); break;
+      default: break;  // NOP, CLAIM_END: only the signal
+    }
+  }
+
+  __device__ void run() {
+    for (;;) {
+      const int slot = c.wk % kWorkRing;
+      bool ok = mbar_wait(p, c, &c.hdr->wfull[slot], (c.wk / kWorkRing) & 1);
+      int32_t w[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) w[k] = c.hdr->work[slot][k];
+      if (ok && ct == 0) {
+        ok = wait_counter(p, c, w[F_WAIT0], (uint32_t)(w[F_TGT0] == TGT_DYN_SPLITS
+                                                             ? (w[F_A0] < p.B ? slices_of(p, __ldg(p.seq_lens + w[F_A0])) : 0)
+                                                             : w[F_TGT0]), w) &&
+             wait_counter(p, c, w[F_WAIT1], (uint32_t)w[F_TGT1], w);
+      }
+      if (bar_or(kBarConsumers, kConsumerThreads, !ok || aborted(c))) return;
+      if (ct == 0) mbar_arrive(&c.hdr->wempty[slot]);
+      ++c.wk;
+      if (w[F_OP] == W_EXIT) return;
+      execute(w);
+      if (bar_or(kBarConsumers, kConsumerThreads, aborted(c))) return;
+      if (ct == 0) {
+        if (w[F_SIG0] >= 0) red_release_add(p.bars + w[F_SIG0], 1u);
+        if (w[F_SIG1] >= 0) red_release_add(p.bars + w[F_SIG1], 1u);
+      }
+    }
+  }
+};
+
+template <class S>
+__global__ void __launch_bounds__(kThreads, 1) mk_persistent(const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Hdr* hdr = reinterpret_cast<Hdr*>(smem + (size_t)kStages * kStageBytes);
+  Scratch<S>* scr = reinterpret_cast<Scratch<S>*>(smem + (size_t)kStages * kStageBytes + sizeof(Hdr));
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&hdr->full[i], 1);
+      mbar_init(&hdr->empty[i], kConsumerWarps);
+    }
+    for (int i = 0; i < kDescRing; ++i) {
+      mbar_init(&hdr->dfull[i], 1);
+      mbar_init(&hdr->dempty[i], 1);
+    }
+    for (int i = 0; i < kWorkRing; ++i) {
+      mbar_init(&hdr->wfull[i], 1);
+      mbar_init(&hdr->wempty[i], 1);
+    }
+    hdr->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  Ctx c{hdr, smem, (int)blockIdx.x, 0u, 0u};
+  const int warp = threadIdx.x / 32;
+  if (warp == 0) {
+    controller(p, c);
+  } else if (warp == 1) {
+    Producer<S> pr{p, c};
+    pr.run();
+  } else {
+    const int ct = threadIdx.x - 64;
+    Consumer<S> cs{p, c, *scr, ct, ct / 32, ct & 31};
+    cs.run();
+  }
+}
+
+}  // namespace dev
+}  // namespace mk

@@ -1,0 +1,805 @@
+// mk_sched.cpp -- the host task scheduler: builds the per-SM task lists of
+// one decode step, validates them, and simulates them on the host.
+//
+// "Cohere: a decode megakernel for North Mini Code", section "Task
+// scheduler": the host builds named waves per layer, puts them in a chosen
+// order, flattens them into one list and assigns task k to SM k mod #SMs;
+// full attention and the MoE, whose sizes depend on live sequence lengths and
+// routing, are drained from shared queues by a fixed number of claimer tasks.
+// Section "How do you write a megakernel?": a wrong arrive count drifts warps
+// onto other tasks and deadlocks much later, so barrier accounting gets
+// explicit invariants -- the validator and the simulator below.
+#include <algorithm>
+#include <cstring>
+#include <deque>
+#include <random>
+#include <sstream>
+
+#include "mk_host.h"
+
+namespace mk {
+
+bool is_full_layer(const mk_config& c, int l) {
+  return c.window == 0 || (l + 1) % c.full_period == 0;
+}
+
+int attn_slices(const mk_sched* s, int seq_len) {
+  return (seq_len + s->split_len - 1) / s->split_len;
+}
+
+size_t WsLayout::off(const char* name) const {
+  for (auto& r : regions)
+    if (r.first == name) return r.second;
+  return (size_t)-1;
+}
+
+size_t WsLayout::add(const char* name, size_t bytes) {
+  total = (total + 255) & ~(size_t)255;
+  regions.emplace_back(name, total);
+  size_t o = total;
+  total += bytes;
+  return o;
+}
+
+namespace {
+
+Desc blank(int op, int layer) {
+  Desc d;
+  d.fill(0);
+  d[F_OP] = op;
+  d[F_LAYER] = layer;
+  d[F_WAIT0] = d[F_WAIT1] = -1;
+  d[F_SIG0] = d[F_SIG1] = -1;
+  return d;
+}
+
+struct Builder {
+  mk_sched* s;
+  int MB, L, E, NKV, K;
+  int nbars = 0;
+
+  int bar(BarKind k, int n = 1) {
+    int b = nbars;
+    nbars += n;
+    for (int i = 0; i < n; ++i) s->bar_kind.push_back(k);
+    return b;
+  }
+
+  void alloc_layer_bars() {
+    s->lb.assign(L + 1, LayerBars());
+    for (int l = 0; l <= L; ++l) {
+      LayerBars& b = s->lb[l];
+      b.norm = bar(BK_STATIC);
+      if (l == L) break;
+      b.qkv = bar(BK_STATIC, NKV);
+      b.router = bar(BK_STATIC);
+      b.topk = bar(BK_STATIC);
+      b.fin = bar(BK_STATIC);
+      if (s->opts.explicit_gather) b.gather = bar(BK_STATIC);
+      b.cnt = bar(BK_ATTN_COUNT, MB * NKV);
+      b.acomb = bar(BK_STATIC, NKV);
+      b.up = bar(BK_UP_EXPERT, E);
+      b.upd = bar(BK_STATIC);
+      b.dnd = bar(BK_STATIC);
+      if (!s->opts.fuse_moe_combine) b.mcomb = bar(BK_STATIC);
+      b.o = bar(BK_STATIC);
+      b.attn_done = bar(BK_STATIC);
+      b.claim_attn = bar(BK_CLAIM);
+      b.claim_up = bar(BK_CLAIM);
+      b.claim_dn = bar(BK_CLAIM);
+    }
+    s->lm_bar = bar(BK_STATIC);
+  }
+
+  static void wait(Desc& d, int slot, int b, int tgt) {
+    d[slot == 0 ? F_WAIT0 : F_WAIT1] = b;
+    d[slot == 0 ? F_TGT0 : F_TGT1] = tgt;
+  }
+
+  // -------- waves of one layer
+  std::vector<Desc> norm_wave(int l, int rows_per_task) {
+    std::vector<Desc> w;
+    LayerBars& b = s->lb[l];
+    for (int b0 = 0; b0 < MB; b0 += rows_per_task) {
+      Desc d = blank(OP_RESID_NORM, l);
+      d[F_A0] = b0;
+      d[F_A0 + 1] = std::min(MB, b0 + rows_per_task);
+      d[F_A0 + 2] = (l == L);
+      d[F_A0 + 3] = s->opts.fuse_moe_combine;
+      if (l > 0) {
+        LayerBars& p = s->lb[l - 1];
+        wait(d, 0, p.o, p.n_o);
+        if (s->opts.fuse_moe_combine) wait(d, 1, p.dnd, p.n_dn_claim);
+        else wait(d, 1, p.mcomb, p.n_mcomb);
+      }
+      d[F_SIG0] = b.norm;
+      w.push_back(d);
+    }
+    b.n_norm = (int)w.size();
+    return w;
+  }
+
+  std::vector<Desc> dense_wave(int op, int l, int rows, int tile, int sig) {
+    std::vector<Desc> w;
+    for (int r0 = 0; r0 < rows; r0 += tile) {
+      Desc d = blank(op, l);
+      d[F_A0] = r0;
+      d[F_A0 + 1] = std::min(tile, rows - r0);
+      d[F_SIG0] = sig;
+      w.push_back(d);
+    }
+    return w;
+  }
+};
+
+int auto_split_pages(const mk_sched* s) {
+  if (s->opts.attn_split_pages > 0) return s->opts.attn_split_pages;
+  const int P = s->cfg.page_size;
+  // about two KV slices per SM for a full-attention layer at the largest batch and context
+  const double tok = (double)s->max_batch * s->cfg.n_kv * s->max_ctx / (2.0 * s->num_sms);
+  int pages = (int)((tok + P - 1) / P);
+  return std::max(1, std::min(pages, 64));
+}
+
+}  // namespace
+
+static int build(mk_sched* s) {
+  const mk_config& c = s->cfg;
+  const ShapeDims& D = s->dims;
+  const MoePlan& mp = s->plan;
+  Builder B{s, s->max_batch, c.n_layers, D.E, D.NKV, D.K};
+  const int MB = s->max_batch, L = c.n_layers, NKV = D.NKV, G = D.NQ / D.NKV;
+  const int QKVROWS = (D.NQ + 2 * D.NKV) * D.D;
+  const mk_sched_opts& o = s->opts;
+
+  s->split_len = auto_split_pages(s) * c.page_size;
+  const int full_slices = (s->max_ctx + s->split_len - 1) / s->split_len;
+  s->n_static = 0;
+  if (c.window > 0) {
+    const int w_slices = (c.window + s->split_len - 1) / s->split_len + 1;
+    s->n_static = std::min(full_slices, w_slices);
+  }
+  s->max_slots = std::max(full_slices, s->n_static);
+  s->max_attn_entries = MB * NKV * full_slices;
+
+  // tile sizes (multiples of the stage rows)
+  const int sr_h = stage_rows(D.H), sr_o = stage_rows(G * D.D);
+  auto round_to = [](int v, int m) { return std::max(m, (v / m) * m); };
+  const int qkv_tile = o.qkv_tile_rows > 0 ? round_to(o.qkv_tile_rows, sr_h) : std::min(64, D.D);
+  if (D.D % qkv_tile != 0 || qkv_tile % sr_h != 0)
+    return fail(MK_ERR_ARG, "qkv_tile_rows must divide head_dim and be a multiple of the stage rows");
+  const int o_tile = o.o_tile_rows > 0 ? round_to(o.o_tile_rows, sr_o) : round_to(64, sr_o);
+  const int lm_tile = o.lm_tile_rows > 0 ? round_to(o.lm_tile_rows, sr_h) : round_to(128, sr_h);
+  const int router_tile = sr_h * std::max(1, 16 / sr_h);
+  const int n_moe = o.moe_claimers > 0 ? o.moe_claimers : s->num_sms;
+  const int attn_claim_default = std::min(s->num_sms, std::max(1, MB * NKV * full_slices));
+  const int n_attn = o.attn_claimers > 0 ? o.attn_claimers : attn_claim_default;
+  const int norm_rows = 4;
+
+  B.alloc_layer_bars();
+  std::vector<Desc> all;
+
+  for (int l = 0; l < L; ++l) {
+    LayerBars& lb = s->lb[l];
+    const bool full = is_full_layer(c, l);
+    std::vector<Desc> w_norm = B.norm_wave(l, norm_rows);
+
+    // QKV: one row tile never straddles a head, so it belongs to one KV group
+    std::vector<Desc> w_qkv;
+    lb.n_qkv_g.assign(NKV, 0);
+    for (int r0 = 0; r0 < QKVROWS; r0 += qkv_tile) {
+      Desc d = blank(OP_QKV_PROJ, l);
+      d[F_A0] = r0;
+      d[F_A0 + 1] = qkv_tile;
+      const int head = r0 / D.D;
+      const int g = head < D.NQ ? head / G : (head < D.NQ + NKV ? head - D.NQ : head - D.NQ - NKV);
+      B.wait(d, 0, lb.norm, lb.n_norm);
+      d[F_SIG0] = lb.qkv + g;
+      lb.n_qkv_g[g]++;
+      w_qkv.push_back(d);
+    }
+
+    std::vector<Desc> w_router = B.dense_wave(OP_ROUTER_GEMM, l, D.E, router_tile, lb.router);
+    for (auto& d : w_router) B.wait(d, 0, lb.norm, lb.n_norm);
+    lb.n_router = (int)w_router.size();
+
+    std::vector<Desc> w_topk, w_fin;
+    const bool fuse_fin = o.fuse_finalize && MB <= kConsumerWarps;
+    const int topk_rows = kConsumerWarps;
+    for (int b0 = 0; b0 < MB; b0 += topk_rows) {
+      Desc d = blank(OP_ROUTER_TOPK, l);
+      d[F_A0] = b0;
+      d[F_A0 + 1] = std::min(MB, b0 + topk_rows);
+      d[F_A0 + 2] = fuse_fin ? 1 : 0;
+      B.wait(d, 0, lb.router, lb.n_router);
+      d[F_SIG0] = lb.topk;
+      if (fuse_fin) d[F_SIG1] = lb.fin;
+      w_topk.push_back(d);
+    }
+    lb.n_topk = (int)w_topk.size();
+    if (!fuse_fin) {
+      Desc d = blank(OP_ROUTE_FINALIZE, l);
+      B.wait(d, 0, lb.topk, lb.n_topk);
+      d[F_SIG0] = lb.fin;
+      w_fin.push_back(d);
+    }
+
+    std::vector<Desc> w_gather;
+    if (o.explicit_gather) {
+      const int rows = MB * D.K, per = 64;
+      for (int r0 = 0; r0 < rows; r0 += per) {
+        Desc d = blank(OP_MOE_GATHER, l);
+        d[F_A0] = r0;
+        d[F_A0 + 1] = std::min(per, rows - r0);
+        B.wait(d, 0, lb.fin, 1);
+        d[F_SIG0] = lb.gather;
+        w_gather.push_back(d);
+      }
+      lb.n_gather = (int)w_gather.size();
+    }
+
+    // attention: static slices for sliding layers, claimers for full layers
+    std::vector<Desc> w_attn;
+    if (full) {
+      for (int i = 0; i < n_attn; ++i) {
+        Desc d = blank(OP_ATTN_DRAIN, l);
+        d[F_A0] = lb.claim_attn;
+        d[F_A0 + 1] = lb.cnt;
+        d[F_A0 + 2] = lb.qkv;
+        d[F_SIG0] = lb.attn_done;
+        w_attn.push_back(d);
+      }
+      lb.n_attn_claim = n_attn;
+    } else {
+      for (int b = 0; b < MB; ++b)
+        for (int g = 0; g < NKV; ++g)
+          for (int j = 0; j < s->n_static; ++j) {
+            Desc d = blank(OP_ATTN_DECODE, l);
+            d[F_A0] = b;
+            d[F_A0 + 1] = g;
+            d[F_A0 + 2] = j;
+            d[F_A0 + 3] = lb.cnt;
+            B.wait(d, 0, lb.qkv + g, lb.n_qkv_g[g]);
+            d[F_SIG0] = lb.cnt + b * NKV + g;
+            w_attn.push_back(d);
+          }
+    }
+    // the QKV targets per group, for the drained slices
+    for (auto& d : w_attn)
+      if (d[F_OP] == OP_ATTN_DRAIN) d[F_A0 + 3] = lb.n_qkv_g[0];
+
+    std::vector<Desc> w_acomb;
+    lb.n_acomb_g.assign(NKV, 0);
+    for (int b = 0; b < MB; ++b)
+      for (int g = 0; g < NKV; ++g) {
+        Desc d = blank(OP_ATTN_COMBINE, l);
+        d[F_A0] = b;
+        d[F_A0 + 1] = g;
+        d[F_A0 + 2] = lb.cnt;
+        B.wait(d, 0, lb.cnt + b * NKV + g, full ? TGT_DYN_SPLITS : s->n_static);
+        d[F_SIG0] = lb.acomb + g;
+        lb.n_acomb_g[g]++;
+        w_acomb.push_back(d);
+      }
+
+    std::vector<Desc> w_up, w_dn, w_mcomb;
+    for (int i = 0; i < n_moe; ++i) {
+      Desc d = blank(OP_MOE_UPGATE_ACT_DRAIN, l);
+      B.wait(d, 0, lb.fin, 1);
+      d[F_A0] = lb.claim_up;
+      d[F_A0 + 1] = lb.up;
+      d[F_A0 + 2] = o.explicit_gather ? lb.gather : -1;
+      d[F_A0 + 3] = o.explicit_gather ? lb.n_gather : 0;
+      d[F_SIG0] = lb.upd;
+      w_up.push_back(d);
+      Desc e = blank(OP_MOE_DOWN_DRAIN, l);
+      B.wait(e, 0, lb.fin, 1);
+      e[F_A0] = lb.claim_dn;
+      e[F_A0 + 1] = lb.up;
+      e[F_A0 + 2] = mp.up_tiles;
+      e[F_SIG0] = lb.dnd;
+      w_dn.push_back(e);
+    }
+    lb.n_up_claim = lb.n_dn_claim = n_moe;
+    if (!o.fuse_moe_combine) {
+      for (int b0 = 0; b0 < MB; b0 += norm_rows) {
+        Desc d = blank(OP_MOE_COMBINE, l);
+        d[F_A0] = b0;
+        d[F_A0 + 1] = std::min(MB, b0 + norm_rows);
+        B.wait(d, 0, lb.dnd, lb.n_dn_claim);
+        d[F_SIG0] = lb.mcomb;
+        w_mcomb.push_back(d);
+      }
+      lb.n_mcomb = (int)w_mcomb.size();
+    }
+
+    std::vector<Desc> w_o;
+    for (int r0 = 0; r0 < D.H; r0 += o_tile)
+      for (int g = 0; g < NKV; ++g) {
+        Desc d = blank(OP_O_PROJ, l);
+        d[F_A0] = r0;
+        d[F_A0 + 1] = std::min(o_tile, D.H - r0);
+        d[F_A0 + 2] = g;
+        B.wait(d, 0, lb.acomb + g, lb.n_acomb_g[g]);
+        d[F_SIG0] = lb.o;
+        w_o.push_back(d);
+      }
+    lb.n_o = (int)w_o.size();
+
+    auto add = [&](std::vector<Desc>& w) { all.insert(all.end(), w.begin(), w.end()); };
+    add(w_norm);
+    add(w_qkv);
+    add(w_router);
+    add(w_topk);
+    add(w_fin);
+    add(w_gather);
+    add(w_attn);
+    switch (o.wave_order) {
+      case MK_WAVES_INTERLEAVED:
+        add(w_up); add(w_dn); add(w_acomb); add(w_mcomb); add(w_o);
+        break;
+      case MK_WAVES_ATTN_FIRST:
+        add(w_acomb); add(w_o); add(w_up); add(w_dn); add(w_mcomb);
+        break;
+      default:
+        add(w_acomb); add(w_up); add(w_dn); add(w_o); add(w_mcomb);
+        break;
+    }
+  }
+  // final RMSNorm and LM head
+  std::vector<Desc> w_final = B.norm_wave(L, norm_rows);
+  all.insert(all.end(), w_final.begin(), w_final.end());
+  for (int r0 = 0; r0 < c.vocab; r0 += lm_tile) {
+    Desc d = blank(OP_LM_HEAD, L);
+    d[F_A0] = r0;
+    d[F_A0 + 1] = std::min(lm_tile, c.vocab - r0);
+    B.wait(d, 0, s->lb[L].norm, s->lb[L].n_norm);
+    d[F_SIG0] = s->lm_bar;
+    all.push_back(d);
+  }
+
+  // flatten: task k -> SM k mod #SMs
+  s->tasks = std::move(all);
+  s->per_sm.assign(s->num_sms, {});
+  for (int k = 0; k < (int)s->tasks.size(); ++k) {
+    s->tasks[k][F_TASK] = k;
+    s->per_sm[k % s->num_sms].push_back(k);
+  }
+  return MK_OK;
+}
+
+static void layout_workspace(mk_sched* s) {
+  const ShapeDims& D = s->dims;
+  const int MB = s->max_batch, L = s->cfg.n_layers, G = D.NQ / D.NKV;
+  WsLayout& w = s->ws;
+  w = WsLayout();
+  w.add("barriers", sizeof(uint32_t) * s->bar_kind.size());
+  w.add("error", sizeof(uint32_t) * 8);
+  w.add("h", sizeof(float) * MB * D.H);
+  w.add("x", 2ull * MB * D.H);
+  w.add("q", sizeof(float) * MB * D.NQ * D.D);
+  w.add("kvnew", 2ull * MB * 2 * D.NKV * D.D);
+  w.add("part_o", sizeof(float) * (size_t)MB * D.NKV * s->max_slots * G * D.D);
+  w.add("part_ml", sizeof(float) * (size_t)MB * D.NKV * s->max_slots * G * 2);
+  w.add("attn_out", 2ull * MB * D.NQ * D.D);
+  w.add("opart", sizeof(float) * (size_t)D.NKV * MB * D.H);
+  w.add("router_logits", sizeof(float) * (size_t)L * MB * D.E);
+  w.add("topk_ids", sizeof(int32_t) * (size_t)L * MB * D.K);
+  w.add("topk_w", sizeof(float) * (size_t)L * MB * D.K);
+  w.add("expert_count", sizeof(int32_t) * (size_t)L * D.E);
+  w.add("expert_offset", sizeof(int32_t) * (D.E + 1));
+  w.add("perm", sizeof(int32_t) * MB * D.K);
+  w.add("inv", sizeof(int32_t) * MB * D.K);
+  w.add("moe_queue", sizeof(int32_t) * (size_t)D.E * s->plan.up_tiles);
+  w.add("moe_down_queue", sizeof(int32_t) * (size_t)D.E * s->plan.dn_tiles);
+  w.add("moe_queue_len", sizeof(int32_t) * 2);
+  w.add("xg", s->opts.explicit_gather ? 2ull * MB * D.K * D.H : 16);
+  w.add("u", 2ull * MB * D.K * D.I);
+  w.add("y", sizeof(float) * (size_t)MB * D.K * D.H);
+  w.add("moe_out", sizeof(float) * (size_t)MB * D.H);
+  if (s->opts.trace_hidden) w.add("hidden_trace", sizeof(float) * (size_t)(L + 1) * MB * D.H);
+  w.total = (w.total + 255) & ~(size_t)255;
+}
+
+// ------------------------------------------------------------- validation
+
+// Every barrier a task waits on must be fed by tasks that can run first, and
+// a static barrier must receive exactly the count its waiters expect.  The
+// lists are deadlock-free iff the graph of (list order on each SM) plus
+// (producer -> barrier -> waiter) edges has no cycle.
+static int validate(const mk_sched* s) {
+  const int T = (int)s->tasks.size();
+  const int NB = (int)s->bar_kind.size();
+  std::vector<int> signals(NB, 0);
+  std::vector<int> expect(NB, -1);
+  std::vector<std::vector<int>> producers(NB), waiters(NB);
+  auto add_wait = [&](int task, int bar, int tgt) {
+    if (bar < 0) return 0;
+    if (bar >= NB) return fail(MK_ERR_ARG, "task " + std::to_string(task) + " waits on barrier out of range");
+    waiters[bar].push_back(task);
+    if (s->bar_kind[bar] == BK_STATIC) {
+      if (expect[bar] >= 0 && expect[bar] != tgt)
+        return fail(MK_ERR_ARG, "barrier " + std::to_string(bar) + " waited on with two counts");
+      expect[bar] = tgt;
+    }
+    return 0;
+  };
+  for (int t = 0; t < T; ++t) {
+    const Desc& d = s->tasks[t];
+    const int op = d[F_OP];
+    if (op < 0 || op >= OP_COUNT) return fail(MK_ERR_ARG, "task " + std::to_string(t) + " has a bad opcode");
+    for (int k : {F_SIG0, F_SIG1}) {
+      const int b = d[k];
+      if (b < 0) continue;
+      if (b >= NB) return fail(MK_ERR_ARG, "task " + std::to_string(t) + " signals barrier out of range");
+      signals[b]++;
+      producers[b].push_back(t);
+    }
+    if (add_wait(t, d[F_WAIT0], d[F_TGT0]) || add_wait(t, d[F_WAIT1], d[F_TGT1])) return MK_ERR_ARG;
+    // claimers: the tiles they run feed and wait on per-expert / per-row barriers
+    if (op == OP_MOE_UPGATE_ACT_DRAIN)
+      for (int e = 0; e < s->dims.E; ++e) producers[d[F_A0 + 1] + e].push_back(t);
+    if (op == OP_MOE_DOWN_DRAIN)
+      for (int e = 0; e < s->dims.E; ++e) waiters[d[F_A0 + 1] + e].push_back(t);
+    if (op == OP_ATTN_DRAIN)
+      for (int i = 0; i < s->max_batch * s->dims.NKV; ++i) producers[d[F_A0 + 1] + i].push_back(t);
+  }
+  for (int b = 0; b < NB; ++b) {
+    if (s->bar_kind[b] != BK_STATIC) continue;
+    if (expect[b] >= 0 && signals[b] != expect[b])
+      return fail(MK_ERR_ARG, "barrier " + std::to_string(b) + " receives " + std::to_string(signals[b]) +
+                                  " arrivals but is waited on for " + std::to_string(expect[b]));
+  }
+  // static slices of a sliding layer: the combine's count must equal the slices
+  for (const Desc& d : s->tasks) {
+    if (d[F_OP] != OP_ATTN_COMBINE || d[F_TGT0] == TGT_DYN_SPLITS) continue;
+    const int b = d[F_WAIT0];
+    int n = 0;
+    for (int p : producers[b])
+      if (s->tasks[p][F_OP] == OP_ATTN_DECODE) ++n;
+    if (n != d[F_TGT0])
+      return fail(MK_ERR_ARG, "attention counter " + std::to_string(b) + " gets " + std::to_string(n) +
+                                  " slices, combine waits for " + std::to_string(d[F_TGT0]));
+  }
+  // cycle check (Kahn) over tasks and barriers
+  const int N = T + NB;
+  std::vector<std::vector<int>> adj(N);
+  std::vector<int> indeg(N, 0);
+  auto edge = [&](int a, int b) { adj[a].push_back(b); indeg[b]++; };
+  for (const auto& lst : s->per_sm)
+    for (size_t i = 1; i < lst.size(); ++i) edge(lst[i - 1], lst[i]);
+  for (int b = 0; b < NB; ++b) {
+    for (int p : producers[b]) edge(p, T + b);
+    for (int w : waiters[b]) edge(T + b, w);
+  }
+  std::deque<int> q;
+  for (int i = 0; i < N; ++i)
+    if (indeg[i] == 0) q.push_back(i);
+  int seen = 0;
+  while (!q.empty()) {
+    int v = q.front();
+    q.pop_front();
+    ++seen;
+    for (int w : adj[v])
+      if (--indeg[w] == 0) q.push_back(w);
+  }
+  if (seen != N) {
+    for (int i = 0; i < T; ++i)
+      if (indeg[i] > 0)
+        return fail(MK_ERR_ARG, "cyclic wait: task " + std::to_string(i) + " (op " +
+                                    std::to_string(s->tasks[i][F_OP]) + ", layer " +
+                                    std::to_string(s->tasks[i][F_LAYER]) + ") can never start");
+    return fail(MK_ERR_ARG, "cyclic wait between barriers");
+  }
+  // every waited barrier has at least one producer
+  for (int b = 0; b < NB; ++b)
+    if (!waiters[b].empty() && producers[b].empty() && s->bar_kind[b] != BK_CLAIM)
+      return fail(MK_ERR_ARG, "barrier " + std::to_string(b) + " is waited on but never signalled");
+  return MK_OK;
+}
+
+// ------------------------------------------------------------- simulation
+
+namespace {
+
+struct SimQueue {
+  std::vector<int32_t> entries;
+};
+
+struct Sim {
+  const mk_sched* s;
+  int B;
+  std::vector<int32_t> seq;
+  std::vector<int32_t> routing;  // [L][B][K]
+  std::vector<int64_t> bars;
+  std::vector<int> pos;            // next task per SM
+  std::vector<int> pending;        // claimed entry index per SM (-1 none)
+  std::vector<int32_t> attn_q;
+  std::vector<std::vector<int32_t>> up_q, dn_q;  // per layer
+  std::vector<int8_t> fin_done;
+  std::string err;
+
+  int64_t target(const Desc& d, int slot) {
+    const int tgt = d[slot == 0 ? F_TGT0 : F_TGT1];
+    if (tgt != TGT_DYN_SPLITS) return tgt;
+    // combine of (b, g) in a full layer: the row's slice count (0 past the batch)
+    const int b = d[F_A0];
+    return b < B ? attn_slices(s, seq[b]) : 0;
+  }
+
+  bool waits_ok(const Desc& d) {
+    for (int slot = 0; slot < 2; ++slot) {
+      const int b = d[slot == 0 ? F_WAIT0 : F_WAIT1];
+      if (b >= 0 && bars[b] < target(d, slot)) return false;
+    }
+    return true;
+  }
+
+  void signal(const Desc& d) {
+    if (d[F_SIG0] >= 0) bars[d[F_SIG0]]++;
+    if (d[F_SIG1] >= 0) bars[d[F_SIG1]]++;
+  }
+
+  void finalize(int l) {
+    const ShapeDims& D = s->dims;
+    std::vector<int> count(D.E, 0);
+    for (int b = 0; b < B; ++b)
+      for (int j = 0; j < D.K; ++j) count[routing[((size_t)l * B + b) * D.K + j]]++;
+    up_q[l].clear();
+    dn_q[l].clear();
+    for (int e = 0; e < D.E; ++e) {
+      if (!count[e]) continue;
+      for (int t = 0; t < s->plan.up_tiles; ++t) up_q[l].push_back((e << 16) | t);
+      for (int t = 0; t < s->plan.dn_tiles; ++t) dn_q[l].push_back((e << 16) | t);
+    }
+    fin_done[l] = 1;
+  }
+
+  // One step of SM `sm`; returns true if it made progress.
+  bool step(int sm) {
+    const auto& lst = s->per_sm[sm];
+    if (pos[sm] >= (int)lst.size()) return false;
+    const Desc& d = s->tasks[lst[pos[sm]]];
+    const int op = d[F_OP], l = d[F_LAYER];
+    const int NKV = s->dims.NKV;
+    if (!waits_ok(d)) return false;
+    switch (op) {
+      case OP_ROUTER_TOPK:
+        if (d[F_A0 + 2]) finalize(l);
+        signal(d);
+        break;
+      case OP_ROUTE_FINALIZE:
+        finalize(l);
+        signal(d);
+        break;
+      case OP_ATTN_DRAIN: {
+        const int claim = d[F_A0];
+        if (pending[sm] < 0) {
+          const int64_t i = bars[claim]++;
+          if (i >= (int64_t)attn_q.size()) {
+            signal(d);
+            break;
+          }
+          pending[sm] = (int)i;
+        }
+        const int32_t e = attn_q[pending[sm]];
+        const int b = (e >> 24) & 0xff, g = (e >> 20) & 0xf;
+        if (bars[d[F_A0 + 2] + g] < d[F_A0 + 3]) return false;  // QKV of this group not done
+        bars[d[F_A0 + 1] + b * NKV + g]++;
+        pending[sm] = -1;
+        return true;  // the claimer stays on this task
+      }
+      case OP_MOE_UPGATE_ACT_DRAIN:
+      case OP_MOE_DOWN_DRAIN: {
+        if (!fin_done[l]) {
+          err = "MoE claimer ran before its queue was built (layer " + std::to_string(l) + ")";
+          return false;
+        }
+        const bool up = op == OP_MOE_UPGATE_ACT_DRAIN;
+        auto& q = up ? up_q[l] : dn_q[l];
+        const int claim = d[F_A0];
+        if (pending[sm] < 0) {
+          const int64_t i = bars[claim]++;
+          if (i >= (int64_t)q.size()) {
+            signal(d);
+            break;
+          }
+          pending[sm] = (int)i;
+        }
+        const int e = q[pending[sm]] >> 16;
+        if (up) {
+          if (d[F_A0 + 2] >= 0 && bars[d[F_A0 + 2]] < d[F_A0 + 3]) return false;
+          bars[d[F_A0 + 1] + e]++;
+        } else {
+          if (bars[d[F_A0 + 1] + e] < d[F_A0 + 2]) return false;  // up tiles of e not done
+        }
+        pending[sm] = -1;
+        return true;
+      }
+      default:
+        signal(d);
+        break;
+    }
+    pos[sm]++;
+    return true;
+  }
+};
+
+}  // namespace
+
+static void build_attn_queue(const mk_sched* s, int B, const int32_t* seq, std::vector<int32_t>& q) {
+  q.clear();
+  for (int b = 0; b < B; ++b)
+    for (int g = 0; g < s->dims.NKV; ++g)
+      for (int j = 0; j < attn_slices(s, seq[b]); ++j) q.push_back((b << 24) | (g << 20) | j);
+}
+
+}  // namespace mk
+
+using namespace mk;
+
+extern "C" {
+
+void mk_default_sched_opts(mk_sched_opts* o) {
+  std::memset(o, 0, sizeof(*o));
+  o->fuse_finalize = 1;
+  o->fuse_moe_combine = 1;
+}
+
+int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const mk_sched_opts* opts,
+                   mk_sched** out) {
+  if (!m || !out) return fail(MK_ERR_ARG, "null argument");
+  *out = nullptr;
+  if (max_batch < 1 || max_batch > kMaxBatch) return fail(MK_ERR_ARG, "max_batch must be in [1, 64]");
+  if (max_ctx < 1) return fail(MK_ERR_ARG, "max_ctx must be >= 1");
+  mk_sched* s = new mk_sched();
+  s->cfg = m->cfg;
+  s->dims = m->dims;
+  s->plan = m->plan;
+  if (opts) s->opts = *opts;
+  else mk_default_sched_opts(&s->opts);
+  s->max_batch = max_batch;
+  s->max_ctx = max_ctx;
+  s->num_sms = s->opts.num_sms;
+  if (s->num_sms <= 0) {
+    s->num_sms = query_num_sms();
+    if (s->num_sms <= 0) {
+      delete s;
+      return fail(MK_ERR_CUDA, "cannot query the SM count (no device?); pass opts.num_sms");
+    }
+  }
+  if (s->opts.wave_order < 0 || s->opts.wave_order > 2) {
+    delete s;
+    return fail(MK_ERR_ARG, "unknown wave order");
+  }
+  s->watchdog_ns = (int64_t)(s->opts.watchdog_ms > 0 ? s->opts.watchdog_ms : 2000) * 1000000;
+  int rc = build(s);
+  if (rc == MK_OK) rc = validate(s);
+  if (rc != MK_OK) {
+    delete s;
+    return rc;
+  }
+  layout_workspace(s);
+  *out = s;
+  return MK_OK;
+}
+
+void mk_free_sched(mk_sched* s) { delete s; }
+
+size_t mk_sched_bytes(const mk_sched* s) {
+  if (!s) return 0;
+  return sizeof(int32_t) * (2 * (size_t)s->num_sms + 32 * s->tasks.size()) + 128;
+}
+
+size_t mk_workspace_bytes(const mk_sched* s) { return s ? s->ws.total : 0; }
+
+int64_t mk_workspace_offset(const mk_sched* s, const char* name) {
+  if (!s || !name) return -1;
+  if (!std::strcmp(name, "moe_queue_len")) return (int64_t)s->ws.off("moe_queue_len");
+  const size_t o = s->ws.off(name);
+  return o == (size_t)-1 ? -1 : (int64_t)o;
+}
+
+int32_t mk_sched_num_sms(const mk_sched* s) { return s ? s->num_sms : 0; }
+
+int32_t mk_sched_num_tasks(const mk_sched* s, int32_t sm) {
+  if (!s || sm < 0 || sm >= s->num_sms) return -1;
+  return (int32_t)s->per_sm[sm].size();
+}
+
+int32_t mk_sched_num_barriers(const mk_sched* s) { return s ? (int32_t)s->bar_kind.size() : 0; }
+
+int mk_sched_get_task(const mk_sched* s, int32_t sm, int32_t idx, int32_t desc[32]) {
+  if (!s || sm < 0 || sm >= s->num_sms || idx < 0 || idx >= (int)s->per_sm[sm].size() || !desc)
+    return fail(MK_ERR_ARG, "task index out of range");
+  std::memcpy(desc, s->tasks[s->per_sm[sm][idx]].data(), sizeof(int32_t) * 32);
+  return MK_OK;
+}
+
+int mk_sched_set_task(mk_sched* s, int32_t sm, int32_t idx, const int32_t desc[32]) {
+  if (!s || sm < 0 || sm >= s->num_sms || idx < 0 || idx >= (int)s->per_sm[sm].size() || !desc)
+    return fail(MK_ERR_ARG, "task index out of range");
+  std::memcpy(s->tasks[s->per_sm[sm][idx]].data(), desc, sizeof(int32_t) * 32);
+  return MK_OK;
+}
+
+int mk_sched_validate(const mk_sched* s) {
+  if (!s) return fail(MK_ERR_ARG, "null schedule");
+  return validate(s);
+}
+
+int mk_sched_simulate(const mk_sched* s, int32_t batch, const int32_t* seq_lens,
+                      const int32_t* routing, uint64_t seed) {
+  if (!s || !seq_lens || batch < 1 || batch > s->max_batch) return fail(MK_ERR_ARG, "bad batch");
+  const int L = s->cfg.n_layers, K = s->dims.K, E = s->dims.E;
+  Sim sim;
+  sim.s = s;
+  sim.B = batch;
+  sim.seq.assign(seq_lens, seq_lens + batch);
+  for (int b = 0; b < batch; ++b)
+    if (seq_lens[b] < 1 || seq_lens[b] > s->max_ctx) return fail(MK_ERR_ARG, "seq_len out of range");
+  std::mt19937_64 rng(seed);
+  sim.routing.resize((size_t)L * batch * K);
+  for (int l = 0; l < L; ++l)
+    for (int b = 0; b < batch; ++b) {
+      int32_t* r = &sim.routing[((size_t)l * batch + b) * K];
+      if (routing) {
+        std::memcpy(r, routing + ((size_t)l * batch + b) * K, sizeof(int32_t) * K);
+      } else {
+        std::vector<int> ex(E);
+        for (int e = 0; e < E; ++e) ex[e] = e;
+        std::shuffle(ex.begin(), ex.end(), rng);
+        for (int j = 0; j < K; ++j) r[j] = ex[j];
+      }
+    }
+  sim.bars.assign(s->bar_kind.size(), 0);
+  sim.pos.assign(s->num_sms, 0);
+  sim.pending.assign(s->num_sms, -1);
+  build_attn_queue(s, batch, seq_lens, sim.attn_q);
+  sim.up_q.assign(L, {});
+  sim.dn_q.assign(L, {});
+  sim.fin_done.assign(L, 0);
+  std::vector<int> order(s->num_sms);
+  for (int i = 0; i < s->num_sms; ++i) order[i] = i;
+  for (;;) {
+    std::shuffle(order.begin(), order.end(), rng);
+    bool progress = false;
+    for (int sm : order) progress |= sim.step(sm);
+    if (!sim.err.empty()) return fail(MK_ERR_ARG, sim.err);
+    if (!progress) break;
+  }
+  for (int sm = 0; sm < s->num_sms; ++sm)
+    if (sim.pos[sm] < (int)s->per_sm[sm].size()) {
+      const Desc& d = s->tasks[s->per_sm[sm][sim.pos[sm]]];
+      return fail(MK_ERR_ARG, "deadlock: SM " + std::to_string(sm) + " stuck at task " +
+                                  std::to_string(d[F_TASK]) + " (op " + std::to_string(d[F_OP]) +
+                                  ", layer " + std::to_string(d[F_LAYER]) + ")");
+    }
+  // every static barrier ends at exactly the count its waiters expect
+  std::vector<int64_t> expect(s->bar_kind.size(), -1);
+  for (const Desc& d : s->tasks)
+    for (int slot = 0; slot < 2; ++slot) {
+      const int b = d[slot == 0 ? F_WAIT0 : F_WAIT1];
+      if (b >= 0 && s->bar_kind[b] == BK_STATIC) expect[b] = d[slot == 0 ? F_TGT0 : F_TGT1];
+    }
+  for (size_t b = 0; b < expect.size(); ++b)
+    if (expect[b] >= 0 && sim.bars[b] != expect[b])
+      return fail(MK_ERR_ARG, "barrier " + std::to_string(b) + " ended at " + std::to_string(sim.bars[b]) +
+                                  ", expected " + std::to_string(expect[b]));
+  // attention counters: each row's slices, each expert's up tiles
+  for (int l = 0; l < L; ++l) {
+    const LayerBars& lb = s->lb[l];
+    for (int b = 0; b < s->max_batch; ++b)
+      for (int g = 0; g < s->dims.NKV; ++g) {
+        const int64_t want = b >= batch ? (is_full_layer(s->cfg, l) ? 0 : s->n_static)
+                                        : (is_full_layer(s->cfg, l) ? attn_slices(s, seq_lens[b]) : s->n_static);
+        if (sim.bars[lb.cnt + b * s->dims.NKV + g] != want)
+          return fail(MK_ERR_ARG, "attention counter of layer " + std::to_string(l) + " row " +
+                                      std::to_string(b) + " ended at " +
+                                      std::to_string(sim.bars[lb.cnt + b * s->dims.NKV + g]));
+      }
+  }
+  return MK_OK;
+}
+
+}  // extern "C"

@@ -80,10 +80,11 @@ class Workload:
     seed: int
     zipf: float | None = None
     desc: str = ""
+    shape_override: ModelShape | None = None
 
     @property
     def shape(self) -> ModelShape:
-        return MODELS[self.model]
+        return self.shape_override if self.shape_override is not None else MODELS[self.model]
 
 
 WORKLOADS = {

@@ -1,0 +1,174 @@
+"""The C ABI library on the host: it loads, exports what include/mk.h declares,
+and its scheduler builds task lists that the validator and the simulator
+accept -- and rejects lists with a wrong arrive count or a cyclic wait."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+import moe_decode_megakernel_gb300 as mk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+NUM_SMS = 152
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not os.path.exists(mk.LIB_PATH):
+        from moe_decode_megakernel_gb300.build import build
+        build()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mk.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mk_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol():
+    names = declared_functions()
+    assert len(names) >= 19
+    L = mk.lib()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def fake_model(shape):
+    w = mk.MkWeights(*[0x10000 * (i + 1) for i in range(len(mk.MkWeights._fields_))])
+    return mk.Model(mk.config_from(shape), w)
+
+
+def test_load_model_rejects_unknown_shape():
+    from dataclasses import replace
+    with pytest.raises(mk.MkError) as e:
+        fake_model(replace(synth.MODELS["tiny"], hidden=512))
+    assert e.value.code == mk.MK_ERR_UNSUPPORTED
+    with pytest.raises(mk.MkError) as e:
+        mk.Model(mk.config_from(synth.MODELS["tiny"]), mk.MkWeights())
+    assert e.value.code == mk.MK_ERR_ARG
+
+
+def sched_for(workload, **opts):
+    w = synth.WORKLOADS[workload]
+    inp = synth.make_inputs(w)
+    m = fake_model(w.shape)
+    o = mk.default_sched_opts(num_sms=NUM_SMS, **opts)
+    s = mk.Sched(m, w.batch, int(inp.seq_lens.max()), o)
+    return m, s, inp
+
+
+@pytest.mark.parametrize("workload", ["tiny", "small", "full_bs1_8k", "batch32_ragged"])
+@pytest.mark.parametrize("order", [0, 1, 2])
+def test_schedules_validate_and_simulate(workload, order):
+    m, s, inp = sched_for(workload, wave_order=order)
+    s.validate()
+    s.simulate(inp.seq_lens, seed=order)
+    # a shorter batch than the schedule's maximum also completes
+    if inp.seq_lens.size > 1:
+        s.simulate(inp.seq_lens[:3], seed=7)
+
+
+@pytest.mark.parametrize("opts", [dict(fuse_finalize=0), dict(fuse_moe_combine=0),
+                                  dict(explicit_gather=1), dict(attn_split_pages=1, moe_claimers=5,
+                                                               attn_claimers=3)])
+def test_schedule_variants(opts):
+    m, s, inp = sched_for("small", **opts)
+    s.validate()
+    s.simulate(inp.seq_lens, seed=1)
+
+
+def test_long_context_bucket():
+    m, s, inp = sched_for("long_256k")
+    s.validate()
+    s.simulate(inp.seq_lens, seed=3)
+
+
+def test_full_list_shape():
+    """Every SM gets tasks; one list covers every layer; counts per opcode."""
+    m, s, inp = sched_for("full_bs1_8k")
+    counts = {}
+    for sm in range(s.num_sms):
+        n = s.num_tasks(sm)
+        assert n > 0
+        for i in range(n):
+            d = s.get_task(sm, i)
+            counts[mk.OPS[int(d[mk.F_OP])]] = counts.get(mk.OPS[int(d[mk.F_OP])], 0) + 1
+    sh = synth.MODELS["full"]
+    assert counts["RESID_NORM"] == sh.n_layers + 1
+    assert counts["QKV_PROJ"] == sh.n_layers * 80  # "a real QKV at batch 1 is 80 tiles"
+    assert counts["ROUTER_TOPK"] == sh.n_layers
+    assert counts["MOE_UPGATE_ACT_DRAIN"] == counts["MOE_DOWN_DRAIN"] == sh.n_layers * NUM_SMS
+    assert counts["ATTN_DRAIN"] > 0 and counts["ATTN_DECODE"] > 0 and counts["LM_HEAD"] > 0
+
+
+def find_task(s, op, layer=None):
+    for sm in range(s.num_sms):
+        for i in range(s.num_tasks(sm)):
+            d = s.get_task(sm, i)
+            if d[mk.F_OP] == op and (layer is None or d[mk.F_LAYER] == layer):
+                return sm, i, d
+    raise LookupError(op)
+
+
+def test_dropped_arrive_is_caught():
+    m, s, inp = sched_for("tiny")
+    sm, i, d = find_task(s, 3, layer=0)  # an O_PROJ task
+    d = d.copy()
+    d[mk.F_SIG0] = -1
+    s.set_task(sm, i, d)
+    with pytest.raises(mk.MkError, match="arrivals"):
+        s.validate()
+    with pytest.raises(mk.MkError, match="deadlock"):
+        s.simulate(inp.seq_lens)
+
+
+def test_doubled_arrive_is_caught():
+    m, s, inp = sched_for("tiny")
+    sm, i, d = find_task(s, 3, layer=0)
+    d = d.copy()
+    d[mk.F_SIG1] = d[mk.F_SIG0]  # arrives twice
+    s.set_task(sm, i, d)
+    with pytest.raises(mk.MkError, match="arrivals"):
+        s.validate()
+    with pytest.raises(mk.MkError, match="ended at"):
+        s.simulate(inp.seq_lens)
+
+
+def test_wrong_wait_count_is_caught():
+    m, s, inp = sched_for("small")
+    sm, i, d = find_task(s, 2, layer=3)  # a QKV task waits on the norm
+    d = d.copy()
+    d[mk.F_TGT0] += 1
+    s.set_task(sm, i, d)
+    with pytest.raises(mk.MkError):
+        s.validate()
+    with pytest.raises(mk.MkError, match="deadlock"):
+        s.simulate(inp.seq_lens)
+
+
+def test_cycle_is_caught():
+    m, s, inp = sched_for("tiny")
+    # layer 0's first RMSNorm waits for the LM head: no order can satisfy it
+    sm, i, d = find_task(s, 1, layer=0)
+    _, _, lm = find_task(s, 6)
+    n_lm = sum(int(s.get_task(k, i)[mk.F_OP] == 6) for k in range(s.num_sms) for i in range(s.num_tasks(k)))
+    d = d.copy()
+    d[mk.F_WAIT0], d[mk.F_TGT0] = lm[mk.F_SIG0], n_lm
+    s.set_task(sm, i, d)
+    with pytest.raises(mk.MkError, match="cyclic"):
+        s.validate()
+    with pytest.raises(mk.MkError, match="deadlock"):
+        s.simulate(inp.seq_lens)
+
+
+def test_rejects_bad_bucket():
+    m = fake_model(synth.MODELS["tiny"])
+    with pytest.raises(mk.MkError):
+        mk.Sched(m, 65, 64, mk.default_sched_opts(num_sms=NUM_SMS))
+    with pytest.raises(mk.MkError):
+        mk.Sched(m, 1, 0, mk.default_sched_opts(num_sms=NUM_SMS))
+    s = mk.Sched(m, 2, 64, mk.default_sched_opts(num_sms=NUM_SMS))
+    with pytest.raises(mk.MkError):
+        s.simulate([65])  # longer than the bucket
