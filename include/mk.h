@@ -78,8 +78,9 @@ int mk_load_model(const mk_config* cfg, const mk_weights* w, mk_model** out);
 void mk_free_model(mk_model* m);
 
 /* Wave orders of one layer ("Task scheduler: mapping tasks to SMs"):
- * DEFAULT     qkv, router, top-k, route setup, gather, attention (+combine),
- *             MoE up/down, O-proj, RMSNorm;
+ * DEFAULT     router, top-k, route setup, gather, qkv, attention (+combine),
+ *             MoE up/down, O-proj, RMSNorm (the pages' order with the
+ *             router ahead of QKV);
  * INTERLEAVED attention, MoE up/down, attention combine, MoE combine,
  *             O-proj, RMSNorm;
  * ATTN_FIRST  attention, attention combine, O-proj, MoE up/down, MoE
@@ -102,6 +103,7 @@ typedef struct {
   int32_t explicit_gather;  /* 1: MOE_GATHER materialises expert-ordered rows */
   int32_t trace_hidden;     /* 1: keep the residual entering every layer in the workspace */
   int32_t watchdog_ms;      /* device-side wait limit; 0 = 2000 ms */
+  int32_t trace;            /* 1: record every work item's timestamps ("trace", "stats") */
 } mk_sched_opts;
 
 /* Fills opts with the defaults (all zero except fuse_* = 1). */
@@ -152,10 +154,17 @@ const char* mk_last_error(void);
 
 /* Byte offsets of named regions inside the workspace (-1 if absent):
  * "topk_ids" int32 [L][B][k], "topk_w" fp32 [L][B][k], "router_logits"
- * fp32 [L][B][E], "expert_count" int32 [L][E], "moe_queue" int32 entries
- * (last layer), "moe_down_queue" int32, "moe_queue_len" int32 [2] (up, down),
+ * fp32 [L][B][E], "expert_count" int32 [L][E], "moe_queue" int32 [E] (last
+ * layer's active experts, ascending: entry i of the up/gate queue is expert
+ * list[i / up_tiles], tile i % up_tiles; likewise for the down queue),
+ * "moe_queue_len" int32 [2] (up, down),
  * "perm" int32 [B*k] (last layer), "hidden_trace" fp32 [L+1][B][H],
- * "error" uint32 [8], "barriers" uint32, and the activations "h", "x", "q",
+ * "error" uint32 [8], "barriers" uint32, with opts.trace "trace" uint64
+ * [num_sms][cap][4] (popped, waits done, end in ns of %globaltimer; op |
+ * layer << 8 | task << 16 | first argument << 40; unused records zero) and
+ * "stats" uint64 [num_sms][8] (consumer: ns waiting on counters, ns waiting on
+ * stages, ns busy, items; producer: ns waiting on free stages, on routing, on
+ * the work ring, claims), and the activations "h", "x", "q",
  * "kvnew", "attn_out", "opart", "u", "y", "moe_out" of the last layer. */
 int64_t mk_workspace_offset(const mk_sched* s, const char* name);
 

@@ -173,12 +173,12 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   p.seq_lens = seq_lens;
   p.max_ctx = s->max_ctx;
   p.h = reinterpret_cast<float*>(at("h"));
-  p.x = reinterpret_cast<uint16_t*>(at("x"));
+  p.x = reinterpret_cast<float*>(at("x"));
   p.q = reinterpret_cast<float*>(at("q"));
   p.kvnew = reinterpret_cast<uint16_t*>(at("kvnew"));
   p.part_o = reinterpret_cast<float*>(at("part_o"));
   p.part_ml = reinterpret_cast<float*>(at("part_ml"));
-  p.attn_out = reinterpret_cast<uint16_t*>(at("attn_out"));
+  p.attn_out = reinterpret_cast<float*>(at("attn_out"));
   p.opart = reinterpret_cast<float*>(at("opart"));
   p.rlog = reinterpret_cast<float*>(at("router_logits"));
   p.topk_ids = reinterpret_cast<int32_t*>(at("topk_ids"));
@@ -188,13 +188,15 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   p.perm = reinterpret_cast<int32_t*>(at("perm"));
   p.inv = reinterpret_cast<int32_t*>(at("inv"));
   p.upq = reinterpret_cast<int32_t*>(at("moe_queue"));
-  p.dnq = reinterpret_cast<int32_t*>(at("moe_down_queue"));
   p.qlen = reinterpret_cast<int32_t*>(at("moe_queue_len"));
-  p.xg = reinterpret_cast<uint16_t*>(at("xg"));
-  p.u = reinterpret_cast<uint16_t*>(at("u"));
+  p.xg = reinterpret_cast<float*>(at("xg"));
+  p.u = reinterpret_cast<float*>(at("u"));
   p.y = reinterpret_cast<float*>(at("y"));
   p.moe_out = reinterpret_cast<float*>(at("moe_out"));
   p.htrace = reinterpret_cast<float*>(at("hidden_trace"));
+  p.trace = reinterpret_cast<uint64_t*>(at("trace"));
+  p.trace_cap = s->trace_cap;
+  p.stats = reinterpret_cast<uint64_t*>(at("stats"));
   p.split_len = s->split_len;
   p.n_static = s->n_static;
   p.max_slots = s->max_slots;

@@ -60,6 +60,7 @@ struct mk_sched {
   int num_sms = 0, max_batch = 0, max_ctx = 0;
   int split_len = 0, n_static = 0, max_slots = 0, max_attn_entries = 0;
   int lm_bar = -1;
+  int trace_cap = 0;
   std::vector<mk::Desc> tasks;              // global order
   std::vector<std::vector<int>> per_sm;     // task indices in execution order
   std::vector<int8_t> bar_kind;

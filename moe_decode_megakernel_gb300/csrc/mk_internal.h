@@ -78,10 +78,13 @@ constexpr int kStages = 6;           // stage ring depth (192 KB)
 constexpr int kDescRing = 4;         // descriptor ring (controller -> producer)
 constexpr int kWorkRing = 8;         // work-item ring (producer -> consumers)
 constexpr int kConsumerWarps = 8;
-constexpr int kThreads = 32 * (2 + kConsumerWarps);  // controller, producer, consumers
-constexpr int kTB = 4;               // activation rows per GEMV pass
+constexpr int kThreads = 32 * (3 + kConsumerWarps);  // controller, producer, storer, consumers
+constexpr int kTB = 2;               // activation rows per GEMV pass
 constexpr int kMaxStageRows = 64;
 constexpr int kMaxBatch = 64;
+// per-SM counters: consumer ns waiting on counters, on stages, busy ns, items;
+// producer ns waiting on free stages, on routing, on the work ring, claims
+constexpr int kStats = 8;
 
 // Rows of a [rows][k] bf16 matrix that fit one stage, a multiple of 8, at most 64.
 constexpr int stage_rows(int k) {
@@ -151,12 +154,12 @@ struct Params {
   const int32_t* seq_lens;  // [B] device, length including the decoded token
   int max_ctx;
   float* h;             // [MB][H] residual stream
-  uint16_t* x;          // [MB][H] normalised layer input (bf16)
+  float* x;             // [MB][H] normalised layer input
   float* q;             // [MB][NQ][D] RoPE'd queries
   uint16_t* kvnew;      // [MB][2][NKV][D] the new token's K and V (bf16, as stored)
   float* part_o;        // [MB][NKV][max_slots][G][D] unnormalised slice outputs
   float* part_ml;       // [MB][NKV][max_slots][G][2] slice max (log2 domain) and sum
-  uint16_t* attn_out;   // [MB][NQ D]
+  float* attn_out;      // [MB][NQ D]
   float* opart;         // [NKV][MB][H] O-proj split-K partials
   float* rlog;          // [L][MB][E] router logits
   int32_t* topk_ids;    // [L][MB][K]
@@ -165,14 +168,17 @@ struct Params {
   int32_t* eoff;        // [E + 1] row offset of each expert (current layer)
   int32_t* perm;        // [MB K] expert-ordered row -> b * K + j
   int32_t* inv;         // [MB K] b * K + j -> expert-ordered row
-  int32_t* upq;         // up tile queue: (e << 16) | tile
-  int32_t* dnq;         // down tile queue
+  int32_t* upq;         // [E] active experts, ascending: the MoE queues' expert list
   int32_t* qlen;        // [2] queue lengths (up, down)
-  uint16_t* xg;         // [MB K][H] gathered rows (explicit gather)
-  uint16_t* u;          // [MB K][I] SwiGLU activations (bf16)
+  float* xg;            // [MB K][H] gathered rows (explicit gather)
+  float* u;             // [MB K][I] SwiGLU activations
   float* y;             // [MB K][H] expert outputs
   float* moe_out;       // [MB][H]
   float* htrace;        // [L + 1][MB][H] or null
+
+  uint64_t* trace;      // [num_sms][trace_cap][2] per work item, or null
+  int trace_cap;
+  uint64_t* stats;      // [num_sms][kStats] stall counters, or null
 
   int split_len;        // tokens per KV slice
   int n_static;         // static slices per (row, group) of a sliding layer

@@ -55,6 +55,9 @@ __device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive_n(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(n) : "memory");
+}
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)),
                "r"(bytes)
@@ -78,6 +81,20 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(b))
       : "memory");
+}
+// The same copy with an L2 cache policy (evict_first for data read once per step).
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* b,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(b)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -130,6 +147,18 @@ __device__ __forceinline__ float dot8(uint4 w, uint4 x, float acc) {
   acc = fmaf(bf16_hi(w.w), bf16_hi(x.w), acc);
   return acc;
 }
+// 8 BF16 weights against 8 fp32 activations
+__device__ __forceinline__ float dot8f(uint4 w, float4 a, float4 b, float acc) {
+  acc = fmaf(bf16_lo(w.x), a.x, acc);
+  acc = fmaf(bf16_hi(w.x), a.y, acc);
+  acc = fmaf(bf16_lo(w.y), a.z, acc);
+  acc = fmaf(bf16_hi(w.y), a.w, acc);
+  acc = fmaf(bf16_lo(w.z), b.x, acc);
+  acc = fmaf(bf16_hi(w.z), b.y, acc);
+  acc = fmaf(bf16_lo(w.w), b.z, acc);
+  acc = fmaf(bf16_hi(w.w), b.w, acc);
+  return acc;
+}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(FULL, v, m);
@@ -142,20 +171,28 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 // Sums N per-lane values over the warp and leaves lane l holding the total of
 // value l / (32 / N) ("transpose reduction": N-1 + log2(32/N) shuffles instead
-// of 5N).
-template <int N>
-__device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
-  static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "power of two");
+// of 5N).  Each halving step keeps the half of the values selected by one lane
+// bit and adds the partner lane's copy of it.
+__device__ __forceinline__ void rs_halve(float* v, int n, int m, int lane) {
+  const bool up = (lane & m) != 0;
 #pragma unroll
-  for (int n = N, m = 16; n > 1; n >>= 1, m >>= 1) {
-    const bool up = (lane & m) != 0;
-#pragma unroll
-    for (int i = 0; i < n / 2; ++i) {
+  for (int i = 0; i < 16; ++i) {
+    if (i < n / 2) {
       const float send = up ? v[i] : v[i + n / 2];
       const float keep = up ? v[i + n / 2] : v[i];
       v[i] = keep + __shfl_xor_sync(FULL, send, m);
     }
   }
+}
+
+template <int N>
+__device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
+  static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "power of two");
+  if constexpr (N >= 32) rs_halve(v, 32, 16, lane);
+  if constexpr (N >= 16) rs_halve(v, 16, N >= 32 ? 8 : 16, lane);
+  if constexpr (N >= 8) rs_halve(v, 8, 16 * 8 / N, lane);
+  if constexpr (N >= 4) rs_halve(v, 4, 16 * 4 / N, lane);
+  if constexpr (N >= 2) rs_halve(v, 2, 16 * 2 / N, lane);
   float r = v[0];
 #pragma unroll
   for (int m = 16 / N; m >= 1; m >>= 1) r += __shfl_xor_sync(FULL, r, m);
@@ -167,6 +204,7 @@ struct Hdr {
   uint64_t full[kStages], empty[kStages];
   uint64_t dfull[kDescRing], dempty[kDescRing];
   uint64_t wfull[kWorkRing], wempty[kWorkRing];
+  uint64_t done[kWorkRing];  // consumers finished the item in this slot
   int32_t desc[kDescRing][32];
   int32_t work[kWorkRing][32];
   volatile int32_t abort;
@@ -175,13 +213,17 @@ struct Hdr {
 
 template <class S>
 struct Scratch {
-  uint16_t xs[kTB * S::H];                  // activation rows of one GEMV pass
+  float xs[kTB * S::H];                     // activation rows of one GEMV pass (tagged)
   float out[2][kTB * kMaxStageRows];        // dot products of one stage (double buffer)
-  float sc[S::G * S::P];                    // attention scores of one page
-  float pr[S::G * S::P];                    // attention probabilities of one page
+  float qs[S::G * S::D];                    // the KV group's queries (tagged), pre-scaled
+  float sc[S::P * S::G];                    // attention scores of one page [token][head]
+  float pr[S::P * S::G];                    // attention probabilities of one page [token][head]
   float am[S::G], al[S::G], aa[S::G];       // running max, sum, rescale per head
   float red[kConsumerWarps * 2];
+  double rope_theta[S::D / 2];              // base^(-2i/D)
+  int32_t xtag[4], qtag[4];                 // what xs / qs hold
   unsigned long long mask[S::E];            // rows routed to each expert (bit b)
+  int32_t ids[kMaxBatch * S::K];            // this layer's routing (top-k / finalize)
   int32_t cnt[S::E], off[S::E + 1], act[S::E + 1];
 };
 
@@ -212,19 +254,26 @@ struct Ctx {
   int sm;
   uint32_t st;  // stages issued (producer) / consumed (consumers)
   uint32_t wk;  // work items pushed / popped
+  uint64_t stat[4];
 };
 
 // ----------------------------------------------------------- errors/waits
-static __device__ __noinline__ void record_error(const Params& p, uint32_t code, int sm, const int32_t* d, int bar,
-                             uint32_t seen, uint32_t tgt) {
+struct ErrWhere {  // what to report with an error: the task, its opcode and layer
+  int32_t task, op, layer;
+};
+__device__ __forceinline__ ErrWhere where_of(const int32_t* d) { return {d[F_TASK], d[F_OP], d[F_LAYER]}; }
+constexpr ErrWhere kNowhere{-1, -1, -1};
+
+static __device__ __noinline__ void record_error(const Params& p, uint32_t code, int sm, ErrWhere at, int bar,
+                                                 uint32_t seen, uint32_t tgt) {
   if (atomicCAS(p.err, 0u, code) == 0u) {
     p.err[1] = (uint32_t)sm;
-    p.err[2] = d ? (uint32_t)d[F_TASK] : 0xffffffffu;
+    p.err[2] = (uint32_t)at.task;
     p.err[3] = (uint32_t)bar;
     p.err[4] = seen;
     p.err[5] = tgt;
-    p.err[6] = d ? (uint32_t)d[F_OP] : 0xffffffffu;
-    p.err[7] = d ? (uint32_t)d[F_LAYER] : 0xffffffffu;
+    p.err[6] = (uint32_t)at.op;
+    p.err[7] = (uint32_t)at.layer;
     __threadfence();
   }
 }
@@ -232,14 +281,14 @@ static __device__ __noinline__ void record_error(const Params& p, uint32_t code,
 static __device__ __forceinline__ bool aborted(const Ctx& c) { return c.hdr->abort != 0; }
 
 // Waits for an mbarrier phase; false if the CTA is aborting or the watchdog fired.
-static __device__ bool mbar_wait(const Params& p, Ctx& c, uint64_t* b, uint32_t parity) {
+static __device__ __forceinline__ bool mbar_wait(const Params& p, Ctx& c, uint64_t* b, uint32_t parity) {
   if (mbar_try_wait(b, parity)) return true;
   const int64_t t0 = gtimer();
   for (;;) {
     if (mbar_try_wait(b, parity)) return true;
     if (aborted(c)) return false;
     if (gtimer() - t0 > p.watchdog_ns) {
-      record_error(p, ERR_TIMEOUT, c.sm, nullptr, -1, 0, 0);
+      record_error(p, ERR_TIMEOUT, c.sm, kNowhere, -1, 0, 0);
       c.hdr->abort = 1;
       return false;
     }
@@ -248,7 +297,7 @@ static __device__ bool mbar_wait(const Params& p, Ctx& c, uint64_t* b, uint32_t 
 
 // Waits until counter `bar` reaches `tgt` (one thread).  "Barriers": spin with
 // a short sleep; here with acquire loads and a time limit.
-static __device__ bool wait_counter(const Params& p, Ctx& c, int bar, uint32_t tgt, const int32_t* d) {
+static __device__ __forceinline__ bool wait_counter(const Params& p, Ctx& c, int bar, uint32_t tgt, ErrWhere at) {
   if (bar < 0 || tgt == 0) return true;
   const uint32_t* a = p.bars + bar;
   if (ld_acquire(a) >= tgt) return true;
@@ -263,7 +312,7 @@ static __device__ bool wait_counter(const Params& p, Ctx& c, int bar, uint32_t t
         return false;
       }
       if (gtimer() - t0 > p.watchdog_ns) {
-        record_error(p, ERR_TIMEOUT, c.sm, d, bar, ld_volatile(a), tgt);
+        record_error(p, ERR_TIMEOUT, c.sm, at, bar, ld_volatile(a), tgt);
         c.hdr->abort = 1;
         return false;
       }
@@ -304,20 +353,31 @@ static __device__ void controller(const Params& p, Ctx& c) {
 template <class S>
 struct Producer {
   const Params& p;
-  Ctx& c;
+  Ctx c;
+  // weights and KV pages are read once per step: streaming them with
+  // evict_first keeps L2 for activations, counters and the kernel's code
+  uint64_t stream_policy;
 
-  __device__ bool acquire_stage(int& slot) {
+  __device__ __forceinline__ bool acquire_stage(int& slot) {
     slot = c.st % kStages;
-    if (c.st >= (uint32_t)kStages)
-      return mbar_wait(p, c, &c.hdr->empty[slot], ((c.st / kStages) - 1) & 1);
+    if (c.st >= (uint32_t)kStages) {
+      const int64_t t0 = p.stats ? gtimer() : 0;
+      const bool ok = mbar_wait(p, c, &c.hdr->empty[slot], ((c.st / kStages) - 1) & 1);
+      if (p.stats) c.stat[0] += gtimer() - t0;
+      return ok;
+    }
     return true;
   }
-  __device__ uint8_t* stage(int slot) { return c.stages + (size_t)slot * kStageBytes; }
+  __device__ __forceinline__ uint8_t* stage(int slot) { return c.stages + (size_t)slot * kStageBytes; }
 
-  __device__ bool push(const int32_t* item) {
+  __device__ __forceinline__ bool push(const int32_t* item) {
     const int slot = c.wk % kWorkRing;
-    if (c.wk >= (uint32_t)kWorkRing && !mbar_wait(p, c, &c.hdr->wempty[slot], ((c.wk / kWorkRing) - 1) & 1))
-      return false;
+    if (c.wk >= (uint32_t)kWorkRing) {
+      const int64_t t0 = p.stats ? gtimer() : 0;
+      const bool ok = mbar_wait(p, c, &c.hdr->wempty[slot], ((c.wk / kWorkRing) - 1) & 1);
+      if (p.stats) c.stat[2] += gtimer() - t0;
+      if (!ok) return false;
+    }
     int32_t* dst = c.hdr->work[slot];
     for (int i = 0; i < 32; ++i) dst[i] = item[i];
     mbar_arrive(&c.hdr->wfull[slot]);
@@ -327,7 +387,7 @@ struct Producer {
 
   // rows [row0, row0+nrows) of a [rows][K] matrix (row stride `ld` elements),
   // SR rows per stage
-  __device__ bool load_rows(const uint16_t* base, int64_t ld, int K, int row0, int nrows, int SR) {
+  __device__ __forceinline__ bool load_rows(const uint16_t* base, int64_t ld, int K, int row0, int nrows, int SR) {
     for (int s0 = 0; s0 < nrows; s0 += SR) {
       const int rs = min(SR, nrows - s0);
       int slot;
@@ -337,18 +397,19 @@ struct Producer {
       const uint32_t bytes = (uint32_t)rs * K * 2;
       mbar_expect_tx(fb, bytes);
       if (ld == K) {
-        bulk_g2s(dst, base + (int64_t)(row0 + s0) * K, bytes, fb);
+        bulk_g2s_hint(dst, base + (int64_t)(row0 + s0) * K, bytes, fb, stream_policy);
       } else {
-        for (int r = 0; r < rs; ++r) bulk_g2s(dst + (size_t)r * K * 2, base + (int64_t)(row0 + s0 + r) * ld, K * 2, fb);
+        for (int r = 0; r < rs; ++r)
+          bulk_g2s_hint(dst + (size_t)r * K * 2, base + (int64_t)(row0 + s0 + r) * ld, K * 2, fb, stream_policy);
       }
       ++c.st;
     }
     return true;
   }
 
-  __device__ int dense_stages(int rows, int SR) { return (rows + SR - 1) / SR; }
+  __device__ __forceinline__ int dense_stages(int rows, int SR) { return (rows + SR - 1) / SR; }
 
-  __device__ bool dense(const int32_t* d) {
+  __device__ __forceinline__ bool dense(const int32_t* d) {
     int32_t it[32];
     for (int i = 0; i < 32; ++i) it[i] = d[i];
     const int op = d[F_OP], l = d[F_LAYER], row0 = d[F_A0], rows = d[F_A0 + 1];
@@ -368,7 +429,7 @@ struct Producer {
     return load_rows(base, ld, K, row0, rows, SR);
   }
 
-  __device__ bool attn_pages(int l, int b, int g, int pf, int np) {
+  __device__ __forceinline__ bool attn_pages(int l, int b, int g, int pf, int np) {
     const int64_t page_elems = (int64_t)S::P * S::D;
     for (int k = 0; k < np; ++k) {
       int slot;
@@ -379,13 +440,13 @@ struct Producer {
       const int lp = pf + k;
       if (lp < p.max_pages) page = __ldg(p.block_tables + (int64_t)b * p.max_pages + lp);
       if (page < 0 || page >= p.num_pages) {
-        record_error(p, ERR_PAGE, c.sm, nullptr, lp, (uint32_t)page, (uint32_t)p.num_pages);
+        record_error(p, ERR_PAGE, c.sm, kNowhere, lp, (uint32_t)page, (uint32_t)p.num_pages);
         mbar_arrive(&c.hdr->full[slot]);  // complete the stage without data
       } else {
         const int64_t off = (((int64_t)l * p.num_pages + page) * S::NKV + g) * page_elems;
         mbar_expect_tx(fb, (uint32_t)(2 * page_elems * 2));
-        bulk_g2s(dst, p.kpool + off, (uint32_t)(page_elems * 2), fb);
-        bulk_g2s(dst + page_elems * 2, p.vpool + off, (uint32_t)(page_elems * 2), fb);
+        bulk_g2s_hint(dst, p.kpool + off, (uint32_t)(page_elems * 2), fb, stream_policy);
+        bulk_g2s_hint(dst + page_elems * 2, p.vpool + off, (uint32_t)(page_elems * 2), fb, stream_policy);
       }
       ++c.st;
     }
@@ -393,7 +454,7 @@ struct Producer {
   }
 
   // one KV slice [t0, t1) of (b, g) as a work item plus its pages
-  __device__ bool attn_item(const int32_t* d, int l, int b, int g, int t0, int t1, int slot_idx, int wait_bar,
+  __device__ __forceinline__ bool attn_item(const int32_t* d, int l, int b, int g, int t0, int t1, int slot_idx, int wait_bar,
                             int wait_tgt, int sig) {
     int32_t it[32];
     for (int i = 0; i < 32; ++i) it[i] = d[i];
@@ -417,7 +478,7 @@ struct Producer {
     return attn_pages(l, b, g, pf, np);
   }
 
-  __device__ bool attn_decode(const int32_t* d) {
+  __device__ __forceinline__ bool attn_decode(const int32_t* d) {
     const int l = d[F_LAYER], b = d[F_A0], g = d[F_A0 + 1], j = d[F_A0 + 2];
     int t0 = 0, t1 = 0;
     if (b < p.B) {
@@ -436,12 +497,14 @@ struct Producer {
   // claims the next entry until the queue is empty).  The queue holds one
   // entry per (row b, KV group g, slice j), ordered (b, g, j); entry i is
   // located from the rows' slice counts, so the queue needs no storage.
-  __device__ bool attn_drain(const int32_t* d) {
+  __device__ __forceinline__ bool attn_drain(const int32_t* d) {
     const int l = d[F_LAYER];
     uint32_t* claim = p.bars + d[F_A0];
+    uint32_t next = atomicAdd(claim, 1u);
+    ++c.stat[3];
     for (;;) {
       if (aborted(c)) return false;
-      const uint32_t i = atomicAdd(claim, 1u);
+      const uint32_t i = next;
       uint32_t acc = 0;
       int b = 0, n = 0, s = 0;
       for (; b < p.B; ++b) {
@@ -451,10 +514,12 @@ struct Producer {
         acc += (uint32_t)n;
       }
       if (b >= p.B) break;  // queue exhausted
+      next = atomicAdd(claim, 1u);
+      ++c.stat[3];
       const int r = (int)(i - acc), per = n / S::NKV;
       const int g = r / per, j = r - g * per;
       if (j >= p.max_slots) {
-        record_error(p, ERR_INDEX, c.sm, d, d[F_A0], (uint32_t)s, (uint32_t)p.max_ctx);
+        record_error(p, ERR_INDEX, c.sm, where_of(d), d[F_A0], (uint32_t)s, (uint32_t)p.max_ctx);
         c.hdr->abort = 1;
         return false;
       }
@@ -465,7 +530,7 @@ struct Producer {
     return claim_end(d);
   }
 
-  __device__ bool claim_end(const int32_t* d) {
+  __device__ __forceinline__ bool claim_end(const int32_t* d) {
     int32_t it[32];
     for (int i = 0; i < 32; ++i) it[i] = d[i];
     it[F_OP] = W_CLAIM_END;
@@ -474,25 +539,38 @@ struct Producer {
     return push(it);
   }
 
-  __device__ bool moe_drain(const int32_t* d, bool up) {
+  __device__ __forceinline__ bool moe_drain(const int32_t* d, bool up) {
     const int l = d[F_LAYER];
     // the routing decides which expert rows to stream: wait for the queue
-    if (!wait_counter(p, c, d[F_WAIT0], (uint32_t)d[F_TGT0], d)) return false;
-    const int qlen = min(__ldcg(p.qlen + (up ? 0 : 1)), S::E * (up ? S::mp.up_tiles : S::mp.dn_tiles));
-    const int32_t* q = up ? p.upq : p.dnq;
+    {
+      const int64_t t0 = p.stats ? gtimer() : 0;
+      const bool ok = wait_counter(p, c, d[F_WAIT0], (uint32_t)d[F_TGT0], where_of(d));
+      if (p.stats) c.stat[1] += gtimer() - t0;
+      if (!ok) return false;
+    }
+    constexpr int kUpTiles = S::mp.up_tiles, kDnTiles = S::mp.dn_tiles;
+    const int tiles = up ? kUpTiles : kDnTiles;
+    const int qlen = min(__ldcg(p.qlen + (up ? 0 : 1)), S::E * tiles);
     uint32_t* claim = p.bars + d[F_A0];
     constexpr MoePlan mp = S::mp;
+    // the next claim is issued before the current tile streams, so the atomic's
+    // round trip overlaps the copies
+    uint32_t next = atomicAdd(claim, 1u);
+    ++c.stat[3];
     for (;;) {
       if (aborted(c)) return false;
-      const uint32_t i = atomicAdd(claim, 1u);
+      const uint32_t i = next;
       if (i >= (uint32_t)qlen) break;
-      const int32_t ent = __ldcg(q + i);
-      const int e = ent >> 16, t = ent & 0xffff;
-      const bool e_ok = e >= 0 && e < S::E && t < (up ? mp.up_tiles : mp.dn_tiles);
+      next = atomicAdd(claim, 1u);
+      ++c.stat[3];
+      const int ai = (int)i / tiles, t = (int)i - ai * tiles;
+      const int e = __ldcg(p.upq + ai);
+      const int32_t ent = (e << 16) | t;
+      const bool e_ok = e >= 0 && e < S::E;
       const int row0 = e_ok ? __ldcg(p.eoff + e) : -1;
       const int nrows = e_ok ? __ldcg(p.ecount + l * S::E + e) : 0;
       if (!e_ok || row0 < 0 || nrows < 1 || row0 + nrows > p.B * S::K) {
-        record_error(p, ERR_INDEX, c.sm, d, d[F_A0], (uint32_t)ent, (uint32_t)qlen);
+        record_error(p, ERR_INDEX, c.sm, where_of(d), d[F_A0], (uint32_t)ent, (uint32_t)qlen);
         c.hdr->abort = 1;
         return false;
       }
@@ -528,8 +606,8 @@ struct Producer {
           const int r0 = t * mp.up_tile + s * mp.up_half;
           const uint32_t half = (uint32_t)mp.up_half * S::H * 2;
           mbar_expect_tx(fb, 2 * half);
-          bulk_g2s(dst, p.wg + (le * S::I + r0) * S::H, half, fb);
-          bulk_g2s(dst + half, p.wu + (le * S::I + r0) * S::H, half, fb);
+          bulk_g2s_hint(dst, p.wg + (le * S::I + r0) * S::H, half, fb, stream_policy);
+          bulk_g2s_hint(dst + half, p.wu + (le * S::I + r0) * S::H, half, fb, stream_policy);
           ++c.st;
         }
       } else {
@@ -539,15 +617,16 @@ struct Producer {
     return claim_end(d);
   }
 
-  __device__ bool passthrough(const int32_t* d) {
+  __device__ __forceinline__ bool passthrough(const int32_t* d) {
     int32_t it[32];
     for (int i = 0; i < 32; ++i) it[i] = d[i];
     it[F_NSTAGE] = 0;
     return push(it);
   }
 
-  __device__ void run() {
+  __device__ __forceinline__ void run() {
     if ((threadIdx.x & 31) != 0) return;
+    stream_policy = l2_evict_first_policy();
     const int n = p.sched[2 * c.sm + 1];
     Hdr* H = c.hdr;
     bool ok = true;
@@ -578,6 +657,8 @@ struct Producer {
       ex[F_OP] = W_EXIT;
       ex[F_WAIT0] = ex[F_WAIT1] = ex[F_SIG0] = ex[F_SIG1] = -1;
       push(ex);
+      if (p.stats)
+        for (int k = 0; k < 4; ++k) p.stats[(int64_t)c.sm * kStats + 4 + k] = c.stat[k];
       return;
     }
     // aborting: wait (bounded) for the copies already issued into the stage ring
@@ -596,33 +677,38 @@ struct Producer {
 template <class S>
 struct Consumer {
   const Params& p;
-  Ctx& c;
+  Ctx c;
   Scratch<S>& sm;
   int ct, cw, lane;
 
   // --- the stage ring
-  __device__ bool stage_wait(int& slot) {
+  __device__ __forceinline__ bool stage_wait(int& slot) {
     slot = c.st % kStages;
-    return mbar_wait(p, c, &c.hdr->full[slot], (c.st / kStages) & 1);
+    const int64_t t0 = (p.stats && ct == 0) ? gtimer() : 0;
+    const bool ok = mbar_wait(p, c, &c.hdr->full[slot], (c.st / kStages) & 1);
+    if (p.stats && ct == 0) c.stat[1] += gtimer() - t0;
+    return ok;
   }
-  __device__ void stage_release(int slot) {
+  __device__ __forceinline__ void stage_release(int slot) {
     __syncwarp();
     if (lane == 0) mbar_arrive(&c.hdr->empty[slot]);
     ++c.st;
   }
-  __device__ const uint8_t* stage(int slot) const { return c.stages + (size_t)slot * kStageBytes; }
+  __device__ __forceinline__ const uint8_t* stage(int slot) const { return c.stages + (size_t)slot * kStageBytes; }
 
   // ---------------------------------------------------------- GEMV core
   // out[t][r] = W[r][:] . xs[t][:] for the rows of one stage (warp per row).
+  // xs row t holds the activation as [half][chunk][4]: lane c reads the two
+  // halves of its 8-element chunk with two conflict-free 16-byte loads.
   template <int K>
-  __device__ void gemv_rows(const uint16_t* W, int rows, int tb, float* out) {
+  __device__ __forceinline__ void gemv_rows(const uint16_t* W, int rows, int tb, float* out) {
     constexpr int C = K / 8;
     constexpr int CPL = (C + 31) / 32;
-    const uint4* xs4 = reinterpret_cast<const uint4*>(sm.xs);
+    const float4* xs4 = reinterpret_cast<const float4*>(sm.xs);
     for (int r = cw; r < rows; r += kConsumerWarps) {
-      float acc[kTB];
+      float acc0[kTB], acc1[kTB];
 #pragma unroll
-      for (int t = 0; t < kTB; ++t) acc[t] = 0.f;
+      for (int t = 0; t < kTB; ++t) acc0[t] = acc1[t] = 0.f;
       const uint4* wr = reinterpret_cast<const uint4*>(W + (size_t)r * K);
 #pragma unroll
       for (int j = 0; j < CPL; ++j) {
@@ -631,59 +717,87 @@ struct Consumer {
           const uint4 w = wr[cc];
 #pragma unroll
           for (int t = 0; t < kTB; ++t)
-            if (t < tb) acc[t] = dot8(w, xs4[t * C + cc], acc[t]);
+            if (t < tb) {
+              const float4 a = xs4[t * 2 * C + cc], b = xs4[t * 2 * C + C + cc];
+              acc0[t] = fmaf(bf16_lo(w.x), a.x, acc0[t]);
+              acc1[t] = fmaf(bf16_hi(w.x), a.y, acc1[t]);
+              acc0[t] = fmaf(bf16_lo(w.y), a.z, acc0[t]);
+              acc1[t] = fmaf(bf16_hi(w.y), a.w, acc1[t]);
+              acc0[t] = fmaf(bf16_lo(w.z), b.x, acc0[t]);
+              acc1[t] = fmaf(bf16_hi(w.z), b.y, acc1[t]);
+              acc0[t] = fmaf(bf16_lo(w.w), b.z, acc0[t]);
+              acc1[t] = fmaf(bf16_hi(w.w), b.w, acc1[t]);
+            }
         }
       }
 #pragma unroll
       for (int t = 0; t < kTB; ++t)
-        if (t < tb) acc[t] = warp_sum(acc[t]);
+        if (t < tb) acc0[t] = warp_sum(acc0[t] + acc1[t]);
       if (lane == 0)
 #pragma unroll
         for (int t = 0; t < kTB; ++t)
-          if (t < tb) out[t * kMaxStageRows + r] = acc[t];
+          if (t < tb) out[t * kMaxStageRows + r] = acc0[t];
     }
   }
 
-  // activation rows [4*chunk, 4*chunk + tb) of the item into sm.xs
+  // activation rows [kTB*chunk, kTB*chunk + tb) of the item into sm.xs (fp32)
   template <int K>
-  __device__ void load_x(int op, const int32_t* w, int chunk, int tb) {
-    constexpr int C = K / 8;
-    uint4* xs4 = reinterpret_cast<uint4*>(sm.xs);
+  __device__ __forceinline__ void load_x(int op, const int32_t* w, int chunk, int tb) {
+    constexpr int C = K / 4;  // float4 per row
+    float4* xs4 = reinterpret_cast<float4*>(sm.xs);
     for (int i = ct; i < tb * C; i += kConsumerThreads) {
       const int t = i / C, cc = i - t * C;
       const int tok = kTB * chunk + t;
-      const uint4* src;
+      const float* src;
       switch (op) {
         case OP_O_PROJ:
-          src = reinterpret_cast<const uint4*>(p.attn_out + (int64_t)tok * S::NQ * S::D +
-                                               (int64_t)w[F_A0 + 2] * S::G * S::D);
+          src = p.attn_out + (int64_t)tok * S::NQ * S::D + (int64_t)w[F_A0 + 2] * S::G * S::D;
           break;
         case W_UP_TILE: {
           const int row = w[F_A0 + 2] + tok;
           if (p.explicit_gather) {
-            src = reinterpret_cast<const uint4*>(p.xg + (int64_t)row * S::H);
+            src = p.xg + (int64_t)row * S::H;
           } else {
             int pr = __ldcg(p.perm + row);
             int b = pr / S::K;
             if (pr < 0 || b >= p.B) b = 0;  // only after a failed step
-            src = reinterpret_cast<const uint4*>(p.x + (int64_t)b * S::H);
+            src = p.x + (int64_t)b * S::H;
           }
           break;
         }
         case W_DOWN_TILE:
-          src = reinterpret_cast<const uint4*>(p.u + (int64_t)(w[F_A0 + 2] + tok) * S::I);
+          src = p.u + (int64_t)(w[F_A0 + 2] + tok) * S::I;
           break;
         default:
-          src = reinterpret_cast<const uint4*>(p.x + (int64_t)tok * S::H);
+          src = p.x + (int64_t)tok * S::H;
           break;
       }
-      xs4[i] = __ldcg(src + cc);
+      // source float4 cc = elements [4cc, 4cc+4): chunk cc/2, half cc%2
+      xs4[t * C + (cc & 1) * (C / 2) + (cc >> 1)] = __ldcg(reinterpret_cast<const float4*>(src) + cc);
+    }
+  }
+
+  // The activation rows an item reads, as a tag: xs is reloaded only when
+  // the tag changes (consecutive items of one layer share their input).
+  __device__ __forceinline__ void x_tag(int op, const int32_t* w, int chunk, int32_t (&tag)[4]) {
+    const int l = w[F_LAYER];
+    switch (op) {
+      case OP_O_PROJ: tag[0] = 2; tag[1] = w[F_A0 + 2]; tag[2] = kTB * chunk; tag[3] = l; break;
+      case W_UP_TILE:
+        if (p.B == 1) {  // one row: the layer input itself, as for QKV and the router
+          tag[0] = 1; tag[1] = 0; tag[2] = 0; tag[3] = l;
+        } else {
+          tag[0] = 3; tag[1] = w[F_A0 + 2] + kTB * chunk; tag[2] = w[F_A0 + 3]; tag[3] = l;
+        }
+        break;
+      case W_DOWN_TILE: tag[0] = 4; tag[1] = w[F_A0 + 2] + kTB * chunk; tag[2] = w[F_A0 + 3]; tag[3] = l; break;
+      default: tag[0] = 1; tag[1] = kTB * chunk; tag[2] = l == p.L ? 1 : 0; tag[3] = l; break;
     }
   }
 
   // epilogue of one stage: rows [r_first, r_first + rows) of the item's output,
   // activation rows [4*chunk, 4*chunk + tb)
-  __device__ void epilogue(int op, const int32_t* w, int s, int rows, int chunk, int tb, const float* out) {
+  __device__ __forceinline__ void epilogue(int op, const int32_t* w, int s, int rows, int chunk, int tb, const float* out) {
     const int l = w[F_LAYER];
     switch (op) {
       case OP_QKV_PROJ: {
@@ -698,13 +812,14 @@ struct Consumer {
           const int head = row / S::D, dd = row - head * S::D;
           const int pos = __ldg(p.seq_lens + b) - 1;
           if (head < S::NQ + S::NKV) {  // rotate q and k: pair (dd, dd+1) by pos * base^(-dd/D)
-            const double theta = pow((double)p.rope_base, -(double)dd / (double)S::D);
-            double sn, cs;
-            sincos((double)pos * theta, &sn, &cs);
-            const float c0 = (float)cs, s0 = (float)sn;
-            const float a = v0 * c0 - v1 * s0, bb = v0 * s0 + v1 * c0;
-            v0 = a;
-            v1 = bb;
+            // the angle is reduced modulo 2 pi in double, then sin/cos in float
+            const double ang = (double)pos * sm.rope_theta[dd / 2];
+            const double red = ang - 6.283185307179586 * rint(ang * 0.15915494309189535);
+            float s0, c0;
+            sincosf((float)red, &s0, &c0);
+            const float r0 = v0 * c0 - v1 * s0, r1 = v0 * s0 + v1 * c0;
+            v0 = r0;
+            v1 = r1;
           }
           if (head < S::NQ) {
             float* qd = p.q + ((int64_t)b * S::NQ + head) * S::D + dd;
@@ -718,7 +833,7 @@ struct Consumer {
             const int lp = pos / S::P;
             int page = lp < p.max_pages ? __ldg(p.block_tables + (int64_t)b * p.max_pages + lp) : -1;
             if (page < 0 || page >= p.num_pages) {
-              record_error(p, ERR_PAGE, c.sm, w, lp, (uint32_t)page, (uint32_t)p.num_pages);
+              record_error(p, ERR_PAGE, c.sm, where_of(w), lp, (uint32_t)page, (uint32_t)p.num_pages);
             } else {
               uint16_t* pool = is_v ? p.vpool : p.kpool;
               const int64_t o = ((((int64_t)l * p.num_pages + page) * S::NKV + g) * S::P + pos % S::P) * S::D + dd;
@@ -758,16 +873,20 @@ struct Consumer {
           const float act = gte / (1.f + expf(-gte)) * upv;
           const int row = w[F_A0 + 2] + kTB * chunk + t;
           const int col = w[F_A0 + 1] * S::mp.up_tile + s * hu + r;
-          p.u[(int64_t)row * S::I + col] = f_bf16(act);
+          p.u[(int64_t)row * S::I + col] = act;
         }
         break;
       }
       case W_DOWN_TILE:
+        // the output goes to the (row b, slot j) it belongs to, times its router weight
         for (int i = ct; i < tb * rows; i += kConsumerThreads) {
           const int t = i / rows, r = i - t * rows;
           const int row = w[F_A0 + 2] + kTB * chunk + t;
+          int slot = __ldcg(p.perm + row);
+          if (slot < 0 || slot >= p.B * S::K) slot = 0;  // only after a failed step
+          const float wt = __ldcg(p.topk_w + (int64_t)l * p.MB * S::K + slot);
           const int n = w[F_A0 + 1] * S::mp.dn_tile + s * S::mp.dn_rows + r;
-          p.y[(int64_t)row * S::H + n] = out[t * kMaxStageRows + r];
+          p.y[(int64_t)slot * S::H + n] = wt * out[t * kMaxStageRows + r];
         }
         break;
       default: break;
@@ -776,7 +895,7 @@ struct Consumer {
 
   // A GEMV item: stages of full weight rows, activation rows in passes of kTB.
   template <int K>
-  __device__ void gemv_item(const int32_t* w, int SR, int total_rows, int ntok) {
+  __device__ __forceinline__ void gemv_item(const int32_t* w, int SR, int total_rows, int ntok) {
     const int op = w[F_OP];
     const int nst = w[F_NSTAGE];
     const int nchunk = (ntok + kTB - 1) / kTB;
@@ -788,9 +907,15 @@ struct Consumer {
       const uint16_t* W = reinterpret_cast<const uint16_t*>(stage(slot));
       for (int chunk = 0; chunk < nchunk; ++chunk) {
         const int tb = min(kTB, ntok - kTB * chunk);
-        if (s == 0 || nchunk > 1) {
+        int32_t tag[4];
+        x_tag(op, w, chunk, tag);
+        if (!(tag[0] == sm.xtag[0] && tag[1] == sm.xtag[1] && tag[2] == sm.xtag[2] && tag[3] == sm.xtag[3])) {
+          consumers_sync();  // every warp is done with the old rows
           if (!aborted(c)) load_x<K>(op, w, chunk, tb);
           consumers_sync();
+          if (ct == 0) {
+            sm.xtag[0] = tag[0]; sm.xtag[1] = tag[1]; sm.xtag[2] = tag[2]; sm.xtag[3] = tag[3];
+          }
         }
         if (__all_sync(FULL, ok && !aborted(c))) gemv_rows<K>(W, rows, tb, sm.out[buf]);
         consumers_sync();
@@ -801,25 +926,206 @@ struct Consumer {
     }
   }
 
+  // Pair epilogue, run by lane t for activation row t: v0, v1 are the dot
+  // products of the pair's two weight rows r0, r1 (rows of stage s).
+  __device__ __forceinline__ void pair_epilogue(int op, const int32_t* w, int s, int r0, int r1, int t, float v0,
+                                                float v1, int dslot, float dwt) {
+    const int l = w[F_LAYER];
+    switch (op) {
+      case OP_QKV_PROJ: {
+        // RoPE in the epilogue, then the new K/V into the pool ("Tasks":
+        // QKV_PROJ applies RoPE in-register before writing back)
+        const int row = w[F_A0] + s * S::SR_H + r0;  // even: (row, row + 1) is a rotation pair
+        const int b = t;
+        const int head = row / S::D, dd = row - head * S::D;
+        const int pos = __ldg(p.seq_lens + b) - 1;
+        if (head < S::NQ + S::NKV) {
+          // the angle pos * base^(-dd/D), reduced modulo 2 pi in double; sin/cos in float
+          const double ang = (double)pos * sm.rope_theta[dd / 2];
+          const double red = ang - 6.283185307179586 * rint(ang * 0.15915494309189535);
+          float s0, c0;
+          sincosf((float)red, &s0, &c0);
+          const float x0 = v0 * c0 - v1 * s0, x1 = v0 * s0 + v1 * c0;
+          v0 = x0;
+          v1 = x1;
+        }
+        if (head < S::NQ) {
+          *reinterpret_cast<float2*>(p.q + ((int64_t)b * S::NQ + head) * S::D + dd) = make_float2(v0, v1);
+        } else if (pos >= 0) {
+          const bool is_v = head >= S::NQ + S::NKV;
+          const int g = head - S::NQ - (is_v ? S::NKV : 0);
+          const uint32_t packed = (uint32_t)f_bf16(v0) | ((uint32_t)f_bf16(v1) << 16);
+          *reinterpret_cast<uint32_t*>(p.kvnew + (((int64_t)b * 2 + (is_v ? 1 : 0)) * S::NKV + g) * S::D + dd) = packed;
+          const int lp = pos / S::P;
+          const int page = lp < p.max_pages ? __ldg(p.block_tables + (int64_t)b * p.max_pages + lp) : -1;
+          if (page < 0 || page >= p.num_pages) {
+            record_error(p, ERR_PAGE, c.sm, where_of(w), lp, (uint32_t)page, (uint32_t)p.num_pages);
+          } else {
+            uint16_t* pool = is_v ? p.vpool : p.kpool;
+            const int64_t o = ((((int64_t)l * p.num_pages + page) * S::NKV + g) * S::P + pos % S::P) * S::D + dd;
+            *reinterpret_cast<uint32_t*>(pool + o) = packed;
+          }
+        }
+        break;
+      }
+      case W_UP_TILE: {  // SiLU(gate) * up ("Tasks": the SiLU-and-multiply epilogue)
+        const float act = v0 / (1.f + expf(-v0)) * v1;
+        const int row = w[F_A0 + 2] + t;
+        p.u[(int64_t)row * S::I + w[F_A0 + 1] * S::mp.up_tile + s * S::mp.up_half + r0] = act;
+        break;
+      }
+      case OP_ROUTER_GEMM: {
+        const int e = w[F_A0] + s * S::SR_H + r0;
+        float* dst = p.rlog + ((int64_t)l * p.MB + t) * S::E + e;
+        dst[0] = v0 + (p.rbias ? p.rbias[e] : 0.f);
+        dst[1] = v1 + (p.rbias ? p.rbias[e + 1] : 0.f);
+        break;
+      }
+      case OP_LM_HEAD: {
+        const int v = w[F_A0] + s * S::SR_H + r0;
+        *reinterpret_cast<float2*>(p.logits + (int64_t)t * p.V + v) = make_float2(v0, v1);
+        break;
+      }
+      case OP_O_PROJ: {
+        const int n = w[F_A0] + s * S::SR_O + r0;
+        *reinterpret_cast<float2*>(p.opart + ((int64_t)w[F_A0 + 2] * p.MB + t) * S::H + n) = make_float2(v0, v1);
+        break;
+      }
+      case W_DOWN_TILE: {  // weighted, into the (row b, slot j) of the output
+        const int n = w[F_A0 + 1] * S::mp.dn_tile + s * S::mp.dn_rows + r0;
+        *reinterpret_cast<float2*>(p.y + (int64_t)dslot * S::H + n) = make_float2(dwt * v0, dwt * v1);
+        break;
+      }
+      default: break;
+    }
+  }
+
+  // GEMV of at most kTB activation rows (decode at small batch).  The
+  // consumer warps form two teams of four that take alternate stages, so two
+  // stages are in process at once; within a stage each warp computes a pair
+  // of weight rows against the same activation loads and finishes the pair's
+  // epilogue itself (the RoPE pair for QKV, gate and up rows for the MoE
+  // up/gate), so a stage needs no block-wide barrier.
+  template <int K>
+  __device__ __forceinline__ void gemv_item_teams(const int32_t* w, int SR, int total_rows, int ntok) {
+    constexpr int C = K / 8;
+    constexpr int CPL = (C + 31) / 32;
+    const int op = w[F_OP];
+    const int nst = w[F_NSTAGE];
+    const int tb = ntok;
+    int32_t tag[4];
+    x_tag(op, w, 0, tag);
+    if (!(tag[0] == sm.xtag[0] && tag[1] == sm.xtag[1] && tag[2] == sm.xtag[2] && tag[3] == sm.xtag[3])) {
+      if (!aborted(c)) load_x<K>(op, w, 0, tb);
+      consumers_sync();
+      if (ct == 0) {
+        sm.xtag[0] = tag[0]; sm.xtag[1] = tag[1]; sm.xtag[2] = tag[2]; sm.xtag[3] = tag[3];
+      }
+    }
+    const int team = cw >> 2, tw = cw & 3;
+    const bool up_pairs = op == W_UP_TILE;
+    // down tiles: lane t's output slot (row b, slot j) and router weight, loaded up front
+    int dslot = 0;
+    float dwt = 0.f;
+    if (op == W_DOWN_TILE && lane < tb) {
+      dslot = __ldcg(p.perm + w[F_A0 + 2] + lane);
+      if (dslot < 0 || dslot >= p.B * S::K) dslot = 0;  // only after a failed step
+      dwt = __ldcg(p.topk_w + (int64_t)w[F_LAYER] * p.MB * S::K + dslot);
+    }
+    const float4* xs4 = reinterpret_cast<const float4*>(sm.xs);
+    for (int s = team; s < nst; s += 2) {
+      const uint32_t gs = c.st + (uint32_t)s;
+      const int slot = gs % kStages;
+      const bool ok = __all_sync(FULL, mbar_wait(p, c, &c.hdr->full[slot], (gs / kStages) & 1) && !aborted(c));
+      const int rows = min(SR, total_rows - s * SR);
+      const int npairs = rows / 2;
+      const uint16_t* W = reinterpret_cast<const uint16_t*>(c.stages + (size_t)slot * kStageBytes);
+      if (ok) {
+        for (int pr = tw; pr < npairs; pr += 4) {
+          const int r0 = up_pairs ? pr : 2 * pr;
+          const int r1 = up_pairs ? pr + npairs : 2 * pr + 1;
+          const uint4* w0 = reinterpret_cast<const uint4*>(W + (size_t)r0 * K);
+          const uint4* w1 = reinterpret_cast<const uint4*>(W + (size_t)r1 * K);
+          float a0[kTB], a1[kTB], b0[kTB], b1[kTB];
+#pragma unroll
+          for (int t = 0; t < kTB; ++t) a0[t] = a1[t] = b0[t] = b1[t] = 0.f;
+#pragma unroll
+          for (int j = 0; j < CPL; ++j) {
+            const int cc = lane + 32 * j;
+            if (C % 32 == 0 || cc < C) {
+              const uint4 u0 = w0[cc], u1 = w1[cc];
+#pragma unroll
+              for (int t = 0; t < kTB; ++t)
+                if (t < tb) {
+                  const float4 xa = xs4[t * 2 * C + cc], xb = xs4[t * 2 * C + C + cc];
+                  a0[t] = fmaf(bf16_lo(u0.x), xa.x, a0[t]);
+                  a1[t] = fmaf(bf16_hi(u0.x), xa.y, a1[t]);
+                  b0[t] = fmaf(bf16_lo(u1.x), xa.x, b0[t]);
+                  b1[t] = fmaf(bf16_hi(u1.x), xa.y, b1[t]);
+                  a0[t] = fmaf(bf16_lo(u0.y), xa.z, a0[t]);
+                  a1[t] = fmaf(bf16_hi(u0.y), xa.w, a1[t]);
+                  b0[t] = fmaf(bf16_lo(u1.y), xa.z, b0[t]);
+                  b1[t] = fmaf(bf16_hi(u1.y), xa.w, b1[t]);
+                  a0[t] = fmaf(bf16_lo(u0.z), xb.x, a0[t]);
+                  a1[t] = fmaf(bf16_hi(u0.z), xb.y, a1[t]);
+                  b0[t] = fmaf(bf16_lo(u1.z), xb.x, b0[t]);
+                  b1[t] = fmaf(bf16_hi(u1.z), xb.y, b1[t]);
+                  a0[t] = fmaf(bf16_lo(u0.w), xb.z, a0[t]);
+                  a1[t] = fmaf(bf16_hi(u0.w), xb.w, a1[t]);
+                  b0[t] = fmaf(bf16_lo(u1.w), xb.z, b0[t]);
+                  b1[t] = fmaf(bf16_hi(u1.w), xb.w, b1[t]);
+                }
+            }
+          }
+          float v0[kTB], v1[kTB];
+#pragma unroll
+          for (int t = 0; t < kTB; ++t)
+            if (t < tb) {
+              v0[t] = warp_sum(a0[t] + a1[t]);
+              v1[t] = warp_sum(b0[t] + b1[t]);
+            }
+#pragma unroll
+          for (int t = 0; t < kTB; ++t)
+            if (t < tb && lane == t && !aborted(c)) pair_epilogue(op, w, s, r0, r1, t, v0[t], v1[t], dslot, dwt);
+        }
+      }
+      // the four warps of the team stand for the eight arrivals the stage expects
+      __syncwarp();
+      if (lane == 0) mbar_arrive_n(&c.hdr->empty[slot], kConsumerWarps / 4);
+    }
+    c.st += (uint32_t)nst;
+  }
+
   // --------------------------------------------------------- attention
   // One KV slice of one (row b, KV group g): its G query heads against the
   // keys in [t0, t1), as an unnormalised partial (running max in the log2
   // domain, sum, weighted values) -- "Tasks": ATTN_DECODE on a partial slice.
-  __device__ void attn(const int32_t* w) {
+  __device__ __forceinline__ void attn(const int32_t* w) {
     constexpr int G = S::G, D = S::D, P = S::P, DPL = D / 32;
     const int l = w[F_LAYER], b = w[F_A0], g = w[F_A0 + 1], t0 = w[F_A0 + 2], t1 = w[F_A0 + 3];
     const int pf = w[F_A0 + 4], slot_idx = w[F_A0 + 5], np = w[F_NSTAGE];
-    (void)l;
     const int s = b < p.B ? __ldg(p.seq_lens + b) : 0;
     const int pos = s - 1;
-    const float scale = 1.4426950408889634f / sqrtf((float)D);
+    // the group's queries, scaled by log2(e)/sqrt(D), kept while (layer, b, g) repeats
+    if (np > 0 && !(sm.qtag[0] == l && sm.qtag[1] == b && sm.qtag[2] == g)) {
+      const float scale = 1.4426950408889634f / sqrtf((float)D);
+      const float4* src = reinterpret_cast<const float4*>(p.q + ((int64_t)b * S::NQ + g * G) * D);
+      for (int i = ct; i < G * D / 4; i += kConsumerThreads) {
+        float4 v = __ldcg(src + i);
+        v.x *= scale; v.y *= scale; v.z *= scale; v.w *= scale;
+        reinterpret_cast<float4*>(sm.qs)[i] = v;
+      }
+      consumers_sync();
+      if (ct == 0) {
+        sm.qtag[0] = l; sm.qtag[1] = b; sm.qtag[2] = g;
+      }
+    }
     float qr[G][DPL];
     if (np > 0) {
 #pragma unroll
       for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int i = 0; i < DPL; ++i)
-          qr[h][i] = __ldcg(p.q + ((int64_t)b * S::NQ + g * G + h) * D + lane * DPL + i) * scale;
+        for (int i = 0; i < DPL; ++i) qr[h][i] = sm.qs[h * D + lane * DPL + i];
     }
     // PV thread map: head h = ct % G, dims [4 c4, 4 c4 + 4) with c4 = ct / G
     const bool pv_thread = ct < G * D / 4;
@@ -870,7 +1176,7 @@ struct Consumer {
           const float sc = reduce_scatter<G>(part, lane);
           if ((lane & (32 / G - 1)) == 0) {
             const int h = lane / (32 / G);
-            sm.sc[h * P + tt] = (tok >= t0 && tok < t1) ? sc : -INFINITY;
+            sm.sc[tt * G + h] = (tok >= t0 && tok < t1) ? sc : -INFINITY;
           }
         }
       }
@@ -879,15 +1185,15 @@ struct Consumer {
       if (ok && cw < G) {
         const int h = cw;
         float mx = -INFINITY;
-        for (int tt = lane; tt < P; tt += 32) mx = fmaxf(mx, sm.sc[h * P + tt]);
+        for (int tt = lane; tt < P; tt += 32) mx = fmaxf(mx, sm.sc[tt * G + h]);
         mx = warp_max(mx);
         const float m_old = sm.am[h];
         const float m_new = fmaxf(m_old, mx);
         float sum = 0.f;
         for (int tt = lane; tt < P; tt += 32) {
-          const float sv = sm.sc[h * P + tt];
+          const float sv = sm.sc[tt * G + h];
           const float pv = (m_new == -INFINITY || sv == -INFINITY) ? 0.f : exp2f(sv - m_new);
-          sm.pr[h * P + tt] = pv;
+          sm.pr[tt * G + h] = pv;
           sum += pv;
         }
         sum = warp_sum(sum);
@@ -903,9 +1209,9 @@ struct Consumer {
         const float alpha = sm.aa[ph];
         o[0] *= alpha; o[1] *= alpha; o[2] *= alpha; o[3] *= alpha;
         const uint16_t* vc = Vp + pc * 4;
-#pragma unroll 4
+#pragma unroll 8
         for (int tt = 0; tt < P; ++tt) {
-          const float pv = sm.pr[ph * P + tt];
+          const float pv = sm.pr[tt * G + ph];
           const uint2 u = *reinterpret_cast<const uint2*>(vc + tt * D);
           o[0] = fmaf(pv, bf16_lo(u.x), o[0]);
           o[1] = fmaf(pv, bf16_hi(u.x), o[1]);
@@ -927,7 +1233,9 @@ struct Consumer {
   }
 
   // Merge of the slice partials of (b, g): warp per head ("Tasks": ATTN_COMBINE).
-  __device__ void attn_combine(const int32_t* w) {
+  // Lanes read 32 slices' (max, sum) at once; the weighted values of a block
+  // of slices are then loaded together, so a combine costs a few round trips.
+  __device__ __forceinline__ void attn_combine(const int32_t* w) {
     constexpr int G = S::G, D = S::D, DPL = D / 32;
     const int l = w[F_LAYER], b = w[F_A0], g = w[F_A0 + 1];
     if (b >= p.B || cw >= G) return;
@@ -937,81 +1245,119 @@ struct Consumer {
     const int64_t base = ((int64_t)b * S::NKV + g) * p.max_slots;
     float M = -INFINITY;
     for (int j = lane; j < n; j += 32) {
-      const float lj = __ldcg(p.part_ml + ((base + j) * G + h) * 2 + 1);
-      if (lj > 0.f) M = fmaxf(M, __ldcg(p.part_ml + ((base + j) * G + h) * 2));
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((base + j) * G + h) * 2));
+      if (ml.y > 0.f) M = fmaxf(M, ml.x);
     }
     M = warp_max(M);
     float z = 0.f, acc[DPL];
 #pragma unroll
     for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
-    for (int j = 0; j < n; ++j) {
-      const float mj = __ldcg(p.part_ml + ((base + j) * G + h) * 2);
-      const float lj = __ldcg(p.part_ml + ((base + j) * G + h) * 2 + 1);
-      if (!(lj > 0.f)) continue;
-      const float cj = exp2f(mj - M);
-      z = fmaf(cj, lj, z);
-      const float* oj = p.part_o + ((base + j) * G + h) * D + lane * DPL;
+    for (int j0 = 0; j0 < n; j0 += 32) {
+      // lane jj: the coefficient of slice j0 + jj
+      float cj = 0.f;
+      if (j0 + lane < n) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((base + j0 + lane) * G + h) * 2));
+        if (ml.y > 0.f) {
+          cj = exp2f(ml.x - M);
+          z = fmaf(cj, ml.y, z);
+        }
+      }
+      const int cnt = min(32, n - j0);
+#pragma unroll 8
+      for (int jj = 0; jj < cnt; ++jj) {
+        const float cb = __shfl_sync(FULL, cj, jj);
+        const float* oj = p.part_o + ((base + j0 + jj) * G + h) * D + lane * DPL;
+        if (DPL == 4) {
+          const float4 o4 = __ldcg(reinterpret_cast<const float4*>(oj));
+          acc[0] = fmaf(cb, o4.x, acc[0]);
+          acc[1] = fmaf(cb, o4.y, acc[1]);
+          acc[2 % DPL] = fmaf(cb, o4.z, acc[2 % DPL]);
+          acc[3 % DPL] = fmaf(cb, o4.w, acc[3 % DPL]);
+        } else {
 #pragma unroll
-      for (int i = 0; i < DPL; ++i) acc[i] = fmaf(cj, __ldcg(oj + i), acc[i]);
+          for (int i = 0; i < DPL; ++i) acc[i] = fmaf(cb, __ldcg(oj + i), acc[i]);
+        }
+      }
     }
+    z = warp_sum(z);
     const float inv = 1.f / z;
-    uint16_t* dst = p.attn_out + (int64_t)b * S::NQ * D + (int64_t)(g * G + h) * D + lane * DPL;
+    float* dst = p.attn_out + (int64_t)b * S::NQ * D + (int64_t)(g * G + h) * D + lane * DPL;
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) dst[i] = f_bf16(acc[i] * inv);
+    for (int i = 0; i < DPL; ++i) dst[i] = acc[i] * inv;
   }
 
   // ------------------------------------------------------------- norm
   // Residual add + RMSNorm ("1. Reduce wave quantization": attention and MoE
   // rejoin only at the fused residual add + RMSNorm at the end of the layer).
   // Layer 0 starts from the embedding row; with the combine fused, the MoE
-  // output of the previous layer is summed here from the expert rows.
-  __device__ void norm(const int32_t* w) {
-    constexpr int PER = S::H / kConsumerThreads;
+  // output of the previous layer is the sum of the row's K expert outputs,
+  // which the down projection stored already weighted, one slot per (row, k).
+  // Every operand is loaded with one round of independent 16-byte loads.
+  __device__ __forceinline__ void norm(const int32_t* w) {
+    constexpr int H4 = S::H / 4, PER = (H4 + kConsumerThreads - 1) / kConsumerThreads;
     const int l = w[F_LAYER], b1 = min(w[F_A0 + 1], p.B);
     const bool final_norm = w[F_A0 + 2] != 0, fused = w[F_A0 + 3] != 0;
     for (int b = w[F_A0]; b < b1; ++b) {
-      float v[PER];
+      float4 v[PER];
+#pragma unroll
+      for (int k = 0; k < PER; ++k) v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (l == 0) {
         const int sl = __ldg(p.seq_lens + b);
-        if ((sl < 1 || sl > p.max_ctx) && ct == 0) record_error(p, ERR_INDEX, c.sm, w, -1, (uint32_t)sl, (uint32_t)p.max_ctx);
+        if ((sl < 1 || sl > p.max_ctx) && ct == 0) record_error(p, ERR_INDEX, c.sm, where_of(w), -1, (uint32_t)sl, (uint32_t)p.max_ctx);
         int tok = __ldg(p.tokens + b);
         if (tok < 0 || tok >= p.V) {
-          if (ct == 0) record_error(p, ERR_INDEX, c.sm, w, -1, (uint32_t)tok, (uint32_t)p.V);
+          if (ct == 0) record_error(p, ERR_INDEX, c.sm, where_of(w), -1, (uint32_t)tok, (uint32_t)p.V);
           tok = 0;
         }
 #pragma unroll
-        for (int k = 0; k < PER; ++k) v[k] = bf16_f(__ldg(p.emb + (int64_t)tok * S::H + ct + k * kConsumerThreads));
-      } else {
-        int rows[S::K];
-        float wts[S::K];
-        if (fused) {
-#pragma unroll
-          for (int j = 0; j < S::K; ++j) {
-            int r = __ldcg(p.inv + b * S::K + j);
-            rows[j] = (r >= 0 && r < p.B * S::K) ? r : 0;
-            wts[j] = __ldcg(p.topk_w + ((int64_t)(l - 1) * p.MB + b) * S::K + j);
+        for (int k = 0; k < PER; ++k) {
+          const int i4 = ct + k * kConsumerThreads;
+          if (H4 % kConsumerThreads == 0 || i4 < H4) {
+            const uint2 e = __ldg(reinterpret_cast<const uint2*>(p.emb + (int64_t)tok * S::H) + i4);
+            v[k] = make_float4(bf16_lo(e.x), bf16_hi(e.x), bf16_lo(e.y), bf16_hi(e.y));
           }
         }
+      } else {
+        const float4* h4 = reinterpret_cast<const float4*>(p.h + (int64_t)b * S::H);
 #pragma unroll
         for (int k = 0; k < PER; ++k) {
-          const int i = ct + k * kConsumerThreads;
-          float a = __ldcg(p.h + (int64_t)b * S::H + i);
+          const int i4 = ct + k * kConsumerThreads;
+          if (H4 % kConsumerThreads == 0 || i4 < H4) {
+            float4 parts[1 + S::NKV + S::K];
+            int n = 0;
+            parts[n++] = __ldcg(h4 + i4);
 #pragma unroll
-          for (int g = 0; g < S::NKV; ++g) a += __ldcg(p.opart + ((int64_t)g * p.MB + b) * S::H + i);
-          if (fused) {
-            float m = 0.f;
+            for (int g = 0; g < S::NKV; ++g)
+              parts[n++] = __ldcg(reinterpret_cast<const float4*>(p.opart + ((int64_t)g * p.MB + b) * S::H) + i4);
+            if (fused) {
 #pragma unroll
-            for (int j = 0; j < S::K; ++j) m = fmaf(wts[j], __ldcg(p.y + (int64_t)rows[j] * S::H + i), m);
-            a += m;
-          } else {
-            a += __ldcg(p.moe_out + (int64_t)b * S::H + i);
+              for (int j = 0; j < S::K; ++j)
+                parts[n++] = __ldcg(reinterpret_cast<const float4*>(p.y + ((int64_t)b * S::K + j) * S::H) + i4);
+            } else {
+              parts[n++] = __ldcg(reinterpret_cast<const float4*>(p.moe_out + (int64_t)b * S::H) + i4);
+            }
+            // residual + attention partials, then the MoE output summed on its own
+            // (the same order as a separate MOE_COMBINE)
+            float4 a = parts[0];
+#pragma unroll
+            for (int q = 1; q <= S::NKV; ++q) {
+              a.x += parts[q].x; a.y += parts[q].y; a.z += parts[q].z; a.w += parts[q].w;
+            }
+            float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 1 + S::NKV; q < 1 + S::NKV + S::K; ++q)
+              if (q < n) {
+                m.x += parts[q].x; m.y += parts[q].y; m.z += parts[q].z; m.w += parts[q].w;
+              }
+            a.x += m.x; a.y += m.y; a.z += m.z; a.w += m.w;
+            v[k] = a;
           }
-          v[k] = a;
         }
       }
       float ss = 0.f;
 #pragma unroll
-      for (int k = 0; k < PER; ++k) ss = fmaf(v[k], v[k], ss);
+      for (int k = 0; k < PER; ++k)
+        ss = fmaf(v[k].x, v[k].x, fmaf(v[k].y, v[k].y, fmaf(v[k].z, v[k].z, fmaf(v[k].w, v[k].w, ss))));
       ss = warp_sum(ss);
       if (lane == 0) sm.red[cw] = ss;
       consumers_sync();
@@ -1019,13 +1365,17 @@ struct Consumer {
 #pragma unroll
       for (int i = 0; i < kConsumerWarps; ++i) tot += sm.red[i];
       const float inv_rms = 1.f / sqrtf(tot / (float)S::H + p.eps);
-      const float* gam = final_norm ? p.gamma_f : p.gamma + (int64_t)l * S::H;
+      const float4* gam = reinterpret_cast<const float4*>(final_norm ? p.gamma_f : p.gamma + (int64_t)l * S::H);
 #pragma unroll
       for (int k = 0; k < PER; ++k) {
-        const int i = ct + k * kConsumerThreads;
-        p.x[(int64_t)b * S::H + i] = f_bf16(v[k] * inv_rms * __ldg(gam + i));
-        p.h[(int64_t)b * S::H + i] = v[k];
-        if (p.htrace) p.htrace[((int64_t)l * p.MB + b) * S::H + i] = v[k];
+        const int i4 = ct + k * kConsumerThreads;
+        if (H4 % kConsumerThreads == 0 || i4 < H4) {
+          const float4 gm = __ldg(gam + i4), a = v[k];
+          reinterpret_cast<float4*>(p.x + (int64_t)b * S::H)[i4] =
+              make_float4(a.x * inv_rms * gm.x, a.y * inv_rms * gm.y, a.z * inv_rms * gm.z, a.w * inv_rms * gm.w);
+          reinterpret_cast<float4*>(p.h + (int64_t)b * S::H)[i4] = a;
+          if (p.htrace) reinterpret_cast<float4*>(p.htrace + ((int64_t)l * p.MB + b) * S::H)[i4] = a;
+        }
       }
       consumers_sync();
     }
@@ -1034,7 +1384,7 @@ struct Consumer {
   // ------------------------------------------------------------ routing
   // Top-k of each row's router logits (higher logit first, lower expert id on
   // ties) and softmax weights over the selected logits ("Tasks": ROUTER_TOPK).
-  __device__ void topk(const int32_t* w) {
+  __device__ __forceinline__ void topk(const int32_t* w) {
     constexpr int E = S::E, K = S::K, PL = (E + 31) / 32;
     const int l = w[F_LAYER], b1 = min(w[F_A0 + 1], p.B);
     for (int b = w[F_A0] + cw; b < b1; b += kConsumerWarps) {
@@ -1084,180 +1434,260 @@ struct Consumer {
         for (int j = 0; j < K; ++j) {
           p.topk_ids[((int64_t)l * p.MB + b) * K + j] = ids[j];
           p.topk_w[((int64_t)l * p.MB + b) * K + j] = e_[j] / z;
+          sm.ids[b * K + j] = ids[j];
         }
       }
     }
-    if (w[F_A0 + 2]) {
-      consumers_sync();
-      finalize(l);
+    if (w[F_A0 + 2]) {  // the one top-k task also builds the queues, from shared memory
+      if (p.B > 1) consumers_sync();
+      else __syncwarp();  // one row: warp 0 wrote the routing
+      finalize(l, false);
     }
   }
 
   // Per-expert counts and offsets, the expert-ordered row list (rows of an
-  // expert by row b ascending) and the tile queues of the up/gate and down
-  // drains, experts ascending ("Tasks": ROUTE_FINALIZE generates the MoE GEMM
-  // work queue).  Deterministic: no order depends on atomics.
-  __device__ void finalize(int l) {
-    constexpr int E = S::E, K = S::K;
+  // expert by row b ascending) and the list of active experts, ascending
+  // ("Tasks": ROUTE_FINALIZE generates the MoE GEMM work queue).  The queue of
+  // the up/gate drain is (active expert a, tile t) for a ascending, t
+  // ascending -- entry i is (list[i / tiles], i % tiles) -- and likewise for the
+  // down drain, so the list is all the queue needs.  One warp does it, with
+  // every lane owning a few experts' row bitmaps; nothing depends on atomics.
+  __device__ __forceinline__ void finalize(int l, bool load_ids) {
+    if (cw != 0) return;
+    constexpr int E = S::E, K = S::K, PL = (E + 31) / 32;
     constexpr MoePlan mp = S::mp;
-    const int B = p.B;
-    for (int e = ct; e < E; e += kConsumerThreads) sm.mask[e] = 0ull;
-    consumers_sync();
-    for (int i = ct; i < B * K; i += kConsumerThreads) {
-      const int b = i / K;
-      int e = __ldcg(p.topk_ids + ((int64_t)l * p.MB + b) * K + (i - b * K));
+    const int B = p.B, n = B * K;
+    if (load_ids) {  // a separate task: the routing comes from global memory
+      for (int i = lane; i < n; i += 32) {
+        const int b = i / K;
+        sm.ids[i] = __ldcg(p.topk_ids + ((int64_t)l * p.MB + b) * K + (i - b * K));
+      }
+      __syncwarp();
+    }
+    unsigned long long m[PL];
+#pragma unroll
+    for (int k = 0; k < PL; ++k) m[k] = 0ull;
+    for (int i = 0; i < n; ++i) {
+      int e = sm.ids[i];
       if (e < 0 || e >= E) {
-        record_error(p, ERR_INDEX, c.sm, nullptr, -1, (uint32_t)e, E);
+        if (lane == 0) record_error(p, ERR_INDEX, c.sm, kNowhere, -1, (uint32_t)e, E);
         e = 0;
       }
-      atomicOr(&sm.mask[e], 1ull << b);
+      const unsigned long long bit = 1ull << (i / K);
+#pragma unroll
+      for (int k = 0; k < PL; ++k)
+        if (e == lane * PL + k) m[k] |= bit;
     }
-    consumers_sync();
-    if (cw == 0) {
-      constexpr int PL = (E + 31) / 32;
-      int cnt[PL], a[PL];
-      int rs = 0, as = 0;
+    int cnt[PL], a[PL];
+    int rs = 0, as = 0;
 #pragma unroll
-      for (int k = 0; k < PL; ++k) {
-        const int e = lane * PL + k;
-        cnt[k] = e < E ? __popcll(sm.mask[e]) : 0;
-        a[k] = cnt[k] > 0;
-        rs += cnt[k];
-        as += a[k];
-      }
-      int ri = rs, ai = as;  // inclusive scans over lanes
+    for (int k = 0; k < PL; ++k) {
+      cnt[k] = __popcll(m[k]);
+      a[k] = cnt[k] > 0;
+      rs += cnt[k];
+      as += a[k];
+    }
+    int ri = rs, ai = as;  // inclusive scans over lanes
 #pragma unroll
-      for (int m = 1; m < 32; m <<= 1) {
-        const int r2 = __shfl_up_sync(FULL, ri, m), a2 = __shfl_up_sync(FULL, ai, m);
-        if (lane >= m) {
-          ri += r2;
-          ai += a2;
-        }
-      }
-      int ro = ri - rs, ao = ai - as;
-#pragma unroll
-      for (int k = 0; k < PL; ++k) {
-        const int e = lane * PL + k;
-        if (e < E) {
-          sm.cnt[e] = cnt[k];
-          sm.off[e] = ro;
-          sm.act[e] = ao;
-        }
-        ro += cnt[k];
-        ao += a[k];
-      }
-      if (lane == 31) {
-        sm.off[E] = ri;
-        sm.act[E] = ai;
+    for (int d = 1; d < 32; d <<= 1) {
+      const int r2 = __shfl_up_sync(FULL, ri, d), a2 = __shfl_up_sync(FULL, ai, d);
+      if (lane >= d) {
+        ri += r2;
+        ai += a2;
       }
     }
-    consumers_sync();
-    for (int i = ct; i < B * K; i += kConsumerThreads) {
+    int ro = ri - rs, ao = ai - as;
+#pragma unroll
+    for (int k = 0; k < PL; ++k) {
+      const int e = lane * PL + k;
+      if (e < E) {
+        sm.mask[e] = m[k];
+        sm.off[e] = ro;
+        p.ecount[(int64_t)l * E + e] = cnt[k];
+        p.eoff[e] = ro;
+        if (a[k]) p.upq[ao] = e;
+      }
+      ro += cnt[k];
+      ao += a[k];
+    }
+    if (lane == 31) {
+      p.eoff[E] = ri;
+      p.qlen[0] = ai * mp.up_tiles;
+      p.qlen[1] = ai * mp.dn_tiles;
+    }
+    __syncwarp();
+    for (int i = lane; i < n; i += 32) {
       const int b = i / K;
-      int e = __ldcg(p.topk_ids + ((int64_t)l * p.MB + b) * K + (i - b * K));
+      int e = sm.ids[i];
       if (e < 0 || e >= E) e = 0;
       const int rank = __popcll(sm.mask[e] & ((1ull << b) - 1ull));
       const int row = sm.off[e] + rank;
       p.perm[row] = i;
       p.inv[i] = row;
     }
-    for (int e = ct; e < E; e += kConsumerThreads) {
-      const int n = sm.cnt[e];
-      p.ecount[(int64_t)l * E + e] = n;
-      p.eoff[e] = sm.off[e];
-      if (n > 0) {
-        const int a = sm.act[e];
-        for (int t = 0; t < mp.up_tiles; ++t) p.upq[a * mp.up_tiles + t] = (e << 16) | t;
-        for (int t = 0; t < mp.dn_tiles; ++t) p.dnq[a * mp.dn_tiles + t] = (e << 16) | t;
-      }
-    }
-    if (ct == 0) {
-      p.eoff[E] = sm.off[E];
-      p.qlen[0] = sm.act[E] * mp.up_tiles;
-      p.qlen[1] = sm.act[E] * mp.dn_tiles;
-    }
   }
 
   // expert-ordered copy of the routed rows ("Tasks": MOE_GATHER)
-  __device__ void gather(const int32_t* w) {
-    constexpr int C = S::H / 8;
+  __device__ __forceinline__ void gather(const int32_t* w) {
+    constexpr int C = S::H / 4;
     const int r0 = w[F_A0], r1 = min(r0 + w[F_A0 + 1], p.B * S::K);
     for (int i = ct; i < (r1 - r0) * C; i += kConsumerThreads) {
       const int r = r0 + i / C, cc = i % C;
       int pr = __ldcg(p.perm + r);
       int b = pr / S::K;
       if (pr < 0 || b >= p.B) b = 0;
-      reinterpret_cast<uint4*>(p.xg + (int64_t)r * S::H)[cc] =
-          __ldcg(reinterpret_cast<const uint4*>(p.x + (int64_t)b * S::H) + cc);
+      reinterpret_cast<float4*>(p.xg + (int64_t)r * S::H)[cc] =
+          __ldcg(reinterpret_cast<const float4*>(p.x + (int64_t)b * S::H) + cc);
     }
   }
 
-  // weighted sum of each row's expert outputs ("Tasks": MOE_COMBINE)
-  __device__ void moe_combine(const int32_t* w) {
-    const int l = w[F_LAYER], b1 = min(w[F_A0 + 1], p.B);
+  // weighted sum of each row's expert outputs ("Tasks": MOE_COMBINE); the
+  // down projection stored each output already weighted in the row's slot
+  __device__ __forceinline__ void moe_combine(const int32_t* w) {
+    const int b1 = min(w[F_A0 + 1], p.B);
     for (int b = w[F_A0]; b < b1; ++b) {
-      int rows[S::K];
-      float wts[S::K];
+      for (int i4 = ct; i4 < S::H / 4; i4 += kConsumerThreads) {
+        float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int j = 0; j < S::K; ++j) {
-        const int r = __ldcg(p.inv + b * S::K + j);
-        rows[j] = (r >= 0 && r < p.B * S::K) ? r : 0;
-        wts[j] = __ldcg(p.topk_w + ((int64_t)l * p.MB + b) * S::K + j);
-      }
-      for (int i = ct; i < S::H; i += kConsumerThreads) {
-        float m = 0.f;
-#pragma unroll
-        for (int j = 0; j < S::K; ++j) m = fmaf(wts[j], __ldcg(p.y + (int64_t)rows[j] * S::H + i), m);
-        p.moe_out[(int64_t)b * S::H + i] = m;
+        for (int j = 0; j < S::K; ++j) {
+          const float4 y = __ldcg(reinterpret_cast<const float4*>(p.y + ((int64_t)b * S::K + j) * S::H) + i4);
+          m.x += y.x; m.y += y.y; m.z += y.z; m.w += y.w;
+        }
+        reinterpret_cast<float4*>(p.moe_out + (int64_t)b * S::H)[i4] = m;
       }
     }
   }
 
-  __device__ void execute(const int32_t* w) {
+  __device__ __forceinline__ void execute(const int32_t* w) {
     switch (w[F_OP]) {
       case OP_QKV_PROJ:
       case OP_ROUTER_GEMM:
-      case OP_LM_HEAD: gemv_item<S::H>(w, S::SR_H, w[F_A0 + 1], p.B); break;
-      case OP_O_PROJ: gemv_item<S::G * S::D>(w, S::SR_O, w[F_A0 + 1], p.B); break;
-      case W_UP_TILE: gemv_item<S::H>(w, 2 * S::mp.up_half, 2 * S::mp.up_half * S::mp.up_stages, w[F_A0 + 3]); break;
-      case W_DOWN_TILE: gemv_item<S::I>(w, S::mp.dn_rows, S::mp.dn_tile, w[F_A0 + 3]); break;
+      case OP_LM_HEAD:
+        if (p.B <= kTB) gemv_item_teams<S::H>(w, S::SR_H, w[F_A0 + 1], p.B);
+        else gemv_item<S::H>(w, S::SR_H, w[F_A0 + 1], p.B);
+        break;
+      case OP_O_PROJ:
+        if (p.B <= kTB) gemv_item_teams<S::G * S::D>(w, S::SR_O, w[F_A0 + 1], p.B);
+        else gemv_item<S::G * S::D>(w, S::SR_O, w[F_A0 + 1], p.B);
+        break;
+      case W_UP_TILE:
+        if (w[F_A0 + 3] <= kTB)
+          gemv_item_teams<S::H>(w, 2 * S::mp.up_half, 2 * S::mp.up_half * S::mp.up_stages, w[F_A0 + 3]);
+        else
+          gemv_item<S::H>(w, 2 * S::mp.up_half, 2 * S::mp.up_half * S::mp.up_stages, w[F_A0 + 3]);
+        break;
+      case W_DOWN_TILE:
+        if (w[F_A0 + 3] <= kTB) gemv_item_teams<S::I>(w, S::mp.dn_rows, S::mp.dn_tile, w[F_A0 + 3]);
+        else gemv_item<S::I>(w, S::mp.dn_rows, S::mp.dn_tile, w[F_A0 + 3]);
+        break;
       case W_ATTN: attn(w); break;
       case OP_ATTN_COMBINE: attn_combine(w); break;
       case OP_RESID_NORM: norm(w); break;
       case OP_ROUTER_TOPK: topk(w); break;
-      case OP_ROUTE_FINALIZE: finalize(w[F_LAYER]); break;
+      case OP_ROUTE_FINALIZE: finalize(w[F_LAYER], true); break;
       case OP_MOE_GATHER: gather(w); break;
       case OP_MOE_COMBINE: moe_combine(w); break;
       default: break;  // NOP, CLAIM_END: only the signal
     }
   }
 
-  __device__ void run() {
+  __device__ __forceinline__ void run() {
+    // per-CTA set-up: the RoPE frequencies and empty activation caches
+    for (int i = ct; i < S::D / 2; i += kConsumerThreads)
+      sm.rope_theta[i] = pow((double)p.rope_base, -(double)(2 * i) / (double)S::D);
+    if (ct < 4) sm.xtag[ct] = sm.qtag[ct] = -1;
+    consumers_sync();
+    // thread 0 remembers a few counters it has already seen reach a count
+    int cbar[4] = {-1, -1, -1, -1};
+    uint32_t cval[4] = {0, 0, 0, 0};
+    int crr = 0;
+    auto wait_cached = [&](int bar, uint32_t tgt, const int32_t* w) -> bool {
+      if (bar < 0 || tgt == 0) return true;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (cbar[k] == bar && cval[k] >= tgt) return true;
+      if (!wait_counter(p, c, bar, tgt, where_of(w))) return false;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (k == crr) {
+          cbar[k] = bar;
+          cval[k] = tgt;
+        }
+      crr = (crr + 1) & 3;
+      return true;
+    };
+    uint32_t n_items = 0;
     for (;;) {
       const int slot = c.wk % kWorkRing;
       bool ok = mbar_wait(p, c, &c.hdr->wfull[slot], (c.wk / kWorkRing) & 1);
       int32_t w[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) w[k] = c.hdr->work[slot][k];
+      const int64_t t_pop = (ct == 0 && (p.trace || p.stats)) ? gtimer() : 0;
       if (ok && ct == 0) {
-        ok = wait_counter(p, c, w[F_WAIT0], (uint32_t)(w[F_TGT0] == TGT_DYN_SPLITS
-                                                             ? (w[F_A0] < p.B ? slices_of(p, __ldg(p.seq_lens + w[F_A0])) : 0)
-                                                             : w[F_TGT0]), w) &&
-             wait_counter(p, c, w[F_WAIT1], (uint32_t)w[F_TGT1], w);
+        const uint32_t tgt0 = (uint32_t)(w[F_TGT0] == TGT_DYN_SPLITS
+                                             ? (w[F_A0] < p.B ? slices_of(p, __ldg(p.seq_lens + w[F_A0])) : 0)
+                                             : w[F_TGT0]);
+        ok = wait_cached(w[F_WAIT0], tgt0, w) && wait_cached(w[F_WAIT1], (uint32_t)w[F_TGT1], w);
       }
+      const int64_t t_go = (ct == 0 && (p.trace || p.stats)) ? gtimer() : 0;
       if (bar_or(kBarConsumers, kConsumerThreads, !ok || aborted(c))) return;
-      if (ct == 0) mbar_arrive(&c.hdr->wempty[slot]);
       ++c.wk;
-      if (w[F_OP] == W_EXIT) return;
-      execute(w);
-      if (bar_or(kBarConsumers, kConsumerThreads, aborted(c))) return;
-      if (ct == 0) {
-        if (w[F_SIG0] >= 0) red_release_add(p.bars + w[F_SIG0], 1u);
-        if (w[F_SIG1] >= 0) red_release_add(p.bars + w[F_SIG1], 1u);
+      if (w[F_OP] == W_EXIT) {
+        if (p.stats && ct == 0) {
+          uint64_t* st = p.stats + (int64_t)c.sm * kStats;
+          st[0] = c.stat[0];
+          st[1] = c.stat[1];
+          st[2] = c.stat[2];
+          st[3] = n_items;
+        }
+        return;
       }
+      execute(w);
+      if (ct == 0 && (p.trace || p.stats)) {
+        const int64_t t_end = gtimer();
+        c.stat[0] += t_go - t_pop;
+        c.stat[2] += t_end - t_go;
+        if (p.trace && (int)n_items < p.trace_cap) {
+          // record: popped, waits done, end (ns), and op | layer << 8 | task << 16 | a0 << 40
+          uint64_t* r = p.trace + ((int64_t)c.sm * p.trace_cap + n_items) * 4;
+          r[0] = (uint64_t)t_pop;
+          r[1] = (uint64_t)t_go;
+          r[2] = (uint64_t)t_end;
+          r[3] = (uint64_t)(w[F_OP] & 0xff) | ((uint64_t)(w[F_LAYER] & 0xff) << 8) |
+                 ((uint64_t)(uint32_t)(w[F_TASK] & 0xffffff) << 16) |
+                 ((uint64_t)(uint32_t)(w[F_A0] & 0xffffff) << 40);
+        }
+      }
+      ++n_items;
+      // hand the item to the storer, which publishes it ("Storer: signal output barriers")
+      mbar_arrive(&c.hdr->done[slot]);
     }
   }
 };
+
+// ======================================================================
+// storer
+// ======================================================================
+// Publishes each finished item: after every consumer has arrived on the
+// slot's `done` barrier (their outputs are written), one release add per
+// signalled counter, then the slot goes back to the producer.
+static __device__ void storer(const Params& p, Ctx& c) {
+  if ((threadIdx.x & 31) != 0) return;
+  Hdr* H = c.hdr;
+  for (;;) {
+    const int slot = c.wk % kWorkRing;
+    const uint32_t par = (c.wk / kWorkRing) & 1;
+    if (!mbar_wait(p, c, &H->wfull[slot], par)) return;
+    const int op = H->work[slot][F_OP], sig0 = H->work[slot][F_SIG0], sig1 = H->work[slot][F_SIG1];
+    if (op == W_EXIT) return;
+    if (!mbar_wait(p, c, &H->done[slot], par)) return;
+    if (sig0 >= 0) red_release_add(p.bars + sig0, 1u);
+    if (sig1 >= 0) red_release_add(p.bars + sig1, 1u);
+    mbar_arrive(&H->wempty[slot]);
+    ++c.wk;
+  }
+}
 
 template <class S>
 __global__ void __launch_bounds__(kThreads, 1) mk_persistent(const __grid_constant__ Params p) {
@@ -1276,20 +1706,23 @@ __global__ void __launch_bounds__(kThreads, 1) mk_persistent(const __grid_consta
     for (int i = 0; i < kWorkRing; ++i) {
       mbar_init(&hdr->wfull[i], 1);
       mbar_init(&hdr->wempty[i], 1);
+      mbar_init(&hdr->done[i], kConsumerThreads);
     }
     hdr->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  Ctx c{hdr, smem, (int)blockIdx.x, 0u, 0u};
+  Ctx c{hdr, smem, (int)blockIdx.x, 0u, 0u, {0, 0, 0, 0}};
   const int warp = threadIdx.x / 32;
   if (warp == 0) {
     controller(p, c);
   } else if (warp == 1) {
-    Producer<S> pr{p, c};
+    Producer<S> pr{p, c, 0ull};
     pr.run();
+  } else if (warp == 2) {
+    storer(p, c);
   } else {
-    const int ct = threadIdx.x - 64;
+    const int ct = threadIdx.x - 96;
     Consumer<S> cs{p, c, *scr, ct, ct / 32, ct & 31};
     cs.run();
   }

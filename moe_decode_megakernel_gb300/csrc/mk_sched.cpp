@@ -165,7 +165,7 @@ static int build(mk_sched* s) {
   // tile sizes (multiples of the stage rows)
   const int sr_h = stage_rows(D.H), sr_o = stage_rows(G * D.D);
   auto round_to = [](int v, int m) { return std::max(m, (v / m) * m); };
-  const int qkv_tile = o.qkv_tile_rows > 0 ? round_to(o.qkv_tile_rows, sr_h) : std::min(64, D.D);
+  const int qkv_tile = o.qkv_tile_rows > 0 ? round_to(o.qkv_tile_rows, sr_h) : std::max(sr_h, std::min(32, D.D));
   if (D.D % qkv_tile != 0 || qkv_tile % sr_h != 0)
     return fail(MK_ERR_ARG, "qkv_tile_rows must divide head_dim and be a multiple of the stage rows");
   const int o_tile = o.o_tile_rows > 0 ? round_to(o.o_tile_rows, sr_o) : round_to(64, sr_o);
@@ -327,12 +327,14 @@ static int build(mk_sched* s) {
     lb.n_o = (int)w_o.size();
 
     auto add = [&](std::vector<Desc>& w) { all.insert(all.end(), w.begin(), w.end()); };
+    // the router and the routing head each layer's list: the MoE branch waits on
+    // them, and QKV tiles would otherwise sit in front of them on their SMs
     add(w_norm);
-    add(w_qkv);
     add(w_router);
     add(w_topk);
     add(w_fin);
     add(w_gather);
+    add(w_qkv);
     add(w_attn);
     switch (o.wave_order) {
       case MK_WAVES_INTERLEAVED:
@@ -376,12 +378,12 @@ static void layout_workspace(mk_sched* s) {
   w.add("barriers", sizeof(uint32_t) * s->bar_kind.size());
   w.add("error", sizeof(uint32_t) * 8);
   w.add("h", sizeof(float) * MB * D.H);
-  w.add("x", 2ull * MB * D.H);
+  w.add("x", sizeof(float) * MB * D.H);
   w.add("q", sizeof(float) * MB * D.NQ * D.D);
   w.add("kvnew", 2ull * MB * 2 * D.NKV * D.D);
   w.add("part_o", sizeof(float) * (size_t)MB * D.NKV * s->max_slots * G * D.D);
   w.add("part_ml", sizeof(float) * (size_t)MB * D.NKV * s->max_slots * G * 2);
-  w.add("attn_out", 2ull * MB * D.NQ * D.D);
+  w.add("attn_out", sizeof(float) * MB * D.NQ * D.D);
   w.add("opart", sizeof(float) * (size_t)D.NKV * MB * D.H);
   w.add("router_logits", sizeof(float) * (size_t)L * MB * D.E);
   w.add("topk_ids", sizeof(int32_t) * (size_t)L * MB * D.K);
@@ -390,14 +392,21 @@ static void layout_workspace(mk_sched* s) {
   w.add("expert_offset", sizeof(int32_t) * (D.E + 1));
   w.add("perm", sizeof(int32_t) * MB * D.K);
   w.add("inv", sizeof(int32_t) * MB * D.K);
-  w.add("moe_queue", sizeof(int32_t) * (size_t)D.E * s->plan.up_tiles);
-  w.add("moe_down_queue", sizeof(int32_t) * (size_t)D.E * s->plan.dn_tiles);
+  w.add("moe_queue", sizeof(int32_t) * (size_t)D.E);
   w.add("moe_queue_len", sizeof(int32_t) * 2);
-  w.add("xg", s->opts.explicit_gather ? 2ull * MB * D.K * D.H : 16);
-  w.add("u", 2ull * MB * D.K * D.I);
+  w.add("xg", s->opts.explicit_gather ? sizeof(float) * MB * D.K * D.H : 16);
+  w.add("u", sizeof(float) * MB * D.K * D.I);
   w.add("y", sizeof(float) * (size_t)MB * D.K * D.H);
   w.add("moe_out", sizeof(float) * (size_t)MB * D.H);
   if (s->opts.trace_hidden) w.add("hidden_trace", sizeof(float) * (size_t)(L + 1) * MB * D.H);
+  if (s->opts.trace) {
+    size_t most = 0;
+    for (const auto& l : s->per_sm) most = std::max(most, l.size());
+    // tasks, plus the tiles and slices a claimer can take
+    s->trace_cap = (int)(2 * most + 64 * (size_t)L + 1024);
+    w.add("trace", sizeof(uint64_t) * 4 * (size_t)s->num_sms * s->trace_cap);
+    w.add("stats", sizeof(uint64_t) * kStats * (size_t)s->num_sms);
+  }
   w.total = (w.total + 255) & ~(size_t)255;
 }
 

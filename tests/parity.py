@@ -74,6 +74,7 @@ def run_gpu(inp: synth.StepInputs, opts=None, steps: int = 1) -> GpuStep:
     torch.cuda.synchronize()
     L, K = shape.n_layers, shape.top_k
     ids = sess.region("topk_ids", torch.int32, L * B * K).view(L, B, K)  # stride MB == B
+    rlog = sess.region("router_logits", torch.float32, L * B * shape.n_experts).view(L, B, -1)
     wts = sess.region("topk_w", torch.float32, L * B * K).view(L, B, K)
     # the new K/V of every layer, read back from the pool at position seq_len - 1
     pos = inp.seq_lens - 1
@@ -83,7 +84,7 @@ def run_gpu(inp: synth.StepInputs, opts=None, steps: int = 1) -> GpuStep:
     vv = torch.stack([vp[:, int(pages[b]), :, int(pos[b] % P), :] for b in range(B)], 1)
     to_f = lambda t: synth.bf16_bits_to_f32(t.cpu().numpy())
     res = GpuStep(logits.cpu().numpy(), ids.cpu().numpy().copy(), wts.cpu().numpy().copy(),
-                  to_f(kk), to_f(vv), sess, {})
+                  to_f(kk), to_f(vv), sess, {"router_logits": rlog.cpu().numpy().copy()})
     del kp, vp
     return res
 
@@ -104,6 +105,9 @@ class Report:
     greedy_agree: int
     greedy_total: int
     kv_max_err: float
+    router_err: np.ndarray  # per layer: max |gpu - oracle| router logit
+    weight_err: float
+    routing_violations: list
 
 
 def compare(inp: synth.StepInputs, g: GpuStep, rows=None) -> Report:
@@ -113,8 +117,11 @@ def compare(inp: synth.StepInputs, g: GpuStep, rows=None) -> Report:
     rows = np.arange(B) if rows is None else np.asarray(rows)
     ref = oracle.decode_step(shape, w.seed, inp.tokens, inp.seq_lens, inp.block_tables,
                              inp.router_bias, rows=rows, force_ids=g.ids, want_kv=True)
+    rerr = np.array([max(float(np.max(np.abs(g.extra["router_logits"][l, b] - ref.router_logits[l, r])))
+                         for r, b in enumerate(rows)) for l in range(L)])
     # routing: the GPU's experts must be a top-k of the oracle's logits (within a tie)
     exact = ties = 0
+    bad = []
     for l in range(L):
         for r, b in enumerate(rows):
             gi = [int(e) for e in g.ids[l, b]]
@@ -128,12 +135,14 @@ def compare(inp: synth.StepInputs, g: GpuStep, rows=None) -> Report:
             ok = all(lg[e] >= kth - MARGIN_TOL for e in gi)
             ok &= all(lg[e] <= kth + MARGIN_TOL for e in set(own) - set(gi))
             ok &= all(lg[gi[j]] >= lg[gi[j + 1]] - MARGIN_TOL for j in range(K - 1))
-            assert ok, f"layer {l} row {b}: GPU experts {gi} vs oracle {own} (logits {lg[gi]} / {lg[own]})"
-            ties += 1
+            if ok:
+                ties += 1
+            else:
+                bad.append(f"layer {l} row {b}: GPU experts {gi} vs oracle {own} "
+                           f"(logits {lg[gi]} / {lg[own]})")
     # weights: softmax over the chosen logits
-    for l in range(L):
-        for r, b in enumerate(rows):
-            assert np.allclose(g.weights[l, b], ref.weights[l, r], atol=2e-3), (l, b)
+    werr = max(float(np.max(np.abs(g.weights[l, b] - ref.weights[l, r])))
+               for l in range(L) for r, b in enumerate(rows))
     # logits
     errs = []
     agree = 0
@@ -155,4 +164,5 @@ def compare(inp: synth.StepInputs, g: GpuStep, rows=None) -> Report:
                 got = gv[l, b]
                 scale = max(1.0, np.max(np.abs(want)))
                 kerr = max(kerr, float(np.max(np.abs(got - want)) / scale))
-    return Report(float(max(errs)), np.array(errs), exact, ties, L * len(rows), agree, len(rows), kerr)
+    return Report(float(max(errs)), np.array(errs), exact, ties, L * len(rows), agree, len(rows), kerr,
+                  rerr, werr, bad)

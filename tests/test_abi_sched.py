@@ -97,7 +97,7 @@ def test_full_list_shape():
             counts[mk.OPS[int(d[mk.F_OP])]] = counts.get(mk.OPS[int(d[mk.F_OP])], 0) + 1
     sh = synth.MODELS["full"]
     assert counts["RESID_NORM"] == sh.n_layers + 1
-    assert counts["QKV_PROJ"] == sh.n_layers * 80  # "a real QKV at batch 1 is 80 tiles"
+    assert counts["QKV_PROJ"] == sh.n_layers * 160  # 32-row tiles (the pages quote 80 tiles of 64)
     assert counts["ROUTER_TOPK"] == sh.n_layers
     assert counts["MOE_UPGATE_ACT_DRAIN"] == counts["MOE_DOWN_DRAIN"] == sh.n_layers * NUM_SMS
     assert counts["ATTN_DRAIN"] > 0 and counts["ATTN_DECODE"] > 0 and counts["LM_HEAD"] > 0

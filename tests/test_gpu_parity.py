@@ -13,6 +13,12 @@ pytestmark = pytest.mark.gpu
 
 
 def check(rep, total_rows):
+    print(f"logit rel err {rep.max_rel_err:.3e}  router err max {rep.router_err.max():.3e} "
+          f"(per layer {np.array2string(rep.router_err, precision=1)})  weights {rep.weight_err:.2e}  "
+          f"routing exact {rep.exact_routing}/{rep.total_routing} ties {rep.tie_routing}  "
+          f"kv {rep.kv_max_err:.2e}")
+    assert not rep.routing_violations, rep.routing_violations
+    assert rep.weight_err <= 1e-4, rep.weight_err
     assert rep.max_rel_err <= parity.LOGIT_TOL, rep
     assert rep.greedy_agree == rep.greedy_total, rep
     assert rep.exact_routing + rep.tie_routing == rep.total_routing
