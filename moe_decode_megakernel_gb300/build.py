@@ -15,6 +15,20 @@ SOURCES = ["mk_api.cpp", "mk_sched.cpp", "mk_shape_tiny.cu", "mk_shape_small.cu"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
+def source_hash() -> str:
+    """sha256 over the kernel sources and the public header (identifies the
+    kernel a recorded profile was taken on)."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)) + ["../../include/mk.h"]:
+        path = os.path.join(CSRC, name)
+        if os.path.isfile(path):
+            h.update(name.encode())
+            with open(path, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
 def _nvcc() -> str:
     return os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 
