@@ -144,6 +144,30 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens,
                    int32_t max_pages, void* k_pool, void* v_pool, int64_t num_pages,
                    void* workspace, size_t workspace_bytes, float* logits, void* stream);
 
+/* mk_decode_step with a built-in workspace, for callers that cannot allocate
+ * device memory: their device memory belongs to another allocator (a host
+ * framework's caching allocator, a runtime whose budget is fixed at start-up)
+ * and they may not call cudaMalloc while running -- cudaMalloc can
+ * synchronise the device and can fail under a fixed budget.  The pages
+ * describe no such entry point; it has no counterpart there.
+ * Same arguments and behaviour as mk_decode_step, without the workspace
+ * pair.  The workspace is one 8 MiB device array inside the library: every
+ * GPU that loads the library holds it until the process exits.  Returns
+ * MK_ERR_ARG if the schedule needs more (mk_workspace_bytes(s) > 8 MiB).  It
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress), with that device current; make that first call
+ * before any stream capture.  All calls share the array and it keeps the
+ * last call's contents (each step zeroes its own counters first): calls
+ * whose executions overlap on the GPU, on any streams, race on it.
+ * Device-side failures (watchdog, page id out of range) are recorded in that
+ * array and cannot be read back through this entry point; where they matter,
+ * use mk_decode_step and mk_check_step. */
+int mk_decode_step_static_ws(mk_model* m, mk_sched* s, const int32_t* last_tokens,
+                             const int32_t* seq_lens, const int32_t* block_tables, int32_t batch,
+                             int32_t max_pages, void* k_pool, void* v_pool, int64_t num_pages,
+                             float* logits, void* stream);
+
 /* Waits for `stream`, then reads the step's device error record: MK_OK,
  * MK_ERR_TIMEOUT or MK_ERR_DEVICE (details in mk_last_error()). */
 int mk_check_step(const mk_sched* s, const void* workspace, void* stream);

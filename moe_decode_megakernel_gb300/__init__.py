@@ -77,6 +77,8 @@ def lib():
             "mk_decode_step": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, vp, vp, i64, vp, sz, vp,
                                               vp]),
             "mk_check_step": (ctypes.c_int, [vp, vp, vp]),
+            "mk_decode_step_static_ws": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, vp, vp, i64, vp,
+                                                        vp]),
             "mk_last_error": (ctypes.c_char_p, []),
             "mk_workspace_offset": (i64, [vp, ctypes.c_char_p]),
             "mk_sched_num_sms": (i32, [vp]),
@@ -211,6 +213,17 @@ def decode_step(model: Model, sched: Sched, last_tokens: int, seq_lens: int, blo
     _check(lib().mk_decode_step(model.handle, sched.handle, last_tokens, seq_lens, block_tables,
                                 batch, max_pages, k_pool, v_pool, num_pages, workspace,
                                 workspace_bytes, logits, stream))
+
+
+def decode_step_static_ws(model: Model, sched: Sched, last_tokens: int, seq_lens: int,
+                          block_tables: int, batch: int, max_pages: int, k_pool: int, v_pool: int,
+                          num_pages: int, logits: int, stream: int = 0) -> None:
+    """mk_decode_step_static_ws: the decode step on the library's built-in
+    8 MiB workspace, for callers that cannot allocate device memory (see
+    include/mk.h for its sharing rules)."""
+    _check(lib().mk_decode_step_static_ws(model.handle, sched.handle, last_tokens, seq_lens,
+                                          block_tables, batch, max_pages, k_pool, v_pool, num_pages,
+                                          logits, stream))
 
 
 def check_step(sched: Sched, workspace: int, stream: int = 0) -> None:
