@@ -104,6 +104,8 @@ typedef struct {
   int32_t trace_hidden;     /* 1: keep the residual entering every layer in the workspace */
   int32_t watchdog_ms;      /* device-side wait limit; 0 = 2000 ms */
   int32_t trace;            /* 1: record every work item's timestamps ("trace", "stats") */
+  int32_t moe_queue;        /* 0: separate up/gate and down drains; 1: one MoE queue with each
+                               expert's down tiles one expert behind its up/gate tiles */
 } mk_sched_opts;
 
 /* Fills opts with the defaults (all zero except fuse_* = 1). */
@@ -178,10 +180,10 @@ const char* mk_last_error(void);
 
 /* Byte offsets of named regions inside the workspace (-1 if absent):
  * "topk_ids" int32 [L][B][k], "topk_w" fp32 [L][B][k], "router_logits"
- * fp32 [L][B][E], "expert_count" int32 [L][E], "moe_queue" int32 [E] (last
- * layer's active experts, ascending: entry i of the up/gate queue is expert
- * list[i / up_tiles], tile i % up_tiles; likewise for the down queue),
- * "moe_queue_len" int32 [2] (up, down),
+ * fp32 [L][B][E], "expert_count" int32 [L][E], "moe_queue" int32 [E][4] (last
+ * layer's active experts, ascending: {expert, first expert-ordered row,
+ * rows, 0}; the MoE queues are (active expert, tile) in that order),
+ * "moe_queue_len" int32 [2] (active experts, routed rows),
  * "perm" int32 [B*k] (last layer), "hidden_trace" fp32 [L+1][B][H],
  * "error" uint32 [8], "barriers" uint32, with opts.trace "trace" uint64
  * [num_sms][cap][4] (popped, waits done, end in ns of %globaltimer; op |

@@ -187,7 +187,7 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   p.eoff = reinterpret_cast<int32_t*>(at("expert_offset"));
   p.perm = reinterpret_cast<int32_t*>(at("perm"));
   p.inv = reinterpret_cast<int32_t*>(at("inv"));
-  p.upq = reinterpret_cast<int32_t*>(at("moe_queue"));
+  p.act = reinterpret_cast<int32_t*>(at("moe_queue"));
   p.qlen = reinterpret_cast<int32_t*>(at("moe_queue_len"));
   p.xg = reinterpret_cast<float*>(at("xg"));
   p.u = reinterpret_cast<float*>(at("u"));

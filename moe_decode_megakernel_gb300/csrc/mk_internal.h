@@ -67,7 +67,8 @@ constexpr int32_t TGT_DYN_SPLITS = -2;
 // ROUTER_TOPK:  A0 b0, A1 b1, A2 1 = also finalize (single top-k task)
 // MOE_GATHER:   A0 row0, A1 n_rows
 // MOE_*_DRAIN:  A0 claim counter, A1 up barrier base (per expert), A2 explicit-gather barrier
-//               (or -1), A3 its target
+//               (or -1), A3 its target, A4 this claimer's index, A5 claimers, A6 queue mode
+//               (0 up and down tiles interleaved, 1 up tiles only)
 // MOE_COMBINE:  A0 b0, A1 b1
 // W_ATTN:       A0 b, A1 g, A2 t0, A3 t1, A4 first page, A5 partial slot
 // W_UP_TILE / W_DOWN_TILE: A0 expert, A1 tile index, A2 row0, A3 n_rows
@@ -168,8 +169,8 @@ struct Params {
   int32_t* eoff;        // [E + 1] row offset of each expert (current layer)
   int32_t* perm;        // [MB K] expert-ordered row -> b * K + j
   int32_t* inv;         // [MB K] b * K + j -> expert-ordered row
-  int32_t* upq;         // [E] active experts, ascending: the MoE queues' expert list
-  int32_t* qlen;        // [2] queue lengths (up, down)
+  int32_t* act;         // [E][4] active experts ascending: {expert, first row, rows, 0}
+  int32_t* qlen;        // [2] active experts, routed rows
   float* xg;            // [MB K][H] gathered rows (explicit gather)
   float* u;             // [MB K][I] SwiGLU activations
   float* y;             // [MB K][H] expert outputs

@@ -281,13 +281,19 @@ static __device__ __noinline__ void record_error(const Params& p, uint32_t code,
 static __device__ __forceinline__ bool aborted(const Ctx& c) { return c.hdr->abort != 0; }
 
 // Waits for an mbarrier phase; false if the CTA is aborting or the watchdog fired.
+// Waits inside the CTA get four times the limit of the cross-SM waits, so that
+// when a dependency never arrives, the wait on it is the one recorded.
 static __device__ __forceinline__ bool mbar_wait(const Params& p, Ctx& c, uint64_t* b, uint32_t parity) {
   if (mbar_try_wait(b, parity)) return true;
   const int64_t t0 = gtimer();
   for (;;) {
     if (mbar_try_wait(b, parity)) return true;
     if (aborted(c)) return false;
-    if (gtimer() - t0 > p.watchdog_ns) {
+    if (ld_volatile(p.err) != 0) {
+      c.hdr->abort = 1;
+      return false;
+    }
+    if (gtimer() - t0 > 4 * p.watchdog_ns) {
       record_error(p, ERR_TIMEOUT, c.sm, kNowhere, -1, 0, 0);
       c.hdr->abort = 1;
       return false;
@@ -539,7 +545,17 @@ struct Producer {
     return push(it);
   }
 
-  __device__ __forceinline__ bool moe_drain(const int32_t* d, bool up) {
+  // Claimer over the MoE tile queue ("Task scheduler": MOE_*_DRAIN claims the
+  // next tile until the queue is empty).  mode 0: one queue of up/gate and down
+  // tiles, each expert's down tiles one expert behind its up tiles --
+  //   up(0) | up(1) down(0) | up(2) down(1) | ... | up(n-1) down(n-2) | down(n-1)
+  // -- so a down tile rarely waits and no SM idles between the two phases;
+  // every unit depends only on units with smaller indices, so the claimers
+  // cannot deadlock.  mode 1: up/gate tiles only; mode 2: down tiles only.
+  // Claimer c takes unit c first without an atomic; later units come from
+  // the layer's claim counter, offset by the number of claimers, and each
+  // claim is issued before the current tile streams.
+  __device__ __forceinline__ bool moe_drain(const int32_t* d, int mode) {
     const int l = d[F_LAYER];
     // the routing decides which expert rows to stream: wait for the queue
     {
@@ -548,29 +564,47 @@ struct Producer {
       if (p.stats) c.stat[1] += gtimer() - t0;
       if (!ok) return false;
     }
-    constexpr int kUpTiles = S::mp.up_tiles, kDnTiles = S::mp.dn_tiles;
-    const int tiles = up ? kUpTiles : kDnTiles;
-    const int qlen = min(__ldcg(p.qlen + (up ? 0 : 1)), S::E * tiles);
-    uint32_t* claim = p.bars + d[F_A0];
     constexpr MoePlan mp = S::mp;
-    // the next claim is issued before the current tile streams, so the atomic's
-    // round trip overlaps the copies
-    uint32_t next = atomicAdd(claim, 1u);
-    ++c.stat[3];
-    for (;;) {
-      if (aborted(c)) return false;
-      const uint32_t i = next;
-      if (i >= (uint32_t)qlen) break;
-      next = atomicAdd(claim, 1u);
+    constexpr int U = mp.up_tiles, DN = mp.dn_tiles;
+    const int n_act = min(__ldcg(p.qlen), S::E);
+    const uint32_t total = (uint32_t)n_act * (mode == 0 ? U + DN : mode == 1 ? U : DN);
+    uint32_t* claim = p.bars + d[F_A0];
+    const uint32_t n_claimers = (uint32_t)d[F_A0 + 5];
+    uint32_t cur = (uint32_t)d[F_A0 + 4];
+    uint32_t nxt = 0;
+    if (cur < total) {
+      nxt = n_claimers + atomicAdd(claim, 1u);
       ++c.stat[3];
-      const int ai = (int)i / tiles, t = (int)i - ai * tiles;
-      const int e = __ldcg(p.upq + ai);
-      const int32_t ent = (e << 16) | t;
-      const bool e_ok = e >= 0 && e < S::E;
-      const int row0 = e_ok ? __ldcg(p.eoff + e) : -1;
-      const int nrows = e_ok ? __ldcg(p.ecount + l * S::E + e) : 0;
-      if (!e_ok || row0 < 0 || nrows < 1 || row0 + nrows > p.B * S::K) {
-        record_error(p, ERR_INDEX, c.sm, where_of(d), d[F_A0], (uint32_t)ent, (uint32_t)qlen);
+    }
+    int cached_a = -1;
+    int4 info = make_int4(0, 0, 0, 0);
+    while (cur < total) {
+      if (aborted(c)) return false;
+      bool up;
+      int a, t;
+      if (mode == 1) {
+        up = true; a = (int)cur / U; t = (int)cur - a * U;
+      } else if (mode == 2) {
+        up = false; a = (int)cur / DN; t = (int)cur - a * DN;
+      } else if ((int)cur < U) {
+        up = true; a = 0; t = (int)cur;
+      } else {
+        const int j = (int)cur - U, blk = j / (U + DN), r = j - blk * (U + DN);
+        if (blk < n_act - 1) {
+          up = r < U;
+          a = up ? blk + 1 : blk;
+          t = up ? r : r - U;
+        } else {
+          up = false; a = n_act - 1; t = r;
+        }
+      }
+      if (a != cached_a) {  // {expert, first row, rows} of active expert a
+        info = __ldcg(reinterpret_cast<const int4*>(p.act) + a);
+        cached_a = a;
+      }
+      const int e = info.x, row0 = info.y, nrows = info.z;
+      if (e < 0 || e >= S::E || row0 < 0 || nrows < 1 || row0 + nrows > p.B * S::K) {
+        record_error(p, ERR_INDEX, c.sm, where_of(d), d[F_A0], (uint32_t)cur, total);
         c.hdr->abort = 1;
         return false;
       }
@@ -591,7 +625,7 @@ struct Producer {
       } else {
         it[F_OP] = W_DOWN_TILE;
         it[F_WAIT0] = d[F_A0 + 1] + e;  // every up tile of expert e
-        it[F_TGT0] = mp.up_tiles;
+        it[F_TGT0] = U;
         it[F_SIG0] = -1;
         it[F_NSTAGE] = mp.dn_stages;
       }
@@ -612,6 +646,11 @@ struct Producer {
         }
       } else {
         if (!load_rows(p.wd + le * S::H * S::I, S::I, S::I, t * mp.dn_tile, mp.dn_tile, mp.dn_rows)) return false;
+      }
+      cur = nxt;
+      if (cur < total) {
+        nxt = n_claimers + atomicAdd(claim, 1u);
+        ++c.stat[3];
       }
     }
     return claim_end(d);
@@ -646,8 +685,8 @@ struct Producer {
         case OP_LM_HEAD: ok = dense(d); break;
         case OP_ATTN_DECODE: ok = attn_decode(d); break;
         case OP_ATTN_DRAIN: ok = attn_drain(d); break;
-        case OP_MOE_UPGATE_ACT_DRAIN: ok = moe_drain(d, true); break;
-        case OP_MOE_DOWN_DRAIN: ok = moe_drain(d, false); break;
+        case OP_MOE_UPGATE_ACT_DRAIN: ok = moe_drain(d, d[F_A0 + 6]); break;
+        case OP_MOE_DOWN_DRAIN: ok = moe_drain(d, 2); break;
         default: ok = passthrough(d); break;
       }
     }
@@ -1455,7 +1494,6 @@ struct Consumer {
   __device__ __forceinline__ void finalize(int l, bool load_ids) {
     if (cw != 0) return;
     constexpr int E = S::E, K = S::K, PL = (E + 31) / 32;
-    constexpr MoePlan mp = S::mp;
     const int B = p.B, n = B * K;
     if (load_ids) {  // a separate task: the routing comes from global memory
       for (int i = lane; i < n; i += 32) {
@@ -1505,15 +1543,15 @@ struct Consumer {
         sm.off[e] = ro;
         p.ecount[(int64_t)l * E + e] = cnt[k];
         p.eoff[e] = ro;
-        if (a[k]) p.upq[ao] = e;
+        if (a[k]) reinterpret_cast<int4*>(p.act)[ao] = make_int4(e, ro, cnt[k], 0);
       }
       ro += cnt[k];
       ao += a[k];
     }
     if (lane == 31) {
       p.eoff[E] = ri;
-      p.qlen[0] = ai * mp.up_tiles;
-      p.qlen[1] = ai * mp.dn_tiles;
+      p.qlen[0] = ai;  // active experts
+      p.qlen[1] = ri;  // routed rows
     }
     __syncwarp();
     for (int i = lane; i < n; i += 32) {

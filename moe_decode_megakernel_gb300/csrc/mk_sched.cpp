@@ -282,7 +282,12 @@ static int build(mk_sched* s) {
         w_acomb.push_back(d);
       }
 
+    // MoE claimers: separate up/gate and down drains as on the pages (default),
+    // or one queue of up/gate and down tiles with each expert's down tiles one
+    // expert behind its up tiles (moe_queue = 1, slower: a down tile claimed
+    // that early holds its SM's pipeline until the expert's up tiles land)
     std::vector<Desc> w_up, w_dn, w_mcomb;
+    const bool unified = o.moe_queue == 1;
     for (int i = 0; i < n_moe; ++i) {
       Desc d = blank(OP_MOE_UPGATE_ACT_DRAIN, l);
       B.wait(d, 0, lb.fin, 1);
@@ -290,15 +295,22 @@ static int build(mk_sched* s) {
       d[F_A0 + 1] = lb.up;
       d[F_A0 + 2] = o.explicit_gather ? lb.gather : -1;
       d[F_A0 + 3] = o.explicit_gather ? lb.n_gather : 0;
-      d[F_SIG0] = lb.upd;
+      d[F_A0 + 4] = i;
+      d[F_A0 + 5] = n_moe;
+      d[F_A0 + 6] = unified ? 0 : 1;
+      d[F_SIG0] = unified ? lb.dnd : lb.upd;
       w_up.push_back(d);
-      Desc e = blank(OP_MOE_DOWN_DRAIN, l);
-      B.wait(e, 0, lb.fin, 1);
-      e[F_A0] = lb.claim_dn;
-      e[F_A0 + 1] = lb.up;
-      e[F_A0 + 2] = mp.up_tiles;
-      e[F_SIG0] = lb.dnd;
-      w_dn.push_back(e);
+      if (!unified) {
+        Desc e = blank(OP_MOE_DOWN_DRAIN, l);
+        B.wait(e, 0, lb.fin, 1);
+        e[F_A0] = lb.claim_dn;
+        e[F_A0 + 1] = lb.up;
+        e[F_A0 + 2] = -1;
+        e[F_A0 + 4] = i;
+        e[F_A0 + 5] = n_moe;
+        e[F_SIG0] = lb.dnd;
+        w_dn.push_back(e);
+      }
     }
     lb.n_up_claim = lb.n_dn_claim = n_moe;
     if (!o.fuse_moe_combine) {
@@ -392,7 +404,7 @@ static void layout_workspace(mk_sched* s) {
   w.add("expert_offset", sizeof(int32_t) * (D.E + 1));
   w.add("perm", sizeof(int32_t) * MB * D.K);
   w.add("inv", sizeof(int32_t) * MB * D.K);
-  w.add("moe_queue", sizeof(int32_t) * (size_t)D.E);
+  w.add("moe_queue", sizeof(int32_t) * 4 * (size_t)D.E);
   w.add("moe_queue_len", sizeof(int32_t) * 2);
   w.add("xg", s->opts.explicit_gather ? sizeof(float) * MB * D.K * D.H : 16);
   w.add("u", sizeof(float) * MB * D.K * D.I);
@@ -446,6 +458,9 @@ static int validate(const mk_sched* s) {
     }
     if (add_wait(t, d[F_WAIT0], d[F_TGT0]) || add_wait(t, d[F_WAIT1], d[F_TGT1])) return MK_ERR_ARG;
     // claimers: the tiles they run feed and wait on per-expert / per-row barriers
+    // (a claimer of the combined queue both feeds and waits on the per-expert
+    // counters; its queue order keeps every wait on earlier units, so only the
+    // feeding edge enters the graph)
     if (op == OP_MOE_UPGATE_ACT_DRAIN)
       for (int e = 0; e < s->dims.E; ++e) producers[d[F_A0 + 1] + e].push_back(t);
     if (op == OP_MOE_DOWN_DRAIN)
@@ -524,7 +539,8 @@ struct Sim {
   std::vector<int> pos;            // next task per SM
   std::vector<int> pending;        // claimed entry index per SM (-1 none)
   std::vector<int32_t> attn_q;
-  std::vector<std::vector<int32_t>> up_q, dn_q;  // per layer
+  std::vector<std::vector<int32_t>> up_q, dn_q, uni_q;  // per layer
+  std::vector<int> first_done;  // per SM: the claimer's static first unit was taken
   std::vector<int8_t> fin_done;
   std::string err;
 
@@ -549,18 +565,30 @@ struct Sim {
     if (d[F_SIG1] >= 0) bars[d[F_SIG1]]++;
   }
 
+  // The layer's queues as the device derives them from the active-expert list:
+  // entries (is_up, expert) for the combined queue, the up queue, the down queue.
   void finalize(int l) {
     const ShapeDims& D = s->dims;
-    std::vector<int> count(D.E, 0);
+    const int U = s->plan.up_tiles, DN = s->plan.dn_tiles;
+    std::vector<int> count(D.E, 0), act;
     for (int b = 0; b < B; ++b)
       for (int j = 0; j < D.K; ++j) count[routing[((size_t)l * B + b) * D.K + j]]++;
+    for (int e = 0; e < D.E; ++e)
+      if (count[e]) act.push_back(e);
+    const int n = (int)act.size();
     up_q[l].clear();
     dn_q[l].clear();
-    for (int e = 0; e < D.E; ++e) {
-      if (!count[e]) continue;
-      for (int t = 0; t < s->plan.up_tiles; ++t) up_q[l].push_back((e << 16) | t);
-      for (int t = 0; t < s->plan.dn_tiles; ++t) dn_q[l].push_back((e << 16) | t);
+    uni_q[l].clear();
+    for (int a = 0; a < n; ++a) {
+      for (int t = 0; t < U; ++t) up_q[l].push_back(act[a]);
+      for (int t = 0; t < DN; ++t) dn_q[l].push_back(act[a]);
     }
+    for (int t = 0; t < U; ++t) uni_q[l].push_back(act[0] | (1 << 30));
+    for (int a = 1; a < n; ++a) {
+      for (int t = 0; t < U; ++t) uni_q[l].push_back(act[a] | (1 << 30));
+      for (int t = 0; t < DN; ++t) uni_q[l].push_back(act[a - 1]);
+    }
+    for (int t = 0; t < DN; ++t) uni_q[l].push_back(act[n - 1]);
     fin_done[l] = 1;
   }
 
@@ -604,23 +632,33 @@ struct Sim {
           err = "MoE claimer ran before its queue was built (layer " + std::to_string(l) + ")";
           return false;
         }
-        const bool up = op == OP_MOE_UPGATE_ACT_DRAIN;
-        auto& q = up ? up_q[l] : dn_q[l];
+        const int mode = op == OP_MOE_DOWN_DRAIN ? 2 : d[F_A0 + 6];
+        auto& q = mode == 0 ? uni_q[l] : mode == 1 ? up_q[l] : dn_q[l];
         const int claim = d[F_A0];
         if (pending[sm] < 0) {
-          const int64_t i = bars[claim]++;
+          // the first unit is the claimer's own index; later ones come from the counter
+          int64_t i;
+          if (!first_done[sm]) {
+            i = d[F_A0 + 4];
+            first_done[sm] = 1;
+          } else {
+            i = d[F_A0 + 5] + bars[claim]++;
+          }
           if (i >= (int64_t)q.size()) {
+            first_done[sm] = 0;
             signal(d);
             break;
           }
           pending[sm] = (int)i;
         }
-        const int e = q[pending[sm]] >> 16;
+        const int32_t u = q[pending[sm]];
+        const bool up = mode == 1 || (mode == 0 && (u & (1 << 30)));
+        const int e = u & 0xffff;
         if (up) {
           if (d[F_A0 + 2] >= 0 && bars[d[F_A0 + 2]] < d[F_A0 + 3]) return false;
           bars[d[F_A0 + 1] + e]++;
         } else {
-          if (bars[d[F_A0 + 1] + e] < d[F_A0 + 2]) return false;  // up tiles of e not done
+          if (bars[d[F_A0 + 1] + e] < s->plan.up_tiles) return false;  // up tiles of e not done
         }
         pending[sm] = -1;
         return true;
@@ -767,6 +805,8 @@ int mk_sched_simulate(const mk_sched* s, int32_t batch, const int32_t* seq_lens,
   build_attn_queue(s, batch, seq_lens, sim.attn_q);
   sim.up_q.assign(L, {});
   sim.dn_q.assign(L, {});
+  sim.uni_q.assign(L, {});
+  sim.first_done.assign(s->num_sms, 0);
   sim.fin_done.assign(L, 0);
   std::vector<int> order(s->num_sms);
   for (int i = 0; i < s->num_sms; ++i) order[i] = i;

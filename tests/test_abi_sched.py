@@ -72,7 +72,8 @@ def test_schedules_validate_and_simulate(workload, order):
 
 @pytest.mark.parametrize("opts", [dict(fuse_finalize=0), dict(fuse_moe_combine=0),
                                   dict(explicit_gather=1), dict(attn_split_pages=1, moe_claimers=5,
-                                                               attn_claimers=3)])
+                                                               attn_claimers=3),
+                                  dict(moe_queue=1), dict(moe_queue=1, moe_claimers=3)])
 def test_schedule_variants(opts):
     m, s, inp = sched_for("small", **opts)
     s.validate()
@@ -99,7 +100,11 @@ def test_full_list_shape():
     assert counts["RESID_NORM"] == sh.n_layers + 1
     assert counts["QKV_PROJ"] == sh.n_layers * 160  # 32-row tiles (the pages quote 80 tiles of 64)
     assert counts["ROUTER_TOPK"] == sh.n_layers
+    # one up/gate and one down claimer per SM per layer
     assert counts["MOE_UPGATE_ACT_DRAIN"] == counts["MOE_DOWN_DRAIN"] == sh.n_layers * NUM_SMS
+    m2, s2, _ = sched_for("full_bs1_8k", moe_queue=1)  # one combined queue
+    n_dn = sum(int(s2.get_task(k, i)[mk.F_OP] == 15) for k in range(s2.num_sms) for i in range(s2.num_tasks(k)))
+    assert n_dn == 0
     assert counts["ATTN_DRAIN"] > 0 and counts["ATTN_DECODE"] > 0 and counts["LM_HEAD"] > 0
 
 
