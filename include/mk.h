@@ -171,7 +171,10 @@ int mk_decode_step_static_ws(mk_model* m, mk_sched* s, const int32_t* last_token
                              float* logits, void* stream);
 
 /* Waits for `stream`, then reads the step's device error record: MK_OK,
- * MK_ERR_TIMEOUT or MK_ERR_DEVICE (details in mk_last_error()). */
+ * MK_ERR_TIMEOUT or MK_ERR_DEVICE (details in mk_last_error()).  A timeout
+ * names the first wait that gave up (SM, task, opcode, layer, barrier index,
+ * count seen, target): the stalled task itself, or a task downstream of it
+ * whose wait began earlier. */
 int mk_check_step(const mk_sched* s, const void* workspace, void* stream);
 
 const char* mk_last_error(void);

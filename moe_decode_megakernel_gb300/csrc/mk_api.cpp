@@ -54,6 +54,43 @@ int cuda_fail(cudaError_t e, const char* what) {
   return fail(MK_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// A KV pool [L][pages][n_kv][P][d] as the 2-D tensor [L*pages*n_kv*P][d]; one
+// TMA box is (P rows, 64 dims) = P x 128 bytes, swizzled in 128-byte rows so
+// the attention's ldmatrix reads hit distinct banks.
+int encode_pool(CUtensorMap* tm, void* pool, const mk_sched* s, int64_t num_pages) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const ShapeDims& D = s->dims;
+  const uint64_t rows = (uint64_t)s->cfg.n_layers * (uint64_t)num_pages * D.NKV * D.P;
+  if (rows >= (1ull << 31)) return fail(MK_ERR_ARG, "KV pool too large for 32-bit TMA row coordinates");
+  cuuint64_t dims[2] = {(cuuint64_t)D.D, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D.D * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)D.P};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pool, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+  return MK_OK;
+}
+
 }  // namespace
 }  // namespace mk
 
@@ -204,6 +241,20 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   p.watchdog_ns = s->watchdog_ns;
   (void)D;
 
+  if (s->tm_kpool != k_pool || s->tm_vpool != v_pool || s->tm_pages != num_pages) {
+    int rc = encode_pool(&s->tm_k, k_pool, s, num_pages);
+    if (rc == MK_OK) rc = encode_pool(&s->tm_v, v_pool, s, num_pages);
+    if (rc != MK_OK) {
+      s->tm_kpool = s->tm_vpool = nullptr;
+      return rc;
+    }
+    s->tm_kpool = k_pool;
+    s->tm_vpool = v_pool;
+    s->tm_pages = num_pages;
+  }
+  p.tm_k = s->tm_k;
+  p.tm_v = s->tm_v;
+
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // "Barriers": the counters are zeroed before each step (with the error record)
   const size_t zero_bytes = s->ws.off("error") + sizeof(uint32_t) * 8;
@@ -230,6 +281,7 @@ int mk_check_step(const mk_sched* s, const void* workspace, void* stream) {
                             std::to_string((int32_t)rec[5]) + ")";
   if (rec[0] == 1) return fail(MK_ERR_TIMEOUT, "device wait timed out" + where);
   if (rec[0] == 2) return fail(MK_ERR_DEVICE, "page id out of range" + where);
+  if (rec[0] == 4) return fail(MK_ERR_DEVICE, "shared memory base not 1024-byte aligned" + where);
   return fail(MK_ERR_DEVICE, "index out of range" + where);
 }
 

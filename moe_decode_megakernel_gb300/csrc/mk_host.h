@@ -67,6 +67,11 @@ struct mk_sched {
   std::vector<mk::LayerBars> lb;            // [L + 1]
   mk::WsLayout ws;
   std::vector<int32_t> upload;              // host image of the device task lists
+  // tensor maps of the last KV pools seen (re-encoded when the pools change)
+  const void* tm_kpool = nullptr;
+  const void* tm_vpool = nullptr;
+  int64_t tm_pages = 0;
+  CUtensorMap tm_k, tm_v;
   const void* sched_dev = nullptr;          // uploaded lists
   int64_t watchdog_ns = 0;
 };

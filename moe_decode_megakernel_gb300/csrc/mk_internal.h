@@ -3,6 +3,7 @@
 // kernel's parameter block.
 #pragma once
 
+#include <cuda.h>
 #include <stdint.h>
 
 namespace mk {
@@ -121,6 +122,9 @@ constexpr MoePlan moe_plan(ShapeDims s) {
 
 // ------------------------------------------------------ kernel parameters
 struct Params {
+  // the KV pools as 2-D tensors [L*pages*n_kv*P][d] for TMA tiles of
+  // (P rows, 64 dims) with the 128-byte swizzle
+  CUtensorMap tm_k, tm_v;
   // weights ([out][in] row-major BF16 unless noted)
   const uint16_t* emb;
   const uint16_t* wqkv;

@@ -35,7 +35,7 @@
 namespace mk {
 namespace dev {
 
-constexpr uint32_t ERR_TIMEOUT = 1, ERR_PAGE = 2, ERR_INDEX = 3;
+constexpr uint32_t ERR_TIMEOUT = 1, ERR_PAGE = 2, ERR_INDEX = 3, ERR_SMEM_ALIGN = 4;
 constexpr uint32_t FULL = 0xffffffffu;
 constexpr int kBarConsumers = 1;  // named barrier id of the consumer warps
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
@@ -96,6 +96,39 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
+// 2-D TMA tile load (coordinates: x = element along the inner dimension, y = row).
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* b, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(b)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+// D += A (16x16, row) * B (16x8, col): BF16 operands, fp32 accumulation.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -135,6 +168,13 @@ __device__ __forceinline__ uint16_t f_bf16(float f) {  // round to nearest even 
   if ((u & 0x7f800000u) == 0x7f800000u) return (uint16_t)((u >> 16) | ((u & 0xffffu) ? 0x40u : 0u));
   u += 0x7fffu + ((u >> 16) & 1u);
   return (uint16_t)(u >> 16);
+}
+// (a, b) as two BF16 pairs whose sum carries 16 mantissa bits: hi = bf16(x),
+// lo = bf16(x - hi).  Two MMAs on hi and lo give fp32-level products.
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const uint16_t ah = f_bf16(a), bh = f_bf16(b);
+  hi = (uint32_t)ah | ((uint32_t)bh << 16);
+  lo = (uint32_t)f_bf16(a - bf16_f(ah)) | ((uint32_t)f_bf16(b - bf16_f(bh)) << 16);
 }
 __device__ __forceinline__ float dot8(uint4 w, uint4 x, float acc) {
   acc = fmaf(bf16_lo(w.x), bf16_lo(x.x), acc);
@@ -215,9 +255,12 @@ template <class S>
 struct Scratch {
   float xs[kTB * S::H];                     // activation rows of one GEMV pass (tagged)
   float out[2][kTB * kMaxStageRows];        // dot products of one stage (double buffer)
-  float qs[S::G * S::D];                    // the KV group's queries (tagged), pre-scaled
-  float sc[S::P * S::G];                    // attention scores of one page [token][head]
-  float pr[S::P * S::G];                    // attention probabilities of one page [token][head]
+  alignas(16) uint16_t qh[8][S::D + 8];     // the KV group's queries (tagged), pre-scaled, as
+  alignas(16) uint16_t ql[8][S::D + 8];     // BF16 hi + lo; rows >= G zero, padded rows
+  float wred[kConsumerWarps][8];            // per-warp page maxima / sums per head
+  float wsum[kConsumerWarps][8];
+  alignas(16) uint16_t ph[8][S::P + 8];     // probabilities of one page, BF16 hi part [head][token]
+  alignas(16) uint16_t pl[8][S::P + 8];     // and lo part (rows padded: conflict-free)
   float am[S::G], al[S::G], aa[S::G];       // running max, sum, rescale per head
   float red[kConsumerWarps * 2];
   double rope_theta[S::D / 2];              // base^(-2i/D)
@@ -245,6 +288,7 @@ struct Shape {
   static_assert(D % 32 == 0 && 32 % G == 0 && (G * D) % 4 == 0, "attention lane maps");
   static_assert((G * D / 4) <= kConsumerThreads, "PV threads");
   static_assert(2 * P * D * 2 <= kStageBytes, "one KV page per stage");
+  static_assert(G <= 8 && D % 64 == 0 && P % 16 == 0 && P <= 64, "MMA attention shape");
   static_assert(E <= 256 && K <= 32, "routing scratch");
 };
 
@@ -435,8 +479,10 @@ struct Producer {
     return load_rows(base, ld, K, row0, rows, SR);
   }
 
+  // KV pages as TMA tiles of (P tokens, 64 dims), swizzled: the K page of group
+  // g at the stage's start, its V page after it
   __device__ __forceinline__ bool attn_pages(int l, int b, int g, int pf, int np) {
-    const int64_t page_elems = (int64_t)S::P * S::D;
+    constexpr int BOXES = S::D / 64, BOX_BYTES = S::P * 128;
     for (int k = 0; k < np; ++k) {
       int slot;
       if (!acquire_stage(slot)) return false;
@@ -449,10 +495,13 @@ struct Producer {
         record_error(p, ERR_PAGE, c.sm, kNowhere, lp, (uint32_t)page, (uint32_t)p.num_pages);
         mbar_arrive(&c.hdr->full[slot]);  // complete the stage without data
       } else {
-        const int64_t off = (((int64_t)l * p.num_pages + page) * S::NKV + g) * page_elems;
-        mbar_expect_tx(fb, (uint32_t)(2 * page_elems * 2));
-        bulk_g2s_hint(dst, p.kpool + off, (uint32_t)(page_elems * 2), fb, stream_policy);
-        bulk_g2s_hint(dst + page_elems * 2, p.vpool + off, (uint32_t)(page_elems * 2), fb, stream_policy);
+        const int row = (int)((((int64_t)l * p.num_pages + page) * S::NKV + g) * S::P);
+        mbar_expect_tx(fb, (uint32_t)(2 * BOXES * BOX_BYTES));
+#pragma unroll
+        for (int bx = 0; bx < BOXES; ++bx) {
+          tma_2d(dst + bx * BOX_BYTES, &p.tm_k, 64 * bx, row, fb, stream_policy);
+          tma_2d(dst + (BOXES + bx) * BOX_BYTES, &p.tm_v, 64 * bx, row, fb, stream_policy);
+        }
       }
       ++c.st;
     }
@@ -1136,49 +1185,62 @@ struct Consumer {
   }
 
   // --------------------------------------------------------- attention
+  // Byte address of (token t, 16-byte chunk c16 of the head dims) in a KV page
+  // stored as TMA tiles of (P tokens x 128 bytes) with the 128-byte swizzle.
+  static __device__ __forceinline__ uint32_t kv_addr(uint32_t base, int t, int c16) {
+    return base + (uint32_t)((c16 >> 3) * S::P * 128 + t * 128 + (((c16 & 7) ^ (t & 7)) << 4));
+  }
+
   // One KV slice of one (row b, KV group g): its G query heads against the
   // keys in [t0, t1), as an unnormalised partial (running max in the log2
   // domain, sum, weighted values) -- "Tasks": ATTN_DECODE on a partial slice.
+  // On tensor cores: per page, S = Q K^T with the heads as the MMA's rows
+  // (padded to 16) and the warp's 8 tokens as its columns, then O += P V with
+  // the warp's head dims as columns.  q and P enter as BF16 hi + lo pairs, so
+  // the products keep fp32-level accuracy; K and V are BF16 as stored.
   __device__ __forceinline__ void attn(const int32_t* w) {
-    constexpr int G = S::G, D = S::D, P = S::P, DPL = D / 32;
+    constexpr int G = S::G, D = S::D, P = S::P, KS = D / 16, NT = D / 64;
     const int l = w[F_LAYER], b = w[F_A0], g = w[F_A0 + 1], t0 = w[F_A0 + 2], t1 = w[F_A0 + 3];
     const int pf = w[F_A0 + 4], slot_idx = w[F_A0 + 5], np = w[F_NSTAGE];
     const int s = b < p.B ? __ldg(p.seq_lens + b) : 0;
     const int pos = s - 1;
-    // the group's queries, scaled by log2(e)/sqrt(D), kept while (layer, b, g) repeats
+    const int qg = lane >> 2, qc = lane & 3;  // MMA fragment coordinates
+    // the group's queries, scaled by log2(e)/sqrt(D), split into BF16 hi + lo,
+    // kept while (layer, b, g) repeats
     if (np > 0 && !(sm.qtag[0] == l && sm.qtag[1] == b && sm.qtag[2] == g)) {
       const float scale = 1.4426950408889634f / sqrtf((float)D);
-      const float4* src = reinterpret_cast<const float4*>(p.q + ((int64_t)b * S::NQ + g * G) * D);
-      for (int i = ct; i < G * D / 4; i += kConsumerThreads) {
-        float4 v = __ldcg(src + i);
-        v.x *= scale; v.y *= scale; v.z *= scale; v.w *= scale;
-        reinterpret_cast<float4*>(sm.qs)[i] = v;
+      const float2* src = reinterpret_cast<const float2*>(p.q + ((int64_t)b * S::NQ + g * G) * D);
+      for (int i = ct; i < 8 * D / 2; i += kConsumerThreads) {
+        const int h = i / (D / 2), d2 = i - h * (D / 2);
+        uint32_t hi = 0u, lo = 0u;
+        if (h < G) {
+          const float2 v = __ldcg(src + i);
+          split_bf16x2(v.x * scale, v.y * scale, hi, lo);
+        }
+        *reinterpret_cast<uint32_t*>(&sm.qh[h][2 * d2]) = hi;
+        *reinterpret_cast<uint32_t*>(&sm.ql[h][2 * d2]) = lo;
       }
       consumers_sync();
       if (ct == 0) {
         sm.qtag[0] = l; sm.qtag[1] = b; sm.qtag[2] = g;
       }
     }
-    float qr[G][DPL];
-    if (np > 0) {
+    // ldmatrix rows of the Q fragments: head lane & 7, 16-byte chunk by lane >> 3
+    const uint32_t qh_a = smem_u32(&sm.qh[lane & 7][8 * (lane >> 3)]);
+    const uint32_t ql_a = smem_u32(&sm.ql[lane & 7][8 * (lane >> 3)]);
+    float o[NT][4];  // this warp's NT tiles of 8 head dims
 #pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int i = 0; i < DPL; ++i) qr[h][i] = sm.qs[h * D + lane * DPL + i];
-    }
-    // PV thread map: head h = ct % G, dims [4 c4, 4 c4 + 4) with c4 = ct / G
-    const bool pv_thread = ct < G * D / 4;
-    const int ph = ct % G, pc = ct / G;
-    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     if (ct < G) {
       sm.am[ct] = -INFINITY;
       sm.al[ct] = 0.f;
     }
+    const bool qk_warp = cw * 8 < P;  // this warp's 8 tokens exist in a page
     for (int k = 0; k < np; ++k) {
       int slot;
       const bool ok = __all_sync(FULL, stage_wait(slot) && !aborted(c));
-      uint16_t* Kp = reinterpret_cast<uint16_t*>(c.stages + (size_t)slot * kStageBytes);
-      uint16_t* Vp = Kp + P * D;
+      uint8_t* page = c.stages + (size_t)slot * kStageBytes;
+      const uint32_t kb = smem_u32(page), vb = kb + (uint32_t)(NT * P * 128);
       const int page_t0 = (pf + k) * P;
       // the new token's K/V replace its slot: the pool page may predate the write
       if (pos >= page_t0 && pos < page_t0 + P && pos >= t0 && pos < t1) {
@@ -1186,76 +1248,93 @@ struct Consumer {
         if (ok && ct < 2 * D / 8) {
           const int which = ct / (D / 8), cc = ct % (D / 8);
           const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p.kvnew + (((int64_t)b * 2 + which) * S::NKV + g) * D) + cc);
-          reinterpret_cast<uint4*>((which ? Vp : Kp) + sl * D)[cc] = v;
+          const uint32_t a = kv_addr(which ? vb : kb, sl, cc);
+          *reinterpret_cast<uint4*>(page + (a - kb)) = v;
           fence_proxy_async_smem();
         }
         consumers_sync();
       }
-      // scores: warp per token, lane per DPL dims, transpose-reduced over heads
+      // S = Q K^T for this warp's 8 tokens
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (ok && qk_warp) {
+        const int tr = cw * 8 + (lane & 7);
+#pragma unroll
+        for (int ks = 0; ks < KS; ks += 2) {
+          uint32_t b0, b1, b2, b3, h0, h1, h2, h3, l0, l1, l2, l3;
+          ldsm_x4(kv_addr(kb, tr, 2 * ks + (lane >> 3)), b0, b1, b2, b3);
+          ldsm_x4(qh_a + ks * 32, h0, h1, h2, h3);
+          ldsm_x4(ql_a + ks * 32, l0, l1, l2, l3);
+          mma_bf16(sc, h0, 0u, h1, 0u, b0, b1);
+          mma_bf16(sc, l0, 0u, l1, 0u, b0, b1);
+          mma_bf16(sc, h2, 0u, h3, 0u, b2, b3);
+          mma_bf16(sc, l2, 0u, l3, 0u, b2, b3);
+        }
+      }
+      // this thread: head qg, tokens cw*8 + 2qc, +1
+      const int tk = page_t0 + cw * 8 + 2 * qc;
+      float s0 = (qk_warp && qg < G && tk >= t0 && tk < t1) ? sc[0] : -INFINITY;
+      float s1 = (qk_warp && qg < G && tk + 1 >= t0 && tk + 1 < t1) ? sc[1] : -INFINITY;
+      float mx = fmaxf(s0, s1);
+      mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
+      if (qc == 0) sm.wred[cw][qg] = mx;
+      consumers_sync();
+      float pm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kConsumerWarps; ++i) pm = fmaxf(pm, sm.wred[i][qg]);
+      const float m_old = sm.am[qg % G];
+      const float m_new = fmaxf(m_old, pm);
+      const float p0 = (s0 == -INFINITY || m_new == -INFINITY) ? 0.f : exp2f(s0 - m_new);
+      const float p1 = (s1 == -INFINITY || m_new == -INFINITY) ? 0.f : exp2f(s1 - m_new);
+      float sum = p0 + p1;
+      sum += __shfl_xor_sync(FULL, sum, 1);
+      sum += __shfl_xor_sync(FULL, sum, 2);
+      if (qc == 0) sm.wsum[cw][qg] = sum;
+      if (qk_warp) {
+        uint32_t hi, lo;
+        split_bf16x2(p0, p1, hi, lo);
+        *reinterpret_cast<uint32_t*>(&sm.ph[qg][cw * 8 + 2 * qc]) = hi;
+        *reinterpret_cast<uint32_t*>(&sm.pl[qg][cw * 8 + 2 * qc]) = lo;
+      }
+      const float alpha = (m_old == -INFINITY) ? 0.f : exp2f(m_old - m_new);
+      consumers_sync();
+      if (cw == 0 && qc == 0 && qg < G) {
+        float tot = 0.f;
+#pragma unroll
+        for (int i = 0; i < kConsumerWarps; ++i) tot += sm.wsum[i][qg];
+        sm.al[qg] = sm.al[qg] * alpha + tot;
+        sm.am[qg] = m_new;
+      }
+      // O += P V for this warp's head dims [8 NT cw, 8 NT (cw + 1))
       if (ok) {
-        for (int tt = cw; tt < P; tt += kConsumerWarps) {
-          const int tok = page_t0 + tt;
-          float part[G];
-          const uint16_t* kr = Kp + tt * D + lane * DPL;
-          float kv[DPL];
-          if (DPL == 4) {
-            const uint2 u = *reinterpret_cast<const uint2*>(kr);
-            kv[0] = bf16_lo(u.x); kv[1] = bf16_hi(u.x); kv[2] = bf16_lo(u.y); kv[3] = bf16_hi(u.y);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          o[n][0] *= alpha;
+          o[n][1] *= alpha;
+        }
+#pragma unroll
+        for (int kt = 0; kt < P / 16; ++kt) {
+          uint32_t ah0 = 0u, ah2 = 0u, al0 = 0u, al2 = 0u;
+          if (qg < G) {
+            ah0 = *reinterpret_cast<const uint32_t*>(&sm.ph[qg][kt * 16 + 2 * qc]);
+            ah2 = *reinterpret_cast<const uint32_t*>(&sm.ph[qg][kt * 16 + 8 + 2 * qc]);
+            al0 = *reinterpret_cast<const uint32_t*>(&sm.pl[qg][kt * 16 + 2 * qc]);
+            al2 = *reinterpret_cast<const uint32_t*>(&sm.pl[qg][kt * 16 + 8 + 2 * qc]);
+          }
+          const int tr = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+          if (NT == 2) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(kv_addr(vb, tr, 2 * cw + (lane >> 4)), b0, b1, b2, b3);
+            mma_bf16(o[0], ah0, 0u, ah2, 0u, b0, b1);
+            mma_bf16(o[0], al0, 0u, al2, 0u, b0, b1);
+            mma_bf16(o[1], ah0, 0u, ah2, 0u, b2, b3);
+            mma_bf16(o[1], al0, 0u, al2, 0u, b2, b3);
           } else {
-            const uint32_t u = *reinterpret_cast<const uint32_t*>(kr);
-            kv[0] = bf16_lo(u); kv[1] = bf16_hi(u);
+            uint32_t b0, b1;
+            ldsm_x2_t(kv_addr(vb, tr, cw), b0, b1);
+            mma_bf16(o[0], ah0, 0u, ah2, 0u, b0, b1);
+            mma_bf16(o[0], al0, 0u, al2, 0u, b0, b1);
           }
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float a = 0.f;
-#pragma unroll
-            for (int i = 0; i < DPL; ++i) a = fmaf(qr[h][i], kv[i], a);
-            part[h] = a;
-          }
-          const float sc = reduce_scatter<G>(part, lane);
-          if ((lane & (32 / G - 1)) == 0) {
-            const int h = lane / (32 / G);
-            sm.sc[tt * G + h] = (tok >= t0 && tok < t1) ? sc : -INFINITY;
-          }
-        }
-      }
-      consumers_sync();
-      // online softmax update: warp h owns head h
-      if (ok && cw < G) {
-        const int h = cw;
-        float mx = -INFINITY;
-        for (int tt = lane; tt < P; tt += 32) mx = fmaxf(mx, sm.sc[tt * G + h]);
-        mx = warp_max(mx);
-        const float m_old = sm.am[h];
-        const float m_new = fmaxf(m_old, mx);
-        float sum = 0.f;
-        for (int tt = lane; tt < P; tt += 32) {
-          const float sv = sm.sc[tt * G + h];
-          const float pv = (m_new == -INFINITY || sv == -INFINITY) ? 0.f : exp2f(sv - m_new);
-          sm.pr[tt * G + h] = pv;
-          sum += pv;
-        }
-        sum = warp_sum(sum);
-        if (lane == 0) {
-          const float alpha = (m_old == -INFINITY) ? 0.f : exp2f(m_old - m_new);
-          sm.aa[h] = alpha;
-          sm.al[h] = sm.al[h] * alpha + sum;
-          sm.am[h] = m_new;
-        }
-      }
-      consumers_sync();
-      if (ok && pv_thread) {
-        const float alpha = sm.aa[ph];
-        o[0] *= alpha; o[1] *= alpha; o[2] *= alpha; o[3] *= alpha;
-        const uint16_t* vc = Vp + pc * 4;
-#pragma unroll 8
-        for (int tt = 0; tt < P; ++tt) {
-          const float pv = sm.pr[tt * G + ph];
-          const uint2 u = *reinterpret_cast<const uint2*>(vc + tt * D);
-          o[0] = fmaf(pv, bf16_lo(u.x), o[0]);
-          o[1] = fmaf(pv, bf16_hi(u.x), o[1]);
-          o[2] = fmaf(pv, bf16_lo(u.y), o[2]);
-          o[3] = fmaf(pv, bf16_hi(u.y), o[3]);
         }
       }
       stage_release(slot);
@@ -1263,8 +1342,13 @@ struct Consumer {
     consumers_sync();
     if (aborted(c)) return;
     const int64_t base = ((int64_t)b * S::NKV + g) * p.max_slots + slot_idx;
-    if (pv_thread)
-      *reinterpret_cast<float4*>(p.part_o + (base * G + ph) * D + 4 * pc) = make_float4(o[0], o[1], o[2], o[3]);
+    if (qg < G) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        const int dcol = (NT * cw + n) * 8 + 2 * qc;
+        *reinterpret_cast<float2*>(p.part_o + (base * G + qg) * D + dcol) = make_float2(o[n][0], o[n][1]);
+      }
+    }
     if (ct < G) {
       p.part_ml[(base * G + ct) * 2 + 0] = np > 0 ? sm.am[ct] : -INFINITY;
       p.part_ml[(base * G + ct) * 2 + 1] = np > 0 ? sm.al[ct] : 0.f;
@@ -1730,6 +1814,13 @@ static __device__ void storer(const Params& p, Ctx& c) {
 template <class S>
 __global__ void __launch_bounds__(kThreads, 1) mk_persistent(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  // the 128-byte TMA swizzle of the KV pages is laid out from a 1024-byte
+  // aligned stage base
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) record_error(p, ERR_SMEM_ALIGN, (int)blockIdx.x, kNowhere, -1, smem_u32(smem), 1024u);
+    return;
+  }
+  static_assert(sizeof(Hdr) % 16 == 0 && alignof(Scratch<S>) <= 16, "scratch alignment");
   Hdr* hdr = reinterpret_cast<Hdr*>(smem + (size_t)kStages * kStageBytes);
   Scratch<S>* scr = reinterpret_cast<Scratch<S>*>(smem + (size_t)kStages * kStageBytes + sizeof(Hdr));
   if (threadIdx.x == 0) {
