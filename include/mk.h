@@ -174,7 +174,10 @@ int mk_decode_step_static_ws(mk_model* m, mk_sched* s, const int32_t* last_token
  * MK_ERR_TIMEOUT or MK_ERR_DEVICE (details in mk_last_error()).  A timeout
  * names the first wait that gave up (SM, task, opcode, layer, barrier index,
  * count seen, target): the stalled task itself, or a task downstream of it
- * whose wait began earlier. */
+ * whose wait began earlier.  The message then adds a diagnosis from the
+ * barrier counts against the schedule: the task whose wait target exceeds
+ * the number of tasks that signal its barrier (the root of the stall), or
+ * else the barriers still short of their signallers. */
 int mk_check_step(const mk_sched* s, const void* workspace, void* stream);
 
 const char* mk_last_error(void);

@@ -2,8 +2,10 @@
 // step launch and its error check.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <string>
+#include <vector>
 
 #include "mk_host.h"
 
@@ -91,6 +93,61 @@ int encode_pool(CUtensorMap* tm, void* pool, const mk_sched* s, int64_t num_page
   return MK_OK;
 }
 
+// After a timeout: the counters as the step left them, against the schedule.
+// A wait whose target exceeds the number of tasks that signal its barrier can
+// never be met; that task is the root of the stall, and every other timed-out
+// wait depends on it.  Otherwise the barriers still short of their signallers
+// are listed.
+std::string stall_diagnosis(const mk_sched* s, const void* workspace, cudaStream_t st) {
+  const size_t nb = s->bar_kind.size();
+  std::vector<uint32_t> cnt(nb);
+  if (cudaMemcpyAsync(cnt.data(), static_cast<const uint8_t*>(workspace) + s->ws.off("barriers"),
+                      sizeof(uint32_t) * nb, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return "";
+  std::vector<int64_t> sig(nb, 0);
+  for (const Desc& d : s->tasks)
+    for (int f : {F_SIG0, F_SIG1})
+      if (d[f] >= 0 && (size_t)d[f] < nb) ++sig[d[f]];
+  for (int sm = 0; sm < s->num_sms; ++sm)
+    for (int ti : s->per_sm[sm]) {
+      const Desc& d = s->tasks[ti];
+      for (int k = 0; k < 2; ++k) {
+        const int b = d[k == 0 ? F_WAIT0 : F_WAIT1], tgt = d[k == 0 ? F_TGT0 : F_TGT1];
+        if (b < 0 || (size_t)b >= nb || s->bar_kind[b] != BK_STATIC || tgt <= sig[b]) continue;
+        return "; root: task " + std::to_string(d[F_TASK]) + " (sm " + std::to_string(sm) + ", op " +
+               std::to_string(d[F_OP]) + ", layer " + std::to_string(d[F_LAYER]) + ") waits for " +
+               std::to_string(tgt) + " signals on barrier " + std::to_string(b) + ", which " +
+               std::to_string(sig[b]) + " tasks signal (count " + std::to_string(cnt[b]) + ")";
+      }
+    }
+  // the SMs whose consumers stopped in the earliest layer: where the stall is
+  std::string lag;
+  std::vector<uint32_t> pr(8 * (size_t)s->num_sms);
+  if (cudaMemcpyAsync(pr.data(), static_cast<const uint8_t*>(workspace) + s->ws.off("progress"),
+                      sizeof(uint32_t) * pr.size(), cudaMemcpyDeviceToHost, st) == cudaSuccess &&
+      cudaStreamSynchronize(st) == cudaSuccess) {
+    std::vector<std::pair<uint32_t, int>> order;
+    for (int sm = 0; sm < s->num_sms; ++sm)
+      if (pr[8 * sm + 3] < s->per_sm[sm].size()) order.push_back({(pr[8 * sm + 1] >> 8) & 0xff, sm});
+    std::sort(order.begin(), order.end());
+    for (size_t k = 0; k < order.size() && k < 3; ++k) {
+      const uint32_t* r = &pr[8 * order[k].second];
+      lag += "; sm " + std::to_string(order[k].second) + ": consumer item " + std::to_string(r[0]) + " (op " +
+             std::to_string(r[1] & 0xff) + ", layer " + std::to_string((r[1] >> 8) & 0xff) + ", task " +
+             std::to_string(r[1] >> 16) + ", stages " + std::to_string(r[2]) + "), producer task " +
+             std::to_string(r[3]) + " of " + std::to_string(s->per_sm[order[k].second].size()) + " (stages " +
+             std::to_string(r[4]) + ", items " + std::to_string(r[5]) + "), storer " + std::to_string(r[6]);
+    }
+  }
+  std::string short_bars;
+  int n = 0;
+  for (size_t b = 0; b < nb; ++b)
+    if (s->bar_kind[b] == BK_STATIC && cnt[b] < sig[b] && n++ < 4)
+      short_bars += " " + std::to_string(b) + " (" + std::to_string(cnt[b]) + " of " + std::to_string(sig[b]) + ")";
+  return (n ? "; barriers short of their signallers:" + short_bars + (n > 4 ? " ..." : "") : std::string()) + lag;
+}
+
 }  // namespace
 }  // namespace mk
 
@@ -141,8 +198,10 @@ int mk_sched_upload(mk_sched* s, void* dev, size_t bytes, void* stream) {
   for (int sm = 0; sm < nsm; ++sm) {
     s->upload[2 * sm] = (int32_t)off;
     s->upload[2 * sm + 1] = (int32_t)s->per_sm[sm].size();
+    int pos = 0;
     for (int t : s->per_sm[sm]) {
       std::memcpy(&s->upload[off], s->tasks[t].data(), sizeof(int32_t) * 32);
+      s->upload[off + F_POS] = pos++;
       off += 32;
     }
   }
@@ -207,6 +266,7 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   p.sched = static_cast<const int32_t*>(s->sched_dev);
   p.bars = reinterpret_cast<uint32_t*>(at("barriers"));
   p.err = reinterpret_cast<uint32_t*>(at("error"));
+  p.prog = reinterpret_cast<uint32_t*>(at("progress"));
   p.seq_lens = seq_lens;
   p.max_ctx = s->max_ctx;
   p.h = reinterpret_cast<float*>(at("h"));
@@ -257,7 +317,7 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // "Barriers": the counters are zeroed before each step (with the error record)
-  const size_t zero_bytes = s->ws.off("error") + sizeof(uint32_t) * 8;
+  const size_t zero_bytes = s->ws.off("progress") + sizeof(uint32_t) * 8 * (size_t)s->num_sms;
   cudaError_t e = cudaMemsetAsync(workspace, 0, zero_bytes, st);
   if (e != cudaSuccess) return cuda_fail(e, "barrier reset");
   const int rc = kShapes[m->shape_id].launch(p, s->num_sms, st);
@@ -279,9 +339,11 @@ int mk_check_step(const mk_sched* s, const void* workspace, void* stream) {
                             std::to_string((int32_t)rec[7]) + ", index " + std::to_string((int32_t)rec[3]) +
                             ", value " + std::to_string((int32_t)rec[4]) + ", limit " +
                             std::to_string((int32_t)rec[5]) + ")";
-  if (rec[0] == 1) return fail(MK_ERR_TIMEOUT, "device wait timed out" + where);
+  if (rec[0] == 1) return fail(MK_ERR_TIMEOUT, "device wait timed out" + where + stall_diagnosis(s, workspace, st));
   if (rec[0] == 2) return fail(MK_ERR_DEVICE, "page id out of range" + where);
   if (rec[0] == 4) return fail(MK_ERR_DEVICE, "shared memory base not 1024-byte aligned" + where);
+  if (rec[0] == 5)
+    return fail(MK_ERR_DEVICE, "descriptor or work ring out of step (a stale entry was read)" + where);
   return fail(MK_ERR_DEVICE, "index out of range" + where);
 }
 

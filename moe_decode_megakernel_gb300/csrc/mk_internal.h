@@ -54,6 +54,8 @@ enum Field : int {
   F_A0 = 8,     // op-specific arguments F_A0 .. F_A0 + 15
   F_TASK = 24,  // global index of the task (error reports, tracing)
   F_NSTAGE = 25,  // work items: shared-memory stages that belong to the item
+  F_POS = 26,   // descriptors as uploaded: position in the SM's list (ring check)
+  F_SEQ = 27,   // work items: sequence number on the SM's work ring (ring check)
   F_DESC_INTS = 32,
 };
 constexpr int32_t TGT_DYN_SPLITS = -2;
@@ -156,6 +158,7 @@ struct Params {
   // workspace regions
   uint32_t* bars;
   uint32_t* err;        // [8]: code, sm, task, barrier, observed, target, op, layer
+  uint32_t* prog;       // [num_sms][8]: where each role of each SM is (read after a failed step)
   const int32_t* seq_lens;  // [B] device, length including the decoded token
   int max_ctx;
   float* h;             // [MB][H] residual stream

@@ -35,7 +35,7 @@
 namespace mk {
 namespace dev {
 
-constexpr uint32_t ERR_TIMEOUT = 1, ERR_PAGE = 2, ERR_INDEX = 3, ERR_SMEM_ALIGN = 4;
+constexpr uint32_t ERR_TIMEOUT = 1, ERR_PAGE = 2, ERR_INDEX = 3, ERR_SMEM_ALIGN = 4, ERR_RING = 5;
 constexpr uint32_t FULL = 0xffffffffu;
 constexpr int kBarConsumers = 1;  // named barrier id of the consumer warps
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
@@ -95,6 +95,11 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
 }
 // 2-D TMA tile load (coordinates: x = element along the inner dimension, y = row).
 __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* b, uint64_t policy) {
@@ -387,6 +392,7 @@ static __device__ void controller(const Params& p, Ctx& c) {
     if (i >= kDescRing && !mbar_wait(p, c, &H->dempty[slot], ((i / kDescRing) - 1) & 1)) break;
     mbar_expect_tx(&H->dfull[slot], 128);
     bulk_g2s(H->desc[slot], p.sched + off + 32 * i, 128, &H->dfull[slot]);
+    p.prog[c.sm * 8 + 7] = (uint32_t)(i + 1);
   }
   if (i < n) {  // aborted: let the copies already issued land before returning
     for (int j = (i > kDescRing ? i - kDescRing : 0); j < i; ++j) {
@@ -430,8 +436,11 @@ struct Producer {
     }
     int32_t* dst = c.hdr->work[slot];
     for (int i = 0; i < 32; ++i) dst[i] = item[i];
+    dst[F_SEQ] = (int32_t)c.wk;
     mbar_arrive(&c.hdr->wfull[slot]);
     ++c.wk;
+    p.prog[c.sm * 8 + 4] = c.st;
+    p.prog[c.sm * 8 + 5] = c.wk;
     return true;
   }
 
@@ -726,7 +735,17 @@ struct Producer {
       }
       int32_t d[32];
       for (int k = 0; k < 32; ++k) d[k] = H->desc[slot][k];
+      // the controller's next TMA copy overwrites this slot: order the reads
+      // (generic proxy) before it (async proxy)
+      fence_proxy_async_smem();
       mbar_arrive(&H->dempty[slot]);
+      p.prog[c.sm * 8 + 3] = (uint32_t)(i + 1);
+      if (d[F_POS] != i) {
+        record_error(p, ERR_RING, c.sm, where_of(d), i, (uint32_t)d[F_POS], (uint32_t)n);
+        H->abort = 1;
+        ok = false;
+        break;
+      }
       switch (d[F_OP]) {
         case OP_QKV_PROJ:
         case OP_O_PROJ:
@@ -777,7 +796,11 @@ struct Consumer {
     if (p.stats && ct == 0) c.stat[1] += gtimer() - t0;
     return ok;
   }
+  // The stage goes back to the producer, whose next TMA copy overwrites it:
+  // the reads of this warp (generic proxy) are ordered before that write
+  // (async proxy) by a cross-proxy fence ahead of the release.
   __device__ __forceinline__ void stage_release(int slot) {
+    fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&c.hdr->empty[slot]);
     ++c.st;
@@ -835,33 +858,29 @@ struct Consumer {
     float4* xs4 = reinterpret_cast<float4*>(sm.xs);
     for (int i = ct; i < tb * C; i += kConsumerThreads) {
       const int t = i / C, cc = i - t * C;
-      const int tok = kTB * chunk + t;
-      const float* src;
-      switch (op) {
-        case OP_O_PROJ:
-          src = p.attn_out + (int64_t)tok * S::NQ * S::D + (int64_t)w[F_A0 + 2] * S::G * S::D;
-          break;
-        case W_UP_TILE: {
-          const int row = w[F_A0 + 2] + tok;
-          if (p.explicit_gather) {
-            src = p.xg + (int64_t)row * S::H;
-          } else {
-            int pr = __ldcg(p.perm + row);
-            int b = pr / S::K;
-            if (pr < 0 || b >= p.B) b = 0;  // only after a failed step
-            src = p.x + (int64_t)b * S::H;
-          }
-          break;
-        }
-        case W_DOWN_TILE:
-          src = p.u + (int64_t)(w[F_A0 + 2] + tok) * S::I;
-          break;
-        default:
-          src = p.x + (int64_t)tok * S::H;
-          break;
-      }
+      const float* src = x_src(op, w, kTB * chunk + t);
       // source float4 cc = elements [4cc, 4cc+4): chunk cc/2, half cc%2
       xs4[t * C + (cc & 1) * (C / 2) + (cc >> 1)] = __ldcg(reinterpret_cast<const float4*>(src) + cc);
+    }
+  }
+
+  // the activation row `tok` of an item's input
+  __device__ __forceinline__ const float* x_src(int op, const int32_t* w, int tok) {
+    switch (op) {
+      case OP_O_PROJ:
+        return p.attn_out + (int64_t)tok * S::NQ * S::D + (int64_t)w[F_A0 + 2] * S::G * S::D;
+      case W_UP_TILE: {
+        const int row = w[F_A0 + 2] + tok;
+        if (p.explicit_gather) return p.xg + (int64_t)row * S::H;
+        const int pr = __ldcg(p.perm + row);
+        int b = pr / S::K;
+        if (pr < 0 || b >= p.B) b = 0;  // only after a failed step
+        return p.x + (int64_t)b * S::H;
+      }
+      case W_DOWN_TILE:
+        return p.u + (int64_t)(w[F_A0 + 2] + tok) * S::I;
+      default:
+        return p.x + (int64_t)tok * S::H;
     }
   }
 
@@ -1016,8 +1035,8 @@ struct Consumer {
 
   // Pair epilogue, run by lane t for activation row t: v0, v1 are the dot
   // products of the pair's two weight rows r0, r1 (rows of stage s).
-  __device__ __forceinline__ void pair_epilogue(int op, const int32_t* w, int s, int r0, int r1, int t, float v0,
-                                                float v1, int dslot, float dwt) {
+  __device__ __noinline__ void pair_epilogue(int op, const int32_t* w, int s, int r0, int r1, int t, float v0,
+                                                float v1, int dslot, float dwt, int pos, int page) {
     const int l = w[F_LAYER];
     switch (op) {
       case OP_QKV_PROJ: {
@@ -1026,7 +1045,6 @@ struct Consumer {
         const int row = w[F_A0] + s * S::SR_H + r0;  // even: (row, row + 1) is a rotation pair
         const int b = t;
         const int head = row / S::D, dd = row - head * S::D;
-        const int pos = __ldg(p.seq_lens + b) - 1;
         if (head < S::NQ + S::NKV) {
           // the angle pos * base^(-dd/D), reduced modulo 2 pi in double; sin/cos in float
           const double ang = (double)pos * sm.rope_theta[dd / 2];
@@ -1044,10 +1062,8 @@ struct Consumer {
           const int g = head - S::NQ - (is_v ? S::NKV : 0);
           const uint32_t packed = (uint32_t)f_bf16(v0) | ((uint32_t)f_bf16(v1) << 16);
           *reinterpret_cast<uint32_t*>(p.kvnew + (((int64_t)b * 2 + (is_v ? 1 : 0)) * S::NKV + g) * S::D + dd) = packed;
-          const int lp = pos / S::P;
-          const int page = lp < p.max_pages ? __ldg(p.block_tables + (int64_t)b * p.max_pages + lp) : -1;
           if (page < 0 || page >= p.num_pages) {
-            record_error(p, ERR_PAGE, c.sm, where_of(w), lp, (uint32_t)page, (uint32_t)p.num_pages);
+            record_error(p, ERR_PAGE, c.sm, where_of(w), pos / S::P, (uint32_t)page, (uint32_t)p.num_pages);
           } else {
             uint16_t* pool = is_v ? p.vpool : p.kpool;
             const int64_t o = ((((int64_t)l * p.num_pages + page) * S::NKV + g) * S::P + pos % S::P) * S::D + dd;
@@ -1101,6 +1117,20 @@ struct Consumer {
     const int op = w[F_OP];
     const int nst = w[F_NSTAGE];
     const int tb = ntok;
+    // epilogue inputs of lane t (activation row t), loaded before the stages
+    int dslot = 0, pos = -1, page = -1;
+    float dwt = 0.f;
+    if (lane < tb) {
+      if (op == W_DOWN_TILE) {
+        dslot = __ldcg(p.perm + w[F_A0 + 2] + lane);
+        if (dslot < 0 || dslot >= p.B * S::K) dslot = 0;  // only after a failed step
+        dwt = __ldcg(p.topk_w + (int64_t)w[F_LAYER] * p.MB * S::K + dslot);
+      } else if (op == OP_QKV_PROJ) {
+        pos = __ldg(p.seq_lens + lane) - 1;
+        const int lp = pos / S::P;
+        if (pos >= 0 && lp < p.max_pages) page = __ldg(p.block_tables + (int64_t)lane * p.max_pages + lp);
+      }
+    }
     int32_t tag[4];
     x_tag(op, w, 0, tag);
     if (!(tag[0] == sm.xtag[0] && tag[1] == sm.xtag[1] && tag[2] == sm.xtag[2] && tag[3] == sm.xtag[3])) {
@@ -1112,40 +1142,36 @@ struct Consumer {
     }
     const int team = cw >> 2, tw = cw & 3;
     const bool up_pairs = op == W_UP_TILE;
-    // down tiles: lane t's output slot (row b, slot j) and router weight, loaded up front
-    int dslot = 0;
-    float dwt = 0.f;
-    if (op == W_DOWN_TILE && lane < tb) {
-      dslot = __ldcg(p.perm + w[F_A0 + 2] + lane);
-      if (dslot < 0 || dslot >= p.B * S::K) dslot = 0;  // only after a failed step
-      dwt = __ldcg(p.topk_w + (int64_t)w[F_LAYER] * p.MB * S::K + dslot);
-    }
-    const float4* xs4 = reinterpret_cast<const float4*>(sm.xs);
+    const uint32_t xs_a = smem_u32(sm.xs) + (uint32_t)lane * 16u;
     for (int s = team; s < nst; s += 2) {
       const uint32_t gs = c.st + (uint32_t)s;
       const int slot = gs % kStages;
       const bool ok = __all_sync(FULL, mbar_wait(p, c, &c.hdr->full[slot], (gs / kStages) & 1) && !aborted(c));
       const int rows = min(SR, total_rows - s * SR);
       const int npairs = rows / 2;
-      const uint16_t* W = reinterpret_cast<const uint16_t*>(c.stages + (size_t)slot * kStageBytes);
+      const uint32_t st_a = smem_u32(stage(slot)) + (uint32_t)lane * 16u;
       if (ok) {
         for (int pr = tw; pr < npairs; pr += 4) {
           const int r0 = up_pairs ? pr : 2 * pr;
           const int r1 = up_pairs ? pr + npairs : 2 * pr + 1;
-          const uint4* w0 = reinterpret_cast<const uint4*>(W + (size_t)r0 * K);
-          const uint4* w1 = reinterpret_cast<const uint4*>(W + (size_t)r1 * K);
+          const uint32_t w0 = st_a + (uint32_t)(r0 * K * 2), w1 = st_a + (uint32_t)(r1 * K * 2);
           float a0[kTB], a1[kTB], b0[kTB], b1[kTB];
 #pragma unroll
           for (int t = 0; t < kTB; ++t) a0[t] = a1[t] = b0[t] = b1[t] = 0.f;
 #pragma unroll
           for (int j = 0; j < CPL; ++j) {
-            const int cc = lane + 32 * j;
-            if (C % 32 == 0 || cc < C) {
-              const uint4 u0 = w0[cc], u1 = w1[cc];
+            if (C % 32 == 0 || lane + 32 * j < C) {
+              const uint4 u0 = lds128(w0 + j * 512), u1 = lds128(w1 + j * 512);
 #pragma unroll
               for (int t = 0; t < kTB; ++t)
                 if (t < tb) {
-                  const float4 xa = xs4[t * 2 * C + cc], xb = xs4[t * 2 * C + C + cc];
+                  // x row t as [half][chunk][4]: chunk c's elements 0..3 and 4..7
+                  const uint4 xa4 = lds128(xs_a + (uint32_t)((t * 2 * C + 32 * j) * 16));
+                  const uint4 xb4 = lds128(xs_a + (uint32_t)((t * 2 * C + C + 32 * j) * 16));
+                  const float4 xa = make_float4(__uint_as_float(xa4.x), __uint_as_float(xa4.y),
+                                                __uint_as_float(xa4.z), __uint_as_float(xa4.w));
+                  const float4 xb = make_float4(__uint_as_float(xb4.x), __uint_as_float(xb4.y),
+                                                __uint_as_float(xb4.z), __uint_as_float(xb4.w));
                   a0[t] = fmaf(bf16_lo(u0.x), xa.x, a0[t]);
                   a1[t] = fmaf(bf16_hi(u0.x), xa.y, a1[t]);
                   b0[t] = fmaf(bf16_lo(u1.x), xa.x, b0[t]);
@@ -1172,12 +1198,15 @@ struct Consumer {
               v0[t] = warp_sum(a0[t] + a1[t]);
               v1[t] = warp_sum(b0[t] + b1[t]);
             }
-#pragma unroll
-          for (int t = 0; t < kTB; ++t)
-            if (t < tb && lane == t && !aborted(c)) pair_epilogue(op, w, s, r0, r1, t, v0[t], v1[t], dslot, dwt);
+          // lane t finishes the pair for activation row t
+          const float e0 = (kTB > 1 && lane == 1) ? v0[kTB - 1] : v0[0];
+          const float e1 = (kTB > 1 && lane == 1) ? v1[kTB - 1] : v1[0];
+          if (lane < tb && !aborted(c)) pair_epilogue(op, w, s, r0, r1, lane, e0, e1, dslot, dwt, pos, page);
         }
       }
-      // the four warps of the team stand for the eight arrivals the stage expects
+      // the four warps of the team stand for the eight arrivals the stage
+      // expects; the fence orders the reads before the producer's next copy
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive_n(&c.hdr->empty[slot], kConsumerWarps / 4);
     }
@@ -1746,11 +1775,22 @@ struct Consumer {
 #pragma unroll
       for (int k = 0; k < 32; ++k) w[k] = c.hdr->work[slot][k];
       const int64_t t_pop = (ct == 0 && (p.trace || p.stats)) ? gtimer() : 0;
+      if (ct == 0) {
+        p.prog[c.sm * 8 + 0] = n_items;
+        p.prog[c.sm * 8 + 1] = (uint32_t)(w[F_OP] & 0xff) | ((uint32_t)(w[F_LAYER] & 0xff) << 8) |
+                               ((uint32_t)(w[F_TASK] & 0xffff) << 16);
+        p.prog[c.sm * 8 + 2] = c.st;
+      }
       if (ok && ct == 0) {
         const uint32_t tgt0 = (uint32_t)(w[F_TGT0] == TGT_DYN_SPLITS
                                              ? (w[F_A0] < p.B ? slices_of(p, __ldg(p.seq_lens + w[F_A0])) : 0)
                                              : w[F_TGT0]);
         ok = wait_cached(w[F_WAIT0], tgt0, w) && wait_cached(w[F_WAIT1], (uint32_t)w[F_TGT1], w);
+      }
+      if (ok && w[F_SEQ] != (int32_t)c.wk) {
+        if (ct == 0) record_error(p, ERR_RING, c.sm, where_of(w), -2, (uint32_t)w[F_SEQ], c.wk);
+        c.hdr->abort = 1;
+        ok = false;
       }
       const int64_t t_go = (ct == 0 && (p.trace || p.stats)) ? gtimer() : 0;
       if (bar_or(kBarConsumers, kConsumerThreads, !ok || aborted(c))) return;
@@ -1802,12 +1842,18 @@ static __device__ void storer(const Params& p, Ctx& c) {
     const uint32_t par = (c.wk / kWorkRing) & 1;
     if (!mbar_wait(p, c, &H->wfull[slot], par)) return;
     const int op = H->work[slot][F_OP], sig0 = H->work[slot][F_SIG0], sig1 = H->work[slot][F_SIG1];
+    if (H->work[slot][F_SEQ] != (int32_t)c.wk) {
+      record_error(p, ERR_RING, c.sm, kNowhere, -3, (uint32_t)H->work[slot][F_SEQ], c.wk);
+      H->abort = 1;
+      return;
+    }
     if (op == W_EXIT) return;
     if (!mbar_wait(p, c, &H->done[slot], par)) return;
     if (sig0 >= 0) red_release_add(p.bars + sig0, 1u);
     if (sig1 >= 0) red_release_add(p.bars + sig1, 1u);
     mbar_arrive(&H->wempty[slot]);
     ++c.wk;
+    p.prog[c.sm * 8 + 6] = c.wk;
   }
 }
 

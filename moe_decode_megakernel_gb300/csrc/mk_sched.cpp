@@ -389,6 +389,7 @@ static void layout_workspace(mk_sched* s) {
   w = WsLayout();
   w.add("barriers", sizeof(uint32_t) * s->bar_kind.size());
   w.add("error", sizeof(uint32_t) * 8);
+  w.add("progress", sizeof(uint32_t) * 8 * (size_t)s->num_sms);
   w.add("h", sizeof(float) * MB * D.H);
   w.add("x", sizeof(float) * MB * D.H);
   w.add("q", sizeof(float) * MB * D.NQ * D.D);

@@ -68,6 +68,11 @@ MODELS = {
     "full": ModelShape("full", n_layers=48, hidden=2048, n_q=32, n_kv=4, head_dim=128,
                        n_experts=128, top_k=8, inter=768, vocab=65536, page_size=64,
                        window=4096, full_period=4),
+    # the full shape's dimensions in two layers, the second one full-attention:
+    # a case small enough for multi-pass profiler captures (about 2.8 GB)
+    "full_l2": ModelShape("full_l2", n_layers=2, hidden=2048, n_q=32, n_kv=4, head_dim=128,
+                          n_experts=128, top_k=8, inter=768, vocab=65536, page_size=64,
+                          window=4096, full_period=2),
 }
 
 
@@ -100,6 +105,8 @@ WORKLOADS = {
                           desc="full shape, B=1, context 262144"),
     "batch64_ragged": Workload("batch64_ragged", "full", 64, ("loguniform", 1024, 65536), 6,
                                desc="full shape, B=64, seq_lens log-uniform [1024,65536]"),
+    "prof_l2_8k": Workload("prof_l2_8k", "full_l2", 1, ("fixed", 8192), 7,
+                           desc="full-shape layers, 2 of them, B=1, context 8192 (profiling case)"),
 }
 
 

@@ -2,8 +2,6 @@
 nothing will reach; the wait gives up after the watchdog limit, the kernel
 returns, mk_check_step reports MK_ERR_TIMEOUT with the stalled wait, and the
 context stays usable for the next step."""
-import re
-
 import numpy as np
 import pytest
 import torch
@@ -46,14 +44,10 @@ def test_unsatisfiable_wait_times_out_and_context_survives():
     with pytest.raises(mk.MkError) as e:
         sess.check()
     assert e.value.code == mk.MK_ERR_TIMEOUT
-    # the first wait to give up is the victim's, or one on a count the victim
-    # would have raised (a dependent that started waiting earlier)
+    # the first wait to give up may be the victim's or one stalled behind it;
+    # the diagnosis against the schedule names the victim as the root
     msg = str(e.value)
-    bar = int(re.search(r"index (-?\d+)", msg).group(1))
-    if bar == d[mk.F_WAIT0]:
-        assert f"task {d[mk.F_TASK]}" in msg and "op 2" in msg
-    else:
-        assert bar in (d[mk.F_SIG0], d[mk.F_SIG1]), msg
+    assert f"root: task {d[mk.F_TASK]} " in msg and f"on barrier {d[mk.F_WAIT0]}," in msg, msg
     # the context is intact: a correct schedule runs and matches the oracle
     good = parity.run_gpu(inp)
     rep = parity.compare(inp, good)
