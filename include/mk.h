@@ -106,9 +106,12 @@ typedef struct {
   int32_t trace;            /* 1: record every work item's timestamps ("trace", "stats") */
   int32_t moe_queue;        /* 0: separate up/gate and down drains; 1: one MoE queue with each
                                expert's down tiles one expert behind its up/gate tiles */
+  int32_t moe_static;       /* 1 (default): claimer c takes MoE units c, c + n, c + 2n, ... of
+                               the queue (n claimers), no atomics; 0: the first unit so and the
+                               rest from a claim counter */
 } mk_sched_opts;
 
-/* Fills opts with the defaults (all zero except fuse_* = 1). */
+/* Fills opts with the defaults (all zero except fuse_* = 1 and moe_static = 1). */
 void mk_default_sched_opts(mk_sched_opts* opts);
 
 /* Builds and validates the per-SM task lists for steps with batch <=

@@ -610,9 +610,11 @@ struct Producer {
   // -- so a down tile rarely waits and no SM idles between the two phases;
   // every unit depends only on units with smaller indices, so the claimers
   // cannot deadlock.  mode 1: up/gate tiles only; mode 2: down tiles only.
-  // Claimer c takes unit c first without an atomic; later units come from
-  // the layer's claim counter, offset by the number of claimers, and each
-  // claim is issued before the current tile streams.
+  // Static assignment (default): claimer c of n takes units c, c + n, ...,
+  // known as soon as the queue is, so the producer streams them back to back.
+  // Otherwise claimer c takes unit c first without an atomic and later units
+  // from the layer's claim counter, offset by n, each claim issued before the
+  // current tile streams.
   __device__ __forceinline__ bool moe_drain(const int32_t* d, int mode) {
     const int l = d[F_LAYER];
     // the routing decides which expert rows to stream: wait for the queue
@@ -628,11 +630,21 @@ struct Producer {
     const uint32_t total = (uint32_t)n_act * (mode == 0 ? U + DN : mode == 1 ? U : DN);
     uint32_t* claim = p.bars + d[F_A0];
     const uint32_t n_claimers = (uint32_t)d[F_A0 + 5];
+    const bool stat = d[F_A0 + 7] != 0;
     uint32_t cur = (uint32_t)d[F_A0 + 4];
+    // static assignment: units cur, cur + n, ...; the down units start after
+    // the last up unit, so the claimers with an extra up/gate tile get no
+    // extra down tile
+    if (stat && mode == 2)
+      cur = (cur + n_claimers - ((uint32_t)n_act * U) % n_claimers) % n_claimers;
     uint32_t nxt = 0;
     if (cur < total) {
-      nxt = n_claimers + atomicAdd(claim, 1u);
-      ++c.stat[3];
+      if (stat) {
+        nxt = cur + n_claimers;
+      } else {
+        nxt = n_claimers + atomicAdd(claim, 1u);
+        ++c.stat[3];
+      }
     }
     int cached_a = -1;
     int4 info = make_int4(0, 0, 0, 0);
@@ -707,8 +719,12 @@ struct Producer {
       }
       cur = nxt;
       if (cur < total) {
-        nxt = n_claimers + atomicAdd(claim, 1u);
-        ++c.stat[3];
+        if (stat) {
+          nxt = cur + n_claimers;
+        } else {
+          nxt = n_claimers + atomicAdd(claim, 1u);
+          ++c.stat[3];
+        }
       }
     }
     return claim_end(d);
@@ -733,10 +749,15 @@ struct Producer {
         ok = false;
         break;
       }
+      // the controller's next TMA copy overwrites this slot: explicit
+      // shared-memory loads, then a cross-proxy fence, then the release
       int32_t d[32];
-      for (int k = 0; k < 32; ++k) d[k] = H->desc[slot][k];
-      // the controller's next TMA copy overwrites this slot: order the reads
-      // (generic proxy) before it (async proxy)
+      const uint32_t da = smem_u32(H->desc[slot]);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint4 v = lds128(da + 16u * k);
+        d[4 * k] = (int32_t)v.x; d[4 * k + 1] = (int32_t)v.y; d[4 * k + 2] = (int32_t)v.z; d[4 * k + 3] = (int32_t)v.w;
+      }
       fence_proxy_async_smem();
       mbar_arrive(&H->dempty[slot]);
       p.prog[c.sm * 8 + 3] = (uint32_t)(i + 1);
@@ -796,11 +817,10 @@ struct Consumer {
     if (p.stats && ct == 0) c.stat[1] += gtimer() - t0;
     return ok;
   }
-  // The stage goes back to the producer, whose next TMA copy overwrites it:
-  // the reads of this warp (generic proxy) are ordered before that write
-  // (async proxy) by a cross-proxy fence ahead of the release.
+  // The stage goes back to the producer, whose next TMA copy overwrites it.
+  // Every read of a stage is an explicit shared-memory load (ld.shared,
+  // ldmatrix), which the release orders before the arrival.
   __device__ __forceinline__ void stage_release(int slot) {
-    fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&c.hdr->empty[slot]);
     ++c.st;
@@ -820,12 +840,12 @@ struct Consumer {
       float acc0[kTB], acc1[kTB];
 #pragma unroll
       for (int t = 0; t < kTB; ++t) acc0[t] = acc1[t] = 0.f;
-      const uint4* wr = reinterpret_cast<const uint4*>(W + (size_t)r * K);
+      const uint32_t wr = smem_u32(W + (size_t)r * K);
 #pragma unroll
       for (int j = 0; j < CPL; ++j) {
         const int cc = lane + 32 * j;
         if (C % 32 == 0 || cc < C) {
-          const uint4 w = wr[cc];
+          const uint4 w = lds128(wr + 16u * cc);
 #pragma unroll
           for (int t = 0; t < kTB; ++t)
             if (t < tb) {
@@ -1035,7 +1055,7 @@ struct Consumer {
 
   // Pair epilogue, run by lane t for activation row t: v0, v1 are the dot
   // products of the pair's two weight rows r0, r1 (rows of stage s).
-  __device__ __noinline__ void pair_epilogue(int op, const int32_t* w, int s, int r0, int r1, int t, float v0,
+  __device__ __forceinline__ void pair_epilogue(int op, const int32_t* w, int s, int r0, int r1, int t, float v0,
                                                 float v1, int dslot, float dwt, int pos, int page) {
     const int l = w[F_LAYER];
     switch (op) {
@@ -1204,9 +1224,7 @@ struct Consumer {
           if (lane < tb && !aborted(c)) pair_epilogue(op, w, s, r0, r1, lane, e0, e1, dslot, dwt, pos, page);
         }
       }
-      // the four warps of the team stand for the eight arrivals the stage
-      // expects; the fence orders the reads before the producer's next copy
-      fence_proxy_async_smem();
+      // the four warps of the team stand for the eight arrivals the stage expects
       __syncwarp();
       if (lane == 0) mbar_arrive_n(&c.hdr->empty[slot], kConsumerWarps / 4);
     }

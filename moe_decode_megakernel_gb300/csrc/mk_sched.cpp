@@ -298,6 +298,7 @@ static int build(mk_sched* s) {
       d[F_A0 + 4] = i;
       d[F_A0 + 5] = n_moe;
       d[F_A0 + 6] = unified ? 0 : 1;
+      d[F_A0 + 7] = o.moe_static ? 1 : 0;
       d[F_SIG0] = unified ? lb.dnd : lb.upd;
       w_up.push_back(d);
       if (!unified) {
@@ -308,6 +309,7 @@ static int build(mk_sched* s) {
         e[F_A0 + 2] = -1;
         e[F_A0 + 4] = i;
         e[F_A0 + 5] = n_moe;
+        e[F_A0 + 7] = o.moe_static ? 1 : 0;
         e[F_SIG0] = lb.dnd;
         w_dn.push_back(e);
       }
@@ -542,6 +544,7 @@ struct Sim {
   std::vector<int32_t> attn_q;
   std::vector<std::vector<int32_t>> up_q, dn_q, uni_q;  // per layer
   std::vector<int> first_done;  // per SM: the claimer's static first unit was taken
+  std::vector<int64_t> last_unit;  // per SM: the claimer's current unit (static assignment)
   std::vector<int8_t> fin_done;
   std::string err;
 
@@ -639,12 +642,17 @@ struct Sim {
         if (pending[sm] < 0) {
           // the first unit is the claimer's own index; later ones come from the counter
           int64_t i;
+          const int64_t n = d[F_A0 + 5];
           if (!first_done[sm]) {
             i = d[F_A0 + 4];
+            // static down units start where the up units left off, so the
+            // claimers with an extra up/gate tile get no extra down tile
+            if (d[F_A0 + 7] && mode == 2) i = (i + n - (int64_t)up_q[l].size() % n) % n;
             first_done[sm] = 1;
           } else {
-            i = d[F_A0 + 5] + bars[claim]++;
+            i = d[F_A0 + 7] ? last_unit[sm] + n : n + bars[claim]++;
           }
+          last_unit[sm] = i;
           if (i >= (int64_t)q.size()) {
             first_done[sm] = 0;
             signal(d);
@@ -692,6 +700,7 @@ void mk_default_sched_opts(mk_sched_opts* o) {
   std::memset(o, 0, sizeof(*o));
   o->fuse_finalize = 1;
   o->fuse_moe_combine = 1;
+  o->moe_static = 1;
 }
 
 int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const mk_sched_opts* opts,
@@ -808,6 +817,7 @@ int mk_sched_simulate(const mk_sched* s, int32_t batch, const int32_t* seq_lens,
   sim.dn_q.assign(L, {});
   sim.uni_q.assign(L, {});
   sim.first_done.assign(s->num_sms, 0);
+  sim.last_unit.assign(s->num_sms, 0);
   sim.fin_done.assign(L, 0);
   std::vector<int> order(s->num_sms);
   for (int i = 0; i < s->num_sms; ++i) order[i] = i;

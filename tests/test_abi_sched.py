@@ -73,7 +73,9 @@ def test_schedules_validate_and_simulate(workload, order):
 @pytest.mark.parametrize("opts", [dict(fuse_finalize=0), dict(fuse_moe_combine=0),
                                   dict(explicit_gather=1), dict(attn_split_pages=1, moe_claimers=5,
                                                                attn_claimers=3),
-                                  dict(moe_queue=1), dict(moe_queue=1, moe_claimers=3)])
+                                  dict(moe_queue=1), dict(moe_queue=1, moe_claimers=3),
+                                  dict(moe_static=0), dict(moe_static=0, moe_claimers=5),
+                                  dict(moe_queue=1, moe_static=0)])
 def test_schedule_variants(opts):
     m, s, inp = sched_for("small", **opts)
     s.validate()
