@@ -10,8 +10,10 @@
 // onto other tasks and deadlocks much later, so barrier accounting gets
 // explicit invariants -- the validator and the simulator below.
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <deque>
+#include <map>
 #include <random>
 #include <sstream>
 
@@ -165,8 +167,8 @@ static int build(mk_sched* s) {
   // tile sizes (multiples of the stage rows)
   const int sr_h = stage_rows(D.H), sr_o = stage_rows(G * D.D);
   auto round_to = [](int v, int m) { return std::max(m, (v / m) * m); };
-  const int qkv_tile = o.qkv_tile_rows > 0 ? round_to(o.qkv_tile_rows, sr_h) : std::max(sr_h, std::min(32, D.D));
-  if (D.D % qkv_tile != 0 || qkv_tile % sr_h != 0)
+  const int qkv_tile = o.qkv_tile_rows > 0 ? round_to(o.qkv_tile_rows, sr_h) : sr_h;
+  if (D.D % qkv_tile != 0 || qkv_tile % sr_h != 0 || D.D % sr_h != 0)
     return fail(MK_ERR_ARG, "qkv_tile_rows must divide head_dim and be a multiple of the stage rows");
   const int o_tile = o.o_tile_rows > 0 ? round_to(o.o_tile_rows, sr_o) : round_to(64, sr_o);
   const int lm_tile = o.lm_tile_rows > 0 ? round_to(o.lm_tile_rows, sr_h) : round_to(128, sr_h);
@@ -184,19 +186,70 @@ static int build(mk_sched* s) {
     const bool full = is_full_layer(c, l);
     std::vector<Desc> w_norm = B.norm_wave(l, norm_rows);
 
-    // QKV: one row tile never straddles a head, so it belongs to one KV group
+    // QKV: a row tile never leaves one KV group's rows (its query heads, its
+    // K head or its V head), so the group's attention waits on its own tiles
     std::vector<Desc> w_qkv;
     lb.n_qkv_g.assign(NKV, 0);
-    for (int r0 = 0; r0 < QKVROWS; r0 += qkv_tile) {
+    auto add_qkv = [&](int r0, int rows, int g) {
       Desc d = blank(OP_QKV_PROJ, l);
       d[F_A0] = r0;
-      d[F_A0 + 1] = qkv_tile;
-      const int head = r0 / D.D;
-      const int g = head < D.NQ ? head / G : (head < D.NQ + NKV ? head - D.NQ : head - D.NQ - NKV);
+      d[F_A0 + 1] = rows;
       B.wait(d, 0, lb.norm, lb.n_norm);
       d[F_SIG0] = lb.qkv + g;
       lb.n_qkv_g[g]++;
       w_qkv.push_back(d);
+    };
+    if (o.qkv_tile_rows > 0) {
+      for (int r0 = 0; r0 < QKVROWS; r0 += qkv_tile) {
+        const int head = r0 / D.D;
+        add_qkv(r0, qkv_tile, head < D.NQ ? head / G : (head < D.NQ + NKV ? head - D.NQ : head - D.NQ - NKV));
+      }
+    } else {
+      // one tile on each SM that holds none of the layer's routing tasks
+      // (the RMSNorm, router and top-k tasks take the SMs just before the
+      // tiles): each group segment gets tiles in proportion to its rows,
+      // largest remainders first, as equal as the stage rows allow (full
+      // shape: 142 tiles of 32 to 48 rows), so no SM holds two
+      // every KV group gets the same tiles (its attention waits for a count
+      // that is the same for all groups): a template of the group's three
+      // segments -- query heads, K head, V head -- apportioned by largest
+      // remainders, repeated per group
+      struct Seg { int r0, rows, g, n; double frac; };
+      const int n_routing = lb.n_norm + (int)((D.E + router_tile - 1) / router_tile) + (MB + kConsumerWarps - 1) / kConsumerWarps;
+      const int per_group = std::max(3, (s->num_sms - n_routing) / NKV);
+      Seg tmpl[3] = {{0, G * D.D, 0, 0, 0.0}, {0, D.D, 0, 0, 0.0}, {0, D.D, 0, 0, 0.0}};
+      int given = 0;
+      for (Seg& sg : tmpl) {
+        const double share = (double)per_group * sg.rows / (G * D.D + 2 * D.D);
+        sg.n = std::max(1, std::min((int)share, sg.rows / sr_h));
+        sg.frac = share - (int)share;
+        given += sg.n;
+      }
+      for (int pass = 0; pass < 3 && given < per_group; ++pass) {
+        int best = -1;
+        for (int k = 0; k < 3; ++k)
+          if (tmpl[k].n < tmpl[k].rows / sr_h && (best < 0 || tmpl[k].frac > tmpl[best].frac)) best = k;
+        if (best < 0) break;
+        ++tmpl[best].n;
+        tmpl[best].frac = -1.0;
+        ++given;
+      }
+      std::vector<Seg> segs;
+      for (int g = 0; g < NKV; ++g) {
+        segs.push_back({g * G * D.D, G * D.D, g, tmpl[0].n, 0.0});
+        segs.push_back({(D.NQ + g) * D.D, D.D, g, tmpl[1].n, 0.0});
+        segs.push_back({(D.NQ + NKV + g) * D.D, D.D, g, tmpl[2].n, 0.0});
+      }
+      for (const Seg& sg : segs) {
+        const int units = sg.rows / sr_h;
+        const int n = sg.n;
+        int r0 = sg.r0;
+        for (int i = 0; i < n; ++i) {
+          const int u = units / n + (i < units % n ? 1 : 0);
+          add_qkv(r0, u * sr_h, sg.g);
+          r0 += u * sr_h;
+        }
+      }
     }
 
     std::vector<Desc> w_router = B.dense_wave(OP_ROUTER_GEMM, l, D.E, router_tile, lb.router);
@@ -828,13 +881,29 @@ int mk_sched_simulate(const mk_sched* s, int32_t batch, const int32_t* seq_lens,
     if (!sim.err.empty()) return fail(MK_ERR_ARG, sim.err);
     if (!progress) break;
   }
-  for (int sm = 0; sm < s->num_sms; ++sm)
-    if (sim.pos[sm] < (int)s->per_sm[sm].size()) {
-      const Desc& d = s->tasks[s->per_sm[sm][sim.pos[sm]]];
-      return fail(MK_ERR_ARG, "deadlock: SM " + std::to_string(sm) + " stuck at task " +
-                                  std::to_string(d[F_TASK]) + " (op " + std::to_string(d[F_OP]) +
-                                  ", layer " + std::to_string(d[F_LAYER]) + ")");
-    }
+  {
+    // a deadlock: report the stuck SMs of the earliest layer with what they wait on
+    std::string msg;
+    int n = 0, min_layer = 1 << 30;
+    for (int sm = 0; sm < s->num_sms; ++sm)
+      if (sim.pos[sm] < (int)s->per_sm[sm].size())
+        min_layer = std::min(min_layer, (int)s->tasks[s->per_sm[sm][sim.pos[sm]]][F_LAYER]);
+    std::map<int, int> hist;
+    for (int sm = 0; sm < s->num_sms; ++sm)
+      if (sim.pos[sm] < (int)s->per_sm[sm].size()) hist[s->tasks[s->per_sm[sm][sim.pos[sm]]][F_OP] * 100 + s->tasks[s->per_sm[sm][sim.pos[sm]]][F_LAYER]]++;
+    for (auto& kv : hist) msg += "[op " + std::to_string(kv.first / 100) + " layer " + std::to_string(kv.first % 100) + ": " + std::to_string(kv.second) + " SMs] ";
+    for (int sm = 0; sm < s->num_sms && n < 4; ++sm)
+      if (sim.pos[sm] < (int)s->per_sm[sm].size()) {
+        const Desc& d = s->tasks[s->per_sm[sm][sim.pos[sm]]];
+        if (d[F_LAYER] != min_layer) continue;
+        msg += (n++ ? "; " : "") + std::string("SM ") + std::to_string(sm) + " stuck at task " +
+               std::to_string(d[F_TASK]) + " (op " + std::to_string(d[F_OP]) + ", layer " +
+               std::to_string(d[F_LAYER]) + ", waits " + std::to_string(d[F_WAIT0]) + ":" +
+               std::to_string(d[F_WAIT0] >= 0 ? sim.bars[d[F_WAIT0]] : 0) + "/" + std::to_string(sim.target(d, 0)) +
+               (sim.pending[sm] >= 0 ? ", unit " + std::to_string(sim.pending[sm]) : std::string()) + ")";
+      }
+    if (n) return fail(MK_ERR_ARG, "deadlock: " + msg);
+  }
   // every static barrier ends at exactly the count its waiters expect
   std::vector<int64_t> expect(s->bar_kind.size(), -1);
   for (const Desc& d : s->tasks)
