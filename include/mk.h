@@ -109,6 +109,10 @@ typedef struct {
   int32_t moe_static;       /* 1 (default): claimer c takes MoE units c, c + n, c + 2n, ... of
                                the queue (n claimers), no atomics; 0: the first unit so and the
                                rest from a claim counter */
+  int32_t fuse_routing;     /* 1 (default): the last router task to finish runs the top-k and
+                               builds the MoE queue (no separate top-k task), and at batch <= 2
+                               each router task computes the layer's RMSNorm itself instead of
+                               waiting for it; needs fuse_finalize */
 } mk_sched_opts;
 
 /* Fills opts with the defaults (all zero except fuse_* = 1 and moe_static = 1). */

@@ -48,7 +48,8 @@ class MkSchedOpts(ctypes.Structure):
                                               "attn_claimers", "moe_claimers", "qkv_tile_rows",
                                               "o_tile_rows", "lm_tile_rows", "fuse_finalize",
                                               "fuse_moe_combine", "explicit_gather",
-                                              "trace_hidden", "watchdog_ms", "trace", "moe_queue", "moe_static")]
+                                              "trace_hidden", "watchdog_ms", "trace", "moe_queue", "moe_static",
+                                              "fuse_routing")]
 
 
 _lib = None

@@ -106,9 +106,14 @@ std::string stall_diagnosis(const mk_sched* s, const void* workspace, cudaStream
       cudaStreamSynchronize(st) != cudaSuccess)
     return "";
   std::vector<int64_t> sig(nb, 0);
-  for (const Desc& d : s->tasks)
+  for (const Desc& d : s->tasks) {
     for (int f : {F_SIG0, F_SIG1})
       if (d[f] >= 0 && (size_t)d[f] < nb) ++sig[d[f]];
+    // fused routing: the last router task of a layer signals the routing barrier
+    if (d[F_OP] == OP_ROUTER_GEMM && d[F_A0 + 5] && d[F_A0 + 6] == 0 && d[F_A0 + 4] >= 0 &&
+        (size_t)d[F_A0 + 4] < nb)
+      ++sig[d[F_A0 + 4]];
+  }
   for (int sm = 0; sm < s->num_sms; ++sm)
     for (int ti : s->per_sm[sm]) {
       const Desc& d = s->tasks[ti];

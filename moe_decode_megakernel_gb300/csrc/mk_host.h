@@ -40,6 +40,7 @@ struct LayerBars {
   int norm = -1, router = -1, topk = -1, fin = -1, gather = -1, o = -1, mcomb = -1;
   int upd = -1, dnd = -1, attn_done = -1;
   int claim_attn = -1, claim_up = -1, claim_dn = -1;
+  int rarrive = -1;  // router tasks that finished (the last one runs the top-k)
   int qkv = -1;    // base, n_kv entries
   int acomb = -1;  // base, n_kv entries
   int cnt = -1;    // base, MB * n_kv entries

@@ -270,6 +270,7 @@ struct Scratch {
   float red[kConsumerWarps * 2];
   double rope_theta[S::D / 2];              // base^(-2i/D)
   int32_t xtag[4], qtag[4];                 // what xs / qs hold
+  int32_t flag;                             // a block-wide decision (the last router task)
   unsigned long long mask[S::E];            // rows routed to each expert (bit b)
   int32_t ids[kMaxBatch * S::K];            // this layer's routing (top-k / finalize)
   int32_t cnt[S::E], off[S::E + 1], act[S::E + 1];
@@ -620,7 +621,8 @@ struct Producer {
     // the routing decides which expert rows to stream: wait for the queue
     {
       const int64_t t0 = p.stats ? gtimer() : 0;
-      const bool ok = wait_counter(p, c, d[F_WAIT0], (uint32_t)d[F_TGT0], where_of(d));
+      const bool ok = wait_counter(p, c, d[F_WAIT0], (uint32_t)d[F_TGT0], where_of(d)) &&
+                      wait_counter(p, c, d[F_WAIT1], (uint32_t)d[F_TGT1], where_of(d));
       if (p.stats) c.stat[1] += gtimer() - t0;
       if (!ok) return false;
     }
@@ -1463,79 +1465,91 @@ struct Consumer {
   // output of the previous layer is the sum of the row's K expert outputs,
   // which the down projection stored already weighted, one slot per (row, k).
   // Every operand is loaded with one round of independent 16-byte loads.
+  // The residual entering layer l for row b -- the embedding at layer 0, else
+  // the previous residual plus the attention partials plus the MoE output --
+  // and its inverse RMS ("Residual + RMSNorm").  The residual buffer is kept
+  // per layer parity, so layer l reads (l - 1) & 1 while its norm writes l & 1.
+  template <int PER>
+  __device__ __forceinline__ float resid_row(const int32_t* w, int l, int b, bool fused, float4 (&v)[PER]) {
+    constexpr int H4 = S::H / 4;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (l == 0) {
+      const int sl = __ldg(p.seq_lens + b);
+      if ((sl < 1 || sl > p.max_ctx) && ct == 0) record_error(p, ERR_INDEX, c.sm, where_of(w), -1, (uint32_t)sl, (uint32_t)p.max_ctx);
+      int tok = __ldg(p.tokens + b);
+      if (tok < 0 || tok >= p.V) {
+        if (ct == 0) record_error(p, ERR_INDEX, c.sm, where_of(w), -1, (uint32_t)tok, (uint32_t)p.V);
+        tok = 0;
+      }
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int i4 = ct + k * kConsumerThreads;
+        if (H4 % kConsumerThreads == 0 || i4 < H4) {
+          const uint2 e = __ldg(reinterpret_cast<const uint2*>(p.emb + (int64_t)tok * S::H) + i4);
+          v[k] = make_float4(bf16_lo(e.x), bf16_hi(e.x), bf16_lo(e.y), bf16_hi(e.y));
+        }
+      }
+    } else {
+      const float4* h4 = reinterpret_cast<const float4*>(p.h + ((int64_t)((l + 1) & 1) * p.MB + b) * S::H);
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int i4 = ct + k * kConsumerThreads;
+        if (H4 % kConsumerThreads == 0 || i4 < H4) {
+          float4 parts[1 + S::NKV + S::K];
+          int n = 0;
+          parts[n++] = __ldcg(h4 + i4);
+#pragma unroll
+          for (int g = 0; g < S::NKV; ++g)
+            parts[n++] = __ldcg(reinterpret_cast<const float4*>(p.opart + ((int64_t)g * p.MB + b) * S::H) + i4);
+          if (fused) {
+#pragma unroll
+            for (int j = 0; j < S::K; ++j)
+              parts[n++] = __ldcg(reinterpret_cast<const float4*>(p.y + ((int64_t)b * S::K + j) * S::H) + i4);
+          } else {
+            parts[n++] = __ldcg(reinterpret_cast<const float4*>(p.moe_out + (int64_t)b * S::H) + i4);
+          }
+          // residual + attention partials, then the MoE output summed on its own
+          // (the same order as a separate MOE_COMBINE)
+          float4 a = parts[0];
+#pragma unroll
+          for (int q = 1; q <= S::NKV; ++q) {
+            a.x += parts[q].x; a.y += parts[q].y; a.z += parts[q].z; a.w += parts[q].w;
+          }
+          float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int q = 1 + S::NKV; q < 1 + S::NKV + S::K; ++q)
+            if (q < n) {
+              m.x += parts[q].x; m.y += parts[q].y; m.z += parts[q].z; m.w += parts[q].w;
+            }
+          a.x += m.x; a.y += m.y; a.z += m.z; a.w += m.w;
+          v[k] = a;
+        }
+      }
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < PER; ++k)
+      ss = fmaf(v[k].x, v[k].x, fmaf(v[k].y, v[k].y, fmaf(v[k].z, v[k].z, fmaf(v[k].w, v[k].w, ss))));
+    ss = warp_sum(ss);
+    if (lane == 0) sm.red[cw] = ss;
+    consumers_sync();
+    float tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < kConsumerWarps; ++i) tot += sm.red[i];
+    consumers_sync();  // sm.red is free again
+    return 1.f / sqrtf(tot / (float)S::H + p.eps);
+  }
+
   __device__ __forceinline__ void norm(const int32_t* w) {
     constexpr int H4 = S::H / 4, PER = (H4 + kConsumerThreads - 1) / kConsumerThreads;
     const int l = w[F_LAYER], b1 = min(w[F_A0 + 1], p.B);
     const bool final_norm = w[F_A0 + 2] != 0, fused = w[F_A0 + 3] != 0;
     for (int b = w[F_A0]; b < b1; ++b) {
       float4 v[PER];
-#pragma unroll
-      for (int k = 0; k < PER; ++k) v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (l == 0) {
-        const int sl = __ldg(p.seq_lens + b);
-        if ((sl < 1 || sl > p.max_ctx) && ct == 0) record_error(p, ERR_INDEX, c.sm, where_of(w), -1, (uint32_t)sl, (uint32_t)p.max_ctx);
-        int tok = __ldg(p.tokens + b);
-        if (tok < 0 || tok >= p.V) {
-          if (ct == 0) record_error(p, ERR_INDEX, c.sm, where_of(w), -1, (uint32_t)tok, (uint32_t)p.V);
-          tok = 0;
-        }
-#pragma unroll
-        for (int k = 0; k < PER; ++k) {
-          const int i4 = ct + k * kConsumerThreads;
-          if (H4 % kConsumerThreads == 0 || i4 < H4) {
-            const uint2 e = __ldg(reinterpret_cast<const uint2*>(p.emb + (int64_t)tok * S::H) + i4);
-            v[k] = make_float4(bf16_lo(e.x), bf16_hi(e.x), bf16_lo(e.y), bf16_hi(e.y));
-          }
-        }
-      } else {
-        const float4* h4 = reinterpret_cast<const float4*>(p.h + (int64_t)b * S::H);
-#pragma unroll
-        for (int k = 0; k < PER; ++k) {
-          const int i4 = ct + k * kConsumerThreads;
-          if (H4 % kConsumerThreads == 0 || i4 < H4) {
-            float4 parts[1 + S::NKV + S::K];
-            int n = 0;
-            parts[n++] = __ldcg(h4 + i4);
-#pragma unroll
-            for (int g = 0; g < S::NKV; ++g)
-              parts[n++] = __ldcg(reinterpret_cast<const float4*>(p.opart + ((int64_t)g * p.MB + b) * S::H) + i4);
-            if (fused) {
-#pragma unroll
-              for (int j = 0; j < S::K; ++j)
-                parts[n++] = __ldcg(reinterpret_cast<const float4*>(p.y + ((int64_t)b * S::K + j) * S::H) + i4);
-            } else {
-              parts[n++] = __ldcg(reinterpret_cast<const float4*>(p.moe_out + (int64_t)b * S::H) + i4);
-            }
-            // residual + attention partials, then the MoE output summed on its own
-            // (the same order as a separate MOE_COMBINE)
-            float4 a = parts[0];
-#pragma unroll
-            for (int q = 1; q <= S::NKV; ++q) {
-              a.x += parts[q].x; a.y += parts[q].y; a.z += parts[q].z; a.w += parts[q].w;
-            }
-            float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int q = 1 + S::NKV; q < 1 + S::NKV + S::K; ++q)
-              if (q < n) {
-                m.x += parts[q].x; m.y += parts[q].y; m.z += parts[q].z; m.w += parts[q].w;
-              }
-            a.x += m.x; a.y += m.y; a.z += m.z; a.w += m.w;
-            v[k] = a;
-          }
-        }
-      }
-      float ss = 0.f;
-#pragma unroll
-      for (int k = 0; k < PER; ++k)
-        ss = fmaf(v[k].x, v[k].x, fmaf(v[k].y, v[k].y, fmaf(v[k].z, v[k].z, fmaf(v[k].w, v[k].w, ss))));
-      ss = warp_sum(ss);
-      if (lane == 0) sm.red[cw] = ss;
-      consumers_sync();
-      float tot = 0.f;
-#pragma unroll
-      for (int i = 0; i < kConsumerWarps; ++i) tot += sm.red[i];
-      const float inv_rms = 1.f / sqrtf(tot / (float)S::H + p.eps);
+      const float inv_rms = resid_row<PER>(w, l, b, fused, v);
       const float4* gam = reinterpret_cast<const float4*>(final_norm ? p.gamma_f : p.gamma + (int64_t)l * S::H);
+      float4* hout = reinterpret_cast<float4*>(p.h + ((int64_t)(l & 1) * p.MB + b) * S::H);
 #pragma unroll
       for (int k = 0; k < PER; ++k) {
         const int i4 = ct + k * kConsumerThreads;
@@ -1543,21 +1557,71 @@ struct Consumer {
           const float4 gm = __ldg(gam + i4), a = v[k];
           reinterpret_cast<float4*>(p.x + (int64_t)b * S::H)[i4] =
               make_float4(a.x * inv_rms * gm.x, a.y * inv_rms * gm.y, a.z * inv_rms * gm.z, a.w * inv_rms * gm.w);
-          reinterpret_cast<float4*>(p.h + (int64_t)b * S::H)[i4] = a;
+          if (!final_norm) hout[i4] = a;
           if (p.htrace) reinterpret_cast<float4*>(p.htrace + ((int64_t)l * p.MB + b) * S::H)[i4] = a;
         }
       }
-      consumers_sync();
     }
+  }
+
+  // A router task that computes the layer's RMSNorm itself (batch <= kTB):
+  // the normalised rows go straight into the activation cache, in the layout
+  // and with the tag the GEMV uses for the layer input.
+  __device__ __forceinline__ void norm_into_cache(const int32_t* w) {
+    constexpr int H4 = S::H / 4, PER = (H4 + kConsumerThreads - 1) / kConsumerThreads;
+    const int l = w[F_LAYER];
+    float4* xs4 = reinterpret_cast<float4*>(sm.xs);
+    for (int b = 0; b < p.B; ++b) {
+      float4 v[PER];
+      const float inv_rms = resid_row<PER>(w, l, b, true, v);
+      const float4* gam = reinterpret_cast<const float4*>(p.gamma + (int64_t)l * S::H);
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int i4 = ct + k * kConsumerThreads;
+        if (H4 % kConsumerThreads == 0 || i4 < H4) {
+          const float4 gm = __ldg(gam + i4), a = v[k];
+          // float4 i4 of the row goes to [half i4 % 2][chunk i4 / 2], as load_x places it
+          xs4[b * H4 + (i4 & 1) * (H4 / 2) + (i4 >> 1)] =
+              make_float4(a.x * inv_rms * gm.x, a.y * inv_rms * gm.y, a.z * inv_rms * gm.z, a.w * inv_rms * gm.w);
+        }
+      }
+    }
+    // the tag is read again within this item: publish it before the barrier
+    if (ct == 0) {
+      sm.xtag[0] = 1; sm.xtag[1] = 0; sm.xtag[2] = 0; sm.xtag[3] = l;
+    }
+    consumers_sync();
+  }
+
+  // The routing step of the last router task of a layer: count this task in;
+  // the last one reads every router logit, runs the top-k and builds the MoE
+  // queue, then signals the routing barrier itself.
+  __device__ __forceinline__ void route_if_last(const int32_t* w) {
+    __threadfence();  // this task's logits before the count
+    consumers_sync();
+    if (ct == 0) {
+      const uint32_t old = atomicAdd(p.bars + w[F_A0 + 2], 1u);
+      __threadfence();
+      sm.flag = (old + 1u == (uint32_t)w[F_A0 + 3] && !aborted(c)) ? 1 : 0;
+    }
+    consumers_sync();
+    if (!sm.flag) return;
+    topk_rows(w[F_LAYER], 0, p.B, true);
+    __threadfence();
+    consumers_sync();
+    if (ct == 0) red_release_add(p.bars + w[F_A0 + 4], 1u);
   }
 
   // ------------------------------------------------------------ routing
   // Top-k of each row's router logits (higher logit first, lower expert id on
   // ties) and softmax weights over the selected logits ("Tasks": ROUTER_TOPK).
   __device__ __forceinline__ void topk(const int32_t* w) {
+    topk_rows(w[F_LAYER], w[F_A0], w[F_A0 + 1], w[F_A0 + 2] != 0);
+  }
+  __device__ __forceinline__ void topk_rows(int l, int b0, int b_end, bool fin) {
     constexpr int E = S::E, K = S::K, PL = (E + 31) / 32;
-    const int l = w[F_LAYER], b1 = min(w[F_A0 + 1], p.B);
-    for (int b = w[F_A0] + cw; b < b1; b += kConsumerWarps) {
+    const int b1 = min(b_end, p.B);
+    for (int b = b0 + cw; b < b1; b += kConsumerWarps) {
       float v[PL];
 #pragma unroll
       for (int k = 0; k < PL; ++k) {
@@ -1608,7 +1672,7 @@ struct Consumer {
         }
       }
     }
-    if (w[F_A0 + 2]) {  // the one top-k task also builds the queues, from shared memory
+    if (fin) {  // the one top-k task also builds the queues, from shared memory
       if (p.B > 1) consumers_sync();
       else __syncwarp();  // one row: warp 0 wrote the routing
       finalize(l, false);
@@ -1729,8 +1793,13 @@ struct Consumer {
 
   __device__ __forceinline__ void execute(const int32_t* w) {
     switch (w[F_OP]) {
-      case OP_QKV_PROJ:
       case OP_ROUTER_GEMM:
+        if (w[F_A0 + 7] && p.B <= kTB) norm_into_cache(w);
+        if (p.B <= kTB) gemv_item_teams<S::H>(w, S::SR_H, w[F_A0 + 1], p.B);
+        else gemv_item<S::H>(w, S::SR_H, w[F_A0 + 1], p.B);
+        if (w[F_A0 + 5]) route_if_last(w);
+        break;
+      case OP_QKV_PROJ:
       case OP_LM_HEAD:
         if (p.B <= kTB) gemv_item_teams<S::H>(w, S::SR_H, w[F_A0 + 1], p.B);
         else gemv_item<S::H>(w, S::SR_H, w[F_A0 + 1], p.B);

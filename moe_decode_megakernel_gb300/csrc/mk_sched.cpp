@@ -89,6 +89,7 @@ struct Builder {
       b.claim_attn = bar(BK_CLAIM);
       b.claim_up = bar(BK_CLAIM);
       b.claim_dn = bar(BK_CLAIM);
+      b.rarrive = bar(BK_CLAIM);
     }
     s->lm_bar = bar(BK_STATIC);
   }
@@ -253,13 +254,34 @@ static int build(mk_sched* s) {
     }
 
     std::vector<Desc> w_router = B.dense_wave(OP_ROUTER_GEMM, l, D.E, router_tile, lb.router);
-    for (auto& d : w_router) B.wait(d, 0, lb.norm, lb.n_norm);
     lb.n_router = (int)w_router.size();
+    const bool fuse_fin = o.fuse_finalize && MB <= kConsumerWarps;
+    // routing fused into the router tasks: each counts itself in on lb.rarrive
+    // and the last one runs the top-k and the queue build, then signals lb.fin;
+    // at batch <= 2 each also computes the RMSNorm from the residual parts
+    const bool fuse_rt = o.fuse_routing && fuse_fin;
+    const bool norm_in_router = fuse_rt && MB <= kTB;
+    for (size_t i = 0; i < w_router.size(); ++i) {
+      Desc& d = w_router[i];
+      if (norm_in_router) {
+        d[F_WAIT0] = w_norm[0][F_WAIT0]; d[F_TGT0] = w_norm[0][F_TGT0];
+        d[F_WAIT1] = w_norm[0][F_WAIT1]; d[F_TGT1] = w_norm[0][F_TGT1];
+      } else {
+        B.wait(d, 0, lb.norm, lb.n_norm);
+      }
+      if (fuse_rt) {
+        d[F_A0 + 2] = lb.rarrive;
+        d[F_A0 + 3] = lb.n_router;
+        d[F_A0 + 4] = lb.fin;
+        d[F_A0 + 5] = 1;
+        d[F_A0 + 6] = (int)i;
+        d[F_A0 + 7] = norm_in_router ? 1 : 0;
+      }
+    }
 
     std::vector<Desc> w_topk, w_fin;
-    const bool fuse_fin = o.fuse_finalize && MB <= kConsumerWarps;
     const int topk_rows = kConsumerWarps;
-    for (int b0 = 0; b0 < MB; b0 += topk_rows) {
+    for (int b0 = 0; b0 < (fuse_rt ? 0 : MB); b0 += topk_rows) {
       Desc d = blank(OP_ROUTER_TOPK, l);
       d[F_A0] = b0;
       d[F_A0 + 1] = std::min(MB, b0 + topk_rows);
@@ -285,6 +307,7 @@ static int build(mk_sched* s) {
         d[F_A0] = r0;
         d[F_A0 + 1] = std::min(per, rows - r0);
         B.wait(d, 0, lb.fin, 1);
+        if (norm_in_router) B.wait(d, 1, lb.norm, lb.n_norm);  // gathers the RMSNorm output
         d[F_SIG0] = lb.gather;
         w_gather.push_back(d);
       }
@@ -344,6 +367,9 @@ static int build(mk_sched* s) {
     for (int i = 0; i < n_moe; ++i) {
       Desc d = blank(OP_MOE_UPGATE_ACT_DRAIN, l);
       B.wait(d, 0, lb.fin, 1);
+      // the routing can finish before the RMSNorm task when the routers
+      // compute the norm themselves: the up/gate tiles read its output
+      if (norm_in_router) B.wait(d, 1, lb.norm, lb.n_norm);
       d[F_A0] = lb.claim_up;
       d[F_A0 + 1] = lb.up;
       d[F_A0 + 2] = o.explicit_gather ? lb.gather : -1;
@@ -445,7 +471,7 @@ static void layout_workspace(mk_sched* s) {
   w.add("barriers", sizeof(uint32_t) * s->bar_kind.size());
   w.add("error", sizeof(uint32_t) * 8);
   w.add("progress", sizeof(uint32_t) * 8 * (size_t)s->num_sms);
-  w.add("h", sizeof(float) * MB * D.H);
+  w.add("h", sizeof(float) * 2 * MB * D.H);  // the residual, by layer parity
   w.add("x", sizeof(float) * MB * D.H);
   w.add("q", sizeof(float) * MB * D.NQ * D.D);
   w.add("kvnew", 2ull * MB * 2 * D.NKV * D.D);
@@ -523,6 +549,14 @@ static int validate(const mk_sched* s) {
       for (int e = 0; e < s->dims.E; ++e) waiters[d[F_A0 + 1] + e].push_back(t);
     if (op == OP_ATTN_DRAIN)
       for (int i = 0; i < s->max_batch * s->dims.NKV; ++i) producers[d[F_A0 + 1] + i].push_back(t);
+    // fused routing: the last router task of the layer signals the routing
+    // barrier once; every router task feeds it
+    if (op == OP_ROUTER_GEMM && d[F_A0 + 5]) {
+      const int b = d[F_A0 + 4];
+      if (b < 0 || b >= NB) return fail(MK_ERR_ARG, "router task signals a barrier out of range");
+      if (d[F_A0 + 6] == 0) signals[b]++;
+      producers[b].push_back(t);
+    }
   }
   for (int b = 0; b < NB; ++b) {
     if (s->bar_kind[b] != BK_STATIC) continue;
@@ -662,6 +696,13 @@ struct Sim {
         if (d[F_A0 + 2]) finalize(l);
         signal(d);
         break;
+      case OP_ROUTER_GEMM:
+        signal(d);
+        if (d[F_A0 + 5] && ++bars[d[F_A0 + 2]] == d[F_A0 + 3]) {  // the last router task
+          finalize(l);
+          bars[d[F_A0 + 4]]++;
+        }
+        break;
       case OP_ROUTE_FINALIZE:
         finalize(l);
         signal(d);
@@ -754,6 +795,7 @@ void mk_default_sched_opts(mk_sched_opts* o) {
   o->fuse_finalize = 1;
   o->fuse_moe_combine = 1;
   o->moe_static = 1;
+  o->fuse_routing = 1;
 }
 
 int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const mk_sched_opts* opts,

@@ -75,7 +75,8 @@ def test_schedules_validate_and_simulate(workload, order):
                                                                attn_claimers=3),
                                   dict(moe_queue=1), dict(moe_queue=1, moe_claimers=3),
                                   dict(moe_static=0), dict(moe_static=0, moe_claimers=5),
-                                  dict(moe_queue=1, moe_static=0)])
+                                  dict(moe_queue=1, moe_static=0), dict(fuse_routing=0),
+                                  dict(fuse_routing=0, fuse_finalize=0)])
 def test_schedule_variants(opts):
     m, s, inp = sched_for("small", **opts)
     s.validate()
@@ -103,7 +104,8 @@ def test_full_list_shape():
     # one QKV tile per SM that holds no routing task (32 to 48 rows, within one
     # KV group); the pages quote 80 tiles of 64
     assert counts["QKV_PROJ"] == sh.n_layers * 140  # 35 per KV group, none on the routing SMs
-    assert counts["ROUTER_TOPK"] == sh.n_layers
+    # the last router task of a layer runs the top-k: no top-k tasks
+    assert counts.get("ROUTER_TOPK", 0) == 0 and counts["ROUTER_GEMM"] == sh.n_layers * 8
     # one up/gate and one down claimer per SM per layer
     assert counts["MOE_UPGATE_ACT_DRAIN"] == counts["MOE_DOWN_DRAIN"] == sh.n_layers * NUM_SMS
     m2, s2, _ = sched_for("full_bs1_8k", moe_queue=1)  # one combined queue
