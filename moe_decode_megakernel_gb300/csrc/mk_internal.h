@@ -109,14 +109,25 @@ struct MoePlan {
   int dn_rows, dn_stages, dn_tile, dn_tiles;
 };
 
+// Tiles are as large as keeps at least 16 up/gate and 32 down tiles per
+// expert: each tile is a work item with a fixed cost (its barrier, its
+// activation load, its epilogue), and at batch 1 the eight routed experts'
+// 128 up/gate tiles and 256 down tiles still cover the SMs (full shape: up/gate
+// tiles of 12 stages, 48 intermediate rows; down tiles of 4 stages, 64 rows).
+constexpr int moe_stages(int rows, int rows_per_stage, int min_tiles) {
+  const int cand[6] = {12, 8, 6, 4, 2, 1};
+  for (int i = 0; i < 6; ++i)
+    if (rows % (cand[i] * rows_per_stage) == 0 && rows / (cand[i] * rows_per_stage) >= min_tiles) return cand[i];
+  return 1;
+}
 constexpr MoePlan moe_plan(ShapeDims s) {
   MoePlan p{};
   p.up_half = stage_rows(s.H) / 2;
-  p.up_stages = (s.I % (2 * p.up_half) == 0) ? 2 : 1;
+  p.up_stages = moe_stages(s.I, p.up_half, 16);
   p.up_tile = p.up_half * p.up_stages;
   p.up_tiles = s.I / p.up_tile;
   p.dn_rows = stage_rows(s.I);
-  p.dn_stages = (s.H % (2 * p.dn_rows) == 0) ? 2 : 1;
+  p.dn_stages = moe_stages(s.H, p.dn_rows, 32);
   p.dn_tile = p.dn_rows * p.dn_stages;
   p.dn_tiles = s.H / p.dn_tile;
   return p;
