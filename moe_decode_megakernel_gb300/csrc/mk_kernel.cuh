@@ -1134,6 +1134,13 @@ struct Consumer {
   // up/gate), so a stage needs no block-wide barrier.
   template <int K>
   __device__ __forceinline__ void gemv_item_teams(const int32_t* w, int SR, int total_rows, int ntok) {
+    // one activation row is the decode case: its own instantiation, without
+    // the second row's predicated work
+    if (ntok <= 1) gemv_item_teams_tb<K, 1>(w, SR, total_rows, ntok);
+    else gemv_item_teams_tb<K, kTB>(w, SR, total_rows, ntok);
+  }
+  template <int K, int TB>
+  __device__ __forceinline__ void gemv_item_teams_tb(const int32_t* w, int SR, int total_rows, int ntok) {
     constexpr int C = K / 8;
     constexpr int CPL = (C + 31) / 32;
     const int op = w[F_OP];
@@ -1177,16 +1184,16 @@ struct Consumer {
           const int r0 = up_pairs ? pr : 2 * pr;
           const int r1 = up_pairs ? pr + npairs : 2 * pr + 1;
           const uint32_t w0 = st_a + (uint32_t)(r0 * K * 2), w1 = st_a + (uint32_t)(r1 * K * 2);
-          float a0[kTB], a1[kTB], b0[kTB], b1[kTB];
+          float a0[TB], a1[TB], b0[TB], b1[TB];
 #pragma unroll
-          for (int t = 0; t < kTB; ++t) a0[t] = a1[t] = b0[t] = b1[t] = 0.f;
+          for (int t = 0; t < TB; ++t) a0[t] = a1[t] = b0[t] = b1[t] = 0.f;
 #pragma unroll
           for (int j = 0; j < CPL; ++j) {
             if (C % 32 == 0 || lane + 32 * j < C) {
               const uint4 u0 = lds128(w0 + j * 512), u1 = lds128(w1 + j * 512);
 #pragma unroll
-              for (int t = 0; t < kTB; ++t)
-                if (t < tb) {
+              for (int t = 0; t < TB; ++t)
+                if (TB == 1 || t < tb) {
                   // x row t as [half][chunk][4]: chunk c's elements 0..3 and 4..7
                   const uint4 xa4 = lds128(xs_a + (uint32_t)((t * 2 * C + 32 * j) * 16));
                   const uint4 xb4 = lds128(xs_a + (uint32_t)((t * 2 * C + C + 32 * j) * 16));
@@ -1213,16 +1220,16 @@ struct Consumer {
                 }
             }
           }
-          float v0[kTB], v1[kTB];
+          float v0[TB], v1[TB];
 #pragma unroll
-          for (int t = 0; t < kTB; ++t)
-            if (t < tb) {
+          for (int t = 0; t < TB; ++t)
+            if (TB == 1 || t < tb) {
               v0[t] = warp_sum(a0[t] + a1[t]);
               v1[t] = warp_sum(b0[t] + b1[t]);
             }
           // lane t finishes the pair for activation row t
-          const float e0 = (kTB > 1 && lane == 1) ? v0[kTB - 1] : v0[0];
-          const float e1 = (kTB > 1 && lane == 1) ? v1[kTB - 1] : v1[0];
+          const float e0 = (TB > 1 && lane == 1) ? v0[TB - 1] : v0[0];
+          const float e1 = (TB > 1 && lane == 1) ? v1[TB - 1] : v1[0];
           if (lane < tb && !aborted(c)) pair_epilogue(op, w, s, r0, r1, lane, e0, e1, dslot, dwt, pos, page);
         }
       }
