@@ -142,6 +142,11 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -271,6 +276,8 @@ struct Scratch {
   double rope_theta[S::D / 2];              // base^(-2i/D)
   int32_t xtag[4], qtag[4];                 // what xs / qs hold
   int32_t flag;                             // a block-wide decision (the last router task)
+  int32_t tk_id[kConsumerWarps][S::K];      // top-k of the row a warp works on
+  uint32_t tk_key[kConsumerWarps][S::K];
   unsigned long long mask[S::E];            // rows routed to each expert (bit b)
   int32_t ids[kMaxBatch * S::K];            // this layer's routing (top-k / finalize)
   int32_t cnt[S::E], off[S::E + 1], act[S::E + 1];
@@ -1604,17 +1611,20 @@ struct Consumer {
   // the last one reads every router logit, runs the top-k and builds the MoE
   // queue, then signals the routing barrier itself.
   __device__ __forceinline__ void route_if_last(const int32_t* w) {
-    __threadfence();  // this task's logits before the count
+    // the block's logit stores, then one acquire-release count: the last
+    // task sees every other task's logits
     consumers_sync();
     if (ct == 0) {
-      const uint32_t old = atomicAdd(p.bars + w[F_A0 + 2], 1u);
-      __threadfence();
+      const uint32_t old = atom_add_acq_rel(p.bars + w[F_A0 + 2], 1u);
       sm.flag = (old + 1u == (uint32_t)w[F_A0 + 3] && !aborted(c)) ? 1 : 0;
     }
     consumers_sync();
     if (!sm.flag) return;
     topk_rows(w[F_LAYER], 0, p.B, true);
-    __threadfence();
+    if (p.B == 1) {  // warp 0 finishes the row and releases the routing itself
+      if (cw == 0) route_one_row(w[F_LAYER], p.bars + w[F_A0 + 4]);
+      return;
+    }
     consumers_sync();
     if (ct == 0) red_release_add(p.bars + w[F_A0 + 4], 1u);
   }
@@ -1623,67 +1633,123 @@ struct Consumer {
   // Top-k of each row's router logits (higher logit first, lower expert id on
   // ties) and softmax weights over the selected logits ("Tasks": ROUTER_TOPK).
   __device__ __forceinline__ void topk(const int32_t* w) {
-    topk_rows(w[F_LAYER], w[F_A0], w[F_A0 + 1], w[F_A0 + 2] != 0);
+    const bool fin = w[F_A0 + 2] != 0;
+    topk_rows(w[F_LAYER], w[F_A0], w[F_A0 + 1], fin);
+    if (fin && p.B == 1 && cw == 0) route_one_row(w[F_LAYER], nullptr);  // the storer signals
   }
+  // Logits as unsigned keys with the same order (finite inputs): a warp-wide
+  // unsigned max then finds the largest logit in one reduction.
+  static __device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  }
+  static __device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+  }
+  // One warp per row: K rounds of (max key over the warp, then the lowest
+  // expert id holding it), written compactly -- this runs once per layer,
+  // usually from a cold instruction cache.
   __device__ __forceinline__ void topk_rows(int l, int b0, int b_end, bool fin) {
     constexpr int E = S::E, K = S::K, PL = (E + 31) / 32;
     const int b1 = min(b_end, p.B);
     for (int b = b0 + cw; b < b1; b += kConsumerWarps) {
-      float v[PL];
+      uint32_t key[PL];
 #pragma unroll
       for (int k = 0; k < PL; ++k) {
         const int e = lane + 32 * k;
-        v[k] = e < E ? __ldcg(p.rlog + ((int64_t)l * p.MB + b) * E + e) : -INFINITY;
+        key[k] = e < E ? order_key(__ldcg(p.rlog + ((int64_t)l * p.MB + b) * E + e)) : 0u;
       }
-      int ids[K];
-      float vals[K];
-#pragma unroll
+#pragma unroll 1
       for (int j = 0; j < K; ++j) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int k = 0; k < PL; ++k) {
-          const int e = lane + 32 * k;
-          if (e < E && (v[k] > bv || (v[k] == bv && e < bi))) {
-            bv = v[k];
-            bi = e;
-          }
-        }
-#pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) {
-          const float ov = __shfl_xor_sync(FULL, bv, m);
-          const int oi = __shfl_xor_sync(FULL, bi, m);
-          if (ov > bv || (ov == bv && oi < bi)) {
-            bv = ov;
-            bi = oi;
-          }
-        }
-        ids[j] = bi;
-        vals[j] = bv;
+        uint32_t lk = 0u;
+        uint32_t le = 0xffffffffu;
 #pragma unroll
         for (int k = 0; k < PL; ++k)
-          if (lane + 32 * k == bi) v[k] = -INFINITY;
-      }
-      if (lane == 0) {
-        float z = 0.f, e_[K];
+          if (key[k] > lk) {
+            lk = key[k];
+            le = (uint32_t)(lane + 32 * k);
+          }
+        const uint32_t mk = __reduce_max_sync(FULL, lk);
+        const uint32_t wi = __reduce_min_sync(FULL, lk == mk ? le : 0xffffffffu);
 #pragma unroll
-        for (int j = 0; j < K; ++j) {
-          e_[j] = expf(vals[j] - vals[0]);
-          z += e_[j];
-        }
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-          p.topk_ids[((int64_t)l * p.MB + b) * K + j] = ids[j];
-          p.topk_w[((int64_t)l * p.MB + b) * K + j] = e_[j] / z;
-          sm.ids[b * K + j] = ids[j];
+        for (int k = 0; k < PL; ++k)
+          if ((uint32_t)(lane + 32 * k) == wi) key[k] = 0u;
+        if (lane == 0) {
+          sm.tk_id[cw][j] = (int32_t)wi;
+          sm.tk_key[cw][j] = mk;
         }
       }
+      __syncwarp();
+      if (fin && p.B == 1) break;  // route_one_row finishes the row
+      // softmax over the selected logits, lane j for choice j
+      const float v0 = key_value(sm.tk_key[cw][0]);
+      const float ej = lane < K ? expf(key_value(sm.tk_key[cw][lane < K ? lane : 0]) - v0) : 0.f;
+      const float z = warp_sum(ej);
+      if (lane < K) {
+        const int id = sm.tk_id[cw][lane];
+        p.topk_ids[((int64_t)l * p.MB + b) * K + lane] = id;
+        p.topk_w[((int64_t)l * p.MB + b) * K + lane] = ej / z;
+        sm.ids[b * K + lane] = id;
+      }
+      __syncwarp();
     }
+    if (fin && p.B == 1) return;  // the caller runs route_one_row
     if (fin) {  // the one top-k task also builds the queues, from shared memory
       if (p.B > 1) consumers_sync();
       else __syncwarp();  // one row: warp 0 wrote the routing
       finalize(l, false);
     }
+  }
+
+  // The routing of a single row (decode at batch 1) after its top-k rounds,
+  // by warp 0, lane j for choice j: the softmax weight, the rank of the
+  // chosen expert among the chosen ids -- each has exactly one routed row, so
+  // the rank is its place in the expert-ordered list -- and the queue record.
+  // What the MoE branch reads is written first and released on `sig`; the
+  // per-expert counts and offsets follow.
+  __device__ __forceinline__ void route_one_row(int l, uint32_t* sig) {
+    constexpr int E = S::E, K = S::K, PL = (E + 31) / 32;
+    int my = 0x7fffffff, rank = 0;
+    if (lane < K) {
+      my = sm.tk_id[0][lane];
+      if (my < 0 || my >= E) {
+        record_error(p, ERR_INDEX, c.sm, kNowhere, -1, (uint32_t)my, E);
+        my = 0;
+      }
+#pragma unroll
+      for (int i = 0; i < K; ++i) rank += sm.tk_id[0][i] < my ? 1 : 0;
+    }
+    const float v0 = key_value(sm.tk_key[0][0]);
+    const float ej = lane < K ? expf(key_value(sm.tk_key[0][lane < K ? lane : 0]) - v0) : 0.f;
+    const float z = warp_sum(ej);
+    if (lane < K) {
+      p.topk_ids[(int64_t)l * p.MB * K + lane] = my;
+      p.topk_w[(int64_t)l * p.MB * K + lane] = ej / z;
+      reinterpret_cast<int4*>(p.act)[rank] = make_int4(my, rank, 1, 0);
+      p.perm[rank] = lane;
+      p.inv[lane] = rank;
+      sm.ids[lane] = my;
+    }
+    if (lane == 0) *reinterpret_cast<int2*>(p.qlen) = make_int2(K, K);  // active experts, routed rows
+    __syncwarp();
+    if (lane == 0 && sig) red_release_add(sig, 1u);
+    // per-expert counts and offsets (outputs; nothing downstream waits on them)
+#pragma unroll
+    for (int k = 0; k < PL; ++k) {
+      const int e = lane + 32 * k;
+      int below = 0, chosen = 0;
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+        const int id = sm.tk_id[0][i];
+        below += id < e ? 1 : 0;
+        chosen += id == e ? 1 : 0;
+      }
+      if (e < E) {
+        p.ecount[(int64_t)l * E + e] = chosen;
+        p.eoff[e] = below;
+      }
+    }
+    if (lane == 0) p.eoff[E] = K;
   }
 
   // Per-expert counts and offsets, the expert-ordered row list (rows of an
