@@ -428,16 +428,21 @@ static int build(mk_sched* s) {
     add(w_fin);
     add(w_gather);
     add(w_qkv);
-    add(w_attn);
     switch (o.wave_order) {
       case MK_WAVES_INTERLEAVED:
-        add(w_up); add(w_dn); add(w_acomb); add(w_mcomb); add(w_o);
+        add(w_attn); add(w_up); add(w_dn); add(w_acomb); add(w_mcomb); add(w_o);
         break;
       case MK_WAVES_ATTN_FIRST:
-        add(w_acomb); add(w_o); add(w_up); add(w_dn); add(w_mcomb);
+        add(w_attn); add(w_acomb); add(w_o); add(w_up); add(w_dn); add(w_mcomb);
+        break;
+      case MK_WAVES_MOE_FIRST:
+        add(w_up); add(w_attn); add(w_acomb); add(w_dn); add(w_o); add(w_mcomb);
+        break;
+      case MK_WAVES_MOE_FIRST_O:
+        add(w_up); add(w_attn); add(w_acomb); add(w_o); add(w_dn); add(w_mcomb);
         break;
       default:
-        add(w_acomb); add(w_up); add(w_dn); add(w_o); add(w_mcomb);
+        add(w_attn); add(w_acomb); add(w_up); add(w_dn); add(w_o); add(w_mcomb);
         break;
     }
   }
@@ -820,7 +825,7 @@ int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const 
       return fail(MK_ERR_CUDA, "cannot query the SM count (no device?); pass opts.num_sms");
     }
   }
-  if (s->opts.wave_order < 0 || s->opts.wave_order > 2) {
+  if (s->opts.wave_order < 0 || s->opts.wave_order > 4) {
     delete s;
     return fail(MK_ERR_ARG, "unknown wave order");
   }
