@@ -115,6 +115,12 @@ typedef struct {
                                builds the MoE queue (no separate top-k task), and at batch <= 2
                                each router task computes the layer's RMSNorm itself instead of
                                waiting for it; needs fuse_finalize */
+  int32_t fuse_norm_qkv;    /* 1 (default) at batch <= 2: each QKV tile computes the layer's
+                               RMSNorm itself instead of waiting for a separate RMSNorm task */
+  int32_t combine_per_head; /* 1: when max_batch * n_kv * (n_q / n_kv) <= num_sms, one
+                               attention-combine task per (row, KV group, query head), each
+                               spread over the whole block; 0 (default): one per (row, KV
+                               group), a warp per head (fewer SMs held by merges) */
 } mk_sched_opts;
 
 /* Fills opts with the defaults (all zero except fuse_* = 1 and moe_static = 1). */

@@ -63,7 +63,8 @@ constexpr int32_t TGT_DYN_SPLITS = -2;
 // op-specific argument slots
 // RESID_NORM:   A0 b0, A1 b1 (row range), A2 final (1 = final norm before the LM head)
 //               A3 fused MoE combine of the previous layer
-// dense GEMV:   A0 row0, A1 n_rows, A2 KV group (O_PROJ split-K slice)
+// dense GEMV:   A0 row0, A1 n_rows, A2 KV group (O_PROJ split-K slice), A3 O_PROJ merges the
+//               group's slices itself, A7 QKV_PROJ computes the RMSNorm itself
 // ATTN_DECODE:  A0 b, A1 g, A2 slice index within the window, A3 counter base
 // ATTN_DRAIN:   A0 claim counter, A1 counter base, A2 QKV barrier base, A3 QKV target
 // ATTN_COMBINE: A0 b, A1 g, A2 counter base
@@ -179,7 +180,7 @@ struct Params {
   float* part_o;        // [MB][NKV][max_slots][G][D] unnormalised slice outputs
   float* part_ml;       // [MB][NKV][max_slots][G][2] slice max (log2 domain) and sum
   float* attn_out;      // [MB][NQ D]
-  float* opart;         // [NKV][MB][H] O-proj split-K partials
+  float* opart;         // [2][NKV][MB][H] O-proj split-K partials, by layer parity
   float* rlog;          // [L][MB][E] router logits
   int32_t* topk_ids;    // [L][MB][K]
   float* topk_w;        // [L][MB][K]

@@ -101,6 +101,21 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
   return v;
 }
+// Eight products of a weight chunk (8 bf16) with activations xa (elements
+// 0..3) and xb (4..7), fp32: even elements into a, odd into b.  Two fp32
+// FMAs per packed instruction (each rounded as fmaf).
+__device__ __forceinline__ void ffma2(float& a, float& b, float wa, float wb, float xa, float xb) {
+  asm("{\n .reg .b64 rw, rx, racc;\n mov.b64 rw, {%2, %3};\n mov.b64 rx, {%4, %5};\n mov.b64 racc, {%0, %1};\n"
+      " fma.rn.f32x2 racc, rw, rx, racc;\n mov.b64 {%0, %1}, racc;\n}"
+      : "+f"(a), "+f"(b)
+      : "f"(wa), "f"(wb), "f"(xa), "f"(xb));
+}
+__device__ __forceinline__ void dot8_bf16(uint4 u, uint4 xa, uint4 xb, float& a, float& b) {
+  ffma2(a, b, __uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(xa.x), __uint_as_float(xa.y));
+  ffma2(a, b, __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u), __uint_as_float(xa.z), __uint_as_float(xa.w));
+  ffma2(a, b, __uint_as_float(u.z << 16), __uint_as_float(u.z & 0xffff0000u), __uint_as_float(xb.x), __uint_as_float(xb.y));
+  ffma2(a, b, __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xffff0000u), __uint_as_float(xb.z), __uint_as_float(xb.w));
+}
 // 2-D TMA tile load (coordinates: x = element along the inner dimension, y = row).
 __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* b, uint64_t policy) {
   asm volatile(
@@ -274,6 +289,8 @@ struct Scratch {
   float am[S::G], al[S::G], aa[S::G];       // running max, sum, rescale per head
   float red[kConsumerWarps * 2];
   double rope_theta[S::D / 2];              // base^(-2i/D)
+  float2 rope_cs[kTB][S::D / 2];            // (cos, sin) of the step's rotation, rows < kTB
+  int32_t row_pos[kTB], row_page[kTB];      // the step's new position and its page, rows < kTB
   int32_t xtag[4], qtag[4];                 // what xs / qs hold
   int32_t flag;                             // a block-wide decision (the last router task)
   int32_t tk_id[kConsumerWarps][S::K];      // top-k of the row a warp works on
@@ -655,8 +672,9 @@ struct Producer {
         ++c.stat[3];
       }
     }
-    int cached_a = -1;
+    int cached_a = -1, dn_a = -1;
     int4 info = make_int4(0, 0, 0, 0);
+    int32_t dn_slot[kTB] = {}, dn_wt[kTB] = {};  // a down tile's rows: output slot and routing weight
     while (cur < total) {
       if (aborted(c)) return false;
       bool up;
@@ -707,6 +725,27 @@ struct Producer {
         it[F_TGT0] = U;
         it[F_SIG0] = -1;
         it[F_NSTAGE] = mp.dn_stages;
+        // at most kTB rows: each row's (row b, choice j) slot and weight travel
+        // with the item, so the epilogue waits on no load
+        if (nrows <= kTB) {
+          if (a != dn_a) {
+#pragma unroll
+            for (int t = 0; t < kTB; ++t) {
+              int ds = t < nrows ? __ldcg(p.perm + row0 + t) : 0;
+              if (ds < 0 || ds >= p.B * S::K) ds = 0;  // only after a failed step
+              dn_slot[t] = ds;
+            }
+#pragma unroll
+            for (int t = 0; t < kTB; ++t)
+              dn_wt[t] = t < nrows ? __float_as_int(__ldcg(p.topk_w + (int64_t)l * p.MB * S::K + dn_slot[t])) : 0;
+            dn_a = a;
+          }
+#pragma unroll
+          for (int t = 0; t < kTB; ++t) {
+            it[F_A0 + 8 + t] = dn_slot[t];
+            it[F_A0 + 10 + t] = dn_wt[t];
+          }
+        }
       }
       if (!push(it)) return false;
       const int64_t le = (int64_t)l * S::E + e;
@@ -997,7 +1036,7 @@ struct Consumer {
         for (int i = ct; i < tb * rows; i += kConsumerThreads) {
           const int t = i / rows, r = i - t * rows;
           const int n = w[F_A0] + s * S::SR_O + r, b = kTB * chunk + t;
-          p.opart[((int64_t)w[F_A0 + 2] * p.MB + b) * S::H + n] = out[t * kMaxStageRows + r];
+          p.opart[(((int64_t)(l & 1) * S::NKV + w[F_A0 + 2]) * p.MB + b) * S::H + n] = out[t * kMaxStageRows + r];
         }
         break;
       case W_UP_TILE: {
@@ -1065,22 +1104,20 @@ struct Consumer {
   // Pair epilogue, run by lane t for activation row t: v0, v1 are the dot
   // products of the pair's two weight rows r0, r1 (rows of stage s).
   __device__ __forceinline__ void pair_epilogue(int op, const int32_t* w, int s, int r0, int r1, int t, float v0,
-                                                float v1, int dslot, float dwt, int pos, int page) {
+                                                float v1, int dslot, float dwt) {
     const int l = w[F_LAYER];
     switch (op) {
       case OP_QKV_PROJ: {
         // RoPE in the epilogue, then the new K/V into the pool ("Tasks":
-        // QKV_PROJ applies RoPE in-register before writing back)
+        // QKV_PROJ applies RoPE in-register before writing back); the row's
+        // rotation by pos * base^(-dd/D) was tabulated for the step
         const int row = w[F_A0] + s * S::SR_H + r0;  // even: (row, row + 1) is a rotation pair
         const int b = t;
         const int head = row / S::D, dd = row - head * S::D;
+        const int pos = sm.row_pos[b], page = sm.row_page[b];
         if (head < S::NQ + S::NKV) {
-          // the angle pos * base^(-dd/D), reduced modulo 2 pi in double; sin/cos in float
-          const double ang = (double)pos * sm.rope_theta[dd / 2];
-          const double red = ang - 6.283185307179586 * rint(ang * 0.15915494309189535);
-          float s0, c0;
-          sincosf((float)red, &s0, &c0);
-          const float x0 = v0 * c0 - v1 * s0, x1 = v0 * s0 + v1 * c0;
+          const float2 cs = sm.rope_cs[b][dd / 2];
+          const float x0 = v0 * cs.x - v1 * cs.y, x1 = v0 * cs.y + v1 * cs.x;
           v0 = x0;
           v1 = x1;
         }
@@ -1121,7 +1158,8 @@ struct Consumer {
       }
       case OP_O_PROJ: {
         const int n = w[F_A0] + s * S::SR_O + r0;
-        *reinterpret_cast<float2*>(p.opart + ((int64_t)w[F_A0 + 2] * p.MB + t) * S::H + n) = make_float2(v0, v1);
+        *reinterpret_cast<float2*>(p.opart + (((int64_t)(l & 1) * S::NKV + w[F_A0 + 2]) * p.MB + t) * S::H + n) =
+            make_float2(v0, v1);
         break;
       }
       case W_DOWN_TILE: {  // weighted, into the (row b, slot j) of the output
@@ -1134,11 +1172,12 @@ struct Consumer {
   }
 
   // GEMV of at most kTB activation rows (decode at small batch).  The
-  // consumer warps form two teams of four that take alternate stages, so two
-  // stages are in process at once; within a stage each warp computes a pair
-  // of weight rows against the same activation loads and finishes the pair's
-  // epilogue itself (the RoPE pair for QKV, gate and up rows for the MoE
-  // up/gate), so a stage needs no block-wide barrier.
+  // consumer warps form four teams of two that take stages in turn, so four
+  // stages are in process at once; within a stage each warp takes half of
+  // the weight rows, two pairs at a time against the same activation loads,
+  // and finishes each pair's epilogue itself (the RoPE pair for QKV, gate and
+  // up rows for the MoE up/gate), so a stage needs no block-wide barrier.
+  // With one activation row the row lives in registers for the whole item.
   template <int K>
   __device__ __forceinline__ void gemv_item_teams(const int32_t* w, int SR, int total_rows, int ntok) {
     // one activation row is the decode case: its own instantiation, without
@@ -1146,6 +1185,12 @@ struct Consumer {
     if (ntok <= 1) gemv_item_teams_tb<K, 1>(w, SR, total_rows, ntok);
     else gemv_item_teams_tb<K, kTB>(w, SR, total_rows, ntok);
   }
+  static constexpr int kTeams = 4, kTeamWarps = kConsumerWarps / kTeams;
+#ifndef MK_XREGS
+#define MK_XREGS 0
+#endif
+  static constexpr bool kXRegs = MK_XREGS;
+  static_assert(kConsumerWarps % kTeams == 0 && F_A0 + 8 + 2 * kTB <= F_TASK, "teams; down-tile row fields");
   template <int K, int TB>
   __device__ __forceinline__ void gemv_item_teams_tb(const int32_t* w, int SR, int total_rows, int ntok) {
     constexpr int C = K / 8;
@@ -1153,19 +1198,13 @@ struct Consumer {
     const int op = w[F_OP];
     const int nst = w[F_NSTAGE];
     const int tb = ntok;
-    // epilogue inputs of lane t (activation row t), loaded before the stages
-    int dslot = 0, pos = -1, page = -1;
+    // epilogue inputs of lane t (activation row t), from the item (the
+    // producer read them when it made the down tile)
+    int dslot = 0;
     float dwt = 0.f;
-    if (lane < tb) {
-      if (op == W_DOWN_TILE) {
-        dslot = __ldcg(p.perm + w[F_A0 + 2] + lane);
-        if (dslot < 0 || dslot >= p.B * S::K) dslot = 0;  // only after a failed step
-        dwt = __ldcg(p.topk_w + (int64_t)w[F_LAYER] * p.MB * S::K + dslot);
-      } else if (op == OP_QKV_PROJ) {
-        pos = __ldg(p.seq_lens + lane) - 1;
-        const int lp = pos / S::P;
-        if (pos >= 0 && lp < p.max_pages) page = __ldg(p.block_tables + (int64_t)lane * p.max_pages + lp);
-      }
+    if (op == W_DOWN_TILE && lane < tb) {  // (constant indices: w stays in registers)
+      dslot = lane == 0 ? w[F_A0 + 8] : w[F_A0 + 9];
+      dwt = __int_as_float(lane == 0 ? w[F_A0 + 10] : w[F_A0 + 11]);
     }
     int32_t tag[4];
     x_tag(op, w, 0, tag);
@@ -1176,73 +1215,86 @@ struct Consumer {
         sm.xtag[0] = tag[0]; sm.xtag[1] = tag[1]; sm.xtag[2] = tag[2]; sm.xtag[3] = tag[3];
       }
     }
-    const int team = cw >> 2, tw = cw & 3;
+    const int team = cw / kTeamWarps, tw = cw % kTeamWarps;
     const bool up_pairs = op == W_UP_TILE;
+    // x row t as [half][chunk][4]: lane's chunk c = lane + 32 j holds elements
+    // 8c .. 8c+3 in half 0 and 8c+4 .. 8c+7 in half 1
     const uint32_t xs_a = smem_u32(sm.xs) + (uint32_t)lane * 16u;
-    for (int s = team; s < nst; s += 2) {
+    constexpr bool XR = TB == 1 && kXRegs;
+    uint4 xr[XR ? CPL : 1][2];
+    if (XR) {
+#pragma unroll
+      for (int j = 0; j < CPL; ++j)
+        if (C % 32 == 0 || lane + 32 * j < C) {
+          xr[j][0] = lds128(xs_a + (uint32_t)((32 * j) * 16));
+          xr[j][1] = lds128(xs_a + (uint32_t)((C + 32 * j) * 16));
+        }
+    }
+    for (int s = team; s < nst; s += kTeams) {
       const uint32_t gs = c.st + (uint32_t)s;
       const int slot = gs % kStages;
-      const bool ok = __all_sync(FULL, mbar_wait(p, c, &c.hdr->full[slot], (gs / kStages) & 1) && !aborted(c));
+      // The slot's previous use (stage s - kStages) may belong to another
+      // team (kStages is not a multiple of kTeams): wait until it is released
+      // first, so the parity wait below cannot match a phase two fills back.
+      bool ok = s < kStages || mbar_wait(p, c, &c.hdr->empty[slot], ((gs / kStages) - 1) & 1);
+      ok = __all_sync(FULL, ok && mbar_wait(p, c, &c.hdr->full[slot], (gs / kStages) & 1) && !aborted(c));
       const int rows = min(SR, total_rows - s * SR);
       const int npairs = rows / 2;
+      // this warp's pairs [p0, p1): the first half of the stage's pairs, or the second
+      const int per = (npairs + kTeamWarps - 1) / kTeamWarps;
+      const int p0 = tw * per, p1 = min(npairs, p0 + per);
       const uint32_t st_a = smem_u32(stage(slot)) + (uint32_t)lane * 16u;
       if (ok) {
-        for (int pr = tw; pr < npairs; pr += 4) {
-          const int r0 = up_pairs ? pr : 2 * pr;
-          const int r1 = up_pairs ? pr + npairs : 2 * pr + 1;
-          const uint32_t w0 = st_a + (uint32_t)(r0 * K * 2), w1 = st_a + (uint32_t)(r1 * K * 2);
-          float a0[TB], a1[TB], b0[TB], b1[TB];
+        for (int pr = p0; pr < p1; pr += 2) {
+          // pairs pr and pr + 1 (the second repeats the first when absent)
+          const int pq = pr + 1 < p1 ? pr + 1 : pr;
+          int rr[4];
+          rr[0] = up_pairs ? pr : 2 * pr;
+          rr[1] = up_pairs ? pr + npairs : 2 * pr + 1;
+          rr[2] = up_pairs ? pq : 2 * pq;
+          rr[3] = up_pairs ? pq + npairs : 2 * pq + 1;
+          // accumulators per row and activation row: even and odd elements
+          float acc[4][TB][2];
 #pragma unroll
-          for (int t = 0; t < TB; ++t) a0[t] = a1[t] = b0[t] = b1[t] = 0.f;
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int t = 0; t < TB; ++t) acc[q][t][0] = acc[q][t][1] = 0.f;
 #pragma unroll
           for (int j = 0; j < CPL; ++j) {
             if (C % 32 == 0 || lane + 32 * j < C) {
-              const uint4 u0 = lds128(w0 + j * 512), u1 = lds128(w1 + j * 512);
+              uint4 u[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) u[q] = lds128(st_a + (uint32_t)(rr[q] * K * 2 + j * 512));
 #pragma unroll
               for (int t = 0; t < TB; ++t)
                 if (TB == 1 || t < tb) {
-                  // x row t as [half][chunk][4]: chunk c's elements 0..3 and 4..7
-                  const uint4 xa4 = lds128(xs_a + (uint32_t)((t * 2 * C + 32 * j) * 16));
-                  const uint4 xb4 = lds128(xs_a + (uint32_t)((t * 2 * C + C + 32 * j) * 16));
-                  const float4 xa = make_float4(__uint_as_float(xa4.x), __uint_as_float(xa4.y),
-                                                __uint_as_float(xa4.z), __uint_as_float(xa4.w));
-                  const float4 xb = make_float4(__uint_as_float(xb4.x), __uint_as_float(xb4.y),
-                                                __uint_as_float(xb4.z), __uint_as_float(xb4.w));
-                  a0[t] = fmaf(bf16_lo(u0.x), xa.x, a0[t]);
-                  a1[t] = fmaf(bf16_hi(u0.x), xa.y, a1[t]);
-                  b0[t] = fmaf(bf16_lo(u1.x), xa.x, b0[t]);
-                  b1[t] = fmaf(bf16_hi(u1.x), xa.y, b1[t]);
-                  a0[t] = fmaf(bf16_lo(u0.y), xa.z, a0[t]);
-                  a1[t] = fmaf(bf16_hi(u0.y), xa.w, a1[t]);
-                  b0[t] = fmaf(bf16_lo(u1.y), xa.z, b0[t]);
-                  b1[t] = fmaf(bf16_hi(u1.y), xa.w, b1[t]);
-                  a0[t] = fmaf(bf16_lo(u0.z), xb.x, a0[t]);
-                  a1[t] = fmaf(bf16_hi(u0.z), xb.y, a1[t]);
-                  b0[t] = fmaf(bf16_lo(u1.z), xb.x, b0[t]);
-                  b1[t] = fmaf(bf16_hi(u1.z), xb.y, b1[t]);
-                  a0[t] = fmaf(bf16_lo(u0.w), xb.z, a0[t]);
-                  a1[t] = fmaf(bf16_hi(u0.w), xb.w, a1[t]);
-                  b0[t] = fmaf(bf16_lo(u1.w), xb.z, b0[t]);
-                  b1[t] = fmaf(bf16_hi(u1.w), xb.w, b1[t]);
+                  const uint4 xa = XR ? xr[XR ? j : 0][0] : lds128(xs_a + (uint32_t)((t * 2 * C + 32 * j) * 16));
+                  const uint4 xb = XR ? xr[XR ? j : 0][1] : lds128(xs_a + (uint32_t)((t * 2 * C + C + 32 * j) * 16));
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) dot8_bf16(u[q], xa, xb, acc[q][t][0], acc[q][t][1]);
                 }
             }
           }
-          float v0[TB], v1[TB];
+          float v[4][TB];
 #pragma unroll
-          for (int t = 0; t < TB; ++t)
-            if (TB == 1 || t < tb) {
-              v0[t] = warp_sum(a0[t] + a1[t]);
-              v1[t] = warp_sum(b0[t] + b1[t]);
-            }
-          // lane t finishes the pair for activation row t
-          const float e0 = (TB > 1 && lane == 1) ? v0[TB - 1] : v0[0];
-          const float e1 = (TB > 1 && lane == 1) ? v1[TB - 1] : v1[0];
-          if (lane < tb && !aborted(c)) pair_epilogue(op, w, s, r0, r1, lane, e0, e1, dslot, dwt, pos, page);
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int t = 0; t < TB; ++t)
+              if (TB == 1 || t < tb) v[q][t] = warp_sum(acc[q][t][0] + acc[q][t][1]);
+          // lane t finishes the pairs for activation row t
+          if (lane < tb && !aborted(c)) {
+            const bool r1 = TB > 1 && lane == 1;
+            pair_epilogue(op, w, s, rr[0], rr[1], lane, r1 ? v[0][TB - 1] : v[0][0], r1 ? v[1][TB - 1] : v[1][0],
+                          dslot, dwt);
+            if (pq != pr)
+              pair_epilogue(op, w, s, rr[2], rr[3], lane, r1 ? v[2][TB - 1] : v[2][0], r1 ? v[3][TB - 1] : v[3][0],
+                            dslot, dwt);
+          }
         }
       }
-      // the four warps of the team stand for the eight arrivals the stage expects
+      // the team's warps stand for the eight arrivals the stage expects
       __syncwarp();
-      if (lane == 0) mbar_arrive_n(&c.hdr->empty[slot], kConsumerWarps / 4);
+      if (lane == 0) mbar_arrive_n(&c.hdr->empty[slot], kConsumerWarps / kTeamWarps);
     }
     c.st += (uint32_t)nst;
   }
@@ -1424,10 +1476,85 @@ struct Consumer {
   __device__ __forceinline__ void attn_combine(const int32_t* w) {
     constexpr int G = S::G, D = S::D, DPL = D / 32;
     const int l = w[F_LAYER], b = w[F_A0], g = w[F_A0 + 1];
+    if (w[F_A0 + 3] >= 0) {
+      attn_combine_one_head(l, b, g, w[F_A0 + 3]);
+      return;
+    }
     if (b >= p.B || cw >= G) return;
+    float o[DPL];
+    combine_head(l, b, g, cw, o);
+    float* dst = p.attn_out + (int64_t)b * S::NQ * D + (int64_t)(g * G + cw) * D + lane * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) dst[i] = o[i];
+  }
+
+  // Head h of (b, g) by the whole block (few rows: the merge is on the path
+  // from the last KV slice to the O projection).  Warp w takes the slices
+  // w, w + 8, ..., so each lane has all its loads in flight at once; the
+  // eight partial sums meet in shared memory, added in warp order.
+  __device__ __forceinline__ void attn_combine_one_head(int l, int b, int g, int h) {
+    constexpr int G = S::G, D = S::D, DPL = D / 32;
+    static_assert(kConsumerWarps * D <= kTB * S::H, "the warps' partial sums fit the activation cache");
+    // the activation cache holds the partial sums below: mark it empty
+    // (read again only after the barrier that ends this item)
+    if (ct == 0) sm.xtag[0] = -1;
+    if (b >= p.B) return;
     const bool full = p.window == 0 || (l + 1) % p.full_period == 0;
     const int n = min(full ? slices_of(p, __ldg(p.seq_lens + b)) : p.n_static, p.max_slots);
-    const int h = cw;
+    const int64_t base = ((int64_t)b * S::NKV + g) * p.max_slots;
+    // the running max over every slice, by each warp (two loads per lane up to 64 slices)
+    float M = -INFINITY;
+    for (int j = lane; j < n; j += 32) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((base + j) * G + h) * 2));
+      if (ml.y > 0.f) M = fmaxf(M, ml.x);
+    }
+    M = warp_max(M);
+    float z = 0.f, acc[DPL];
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+#pragma unroll 4
+    for (int j = cw; j < n; j += kConsumerWarps) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((base + j) * G + h) * 2));
+      const float* oj = p.part_o + ((base + j) * G + h) * D + lane * DPL;
+      float o[DPL];
+      if (DPL == 4) {
+        const float4 o4 = __ldcg(reinterpret_cast<const float4*>(oj));
+        o[0] = o4.x; o[1 % DPL] = o4.y; o[2 % DPL] = o4.z; o[3 % DPL] = o4.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) o[i] = __ldcg(oj + i);
+      }
+      if (ml.y > 0.f) {
+        const float cj = exp2f(ml.x - M);
+        z = fmaf(cj, ml.y, z);
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[i] = fmaf(cj, o[i], acc[i]);
+      }
+    }
+    float* red = sm.xs;  // [warp][D]
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) red[cw * D + lane * DPL + i] = acc[i];
+    if (lane == 0) sm.red[cw] = z;
+    consumers_sync();
+    if (ct < D) {
+      float zt = 0.f, a = 0.f;
+#pragma unroll
+      for (int k = 0; k < kConsumerWarps; ++k) {
+        zt += sm.red[k];
+        a += red[k * D + ct];
+      }
+      p.attn_out[(int64_t)b * S::NQ * D + (int64_t)(g * G + h) * D + ct] = a / zt;
+    }
+  }
+
+  // Head h of (b, g) merged over the slices, by one warp: lane holds dims
+  // [lane * DPL, lane * DPL + DPL).
+  template <int DPL>
+  __device__ __forceinline__ void combine_head(int l, int b, int g, int h, float (&out)[DPL]) {
+    constexpr int G = S::G, D = S::D;
+    static_assert(DPL == D / 32, "lane dims");
+    const bool full = p.window == 0 || (l + 1) % p.full_period == 0;
+    const int n = min(full ? slices_of(p, __ldg(p.seq_lens + b)) : p.n_static, p.max_slots);
     const int64_t base = ((int64_t)b * S::NKV + g) * p.max_slots;
     float M = -INFINITY;
     for (int j = lane; j < n; j += 32) {
@@ -1467,9 +1594,8 @@ struct Consumer {
     }
     z = warp_sum(z);
     const float inv = 1.f / z;
-    float* dst = p.attn_out + (int64_t)b * S::NQ * D + (int64_t)(g * G + h) * D + lane * DPL;
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) dst[i] = acc[i] * inv;
+    for (int i = 0; i < DPL; ++i) out[i] = acc[i] * inv;
   }
 
   // ------------------------------------------------------------- norm
@@ -1515,7 +1641,8 @@ struct Consumer {
           parts[n++] = __ldcg(h4 + i4);
 #pragma unroll
           for (int g = 0; g < S::NKV; ++g)
-            parts[n++] = __ldcg(reinterpret_cast<const float4*>(p.opart + ((int64_t)g * p.MB + b) * S::H) + i4);
+            parts[n++] = __ldcg(
+                reinterpret_cast<const float4*>(p.opart + (((int64_t)((l + 1) & 1) * S::NKV + g) * p.MB + b) * S::H) + i4);
           if (fused) {
 #pragma unroll
             for (int j = 0; j < S::K; ++j)
@@ -1584,6 +1711,8 @@ struct Consumer {
   __device__ __forceinline__ void norm_into_cache(const int32_t* w) {
     constexpr int H4 = S::H / 4, PER = (H4 + kConsumerThreads - 1) / kConsumerThreads;
     const int l = w[F_LAYER];
+    // a previous item of this SM left the same rows (uniform, as for the combine)
+    if (sm.xtag[0] == 1 && sm.xtag[1] == 0 && sm.xtag[2] == 0 && sm.xtag[3] == l) return;
     float4* xs4 = reinterpret_cast<float4*>(sm.xs);
     for (int b = 0; b < p.B; ++b) {
       float4 v[PER];
@@ -1874,6 +2003,7 @@ struct Consumer {
         break;
       case OP_QKV_PROJ:
       case OP_LM_HEAD:
+        if (w[F_OP] == OP_QKV_PROJ && w[F_A0 + 7] && p.B <= kTB) norm_into_cache(w);
         if (p.B <= kTB) gemv_item_teams<S::H>(w, S::SR_H, w[F_A0 + 1], p.B);
         else gemv_item<S::H>(w, S::SR_H, w[F_A0 + 1], p.B);
         break;
@@ -1908,6 +2038,26 @@ struct Consumer {
       sm.rope_theta[i] = pow((double)p.rope_base, -(double)(2 * i) / (double)S::D);
     if (ct < 4) sm.xtag[ct] = sm.qtag[ct] = -1;
     consumers_sync();
+    // at batch <= kTB the rows' rotations and KV pages hold for every layer:
+    // computed once here, as the QKV epilogue would (angle reduced modulo
+    // 2 pi in double, then sin/cos in float)
+    if (p.B <= kTB) {
+      for (int i = ct; i < p.B * (S::D / 2); i += kConsumerThreads) {
+        const int b = i / (S::D / 2), k = i - b * (S::D / 2);
+        const int pos = __ldg(p.seq_lens + b) - 1;
+        const double ang = (double)pos * sm.rope_theta[k];
+        const double red = ang - 6.283185307179586 * rint(ang * 0.15915494309189535);
+        float s0, c0;
+        sincosf((float)red, &s0, &c0);
+        sm.rope_cs[b][k] = make_float2(c0, s0);
+        if (k == 0) {
+          const int lp = pos / S::P;
+          sm.row_pos[b] = pos;
+          sm.row_page[b] = (pos >= 0 && lp < p.max_pages) ? __ldg(p.block_tables + (int64_t)b * p.max_pages + lp) : -1;
+        }
+      }
+      consumers_sync();
+    }
     // thread 0 remembers a few counters it has already seen reach a count
     int cbar[4] = {-1, -1, -1, -1};
     uint32_t cval[4] = {0, 0, 0, 0};

@@ -191,11 +191,18 @@ static int build(mk_sched* s) {
     // K head or its V head), so the group's attention waits on its own tiles
     std::vector<Desc> w_qkv;
     lb.n_qkv_g.assign(NKV, 0);
+    const bool fuse_norm_qkv = o.fuse_norm_qkv && MB <= kTB;
     auto add_qkv = [&](int r0, int rows, int g) {
       Desc d = blank(OP_QKV_PROJ, l);
       d[F_A0] = r0;
       d[F_A0 + 1] = rows;
-      B.wait(d, 0, lb.norm, lb.n_norm);
+      if (fuse_norm_qkv) {  // the tile computes the RMSNorm: it waits for what the norm waits for
+        d[F_WAIT0] = w_norm[0][F_WAIT0]; d[F_TGT0] = w_norm[0][F_TGT0];
+        d[F_WAIT1] = w_norm[0][F_WAIT1]; d[F_TGT1] = w_norm[0][F_TGT1];
+        d[F_A0 + 7] = 1;
+      } else {
+        B.wait(d, 0, lb.norm, lb.n_norm);
+      }
       d[F_SIG0] = lb.qkv + g;
       lb.n_qkv_g[g]++;
       w_qkv.push_back(d);
@@ -344,19 +351,24 @@ static int build(mk_sched* s) {
     for (auto& d : w_attn)
       if (d[F_OP] == OP_ATTN_DRAIN) d[F_A0 + 3] = lb.n_qkv_g[0];
 
+    // one merge task per (row, group), or per (row, group, head) when there
+    // are few rows: the merge is on the way from the last slice to the O tiles
     std::vector<Desc> w_acomb;
     lb.n_acomb_g.assign(NKV, 0);
+    const int comb_heads = (o.combine_per_head && MB * NKV * G <= s->num_sms) ? G : 1;
     for (int b = 0; b < MB; ++b)
-      for (int g = 0; g < NKV; ++g) {
-        Desc d = blank(OP_ATTN_COMBINE, l);
-        d[F_A0] = b;
-        d[F_A0 + 1] = g;
-        d[F_A0 + 2] = lb.cnt;
-        B.wait(d, 0, lb.cnt + b * NKV + g, full ? TGT_DYN_SPLITS : s->n_static);
-        d[F_SIG0] = lb.acomb + g;
-        lb.n_acomb_g[g]++;
-        w_acomb.push_back(d);
-      }
+      for (int g = 0; g < NKV; ++g)
+        for (int h = 0; h < comb_heads; ++h) {
+          Desc d = blank(OP_ATTN_COMBINE, l);
+          d[F_A0] = b;
+          d[F_A0 + 1] = g;
+          d[F_A0 + 2] = lb.cnt;
+          d[F_A0 + 3] = comb_heads > 1 ? h : -1;
+          B.wait(d, 0, lb.cnt + b * NKV + g, full ? TGT_DYN_SPLITS : s->n_static);
+          d[F_SIG0] = lb.acomb + g;
+          lb.n_acomb_g[g]++;
+          w_acomb.push_back(d);
+        }
 
     // MoE claimers: separate up/gate and down drains as on the pages (default),
     // or one queue of up/gate and down tiles with each expert's down tiles one
@@ -483,7 +495,7 @@ static void layout_workspace(mk_sched* s) {
   w.add("part_o", sizeof(float) * (size_t)MB * D.NKV * s->max_slots * G * D.D);
   w.add("part_ml", sizeof(float) * (size_t)MB * D.NKV * s->max_slots * G * 2);
   w.add("attn_out", sizeof(float) * MB * D.NQ * D.D);
-  w.add("opart", sizeof(float) * (size_t)D.NKV * MB * D.H);
+  w.add("opart", sizeof(float) * 2 * (size_t)D.NKV * MB * D.H);  // by layer parity
   w.add("router_logits", sizeof(float) * (size_t)L * MB * D.E);
   w.add("topk_ids", sizeof(int32_t) * (size_t)L * MB * D.K);
   w.add("topk_w", sizeof(float) * (size_t)L * MB * D.K);
@@ -801,6 +813,8 @@ void mk_default_sched_opts(mk_sched_opts* o) {
   o->fuse_moe_combine = 1;
   o->moe_static = 1;
   o->fuse_routing = 1;
+  o->fuse_norm_qkv = 1;
+  o->combine_per_head = 0;
 }
 
 int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const mk_sched_opts* opts,

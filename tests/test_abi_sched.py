@@ -76,7 +76,8 @@ def test_schedules_validate_and_simulate(workload, order):
                                   dict(moe_queue=1), dict(moe_queue=1, moe_claimers=3),
                                   dict(moe_static=0), dict(moe_static=0, moe_claimers=5),
                                   dict(moe_queue=1, moe_static=0), dict(fuse_routing=0),
-                                  dict(fuse_routing=0, fuse_finalize=0)])
+                                  dict(fuse_routing=0, fuse_finalize=0), dict(fuse_norm_qkv=0),
+                                  dict(fuse_norm_qkv=0, fuse_routing=0), dict(combine_per_head=1)])
 def test_schedule_variants(opts):
     m, s, inp = sched_for("small", **opts)
     s.validate()
@@ -183,3 +184,26 @@ def test_rejects_bad_bucket():
     s = mk.Sched(m, 2, 64, mk.default_sched_opts(num_sms=NUM_SMS))
     with pytest.raises(mk.MkError):
         s.simulate([65])  # longer than the bucket
+
+
+@pytest.mark.parametrize("seq", [[8192, 3000], [8192], [1, 40000]])
+def test_two_row_schedule(seq):
+    """A schedule for at most two rows: the QKV tiles compute the RMSNorm
+    (they wait for what the RMSNorm waits for); one merge task per (row, KV
+    group), or per (row, KV group, head); a one-row step on it waits for no
+    slices of the absent row."""
+    w = synth.WORKLOADS["full_bs1_8k"]
+    sh = w.shape
+    G = sh.n_q // sh.n_kv
+    m = fake_model(sh)
+    for per_head in (0, 1):
+        s = mk.Sched(m, 2, 40000, mk.default_sched_opts(num_sms=NUM_SMS, combine_per_head=per_head))
+        s.validate()
+        tasks = [s.get_task(sm, i) for sm in range(s.num_sms) for i in range(s.num_tasks(sm))]
+        comb = [d for d in tasks if mk.OPS[int(d[mk.F_OP])] == "ATTN_COMBINE"]
+        assert len(comb) == sh.n_layers * 2 * sh.n_kv * (G if per_head else 1)
+        heads = sorted({int(d[mk.F_A0 + 3]) for d in comb})
+        assert heads == (list(range(G)) if per_head else [-1])
+        qkv = [d for d in tasks if mk.OPS[int(d[mk.F_OP])] == "QKV_PROJ"]
+        assert all(int(d[mk.F_A0 + 7]) == 1 for d in qkv)
+        s.simulate(np.asarray(seq, np.int32), seed=5)
