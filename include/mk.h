@@ -90,6 +90,7 @@ void mk_free_model(mk_model* m);
 #define MK_WAVES_ATTN_FIRST 2
 #define MK_WAVES_MOE_FIRST 3   /* up/gate tiles ahead of attention on each SM */
 #define MK_WAVES_MOE_FIRST_O 4 /* the same, with O-proj ahead of the down tiles */
+#define MK_WAVES_O_BEFORE_DOWN 5 /* attention, merge, up/gate, O-proj, then the down tiles */
 
 typedef struct {
   int32_t num_sms;          /* SMs to schedule for; 0 = the current device's count */

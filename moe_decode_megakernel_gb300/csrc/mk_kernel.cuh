@@ -400,6 +400,38 @@ static __device__ __forceinline__ bool wait_counter(const Params& p, Ctx& c, int
   }
 }
 
+// Two waits at once (either may be absent: bar < 0 or tgt 0): both counters
+// are read in every round.
+static __device__ __forceinline__ bool wait_counters(const Params& p, Ctx& c, int b0, uint32_t t0, int b1,
+                                                     uint32_t t1, ErrWhere at) {
+  const bool n0 = b0 >= 0 && t0 > 0, n1 = b1 >= 0 && t1 > 0;
+  if (!n0 && !n1) return true;
+  if (!n0) return wait_counter(p, c, b1, t1, at);
+  if (!n1) return wait_counter(p, c, b0, t0, at);
+  const uint32_t* a0 = p.bars + b0;
+  const uint32_t* a1 = p.bars + b1;
+  int64_t ts = 0;
+  for (uint32_t it = 0;; ++it) {
+    const uint32_t v0 = ld_acquire(a0), v1 = ld_acquire(a1);
+    if (v0 >= t0 && v1 >= t1) return true;
+    if (it == 0) ts = gtimer();
+    __nanosleep(20);
+    if ((it & 31u) == 31u) {
+      if (aborted(c)) return false;
+      if (ld_volatile(p.err) != 0) {
+        c.hdr->abort = 1;
+        return false;
+      }
+      if (gtimer() - ts > p.watchdog_ns) {
+        const bool first = v0 < t0;
+        record_error(p, ERR_TIMEOUT, c.sm, at, first ? b0 : b1, first ? v0 : v1, first ? t0 : t1);
+        c.hdr->abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 static __device__ __forceinline__ int slices_of(const Params& p, int seq) {
   return (seq + p.split_len - 1) / p.split_len;
 }
@@ -467,6 +499,16 @@ struct Producer {
     p.prog[c.sm * 8 + 4] = c.st;
     p.prog[c.sm * 8 + 5] = c.wk;
     return true;
+  }
+
+  // Waits until the consumers finished work item k of this SM (the storer
+  // handed its slot back).  k is the latest item pushed or an earlier one,
+  // so the slot's barrier is at most one phase short of it.
+  __device__ __forceinline__ bool item_finished(uint32_t k) {
+    const int64_t t0 = p.stats ? gtimer() : 0;
+    const bool ok = mbar_wait(p, c, &c.hdr->wempty[k % kWorkRing], (k / kWorkRing) & 1);
+    if (p.stats) c.stat[2] += gtimer() - t0;
+    return ok;
   }
 
   // rows [row0, row0+nrows) of a [rows][K] matrix (row stride `ld` elements),
@@ -586,6 +628,11 @@ struct Producer {
   // claims the next entry until the queue is empty).  The queue holds one
   // entry per (row b, KV group g, slice j), ordered (b, g, j); entry i is
   // located from the rows' slice counts, so the queue needs no storage.
+  // A claimer holds at most one slice beyond the one its consumers work on:
+  // after pushing slice i it claims the next slice only when the item before
+  // i is finished (its pages then load while i runs).  Run-ahead would leave
+  // the early claimers with a backlog of slices while the late ones find the
+  // queue empty.
   __device__ __forceinline__ bool attn_drain(const int32_t* d) {
     const int l = d[F_LAYER];
     uint32_t* claim = p.bars + d[F_A0];
@@ -603,8 +650,6 @@ struct Producer {
         acc += (uint32_t)n;
       }
       if (b >= p.B) break;  // queue exhausted
-      next = atomicAdd(claim, 1u);
-      ++c.stat[3];
       const int r = (int)(i - acc), per = n / S::NKV;
       const int g = r / per, j = r - g * per;
       if (j >= p.max_slots) {
@@ -615,6 +660,9 @@ struct Producer {
       const int t0 = j * p.split_len, t1 = min(s, t0 + p.split_len);
       if (!attn_item(d, l, b, g, t0, t1, j, d[F_A0 + 2] + g, d[F_A0 + 3], d[F_A0 + 1] + b * S::NKV + g))
         return false;
+      if (c.wk >= 2u && !item_finished(c.wk - 2u)) return false;
+      next = atomicAdd(claim, 1u);
+      ++c.stat[3];
     }
     return claim_end(d);
   }
@@ -645,8 +693,7 @@ struct Producer {
     // the routing decides which expert rows to stream: wait for the queue
     {
       const int64_t t0 = p.stats ? gtimer() : 0;
-      const bool ok = wait_counter(p, c, d[F_WAIT0], (uint32_t)d[F_TGT0], where_of(d)) &&
-                      wait_counter(p, c, d[F_WAIT1], (uint32_t)d[F_TGT1], where_of(d));
+      const bool ok = wait_counters(p, c, d[F_WAIT0], (uint32_t)d[F_TGT0], d[F_WAIT1], (uint32_t)d[F_TGT1], where_of(d));
       if (p.stats) c.stat[1] += gtimer() - t0;
       if (!ok) return false;
     }
@@ -672,6 +719,7 @@ struct Producer {
         ++c.stat[3];
       }
     }
+    bool carried = false;  // the last unit carried the drain's signal
     int cached_a = -1, dn_a = -1;
     int4 info = make_int4(0, 0, 0, 0);
     int32_t dn_slot[kTB] = {}, dn_wt[kTB] = {};  // a down tile's rows: output slot and routing weight
@@ -747,6 +795,18 @@ struct Producer {
           }
         }
       }
+      // A static claimer's last unit carries the drain's own completion
+      // signal (the storer publishes it after the tile): no claim-end item.
+      if (stat && nxt >= total) {
+        if (!up) {
+          it[F_SIG0] = d[F_SIG0];
+          it[F_SIG1] = d[F_SIG1];
+          carried = true;
+        } else if (d[F_SIG1] < 0) {
+          it[F_SIG1] = d[F_SIG0];
+          carried = true;
+        }
+      }
       if (!push(it)) return false;
       const int64_t le = (int64_t)l * S::E + e;
       if (up) {
@@ -775,7 +835,7 @@ struct Producer {
         }
       }
     }
-    return claim_end(d);
+    return carried || claim_end(d);
   }
 
   __device__ __forceinline__ bool passthrough(const int32_t* d) {
@@ -1489,11 +1549,12 @@ struct Consumer {
   }
 
   // Head h of (b, g) by the whole block (few rows: the merge is on the path
-  // from the last KV slice to the O projection).  Warp w takes the slices
-  // w, w + 8, ..., so each lane has all its loads in flight at once; the
-  // eight partial sums meet in shared memory, added in warp order.
+  // from the last KV slice to the O projection).  Warp w merges a contiguous
+  // block of the slices against its own running max, loading eight slices'
+  // (max, sum) and values at once, so a block costs one round trip; the
+  // eight partial merges meet in shared memory, taken in warp order.
   __device__ __forceinline__ void attn_combine_one_head(int l, int b, int g, int h) {
-    constexpr int G = S::G, D = S::D, DPL = D / 32;
+    constexpr int G = S::G, D = S::D, DPL = D / 32, J = 8;
     static_assert(kConsumerWarps * D <= kTB * S::H, "the warps' partial sums fit the activation cache");
     // the activation cache holds the partial sums below: mark it empty
     // (read again only after the barrier that ends this item)
@@ -1502,47 +1563,68 @@ struct Consumer {
     const bool full = p.window == 0 || (l + 1) % p.full_period == 0;
     const int n = min(full ? slices_of(p, __ldg(p.seq_lens + b)) : p.n_static, p.max_slots);
     const int64_t base = ((int64_t)b * S::NKV + g) * p.max_slots;
-    // the running max over every slice, by each warp (two loads per lane up to 64 slices)
-    float M = -INFINITY;
-    for (int j = lane; j < n; j += 32) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((base + j) * G + h) * 2));
-      if (ml.y > 0.f) M = fmaxf(M, ml.x);
-    }
-    M = warp_max(M);
-    float z = 0.f, acc[DPL];
+    const int per = (n + kConsumerWarps - 1) / kConsumerWarps;
+    const int j0 = cw * per, j1 = min(n, j0 + per);
+    float m = -INFINITY, z = 0.f, acc[DPL];
 #pragma unroll
     for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
-#pragma unroll 4
-    for (int j = cw; j < n; j += kConsumerWarps) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((base + j) * G + h) * 2));
-      const float* oj = p.part_o + ((base + j) * G + h) * D + lane * DPL;
-      float o[DPL];
-      if (DPL == 4) {
-        const float4 o4 = __ldcg(reinterpret_cast<const float4*>(oj));
-        o[0] = o4.x; o[1 % DPL] = o4.y; o[2 % DPL] = o4.z; o[3 % DPL] = o4.w;
-      } else {
+    for (int jb = j0; jb < j1; jb += J) {
+      float2 ml[J];
+      float o[J][DPL];
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) o[i] = __ldcg(oj + i);
-      }
-      if (ml.y > 0.f) {
-        const float cj = exp2f(ml.x - M);
-        z = fmaf(cj, ml.y, z);
+      for (int k = 0; k < J; ++k) {
+        const int j = min(jb + k, j1 - 1);  // past the block: a repeated load, not used
+        ml[k] = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((base + j) * G + h) * 2));
+        const float* oj = p.part_o + ((base + j) * G + h) * D + lane * DPL;
+        if (DPL == 4) {
+          const float4 o4 = __ldcg(reinterpret_cast<const float4*>(oj));
+          o[k][0] = o4.x; o[k][1 % DPL] = o4.y; o[k][2 % DPL] = o4.z; o[k][3 % DPL] = o4.w;
+        } else {
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) acc[i] = fmaf(cj, o[i], acc[i]);
+          for (int i = 0; i < DPL; ++i) o[k][i] = __ldcg(oj + i);
+        }
       }
+      float mb = m;
+#pragma unroll
+      for (int k = 0; k < J; ++k)
+        if (jb + k < j1 && ml[k].y > 0.f) mb = fmaxf(mb, ml[k].x);
+      if (mb > m) {  // rescale what the warp has so far to the new max
+        const float sc = exp2f(m - mb);
+        z *= sc;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[i] *= sc;
+        m = mb;
+      }
+#pragma unroll
+      for (int k = 0; k < J; ++k)
+        if (jb + k < j1 && ml[k].y > 0.f) {
+          const float cj = exp2f(ml[k].x - m);
+          z = fmaf(cj, ml[k].y, z);
+#pragma unroll
+          for (int i = 0; i < DPL; ++i) acc[i] = fmaf(cj, o[k][i], acc[i]);
+        }
     }
     float* red = sm.xs;  // [warp][D]
 #pragma unroll
     for (int i = 0; i < DPL; ++i) red[cw * D + lane * DPL + i] = acc[i];
-    if (lane == 0) sm.red[cw] = z;
+    if (lane == 0) {
+      sm.red[cw] = z;
+      sm.red[kConsumerWarps + cw] = m;
+    }
     consumers_sync();
     if (ct < D) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kConsumerWarps; ++k)
+        if (sm.red[k] > 0.f) M = fmaxf(M, sm.red[kConsumerWarps + k]);
       float zt = 0.f, a = 0.f;
 #pragma unroll
-      for (int k = 0; k < kConsumerWarps; ++k) {
-        zt += sm.red[k];
-        a += red[k * D + ct];
-      }
+      for (int k = 0; k < kConsumerWarps; ++k)
+        if (sm.red[k] > 0.f) {
+          const float sc = exp2f(sm.red[kConsumerWarps + k] - M);
+          zt = fmaf(sc, sm.red[k], zt);
+          a = fmaf(sc, red[k * D + ct], a);
+        }
       p.attn_out[(int64_t)b * S::NQ * D + (int64_t)(g * G + h) * D + ct] = a / zt;
     }
   }
@@ -2062,12 +2144,15 @@ struct Consumer {
     int cbar[4] = {-1, -1, -1, -1};
     uint32_t cval[4] = {0, 0, 0, 0};
     int crr = 0;
-    auto wait_cached = [&](int bar, uint32_t tgt, const int32_t* w) -> bool {
+    auto seen = [&](int bar, uint32_t tgt) -> bool {
       if (bar < 0 || tgt == 0) return true;
+      bool hit = false;
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (cbar[k] == bar && cval[k] >= tgt) return true;
-      if (!wait_counter(p, c, bar, tgt, where_of(w))) return false;
+      for (int k = 0; k < 4; ++k) hit |= cbar[k] == bar && cval[k] >= tgt;
+      return hit;
+    };
+    auto remember = [&](int bar, uint32_t tgt) {
+      if (bar < 0 || tgt == 0) return;
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         if (k == crr) {
@@ -2075,6 +2160,14 @@ struct Consumer {
           cval[k] = tgt;
         }
       crr = (crr + 1) & 3;
+    };
+    // an item's two waits, read together; counters seen complete are skipped
+    auto wait_cached = [&](int b0, uint32_t t0, int b1, uint32_t t1, const int32_t* w) -> bool {
+      const bool s0 = seen(b0, t0), s1 = seen(b1, t1);
+      if (s0 && s1) return true;
+      if (!wait_counters(p, c, s0 ? -1 : b0, t0, s1 ? -1 : b1, t1, where_of(w))) return false;
+      if (!s0) remember(b0, t0);
+      if (!s1) remember(b1, t1);
       return true;
     };
     uint32_t n_items = 0;
@@ -2084,6 +2177,14 @@ struct Consumer {
       int32_t w[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) w[k] = c.hdr->work[slot][k];
+      // a claim end is only a signal: each thread hands it on without the
+      // block barrier (every thread arrives after its earlier items, so the
+      // storer still publishes it after them); the decision is uniform
+      if (ok && w[F_OP] == W_CLAIM_END && w[F_SEQ] == (int32_t)c.wk && !aborted(c)) {
+        ++c.wk;
+        mbar_arrive(&c.hdr->done[slot]);
+        continue;
+      }
       const int64_t t_pop = (ct == 0 && (p.trace || p.stats)) ? gtimer() : 0;
       if (ct == 0) {
         p.prog[c.sm * 8 + 0] = n_items;
@@ -2095,7 +2196,7 @@ struct Consumer {
         const uint32_t tgt0 = (uint32_t)(w[F_TGT0] == TGT_DYN_SPLITS
                                              ? (w[F_A0] < p.B ? slices_of(p, __ldg(p.seq_lens + w[F_A0])) : 0)
                                              : w[F_TGT0]);
-        ok = wait_cached(w[F_WAIT0], tgt0, w) && wait_cached(w[F_WAIT1], (uint32_t)w[F_TGT1], w);
+        ok = wait_cached(w[F_WAIT0], tgt0, w[F_WAIT1], (uint32_t)w[F_TGT1], w);
       }
       if (ok && w[F_SEQ] != (int32_t)c.wk) {
         if (ct == 0) record_error(p, ERR_RING, c.sm, where_of(w), -2, (uint32_t)w[F_SEQ], c.wk);

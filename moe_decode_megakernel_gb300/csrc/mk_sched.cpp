@@ -453,6 +453,9 @@ static int build(mk_sched* s) {
       case MK_WAVES_MOE_FIRST_O:
         add(w_up); add(w_attn); add(w_acomb); add(w_o); add(w_dn); add(w_mcomb);
         break;
+      case MK_WAVES_O_BEFORE_DOWN:
+        add(w_attn); add(w_acomb); add(w_up); add(w_o); add(w_dn); add(w_mcomb);
+        break;
       default:
         add(w_attn); add(w_acomb); add(w_up); add(w_dn); add(w_o); add(w_mcomb);
         break;
@@ -839,7 +842,7 @@ int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const 
       return fail(MK_ERR_CUDA, "cannot query the SM count (no device?); pass opts.num_sms");
     }
   }
-  if (s->opts.wave_order < 0 || s->opts.wave_order > 4) {
+  if (s->opts.wave_order < 0 || s->opts.wave_order > 5) {
     delete s;
     return fail(MK_ERR_ARG, "unknown wave order");
   }
