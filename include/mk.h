@@ -118,6 +118,10 @@ typedef struct {
                                waiting for it; needs fuse_finalize */
   int32_t fuse_norm_qkv;    /* 1 (default) at batch <= 2: each QKV tile computes the layer's
                                RMSNorm itself instead of waiting for a separate RMSNorm task */
+  int32_t attn_static;      /* 1 (default): full-attention claimer i of n takes queue entries
+                               i, i + n, ... (no atomics; the claimers start together, after
+                               the QKV tiles); 0: each claims the next entry from a counter,
+                               at most one slice ahead of its running one */
   int32_t combine_per_head; /* 1: when max_batch * n_kv * (n_q / n_kv) <= num_sms, one
                                attention-combine task per (row, KV group, query head), each
                                spread over the whole block; 0 (default): one per (row, KV

@@ -66,7 +66,8 @@ constexpr int32_t TGT_DYN_SPLITS = -2;
 // dense GEMV:   A0 row0, A1 n_rows, A2 KV group (O_PROJ split-K slice), A3 O_PROJ merges the
 //               group's slices itself, A7 QKV_PROJ computes the RMSNorm itself
 // ATTN_DECODE:  A0 b, A1 g, A2 slice index within the window, A3 counter base
-// ATTN_DRAIN:   A0 claim counter, A1 counter base, A2 QKV barrier base, A3 QKV target
+// ATTN_DRAIN:   A0 claim counter, A1 counter base, A2 QKV barrier base, A3 QKV target,
+//               A4 static claimer index (-1: claims from the counter), A5 claimers
 // ATTN_COMBINE: A0 b, A1 g, A2 counter base
 // ROUTER_TOPK:  A0 b0, A1 b1, A2 1 = also finalize (single top-k task)
 // MOE_GATHER:   A0 row0, A1 n_rows

@@ -628,7 +628,7 @@ struct Producer {
   // claims the next entry until the queue is empty).  The queue holds one
   // entry per (row b, KV group g, slice j), ordered (b, g, j); entry i is
   // located from the rows' slice counts, so the queue needs no storage.
-  // A claimer holds at most one slice beyond the one its consumers work on:
+  // Dynamic claims: a claimer holds at most one slice beyond the one its consumers work on:
   // after pushing slice i it claims the next slice only when the item before
   // i is finished (its pages then load while i runs).  Run-ahead would leave
   // the early claimers with a backlog of slices while the late ones find the
@@ -636,8 +636,12 @@ struct Producer {
   __device__ __forceinline__ bool attn_drain(const int32_t* d) {
     const int l = d[F_LAYER];
     uint32_t* claim = p.bars + d[F_A0];
-    uint32_t next = atomicAdd(claim, 1u);
-    ++c.stat[3];
+    // static claims: claimer ci of n takes the entries ci, ci + n, ...
+    const int ci = d[F_A0 + 4];
+    const uint32_t n_cl = (uint32_t)d[F_A0 + 5];
+    const bool stat = ci >= 0;
+    uint32_t next = stat ? (uint32_t)ci : atomicAdd(claim, 1u);
+    if (!stat) ++c.stat[3];
     for (;;) {
       if (aborted(c)) return false;
       const uint32_t i = next;
@@ -660,9 +664,13 @@ struct Producer {
       const int t0 = j * p.split_len, t1 = min(s, t0 + p.split_len);
       if (!attn_item(d, l, b, g, t0, t1, j, d[F_A0 + 2] + g, d[F_A0 + 3], d[F_A0 + 1] + b * S::NKV + g))
         return false;
-      if (c.wk >= 2u && !item_finished(c.wk - 2u)) return false;
-      next = atomicAdd(claim, 1u);
-      ++c.stat[3];
+      if (stat) {
+        next = i + n_cl;
+      } else {
+        if (c.wk >= 2u && !item_finished(c.wk - 2u)) return false;
+        next = atomicAdd(claim, 1u);
+        ++c.stat[3];
+      }
     }
     return claim_end(d);
   }
