@@ -122,6 +122,10 @@ typedef struct {
                                i, i + n, ... (no atomics; the claimers start together, after
                                the QKV tiles); 0: each claims the next entry from a counter,
                                at most one slice ahead of its running one */
+  int32_t moe_balance;      /* 1 (with moe_static and separate up/down drains): the claimers'
+                               static ranks go to the SMs estimated to reach their claimer
+                               first, so the extra MoE tiles land there; 0 (default): rank =
+                               claimer index, down units shifted past the up units */
   int32_t combine_per_head; /* 1: when max_batch * n_kv * (n_q / n_kv) <= num_sms, one
                                attention-combine task per (row, KV group, query head), each
                                spread over the whole block; 0 (default): one per (row, KV

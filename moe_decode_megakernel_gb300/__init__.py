@@ -49,7 +49,8 @@ class MkSchedOpts(ctypes.Structure):
                                               "o_tile_rows", "lm_tile_rows", "fuse_finalize",
                                               "fuse_moe_combine", "explicit_gather",
                                               "trace_hidden", "watchdog_ms", "trace", "moe_queue", "moe_static",
-                                              "fuse_routing", "fuse_norm_qkv", "attn_static", "combine_per_head")]
+                                              "fuse_routing", "fuse_norm_qkv", "attn_static", "moe_balance",
+                                              "combine_per_head")]
 
 
 _lib = None

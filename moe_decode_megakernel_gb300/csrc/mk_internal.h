@@ -72,8 +72,9 @@ constexpr int32_t TGT_DYN_SPLITS = -2;
 // ROUTER_TOPK:  A0 b0, A1 b1, A2 1 = also finalize (single top-k task)
 // MOE_GATHER:   A0 row0, A1 n_rows
 // MOE_*_DRAIN:  A0 claim counter, A1 up barrier base (per expert), A2 explicit-gather barrier
-//               (or -1), A3 its target, A4 this claimer's index, A5 claimers, A6 queue mode
-//               (0 up and down tiles interleaved, 1 up tiles only)
+//               (or -1), A3 its target, A4 this claimer's index (or rank), A5 claimers, A6 queue
+//               mode (0 up and down tiles interleaved, 1 up tiles only), A7 static claims (0 no,
+//               1 by index with the down units shifted past the up units, 2 by host-set rank)
 // MOE_COMBINE:  A0 b0, A1 b1
 // W_ATTN:       A0 b, A1 g, A2 t0, A3 t1, A4 first page, A5 partial slot
 // W_UP_TILE / W_DOWN_TILE: A0 expert, A1 tile index, A2 row0, A3 n_rows

@@ -716,7 +716,7 @@ struct Producer {
     // static assignment: units cur, cur + n, ...; the down units start after
     // the last up unit, so the claimers with an extra up/gate tile get no
     // extra down tile
-    if (stat && mode == 2)
+    if (d[F_A0 + 7] == 1 && mode == 2)
       cur = (cur + n_claimers - ((uint32_t)n_act * U) % n_claimers) % n_claimers;
     uint32_t nxt = 0;
     if (cur < total) {

@@ -145,6 +145,76 @@ int auto_split_pages(const mk_sched* s) {
   return std::max(1, std::min(pages, 64));
 }
 
+// Static MoE claims by readiness: the claimer of rank r takes units r, r + n,
+// ..., so the lowest ranks get the extra units.  The ranks go to the SMs that
+// reach their claimer earliest, estimated by walking the layer's tasks in
+// list order (task k runs on SM k mod n) with each task starting no earlier
+// than its inputs are typically ready and taking its typical busy time (the
+// full shape's measured values, 0.1 us, from the layer's start); the up/gate
+// ranks first, then the down ranks with the up/gate units counted in.
+void balance_moe_ranks(mk_sched* s, std::vector<Desc>& all, size_t begin, int MB, bool full) {
+  const int n = s->num_sms;
+  const ShapeDims& D = s->dims;
+  const int U = s->plan.up_tiles, DN = s->plan.dn_tiles;
+  const int n_act = std::min(D.E, MB * D.K);  // fewest active experts: one row's K
+  const int64_t up_units = (int64_t)n_act * U, dn_units = (int64_t)n_act * DN;
+  const int64_t attn_entries = (int64_t)MB * D.NKV * ((s->max_ctx + s->split_len - 1) / s->split_len);
+  std::vector<int> up_rank(n, -1), dn_rank(n, -1);
+  std::vector<int64_t> at_up(n, 0), at_dn(n, 0);
+  std::vector<size_t> up_at(n, SIZE_MAX), dn_at(n, SIZE_MAX);
+  auto units_of = [](int r, int64_t units, int nc) -> int64_t { return r < units ? (units - r + nc - 1) / nc : 0; };
+  auto walk = [&]() {
+    std::vector<int64_t> t(n, 0);
+    for (size_t k = begin; k < all.size(); ++k) {
+      const Desc& d = all[k];
+      const int sm = (int)(k % (size_t)n);
+      int64_t earliest = 0, dur = 0;
+      switch (d[F_OP]) {
+        case OP_RESID_NORM: dur = 24; break;
+        case OP_ROUTER_GEMM: dur = 60; break;
+        case OP_QKV_PROJ: dur = 55; break;
+        case OP_ATTN_DECODE: earliest = 75; dur = 56; break;
+        case OP_ATTN_DRAIN: {
+          const int64_t ci = d[F_A0 + 4], nc = std::max(1, d[F_A0 + 5]);
+          earliest = 75;
+          dur = 64 * (ci >= 0 ? units_of((int)ci, attn_entries, (int)nc) : (attn_entries + nc - 1) / nc);
+          break;
+        }
+        case OP_ATTN_COMBINE: earliest = full ? 155 : 145; dur = 50; break;
+        case OP_O_PROJ: earliest = 215; dur = 25; break;
+        case OP_MOE_UPGATE_ACT_DRAIN:
+          up_at[sm] = k;
+          at_up[sm] = std::max(t[sm], (int64_t)90);
+          t[sm] = at_up[sm] + (up_rank[sm] >= 0 ? 60 * units_of(up_rank[sm], up_units, n) : 0);
+          continue;
+        case OP_MOE_DOWN_DRAIN:
+          dn_at[sm] = k;
+          at_dn[sm] = std::max(t[sm], (int64_t)190);
+          t[sm] = at_dn[sm] + (dn_rank[sm] >= 0 ? 23 * units_of(dn_rank[sm], dn_units, n) : 0);
+          continue;
+        default: break;
+      }
+      t[sm] = std::max(t[sm], earliest) + dur;
+    }
+  };
+  auto rank = [&](std::vector<size_t>& at, std::vector<int64_t>& when, std::vector<int>& out) {
+    std::vector<int> order;
+    for (int sm = 0; sm < n; ++sm)
+      if (at[sm] != SIZE_MAX) order.push_back(sm);
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return when[a] < when[b]; });
+    for (int r = 0; r < (int)order.size(); ++r) {
+      Desc& d = all[at[order[r]]];
+      d[F_A0 + 4] = r;
+      d[F_A0 + 7] = 2;  // static by rank, no shift of the down units
+      out[order[r]] = r;
+    }
+  };
+  walk();
+  rank(up_at, at_up, up_rank);
+  walk();
+  rank(dn_at, at_dn, dn_rank);
+}
+
 }  // namespace
 
 static int build(mk_sched* s) {
@@ -435,6 +505,7 @@ static int build(mk_sched* s) {
     lb.n_o = (int)w_o.size();
 
     auto add = [&](std::vector<Desc>& w) { all.insert(all.end(), w.begin(), w.end()); };
+    const size_t layer_begin = all.size();
     // the router and the routing head each layer's list: the MoE branch waits on
     // them, and QKV tiles would otherwise sit in front of them on their SMs
     add(w_norm);
@@ -463,6 +534,7 @@ static int build(mk_sched* s) {
         add(w_attn); add(w_acomb); add(w_up); add(w_dn); add(w_o); add(w_mcomb);
         break;
     }
+    if (o.moe_static && o.moe_balance && !unified) balance_moe_ranks(s, all, layer_begin, MB, full);
   }
   // final RMSNorm and LM head
   std::vector<Desc> w_final = B.norm_wave(L, norm_rows);
@@ -772,7 +844,7 @@ struct Sim {
             i = d[F_A0 + 4];
             // static down units start where the up units left off, so the
             // claimers with an extra up/gate tile get no extra down tile
-            if (d[F_A0 + 7] && mode == 2) i = (i + n - (int64_t)up_q[l].size() % n) % n;
+            if (d[F_A0 + 7] == 1 && mode == 2) i = (i + n - (int64_t)up_q[l].size() % n) % n;
             first_done[sm] = 1;
           } else {
             i = d[F_A0 + 7] ? last_unit[sm] + n : n + bars[claim]++;
@@ -829,6 +901,7 @@ void mk_default_sched_opts(mk_sched_opts* o) {
   o->fuse_routing = 1;
   o->fuse_norm_qkv = 1;
   o->attn_static = 1;
+  o->moe_balance = 0;
   o->combine_per_head = 0;
 }
 
