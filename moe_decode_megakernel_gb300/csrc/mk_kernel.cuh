@@ -1385,8 +1385,8 @@ struct Consumer {
     constexpr int G = S::G, D = S::D, P = S::P, KS = D / 16, NT = D / 64;
     const int l = w[F_LAYER], b = w[F_A0], g = w[F_A0 + 1], t0 = w[F_A0 + 2], t1 = w[F_A0 + 3];
     const int pf = w[F_A0 + 4], slot_idx = w[F_A0 + 5], np = w[F_NSTAGE];
-    const int s = b < p.B ? __ldg(p.seq_lens + b) : 0;
-    const int pos = s - 1;
+    // the row's new position (tabulated for the step at batch <= kTB)
+    const int pos = b < p.B ? (p.B <= kTB ? sm.row_pos[b] : __ldg(p.seq_lens + b) - 1) : -1;
     const int qg = lane >> 2, qc = lane & 3;  // MMA fragment coordinates
     // the group's queries, scaled by log2(e)/sqrt(D), split into BF16 hi + lo,
     // kept while (layer, b, g) repeats
@@ -1437,21 +1437,24 @@ struct Consumer {
         }
         consumers_sync();
       }
-      // S = Q K^T for this warp's 8 tokens
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      // S = Q K^T for this warp's 8 tokens: Q's BF16 hi part in rows 0-7 of
+      // the MMA and its lo part in rows 8-15 (one MMA takes both), even and
+      // odd k-steps in separate accumulators (half the dependent chain)
+      float sc[2] = {0.f, 0.f};
       if (ok && qk_warp) {
         const int tr = cw * 8 + (lane & 7);
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int ks = 0; ks < KS; ks += 2) {
           uint32_t b0, b1, b2, b3, h0, h1, h2, h3, l0, l1, l2, l3;
           ldsm_x4(kv_addr(kb, tr, 2 * ks + (lane >> 3)), b0, b1, b2, b3);
           ldsm_x4(qh_a + ks * 32, h0, h1, h2, h3);
           ldsm_x4(ql_a + ks * 32, l0, l1, l2, l3);
-          mma_bf16(sc, h0, 0u, h1, 0u, b0, b1);
-          mma_bf16(sc, l0, 0u, l1, 0u, b0, b1);
-          mma_bf16(sc, h2, 0u, h3, 0u, b2, b3);
-          mma_bf16(sc, l2, 0u, l3, 0u, b2, b3);
+          mma_bf16(sa, h0, l0, h1, l1, b0, b1);
+          mma_bf16(sb, h2, l2, h3, l3, b2, b3);
         }
+        sc[0] = (sa[0] + sa[2]) + (sb[0] + sb[2]);
+        sc[1] = (sa[1] + sa[3]) + (sb[1] + sb[3]);
       }
       // this thread: head qg, tokens cw*8 + 2qc, +1
       const int tk = page_t0 + cw * 8 + 2 * qc;
@@ -1494,6 +1497,8 @@ struct Consumer {
         for (int n = 0; n < NT; ++n) {
           o[n][0] *= alpha;
           o[n][1] *= alpha;
+          o[n][2] *= alpha;
+          o[n][3] *= alpha;
         }
 #pragma unroll
         for (int kt = 0; kt < P / 16; ++kt) {
@@ -1505,18 +1510,16 @@ struct Consumer {
             al2 = *reinterpret_cast<const uint32_t*>(&sm.pl[qg][kt * 16 + 8 + 2 * qc]);
           }
           const int tr = kt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+          // P's hi part in rows 0-7, its lo part in rows 8-15 (summed at the end)
           if (NT == 2) {
             uint32_t b0, b1, b2, b3;
             ldsm_x4_t(kv_addr(vb, tr, 2 * cw + (lane >> 4)), b0, b1, b2, b3);
-            mma_bf16(o[0], ah0, 0u, ah2, 0u, b0, b1);
-            mma_bf16(o[0], al0, 0u, al2, 0u, b0, b1);
-            mma_bf16(o[1], ah0, 0u, ah2, 0u, b2, b3);
-            mma_bf16(o[1], al0, 0u, al2, 0u, b2, b3);
+            mma_bf16(o[0], ah0, al0, ah2, al2, b0, b1);
+            mma_bf16(o[1], ah0, al0, ah2, al2, b2, b3);
           } else {
             uint32_t b0, b1;
             ldsm_x2_t(kv_addr(vb, tr, cw), b0, b1);
-            mma_bf16(o[0], ah0, 0u, ah2, 0u, b0, b1);
-            mma_bf16(o[0], al0, 0u, al2, 0u, b0, b1);
+            mma_bf16(o[0], ah0, al0, ah2, al2, b0, b1);
           }
         }
       }
@@ -1529,7 +1532,8 @@ struct Consumer {
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
         const int dcol = (NT * cw + n) * 8 + 2 * qc;
-        *reinterpret_cast<float2*>(p.part_o + (base * G + qg) * D + dcol) = make_float2(o[n][0], o[n][1]);
+        *reinterpret_cast<float2*>(p.part_o + (base * G + qg) * D + dcol) =
+            make_float2(o[n][0] + o[n][2], o[n][1] + o[n][3]);
       }
     }
     if (ct < G) {

@@ -243,7 +243,10 @@ static int build(mk_sched* s) {
   if (D.D % qkv_tile != 0 || qkv_tile % sr_h != 0 || D.D % sr_h != 0)
     return fail(MK_ERR_ARG, "qkv_tile_rows must divide head_dim and be a multiple of the stage rows");
   const int o_tile = o.o_tile_rows > 0 ? round_to(o.o_tile_rows, sr_o) : round_to(64, sr_o);
-  const int lm_tile = o.lm_tile_rows > 0 ? round_to(o.lm_tile_rows, sr_h) : round_to(128, sr_h);
+  // LM head: one tile per SM by default (the vocabulary split evenly in stage rows), so the
+  // last wave of the step has no tail of SMs with one tile more than the others
+  const int lm_even = ((c.vocab + s->num_sms - 1) / s->num_sms + sr_h - 1) / sr_h * sr_h;
+  const int lm_tile = o.lm_tile_rows > 0 ? round_to(o.lm_tile_rows, sr_h) : std::max(sr_h, lm_even);
   const int router_tile = sr_h * std::max(1, 16 / sr_h);
   const int n_moe = o.moe_claimers > 0 ? o.moe_claimers : s->num_sms;
   const int attn_claim_default = std::min(s->num_sms, std::max(1, MB * NKV * full_slices));
