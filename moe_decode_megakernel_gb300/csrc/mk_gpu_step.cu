@@ -1,0 +1,179 @@
+// mk_gpu_step.cu -- the decode service's step on the GPU: the host arrays
+// to the device, mk_decode_step with the smallest schedule that covers the
+// batch, a greedy argmax per row on the device, the tokens back.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cfloat>
+#include <string>
+#include <vector>
+
+#include "../../include/mk_service.h"
+#include "mk_host.h"
+
+using mk::fail;
+
+namespace {
+
+constexpr int kArgmaxThreads = 512;
+
+// One block per row: each thread scans a strided part of the row; the
+// (value, index) pairs meet by warp shuffles, then across warps in shared
+// memory.  Ties go to the lower index; NaN compares false, so it never wins.
+__global__ void __launch_bounds__(kArgmaxThreads) argmax_rows(const float* __restrict__ logits, int vocab,
+                                                                int32_t* __restrict__ next) {
+  const float* row = logits + (size_t)blockIdx.x * vocab;
+  float best = -FLT_MAX;
+  int idx = vocab;  // "none yet": any real index is lower
+  for (int i = threadIdx.x; i < vocab; i += blockDim.x) {
+    const float v = row[i];
+    if (v > best || (v == best && i < idx)) {
+      best = v;
+      idx = i;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+    if (b2 > best || (b2 == best && i2 < idx)) {
+      best = b2;
+      idx = i2;
+    }
+  }
+  __shared__ float wb[kArgmaxThreads / 32];
+  __shared__ int wi[kArgmaxThreads / 32];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    wb[w] = best;
+    wi[w] = idx;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int k = 1; k < (int)(blockDim.x >> 5); ++k)
+      if (wb[k] > best || (wb[k] == best && wi[k] < idx)) {
+        best = wb[k];
+        idx = wi[k];
+      }
+    next[blockIdx.x] = idx < vocab ? idx : 0;  // every value NaN: token 0
+  }
+}
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+}  // namespace
+
+struct mk_gpu_step {
+  mk_model* model = nullptr;
+  std::vector<mk_sched*> scheds;
+  void* k_pool = nullptr;
+  void* v_pool = nullptr;
+  int64_t num_pages = 0;
+  int32_t max_pages = 0, max_batch = 0;
+  void* workspace = nullptr;
+  size_t ws_bytes = 0;
+  cudaStream_t stream = nullptr;
+  // device parts of dev_buf
+  int32_t* d_tok = nullptr;
+  int32_t* d_len = nullptr;
+  int32_t* d_bt = nullptr;
+  float* d_logits = nullptr;
+  int32_t* d_next = nullptr;
+};
+
+extern "C" {
+
+int mk_argmax_rows(const float* logits, int32_t rows, int32_t vocab, int32_t* next, void* stream) {
+  if (!logits || !next || rows < 0 || vocab < 1) return fail(MK_ERR_ARG, "bad argmax arguments");
+  if (rows == 0) return MK_OK;
+  argmax_rows<<<rows, kArgmaxThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(logits, vocab, next);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MK_ERR_CUDA, std::string("argmax launch: ") + cudaGetErrorString(e));
+  return MK_OK;
+}
+
+size_t mk_gpu_step_dev_bytes(const mk_model* m, int32_t max_batch, int32_t max_pages) {
+  if (!m || max_batch < 1 || max_pages < 1) return 0;
+  const size_t B = (size_t)max_batch;
+  return 3 * align256(sizeof(int32_t) * B) + align256(sizeof(int32_t) * B * max_pages) +
+         align256(sizeof(float) * B * m->cfg.vocab);
+}
+
+int mk_gpu_step_create(mk_model* m, mk_sched* const* scheds, int32_t n_scheds, void* k_pool, void* v_pool,
+                       int64_t num_pages, int32_t max_pages, void* workspace, size_t workspace_bytes,
+                       void* dev_buf, size_t dev_bytes, void* stream, mk_gpu_step** out) {
+  if (!m || !scheds || n_scheds < 1 || !k_pool || !v_pool || !workspace || !dev_buf || !out)
+    return fail(MK_ERR_ARG, "null argument");
+  *out = nullptr;
+  if (num_pages < 1 || max_pages < 1) return fail(MK_ERR_ARG, "num_pages and max_pages must be positive");
+  int32_t mb = 0;
+  for (int32_t i = 0; i < n_scheds; ++i) {
+    if (!scheds[i] || !scheds[i]->sched_dev) return fail(MK_ERR_ARG, "schedule " + std::to_string(i) + " not uploaded");
+    if (mk_workspace_bytes(scheds[i]) > workspace_bytes)
+      return fail(MK_ERR_ARG, "workspace smaller than schedule " + std::to_string(i) + " needs");
+    mb = std::max(mb, (int32_t)scheds[i]->max_batch);
+  }
+  const size_t need = mk_gpu_step_dev_bytes(m, mb, max_pages);
+  if (dev_bytes < need) return fail(MK_ERR_ARG, "dev_buf holds " + std::to_string(dev_bytes) + " bytes, " +
+                                                    std::to_string(need) + " needed");
+  mk_gpu_step* g = new mk_gpu_step;
+  g->model = m;
+  g->scheds.assign(scheds, scheds + n_scheds);
+  g->k_pool = k_pool;
+  g->v_pool = v_pool;
+  g->num_pages = num_pages;
+  g->max_pages = max_pages;
+  g->max_batch = mb;
+  g->workspace = workspace;
+  g->ws_bytes = workspace_bytes;
+  g->stream = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* b = static_cast<uint8_t*>(dev_buf);
+  const size_t B = (size_t)mb;
+  g->d_tok = reinterpret_cast<int32_t*>(b);
+  b += align256(sizeof(int32_t) * B);
+  g->d_len = reinterpret_cast<int32_t*>(b);
+  b += align256(sizeof(int32_t) * B);
+  g->d_next = reinterpret_cast<int32_t*>(b);
+  b += align256(sizeof(int32_t) * B);
+  g->d_bt = reinterpret_cast<int32_t*>(b);
+  b += align256(sizeof(int32_t) * B * max_pages);
+  g->d_logits = reinterpret_cast<float*>(b);
+  *out = g;
+  return MK_OK;
+}
+
+void mk_gpu_step_free(mk_gpu_step* g) { delete g; }
+
+int mk_gpu_step_run(void* ctx, const int32_t* last_tokens, const int32_t* seq_lens, const int32_t* block_tables,
+                    int32_t batch, int32_t max_pages, int32_t* next_tokens) {
+  mk_gpu_step* g = static_cast<mk_gpu_step*>(ctx);
+  if (!g || !last_tokens || !seq_lens || !block_tables || !next_tokens) return fail(MK_ERR_ARG, "null argument");
+  if (batch < 1 || batch > g->max_batch || max_pages != g->max_pages)
+    return fail(MK_ERR_ARG, "batch or block-table width outside what the GPU step was made for");
+  int32_t longest = 0;
+  for (int32_t r = 0; r < batch; ++r) longest = std::max(longest, seq_lens[r]);
+  mk_sched* s = nullptr;
+  for (mk_sched* c : g->scheds)
+    if (c->max_batch >= batch && c->max_ctx >= longest) {
+      s = c;
+      break;
+    }
+  if (!s) return fail(MK_ERR_ARG, "no schedule covers batch " + std::to_string(batch) + " at context " +
+                                      std::to_string(longest));
+  cudaStream_t st = g->stream;
+  const size_t B = (size_t)batch;
+  cudaError_t e = cudaMemcpyAsync(g->d_tok, last_tokens, sizeof(int32_t) * B, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(g->d_len, seq_lens, sizeof(int32_t) * B, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(g->d_bt, block_tables, sizeof(int32_t) * B * max_pages, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return fail(MK_ERR_CUDA, std::string("step inputs: ") + cudaGetErrorString(e));
+  int rc = mk_decode_step(g->model, s, g->d_tok, g->d_len, g->d_bt, batch, max_pages, g->k_pool, g->v_pool,
+                          g->num_pages, g->workspace, g->ws_bytes, g->d_logits, st);
+  if (rc != MK_OK) return rc;
+  rc = mk_argmax_rows(g->d_logits, batch, g->model->cfg.vocab, g->d_next, st);
+  if (rc != MK_OK) return rc;
+  e = cudaMemcpyAsync(next_tokens, g->d_next, sizeof(int32_t) * B, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return fail(MK_ERR_CUDA, std::string("step outputs: ") + cudaGetErrorString(e));
+  return mk_check_step(s, g->workspace, st);  // waits for the stream
+}
+
+}  // extern "C"

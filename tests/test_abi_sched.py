@@ -22,14 +22,18 @@ def built():
 
 
 def declared_functions():
-    src = open(os.path.join(ROOT, "include", "mk.h")).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(mk_\w+)\s*\(", src)))
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for h in sorted(os.listdir(inc)):
+        if h.endswith(".h"):
+            src = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, h)).read(), flags=re.S)
+            names |= set(re.findall(r"\b(mk_\w+)\s*\(", src))
+    return sorted(names)
 
 
 def test_exports_every_declared_symbol():
     names = declared_functions()
-    assert len(names) >= 19
+    assert len(names) >= 19 + 19 and "mk_service_step" in names and "mk_gpu_step_run" in names
     L = mk.lib()
     for n in names:
         assert hasattr(L, n), n

@@ -1,0 +1,140 @@
+"""The decode service with the GPU step (mk_gpu_step: mk_decode_step plus
+the library's argmax) on the tiny model: prompts fed token by token, greedy
+samples, two sequences batched -- against one-sequence-at-a-time loops of
+mk_decode_step and torch.argmax over the same positions and pages.
+
+"Cohere: a serving engine for North Mini Code built around a decode
+megakernel", section "The inference engine around the kernel"."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+import synth.device
+import moe_decode_megakernel_gb300 as mk
+from moe_decode_megakernel_gb300 import service as sv
+
+pytestmark = pytest.mark.gpu
+
+SH = synth.MODELS["tiny"]
+SEED = 31
+NUM_PAGES = 24
+MAX_PAGES = 8
+
+
+def _model():
+    w = synth.device.device_weights(SH, SEED)
+    return mk.Model(mk.config_from(SH), mk.weights_from(w), keepalive=w)
+
+
+def _manual(model, prompt, n_new, pages):
+    """One sequence through Session.step: feed the prompt, then the samples."""
+    kp, vp = synth.device.device_pools(SH, SEED, NUM_PAGES)
+    sched = mk.Sched(model, 1, MAX_PAGES * SH.page_size)
+    sess = mk.Session(model, sched)
+    bt = torch.full((1, MAX_PAGES), -1, dtype=torch.int32, device="cuda")
+    logits = torch.empty(1, SH.vocab, device="cuda")
+    feed, out, n_ctx = list(prompt), [], 0
+    while len(out) < n_new:
+        tok = feed.pop(0)
+        bt[0, n_ctx // SH.page_size] = pages[n_ctx // SH.page_size]
+        sess.step(torch.tensor([tok], dtype=torch.int32, device="cuda"),
+                  torch.tensor([n_ctx + 1], dtype=torch.int32, device="cuda"), bt, kp, vp, logits)
+        sess.check()
+        n_ctx += 1
+        if not feed:
+            t = int(torch.argmax(logits[0]).item())
+            out.append(t)
+            feed.append(t)
+    return out
+
+
+def test_argmax_rows_ties_and_nan():
+    g = torch.Generator(device="cuda").manual_seed(3)
+    x = torch.randn(5, 1000, device="cuda", generator=g)
+    x[1, 10] = x[1, 900] = 50.0  # a tie: the lower index wins
+    x[2, :] = float("nan")
+    x[2, 17] = 1.0  # NaN never wins
+    x[3, :] = -3.0  # all equal: index 0
+    nxt = torch.empty(5, dtype=torch.int32, device="cuda")
+    sv.argmax_rows(x, nxt, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    ref = torch.argmax(torch.nan_to_num(x, nan=-float("inf")), dim=1).to(torch.int32)
+    assert nxt.tolist() == ref.tolist()
+    assert nxt[1].item() == 10 and nxt[2].item() == 17 and nxt[3].item() == 0
+
+
+def test_service_matches_single_sequence_loops():
+    model = _model()
+    kp, vp = synth.device.device_pools(SH, SEED, NUM_PAGES)
+    ctx = MAX_PAGES * SH.page_size
+    scheds = [mk.Sched(model, 1, ctx), mk.Sched(model, 2, ctx)]
+    gstep = sv.GpuStep(model, scheds, kp, vp, MAX_PAGES)
+    svc = sv.Service(NUM_PAGES, SH.page_size, MAX_PAGES, 2, gstep)
+    rng = np.random.default_rng(8)
+    prompts = {1: rng.integers(0, SH.vocab, 5).tolist(), 2: rng.integers(0, SH.vocab, 21).tolist()}
+    svc.add(1, prompts[1], max_new=12)
+    svc.add(2, prompts[2], max_new=6)
+    pages = {}
+    out = {}
+    while True:
+        for sid in (1, 2):  # record the pages while the sequences hold them
+            if svc.query(sid).state != sv.FINISHED:
+                pages[sid] = svc.pages(sid)
+        rows, toks = svc.step()
+        for sid, t in toks:
+            out.setdefault(sid, []).append(t)
+        if rows == 0:
+            break
+    assert len(out[1]) == 12 and len(out[2]) == 6
+    assert svc.free_pages == NUM_PAGES
+    for sid, n in ((1, 12), (2, 6)):
+        assert out[sid] == _manual(model, prompts[sid], n, pages[sid]), sid
+
+
+def test_park_resume_on_the_gpu():
+    model = _model()
+    kp, vp = synth.device.device_pools(SH, SEED, NUM_PAGES)
+    ctx = MAX_PAGES * SH.page_size
+    gstep = sv.GpuStep(model, [mk.Sched(model, 2, ctx)], kp, vp, MAX_PAGES)
+    svc = sv.Service(NUM_PAGES, SH.page_size, MAX_PAGES, 2, gstep)
+    prompt = [3, 14, 15, 92]
+    svc.add(5, prompt, max_new=8)
+    first = []
+    while len(first) < 3:
+        _, toks = svc.step()
+        first += [t for _, t in toks]
+    svc.park(5)
+    assert svc.step() == (0, [])
+    appended = [65, 35, 89]
+    svc.resume(5, appended)
+    rest = svc.run()[5]
+    # one uninterrupted loop with the appended tokens fed after the third
+    # sample, over the same pages (the only sequence: pages 0, 1, ... in order)
+    ref = _manual_forced(model, prompt, first, appended, 5, list(range(MAX_PAGES)))
+    assert first + rest == ref
+
+
+def _manual_forced(model, prompt, first, appended, n_more, pages):
+    kp, vp = synth.device.device_pools(SH, SEED, NUM_PAGES)
+    sched = mk.Sched(model, 1, MAX_PAGES * SH.page_size)
+    sess = mk.Session(model, sched)
+    bt = torch.full((1, MAX_PAGES), -1, dtype=torch.int32, device="cuda")
+    logits = torch.empty(1, SH.vocab, device="cuda")
+    out = []
+    feed = list(prompt)
+    n_ctx = 0
+    forced_after = {len(first): list(appended)}
+    while len(out) < len(first) + n_more:
+        tok = feed.pop(0)
+        bt[0, n_ctx // SH.page_size] = pages[n_ctx // SH.page_size]
+        sess.step(torch.tensor([tok], dtype=torch.int32, device="cuda"),
+                  torch.tensor([n_ctx + 1], dtype=torch.int32, device="cuda"), bt, kp, vp, logits)
+        sess.check()
+        n_ctx += 1
+        if not feed:
+            t = int(torch.argmax(logits[0]).item())
+            out.append(t)
+            feed.append(t)
+            feed += forced_after.pop(len(out), [])
+    return out
