@@ -40,10 +40,14 @@ extern "C" {
 
 /* Model shape.  Layer l attends to its whole context iff window == 0 or
  * (l + 1) % full_period == 0; otherwise to the last `window` positions.
- * The compiled kernels cover three shapes (hidden, n_q, n_kv, head_dim,
+ * The compiled kernels cover four shapes (hidden, n_q, n_kv, head_dim,
  * n_experts, top_k, inter, page_size): (256,4,2,64,16,4,128,16),
- * (1024,16,2,64,32,4,512,64) and (2048,32,4,128,128,8,768,64); n_layers,
- * vocab, window and full_period are free. */
+ * (1024,16,2,64,32,4,512,64), (2048,32,4,128,128,8,768,64) and the dense
+ * (1024,16,2,64,1,1,2048,64); n_layers, vocab, window and full_period are
+ * free.  n_experts = top_k = 1 is a dense model: every token takes the one
+ * expert with weight 1, i.e. a SwiGLU FFN (w_gate, w_up, w_down of "expert
+ * 0"), run as static FFN_UPGATE_ACT / FFN_DOWN tiles with no router (the
+ * pages' "Tasks": the dense FFN opcodes); w_router may then be NULL. */
 typedef struct {
   int32_t n_layers, hidden, n_q, n_kv, head_dim, n_experts, top_k, inter, vocab;
   int32_t page_size, window, full_period;

@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 SOURCES = ["mk_api.cpp", "mk_sched.cpp", "mk_shape_tiny.cu", "mk_shape_small.cu", "mk_shape_full.cu",
-           "mk_static_ws.cu", "mk_service.cpp", "mk_gpu_step.cu"]
+           "mk_shape_dense.cu", "mk_static_ws.cu", "mk_service.cpp", "mk_gpu_step.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -37,6 +37,7 @@ int query_num_sms() {
 
 int launch_tiny(const Params& p, int grid, cudaStream_t s);
 int launch_small(const Params& p, int grid, cudaStream_t s);
+int launch_dense(const Params& p, int grid, cudaStream_t s);
 int launch_full(const Params& p, int grid, cudaStream_t s);
 
 namespace {
@@ -49,6 +50,7 @@ struct CompiledShape {
 const CompiledShape kShapes[] = {
     {{256, 4, 2, 64, 16, 4, 128, 16}, launch_tiny},
     {{1024, 16, 2, 64, 32, 4, 512, 64}, launch_small},
+    {{1024, 16, 2, 64, 1, 1, 2048, 64}, launch_dense},  // dense SwiGLU FFN (one expert, top-1)
     {{2048, 32, 4, 128, 128, 8, 768, 64}, launch_full},
 };
 
@@ -177,8 +179,9 @@ int mk_load_model(const mk_config* cfg, const mk_weights* w, mk_model** out) {
       id = i;
   }
   if (id < 0) return fail(MK_ERR_UNSUPPORTED, "no compiled kernel for this model shape");
-  if (!w->embedding || !w->w_qkv || !w->w_o || !w->w_router || !w->w_gate || !w->w_up || !w->w_down ||
-      !w->norm_gamma || !w->final_gamma || !w->w_lm)
+  const bool dense = c.n_experts == 1 && c.top_k == 1;  // no router: w_router may be null
+  if (!w->embedding || !w->w_qkv || !w->w_o || (!w->w_router && !dense) || !w->w_gate || !w->w_up ||
+      !w->w_down || !w->norm_gamma || !w->final_gamma || !w->w_lm)
     return fail(MK_ERR_ARG, "a weight pointer is null");
   mk_model* m = new mk_model();
   m->cfg = c;

@@ -16,8 +16,8 @@ enum Op : int32_t {
   OP_RESID_NORM = 1,        // residual add (+ MoE combine) + RMSNorm; embedding at layer 0
   OP_QKV_PROJ = 2,          // one row tile of x W_qkv, RoPE + KV append in the epilogue
   OP_O_PROJ = 3,            // one row tile of attn W_o over one KV group's columns (split-K)
-  OP_FFN_UPGATE_ACT = 4,    // dense SwiGLU up/gate (dense-layer models; reserved)
-  OP_FFN_DOWN = 5,          // dense down projection (reserved)
+  OP_FFN_UPGATE_ACT = 4,    // dense SwiGLU up/gate tile (a one-expert, top-1 model)
+  OP_FFN_DOWN = 5,          // dense down projection tile
   OP_LM_HEAD = 6,           // one vocab tile of the LM head
   OP_ATTN_DECODE = 7,       // one static KV slice of one (row, KV group)
   OP_ATTN_COMBINE = 8,      // merge of the slice partials of one (row, KV group)
@@ -77,7 +77,10 @@ constexpr int32_t TGT_DYN_SPLITS = -2;
 //               1 by index with the down units shifted past the up units, 2 by host-set rank)
 // MOE_COMBINE:  A0 b0, A1 b1
 // W_ATTN:       A0 b, A1 g, A2 t0, A3 t1, A4 first page, A5 partial slot
-// W_UP_TILE / W_DOWN_TILE: A0 expert, A1 tile index, A2 row0, A3 n_rows
+// FFN_UPGATE_ACT / FFN_DOWN: A0 tile index
+// W_UP_TILE / W_DOWN_TILE: A0 expert, A1 tile index, A2 row0, A3 n_rows, A8..A9 the
+//               rows' output slots and A10..A11 their weights (down tiles of <= kTB rows),
+//               A12 dense (rows are the batch rows: slot = row, weight 1)
 
 // ------------------------------------------------------- stage geometry
 constexpr int kStageBytes = 32768;   // one shared-memory stage

@@ -276,9 +276,16 @@ struct Hdr {
   int32_t pad[31];
 };
 
+// the longest activation row a GEMV reads: hidden, intermediate (down
+// projection) or one KV group's attention output (O projection)
+template <class S>
+__host__ __device__ constexpr int xs_row() {
+  return S::H > S::I ? (S::H > S::G * S::D ? S::H : S::G * S::D) : (S::I > S::G * S::D ? S::I : S::G * S::D);
+}
+
 template <class S>
 struct Scratch {
-  float xs[kTB * S::H];                     // activation rows of one GEMV pass (tagged)
+  float xs[kTB * xs_row<S>()];              // activation rows of one GEMV pass (tagged)
   float out[2][kTB * kMaxStageRows];        // dot products of one stage (double buffer)
   alignas(16) uint16_t qh[8][S::D + 8];     // the KV group's queries (tagged), pre-scaled, as
   alignas(16) uint16_t ql[8][S::D + 8];     // BF16 hi + lo; rows >= G zero, padded rows
@@ -816,23 +823,7 @@ struct Producer {
         }
       }
       if (!push(it)) return false;
-      const int64_t le = (int64_t)l * S::E + e;
-      if (up) {
-        for (int s = 0; s < mp.up_stages; ++s) {
-          int slot;
-          if (!acquire_stage(slot)) return false;
-          uint64_t* fb = &c.hdr->full[slot];
-          uint8_t* dst = stage(slot);
-          const int r0 = t * mp.up_tile + s * mp.up_half;
-          const uint32_t half = (uint32_t)mp.up_half * S::H * 2;
-          mbar_expect_tx(fb, 2 * half);
-          bulk_g2s_hint(dst, p.wg + (le * S::I + r0) * S::H, half, fb, stream_policy);
-          bulk_g2s_hint(dst + half, p.wu + (le * S::I + r0) * S::H, half, fb, stream_policy);
-          ++c.st;
-        }
-      } else {
-        if (!load_rows(p.wd + le * S::H * S::I, S::I, S::I, t * mp.dn_tile, mp.dn_tile, mp.dn_rows)) return false;
-      }
+      if (!tile_stages(l, e, t, up)) return false;
       cur = nxt;
       if (cur < total) {
         if (stat) {
@@ -844,6 +835,51 @@ struct Producer {
       }
     }
     return carried || claim_end(d);
+  }
+
+  // The weight stages of tile t of expert e: up/gate stages of up_half gate
+  // rows and as many up rows, or down stages of dn_rows rows of W_down[e].
+  __device__ __forceinline__ bool tile_stages(int l, int e, int t, bool up) {
+    constexpr MoePlan mp = S::mp;
+    const int64_t le = (int64_t)l * S::E + e;
+    if (!up) return load_rows(p.wd + le * S::H * S::I, S::I, S::I, t * mp.dn_tile, mp.dn_tile, mp.dn_rows);
+    for (int s = 0; s < mp.up_stages; ++s) {
+      int slot;
+      if (!acquire_stage(slot)) return false;
+      uint64_t* fb = &c.hdr->full[slot];
+      uint8_t* dst = stage(slot);
+      const int r0 = t * mp.up_tile + s * mp.up_half;
+      const uint32_t half = (uint32_t)mp.up_half * S::H * 2;
+      mbar_expect_tx(fb, 2 * half);
+      bulk_g2s_hint(dst, p.wg + (le * S::I + r0) * S::H, half, fb, stream_policy);
+      bulk_g2s_hint(dst + half, p.wu + (le * S::I + r0) * S::H, half, fb, stream_policy);
+      ++c.st;
+    }
+    return true;
+  }
+
+  // A dense FFN tile ("Tasks": FFN_UPGATE_ACT, FFN_DOWN): a static task for
+  // tile A0 of the layer's one FFN (stored as expert 0), over every row of
+  // the batch; the same work item as an MoE tile, with each row its own slot
+  // and weight 1 (the dense flag A12).
+  __device__ __forceinline__ bool ffn_tile(const int32_t* d) {
+    constexpr MoePlan mp = S::mp;
+    const bool up = d[F_OP] == OP_FFN_UPGATE_ACT;
+    int32_t it[32];
+    for (int k = 0; k < 32; ++k) it[k] = d[k];
+    it[F_OP] = up ? W_UP_TILE : W_DOWN_TILE;
+    it[F_A0] = 0;          // expert
+    it[F_A0 + 1] = d[F_A0];  // tile
+    it[F_A0 + 2] = 0;      // first row
+    it[F_A0 + 3] = p.B;    // rows
+    it[F_A0 + 12] = 1;     // dense
+    for (int t = 0; t < kTB; ++t) {
+      it[F_A0 + 8 + t] = t;  // row b's output goes to slot b (one choice per row)
+      it[F_A0 + 10 + t] = __float_as_int(1.f);
+    }
+    it[F_NSTAGE] = up ? mp.up_stages : mp.dn_stages;
+    if (!push(it)) return false;
+    return tile_stages(d[F_LAYER], 0, d[F_A0], up);
   }
 
   __device__ __forceinline__ bool passthrough(const int32_t* d) {
@@ -892,6 +928,8 @@ struct Producer {
         case OP_ATTN_DRAIN: ok = attn_drain(d); break;
         case OP_MOE_UPGATE_ACT_DRAIN: ok = moe_drain(d, d[F_A0 + 6]); break;
         case OP_MOE_DOWN_DRAIN: ok = moe_drain(d, 2); break;
+        case OP_FFN_UPGATE_ACT:
+        case OP_FFN_DOWN: ok = ffn_tile(d); break;
         default: ok = passthrough(d); break;
       }
     }
@@ -990,6 +1028,7 @@ struct Consumer {
   // activation rows [kTB*chunk, kTB*chunk + tb) of the item into sm.xs (fp32)
   template <int K>
   __device__ __forceinline__ void load_x(int op, const int32_t* w, int chunk, int tb) {
+    static_assert(K <= xs_row<S>(), "kTB activation rows of K fit the cache");
     constexpr int C = K / 4;  // float4 per row
     float4* xs4 = reinterpret_cast<float4*>(sm.xs);
     for (int i = ct; i < tb * C; i += kConsumerThreads) {
@@ -1007,6 +1046,7 @@ struct Consumer {
         return p.attn_out + (int64_t)tok * S::NQ * S::D + (int64_t)w[F_A0 + 2] * S::G * S::D;
       case W_UP_TILE: {
         const int row = w[F_A0 + 2] + tok;
+        if (w[F_A0 + 12]) return p.x + (int64_t)row * S::H;  // dense: the rows are the batch
         if (p.explicit_gather) return p.xg + (int64_t)row * S::H;
         const int pr = __ldcg(p.perm + row);
         int b = pr / S::K;
@@ -1125,9 +1165,10 @@ struct Consumer {
         for (int i = ct; i < tb * rows; i += kConsumerThreads) {
           const int t = i / rows, r = i - t * rows;
           const int row = w[F_A0 + 2] + kTB * chunk + t;
-          int slot = __ldcg(p.perm + row);
+          const bool dense = w[F_A0 + 12] != 0;  // row b is slot b, weight 1
+          int slot = dense ? row : __ldcg(p.perm + row);
           if (slot < 0 || slot >= p.B * S::K) slot = 0;  // only after a failed step
-          const float wt = __ldcg(p.topk_w + (int64_t)l * p.MB * S::K + slot);
+          const float wt = dense ? 1.f : __ldcg(p.topk_w + (int64_t)l * p.MB * S::K + slot);
           const int n = w[F_A0 + 1] * S::mp.dn_tile + s * S::mp.dn_rows + r;
           p.y[(int64_t)slot * S::H + n] = wt * out[t * kMaxStageRows + r];
         }
@@ -1567,7 +1608,7 @@ struct Consumer {
   // eight partial merges meet in shared memory, taken in warp order.
   __device__ __forceinline__ void attn_combine_one_head(int l, int b, int g, int h) {
     constexpr int G = S::G, D = S::D, DPL = D / 32, J = 8;
-    static_assert(kConsumerWarps * D <= kTB * S::H, "the warps' partial sums fit the activation cache");
+    static_assert(kConsumerWarps * D <= kTB * xs_row<S>(), "the warps' partial sums fit the activation cache");
     // the activation cache holds the partial sums below: mark it empty
     // (read again only after the barrier that ends this item)
     if (ct == 0) sm.xtag[0] = -1;

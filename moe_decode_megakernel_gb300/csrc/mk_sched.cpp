@@ -260,6 +260,9 @@ static int build(mk_sched* s) {
     LayerBars& lb = s->lb[l];
     const bool full = is_full_layer(c, l);
     std::vector<Desc> w_norm = B.norm_wave(l, norm_rows);
+    // one expert taken by every token: a dense SwiGLU FFN ("Tasks":
+    // FFN_UPGATE_ACT, FFN_DOWN) in static tiles, with no routing
+    const bool dense = D.E == 1 && D.K == 1;
 
     // QKV: a row tile never leaves one KV group's rows (its query heads, its
     // K head or its V head), so the group's attention waits on its own tiles
@@ -297,7 +300,8 @@ static int build(mk_sched* s) {
       // segments -- query heads, K head, V head -- apportioned by largest
       // remainders, repeated per group
       struct Seg { int r0, rows, g, n; double frac; };
-      const int n_routing = lb.n_norm + (int)((D.E + router_tile - 1) / router_tile) + (MB + kConsumerWarps - 1) / kConsumerWarps;
+      const int n_routing = lb.n_norm + (dense ? 0 : (int)((D.E + router_tile - 1) / router_tile) +
+                                                     (MB + kConsumerWarps - 1) / kConsumerWarps);
       const int per_group = std::max(3, (s->num_sms - n_routing) / NKV);
       Seg tmpl[3] = {{0, G * D.D, 0, 0, 0.0}, {0, D.D, 0, 0, 0.0}, {0, D.D, 0, 0, 0.0}};
       int given = 0;
@@ -334,7 +338,8 @@ static int build(mk_sched* s) {
       }
     }
 
-    std::vector<Desc> w_router = B.dense_wave(OP_ROUTER_GEMM, l, D.E, router_tile, lb.router);
+    std::vector<Desc> w_router;
+    if (!dense) w_router = B.dense_wave(OP_ROUTER_GEMM, l, D.E, router_tile, lb.router);
     lb.n_router = (int)w_router.size();
     const bool fuse_fin = o.fuse_finalize && MB <= kConsumerWarps;
     // routing fused into the router tasks: each counts itself in on lb.rarrive
@@ -362,7 +367,7 @@ static int build(mk_sched* s) {
 
     std::vector<Desc> w_topk, w_fin;
     const int topk_rows = kConsumerWarps;
-    for (int b0 = 0; b0 < (fuse_rt ? 0 : MB); b0 += topk_rows) {
+    for (int b0 = 0; b0 < (fuse_rt || dense ? 0 : MB); b0 += topk_rows) {
       Desc d = blank(OP_ROUTER_TOPK, l);
       d[F_A0] = b0;
       d[F_A0 + 1] = std::min(MB, b0 + topk_rows);
@@ -373,7 +378,7 @@ static int build(mk_sched* s) {
       w_topk.push_back(d);
     }
     lb.n_topk = (int)w_topk.size();
-    if (!fuse_fin) {
+    if (!fuse_fin && !dense) {
       Desc d = blank(OP_ROUTE_FINALIZE, l);
       B.wait(d, 0, lb.topk, lb.n_topk);
       d[F_SIG0] = lb.fin;
@@ -381,7 +386,7 @@ static int build(mk_sched* s) {
     }
 
     std::vector<Desc> w_gather;
-    if (o.explicit_gather) {
+    if (o.explicit_gather && !dense) {
       const int rows = MB * D.K, per = 64;
       for (int r0 = 0; r0 < rows; r0 += per) {
         Desc d = blank(OP_MOE_GATHER, l);
@@ -452,7 +457,27 @@ static int build(mk_sched* s) {
     // that early holds its SM's pipeline until the expert's up tiles land)
     std::vector<Desc> w_up, w_dn, w_mcomb;
     const bool unified = o.moe_queue == 1;
-    for (int i = 0; i < n_moe; ++i) {
+    if (dense) {
+      // every up/gate tile reads the RMSNorm output; a down tile needs all
+      // of the intermediate
+      for (int t = 0; t < mp.up_tiles; ++t) {
+        Desc d = blank(OP_FFN_UPGATE_ACT, l);
+        d[F_A0] = t;
+        B.wait(d, 0, lb.norm, lb.n_norm);
+        d[F_SIG0] = lb.upd;
+        w_up.push_back(d);
+      }
+      for (int t = 0; t < mp.dn_tiles; ++t) {
+        Desc d = blank(OP_FFN_DOWN, l);
+        d[F_A0] = t;
+        B.wait(d, 0, lb.upd, mp.up_tiles);
+        d[F_SIG0] = lb.dnd;
+        w_dn.push_back(d);
+      }
+      lb.n_up_claim = mp.up_tiles;
+      lb.n_dn_claim = mp.dn_tiles;
+    }
+    for (int i = 0; i < (dense ? 0 : n_moe); ++i) {
       Desc d = blank(OP_MOE_UPGATE_ACT_DRAIN, l);
       B.wait(d, 0, lb.fin, 1);
       // the routing can finish before the RMSNorm task when the routers
@@ -481,7 +506,7 @@ static int build(mk_sched* s) {
         w_dn.push_back(e);
       }
     }
-    lb.n_up_claim = lb.n_dn_claim = n_moe;
+    if (!dense) lb.n_up_claim = lb.n_dn_claim = n_moe;
     if (!o.fuse_moe_combine) {
       for (int b0 = 0; b0 < MB; b0 += norm_rows) {
         Desc d = blank(OP_MOE_COMBINE, l);
@@ -537,7 +562,7 @@ static int build(mk_sched* s) {
         add(w_attn); add(w_acomb); add(w_up); add(w_dn); add(w_o); add(w_mcomb);
         break;
     }
-    if (o.moe_static && o.moe_balance && !unified) balance_moe_ranks(s, all, layer_begin, MB, full);
+    if (o.moe_static && o.moe_balance && !unified && !dense) balance_moe_ranks(s, all, layer_begin, MB, full);
   }
   // final RMSNorm and LM head
   std::vector<Desc> w_final = B.norm_wave(L, norm_rows);

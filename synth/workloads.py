@@ -73,6 +73,10 @@ MODELS = {
     "full_l2": ModelShape("full_l2", n_layers=2, hidden=2048, n_q=32, n_kv=4, head_dim=128,
                           n_experts=128, top_k=8, inter=768, vocab=65536, page_size=64,
                           window=4096, full_period=2),
+    # a dense model: one expert that every token takes with weight 1 is a
+    # SwiGLU FFN (intermediate 2048); half the layers sliding-window
+    "dense": ModelShape("dense", n_layers=8, hidden=1024, n_q=16, n_kv=2, head_dim=64, n_experts=1,
+                        top_k=1, inter=2048, vocab=32768, page_size=64, window=512, full_period=2),
 }
 
 
@@ -105,6 +109,10 @@ WORKLOADS = {
                           desc="full shape, B=1, context 262144"),
     "batch64_ragged": Workload("batch64_ragged", "full", 64, ("loguniform", 1024, 65536), 6,
                                desc="full shape, B=64, seq_lens log-uniform [1024,65536]"),
+    "dense_small": Workload("dense_small", "dense", 1, ("fixed", 1024), 9,
+                            desc="dense SwiGLU model: 8 layers, B=1, context 1024"),
+    "dense_batch5": Workload("dense_batch5", "dense", 5, ("uniform", 1, 1500), 10,
+                             desc="dense SwiGLU model: 8 layers, B=5, seq_lens U[1,1500]"),
     "prof_l2_8k": Workload("prof_l2_8k", "full_l2", 1, ("fixed", 8192), 7,
                            desc="full-shape layers, 2 of them, B=1, context 8192 (profiling case)"),
 }

@@ -115,16 +115,21 @@ def compare(inp: synth.StepInputs, g: GpuStep, rows=None) -> Report:
     shape = w.shape
     B, L, K = w.batch, shape.n_layers, shape.top_k
     rows = np.arange(B) if rows is None else np.asarray(rows)
+    # a dense model (one expert, top-1) has no router on the GPU: every row
+    # takes expert 0 with weight 1, which is the oracle's routing too
+    dense = shape.n_experts == 1 and K == 1
+    ids = np.zeros_like(g.ids) if dense else g.ids
     ref = oracle.decode_step(shape, w.seed, inp.tokens, inp.seq_lens, inp.block_tables,
-                             inp.router_bias, rows=rows, force_ids=g.ids, want_kv=True)
-    rerr = np.array([max(float(np.max(np.abs(g.extra["router_logits"][l, b] - ref.router_logits[l, r])))
-                         for r, b in enumerate(rows)) for l in range(L)])
+                             inp.router_bias, rows=rows, force_ids=ids, want_kv=True)
+    rerr = np.zeros(L) if dense else np.array(
+        [max(float(np.max(np.abs(g.extra["router_logits"][l, b] - ref.router_logits[l, r])))
+             for r, b in enumerate(rows)) for l in range(L)])
     # routing: the GPU's experts must be a top-k of the oracle's logits (within a tie)
     exact = ties = 0
     bad = []
     for l in range(L):
         for r, b in enumerate(rows):
-            gi = [int(e) for e in g.ids[l, b]]
+            gi = [int(e) for e in ids[l, b]]
             own = [int(e) for e in ref.own_ids[l, r]]
             lg = ref.router_logits[l, r].astype(np.float64)
             assert len(set(gi)) == K and all(0 <= e < shape.n_experts for e in gi), (l, b, gi)
@@ -141,8 +146,8 @@ def compare(inp: synth.StepInputs, g: GpuStep, rows=None) -> Report:
                 bad.append(f"layer {l} row {b}: GPU experts {gi} vs oracle {own} "
                            f"(logits {lg[gi]} / {lg[own]})")
     # weights: softmax over the chosen logits
-    werr = max(float(np.max(np.abs(g.weights[l, b] - ref.weights[l, r])))
-               for l in range(L) for r, b in enumerate(rows))
+    werr = 0.0 if dense else max(float(np.max(np.abs(g.weights[l, b] - ref.weights[l, r])))
+                                 for l in range(L) for r, b in enumerate(rows))
     # logits
     errs = []
     agree = 0

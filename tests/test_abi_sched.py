@@ -213,3 +213,23 @@ def test_two_row_schedule(seq):
         qkv = [d for d in tasks if mk.OPS[int(d[mk.F_OP])] == "QKV_PROJ"]
         assert all(int(d[mk.F_A0 + 7]) == 1 for d in qkv)
         s.simulate(np.asarray(seq, np.int32), seed=5)
+
+
+@pytest.mark.parametrize("workload", ["dense_small", "dense_batch5"])
+def test_dense_schedules(workload):
+    """A dense model: no router, top-k or MoE claimers; one static FFN
+    up/gate tile per 64-row slice of the intermediate and one down tile per
+    32 outputs, every down tile after all the up/gate tiles of its layer."""
+    m, s, inp = sched_for(workload)
+    s.validate()
+    s.simulate(inp.seq_lens, seed=2)
+    sh = synth.WORKLOADS[workload].shape
+    counts = {}
+    for sm in range(s.num_sms):
+        for i in range(s.num_tasks(sm)):
+            op = mk.OPS[int(s.get_task(sm, i)[mk.F_OP])]
+            counts[op] = counts.get(op, 0) + 1
+    assert not any(k in counts for k in ("ROUTER_GEMM", "ROUTER_TOPK", "ROUTE_FINALIZE",
+                                          "MOE_UPGATE_ACT_DRAIN", "MOE_DOWN_DRAIN"))
+    assert counts["FFN_UPGATE_ACT"] == sh.n_layers * (sh.inter // 64)
+    assert counts["FFN_DOWN"] == sh.n_layers * (sh.hidden // 32)
