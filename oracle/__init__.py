@@ -12,6 +12,8 @@ from dataclasses import dataclass
 
 import numpy as np
 
+import synth as synth_kinds  # tensor kind ids only
+
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "liboracle.so")
 
@@ -25,7 +27,8 @@ class OrcConfig(ctypes.Structure):
     _fields_ = [(n, c_int) for n in ("n_layers", "hidden", "n_q", "n_kv", "head_dim",
                                      "n_experts", "top_k", "inter", "vocab", "page_size",
                                      "window", "full_period")] + \
-               [(n, c_double) for n in ("rope_base", "eps", "weight_sigma", "kv_sigma")]
+               [(n, c_double) for n in ("rope_base", "eps", "weight_sigma", "kv_sigma")] + \
+               [("expert_fp8", c_int)]
 
 
 class OrcMatrix(ctypes.Structure):
@@ -62,6 +65,10 @@ def lib():
         L.orc_rmsnorm.argtypes = [c_int, P_D, P_D, c_double, P_D]
         L.orc_rope.argtypes = [c_int, P_D, ctypes.c_int64, c_double]
         L.orc_softmax.argtypes = [c_int, P_D, P_D]
+        L.orc_synth_dense.argtypes = [ctypes.POINTER(OrcConfig), ctypes.c_uint64, c_int, c_int, c_int, P_D]
+        L.orc_synth_dense.restype = ctypes.c_int64
+        L.orc_e4m3_value.argtypes = [c_int]
+        L.orc_e4m3_value.restype = c_double
         L.orc_silu.argtypes = [c_double]
         L.orc_silu.restype = c_double
         L.orc_matvec.argtypes = [ctypes.POINTER(OrcMatrix), P_D, P_D]
@@ -104,7 +111,7 @@ def config_from_shape(shape) -> OrcConfig:
     return OrcConfig(shape.n_layers, shape.hidden, shape.n_q, shape.n_kv, shape.head_dim,
                      shape.n_experts, shape.top_k, shape.inter, shape.vocab, shape.page_size,
                      shape.window, shape.full_period, shape.rope_base, shape.eps,
-                     shape.weight_sigma, shape.kv_sigma)
+                     shape.weight_sigma, shape.kv_sigma, int(getattr(shape, "expert_fp8", False)))
 
 
 # ----------------------------------------------------------- layer operations
@@ -132,6 +139,22 @@ def softmax(s):
 
 def silu(x):
     return lib().orc_silu(float(x))
+
+
+def synth_matrix(shape, seed: int, kind: int, layer: int = 0, expert: int = 0) -> np.ndarray:
+    """A weight matrix exactly as the oracle reads it (FP8 experts dequantized)."""
+    rows, cols = {synth_kinds.WG: (shape.inter, shape.hidden), synth_kinds.WU: (shape.inter, shape.hidden),
+                  synth_kinds.WD: (shape.hidden, shape.inter)}[kind]
+    cfg = config_from_shape(shape)
+    out = np.empty((rows, cols), np.float64)
+    n = lib().orc_synth_dense(ctypes.byref(cfg), seed, kind, layer, expert, _d(out))
+    assert n == rows * cols
+    return out
+
+
+def e4m3_value(code: int) -> float:
+    """The value of an OCP FP8 E4M3 code (the oracle's own decoding)."""
+    return lib().orc_e4m3_value(int(code))
 
 
 class Dense:

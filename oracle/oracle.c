@@ -236,10 +236,27 @@ int orc_kv_slot(int64_t pos, int page_size, const int32_t* block_row, int max_pa
 
 /* ------------------------------------------------ the synthetic model */
 
+double orc_e4m3_value(int code) {
+  const int e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double v = e ? ldexp(1.0 + m / 8.0, e - 7) : ldexp(m / 8.0, -6);
+  return (code & 0x80) ? -v : v;
+}
+
 void orc_synth_row(const void* ctx, int row, double* out) {
   const orc_synth_src* s = (const orc_synth_src*)ctx;
   const uint64_t key = synth_key(s->seed, synth_stream((uint32_t)s->kind, (uint32_t)s->layer,
                                                        (uint32_t)s->expert));
+  if (s->cfg->expert_fp8 && (s->kind == SYNTH_WG || s->kind == SYNTH_WU || s->kind == SYNTH_WD)) {
+    /* an FP8 expert row: its E4M3 codes times the row's scale */
+    const int skind = s->kind == SYNTH_WG ? SYNTH_SG : s->kind == SYNTH_WU ? SYNTH_SU : SYNTH_SD;
+    const uint64_t skey = synth_key(s->seed, synth_stream((uint32_t)skind, (uint32_t)s->layer,
+                                                          (uint32_t)s->expert));
+    const double scale = (double)synth_row_scale(skey, (uint64_t)row, synth_fp8_base(s->sigma));
+    const uint64_t base = (uint64_t)row * (uint64_t)s->cols;
+    for (int c = 0; c < s->cols; ++c) out[c] = orc_e4m3_value(synth_fp8(key, base + (uint64_t)c)) * scale;
+    return;
+  }
   const float scale = synth_scale(s->sigma);
   const uint64_t base = (uint64_t)row * (uint64_t)s->cols;
   for (int c = 0; c < s->cols; ++c)
@@ -269,6 +286,13 @@ orc_matrix orc_synth_matrix(const orc_config* cfg, uint64_t seed, int kind, int 
   st->sigma = cfg->weight_sigma;
   orc_matrix m = {orc_synth_row, st, rows, cols};
   return m;
+}
+
+int64_t orc_synth_dense(const orc_config* cfg, uint64_t seed, int kind, int layer, int expert, double* out) {
+  orc_synth_src st;
+  const orc_matrix m = orc_synth_matrix(cfg, seed, kind, layer, expert, &st);
+  for (int r = 0; r < m.rows; ++r) m.row(m.ctx, r, out + (int64_t)r * m.cols);
+  return (int64_t)m.rows * m.cols;
 }
 
 /* Pool layout of one layer: [page][kv head][slot][d] (the layout the decode

@@ -35,7 +35,13 @@ typedef struct {
   int window;      /* 0: no sliding window */
   int full_period; /* layer l attends to the whole context iff window == 0 or (l+1) % full_period == 0 */
   double rope_base, eps, weight_sigma, kv_sigma;
+  int expert_fp8;  /* 1: expert matrices are E4M3 codes times one scale per output row */
 } orc_config;
+
+/* OCP FP8 E4M3 code -> value: (-1)^s 2^(e-7) (1 + m/8) for exponent field
+ * e > 0, (-1)^s 2^-6 (m/8) for e = 0 (1 sign, 4 exponent, 3 mantissa bits;
+ * no infinities; codes 0x7f and 0xff are NaN). */
+double orc_e4m3_value(int code);
 
 /* A matrix given row by row: row(ctx, r, out) writes the `cols` doubles of row r. */
 typedef void (*orc_row_fn)(const void* ctx, int row, double* out);
@@ -86,6 +92,9 @@ typedef struct {
 void orc_synth_row(const void* ctx, int row, double* out);
 orc_matrix orc_synth_matrix(const orc_config* cfg, uint64_t seed, int kind, int layer, int expert,
                             orc_synth_src* storage);
+/* The whole matrix of a weight kind as the oracle reads it, row-major into out
+ * (rows * cols doubles); returns rows * cols. */
+int64_t orc_synth_dense(const orc_config* cfg, uint64_t seed, int kind, int layer, int expert, double* out);
 /* K (is_v = 0) or V (is_v = 1) of one pool slot, as the generator filled it. */
 void orc_pool_vec(const orc_config* cfg, uint64_t seed, int is_v, int layer, int page, int head,
                   int slot, double* out);

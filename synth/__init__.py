@@ -19,7 +19,7 @@ from .workloads import (MODELS, WORKLOADS, ModelShape, Workload, StepInputs, mak
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libsynth.so")
 
-EMB, WQKV, WO, WR, WG, WU, WD, WLM, KPOOL, VPOOL = range(1, 11)
+EMB, WQKV, WO, WR, WG, WU, WD, WLM, KPOOL, VPOOL, SG, SU, SD = range(1, 14)
 
 _lib = None
 
@@ -40,6 +40,18 @@ def lib():
                                       ctypes.c_double]
         L.synth_raw.restype = u64
         L.synth_raw.argtypes = [u64, u64]
+        L.synth_fill_fp8_device.restype = ctypes.c_int
+        L.synth_fill_fp8_device.argtypes = [ctypes.c_void_p, u64, u64, u64, u32, u32, u32, ctypes.c_int,
+                                            ctypes.c_void_p]
+        L.synth_fill_scales_device.restype = ctypes.c_int
+        L.synth_fill_scales_device.argtypes = [ctypes.c_void_p, u64, u64, u64, u32, u32, u32, ctypes.c_int,
+                                               ctypes.c_double, ctypes.c_void_p]
+        L.synth_fill_fp8_host.restype = None
+        L.synth_fill_fp8_host.argtypes = [ctypes.c_void_p, u64, u64, u32, u32, u32]
+        L.synth_fill_scales_host.restype = None
+        L.synth_fill_scales_host.argtypes = [ctypes.c_void_p, u64, u64, u32, u32, u32, ctypes.c_double]
+        L.synth_e4m3.restype = ctypes.c_uint8
+        L.synth_e4m3.argtypes = [ctypes.c_float]
         _lib = L
     return _lib
 
@@ -60,6 +72,43 @@ def fill_device(ptr: int, n_streams: int, per_stream: int, seed: int, kind: int,
                                  int(vary_layer), sigma, stream)
     if rc != 0:
         raise RuntimeError(f"synth_fill_device failed with CUDA error {rc}")
+
+
+def fill_fp8_host(n: int, seed: int, kind: int, layer: int = 0, expert: int = 0) -> np.ndarray:
+    """uint8 E4M3 codes of one FP8 expert matrix (n elements, row-major)."""
+    out = np.empty(n, dtype=np.uint8)
+    lib().synth_fill_fp8_host(out.ctypes.data, n, seed, kind, layer, expert)
+    return out
+
+
+def fill_scales_host(rows: int, seed: int, kind: int, layer: int = 0, expert: int = 0,
+                     sigma: float = 0.02) -> np.ndarray:
+    """float32 row scales of one FP8 expert matrix (kind SG, SU or SD)."""
+    out = np.empty(rows, dtype=np.float32)
+    lib().synth_fill_scales_host(out.ctypes.data, rows, seed, kind, layer, expert, sigma)
+    return out
+
+
+def e4m3(f: float) -> int:
+    """The generator's E4M3 encoding of one binary32 (|f| <= 448)."""
+    return int(lib().synth_e4m3(f))
+
+
+def fill_fp8_device(ptr: int, n_streams: int, per_stream: int, seed: int, kind: int, layer0: int = 0,
+                    expert0: int = 0, vary_layer: bool = False, stream: int = 0) -> None:
+    rc = lib().synth_fill_fp8_device(ptr, n_streams, per_stream, seed, kind, layer0, expert0,
+                                     int(vary_layer), stream)
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_fp8_device failed with CUDA error {rc}")
+
+
+def fill_scales_device(ptr: int, n_streams: int, rows: int, seed: int, kind: int, layer0: int = 0,
+                       expert0: int = 0, vary_layer: bool = False, sigma: float = 0.02,
+                       stream: int = 0) -> None:
+    rc = lib().synth_fill_scales_device(ptr, n_streams, rows, seed, kind, layer0, expert0,
+                                        int(vary_layer), sigma, stream)
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_scales_device failed with CUDA error {rc}")
 
 
 def raw(key: int, idx: int) -> int:

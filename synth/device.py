@@ -8,7 +8,8 @@ from __future__ import annotations
 
 import torch
 
-from . import EMB, WQKV, WO, WR, WG, WU, WD, WLM, KPOOL, VPOOL, fill_device
+from . import (EMB, WQKV, WO, WR, WG, WU, WD, WLM, KPOOL, VPOOL, SG, SU, SD, fill_device, fill_fp8_device,
+               fill_scales_device)
 from .workloads import ModelShape
 
 
@@ -20,7 +21,8 @@ def _fill(t: torch.Tensor, n_streams: int, per: int, seed: int, kind: int, layer
 
 
 def device_weights(shape: ModelShape, seed: int, device="cuda", router_bias=None) -> dict:
-    """All weights of the model as torch tensors (BF16 stored as uint16)."""
+    """All weights of the model as torch tensors (BF16 stored as uint16; with
+    expert_fp8 the expert matrices as uint8 E4M3 codes plus fp32 row scales)."""
     st = torch.cuda.current_stream(device).cuda_stream
     L, H, E, I, V = shape.n_layers, shape.hidden, shape.n_experts, shape.inter, shape.vocab
     QKV, NQD = shape.qkv_rows(), shape.n_q * shape.head_dim
@@ -31,9 +33,6 @@ def device_weights(shape: ModelShape, seed: int, device="cuda", router_bias=None
         "w_qkv": torch.empty(L, QKV, H, **u16),
         "w_o": torch.empty(L, H, NQD, **u16),
         "w_router": torch.empty(L, E, H, **u16),
-        "w_gate": torch.empty(L, E, I, H, **u16),
-        "w_up": torch.empty(L, E, I, H, **u16),
-        "w_down": torch.empty(L, E, H, I, **u16),
         "w_lm": torch.empty(V, H, **u16),
         "norm_gamma": torch.ones(L, H, dtype=torch.float32, device=device),
         "final_gamma": torch.ones(H, dtype=torch.float32, device=device),
@@ -44,10 +43,35 @@ def device_weights(shape: ModelShape, seed: int, device="cuda", router_bias=None
     _fill(w["w_qkv"], L, QKV * H, seed, WQKV, vary_layer=True, sigma=sg, stream=st)
     _fill(w["w_o"], L, H * NQD, seed, WO, vary_layer=True, sigma=sg, stream=st)
     _fill(w["w_router"], L, E * H, seed, WR, vary_layer=True, sigma=sg, stream=st)
+    if getattr(shape, "expert_fp8", False):
+        # E4M3 codes and one fp32 scale per output row (synth.h, "FP8 expert weights")
+        u8 = dict(dtype=torch.uint8, device=device)
+        f32 = dict(dtype=torch.float32, device=device)
+        w["w_gate"] = torch.empty(L, E, I, H, **u8)
+        w["w_up"] = torch.empty(L, E, I, H, **u8)
+        w["w_down"] = torch.empty(L, E, H, I, **u8)
+        w["w_gate_scale"] = torch.empty(L, E, I, **f32)
+        w["w_up_scale"] = torch.empty(L, E, I, **f32)
+        w["w_down_scale"] = torch.empty(L, E, H, **f32)
+        for l in range(L):
+            for t, kind in ((w["w_gate"], WG), (w["w_up"], WU), (w["w_down"], WD)):
+                fill_fp8_device(t[l].data_ptr(), E, t[l].numel() // E, seed, kind, layer0=l, stream=st)
+            for t, kind in ((w["w_gate_scale"], SG), (w["w_up_scale"], SU), (w["w_down_scale"], SD)):
+                fill_scales_device(t[l].data_ptr(), E, t[l].numel() // E, seed, kind, layer0=l, sigma=sg,
+                                   stream=st)
+        return _rest(w, shape, seed, sg, st)
+    w["w_gate"] = torch.empty(L, E, I, H, **u16)
+    w["w_up"] = torch.empty(L, E, I, H, **u16)
+    w["w_down"] = torch.empty(L, E, H, I, **u16)
     for l in range(L):
         _fill(w["w_gate"][l], E, I * H, seed, WG, layer0=l, sigma=sg, stream=st)
         _fill(w["w_up"][l], E, I * H, seed, WU, layer0=l, sigma=sg, stream=st)
         _fill(w["w_down"][l], E, H * I, seed, WD, layer0=l, sigma=sg, stream=st)
+    return _rest(w, shape, seed, sg, st)
+
+
+def _rest(w, shape, seed, sg, st):
+    V, H = shape.vocab, shape.hidden
     _fill(w["w_lm"], 1, V * H, seed, WLM, sigma=sg, stream=st)
     return w
 

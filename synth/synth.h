@@ -27,6 +27,17 @@
  * The values are bounded by +-3.46 sigma and have the first two moments of
  * N(0, sigma^2); the decode step's inputs only need "random BF16 of scale
  * sigma", not exact Gaussian tails.
+ *
+ * FP8 expert weights (the FP8 variant of a model): element i of an expert
+ * matrix is the OCP FP8 E4M3 code (1 sign bit, 4 exponent bits biased by
+ * 7, 3 mantissa bits, subnormals below 2^-6, largest finite 448) of
+ *   ih4(draw(key, i)) * 3.5 * 2^-10          (exact in binary32, |.| < 448)
+ * rounded to nearest, ties to even; each output row r of the matrix has
+ * one binary32 scale
+ *   base * (1 + k * 2^-10),  k = draw(key', r) >> 55  (0 .. 511),
+ *   base = (float)(sigma / (37837.2265... * 3.5 * 2^-10)),
+ * with key' the key of the scale stream, so row r's weights are
+ * e4m3(code) * scale_r, of standard deviation sigma to 1.5 sigma.
  */
 #ifndef SYNTH_H
 #define SYNTH_H
@@ -54,7 +65,10 @@ enum {
   SYNTH_WD = 7,    /* expert down [H][I]                        */
   SYNTH_WLM = 8,   /* LM head [V][H]                            */
   SYNTH_KPOOL = 9, /* K pool of one layer [pages][nkv][P][d]    */
-  SYNTH_VPOOL = 10 /* V pool of one layer [pages][nkv][P][d]    */
+  SYNTH_VPOOL = 10, /* V pool of one layer [pages][nkv][P][d]   */
+  SYNTH_SG = 11,   /* FP8 expert gate row scales [I]            */
+  SYNTH_SU = 12,   /* FP8 expert up row scales [I]              */
+  SYNTH_SD = 13    /* FP8 expert down row scales [H]            */
 };
 
 SYNTH_FN uint64_t synth_mix64(uint64_t z) {
@@ -111,6 +125,62 @@ SYNTH_FN float synth_bf16_to_f32(uint16_t b) {
   memcpy(&f, &u, sizeof f);
 #endif
   return f;
+}
+
+/* ---- FP8 expert weights ---- */
+
+#define SYNTH_FP8_STEP 0.00341796875f /* 3.5 * 2^-10: ih4 * step is exact, below 448 */
+
+/* OCP E4M3 code of a finite binary32 of magnitude <= 448, round to nearest
+ * even, by integer operations on the bits (no rounding mode involved). */
+SYNTH_FN uint8_t synth_f32_to_e4m3_rne(float f) {
+  uint32_t u;
+#if defined(__CUDA_ARCH__)
+  u = __float_as_uint(f);
+#else
+  memcpy(&u, &f, sizeof u);
+#endif
+  const uint32_t sign = (u >> 24) & 0x80u;
+  const int32_t E = (int32_t)((u >> 23) & 0xffu);
+  const uint32_t M = u & 0x7fffffu;
+  if (E == 0) return (uint8_t)sign; /* zero or a binary32 subnormal: far below 2^-10 */
+  const int32_t e = E - 127;
+  uint32_t code;
+  if (e >= -6) { /* normal: keep 3 of the 23 mantissa bits */
+    uint32_t m = M >> 20, rem = M & 0xfffffu;
+    int32_t ee = e;
+    if (rem > 0x80000u || (rem == 0x80000u && (m & 1u))) ++m;
+    if (m == 8u) {
+      m = 0u;
+      ++ee;
+    }
+    code = ((uint32_t)(ee + 7) << 3) | m;
+  } else { /* subnormal: multiples of 2^-9 */
+    const int32_t sh = 14 - e; /* value * 2^9 = (M | 2^23) >> sh */
+    if (sh > 24) return (uint8_t)sign; /* below 2^-10 */
+    const uint32_t full = M | 0x800000u;
+    uint32_t m = full >> sh;
+    const uint32_t rem = full & ((1u << sh) - 1u), half = 1u << (sh - 1);
+    if (rem > half || (rem == half && (m & 1u))) ++m;
+    code = m; /* m == 8 is the smallest normal, 0x08 */
+  }
+  return (uint8_t)(sign | code);
+}
+
+/* One FP8 expert weight: the E4M3 code of element idx of stream key. */
+SYNTH_FN uint8_t synth_fp8(uint64_t key, uint64_t idx) {
+  return synth_f32_to_e4m3_rne((float)synth_ih4(synth_draw(key, idx)) * SYNTH_FP8_STEP);
+}
+
+/* The base of the row scales (one rounding of sigma / (std * step)). */
+SYNTH_FN float synth_fp8_base(double sigma) {
+  return (float)(sigma / (SYNTH_IH4_STD * 0.00341796875));
+}
+
+/* The scale of output row `row` (stream key of the scale kind). */
+SYNTH_FN float synth_row_scale(uint64_t key, uint64_t row, float base) {
+  const uint32_t k = (uint32_t)(synth_draw(key, row) >> 55);
+  return base * (1.0f + (float)k * 0.0009765625f); /* 1 + k 2^-10 is exact */
 }
 
 #endif /* SYNTH_H */

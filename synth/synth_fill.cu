@@ -56,7 +56,87 @@ __global__ void fill_scalar(uint16_t* __restrict__ dst, uint64_t n_streams, uint
   }
 }
 
+// FP8 expert weights: 16 consecutive E4M3 codes per thread, one 16-byte store
+// (per_stream % 16 == 0, dst 16-byte aligned).
+__global__ void fill_fp8_vec16(uint8_t* __restrict__ dst, uint64_t n_streams, uint64_t per_stream,
+                               uint64_t seed, uint32_t kind, uint32_t layer0, uint32_t expert0,
+                               int vary_layer) {
+  const uint64_t groups_per_stream = per_stream / 16;
+  const uint64_t total = n_streams * groups_per_stream;
+  for (uint64_t g = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+       g += (uint64_t)gridDim.x * blockDim.x) {
+    const uint64_t j = g / groups_per_stream;
+    const uint64_t i0 = (g - j * groups_per_stream) * 16;
+    const uint64_t key = synth_key(seed, stream_of(kind, layer0, expert0, vary_layer, j));
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      w[q] = 0u;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) w[q] |= (uint32_t)synth_fp8(key, i0 + 4 * q + b) << (8 * b);
+    }
+    *reinterpret_cast<uint4*>(dst + j * per_stream + i0) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Row scales of FP8 expert matrices: element r of sub-stream j.
+__global__ void fill_row_scales(float* __restrict__ dst, uint64_t n_streams, uint64_t rows, uint64_t seed,
+                                uint32_t kind, uint32_t layer0, uint32_t expert0, int vary_layer, float base) {
+  const uint64_t total = n_streams * rows;
+  for (uint64_t g = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+       g += (uint64_t)gridDim.x * blockDim.x) {
+    const uint64_t j = g / rows, r = g - j * rows;
+    const uint64_t key = synth_key(seed, stream_of(kind, layer0, expert0, vary_layer, j));
+    dst[g] = synth_row_scale(key, r, base);
+  }
+}
+
+int launch_blocks() {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return (sms > 0 ? sms : 1) * 8;
+}
+
 }  // namespace
+
+// FP8 expert weights (E4M3 codes) on the device: element i of sub-stream j
+// goes to dst[j*per_stream+i]; per_stream % 16 == 0 and dst 16-byte aligned.
+extern "C" int synth_fill_fp8_device(void* dst, uint64_t n_streams, uint64_t per_stream, uint64_t seed,
+                                     uint32_t kind, uint32_t layer0, uint32_t expert0, int vary_layer,
+                                     void* stream) {
+  if (dst == nullptr || n_streams == 0 || per_stream == 0 || per_stream % 16 != 0 ||
+      (reinterpret_cast<uintptr_t>(dst) & 15u) != 0)
+    return (int)cudaErrorInvalidValue;
+  fill_fp8_vec16<<<launch_blocks(), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint8_t*>(dst), n_streams, per_stream, seed, kind, layer0, expert0, vary_layer);
+  return (int)cudaGetLastError();
+}
+
+// Row scales (binary32) on the device: `rows` per sub-stream.
+extern "C" int synth_fill_scales_device(float* dst, uint64_t n_streams, uint64_t rows, uint64_t seed,
+                                        uint32_t kind, uint32_t layer0, uint32_t expert0, int vary_layer,
+                                        double sigma, void* stream) {
+  if (dst == nullptr || n_streams == 0 || rows == 0) return (int)cudaErrorInvalidValue;
+  fill_row_scales<<<launch_blocks(), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      dst, n_streams, rows, seed, kind, layer0, expert0, vary_layer, synth_fp8_base(sigma));
+  return (int)cudaGetLastError();
+}
+
+extern "C" void synth_fill_fp8_host(uint8_t* dst, uint64_t n, uint64_t seed, uint32_t kind, uint32_t layer,
+                                    uint32_t expert) {
+  const uint64_t key = synth_key(seed, synth_stream(kind, layer, expert));
+  for (uint64_t i = 0; i < n; ++i) dst[i] = synth_fp8(key, i);
+}
+
+extern "C" void synth_fill_scales_host(float* dst, uint64_t rows, uint64_t seed, uint32_t kind, uint32_t layer,
+                                       uint32_t expert, double sigma) {
+  const uint64_t key = synth_key(seed, synth_stream(kind, layer, expert));
+  const float base = synth_fp8_base(sigma);
+  for (uint64_t r = 0; r < rows; ++r) dst[r] = synth_row_scale(key, r, base);
+}
+
+extern "C" uint8_t synth_e4m3(float f) { return synth_f32_to_e4m3_rne(f); }
 
 extern "C" int synth_fill_device(void* dst, uint64_t n_streams, uint64_t per_stream, uint64_t seed,
                                  uint32_t kind, uint32_t layer0, uint32_t expert0, int vary_layer,

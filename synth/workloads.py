@@ -37,6 +37,7 @@ class ModelShape:
     eps: float = 1e-5
     weight_sigma: float = 0.02
     kv_sigma: float = 1.0
+    expert_fp8: bool = False  # expert matrices as E4M3 codes with one scale per output row
 
     def is_full_layer(self, layer: int) -> bool:
         return self.window == 0 or (layer + 1) % self.full_period == 0
@@ -53,6 +54,8 @@ class ModelShape:
         return 2 * (self.qkv_rows() * h + h * self.n_q * self.head_dim + self.n_experts * h)
 
     def expert_bytes(self) -> int:
+        if self.expert_fp8:  # E4M3 codes plus one fp32 scale per output row
+            return 3 * self.hidden * self.inter + 4 * (2 * self.inter + self.hidden)
         return 2 * 3 * self.hidden * self.inter
 
     def kv_bytes_per_token_layer(self) -> int:
@@ -75,6 +78,13 @@ MODELS = {
                           window=4096, full_period=2),
     # a dense model: one expert that every token takes with weight 1 is a
     # SwiGLU FFN (intermediate 2048); half the layers sliding-window
+    # FP8 expert weights (E4M3 codes, one fp32 scale per output row)
+    "small_fp8": ModelShape("small_fp8", n_layers=8, hidden=1024, n_q=16, n_kv=2, head_dim=64,
+                            n_experts=32, top_k=4, inter=512, vocab=32768, page_size=64, window=0,
+                            full_period=1, expert_fp8=True),
+    "full_fp8": ModelShape("full_fp8", n_layers=48, hidden=2048, n_q=32, n_kv=4, head_dim=128,
+                           n_experts=128, top_k=8, inter=768, vocab=65536, page_size=64,
+                           window=4096, full_period=4, expert_fp8=True),
     "dense": ModelShape("dense", n_layers=8, hidden=1024, n_q=16, n_kv=2, head_dim=64, n_experts=1,
                         top_k=1, inter=2048, vocab=32768, page_size=64, window=512, full_period=2),
 }
@@ -113,6 +123,12 @@ WORKLOADS = {
                             desc="dense SwiGLU model: 8 layers, B=1, context 1024"),
     "dense_batch5": Workload("dense_batch5", "dense", 5, ("uniform", 1, 1500), 10,
                              desc="dense SwiGLU model: 8 layers, B=5, seq_lens U[1,1500]"),
+    "small_fp8": Workload("small_fp8", "small_fp8", 1, ("fixed", 1024), 12,
+                          desc="small shape with FP8 experts: 8 layers, B=1, context 1024"),
+    "small_fp8_b2": Workload("small_fp8_b2", "small_fp8", 2, ("uniform", 1, 1024), 13,
+                             desc="small shape with FP8 experts: 8 layers, B=2, seq_lens U[1,1024]"),
+    "full_fp8_bs1_8k": Workload("full_fp8_bs1_8k", "full_fp8", 1, ("fixed", 8192), 3,
+                                desc="full shape with FP8 experts, B=1, context 8192"),
     "prof_l2_8k": Workload("prof_l2_8k", "full_l2", 1, ("fixed", 8192), 7,
                            desc="full-shape layers, 2 of them, B=1, context 8192 (profiling case)"),
 }
