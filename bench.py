@@ -194,6 +194,17 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def dtype_text(sh):
+    return "f32 (fp8 E4M3 experts, bf16 other weights and KV)" if sh.expert_fp8 else "f32 (bf16 weights and KV)"
+
+
+def weights_text(sh):
+    if sh.expert_fp8:
+        return ("experts: E4M3 codes with one fp32 scale per output row (std 0.02 to 0.03 after "
+                "scaling); the rest bf16 random N(0,0.02)")
+    return "bf16 random N(0,0.02)"
+
+
 def workload_config(w, inp):
     sh = w.shape
     attn = (f"sliding window {sh.window} except every {sh.full_period}th layer" if sh.window
@@ -202,8 +213,8 @@ def workload_config(w, inp):
                                           f"{sh.n_q}q/{sh.n_kv}kv heads x {sh.head_dim}, {sh.n_experts} experts "
                                           f"top-{sh.top_k}, intermediate {sh.inter}, vocab {sh.vocab}, {attn}"),
             "global_batch": int(w.batch), "seq_len": int(inp.seq_lens.max()), "page_size": sh.page_size,
-            "weights": "bf16 random N(0,0.02)", "kv": "bf16 random N(0,1)",
-            "l2": "inputs larger than L2 (6.2 GB streamed per step), no flush",
+            "weights": weights_text(sh), "kv": "bf16 random N(0,1)",
+            "l2": "inputs larger than L2 (whole model and KV streamed every step), no flush",
             "parallelism": "replicas (no cross-GPU exchange)"}
 
 
@@ -336,7 +347,7 @@ def run_mine(args):
             "warmup": max(3, args.warmup), "ms_per_step": mean_ms,
             "ms_per_step_median": statistics.median(step_ms),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32 (bf16 weights and KV)", "data": "synthetic",
+            "dtype": dtype_text(sh), "data": "synthetic",
             "config": workload_config(w, inp),
             "hbm_bytes_per_step": alg, "achieved_TBps": achieved / 1e3,
             "frac_of_sol_8TBps": achieved / 1e3 / SOL_TBPS,

@@ -52,12 +52,18 @@ typedef struct {
   int32_t n_layers, hidden, n_q, n_kv, head_dim, n_experts, top_k, inter, vocab;
   int32_t page_size, window, full_period;
   float rope_base, eps;
+  int32_t expert_fp8;  /* 1: w_gate, w_up, w_down hold OCP FP8 E4M3 codes (1 byte each,
+                          same [L][E][rows][cols] layout) and each output row has one
+                          fp32 scale (w_*_scale): weight = e4m3 value * row scale.
+                          Schedules for it need max_batch <= 2 */
 } mk_config;
 
 /* Device pointers to the weights, row-major with the output dimension first
  * ([out][in], the layout of a linear layer's weight).  Stacked over layers
- * (and experts) with no padding.  The library keeps the pointers; the
- * caller keeps the memory alive and unchanged while the model is in use. */
+ * (and experts) with no padding.  Every pointer is 16-byte aligned (the rows
+ * are streamed by bulk copies); mk_load_model fails with MK_ERR_ARG
+ * otherwise.  The library keeps the pointers; the caller keeps the memory
+ * alive and unchanged while the model is in use. */
 typedef struct {
   const void* embedding;   /* bf16 [vocab][hidden] */
   const void* w_qkv;       /* bf16 [L][(n_q + 2 n_kv) head_dim][hidden]: q heads, k heads, v heads */
@@ -70,6 +76,9 @@ typedef struct {
   const float* norm_gamma; /* fp32 [L][hidden] input RMSNorm gain of each layer */
   const float* final_gamma;/* fp32 [hidden] final RMSNorm gain */
   const void* w_lm;        /* bf16 [vocab][hidden] */
+  const float* w_gate_scale; /* fp32 [L][n_experts][inter] (expert_fp8 only, else NULL) */
+  const float* w_up_scale;   /* fp32 [L][n_experts][inter] */
+  const float* w_down_scale; /* fp32 [L][n_experts][hidden] */
 } mk_weights;
 
 typedef struct mk_model mk_model;

@@ -183,12 +183,27 @@ int mk_load_model(const mk_config* cfg, const mk_weights* w, mk_model** out) {
   if (!w->embedding || !w->w_qkv || !w->w_o || (!w->w_router && !dense) || !w->w_gate || !w->w_up ||
       !w->w_down || !w->norm_gamma || !w->final_gamma || !w->w_lm)
     return fail(MK_ERR_ARG, "a weight pointer is null");
+  if (c.expert_fp8 != 0 && c.expert_fp8 != 1) return fail(MK_ERR_ARG, "expert_fp8 must be 0 or 1");
+  if (c.expert_fp8 && (!w->w_gate_scale || !w->w_up_scale || !w->w_down_scale))
+    return fail(MK_ERR_ARG, "FP8 experts need the three row-scale arrays");
+  const void* ptrs[] = {w->embedding, w->w_qkv, w->w_o, w->w_router, w->router_bias, w->w_gate, w->w_up,
+                        w->w_down, w->norm_gamma, w->final_gamma, w->w_lm, w->w_gate_scale, w->w_up_scale,
+                        w->w_down_scale};
+  for (const void* q : ptrs)
+    if (reinterpret_cast<uintptr_t>(q) & 15u) return fail(MK_ERR_ARG, "weight pointers must be 16-byte aligned");
+  if (c.expert_fp8) {
+    // the row scales travel with each stage in 16-byte units
+    const MoePlan p8 = moe_plan8(kShapes[id].dims);
+    // and the rows go to the tensor cores in groups of 16 (gate/up: 8 + 8)
+    if (p8.up_half % 8 || p8.dn_rows % 16 || 2 * p8.up_half > kMaxStageRows || p8.dn_rows > kMaxStageRows)
+      return fail(MK_ERR_UNSUPPORTED, "no FP8 stage plan for this model shape");
+  }
   mk_model* m = new mk_model();
   m->cfg = c;
   m->w = *w;
   m->shape_id = id;
   m->dims = kShapes[id].dims;
-  m->plan = moe_plan(m->dims);
+  m->plan = c.expert_fp8 ? moe_plan8(m->dims) : moe_plan(m->dims);
   *out = m;
   return MK_OK;
 }
@@ -253,6 +268,10 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   p.wg = static_cast<const uint16_t*>(w.w_gate);
   p.wu = static_cast<const uint16_t*>(w.w_up);
   p.wd = static_cast<const uint16_t*>(w.w_down);
+  p.expert_fp8 = m->cfg.expert_fp8;
+  p.sg = w.w_gate_scale;
+  p.su = w.w_up_scale;
+  p.sd = w.w_down_scale;
   p.gamma = w.norm_gamma;
   p.gamma_f = w.final_gamma;
   p.wlm = static_cast<const uint16_t*>(w.w_lm);
@@ -352,6 +371,8 @@ int mk_check_step(const mk_sched* s, const void* workspace, void* stream) {
   if (rec[0] == 4) return fail(MK_ERR_DEVICE, "shared memory base not 1024-byte aligned" + where);
   if (rec[0] == 5)
     return fail(MK_ERR_DEVICE, "descriptor or work ring out of step (a stale entry was read)" + where);
+  if (rec[0] == 6)
+    return fail(MK_ERR_DEVICE, "an FP8 expert tile's activation is beyond the f16 range (|x| > 65504)" + where);
   return fail(MK_ERR_DEVICE, "index out of range" + where);
 }
 

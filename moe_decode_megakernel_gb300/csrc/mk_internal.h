@@ -126,6 +126,16 @@ constexpr int moe_stages(int rows, int rows_per_stage, int min_tiles) {
     if (rows % (cand[i] * rows_per_stage) == 0 && rows / (cand[i] * rows_per_stage) >= min_tiles) return cand[i];
   return 1;
 }
+// Rows of a [rows][k] matrix of 1-byte (FP8) elements per stage: a power of
+// two (so the stages divide the power-of-two matrix sides), at most 64.
+constexpr int stage_rows8(int k) {
+  int r = kStageBytes / k;
+  r = r > kMaxStageRows ? kMaxStageRows : r;
+  int p = 8;
+  while (p * 2 <= r) p *= 2;
+  return r >= 8 ? p : r;
+}
+
 constexpr MoePlan moe_plan(ShapeDims s) {
   MoePlan p{};
   p.up_half = stage_rows(s.H) / 2;
@@ -133,6 +143,19 @@ constexpr MoePlan moe_plan(ShapeDims s) {
   p.up_tile = p.up_half * p.up_stages;
   p.up_tiles = s.I / p.up_tile;
   p.dn_rows = stage_rows(s.I);
+  p.dn_stages = moe_stages(s.H, p.dn_rows, 32);
+  p.dn_tile = p.dn_rows * p.dn_stages;
+  p.dn_tiles = s.H / p.dn_tile;
+  return p;
+}
+// the same plan for FP8 expert rows (twice the rows per stage)
+constexpr MoePlan moe_plan8(ShapeDims s) {
+  MoePlan p{};
+  p.up_half = stage_rows8(s.H) / 2;
+  p.up_stages = moe_stages(s.I, p.up_half, 16);
+  p.up_tile = p.up_half * p.up_stages;
+  p.up_tiles = s.I / p.up_tile;
+  p.dn_rows = stage_rows8(s.I);
   p.dn_stages = moe_stages(s.H, p.dn_rows, 32);
   p.dn_tile = p.dn_rows * p.dn_stages;
   p.dn_tiles = s.H / p.dn_tile;
@@ -150,9 +173,13 @@ struct Params {
   const uint16_t* wo;
   const uint16_t* wr;
   const float* rbias;
-  const uint16_t* wg;
+  const uint16_t* wg;   // bf16, or FP8 (E4M3 bytes) when expert_fp8
   const uint16_t* wu;
   const uint16_t* wd;
+  int expert_fp8;       // expert rows are E4M3 bytes with one fp32 scale per row
+  const float* sg;      // [L][E][I] row scales of w_gate (FP8 only)
+  const float* su;      // [L][E][I]
+  const float* sd;      // [L][E][H]
   const float* gamma;
   const float* gamma_f;
   const uint16_t* wlm;

@@ -35,7 +35,7 @@
 namespace mk {
 namespace dev {
 
-constexpr uint32_t ERR_TIMEOUT = 1, ERR_PAGE = 2, ERR_INDEX = 3, ERR_SMEM_ALIGN = 4, ERR_RING = 5;
+constexpr uint32_t ERR_TIMEOUT = 1, ERR_PAGE = 2, ERR_INDEX = 3, ERR_SMEM_ALIGN = 4, ERR_RING = 5, ERR_RANGE = 6;
 constexpr uint32_t FULL = 0xffffffffu;
 constexpr int kBarConsumers = 1;  // named barrier id of the consumer warps
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
@@ -116,6 +116,28 @@ __device__ __forceinline__ void dot8_bf16(uint4 u, uint4 xa, uint4 xb, float& a,
   ffma2(a, b, __uint_as_float(u.z << 16), __uint_as_float(u.z & 0xffff0000u), __uint_as_float(xb.x), __uint_as_float(xb.y));
   ffma2(a, b, __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xffff0000u), __uint_as_float(xb.z), __uint_as_float(xb.w));
 }
+// Four E4M3 codes (bytes of c, lowest first) as two f16x2 words: lo holds
+// bytes 0 and 1, hi bytes 2 and 3 (the lower byte in the lower half).  Every
+// E4M3 value is exact in f16.
+__device__ __forceinline__ void e4m3x4_f16(uint32_t c, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(c));
+}
+// f16x2 of (a, b), a in the lower half, round to nearest even
+__device__ __forceinline__ uint32_t f16x2_rn(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+// the two halves of an f16x2 word as binary32 (exact)
+__device__ __forceinline__ float2 f16x2_f32(uint32_t h) {
+  float a, b;
+  asm("{\n .reg .b16 x, y;\n mov.b32 {x, y}, %2;\n cvt.f32.f16 %0, x;\n cvt.f32.f16 %1, y;\n}"
+      : "=f"(a), "=f"(b)
+      : "r"(h));
+  return make_float2(a, b);
+}
 // 2-D TMA tile load (coordinates: x = element along the inner dimension, y = row).
 __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* b, uint64_t policy) {
   asm volatile(
@@ -141,6 +163,14 @@ __device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t&
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 // D += A (16x16, row) * B (16x8, col): BF16 operands, fp32 accumulation.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -272,6 +302,9 @@ struct Hdr {
   uint64_t done[kWorkRing];  // consumers finished the item in this slot
   int32_t desc[kDescRing][32];
   int32_t work[kWorkRing][32];
+  // FP8 expert stages: the fp32 scales of the stage's rows, copied with the
+  // rows (same full barrier); up/gate stages hold gate scales then up scales
+  alignas(16) float scl[kStages][kMaxStageRows];
   volatile int32_t abort;
   int32_t pad[31];
 };
@@ -281,6 +314,13 @@ struct Hdr {
 template <class S>
 __host__ __device__ constexpr int xs_row() {
   return S::H > S::I ? (S::H > S::G * S::D ? S::H : S::G * S::D) : (S::I > S::G * S::D ? S::I : S::G * S::D);
+}
+
+// The MoE tile plan of the step's expert weights (BF16 or FP8 rows).
+template <class S>
+__device__ __forceinline__ MoePlan plan_of(const Params& p) {
+  constexpr MoePlan m16 = S::mp, m8 = S::mp8;
+  return p.expert_fp8 ? m8 : m16;
 }
 
 template <class S>
@@ -320,6 +360,7 @@ struct Shape {
   static constexpr int QKV = (NQ + 2 * NKV) * D;
   static constexpr ShapeDims dims{H, NQ, NKV, D, E, K, I, P};
   static constexpr MoePlan mp = moe_plan(dims);
+  static constexpr MoePlan mp8 = moe_plan8(dims);  // FP8 expert rows
   static constexpr int SR_H = stage_rows(H), SR_O = stage_rows(G * D), SR_I = stage_rows(I);
   static_assert(H % 256 == 0 && (G * D) % 8 == 0 && I % 8 == 0, "row chunks");
   static_assert(D % 32 == 0 && 32 % G == 0 && (G * D) % 4 == 0, "attention lane maps");
@@ -712,8 +753,8 @@ struct Producer {
       if (p.stats) c.stat[1] += gtimer() - t0;
       if (!ok) return false;
     }
-    constexpr MoePlan mp = S::mp;
-    constexpr int U = mp.up_tiles, DN = mp.dn_tiles;
+    const MoePlan mp = plan_of<S>(p);
+    const int U = mp.up_tiles, DN = mp.dn_tiles;
     const int n_act = min(__ldcg(p.qlen), S::E);
     const uint32_t total = (uint32_t)n_act * (mode == 0 ? U + DN : mode == 1 ? U : DN);
     uint32_t* claim = p.bars + d[F_A0];
@@ -839,20 +880,49 @@ struct Producer {
 
   // The weight stages of tile t of expert e: up/gate stages of up_half gate
   // rows and as many up rows, or down stages of dn_rows rows of W_down[e].
+  // FP8 rows are 1 byte per weight: a row of K weights is K / 2 16-bit units.
   __device__ __forceinline__ bool tile_stages(int l, int e, int t, bool up) {
-    constexpr MoePlan mp = S::mp;
+    const MoePlan mp = plan_of<S>(p);
     const int64_t le = (int64_t)l * S::E + e;
-    if (!up) return load_rows(p.wd + le * S::H * S::I, S::I, S::I, t * mp.dn_tile, mp.dn_tile, mp.dn_rows);
+    const int eb = p.expert_fp8 ? 1 : 2;  // bytes per weight
+    if (!up && !p.expert_fp8) {
+      const uint16_t* base = reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(p.wd) +
+                                                               le * S::H * S::I * eb);
+      return load_rows(base, S::I, S::I, t * mp.dn_tile, mp.dn_tile, mp.dn_rows);
+    }
+    if (!up) {
+      // FP8 down stages: dn_rows rows of I bytes and their dn_rows scales
+      const uint8_t* wd = reinterpret_cast<const uint8_t*>(p.wd) + le * S::H * S::I;
+      for (int s = 0; s < mp.dn_stages; ++s) {
+        int slot;
+        if (!acquire_stage(slot)) return false;
+        uint64_t* fb = &c.hdr->full[slot];
+        const int r0 = t * mp.dn_tile + s * mp.dn_rows;
+        const uint32_t bytes = (uint32_t)mp.dn_rows * S::I;
+        mbar_expect_tx(fb, bytes + (uint32_t)mp.dn_rows * 4);
+        bulk_g2s_hint(stage(slot), wd + (int64_t)r0 * S::I, bytes, fb, stream_policy);
+        bulk_g2s(c.hdr->scl[slot], p.sd + le * S::H + r0, (uint32_t)mp.dn_rows * 4, fb);
+        ++c.st;
+      }
+      return true;
+    }
+    const uint8_t* wg = reinterpret_cast<const uint8_t*>(p.wg);
+    const uint8_t* wu = reinterpret_cast<const uint8_t*>(p.wu);
     for (int s = 0; s < mp.up_stages; ++s) {
       int slot;
       if (!acquire_stage(slot)) return false;
       uint64_t* fb = &c.hdr->full[slot];
       uint8_t* dst = stage(slot);
       const int r0 = t * mp.up_tile + s * mp.up_half;
-      const uint32_t half = (uint32_t)mp.up_half * S::H * 2;
-      mbar_expect_tx(fb, 2 * half);
-      bulk_g2s_hint(dst, p.wg + (le * S::I + r0) * S::H, half, fb, stream_policy);
-      bulk_g2s_hint(dst + half, p.wu + (le * S::I + r0) * S::H, half, fb, stream_policy);
+      const uint32_t half = (uint32_t)mp.up_half * S::H * eb;
+      const uint32_t sb = p.expert_fp8 ? (uint32_t)mp.up_half * 4 : 0u;  // FP8: scales
+      mbar_expect_tx(fb, 2 * half + 2 * sb);
+      bulk_g2s_hint(dst, wg + (le * S::I + r0) * S::H * eb, half, fb, stream_policy);
+      bulk_g2s_hint(dst + half, wu + (le * S::I + r0) * S::H * eb, half, fb, stream_policy);
+      if (sb) {
+        bulk_g2s(c.hdr->scl[slot], p.sg + le * S::I + r0, sb, fb);
+        bulk_g2s(c.hdr->scl[slot] + mp.up_half, p.su + le * S::I + r0, sb, fb);
+      }
       ++c.st;
     }
     return true;
@@ -863,7 +933,7 @@ struct Producer {
   // the batch; the same work item as an MoE tile, with each row its own slot
   // and weight 1 (the dense flag A12).
   __device__ __forceinline__ bool ffn_tile(const int32_t* d) {
-    constexpr MoePlan mp = S::mp;
+    const MoePlan mp = plan_of<S>(p);
     const bool up = d[F_OP] == OP_FFN_UPGATE_ACT;
     int32_t it[32];
     for (int k = 0; k < 32; ++k) it[k] = d[k];
@@ -1210,6 +1280,155 @@ struct Consumer {
     }
   }
 
+  // Activation rows of an FP8 expert tile as the B operand of f16 MMAs
+  // (m16n8k16, the weights as A).  Column 2t of B is the f16 rounding of
+  // activation row t, column 2t + 1 the f16 rounding of what that leaves
+  // (x - hi): hi + lo carry about 22 bits of x, and the MMA accumulates in
+  // fp32.  In one MMA, thread (n = lane / 4, q = lane % 4) holds the logical
+  // k 2q, 2q+1, 2q+8, 2q+9; they stand for the physical elements
+  // 64 kc + 16 q + 4 j + 0..3 of MMA j (0..3) of 64-element chunk kc, which
+  // are the bytes one 16-byte load of a weight row gives thread q.  Layout:
+  // uint4 [kc][j / 2][n][q] holding the (b0b1, b2b3) words of MMAs 2(j/2) and
+  // 2(j/2) + 1.  An activation beyond the f16 range is reported as an error.
+  template <int K>
+  __device__ __forceinline__ void load_x_f16(int op, const int32_t* w, int tb) {
+    static_assert(kTB <= 2 && K * 8 <= (int)sizeof(sm.xs), "the hi/lo columns of kTB rows of K fit the cache");
+    constexpr int U = K / 8;  // 8-element units per row
+    uint4* xb = reinterpret_cast<uint4*>(sm.xs);
+    int bad = -1;
+    for (int i = ct; i < tb * U; i += kConsumerThreads) {
+      const int t = i / U, m = i - t * U;
+      const float4* src = reinterpret_cast<const float4*>(x_src(op, w, t)) + 2 * m;
+      const float4 a = __ldcg(src), b = __ldcg(src + 1);
+      const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (fabsf(v[2 * k]) > 65504.f || fabsf(v[2 * k + 1]) > 65504.f) bad = 8 * m + 2 * k;
+        hi[k] = f16x2_rn(v[2 * k], v[2 * k + 1]);
+        const float2 h = f16x2_f32(hi[k]);
+        lo[k] = f16x2_rn(v[2 * k] - h.x, v[2 * k + 1] - h.y);
+      }
+      const int e = 8 * m, kc = e >> 6, q = (e >> 4) & 3, jp = (e >> 3) & 1;
+      const int at = (kc * 2 + jp) * 16 + q;
+      xb[at + 2 * t * 4] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      xb[at + (2 * t + 1) * 4] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    if (bad >= 0) record_error(p, ERR_RANGE, c.sm, where_of(w), bad, 0u, 65504u);
+  }
+
+  // FP8 expert tiles (batch <= kTB) on the tensor cores.  A stage's rows, 16
+  // at a time, are the A operand of m16n8k16 MMAs (each E4M3 code converted
+  // exactly to f16), the activations' hi/lo columns the B operand; the row
+  // scale multiplies the finished fp32 dot product.  The same four teams of
+  // two warps take the stages; a warp takes whole 16-row groups, or, when a
+  // stage is one group, half of its chunks, the halves added through shared
+  // memory.  A group pairs what one thread finishes: gate row i with up row
+  // i (up/gate), rows 2i and 2i + 1 (down).
+  static constexpr int kBarTeam0 = kBarConsumers + 1;  // named barriers of the teams' warp pairs
+  template <int K, int TB>
+  __device__ __forceinline__ void gemv_item_fp8(const int32_t* w, int SR, int ntok) {
+    static_assert(K % 128 == 0, "FP8 rows in pairs of 64-byte chunks");
+    static_assert(kTeamWarps == 2 && kTeams * 2 * kTB * 16 <= (int)(sizeof(sm.out) / sizeof(float)),
+                  "partial sums of split stages fit the stage-output buffer");
+    constexpr int NP = K / 128;  // pairs of 64-byte chunks per row
+    const int op = w[F_OP];
+    const int nst = w[F_NSTAGE];
+    const int tb = ntok;
+    const int g = lane >> 2, q = lane & 3;
+    // epilogue inputs of activation row t = q, from the item
+    int dslot = 0;
+    float dwt = 0.f;
+    if (op == W_DOWN_TILE && q < tb) {
+      dslot = q == 0 ? w[F_A0 + 8] : w[F_A0 + 9];
+      dwt = __int_as_float(q == 0 ? w[F_A0 + 10] : w[F_A0 + 11]);
+    }
+    int32_t tag[4];
+    x_tag(op, w, 0, tag);
+    tag[0] += 16;  // the same rows in the f16 hi/lo layout
+    if (!(tag[0] == sm.xtag[0] && tag[1] == sm.xtag[1] && tag[2] == sm.xtag[2] && tag[3] == sm.xtag[3])) {
+      if (!aborted(c)) load_x_f16<K>(op, w, tb);
+      consumers_sync();
+      if (ct == 0) {
+        sm.xtag[0] = tag[0]; sm.xtag[1] = tag[1]; sm.xtag[2] = tag[2]; sm.xtag[3] = tag[3];
+      }
+    }
+    const int team = cw / kTeamWarps, tw = cw % kTeamWarps;
+    const bool up = op == W_UP_TILE;
+    const int ngroups = SR / 16;
+    const bool split = ngroups < kTeamWarps;
+    const bool bon = g < 2 * (TB == 1 ? 1 : tb);  // lanes that hold a B column
+    const uint32_t xb_a = smem_u32(sm.xs) + (uint32_t)lane * 16u;
+    float* red = &sm.out[0][0];  // [team][2][kTB][16]
+    int it = 0;
+    for (int s = team; s < nst; s += kTeams, ++it) {
+      const uint32_t gs = c.st + (uint32_t)s;
+      const int slot = gs % kStages;
+      bool ok = s < kStages || mbar_wait(p, c, &c.hdr->empty[slot], ((gs / kStages) - 1) & 1);
+      ok = __all_sync(FULL, ok && mbar_wait(p, c, &c.hdr->full[slot], (gs / kStages) & 1) && !aborted(c));
+      const uint32_t st = smem_u32(stage(slot)) + (uint32_t)q * 16u;
+      for (int grp = split ? 0 : tw; grp < ngroups; grp += split ? ngroups : kTeamWarps) {
+        const int rlo = up ? 8 * grp + g : 16 * grp + 2 * g;
+        const int rhi = up ? SR / 2 + 8 * grp + g : rlo + 1;
+        const int m0 = split ? tw * NP / 2 : 0, m1 = split ? (tw + 1) * NP / 2 : NP;
+        float d[4][4];  // one accumulator per MMA slot j: four independent chains
+#pragma unroll
+        for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+        if (ok) {
+          const uint32_t alo = st + (uint32_t)(rlo * K), ahi = st + (uint32_t)(rhi * K);
+          for (int m = m0; m < m1; ++m) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int kc = 2 * m + h;
+              const uint4 ul = lds128(alo + (uint32_t)(kc * 64)), uh = lds128(ahi + (uint32_t)(kc * 64));
+              uint4 b01 = make_uint4(0u, 0u, 0u, 0u), b23 = b01;
+              if (bon) {
+                b01 = lds128(xb_a + (uint32_t)((2 * kc) * 256));
+                b23 = lds128(xb_a + (uint32_t)((2 * kc + 1) * 256));
+              }
+              uint32_t a0, a1, a2, a3;
+              e4m3x4_f16(ul.x, a0, a2);
+              e4m3x4_f16(uh.x, a1, a3);
+              mma_f16(d[0], a0, a1, a2, a3, b01.x, b01.y);
+              e4m3x4_f16(ul.y, a0, a2);
+              e4m3x4_f16(uh.y, a1, a3);
+              mma_f16(d[1], a0, a1, a2, a3, b01.z, b01.w);
+              e4m3x4_f16(ul.z, a0, a2);
+              e4m3x4_f16(uh.z, a1, a3);
+              mma_f16(d[2], a0, a1, a2, a3, b23.x, b23.y);
+              e4m3x4_f16(ul.w, a0, a2);
+              e4m3x4_f16(uh.w, a1, a3);
+              mma_f16(d[3], a0, a1, a2, a3, b23.z, b23.w);
+            }
+          }
+        }
+        // column 2t + {0, 1} of rows g and g + 8: thread q = t holds both
+        float vlo = (d[0][0] + d[1][0]) + (d[2][0] + d[3][0]) + ((d[0][1] + d[1][1]) + (d[2][1] + d[3][1]));
+        float vhi = (d[0][2] + d[1][2]) + (d[2][2] + d[3][2]) + ((d[0][3] + d[1][3]) + (d[2][3] + d[3][3]));
+        if (split) {
+          float* rb = red + (team * 2 + (it & 1)) * kTB * 16;
+          if (tw == 1 && q < tb) {
+            rb[q * 16 + g] = vlo;
+            rb[q * 16 + 8 + g] = vhi;
+          }
+          bar_sync(kBarTeam0 + team, 2 * 32);
+          if (tw == 1) continue;
+          if (q < tb) {
+            vlo += rb[q * 16 + g];
+            vhi += rb[q * 16 + 8 + g];
+          }
+        }
+        if (ok && q < tb && !aborted(c)) {
+          const float slo = c.hdr->scl[slot][rlo], shi = c.hdr->scl[slot][rhi];
+          pair_epilogue(op, w, s, up ? 8 * grp + g : rlo, rhi, q, vlo * slo, vhi * shi, dslot, dwt);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_n(&c.hdr->empty[slot], kConsumerWarps / kTeamWarps);
+    }
+    c.st += (uint32_t)nst;
+  }
+
   // Pair epilogue, run by lane t for activation row t: v0, v1 are the dot
   // products of the pair's two weight rows r0, r1 (rows of stage s).
   __device__ __forceinline__ void pair_epilogue(int op, const int32_t* w, int s, int r0, int r1, int t, float v0,
@@ -1248,9 +1467,10 @@ struct Consumer {
         break;
       }
       case W_UP_TILE: {  // SiLU(gate) * up ("Tasks": the SiLU-and-multiply epilogue)
+        const MoePlan mp = plan_of<S>(p);
         const float act = v0 / (1.f + expf(-v0)) * v1;
         const int row = w[F_A0 + 2] + t;
-        p.u[(int64_t)row * S::I + w[F_A0 + 1] * S::mp.up_tile + s * S::mp.up_half + r0] = act;
+        p.u[(int64_t)row * S::I + w[F_A0 + 1] * mp.up_tile + s * mp.up_half + r0] = act;
         break;
       }
       case OP_ROUTER_GEMM: {
@@ -1272,7 +1492,8 @@ struct Consumer {
         break;
       }
       case W_DOWN_TILE: {  // weighted, into the (row b, slot j) of the output
-        const int n = w[F_A0 + 1] * S::mp.dn_tile + s * S::mp.dn_rows + r0;
+        const MoePlan mp = plan_of<S>(p);
+        const int n = w[F_A0 + 1] * mp.dn_tile + s * mp.dn_rows + r0;
         *reinterpret_cast<float2*>(p.y + (int64_t)dslot * S::H + n) = make_float2(dwt * v0, dwt * v1);
         break;
       }
@@ -2147,13 +2368,21 @@ struct Consumer {
         else gemv_item<S::G * S::D>(w, S::SR_O, w[F_A0 + 1], p.B);
         break;
       case W_UP_TILE:
-        if (w[F_A0 + 3] <= kTB)
+        if (p.expert_fp8) {  // schedules with FP8 experts have max_batch <= kTB
+          constexpr MoePlan m8 = S::mp8;
+          if (w[F_A0 + 3] <= 1) gemv_item_fp8<S::H, 1>(w, 2 * m8.up_half, w[F_A0 + 3]);
+          else gemv_item_fp8<S::H, kTB>(w, 2 * m8.up_half, w[F_A0 + 3]);
+        } else if (w[F_A0 + 3] <= kTB)
           gemv_item_teams<S::H>(w, 2 * S::mp.up_half, 2 * S::mp.up_half * S::mp.up_stages, w[F_A0 + 3]);
         else
           gemv_item<S::H>(w, 2 * S::mp.up_half, 2 * S::mp.up_half * S::mp.up_stages, w[F_A0 + 3]);
         break;
       case W_DOWN_TILE:
-        if (w[F_A0 + 3] <= kTB) gemv_item_teams<S::I>(w, S::mp.dn_rows, S::mp.dn_tile, w[F_A0 + 3]);
+        if (p.expert_fp8) {
+          constexpr MoePlan m8 = S::mp8;
+          if (w[F_A0 + 3] <= 1) gemv_item_fp8<S::I, 1>(w, m8.dn_rows, w[F_A0 + 3]);
+          else gemv_item_fp8<S::I, kTB>(w, m8.dn_rows, w[F_A0 + 3]);
+        } else if (w[F_A0 + 3] <= kTB) gemv_item_teams<S::I>(w, S::mp.dn_rows, S::mp.dn_tile, w[F_A0 + 3]);
         else gemv_item<S::I>(w, S::mp.dn_rows, S::mp.dn_tile, w[F_A0 + 3]);
         break;
       case W_ATTN: attn(w); break;

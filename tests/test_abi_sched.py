@@ -54,6 +54,16 @@ def test_load_model_rejects_unknown_shape():
     assert e.value.code == mk.MK_ERR_ARG
 
 
+def test_load_model_rejects_misaligned_weights():
+    n = len(mk.MkWeights._fields_)
+    for i in range(n):  # every pointer is streamed in 16-byte units
+        ptrs = [0x10000 * (k + 1) for k in range(n)]
+        ptrs[i] += 8
+        with pytest.raises(mk.MkError) as e:
+            mk.Model(mk.config_from(synth.MODELS["tiny"]), mk.MkWeights(*ptrs))
+        assert e.value.code == mk.MK_ERR_ARG, mk.MkWeights._fields_[i]
+
+
 def sched_for(workload, **opts):
     w = synth.WORKLOADS[workload]
     inp = synth.make_inputs(w)

@@ -9,6 +9,8 @@ import pytest
 
 import oracle
 import synth
+import moe_decode_megakernel_gb300 as mk
+from test_abi_sched import fake_model, NUM_SMS
 
 
 def test_golden_codes():
@@ -72,3 +74,20 @@ def test_oracle_fp8_expert_rows():
     sc = synth.fill_scales_host(sh.hidden, seed, synth.SD, layer, expert, sh.weight_sigma)
     want = np.vectorize(oracle.e4m3_value)(codes) * sc[:, None].astype(np.float64)
     assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("workload", ["small_fp8", "small_fp8_b2"])
+def test_fp8_schedules(workload):
+    w = synth.WORKLOADS[workload]
+    inp = synth.make_inputs(w)
+    m = fake_model(w.shape)
+    s = mk.Sched(m, w.batch, int(inp.seq_lens.max()), mk.default_sched_opts(num_sms=NUM_SMS))
+    s.validate()
+    s.simulate(inp.seq_lens, seed=4)
+
+
+def test_fp8_needs_small_batch():
+    m = fake_model(synth.MODELS["small_fp8"])
+    with pytest.raises(mk.MkError) as e:
+        mk.Sched(m, 3, 1024, mk.default_sched_opts(num_sms=NUM_SMS))
+    assert e.value.code == mk.MK_ERR_UNSUPPORTED
