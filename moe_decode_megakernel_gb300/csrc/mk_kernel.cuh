@@ -744,22 +744,40 @@ struct Producer {
   // Otherwise claimer c takes unit c first without an atomic and later units
   // from the layer's claim counter, offset by n, each claim issued before the
   // current tile streams.
+  // the layer whose routing this SM's MoE drains have already waited for,
+  // and its active-expert count
+  int routed_layer = -1, routed_n_act = 0;
+
   __device__ __forceinline__ bool moe_drain(const int32_t* d, int mode) {
     const int l = d[F_LAYER];
+    const MoePlan mp = plan_of<S>(p);
+    const int U = mp.up_tiles, DN = mp.dn_tiles;
+    uint32_t* claim = p.bars + d[F_A0];
+    const uint32_t n_claimers = (uint32_t)d[F_A0 + 5];
+    const bool stat = d[F_A0 + 7] != 0;
     // the routing decides which expert rows to stream: wait for the queue
-    {
+    // (once per layer: the down drain follows the up/gate drain's wait)
+    int n_act;
+    int4 first = make_int4(0, 0, 0, 0);
+    int first_a = -1;
+    if (routed_layer == l) {
+      n_act = routed_n_act;
+    } else {
       const int64_t t0 = p.stats ? gtimer() : 0;
       const bool ok = wait_counters(p, c, d[F_WAIT0], (uint32_t)d[F_TGT0], d[F_WAIT1], (uint32_t)d[F_TGT1], where_of(d));
       if (p.stats) c.stat[1] += gtimer() - t0;
       if (!ok) return false;
+      // the active-expert count and a static claimer's first queue record in
+      // one round trip (the record is read before knowing it is in range)
+      if (stat && mode == 1 && (int)d[F_A0 + 4] / U < S::E) {
+        first_a = (int)d[F_A0 + 4] / U;
+        first = __ldcg(reinterpret_cast<const int4*>(p.act) + first_a);
+      }
+      n_act = min(__ldcg(p.qlen), S::E);
+      routed_layer = l;
+      routed_n_act = n_act;
     }
-    const MoePlan mp = plan_of<S>(p);
-    const int U = mp.up_tiles, DN = mp.dn_tiles;
-    const int n_act = min(__ldcg(p.qlen), S::E);
     const uint32_t total = (uint32_t)n_act * (mode == 0 ? U + DN : mode == 1 ? U : DN);
-    uint32_t* claim = p.bars + d[F_A0];
-    const uint32_t n_claimers = (uint32_t)d[F_A0 + 5];
-    const bool stat = d[F_A0 + 7] != 0;
     uint32_t cur = (uint32_t)d[F_A0 + 4];
     // static assignment: units cur, cur + n, ...; the down units start after
     // the last up unit, so the claimers with an extra up/gate tile get no
@@ -776,8 +794,8 @@ struct Producer {
       }
     }
     bool carried = false;  // the last unit carried the drain's signal
-    int cached_a = -1, dn_a = -1;
-    int4 info = make_int4(0, 0, 0, 0);
+    int cached_a = first_a, dn_a = -1;
+    int4 info = first;
     int32_t dn_slot[kTB] = {}, dn_wt[kTB] = {};  // a down tile's rows: output slot and routing weight
     while (cur < total) {
       if (aborted(c)) return false;
