@@ -28,7 +28,7 @@ class OrcConfig(ctypes.Structure):
                                      "n_experts", "top_k", "inter", "vocab", "page_size",
                                      "window", "full_period")] + \
                [(n, c_double) for n in ("rope_base", "eps", "weight_sigma", "kv_sigma")] + \
-               [("expert_fp8", c_int)]
+               [("expert_fp8", c_int), ("expert_fp4", c_int)]
 
 
 class OrcMatrix(ctypes.Structure):
@@ -69,6 +69,8 @@ def lib():
         L.orc_synth_dense.restype = ctypes.c_int64
         L.orc_e4m3_value.argtypes = [c_int]
         L.orc_e4m3_value.restype = c_double
+        L.orc_e2m1_value.argtypes = [c_int]
+        L.orc_e2m1_value.restype = c_double
         L.orc_silu.argtypes = [c_double]
         L.orc_silu.restype = c_double
         L.orc_matvec.argtypes = [ctypes.POINTER(OrcMatrix), P_D, P_D]
@@ -111,7 +113,8 @@ def config_from_shape(shape) -> OrcConfig:
     return OrcConfig(shape.n_layers, shape.hidden, shape.n_q, shape.n_kv, shape.head_dim,
                      shape.n_experts, shape.top_k, shape.inter, shape.vocab, shape.page_size,
                      shape.window, shape.full_period, shape.rope_base, shape.eps,
-                     shape.weight_sigma, shape.kv_sigma, int(getattr(shape, "expert_fp8", False)))
+                     shape.weight_sigma, shape.kv_sigma, int(getattr(shape, "expert_fp8", False)),
+                     int(getattr(shape, "expert_fp4", False)))
 
 
 # ----------------------------------------------------------- layer operations
@@ -142,7 +145,7 @@ def silu(x):
 
 
 def synth_matrix(shape, seed: int, kind: int, layer: int = 0, expert: int = 0) -> np.ndarray:
-    """A weight matrix exactly as the oracle reads it (FP8 experts dequantized)."""
+    """A weight matrix exactly as the oracle reads it (FP8 / FP4 experts dequantized)."""
     rows, cols = {synth_kinds.WG: (shape.inter, shape.hidden), synth_kinds.WU: (shape.inter, shape.hidden),
                   synth_kinds.WD: (shape.hidden, shape.inter)}[kind]
     cfg = config_from_shape(shape)
@@ -150,6 +153,11 @@ def synth_matrix(shape, seed: int, kind: int, layer: int = 0, expert: int = 0) -
     n = lib().orc_synth_dense(ctypes.byref(cfg), seed, kind, layer, expert, _d(out))
     assert n == rows * cols
     return out
+
+
+def e2m1_value(code: int) -> float:
+    """The value of an FP4 E2M1 code (the oracle's own decoding)."""
+    return lib().orc_e2m1_value(int(code))
 
 
 def e4m3_value(code: int) -> float:

@@ -243,6 +243,12 @@ double orc_e4m3_value(int code) {
   return (code & 0x80) ? -v : v;
 }
 
+double orc_e2m1_value(int code) {
+  const int e = (code >> 1) & 3, m = code & 1;
+  const double v = e ? ldexp(1.0 + m / 2.0, e - 1) : m / 2.0;
+  return (code & 8) ? -v : v;
+}
+
 void orc_synth_row(const void* ctx, int row, double* out) {
   const orc_synth_src* s = (const orc_synth_src*)ctx;
   const uint64_t key = synth_key(s->seed, synth_stream((uint32_t)s->kind, (uint32_t)s->layer,
@@ -255,6 +261,26 @@ void orc_synth_row(const void* ctx, int row, double* out) {
     const double scale = (double)synth_row_scale(skey, (uint64_t)row, synth_fp8_base(s->sigma));
     const uint64_t base = (uint64_t)row * (uint64_t)s->cols;
     for (int c = 0; c < s->cols; ++c) out[c] = orc_e4m3_value(synth_fp8(key, base + (uint64_t)c)) * scale;
+    return;
+  }
+  if (s->cfg->expert_fp4 && (s->kind == SYNTH_WG || s->kind == SYNTH_WU || s->kind == SYNTH_WD)) {
+    /* an FP4 expert row: element i of the matrix is nibble i % 2 of byte i / 2;
+       each 16 elements of the row share a block scale, the row a row scale */
+    const int skind = s->kind == SYNTH_WG ? SYNTH_SG : s->kind == SYNTH_WU ? SYNTH_SU : SYNTH_SD;
+    const int bkind = s->kind == SYNTH_WG ? SYNTH_BG : s->kind == SYNTH_WU ? SYNTH_BU : SYNTH_BD;
+    const uint64_t skey = synth_key(s->seed, synth_stream((uint32_t)skind, (uint32_t)s->layer,
+                                                          (uint32_t)s->expert));
+    const uint64_t bkey = synth_key(s->seed, synth_stream((uint32_t)bkind, (uint32_t)s->layer,
+                                                          (uint32_t)s->expert));
+    const double rscale = (double)synth_row_scale(skey, (uint64_t)row, synth_fp4_base(s->sigma));
+    const uint64_t base = (uint64_t)row * (uint64_t)s->cols;
+    for (int c = 0; c < s->cols; ++c) {
+      const uint64_t i = base + (uint64_t)c;
+      const int byte = synth_fp4_byte(key, i / 2);
+      const int code = (i & 1) ? byte >> 4 : byte & 15;
+      const int bcode = synth_fp4_bscale(bkey, (uint64_t)row * (uint64_t)(s->cols / 16) + (uint64_t)(c / 16));
+      out[c] = orc_e2m1_value(code) * orc_e4m3_value(bcode) * rscale;
+    }
     return;
   }
   const float scale = synth_scale(s->sigma);
@@ -317,7 +343,8 @@ static int config_ok(const orc_config* c) {
   return c->n_layers > 0 && c->hidden > 0 && c->n_q > 0 && c->n_kv > 0 &&
          c->n_q % c->n_kv == 0 && c->head_dim > 0 && c->head_dim % 2 == 0 &&
          c->n_experts > 0 && c->top_k > 0 && c->top_k <= c->n_experts && c->inter > 0 &&
-         c->vocab > 0 && c->page_size > 0 && c->window >= 0 && c->full_period > 0;
+         c->vocab > 0 && c->page_size > 0 && c->window >= 0 && c->full_period > 0 &&
+         !(c->expert_fp8 && c->expert_fp4) && (!c->expert_fp4 || (c->hidden % 16 == 0 && c->inter % 16 == 0));
 }
 
 /* One decode step for the requested rows.  The layer is the parallel layer

@@ -36,7 +36,13 @@ typedef struct {
   int full_period; /* layer l attends to the whole context iff window == 0 or (l+1) % full_period == 0 */
   double rope_base, eps, weight_sigma, kv_sigma;
   int expert_fp8;  /* 1: expert matrices are E4M3 codes times one scale per output row */
+  int expert_fp4;  /* 1: expert matrices are E2M1 codes times an E4M3 scale per 16 inputs
+                      times one scale per output row */
 } orc_config;
+
+/* FP4 E2M1 code (4 bits) -> value: (-1)^s 2^(e-1) (1 + m/2) for exponent field
+ * e > 0, (-1)^s m/2 for e = 0 (1 sign, 2 exponent, 1 mantissa bit). */
+double orc_e2m1_value(int code);
 
 /* OCP FP8 E4M3 code -> value: (-1)^s 2^(e-7) (1 + m/8) for exponent field
  * e > 0, (-1)^s 2^-6 (m/8) for e = 0 (1 sign, 4 exponent, 3 mantissa bits;

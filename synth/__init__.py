@@ -19,7 +19,7 @@ from .workloads import (MODELS, WORKLOADS, ModelShape, Workload, StepInputs, mak
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libsynth.so")
 
-EMB, WQKV, WO, WR, WG, WU, WD, WLM, KPOOL, VPOOL, SG, SU, SD = range(1, 14)
+EMB, WQKV, WO, WR, WG, WU, WD, WLM, KPOOL, VPOOL, SG, SU, SD, BG, BU, BD = range(1, 17)
 
 _lib = None
 
@@ -52,6 +52,23 @@ def lib():
         L.synth_fill_scales_host.argtypes = [ctypes.c_void_p, u64, u64, u32, u32, u32, ctypes.c_double]
         L.synth_e4m3.restype = ctypes.c_uint8
         L.synth_e4m3.argtypes = [ctypes.c_float]
+        for name in ("synth_fill_fp4_device", "synth_fill_bscales_device"):
+            f = getattr(L, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [ctypes.c_void_p, u64, u64, u64, u32, u32, u32, ctypes.c_int, ctypes.c_void_p]
+        L.synth_fill_scales_base_device.restype = ctypes.c_int
+        L.synth_fill_scales_base_device.argtypes = [ctypes.c_void_p, u64, u64, u64, u32, u32, u32, ctypes.c_int,
+                                                    ctypes.c_float, ctypes.c_void_p]
+        for name in ("synth_fill_fp4_host", "synth_fill_bscales_host"):
+            f = getattr(L, name)
+            f.restype = None
+            f.argtypes = [ctypes.c_void_p, u64, u64, u32, u32, u32]
+        L.synth_fill_scales_base_host.restype = None
+        L.synth_fill_scales_base_host.argtypes = [ctypes.c_void_p, u64, u64, u32, u32, u32, ctypes.c_float]
+        L.synth_fp4_base_of.restype = ctypes.c_float
+        L.synth_fp4_base_of.argtypes = [ctypes.c_double]
+        L.synth_e2m1.restype = ctypes.c_uint8
+        L.synth_e2m1.argtypes = [ctypes.c_float]
         _lib = L
     return _lib
 
@@ -109,6 +126,63 @@ def fill_scales_device(ptr: int, n_streams: int, rows: int, seed: int, kind: int
                                         int(vary_layer), sigma, stream)
     if rc != 0:
         raise RuntimeError(f"synth_fill_scales_device failed with CUDA error {rc}")
+
+
+def fill_fp4_host(n_bytes: int, seed: int, kind: int, layer: int = 0, expert: int = 0) -> np.ndarray:
+    """uint8 packed E2M1 codes of one FP4 expert matrix (element 2j in the low
+    nibble of byte j), n_bytes = elements / 2."""
+    out = np.empty(n_bytes, dtype=np.uint8)
+    lib().synth_fill_fp4_host(out.ctypes.data, n_bytes, seed, kind, layer, expert)
+    return out
+
+
+def fill_bscales_host(n: int, seed: int, kind: int, layer: int = 0, expert: int = 0) -> np.ndarray:
+    """uint8 E4M3 block scales of one FP4 expert matrix (kind BG, BU or BD)."""
+    out = np.empty(n, dtype=np.uint8)
+    lib().synth_fill_bscales_host(out.ctypes.data, n, seed, kind, layer, expert)
+    return out
+
+
+def fp4_base(sigma: float = 0.02) -> float:
+    return float(lib().synth_fp4_base_of(sigma))
+
+
+def fill_scales4_host(rows: int, seed: int, kind: int, layer: int = 0, expert: int = 0,
+                      sigma: float = 0.02) -> np.ndarray:
+    """float32 row scales of one FP4 expert matrix (kind SG, SU or SD)."""
+    out = np.empty(rows, dtype=np.float32)
+    lib().synth_fill_scales_base_host(out.ctypes.data, rows, seed, kind, layer, expert, fp4_base(sigma))
+    return out
+
+
+def e2m1(f: float) -> int:
+    """The generator's E2M1 encoding of one binary32 (|f| <= 6)."""
+    return int(lib().synth_e2m1(f))
+
+
+def fill_fp4_device(ptr: int, n_streams: int, per_stream: int, seed: int, kind: int, layer0: int = 0,
+                    expert0: int = 0, vary_layer: bool = False, stream: int = 0) -> None:
+    rc = lib().synth_fill_fp4_device(ptr, n_streams, per_stream, seed, kind, layer0, expert0,
+                                     int(vary_layer), stream)
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_fp4_device failed with CUDA error {rc}")
+
+
+def fill_bscales_device(ptr: int, n_streams: int, per_stream: int, seed: int, kind: int, layer0: int = 0,
+                        expert0: int = 0, vary_layer: bool = False, stream: int = 0) -> None:
+    rc = lib().synth_fill_bscales_device(ptr, n_streams, per_stream, seed, kind, layer0, expert0,
+                                         int(vary_layer), stream)
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_bscales_device failed with CUDA error {rc}")
+
+
+def fill_scales4_device(ptr: int, n_streams: int, rows: int, seed: int, kind: int, layer0: int = 0,
+                        expert0: int = 0, vary_layer: bool = False, sigma: float = 0.02,
+                        stream: int = 0) -> None:
+    rc = lib().synth_fill_scales_base_device(ptr, n_streams, rows, seed, kind, layer0, expert0,
+                                             int(vary_layer), fp4_base(sigma), stream)
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_scales_base_device failed with CUDA error {rc}")
 
 
 def raw(key: int, idx: int) -> int:

@@ -8,7 +8,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (EMB, WQKV, WO, WR, WG, WU, WD, WLM, KPOOL, VPOOL, SG, SU, SD, fill_device, fill_fp8_device,
+from . import (EMB, WQKV, WO, WR, WG, WU, WD, WLM, KPOOL, VPOOL, SG, SU, SD, BG, BU, BD, fill_device,
+               fill_fp4_device, fill_bscales_device, fill_scales4_device, fill_fp8_device,
                fill_scales_device)
 from .workloads import ModelShape
 
@@ -22,7 +23,8 @@ def _fill(t: torch.Tensor, n_streams: int, per: int, seed: int, kind: int, layer
 
 def device_weights(shape: ModelShape, seed: int, device="cuda", router_bias=None) -> dict:
     """All weights of the model as torch tensors (BF16 stored as uint16; with
-    expert_fp8 the expert matrices as uint8 E4M3 codes plus fp32 row scales)."""
+    expert_fp8 the expert matrices as uint8 E4M3 codes plus fp32 row scales; with
+    expert_fp4 packed E2M1 codes, E4M3 block scales and fp32 row scales)."""
     st = torch.cuda.current_stream(device).cuda_stream
     L, H, E, I, V = shape.n_layers, shape.hidden, shape.n_experts, shape.inter, shape.vocab
     QKV, NQD = shape.qkv_rows(), shape.n_q * shape.head_dim
@@ -59,6 +61,29 @@ def device_weights(shape: ModelShape, seed: int, device="cuda", router_bias=None
             for t, kind in ((w["w_gate_scale"], SG), (w["w_up_scale"], SU), (w["w_down_scale"], SD)):
                 fill_scales_device(t[l].data_ptr(), E, t[l].numel() // E, seed, kind, layer0=l, sigma=sg,
                                    stream=st)
+        return _rest(w, shape, seed, sg, st)
+    if getattr(shape, "expert_fp4", False):
+        # two E2M1 codes per byte, an E4M3 scale per 16 inputs, a scale per output row
+        # (synth.h, "FP4 expert weights")
+        u8 = dict(dtype=torch.uint8, device=device)
+        f32 = dict(dtype=torch.float32, device=device)
+        w["w_gate"] = torch.empty(L, E, I, H // 2, **u8)
+        w["w_up"] = torch.empty(L, E, I, H // 2, **u8)
+        w["w_down"] = torch.empty(L, E, H, I // 2, **u8)
+        w["w_gate_bscale"] = torch.empty(L, E, I, H // 16, **u8)
+        w["w_up_bscale"] = torch.empty(L, E, I, H // 16, **u8)
+        w["w_down_bscale"] = torch.empty(L, E, H, I // 16, **u8)
+        w["w_gate_scale"] = torch.empty(L, E, I, **f32)
+        w["w_up_scale"] = torch.empty(L, E, I, **f32)
+        w["w_down_scale"] = torch.empty(L, E, H, **f32)
+        for l in range(L):
+            for t, kind in ((w["w_gate"], WG), (w["w_up"], WU), (w["w_down"], WD)):
+                fill_fp4_device(t[l].data_ptr(), E, t[l].numel() // E, seed, kind, layer0=l, stream=st)
+            for t, kind in ((w["w_gate_bscale"], BG), (w["w_up_bscale"], BU), (w["w_down_bscale"], BD)):
+                fill_bscales_device(t[l].data_ptr(), E, t[l].numel() // E, seed, kind, layer0=l, stream=st)
+            for t, kind in ((w["w_gate_scale"], SG), (w["w_up_scale"], SU), (w["w_down_scale"], SD)):
+                fill_scales4_device(t[l].data_ptr(), E, t[l].numel() // E, seed, kind, layer0=l, sigma=sg,
+                                    stream=st)
         return _rest(w, shape, seed, sg, st)
     w["w_gate"] = torch.empty(L, E, I, H, **u16)
     w["w_up"] = torch.empty(L, E, I, H, **u16)

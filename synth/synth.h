@@ -38,6 +38,17 @@
  *   base = (float)(sigma / (37837.2265... * 3.5 * 2^-10)),
  * with key' the key of the scale stream, so row r's weights are
  * e4m3(code) * scale_r, of standard deviation sigma to 1.5 sigma.
+ *
+ * FP4 expert weights (NVFP4-style): element i is the E2M1 code (1 sign
+ * bit, 2 exponent bits biased by 1, 1 mantissa bit: magnitudes 0, 0.5, 1,
+ * 1.5, 2, 3, 4, 6) of
+ *   ih4(draw(key, i)) * 3 * 2^-16            (exact in binary32, |.| < 6)
+ * rounded to nearest, ties to even; two elements per byte, element 2j in the
+ * low nibble of byte j.  Each run of 16 elements along a row has an E4M3
+ * block scale, code 0x30 | (draw(key_b, blk) >> 61) (0.5 * (1 + m/8)), and
+ * each output row the row scale above with
+ *   base = (float)(sigma / (37837.2265... * 3 * 2^-16 * 0.71875))
+ * (0.71875 is the mean block scale): weight = e2m1 * block scale * row scale.
  */
 #ifndef SYNTH_H
 #define SYNTH_H
@@ -66,9 +77,12 @@ enum {
   SYNTH_WLM = 8,   /* LM head [V][H]                            */
   SYNTH_KPOOL = 9, /* K pool of one layer [pages][nkv][P][d]    */
   SYNTH_VPOOL = 10, /* V pool of one layer [pages][nkv][P][d]   */
-  SYNTH_SG = 11,   /* FP8 expert gate row scales [I]            */
-  SYNTH_SU = 12,   /* FP8 expert up row scales [I]              */
-  SYNTH_SD = 13    /* FP8 expert down row scales [H]            */
+  SYNTH_SG = 11,   /* FP8 / FP4 expert gate row scales [I]      */
+  SYNTH_SU = 12,   /* FP8 / FP4 expert up row scales [I]        */
+  SYNTH_SD = 13,   /* FP8 / FP4 expert down row scales [H]      */
+  SYNTH_BG = 14,   /* FP4 expert gate block scales [I][H/16]    */
+  SYNTH_BU = 15,   /* FP4 expert up block scales [I][H/16]      */
+  SYNTH_BD = 16    /* FP4 expert down block scales [H][I/16]    */
 };
 
 SYNTH_FN uint64_t synth_mix64(uint64_t z) {
@@ -181,6 +195,42 @@ SYNTH_FN float synth_fp8_base(double sigma) {
 SYNTH_FN float synth_row_scale(uint64_t key, uint64_t row, float base) {
   const uint32_t k = (uint32_t)(synth_draw(key, row) >> 55);
   return base * (1.0f + (float)k * 0.0009765625f); /* 1 + k 2^-10 is exact */
+}
+
+/* ---- FP4 expert weights ---- */
+
+#define SYNTH_FP4_STEP 4.57763671875e-05f /* 3 * 2^-16: ih4 * step is exact, below 6 */
+
+/* E2M1 code of a finite binary32 of magnitude <= 6, round to nearest even.
+ * The midpoints between neighbouring magnitudes are exact in binary32, so
+ * the comparisons decide exactly. */
+SYNTH_FN uint8_t synth_f32_to_e2m1_rne(float f) {
+  const float mid[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
+  const uint8_t sign = f < 0.0f ? 8u : 0u;
+  const float a = f < 0.0f ? -f : f;
+  uint8_t code = 0;
+  for (int i = 0; i < 7; ++i) {
+    if (a > mid[i]) code = (uint8_t)(i + 1);
+    else if (a == mid[i]) code = (uint8_t)((i & 1) ? i + 1 : i); /* the even code */
+  }
+  return (uint8_t)(sign | code);
+}
+
+/* Byte j of an FP4 matrix of stream key: elements 2j (low nibble), 2j+1. */
+SYNTH_FN uint8_t synth_fp4_byte(uint64_t key, uint64_t j) {
+  const uint8_t lo = synth_f32_to_e2m1_rne((float)synth_ih4(synth_draw(key, 2 * j)) * SYNTH_FP4_STEP);
+  const uint8_t hi = synth_f32_to_e2m1_rne((float)synth_ih4(synth_draw(key, 2 * j + 1)) * SYNTH_FP4_STEP);
+  return (uint8_t)(lo | (hi << 4));
+}
+
+/* The E4M3 block scale of 16-element block blk (stream key of the block kind). */
+SYNTH_FN uint8_t synth_fp4_bscale(uint64_t key, uint64_t blk) {
+  return (uint8_t)(0x30u | (uint32_t)(synth_draw(key, blk) >> 61));
+}
+
+/* The base of the FP4 row scales. */
+SYNTH_FN float synth_fp4_base(double sigma) {
+  return (float)(sigma / (SYNTH_IH4_STD * 4.57763671875e-05 * 0.71875));
 }
 
 #endif /* SYNTH_H */

@@ -91,6 +91,41 @@ __global__ void fill_row_scales(float* __restrict__ dst, uint64_t n_streams, uin
   }
 }
 
+// FP4 expert weights: 16 bytes (32 E2M1 codes) per thread, one 16-byte store
+// (per_stream bytes % 16 == 0, dst 16-byte aligned).
+__global__ void fill_fp4_vec16(uint8_t* __restrict__ dst, uint64_t n_streams, uint64_t per_stream,
+                               uint64_t seed, uint32_t kind, uint32_t layer0, uint32_t expert0,
+                               int vary_layer) {
+  const uint64_t groups_per_stream = per_stream / 16;
+  const uint64_t total = n_streams * groups_per_stream;
+  for (uint64_t g = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+       g += (uint64_t)gridDim.x * blockDim.x) {
+    const uint64_t j = g / groups_per_stream;
+    const uint64_t i0 = (g - j * groups_per_stream) * 16;
+    const uint64_t key = synth_key(seed, stream_of(kind, layer0, expert0, vary_layer, j));
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      w[q] = 0u;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) w[q] |= (uint32_t)synth_fp4_byte(key, i0 + 4 * q + b) << (8 * b);
+    }
+    *reinterpret_cast<uint4*>(dst + j * per_stream + i0) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// Block scales (E4M3 bytes) of FP4 expert matrices: block b of sub-stream j.
+__global__ void fill_block_scales(uint8_t* __restrict__ dst, uint64_t n_streams, uint64_t per_stream, uint64_t seed,
+                                  uint32_t kind, uint32_t layer0, uint32_t expert0, int vary_layer) {
+  const uint64_t total = n_streams * per_stream;
+  for (uint64_t g = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+       g += (uint64_t)gridDim.x * blockDim.x) {
+    const uint64_t j = g / per_stream, b = g - j * per_stream;
+    const uint64_t key = synth_key(seed, stream_of(kind, layer0, expert0, vary_layer, j));
+    dst[g] = synth_fp4_bscale(key, b);
+  }
+}
+
 int launch_blocks() {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -122,6 +157,60 @@ extern "C" int synth_fill_scales_device(float* dst, uint64_t n_streams, uint64_t
       dst, n_streams, rows, seed, kind, layer0, expert0, vary_layer, synth_fp8_base(sigma));
   return (int)cudaGetLastError();
 }
+
+// FP4 expert weights on the device: byte i of sub-stream j goes to
+// dst[j*per_stream+i]; per_stream % 16 == 0 and dst 16-byte aligned.
+extern "C" int synth_fill_fp4_device(void* dst, uint64_t n_streams, uint64_t per_stream, uint64_t seed,
+                                     uint32_t kind, uint32_t layer0, uint32_t expert0, int vary_layer,
+                                     void* stream) {
+  if (dst == nullptr || n_streams == 0 || per_stream == 0 || per_stream % 16 != 0 ||
+      (reinterpret_cast<uintptr_t>(dst) & 15u) != 0)
+    return (int)cudaErrorInvalidValue;
+  fill_fp4_vec16<<<launch_blocks(), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint8_t*>(dst), n_streams, per_stream, seed, kind, layer0, expert0, vary_layer);
+  return (int)cudaGetLastError();
+}
+
+// FP4 block scales on the device: `per_stream` blocks per sub-stream.
+extern "C" int synth_fill_bscales_device(void* dst, uint64_t n_streams, uint64_t per_stream, uint64_t seed,
+                                         uint32_t kind, uint32_t layer0, uint32_t expert0, int vary_layer,
+                                         void* stream) {
+  if (dst == nullptr || n_streams == 0 || per_stream == 0) return (int)cudaErrorInvalidValue;
+  fill_block_scales<<<launch_blocks(), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint8_t*>(dst), n_streams, per_stream, seed, kind, layer0, expert0, vary_layer);
+  return (int)cudaGetLastError();
+}
+
+// Row scales with an explicit base (FP4 matrices use synth_fp4_base).
+extern "C" int synth_fill_scales_base_device(float* dst, uint64_t n_streams, uint64_t rows, uint64_t seed,
+                                             uint32_t kind, uint32_t layer0, uint32_t expert0, int vary_layer,
+                                             float base, void* stream) {
+  if (dst == nullptr || n_streams == 0 || rows == 0) return (int)cudaErrorInvalidValue;
+  fill_row_scales<<<launch_blocks(), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      dst, n_streams, rows, seed, kind, layer0, expert0, vary_layer, base);
+  return (int)cudaGetLastError();
+}
+
+extern "C" void synth_fill_fp4_host(uint8_t* dst, uint64_t n_bytes, uint64_t seed, uint32_t kind, uint32_t layer,
+                                    uint32_t expert) {
+  const uint64_t key = synth_key(seed, synth_stream(kind, layer, expert));
+  for (uint64_t j = 0; j < n_bytes; ++j) dst[j] = synth_fp4_byte(key, j);
+}
+
+extern "C" void synth_fill_bscales_host(uint8_t* dst, uint64_t n, uint64_t seed, uint32_t kind, uint32_t layer,
+                                        uint32_t expert) {
+  const uint64_t key = synth_key(seed, synth_stream(kind, layer, expert));
+  for (uint64_t b = 0; b < n; ++b) dst[b] = synth_fp4_bscale(key, b);
+}
+
+extern "C" void synth_fill_scales_base_host(float* dst, uint64_t rows, uint64_t seed, uint32_t kind, uint32_t layer,
+                                            uint32_t expert, float base) {
+  const uint64_t key = synth_key(seed, synth_stream(kind, layer, expert));
+  for (uint64_t r = 0; r < rows; ++r) dst[r] = synth_row_scale(key, r, base);
+}
+
+extern "C" float synth_fp4_base_of(double sigma) { return synth_fp4_base(sigma); }
+extern "C" uint8_t synth_e2m1(float f) { return synth_f32_to_e2m1_rne(f); }
 
 extern "C" void synth_fill_fp8_host(uint8_t* dst, uint64_t n, uint64_t seed, uint32_t kind, uint32_t layer,
                                     uint32_t expert) {

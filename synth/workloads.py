@@ -38,6 +38,7 @@ class ModelShape:
     weight_sigma: float = 0.02
     kv_sigma: float = 1.0
     expert_fp8: bool = False  # expert matrices as E4M3 codes with one scale per output row
+    expert_fp4: bool = False  # E2M1 codes, an E4M3 scale per 16 inputs, one fp32 scale per output row
 
     def is_full_layer(self, layer: int) -> bool:
         return self.window == 0 or (layer + 1) % self.full_period == 0
@@ -56,6 +57,9 @@ class ModelShape:
     def expert_bytes(self) -> int:
         if self.expert_fp8:  # E4M3 codes plus one fp32 scale per output row
             return 3 * self.hidden * self.inter + 4 * (2 * self.inter + self.hidden)
+        if self.expert_fp4:  # half-byte codes, a byte per 16 codes, fp32 per output row
+            return 3 * self.hidden * self.inter // 2 + 3 * self.hidden * self.inter // 16 + \
+                4 * (2 * self.inter + self.hidden)
         return 2 * 3 * self.hidden * self.inter
 
     def kv_bytes_per_token_layer(self) -> int:
@@ -85,6 +89,13 @@ MODELS = {
     "full_fp8": ModelShape("full_fp8", n_layers=48, hidden=2048, n_q=32, n_kv=4, head_dim=128,
                            n_experts=128, top_k=8, inter=768, vocab=65536, page_size=64,
                            window=4096, full_period=4, expert_fp8=True),
+    # FP4 expert weights (E2M1 codes, E4M3 block scales, fp32 row scales)
+    "small_fp4": ModelShape("small_fp4", n_layers=8, hidden=1024, n_q=16, n_kv=2, head_dim=64,
+                            n_experts=32, top_k=4, inter=512, vocab=32768, page_size=64, window=0,
+                            full_period=1, expert_fp4=True),
+    "full_fp4": ModelShape("full_fp4", n_layers=48, hidden=2048, n_q=32, n_kv=4, head_dim=128,
+                           n_experts=128, top_k=8, inter=768, vocab=65536, page_size=64,
+                           window=4096, full_period=4, expert_fp4=True),
     "dense": ModelShape("dense", n_layers=8, hidden=1024, n_q=16, n_kv=2, head_dim=64, n_experts=1,
                         top_k=1, inter=2048, vocab=32768, page_size=64, window=512, full_period=2),
 }
@@ -129,6 +140,12 @@ WORKLOADS = {
                              desc="small shape with FP8 experts: 8 layers, B=2, seq_lens U[1,1024]"),
     "full_fp8_bs1_8k": Workload("full_fp8_bs1_8k", "full_fp8", 1, ("fixed", 8192), 3,
                                 desc="full shape with FP8 experts, B=1, context 8192"),
+    "small_fp4": Workload("small_fp4", "small_fp4", 1, ("fixed", 1024), 14,
+                          desc="small shape with FP4 experts: 8 layers, B=1, context 1024"),
+    "small_fp4_b2": Workload("small_fp4_b2", "small_fp4", 2, ("uniform", 1, 1024), 15,
+                             desc="small shape with FP4 experts: 8 layers, B=2, seq_lens U[1,1024]"),
+    "full_fp4_bs1_8k": Workload("full_fp4_bs1_8k", "full_fp4", 1, ("fixed", 8192), 3,
+                                desc="full shape with FP4 experts, B=1, context 8192"),
     "prof_l2_8k": Workload("prof_l2_8k", "full_l2", 1, ("fixed", 8192), 7,
                            desc="full-shape layers, 2 of them, B=1, context 8192 (profiling case)"),
 }
