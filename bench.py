@@ -195,13 +195,20 @@ def run_reference(args):
 
 
 def dtype_text(sh):
-    return "f32 (fp8 E4M3 experts, bf16 other weights and KV)" if sh.expert_fp8 else "f32 (bf16 weights and KV)"
+    if sh.expert_fp8:
+        return "f32 (fp8 E4M3 experts, bf16 other weights and KV)"
+    if sh.expert_fp4:
+        return "f32 (fp4 E2M1 experts with E4M3 block scales, bf16 other weights and KV)"
+    return "f32 (bf16 weights and KV)"
 
 
 def weights_text(sh):
     if sh.expert_fp8:
         return ("experts: E4M3 codes with one fp32 scale per output row (std 0.02 to 0.03 after "
                 "scaling); the rest bf16 random N(0,0.02)")
+    if sh.expert_fp4:
+        return ("experts: E2M1 codes, an E4M3 scale per 16 inputs and an fp32 scale per output row "
+                "(std about 0.02 after scaling); the rest bf16 random N(0,0.02)")
     return "bf16 random N(0,0.02)"
 
 

@@ -56,6 +56,12 @@ typedef struct {
                           same [L][E][rows][cols] layout) and each output row has one
                           fp32 scale (w_*_scale): weight = e4m3 value * row scale.
                           Schedules for it need max_batch <= 2 */
+  int32_t expert_fp4;  /* 1 (not with expert_fp8): w_gate, w_up, w_down hold FP4 E2M1 codes,
+                          two per byte (element 2j in the low nibble of byte j), the same
+                          [L][E][rows][cols] layout at half a byte per weight; each run of 16
+                          inputs of a row has an E4M3 block scale (w_*_bscale) and each output
+                          row an fp32 scale (w_*_scale): weight = e2m1 * block scale * row
+                          scale.  hidden and inter multiples of 128; max_batch <= 2 */
 } mk_config;
 
 /* Device pointers to the weights, row-major with the output dimension first
@@ -79,6 +85,9 @@ typedef struct {
   const float* w_gate_scale; /* fp32 [L][n_experts][inter] (expert_fp8 only, else NULL) */
   const float* w_up_scale;   /* fp32 [L][n_experts][inter] */
   const float* w_down_scale; /* fp32 [L][n_experts][hidden] */
+  const void* w_gate_bscale; /* E4M3 bytes [L][n_experts][inter][hidden/16] (expert_fp4 only) */
+  const void* w_up_bscale;   /* E4M3 bytes [L][n_experts][inter][hidden/16] */
+  const void* w_down_bscale; /* E4M3 bytes [L][n_experts][hidden][inter/16] */
 } mk_weights;
 
 typedef struct mk_model mk_model;

@@ -34,14 +34,16 @@ class MkConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("n_layers", "hidden", "n_q", "n_kv", "head_dim",
                                               "n_experts", "top_k", "inter", "vocab", "page_size",
                                               "window", "full_period")] + \
-               [("rope_base", ctypes.c_float), ("eps", ctypes.c_float), ("expert_fp8", ctypes.c_int32)]
+               [("rope_base", ctypes.c_float), ("eps", ctypes.c_float), ("expert_fp8", ctypes.c_int32),
+                                                                        ("expert_fp4", ctypes.c_int32)]
 
 
 class MkWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("embedding", "w_qkv", "w_o", "w_router",
                                                "router_bias", "w_gate", "w_up", "w_down",
                                                "norm_gamma", "final_gamma", "w_lm", "w_gate_scale",
-                                               "w_up_scale", "w_down_scale")]
+                                               "w_up_scale", "w_down_scale", "w_gate_bscale",
+                                               "w_up_bscale", "w_down_bscale")]
 
 
 class MkSchedOpts(ctypes.Structure):
@@ -278,7 +280,7 @@ def config_from(shape) -> MkConfig:
     return MkConfig(shape.n_layers, shape.hidden, shape.n_q, shape.n_kv, shape.head_dim,
                     shape.n_experts, shape.top_k, shape.inter, shape.vocab, shape.page_size,
                     shape.window, shape.full_period, shape.rope_base, shape.eps,
-                    int(getattr(shape, "expert_fp8", False)))
+                    int(getattr(shape, "expert_fp8", False)), int(getattr(shape, "expert_fp4", False)))
 
 
 def weights_from(tensors: dict) -> MkWeights:

@@ -186,9 +186,14 @@ int mk_load_model(const mk_config* cfg, const mk_weights* w, mk_model** out) {
   if (c.expert_fp8 != 0 && c.expert_fp8 != 1) return fail(MK_ERR_ARG, "expert_fp8 must be 0 or 1");
   if (c.expert_fp8 && (!w->w_gate_scale || !w->w_up_scale || !w->w_down_scale))
     return fail(MK_ERR_ARG, "FP8 experts need the three row-scale arrays");
+  if (c.expert_fp4 != 0 && c.expert_fp4 != 1) return fail(MK_ERR_ARG, "expert_fp4 must be 0 or 1");
+  if (c.expert_fp4 && c.expert_fp8) return fail(MK_ERR_ARG, "expert_fp8 and expert_fp4 exclude each other");
+  if (c.expert_fp4 && (!w->w_gate_scale || !w->w_up_scale || !w->w_down_scale || !w->w_gate_bscale ||
+                       !w->w_up_bscale || !w->w_down_bscale))
+    return fail(MK_ERR_ARG, "FP4 experts need the three row-scale and three block-scale arrays");
   const void* ptrs[] = {w->embedding, w->w_qkv, w->w_o, w->w_router, w->router_bias, w->w_gate, w->w_up,
                         w->w_down, w->norm_gamma, w->final_gamma, w->w_lm, w->w_gate_scale, w->w_up_scale,
-                        w->w_down_scale};
+                        w->w_down_scale, w->w_gate_bscale, w->w_up_bscale, w->w_down_bscale};
   for (const void* q : ptrs)
     if (reinterpret_cast<uintptr_t>(q) & 15u) return fail(MK_ERR_ARG, "weight pointers must be 16-byte aligned");
   if (c.expert_fp8) {
@@ -198,12 +203,20 @@ int mk_load_model(const mk_config* cfg, const mk_weights* w, mk_model** out) {
     if (p8.up_half % 8 || p8.dn_rows % 16 || 2 * p8.up_half > kMaxStageRows || p8.dn_rows > kMaxStageRows)
       return fail(MK_ERR_UNSUPPORTED, "no FP8 stage plan for this model shape");
   }
+  if (c.expert_fp4) {
+    // 128-input chunks per MMA step; a 16-row stage (codes and block scales) in one slot
+    const ShapeDims& d = kShapes[id].dims;
+    const MoePlan p4 = moe_plan4(d);
+    if (d.H % 128 || d.I % 128 || fp4_stage_bytes(d.H) > kStageBytes || fp4_stage_bytes(d.I) > kStageBytes ||
+        p4.up_tile * p4.up_tiles != d.I || p4.dn_tile * p4.dn_tiles != d.H)
+      return fail(MK_ERR_UNSUPPORTED, "no FP4 stage plan for this model shape");
+  }
   mk_model* m = new mk_model();
   m->cfg = c;
   m->w = *w;
   m->shape_id = id;
   m->dims = kShapes[id].dims;
-  m->plan = c.expert_fp8 ? moe_plan8(m->dims) : moe_plan(m->dims);
+  m->plan = c.expert_fp8 ? moe_plan8(m->dims) : c.expert_fp4 ? moe_plan4(m->dims) : moe_plan(m->dims);
   *out = m;
   return MK_OK;
 }
@@ -272,6 +285,10 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   p.sg = w.w_gate_scale;
   p.su = w.w_up_scale;
   p.sd = w.w_down_scale;
+  p.expert_fp4 = m->cfg.expert_fp4;
+  p.bg = static_cast<const uint8_t*>(w.w_gate_bscale);
+  p.bu = static_cast<const uint8_t*>(w.w_up_bscale);
+  p.bd = static_cast<const uint8_t*>(w.w_down_bscale);
   p.gamma = w.norm_gamma;
   p.gamma_f = w.final_gamma;
   p.wlm = static_cast<const uint16_t*>(w.w_lm);

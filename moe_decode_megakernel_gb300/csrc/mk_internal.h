@@ -136,6 +136,11 @@ constexpr int stage_rows8(int k) {
   return r >= 8 ? p : r;
 }
 
+// FP4 stages are one 16-row group of the tensor-core GEMV (up/gate: 8 gate
+// and 8 up rows), the rows' E2M1 codes followed by their block scales.
+constexpr int kFp4StageRows = 16;
+constexpr int fp4_stage_bytes(int k) { return kFp4StageRows * (k / 2 + k / 16); }
+
 constexpr MoePlan moe_plan(ShapeDims s) {
   MoePlan p{};
   p.up_half = stage_rows(s.H) / 2;
@@ -161,6 +166,19 @@ constexpr MoePlan moe_plan8(ShapeDims s) {
   p.dn_tiles = s.H / p.dn_tile;
   return p;
 }
+// the plan for FP4 expert rows: 16-row stages
+constexpr MoePlan moe_plan4(ShapeDims s) {
+  MoePlan p{};
+  p.up_half = kFp4StageRows / 2;
+  p.up_stages = moe_stages(s.I, p.up_half, 16);
+  p.up_tile = p.up_half * p.up_stages;
+  p.up_tiles = s.I / p.up_tile;
+  p.dn_rows = kFp4StageRows;
+  p.dn_stages = moe_stages(s.H, p.dn_rows, 32);
+  p.dn_tile = p.dn_rows * p.dn_stages;
+  p.dn_tiles = s.H / p.dn_tile;
+  return p;
+}
 
 // ------------------------------------------------------ kernel parameters
 struct Params {
@@ -180,6 +198,10 @@ struct Params {
   const float* sg;      // [L][E][I] row scales of w_gate (FP8 only)
   const float* su;      // [L][E][I]
   const float* sd;      // [L][E][H]
+  int expert_fp4;       // expert rows are E2M1 nibbles, an E4M3 scale per 16, fp32 per row
+  const uint8_t* bg;    // [L][E][I][H/16] block scales of w_gate (FP4 only)
+  const uint8_t* bu;    // [L][E][I][H/16]
+  const uint8_t* bd;    // [L][E][H][I/16]
   const float* gamma;
   const float* gamma_f;
   const uint16_t* wlm;

@@ -124,6 +124,31 @@ __device__ __forceinline__ void e4m3x4_f16(uint32_t c, uint32_t& lo, uint32_t& h
       : "=r"(lo), "=r"(hi)
       : "r"(c));
 }
+// Four E2M1 codes (the low 16 bits of c; a byte holds two codes, the
+// earlier element in its low nibble) as two f16x2 words: lo from the low
+// byte, hi from the next.  Every E2M1 value is exact in f16.
+__device__ __forceinline__ void e2m1x4_f16(uint32_t c, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b8 a, b;\n .reg .b32 t;\n cvt.u8.u32 a, %2;\n shr.b32 t, %2, 8;\n cvt.u8.u32 b, t;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, a;\n cvt.rn.f16x2.e2m1x2 %1, b;\n}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(c));
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// the lower (sel 0x1010) or upper (0x3232) half of an f16x2 in both halves
+__device__ __forceinline__ uint32_t half_bcast(uint32_t a, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %1, %2;" : "=r"(r) : "r"(a), "r"(sel));
+  return r;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
 // f16x2 of (a, b), a in the lower half, round to nearest even
 __device__ __forceinline__ uint32_t f16x2_rn(float a, float b) {
   uint32_t r;
@@ -319,8 +344,8 @@ __host__ __device__ constexpr int xs_row() {
 // The MoE tile plan of the step's expert weights (BF16 or FP8 rows).
 template <class S>
 __device__ __forceinline__ MoePlan plan_of(const Params& p) {
-  constexpr MoePlan m16 = S::mp, m8 = S::mp8;
-  return p.expert_fp8 ? m8 : m16;
+  constexpr MoePlan m16 = S::mp, m8 = S::mp8, m4 = S::mp4;
+  return p.expert_fp4 ? m4 : p.expert_fp8 ? m8 : m16;
 }
 
 template <class S>
@@ -361,6 +386,7 @@ struct Shape {
   static constexpr ShapeDims dims{H, NQ, NKV, D, E, K, I, P};
   static constexpr MoePlan mp = moe_plan(dims);
   static constexpr MoePlan mp8 = moe_plan8(dims);  // FP8 expert rows
+  static constexpr MoePlan mp4 = moe_plan4(dims);  // FP4 expert rows
   static constexpr int SR_H = stage_rows(H), SR_O = stage_rows(G * D), SR_I = stage_rows(I);
   static_assert(H % 256 == 0 && (G * D) % 8 == 0 && I % 8 == 0, "row chunks");
   static_assert(D % 32 == 0 && 32 % G == 0 && (G * D) % 4 == 0, "attention lane maps");
@@ -899,7 +925,47 @@ struct Producer {
   // The weight stages of tile t of expert e: up/gate stages of up_half gate
   // rows and as many up rows, or down stages of dn_rows rows of W_down[e].
   // FP8 rows are 1 byte per weight: a row of K weights is K / 2 16-bit units.
+  // FP4 stages: 16 rows (up/gate: 8 gate, then 8 up) of K/2 bytes of E2M1
+  // codes, then the same rows' K/16 block scales; their row scales go to the
+  // slot's scale area.  All on the stage's one full barrier.
+  __device__ __forceinline__ bool tile_stages4(int l, int e, int t, bool up) {
+    constexpr int R = kFp4StageRows;
+    constexpr MoePlan mp = S::mp4;
+    const int64_t le = (int64_t)l * S::E + e;
+    const uint8_t* wg = reinterpret_cast<const uint8_t*>(p.wg);
+    const uint8_t* wu = reinterpret_cast<const uint8_t*>(p.wu);
+    const uint8_t* wd = reinterpret_cast<const uint8_t*>(p.wd);
+    const int nst = up ? mp.up_stages : mp.dn_stages;
+    for (int s = 0; s < nst; ++s) {
+      int slot;
+      if (!acquire_stage(slot)) return false;
+      uint64_t* fb = &c.hdr->full[slot];
+      uint8_t* dst = stage(slot);
+      if (up) {
+        constexpr uint32_t cb = (R / 2) * S::H / 2, bb = (R / 2) * S::H / 16, sb = (R / 2) * 4;
+        const int64_t r0 = le * S::I + t * mp.up_tile + s * (R / 2);  // row of [L][E][I]
+        mbar_expect_tx(fb, 2 * (cb + bb + sb));
+        bulk_g2s_hint(dst, wg + r0 * (S::H / 2), cb, fb, stream_policy);
+        bulk_g2s_hint(dst + cb, wu + r0 * (S::H / 2), cb, fb, stream_policy);
+        bulk_g2s_hint(dst + 2 * cb, p.bg + r0 * (S::H / 16), bb, fb, stream_policy);
+        bulk_g2s_hint(dst + 2 * cb + bb, p.bu + r0 * (S::H / 16), bb, fb, stream_policy);
+        bulk_g2s(c.hdr->scl[slot], p.sg + r0, sb, fb);
+        bulk_g2s(c.hdr->scl[slot] + R / 2, p.su + r0, sb, fb);
+      } else {
+        constexpr uint32_t cb = R * S::I / 2, bb = R * S::I / 16, sb = R * 4;
+        const int64_t r0 = le * S::H + t * mp.dn_tile + s * R;  // row of [L][E][H]
+        mbar_expect_tx(fb, cb + bb + sb);
+        bulk_g2s_hint(dst, wd + r0 * (S::I / 2), cb, fb, stream_policy);
+        bulk_g2s_hint(dst + cb, p.bd + r0 * (S::I / 16), bb, fb, stream_policy);
+        bulk_g2s(c.hdr->scl[slot], p.sd + r0, sb, fb);
+      }
+      ++c.st;
+    }
+    return true;
+  }
+
   __device__ __forceinline__ bool tile_stages(int l, int e, int t, bool up) {
+    if (p.expert_fp4) return tile_stages4(l, e, t, up);
     const MoePlan mp = plan_of<S>(p);
     const int64_t le = (int64_t)l * S::E + e;
     const int eb = p.expert_fp8 ? 1 : 2;  // bytes per weight
@@ -1298,17 +1364,18 @@ struct Consumer {
     }
   }
 
-  // Activation rows of an FP8 expert tile as the B operand of f16 MMAs
+  // Activation rows of an FP8 / FP4 expert tile as the B operand of f16 MMAs
   // (m16n8k16, the weights as A).  Column 2t of B is the f16 rounding of
   // activation row t, column 2t + 1 the f16 rounding of what that leaves
   // (x - hi): hi + lo carry about 22 bits of x, and the MMA accumulates in
   // fp32.  In one MMA, thread (n = lane / 4, q = lane % 4) holds the logical
   // k 2q, 2q+1, 2q+8, 2q+9; they stand for the physical elements
-  // 64 kc + 16 q + 4 j + 0..3 of MMA j (0..3) of 64-element chunk kc, which
-  // are the bytes one 16-byte load of a weight row gives thread q.  Layout:
-  // uint4 [kc][j / 2][n][q] holding the (b0b1, b2b3) words of MMAs 2(j/2) and
-  // 2(j/2) + 1.  An activation beyond the f16 range is reported as an error.
-  template <int K>
+  // CH kc + (CH/4) q + 4 j + 0..3 of MMA j of CH-element chunk kc (CH = 64
+  // for FP8, 128 for FP4): the elements one 16-byte load of a weight row
+  // gives thread q.  Layout: uint4 [kc][j / 2][n][q] holding the (b0b1,
+  // b2b3) words of MMAs 2(j/2) and 2(j/2) + 1.  An activation beyond the f16
+  // range is reported as an error.
+  template <int K, int CH>
   __device__ __forceinline__ void load_x_f16(int op, const int32_t* w, int tb) {
     static_assert(kTB <= 2 && K * 8 <= (int)sizeof(sm.xs), "the hi/lo columns of kTB rows of K fit the cache");
     constexpr int U = K / 8;  // 8-element units per row
@@ -1327,8 +1394,9 @@ struct Consumer {
         const float2 h = f16x2_f32(hi[k]);
         lo[k] = f16x2_rn(v[2 * k] - h.x, v[2 * k + 1] - h.y);
       }
-      const int e = 8 * m, kc = e >> 6, q = (e >> 4) & 3, jp = (e >> 3) & 1;
-      const int at = (kc * 2 + jp) * 16 + q;
+      constexpr int QS = CH / 4, JP = QS / 8;
+      const int e = 8 * m, kc = e / CH, q = (e % CH) / QS, jp = (e % QS) / 8;
+      const int at = (kc * JP + jp) * 16 + q;
       xb[at + 2 * t * 4] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       xb[at + (2 * t + 1) * 4] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
@@ -1365,7 +1433,7 @@ struct Consumer {
     x_tag(op, w, 0, tag);
     tag[0] += 16;  // the same rows in the f16 hi/lo layout
     if (!(tag[0] == sm.xtag[0] && tag[1] == sm.xtag[1] && tag[2] == sm.xtag[2] && tag[3] == sm.xtag[3])) {
-      if (!aborted(c)) load_x_f16<K>(op, w, tb);
+      if (!aborted(c)) load_x_f16<K, 64>(op, w, tb);
       consumers_sync();
       if (ct == 0) {
         sm.xtag[0] = tag[0]; sm.xtag[1] = tag[1]; sm.xtag[2] = tag[2]; sm.xtag[3] = tag[3];
@@ -1439,6 +1507,115 @@ struct Consumer {
         if (ok && q < tb && !aborted(c)) {
           const float slo = c.hdr->scl[slot][rlo], shi = c.hdr->scl[slot][rhi];
           pair_epilogue(op, w, s, up ? 8 * grp + g : rlo, rhi, q, vlo * slo, vhi * shi, dslot, dwt);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_n(&c.hdr->empty[slot], kConsumerWarps / kTeamWarps);
+    }
+    c.st += (uint32_t)nst;
+  }
+
+  // FP4 expert tiles (batch <= kTB) on the tensor cores: each 16-row stage
+  // is one group of m16n8k16 f16 MMAs.  A thread's 16-byte load of a row
+  // holds 32 codes (two 16-input blocks) and feeds eight MMAs; each code pair
+  // is converted exactly to f16 and multiplied (exactly: at most 6
+  // significant bits, within the f16 range) by its block's E4M3 scale before
+  // the MMA.  The two warps of a team take half of the stage's 128-input
+  // chunks each and add their sums through shared memory; the row scale
+  // multiplies the finished dot product.
+  template <int K, int TB>
+  __device__ __forceinline__ void gemv_item_fp4(const int32_t* w, int ntok) {
+    static_assert(K % 128 == 0, "FP4 rows in 128-input chunks");
+    static_assert(kTeamWarps == 2 && kTeams * 2 * kTB * 16 <= (int)(sizeof(sm.out) / sizeof(float)),
+                  "partial sums of the stages fit the stage-output buffer");
+    constexpr int R = kFp4StageRows, NKC = K / 128, CB = R * K / 2;  // codes, then block scales
+    const int op = w[F_OP];
+    const int nst = w[F_NSTAGE];
+    const int tb = ntok;
+    const int g = lane >> 2, q = lane & 3;
+    int dslot = 0;
+    float dwt = 0.f;
+    if (op == W_DOWN_TILE && q < tb) {
+      dslot = q == 0 ? w[F_A0 + 8] : w[F_A0 + 9];
+      dwt = __int_as_float(q == 0 ? w[F_A0 + 10] : w[F_A0 + 11]);
+    }
+    int32_t tag[4];
+    x_tag(op, w, 0, tag);
+    tag[0] += 32;  // the same rows in the FP4 hi/lo layout
+    if (!(tag[0] == sm.xtag[0] && tag[1] == sm.xtag[1] && tag[2] == sm.xtag[2] && tag[3] == sm.xtag[3])) {
+      if (!aborted(c)) load_x_f16<K, 128>(op, w, tb);
+      consumers_sync();
+      if (ct == 0) {
+        sm.xtag[0] = tag[0]; sm.xtag[1] = tag[1]; sm.xtag[2] = tag[2]; sm.xtag[3] = tag[3];
+      }
+    }
+    const int team = cw / kTeamWarps, tw = cw % kTeamWarps;
+    const bool up = op == W_UP_TILE;
+    const int rlo = up ? g : 2 * g, rhi = up ? R / 2 + g : 2 * g + 1;  // gate/up row g; rows 2g, 2g+1
+    const int c0 = tw * NKC / 2, c1 = (tw + 1) * NKC / 2;
+    const bool bon = g < 2 * (TB == 1 ? 1 : tb);
+    const uint32_t xb_a = smem_u32(sm.xs) + (uint32_t)lane * 16u;
+    float* red = &sm.out[0][0];  // [team][2][kTB][16]
+    int it = 0;
+    for (int s = team; s < nst; s += kTeams, ++it) {
+      const uint32_t gs = c.st + (uint32_t)s;
+      const int slot = gs % kStages;
+      bool ok = s < kStages || mbar_wait(p, c, &c.hdr->empty[slot], ((gs / kStages) - 1) & 1);
+      ok = __all_sync(FULL, ok && mbar_wait(p, c, &c.hdr->full[slot], (gs / kStages) & 1) && !aborted(c));
+      const uint32_t st = smem_u32(stage(slot));
+      float d[4][4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+      if (ok) {
+        const uint32_t alo = st + (uint32_t)(rlo * (K / 2) + q * 16), ahi = st + (uint32_t)(rhi * (K / 2) + q * 16);
+        const uint32_t blo = st + (uint32_t)(CB + rlo * (K / 16) + q * 2);
+        const uint32_t bhi = st + (uint32_t)(CB + rhi * (K / 16) + q * 2);
+        for (int kc = c0; kc < c1; ++kc) {
+          const uint4 ul = lds128(alo + (uint32_t)(kc * 64)), uh = lds128(ahi + (uint32_t)(kc * 64));
+          // the scales of blocks 2q (MMAs 0-3) and 2q + 1 (MMAs 4-7) of the chunk
+          uint32_t sl, sh, unused;
+          e4m3x4_f16(lds_u16(blo + (uint32_t)(kc * 8)), sl, unused);
+          e4m3x4_f16(lds_u16(bhi + (uint32_t)(kc * 8)), sh, unused);
+          const uint32_t sl0 = half_bcast(sl, 0x1010u), sl1 = half_bcast(sl, 0x3232u);
+          const uint32_t sh0 = half_bcast(sh, 0x1010u), sh1 = half_bcast(sh, 0x3232u);
+          uint4 b[4];
+#pragma unroll
+          for (int jp = 0; jp < 4; ++jp)
+            b[jp] = bon ? lds128(xb_a + (uint32_t)((kc * 4 + jp) * 256)) : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t wl[4] = {ul.x, ul.y, ul.z, ul.w}, wh[4] = {uh.x, uh.y, uh.z, uh.w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            // MMA j: codes 4j .. 4j+3 of the thread's 32 (bytes 2j, 2j+1)
+            const uint32_t cl = (j & 1) ? wl[j >> 1] >> 16 : wl[j >> 1];
+            const uint32_t chh = (j & 1) ? wh[j >> 1] >> 16 : wh[j >> 1];
+            uint32_t a0, a1, a2, a3;
+            e2m1x4_f16(cl, a0, a2);
+            e2m1x4_f16(chh, a1, a3);
+            const uint32_t fl = j < 4 ? sl0 : sl1, fh = j < 4 ? sh0 : sh1;
+            a0 = hmul2(a0, fl);
+            a2 = hmul2(a2, fl);
+            a1 = hmul2(a1, fh);
+            a3 = hmul2(a3, fh);
+            const uint32_t b0 = (j & 1) ? b[j >> 1].z : b[j >> 1].x, b1 = (j & 1) ? b[j >> 1].w : b[j >> 1].y;
+            mma_f16(d[j & 3], a0, a1, a2, a3, b0, b1);
+          }
+        }
+      }
+      // columns 2t + {0, 1} of rows g and g + 8: thread q = t holds both
+      float vlo = (d[0][0] + d[1][0]) + (d[2][0] + d[3][0]) + ((d[0][1] + d[1][1]) + (d[2][1] + d[3][1]));
+      float vhi = (d[0][2] + d[1][2]) + (d[2][2] + d[3][2]) + ((d[0][3] + d[1][3]) + (d[2][3] + d[3][3]));
+      float* rb = red + (team * 2 + (it & 1)) * kTB * 16;
+      if (tw == 1 && q < tb) {
+        rb[q * 16 + g] = vlo;
+        rb[q * 16 + 8 + g] = vhi;
+      }
+      bar_sync(kBarTeam0 + team, 2 * 32);
+      if (tw == 0 && q < tb) {
+        vlo += rb[q * 16 + g];
+        vhi += rb[q * 16 + 8 + g];
+        if (ok && !aborted(c)) {
+          const float slo = c.hdr->scl[slot][rlo], shi = c.hdr->scl[slot][rhi];
+          pair_epilogue(op, w, s, up ? g : rlo, rhi, q, vlo * slo, vhi * shi, dslot, dwt);
         }
       }
       __syncwarp();
@@ -2386,7 +2563,10 @@ struct Consumer {
         else gemv_item<S::G * S::D>(w, S::SR_O, w[F_A0 + 1], p.B);
         break;
       case W_UP_TILE:
-        if (p.expert_fp8) {  // schedules with FP8 experts have max_batch <= kTB
+        if (p.expert_fp4) {  // schedules with FP8 / FP4 experts have max_batch <= kTB
+          if (w[F_A0 + 3] <= 1) gemv_item_fp4<S::H, 1>(w, w[F_A0 + 3]);
+          else gemv_item_fp4<S::H, kTB>(w, w[F_A0 + 3]);
+        } else if (p.expert_fp8) {
           constexpr MoePlan m8 = S::mp8;
           if (w[F_A0 + 3] <= 1) gemv_item_fp8<S::H, 1>(w, 2 * m8.up_half, w[F_A0 + 3]);
           else gemv_item_fp8<S::H, kTB>(w, 2 * m8.up_half, w[F_A0 + 3]);
@@ -2396,7 +2576,10 @@ struct Consumer {
           gemv_item<S::H>(w, 2 * S::mp.up_half, 2 * S::mp.up_half * S::mp.up_stages, w[F_A0 + 3]);
         break;
       case W_DOWN_TILE:
-        if (p.expert_fp8) {
+        if (p.expert_fp4) {
+          if (w[F_A0 + 3] <= 1) gemv_item_fp4<S::I, 1>(w, w[F_A0 + 3]);
+          else gemv_item_fp4<S::I, kTB>(w, w[F_A0 + 3]);
+        } else if (p.expert_fp8) {
           constexpr MoePlan m8 = S::mp8;
           if (w[F_A0 + 3] <= 1) gemv_item_fp8<S::I, 1>(w, m8.dn_rows, w[F_A0 + 3]);
           else gemv_item_fp8<S::I, kTB>(w, m8.dn_rows, w[F_A0 + 3]);

@@ -939,8 +939,8 @@ int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const 
   *out = nullptr;
   if (max_batch < 1 || max_batch > kMaxBatch) return fail(MK_ERR_ARG, "max_batch must be in [1, 64]");
   if (max_ctx < 1) return fail(MK_ERR_ARG, "max_ctx must be >= 1");
-  if (m->cfg.expert_fp8 && max_batch > kTB)
-    return fail(MK_ERR_UNSUPPORTED, "FP8 experts are compiled for max_batch <= 2");
+  if ((m->cfg.expert_fp8 || m->cfg.expert_fp4) && max_batch > kTB)
+    return fail(MK_ERR_UNSUPPORTED, "FP8 and FP4 experts are compiled for max_batch <= 2");
   mk_sched* s = new mk_sched();
   s->cfg = m->cfg;
   s->dims = m->dims;

@@ -80,3 +80,35 @@ def test_oracle_fp4_expert_rows(kind, rows_of):
     bv = np.repeat(np.vectorize(oracle.e4m3_value)(bs), 16, axis=1)
     rs = synth.fill_scales4_host(rows, seed, skind, layer, expert, sh.weight_sigma).astype(np.float64)
     assert np.array_equal(got, q * bv * rs[:, None])
+
+
+# ---- the boundary: FP4 models and schedules (no GPU)
+
+import moe_decode_megakernel_gb300 as mk  # noqa: E402
+from test_abi_sched import fake_model, NUM_SMS  # noqa: E402
+
+
+@pytest.mark.parametrize("workload", ["small_fp4", "small_fp4_b2", "full_fp4_bs1_8k"])
+def test_fp4_schedules(workload):
+    w = synth.WORKLOADS[workload]
+    inp = synth.make_inputs(w)
+    m = fake_model(w.shape)
+    s = mk.Sched(m, w.batch, int(inp.seq_lens.max()), mk.default_sched_opts(num_sms=NUM_SMS))
+    s.validate()
+    s.simulate(inp.seq_lens, seed=4)
+
+
+def test_fp4_needs_small_batch_and_one_format():
+    from dataclasses import replace
+    m = fake_model(synth.MODELS["small_fp4"])
+    with pytest.raises(mk.MkError) as e:
+        mk.Sched(m, 3, 1024, mk.default_sched_opts(num_sms=NUM_SMS))
+    assert e.value.code == mk.MK_ERR_UNSUPPORTED
+    with pytest.raises(mk.MkError) as e:
+        fake_model(replace(synth.MODELS["small_fp4"], expert_fp8=True))
+    assert e.value.code == mk.MK_ERR_ARG
+    w = mk.MkWeights(*[0x10000 * (i + 1) for i in range(len(mk.MkWeights._fields_))])
+    w.w_down_bscale = None
+    with pytest.raises(mk.MkError) as e:
+        mk.Model(mk.config_from(synth.MODELS["small_fp4"]), w)
+    assert e.value.code == mk.MK_ERR_ARG
