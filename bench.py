@@ -52,6 +52,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's x: N replicas take as long as the slowest."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput of `world` replicas that each processed
+    `units_per_rank` units within `ms` milliseconds."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -280,13 +297,8 @@ def run_mine(args):
     clocks = sampler.stop()
     sess.check()
     step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(K)]
-    total_ms = ev[0].elapsed_time(ev[K])
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * w.batch * K / (total_ms / 1e3)
+    total_ms = max_over_ranks(ev[0].elapsed_time(ev[K]), world, dev)
+    value = job_rate(w.batch * K, world, total_ms)
 
     # ---- end to end through the C ABI: host inputs in, host logits out
     h_tok = torch.as_tensor(inp.tokens).pin_memory()
@@ -310,13 +322,8 @@ def run_mine(args):
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     barrier()
-    e2e_ms = max(e0.elapsed_time(e1), wall * 1e3)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * w.batch * Ke / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(max(e0.elapsed_time(e1), wall * 1e3), world, dev)
+    e2e_value = job_rate(w.batch * Ke, world, e2e_ms)
     h2d = (h_tok.numel() + h_sl.numel() + h_bt.numel()) * 4
     d2h = h_logits.numel() * 4
 
