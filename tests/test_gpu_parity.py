@@ -119,6 +119,30 @@ def test_batch_below_schedule_max():
     assert np.array_equal(logits.cpu().numpy(), ref.logits)
 
 
+def test_empty_batch_is_rejected_before_launch():
+    """A step of no rows is an argument error: nothing is launched, the
+    logits and the schedule's next step are untouched."""
+    inp = _ragged_tiny([10, 40, 64])
+    w = inp.workload
+    model = parity._device_model(w.shape, w.seed, None)
+    sched = mk.Sched(model, 4, 64, mk.default_sched_opts())
+    sess = mk.Session(model, sched)
+    kp, vp = synth.device.device_pools(w.shape, w.seed, inp.num_pages)
+    dev = "cuda"
+    logits = torch.full((3, w.shape.vocab), 7.0, device=dev)
+    tok = torch.as_tensor(inp.tokens, device=dev)
+    sl = torch.as_tensor(inp.seq_lens, device=dev)
+    bt = torch.as_tensor(inp.block_tables, device=dev)
+    with pytest.raises(mk.MkError) as e:
+        sess.step(tok[:0], sl[:0], bt, kp, vp, logits)
+    assert e.value.code == mk.MK_ERR_ARG
+    torch.cuda.synchronize()
+    assert bool((logits == 7.0).all())
+    sess.step(tok, sl, bt, kp, vp, logits)  # the session still works
+    sess.check()
+    assert np.array_equal(logits.cpu().numpy(), parity.run_gpu(inp).logits)
+
+
 def test_two_rows_window_layers():
     """Two rows, sliding and full layers (tiny shape): the QKV tiles compute
     the RMSNorm themselves and the slices are merged per (row, group),
