@@ -152,6 +152,10 @@ typedef struct {
                                attention-combine task per (row, KV group, query head), each
                                spread over the whole block; 0 (default): one per (row, KV
                                group), a warp per head (fewer SMs held by merges) */
+  int32_t placement;        /* 0 (default): task k of the flattened waves runs on SM k mod
+                               num_sms; 1: greedy, each layer's tasks in order go to the SM
+                               where a cost model (typical ready and busy time per op, a
+                               claimer's static unit count) says they finish first */
 } mk_sched_opts;
 
 /* Fills opts with the defaults (all zero except fuse_* = 1 and moe_static = 1). */

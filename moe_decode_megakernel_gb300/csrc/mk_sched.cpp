@@ -215,6 +215,68 @@ void balance_moe_ranks(mk_sched* s, std::vector<Desc>& all, size_t begin, int MB
   rank(dn_at, at_dn, dn_rank);
 }
 
+// Greedy placement ("Task scheduler": the cost-model scheduler the pages
+// tried before round robin): each layer's tasks, in list order, go one by one
+// to the SM where they are estimated to finish first, every SM starting the
+// layer at time 0.  A task's estimate is its typical input-ready time and
+// busy time at the full shape (0.1 us; a claimer's busy time is its static
+// units times one unit's), scaled by its weight bytes for GEMV tiles of other
+// sizes.  Each SM's list stays in list order, so every wait still points to
+// an earlier task.
+std::vector<int> place_greedy(const mk_sched* s, const std::vector<Desc>& all,
+                              const std::vector<size_t>& layer_begin, int MB) {
+  const int n = s->num_sms;
+  const ShapeDims& D = s->dims;
+  const int U = s->plan.up_tiles, DN = s->plan.dn_tiles;
+  const int n_act = std::min(D.E, MB * D.K);
+  const int64_t up_units = (int64_t)n_act * U, dn_units = (int64_t)n_act * DN;
+  auto units_of = [](int64_t r, int64_t units, int64_t nc) -> int64_t {
+    return r >= 0 && r < units ? (units - r + nc - 1) / nc : 0;
+  };
+  std::vector<int> sm_of(all.size(), 0);
+  std::vector<int64_t> t(n, 0);
+  for (size_t li = 0; li < layer_begin.size(); ++li) {
+    const size_t b = layer_begin[li], e = li + 1 < layer_begin.size() ? layer_begin[li + 1] : all.size();
+    std::fill(t.begin(), t.end(), 0);
+    const bool full = is_full_layer(s->cfg, (int)li);
+    const int64_t entries = (int64_t)MB * D.NKV * ((s->max_ctx + s->split_len - 1) / s->split_len);
+    for (size_t k = b; k < e; ++k) {
+      const Desc& d = all[k];
+      int64_t earliest = 0, dur = 10;
+      const int64_t nc = std::max(1, d[F_A0 + 5]);
+      switch (d[F_OP]) {
+        case OP_RESID_NORM: dur = 24; break;
+        case OP_ROUTER_GEMM: dur = 60; break;
+        case OP_QKV_PROJ: dur = 55; break;
+        case OP_ATTN_DECODE: earliest = 75; dur = 56; break;
+        case OP_ATTN_DRAIN: earliest = 75; dur = 64 * units_of(d[F_A0 + 4], entries, nc); break;
+        case OP_ATTN_COMBINE: earliest = full ? 155 : 145; dur = 50; break;
+        case OP_O_PROJ: earliest = 215; dur = 25; break;
+        case OP_MOE_UPGATE_ACT_DRAIN: earliest = 90; dur = 90 * units_of(d[F_A0 + 4], up_units, nc); break;
+        case OP_MOE_DOWN_DRAIN: earliest = 190; dur = 24 * units_of(d[F_A0 + 4], dn_units, nc); break;
+        case OP_FFN_UPGATE_ACT: earliest = 30; dur = 60; break;
+        case OP_FFN_DOWN: earliest = 90; dur = 30; break;
+        case OP_LM_HEAD: dur = 40; break;
+        default: break;
+      }
+      // ties (zero-cost claimers, an idle start) go round robin from task k's own SM
+      int best = (int)(k % (size_t)n);
+      int64_t best_end = INT64_MAX;
+      for (int i = 0; i < n; ++i) {
+        const int sm = (int)((k + (size_t)i) % (size_t)n);
+        const int64_t end = std::max(t[sm], earliest) + dur;
+        if (end < best_end) {
+          best_end = end;
+          best = sm;
+        }
+      }
+      sm_of[k] = best;
+      t[best] = best_end;
+    }
+  }
+  return sm_of;
+}
+
 }  // namespace
 
 static int build(mk_sched* s) {
@@ -255,6 +317,7 @@ static int build(mk_sched* s) {
 
   B.alloc_layer_bars();
   std::vector<Desc> all;
+  std::vector<size_t> layer_begin;  // first task of each layer (and of the final norm + LM head)
 
   for (int l = 0; l < L; ++l) {
     LayerBars& lb = s->lb[l];
@@ -533,7 +596,7 @@ static int build(mk_sched* s) {
     lb.n_o = (int)w_o.size();
 
     auto add = [&](std::vector<Desc>& w) { all.insert(all.end(), w.begin(), w.end()); };
-    const size_t layer_begin = all.size();
+    layer_begin.push_back(all.size());
     // the router and the routing head each layer's list: the MoE branch waits on
     // them, and QKV tiles would otherwise sit in front of them on their SMs
     add(w_norm);
@@ -562,10 +625,12 @@ static int build(mk_sched* s) {
         add(w_attn); add(w_acomb); add(w_up); add(w_dn); add(w_o); add(w_mcomb);
         break;
     }
-    if (o.moe_static && o.moe_balance && !unified && !dense) balance_moe_ranks(s, all, layer_begin, MB, full);
+    if (o.moe_static && o.moe_balance && !unified && !dense && o.placement == 0)
+      balance_moe_ranks(s, all, layer_begin.back(), MB, full);
   }
   // final RMSNorm and LM head
   std::vector<Desc> w_final = B.norm_wave(L, norm_rows);
+  layer_begin.push_back(all.size());
   all.insert(all.end(), w_final.begin(), w_final.end());
   for (int r0 = 0; r0 < c.vocab; r0 += lm_tile) {
     Desc d = blank(OP_LM_HEAD, L);
@@ -576,12 +641,13 @@ static int build(mk_sched* s) {
     all.push_back(d);
   }
 
-  // flatten: task k -> SM k mod #SMs
+  // flatten: task k -> SM k mod #SMs, or the greedy placement
+  const std::vector<int> sm_of = o.placement == 1 ? place_greedy(s, all, layer_begin, MB) : std::vector<int>();
   s->tasks = std::move(all);
   s->per_sm.assign(s->num_sms, {});
   for (int k = 0; k < (int)s->tasks.size(); ++k) {
     s->tasks[k][F_TASK] = k;
-    s->per_sm[k % s->num_sms].push_back(k);
+    s->per_sm[o.placement == 1 ? sm_of[k] : k % s->num_sms].push_back(k);
   }
   return MK_OK;
 }
@@ -931,6 +997,7 @@ void mk_default_sched_opts(mk_sched_opts* o) {
   o->attn_static = 1;
   o->moe_balance = 0;
   o->combine_per_head = 0;
+  o->placement = 0;
 }
 
 int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const mk_sched_opts* opts,
@@ -960,6 +1027,10 @@ int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const 
   if (s->opts.wave_order < 0 || s->opts.wave_order > 5) {
     delete s;
     return fail(MK_ERR_ARG, "unknown wave order");
+  }
+  if (s->opts.placement < 0 || s->opts.placement > 1) {
+    delete s;
+    return fail(MK_ERR_ARG, "unknown placement");
   }
   s->watchdog_ns = (int64_t)(s->opts.watchdog_ms > 0 ? s->opts.watchdog_ms : 2000) * 1000000;
   int rc = build(s);

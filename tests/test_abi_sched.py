@@ -93,7 +93,8 @@ def test_schedules_validate_and_simulate(workload, order):
                                   dict(fuse_routing=0, fuse_finalize=0), dict(fuse_norm_qkv=0),
                                   dict(fuse_norm_qkv=0, fuse_routing=0), dict(combine_per_head=1),
                                   dict(attn_static=0), dict(attn_static=0, attn_claimers=3),
-                                  dict(moe_balance=1)])
+                                  dict(moe_balance=1), dict(placement=1), dict(placement=1, wave_order=1),
+                                  dict(placement=1, moe_static=0), dict(placement=1, moe_claimers=5)])
 def test_schedule_variants(opts):
     m, s, inp = sched_for("small", **opts)
     s.validate()

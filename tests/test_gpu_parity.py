@@ -60,7 +60,7 @@ def test_wave_orders_bit_identical(order):
                                   dict(moe_claimers=7), dict(moe_static=0),
                                   dict(moe_static=0, moe_claimers=7), dict(fuse_routing=0),
                                   dict(fuse_norm_qkv=0), dict(attn_static=0),
-                                  dict(moe_balance=1)])
+                                  dict(moe_balance=1), dict(placement=1)])
 def test_unfused_variants_bit_identical(opts):
     inp = synth.make_inputs("small")
     a = parity.run_gpu(inp)
