@@ -124,6 +124,11 @@ WORKLOADS = {
                       desc="small: 8 layers, B=1, context 1024 in 64-token pages"),
     "full_bs1_8k": Workload("full_bs1_8k", "full", 1, ("fixed", 8192), 3,
                             desc="full shape, B=1, context 8192"),
+    # the wave-order ablation's other batch sizes (8K context, uniform routing)
+    "full_bs2_8k": Workload("full_bs2_8k", "full", 2, ("fixed", 8192), 16,
+                            desc="full shape, B=2, context 8192"),
+    "full_bs4_8k": Workload("full_bs4_8k", "full", 4, ("fixed", 8192), 17,
+                            desc="full shape, B=4, context 8192"),
     "batch32_ragged": Workload("batch32_ragged", "full", 32, ("uniform", 512, 32768), 4, zipf=1.1,
                                desc="full shape, B=32, seq_lens U[512,32768], Zipf(1.1) router bias"),
     "long_256k": Workload("long_256k", "full", 1, ("fixed", 262144), 5,
