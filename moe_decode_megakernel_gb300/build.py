@@ -11,8 +11,13 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["mk_api.cpp", "mk_sched.cpp", "mk_shape_tiny.cu", "mk_shape_small.cu", "mk_shape_full.cu",
-           "mk_shape_dense.cu", "mk_static_ws.cu", "mk_service.cpp", "mk_gpu_step.cu"]
+SOURCES = ["mk_api.cpp", "mk_sched.cpp", "mk_static_ws.cu", "mk_service.cpp", "mk_gpu_step.cu"]
+# the compiled model shapes (hidden, n_q, n_kv, head_dim, n_experts, top_k, inter,
+# page_size; the same table as kShapes in mk_api.cpp) and kernel modes (KernelMode):
+# mk_shape.cu is compiled once per pair
+SHAPES = {"tiny": "256,4,2,64,16,4,128,16", "small": "1024,16,2,64,32,4,512,64",
+          "dense": "1024,16,2,64,1,1,2048,64", "full": "2048,32,4,128,128,8,768,64"}
+MODES = 4
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -41,9 +46,10 @@ def build(verbose: bool = False, ptxas_verbose: bool = False) -> str:
     if ptxas_verbose:
         common += ["-Xptxas", "-v"]
 
-    def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = common + ["-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(unit) -> str:
+        src, defs, name = unit
+        obj = os.path.join(BUILD, name + ".o")
+        cmd = common + defs + ["-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd))
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -53,8 +59,15 @@ def build(verbose: bool = False, ptxas_verbose: bool = False) -> str:
             print(r.stderr)
         return obj
 
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
+    units = [(src, [], os.path.splitext(src)[0]) for src in SOURCES]
+    for shape, dims in SHAPES.items():
+        for mode in range(MODES):
+            fn = f"launch_{shape}_{mode}"
+            defs = [f"-DMK_DIM{i}={v}" for i, v in enumerate(dims.split(","))]  # nvcc splits -D at commas
+            units.append(("mk_shape.cu", defs + [f"-DMK_MODE={mode}", f"-DMK_LAUNCH_FN={fn}"],
+                          f"mk_shape_{shape}_{mode}"))
+    with cf.ThreadPoolExecutor(max_workers=min(len(units), max(4, os.cpu_count() or 4))) as ex:
+        objs = list(ex.map(compile_one, units))
     out = os.path.join(HERE, "libmk.so")
     cmd = [_nvcc(), "-shared", *ARCH, "-o", out + ".tmp", *objs, "-lcudart"]
     if verbose:

@@ -35,23 +35,31 @@ int query_num_sms() {
   return n;
 }
 
-int launch_tiny(const Params& p, int grid, cudaStream_t s);
-int launch_small(const Params& p, int grid, cudaStream_t s);
-int launch_dense(const Params& p, int grid, cudaStream_t s);
-int launch_full(const Params& p, int grid, cudaStream_t s);
+// launch_<shape>_<mode>: mk_shape.cu compiled per shape and KernelMode
+#define MK_DECLARE_SHAPE(name)                                     \
+  int launch_##name##_0(const Params& p, int grid, cudaStream_t s); \
+  int launch_##name##_1(const Params& p, int grid, cudaStream_t s); \
+  int launch_##name##_2(const Params& p, int grid, cudaStream_t s); \
+  int launch_##name##_3(const Params& p, int grid, cudaStream_t s);
+MK_DECLARE_SHAPE(tiny)
+MK_DECLARE_SHAPE(small)
+MK_DECLARE_SHAPE(dense)
+MK_DECLARE_SHAPE(full)
+#undef MK_DECLARE_SHAPE
 
 namespace {
 
 struct CompiledShape {
   ShapeDims dims;
-  int (*launch)(const Params&, int, cudaStream_t);
+  int (*launch[kModeCount])(const Params&, int, cudaStream_t);  // by KernelMode
 };
 
 const CompiledShape kShapes[] = {
-    {{256, 4, 2, 64, 16, 4, 128, 16}, launch_tiny},
-    {{1024, 16, 2, 64, 32, 4, 512, 64}, launch_small},
-    {{1024, 16, 2, 64, 1, 1, 2048, 64}, launch_dense},  // dense SwiGLU FFN (one expert, top-1)
-    {{2048, 32, 4, 128, 128, 8, 768, 64}, launch_full},
+    {{256, 4, 2, 64, 16, 4, 128, 16}, {launch_tiny_0, launch_tiny_1, launch_tiny_2, launch_tiny_3}},
+    {{1024, 16, 2, 64, 32, 4, 512, 64}, {launch_small_0, launch_small_1, launch_small_2, launch_small_3}},
+    // dense SwiGLU FFN (one expert, top-1)
+    {{1024, 16, 2, 64, 1, 1, 2048, 64}, {launch_dense_0, launch_dense_1, launch_dense_2, launch_dense_3}},
+    {{2048, 32, 4, 128, 128, 8, 768, 64}, {launch_full_0, launch_full_1, launch_full_2, launch_full_3}},
 };
 
 int cuda_fail(cudaError_t e, const char* what) {
@@ -364,7 +372,11 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   const size_t zero_bytes = s->ws.off("progress") + sizeof(uint32_t) * 8 * (size_t)s->num_sms;
   cudaError_t e = cudaMemsetAsync(workspace, 0, zero_bytes, st);
   if (e != cudaSuccess) return cuda_fail(e, "barrier reset");
-  const int rc = kShapes[m->shape_id].launch(p, s->num_sms, st);
+  // the kernel build for the model's expert format and the schedule's batch
+  const int mode = m->cfg.expert_fp4 ? kModeFp4
+                   : m->cfg.expert_fp8 ? kModeFp8
+                   : s->max_batch <= kTB ? kModeSmallBatch : kModeAnyBatch;
+  const int rc = kShapes[m->shape_id].launch[mode](p, s->num_sms, st);
   if (rc != 0) return cuda_fail((cudaError_t)rc, "megakernel launch");
   return MK_OK;
 }

@@ -103,6 +103,17 @@ constexpr int stage_rows(int k) {
   return r >= 8 ? (r / 8) * 8 : r;
 }
 
+// Kernel builds: the persistent kernel is instantiated per shape and per
+// mode, each instantiation holding only the GEMV paths its steps take (the
+// kernel's code size matters: instruction fetch is among its top stalls).
+enum KernelMode : int {
+  kModeSmallBatch = 0,  // BF16 experts, schedules with max_batch <= kTB
+  kModeAnyBatch = 1,    // BF16 experts, any batch (two-row passes above kTB)
+  kModeFp8 = 2,         // FP8 experts (max_batch <= kTB)
+  kModeFp4 = 3,         // FP4 experts (max_batch <= kTB)
+  kModeCount = 4
+};
+
 struct ShapeDims {
   int H, NQ, NKV, D, E, K, I, P;
 };

@@ -341,11 +341,10 @@ __host__ __device__ constexpr int xs_row() {
   return S::H > S::I ? (S::H > S::G * S::D ? S::H : S::G * S::D) : (S::I > S::G * S::D ? S::I : S::G * S::D);
 }
 
-// The MoE tile plan of the step's expert weights (BF16 or FP8 rows).
-template <class S>
-__device__ __forceinline__ MoePlan plan_of(const Params& p) {
-  constexpr MoePlan m16 = S::mp, m8 = S::mp8, m4 = S::mp4;
-  return p.expert_fp4 ? m4 : p.expert_fp8 ? m8 : m16;
+// The MoE tile plan of a kernel mode's expert weights (BF16, FP8 or FP4 rows).
+template <class S, int M>
+__host__ __device__ constexpr MoePlan plan_of() {
+  return M == kModeFp4 ? S::mp4 : M == kModeFp8 ? S::mp8 : S::mp;
 }
 
 template <class S>
@@ -537,7 +536,7 @@ static __device__ void controller(const Params& p, Ctx& c) {
 // ======================================================================
 // producer
 // ======================================================================
-template <class S>
+template <class S, int M>
 struct Producer {
   const Params& p;
   Ctx c;
@@ -609,6 +608,15 @@ struct Producer {
 
   __device__ __forceinline__ int dense_stages(int rows, int SR) { return (rows + SR - 1) / SR; }
 
+  // A GEMV item with more activation rows than the consumers' cache holds
+  // (kTB) is streamed once per kTB rows: the consumers load each pair of
+  // rows once and run every stage against it (a repeat pass mostly reads
+  // the rows from L2, where the previous pass left them).
+  __device__ __forceinline__ int gemv_passes(int ntok) {
+    if constexpr (M != kModeAnyBatch) return 1;  // the other modes' steps have at most kTB rows
+    return ntok > kTB ? (ntok + kTB - 1) / kTB : 1;
+  }
+
   __device__ __forceinline__ bool dense(const int32_t* d) {
     int32_t it[32];
     for (int i = 0; i < 32; ++i) it[i] = d[i];
@@ -624,9 +632,12 @@ struct Producer {
         base = p.wo + (int64_t)l * S::H * S::NQ * S::D + (int64_t)d[F_A0 + 2] * S::G * S::D;
         ld = S::NQ * S::D; K = S::G * S::D; SR = S::SR_O; break;
     }
-    it[F_NSTAGE] = dense_stages(rows, SR);
+    const int passes = gemv_passes(p.B);
+    it[F_NSTAGE] = dense_stages(rows, SR) * passes;
     if (!push(it)) return false;
-    return load_rows(base, ld, K, row0, rows, SR);
+    for (int ps = 0; ps < passes; ++ps)
+      if (!load_rows(base, ld, K, row0, rows, SR)) return false;
+    return true;
   }
 
   // KV pages as TMA tiles of (P tokens, 64 dims), swizzled: the K page of group
@@ -776,7 +787,7 @@ struct Producer {
 
   __device__ __forceinline__ bool moe_drain(const int32_t* d, int mode) {
     const int l = d[F_LAYER];
-    const MoePlan mp = plan_of<S>(p);
+    constexpr MoePlan mp = plan_of<S, M>();
     const int U = mp.up_tiles, DN = mp.dn_tiles;
     uint32_t* claim = p.bars + d[F_A0];
     const uint32_t n_claimers = (uint32_t)d[F_A0 + 5];
@@ -866,13 +877,13 @@ struct Producer {
         it[F_WAIT0] = d[F_A0 + 2];  // explicit gather barrier (or -1)
         it[F_TGT0] = d[F_A0 + 3];
         it[F_SIG0] = d[F_A0 + 1] + e;
-        it[F_NSTAGE] = mp.up_stages;
+        it[F_NSTAGE] = mp.up_stages * gemv_passes(nrows);
       } else {
         it[F_OP] = W_DOWN_TILE;
         it[F_WAIT0] = d[F_A0 + 1] + e;  // every up tile of expert e
         it[F_TGT0] = U;
         it[F_SIG0] = -1;
-        it[F_NSTAGE] = mp.dn_stages;
+        it[F_NSTAGE] = mp.dn_stages * gemv_passes(nrows);
         // at most kTB rows: each row's (row b, choice j) slot and weight travel
         // with the item, so the epilogue waits on no load
         if (nrows <= kTB) {
@@ -908,7 +919,8 @@ struct Producer {
         }
       }
       if (!push(it)) return false;
-      if (!tile_stages(l, e, t, up)) return false;
+      for (int ps = gemv_passes(nrows); ps > 0; --ps)
+        if (!tile_stages(l, e, t, up)) return false;
       cur = nxt;
       if (cur < total) {
         if (stat) {
@@ -965,11 +977,12 @@ struct Producer {
   }
 
   __device__ __forceinline__ bool tile_stages(int l, int e, int t, bool up) {
-    if (p.expert_fp4) return tile_stages4(l, e, t, up);
-    const MoePlan mp = plan_of<S>(p);
+    if constexpr (M == kModeFp4) return tile_stages4(l, e, t, up);
+    constexpr bool fp8 = M == kModeFp8;
+    constexpr MoePlan mp = plan_of<S, M>();
     const int64_t le = (int64_t)l * S::E + e;
-    const int eb = p.expert_fp8 ? 1 : 2;  // bytes per weight
-    if (!up && !p.expert_fp8) {
+    constexpr int eb = fp8 ? 1 : 2;  // bytes per weight
+    if (!up && !fp8) {
       const uint16_t* base = reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(p.wd) +
                                                                le * S::H * S::I * eb);
       return load_rows(base, S::I, S::I, t * mp.dn_tile, mp.dn_tile, mp.dn_rows);
@@ -999,7 +1012,7 @@ struct Producer {
       uint8_t* dst = stage(slot);
       const int r0 = t * mp.up_tile + s * mp.up_half;
       const uint32_t half = (uint32_t)mp.up_half * S::H * eb;
-      const uint32_t sb = p.expert_fp8 ? (uint32_t)mp.up_half * 4 : 0u;  // FP8: scales
+      const uint32_t sb = fp8 ? (uint32_t)mp.up_half * 4 : 0u;  // FP8: scales
       mbar_expect_tx(fb, 2 * half + 2 * sb);
       bulk_g2s_hint(dst, wg + (le * S::I + r0) * S::H * eb, half, fb, stream_policy);
       bulk_g2s_hint(dst + half, wu + (le * S::I + r0) * S::H * eb, half, fb, stream_policy);
@@ -1017,7 +1030,7 @@ struct Producer {
   // the batch; the same work item as an MoE tile, with each row its own slot
   // and weight 1 (the dense flag A12).
   __device__ __forceinline__ bool ffn_tile(const int32_t* d) {
-    const MoePlan mp = plan_of<S>(p);
+    constexpr MoePlan mp = plan_of<S, M>();
     const bool up = d[F_OP] == OP_FFN_UPGATE_ACT;
     int32_t it[32];
     for (int k = 0; k < 32; ++k) it[k] = d[k];
@@ -1031,9 +1044,11 @@ struct Producer {
       it[F_A0 + 8 + t] = t;  // row b's output goes to slot b (one choice per row)
       it[F_A0 + 10 + t] = __float_as_int(1.f);
     }
-    it[F_NSTAGE] = up ? mp.up_stages : mp.dn_stages;
+    it[F_NSTAGE] = (up ? mp.up_stages : mp.dn_stages) * gemv_passes(p.B);
     if (!push(it)) return false;
-    return tile_stages(d[F_LAYER], 0, d[F_A0], up);
+    for (int ps = gemv_passes(p.B); ps > 0; --ps)
+      if (!tile_stages(d[F_LAYER], 0, d[F_A0], up)) return false;
+    return true;
   }
 
   __device__ __forceinline__ bool passthrough(const int32_t* d) {
@@ -1110,7 +1125,7 @@ struct Producer {
 // ======================================================================
 // consumers
 // ======================================================================
-template <class S>
+template <class S, int M>
 struct Consumer {
   const Params& p;
   Ctx c;
@@ -1331,38 +1346,41 @@ struct Consumer {
     }
   }
 
-  // A GEMV item: stages of full weight rows, activation rows in passes of kTB.
+  // A GEMV item: stages of full weight rows, activation rows in passes of
+  // kTB.  The producer streams the stages once per pass; each pass loads its
+  // activation rows once and runs every stage against them.
   template <int K>
   __device__ __forceinline__ void gemv_item(const int32_t* w, int SR, int total_rows, int ntok) {
     const int op = w[F_OP];
-    const int nst = w[F_NSTAGE];
     const int nchunk = (ntok + kTB - 1) / kTB;
+    const int nst = w[F_NSTAGE] / nchunk;
     int buf = 0;
-    for (int s = 0; s < nst; ++s) {
-      int slot;
-      const bool ok = stage_wait(slot);
-      const int rows = min(SR, total_rows - s * SR);
-      const uint16_t* W = reinterpret_cast<const uint16_t*>(stage(slot));
-      for (int chunk = 0; chunk < nchunk; ++chunk) {
-        const int tb = min(kTB, ntok - kTB * chunk);
-        int32_t tag[4];
-        x_tag(op, w, chunk, tag);
-        if (!(tag[0] == sm.xtag[0] && tag[1] == sm.xtag[1] && tag[2] == sm.xtag[2] && tag[3] == sm.xtag[3])) {
-          consumers_sync();  // every warp is done with the old rows
-          if (!aborted(c)) load_x<K>(op, w, chunk, tb);
-          consumers_sync();
-          if (ct == 0) {
-            sm.xtag[0] = tag[0]; sm.xtag[1] = tag[1]; sm.xtag[2] = tag[2]; sm.xtag[3] = tag[3];
-          }
+    for (int chunk = 0; chunk < nchunk; ++chunk) {
+      const int tb = min(kTB, ntok - kTB * chunk);
+      int32_t tag[4];
+      x_tag(op, w, chunk, tag);
+      if (!(tag[0] == sm.xtag[0] && tag[1] == sm.xtag[1] && tag[2] == sm.xtag[2] && tag[3] == sm.xtag[3])) {
+        consumers_sync();  // every warp is done with the old rows
+        if (!aborted(c)) load_x<K>(op, w, chunk, tb);
+        consumers_sync();
+        if (ct == 0) {
+          sm.xtag[0] = tag[0]; sm.xtag[1] = tag[1]; sm.xtag[2] = tag[2]; sm.xtag[3] = tag[3];
         }
+      }
+      for (int s = 0; s < nst; ++s) {
+        int slot;
+        const bool ok = stage_wait(slot);
+        const int rows = min(SR, total_rows - s * SR);
+        const uint16_t* W = reinterpret_cast<const uint16_t*>(stage(slot));
         if (__all_sync(FULL, ok && !aborted(c))) gemv_rows<K>(W, rows, tb, sm.out[buf]);
         consumers_sync();
         if (!aborted(c)) epilogue(op, w, s, rows, chunk, tb, sm.out[buf]);
         buf ^= 1;
+        stage_release(slot);
       }
-      stage_release(slot);
     }
   }
+
 
   // Activation rows of an FP8 / FP4 expert tile as the B operand of f16 MMAs
   // (m16n8k16, the weights as A).  Column 2t of B is the f16 rounding of
@@ -1662,7 +1680,7 @@ struct Consumer {
         break;
       }
       case W_UP_TILE: {  // SiLU(gate) * up ("Tasks": the SiLU-and-multiply epilogue)
-        const MoePlan mp = plan_of<S>(p);
+        constexpr MoePlan mp = plan_of<S, M>();
         const float act = v0 / (1.f + expf(-v0)) * v1;
         const int row = w[F_A0 + 2] + t;
         p.u[(int64_t)row * S::I + w[F_A0 + 1] * mp.up_tile + s * mp.up_half + r0] = act;
@@ -1687,7 +1705,7 @@ struct Consumer {
         break;
       }
       case W_DOWN_TILE: {  // weighted, into the (row b, slot j) of the output
-        const MoePlan mp = plan_of<S>(p);
+        constexpr MoePlan mp = plan_of<S, M>();
         const int n = w[F_A0 + 1] * mp.dn_tile + s * mp.dn_rows + r0;
         *reinterpret_cast<float2*>(p.y + (int64_t)dslot * S::H + n) = make_float2(dwt * v0, dwt * v1);
         break;
@@ -2545,46 +2563,53 @@ struct Consumer {
   }
 
   __device__ __forceinline__ void execute(const int32_t* w) {
+    // above kTB rows (any-batch mode only) the two-row GEMV; FP8 / FP4
+    // experts take their tensor-core GEMVs
+    constexpr bool any_batch = M == kModeAnyBatch;
     switch (w[F_OP]) {
       case OP_ROUTER_GEMM:
         if (w[F_A0 + 7] && p.B <= kTB) norm_into_cache(w);
-        if (p.B <= kTB) gemv_item_teams<S::H>(w, S::SR_H, w[F_A0 + 1], p.B);
-        else gemv_item<S::H>(w, S::SR_H, w[F_A0 + 1], p.B);
+        if (!any_batch || p.B <= kTB) gemv_item_teams<S::H>(w, S::SR_H, w[F_A0 + 1], p.B);
+        else if constexpr (any_batch) gemv_item<S::H>(w, S::SR_H, w[F_A0 + 1], p.B);
         if (w[F_A0 + 5]) route_if_last(w);
         break;
       case OP_QKV_PROJ:
       case OP_LM_HEAD:
         if (w[F_OP] == OP_QKV_PROJ && w[F_A0 + 7] && p.B <= kTB) norm_into_cache(w);
-        if (p.B <= kTB) gemv_item_teams<S::H>(w, S::SR_H, w[F_A0 + 1], p.B);
-        else gemv_item<S::H>(w, S::SR_H, w[F_A0 + 1], p.B);
+        if (!any_batch || p.B <= kTB) gemv_item_teams<S::H>(w, S::SR_H, w[F_A0 + 1], p.B);
+        else if constexpr (any_batch) gemv_item<S::H>(w, S::SR_H, w[F_A0 + 1], p.B);
         break;
       case OP_O_PROJ:
-        if (p.B <= kTB) gemv_item_teams<S::G * S::D>(w, S::SR_O, w[F_A0 + 1], p.B);
-        else gemv_item<S::G * S::D>(w, S::SR_O, w[F_A0 + 1], p.B);
+        if (!any_batch || p.B <= kTB) gemv_item_teams<S::G * S::D>(w, S::SR_O, w[F_A0 + 1], p.B);
+        else if constexpr (any_batch) gemv_item<S::G * S::D>(w, S::SR_O, w[F_A0 + 1], p.B);
         break;
       case W_UP_TILE:
-        if (p.expert_fp4) {  // schedules with FP8 / FP4 experts have max_batch <= kTB
+        if constexpr (M == kModeFp4) {
           if (w[F_A0 + 3] <= 1) gemv_item_fp4<S::H, 1>(w, w[F_A0 + 3]);
           else gemv_item_fp4<S::H, kTB>(w, w[F_A0 + 3]);
-        } else if (p.expert_fp8) {
+        } else if constexpr (M == kModeFp8) {
           constexpr MoePlan m8 = S::mp8;
           if (w[F_A0 + 3] <= 1) gemv_item_fp8<S::H, 1>(w, 2 * m8.up_half, w[F_A0 + 3]);
           else gemv_item_fp8<S::H, kTB>(w, 2 * m8.up_half, w[F_A0 + 3]);
-        } else if (w[F_A0 + 3] <= kTB)
-          gemv_item_teams<S::H>(w, 2 * S::mp.up_half, 2 * S::mp.up_half * S::mp.up_stages, w[F_A0 + 3]);
-        else
-          gemv_item<S::H>(w, 2 * S::mp.up_half, 2 * S::mp.up_half * S::mp.up_stages, w[F_A0 + 3]);
+        } else {
+          if (!any_batch || w[F_A0 + 3] <= kTB)
+            gemv_item_teams<S::H>(w, 2 * S::mp.up_half, 2 * S::mp.up_half * S::mp.up_stages, w[F_A0 + 3]);
+          else if constexpr (any_batch)
+            gemv_item<S::H>(w, 2 * S::mp.up_half, 2 * S::mp.up_half * S::mp.up_stages, w[F_A0 + 3]);
+        }
         break;
       case W_DOWN_TILE:
-        if (p.expert_fp4) {
+        if constexpr (M == kModeFp4) {
           if (w[F_A0 + 3] <= 1) gemv_item_fp4<S::I, 1>(w, w[F_A0 + 3]);
           else gemv_item_fp4<S::I, kTB>(w, w[F_A0 + 3]);
-        } else if (p.expert_fp8) {
+        } else if constexpr (M == kModeFp8) {
           constexpr MoePlan m8 = S::mp8;
           if (w[F_A0 + 3] <= 1) gemv_item_fp8<S::I, 1>(w, m8.dn_rows, w[F_A0 + 3]);
           else gemv_item_fp8<S::I, kTB>(w, m8.dn_rows, w[F_A0 + 3]);
-        } else if (w[F_A0 + 3] <= kTB) gemv_item_teams<S::I>(w, S::mp.dn_rows, S::mp.dn_tile, w[F_A0 + 3]);
-        else gemv_item<S::I>(w, S::mp.dn_rows, S::mp.dn_tile, w[F_A0 + 3]);
+        } else {
+          if (!any_batch || w[F_A0 + 3] <= kTB) gemv_item_teams<S::I>(w, S::mp.dn_rows, S::mp.dn_tile, w[F_A0 + 3]);
+          else if constexpr (any_batch) gemv_item<S::I>(w, S::mp.dn_rows, S::mp.dn_tile, w[F_A0 + 3]);
+        }
         break;
       case W_ATTN: attn(w); break;
       case OP_ATTN_COMBINE: attn_combine(w); break;
@@ -2751,7 +2776,7 @@ static __device__ void storer(const Params& p, Ctx& c) {
   }
 }
 
-template <class S>
+template <class S, int M>
 __global__ void __launch_bounds__(kThreads, 1) mk_persistent(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   // the 128-byte TMA swizzle of the KV pages is laid out from a 1024-byte
@@ -2786,13 +2811,13 @@ __global__ void __launch_bounds__(kThreads, 1) mk_persistent(const __grid_consta
   if (warp == 0) {
     controller(p, c);
   } else if (warp == 1) {
-    Producer<S> pr{p, c, 0ull};
+    Producer<S, M> pr{p, c, 0ull};
     pr.run();
   } else if (warp == 2) {
     storer(p, c);
   } else {
     const int ct = threadIdx.x - 96;
-    Consumer<S> cs{p, c, *scr, ct, ct / 32, ct & 31};
+    Consumer<S, M> cs{p, c, *scr, ct, ct / 32, ct & 31};
     cs.run();
   }
 }

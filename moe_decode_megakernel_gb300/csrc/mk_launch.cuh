@@ -8,9 +8,9 @@ namespace mk {
 // One CTA per SM; a cooperative launch so that every CTA is resident at once
 // (CTAs wait on each other's counters, so a CTA left unscheduled would stall
 // the step until the watchdog).
-template <class S>
+template <class S, int M>
 int launch_shape(const Params& p, int grid, cudaStream_t stream) {
-  const void* fn = reinterpret_cast<const void*>(&dev::mk_persistent<S>);
+  const void* fn = reinterpret_cast<const void*>(&dev::mk_persistent<S, M>);
   const size_t smem = dev::smem_bytes<S>();
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
