@@ -375,7 +375,7 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   // the kernel build for the model's expert format and the schedule's batch
   const int mode = m->cfg.expert_fp4 ? kModeFp4
                    : m->cfg.expert_fp8 ? kModeFp8
-                   : s->max_batch <= kTB ? kModeSmallBatch : kModeAnyBatch;
+                   : s->max_batch <= kTB && s->lean ? kModeSmallBatch : kModeAnyBatch;
   const int rc = kShapes[m->shape_id].launch[mode](p, s->num_sms, st);
   if (rc != 0) return cuda_fail((cudaError_t)rc, "megakernel launch");
   return MK_OK;

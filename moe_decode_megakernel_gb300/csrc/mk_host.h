@@ -59,6 +59,9 @@ struct mk_sched {
   mk::MoePlan plan;
   mk_sched_opts opts;
   int num_sms = 0, max_batch = 0, max_ctx = 0;
+  // the lean kernel build runs it: fused routing and MoE combine, merges a
+  // warp per head, static separate claims (no task the lean build leaves out)
+  bool lean = false;
   int split_len = 0, n_static = 0, max_slots = 0, max_attn_entries = 0;
   int lm_bar = -1;
   int trace_cap = 0;

@@ -107,7 +107,8 @@ constexpr int stage_rows(int k) {
 // mode, each instantiation holding only the GEMV paths its steps take (the
 // kernel's code size matters: instruction fetch is among its top stalls).
 enum KernelMode : int {
-  kModeSmallBatch = 0,  // BF16 experts, schedules with max_batch <= kTB
+  kModeSmallBatch = 0,  // BF16 experts, max_batch <= kTB, lean schedules: fused routing and MoE
+                        // combine, a warp per head in the merges, static separate claims
   kModeAnyBatch = 1,    // BF16 experts, any batch (two-row passes above kTB)
   kModeFp8 = 2,         // FP8 experts (max_batch <= kTB)
   kModeFp4 = 3,         // FP4 experts (max_batch <= kTB)

@@ -538,6 +538,8 @@ static __device__ void controller(const Params& p, Ctx& c) {
 // ======================================================================
 template <class S, int M>
 struct Producer {
+  // the lean build (kModeSmallBatch): static claims and separate MoE drains only
+  static constexpr bool kLean = M == kModeSmallBatch;
   const Params& p;
   Ctx c;
   // weights and KV pages are read once per step: streaming them with
@@ -724,7 +726,7 @@ struct Producer {
     // static claims: claimer ci of n takes the entries ci, ci + n, ...
     const int ci = d[F_A0 + 4];
     const uint32_t n_cl = (uint32_t)d[F_A0 + 5];
-    const bool stat = ci >= 0;
+    const bool stat = kLean || ci >= 0;
     uint32_t next = stat ? (uint32_t)ci : atomicAdd(claim, 1u);
     if (!stat) ++c.stat[3];
     for (;;) {
@@ -791,7 +793,7 @@ struct Producer {
     const int U = mp.up_tiles, DN = mp.dn_tiles;
     uint32_t* claim = p.bars + d[F_A0];
     const uint32_t n_claimers = (uint32_t)d[F_A0 + 5];
-    const bool stat = d[F_A0 + 7] != 0;
+    const bool stat = kLean || d[F_A0 + 7] != 0;
     // the routing decides which expert rows to stream: wait for the queue
     // (once per layer: the down drain follows the up/gate drain's wait)
     int n_act;
@@ -1095,7 +1097,7 @@ struct Producer {
         case OP_LM_HEAD: ok = dense(d); break;
         case OP_ATTN_DECODE: ok = attn_decode(d); break;
         case OP_ATTN_DRAIN: ok = attn_drain(d); break;
-        case OP_MOE_UPGATE_ACT_DRAIN: ok = moe_drain(d, d[F_A0 + 6]); break;
+        case OP_MOE_UPGATE_ACT_DRAIN: ok = moe_drain(d, kLean ? 1 : d[F_A0 + 6]); break;
         case OP_MOE_DOWN_DRAIN: ok = moe_drain(d, 2); break;
         case OP_FFN_UPGATE_ACT:
         case OP_FFN_DOWN: ok = ffn_tile(d); break;
@@ -1127,6 +1129,8 @@ struct Producer {
 // ======================================================================
 template <class S, int M>
 struct Consumer {
+  // the lean build (kModeSmallBatch) leaves out the tasks of unfused schedules
+  static constexpr bool kLean = M == kModeSmallBatch;
   const Params& p;
   Ctx c;
   Scratch<S>& sm;
@@ -2023,9 +2027,11 @@ struct Consumer {
   __device__ __forceinline__ void attn_combine(const int32_t* w) {
     constexpr int G = S::G, D = S::D, DPL = D / 32;
     const int l = w[F_LAYER], b = w[F_A0], g = w[F_A0 + 1];
-    if (w[F_A0 + 3] >= 0) {
-      attn_combine_one_head(l, b, g, w[F_A0 + 3]);
-      return;
+    if constexpr (!kLean) {
+      if (w[F_A0 + 3] >= 0) {  // one task per head
+        attn_combine_one_head(l, b, g, w[F_A0 + 3]);
+        return;
+      }
     }
     if (b >= p.B || cw >= G) return;
     float o[DPL];
@@ -2614,10 +2620,11 @@ struct Consumer {
       case W_ATTN: attn(w); break;
       case OP_ATTN_COMBINE: attn_combine(w); break;
       case OP_RESID_NORM: norm(w); break;
-      case OP_ROUTER_TOPK: topk(w); break;
-      case OP_ROUTE_FINALIZE: finalize(w[F_LAYER], true); break;
-      case OP_MOE_GATHER: gather(w); break;
-      case OP_MOE_COMBINE: moe_combine(w); break;
+      // tasks of unfused schedules: not in the lean build
+      case OP_ROUTER_TOPK: if constexpr (!kLean) topk(w); break;
+      case OP_ROUTE_FINALIZE: if constexpr (!kLean) finalize(w[F_LAYER], true); break;
+      case OP_MOE_GATHER: if constexpr (!kLean) gather(w); break;
+      case OP_MOE_COMBINE: if constexpr (!kLean) moe_combine(w); break;
       default: break;  // NOP, CLAIM_END: only the signal
     }
   }

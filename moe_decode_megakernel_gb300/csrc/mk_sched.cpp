@@ -1039,6 +1039,15 @@ int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const 
     delete s;
     return rc;
   }
+  s->lean = true;
+  for (const Desc& d : s->tasks) {
+    const int op = d[F_OP];
+    if (op == OP_ROUTER_TOPK || op == OP_ROUTE_FINALIZE || op == OP_MOE_GATHER || op == OP_MOE_COMBINE ||
+        (op == OP_ATTN_COMBINE && d[F_A0 + 3] >= 0) || (op == OP_ATTN_DRAIN && d[F_A0 + 4] < 0) ||
+        (op == OP_MOE_UPGATE_ACT_DRAIN && (d[F_A0 + 6] != 1 || d[F_A0 + 7] == 0)) ||
+        (op == OP_MOE_DOWN_DRAIN && d[F_A0 + 7] == 0))
+      s->lean = false;
+  }
   layout_workspace(s);
   *out = s;
   return MK_OK;
