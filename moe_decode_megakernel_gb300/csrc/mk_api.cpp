@@ -40,7 +40,9 @@ int query_num_sms() {
   int launch_##name##_0(const Params& p, int grid, cudaStream_t s); \
   int launch_##name##_1(const Params& p, int grid, cudaStream_t s); \
   int launch_##name##_2(const Params& p, int grid, cudaStream_t s); \
-  int launch_##name##_3(const Params& p, int grid, cudaStream_t s);
+  int launch_##name##_3(const Params& p, int grid, cudaStream_t s); \
+  int launch_##name##_4(const Params& p, int grid, cudaStream_t s); \
+  int launch_##name##_5(const Params& p, int grid, cudaStream_t s);
 MK_DECLARE_SHAPE(tiny)
 MK_DECLARE_SHAPE(small)
 MK_DECLARE_SHAPE(dense)
@@ -55,11 +57,11 @@ struct CompiledShape {
 };
 
 const CompiledShape kShapes[] = {
-    {{256, 4, 2, 64, 16, 4, 128, 16}, {launch_tiny_0, launch_tiny_1, launch_tiny_2, launch_tiny_3}},
-    {{1024, 16, 2, 64, 32, 4, 512, 64}, {launch_small_0, launch_small_1, launch_small_2, launch_small_3}},
+    {{256, 4, 2, 64, 16, 4, 128, 16}, {launch_tiny_0, launch_tiny_1, launch_tiny_2, launch_tiny_3, launch_tiny_4, launch_tiny_5}},
+    {{1024, 16, 2, 64, 32, 4, 512, 64}, {launch_small_0, launch_small_1, launch_small_2, launch_small_3, launch_small_4, launch_small_5}},
     // dense SwiGLU FFN (one expert, top-1)
-    {{1024, 16, 2, 64, 1, 1, 2048, 64}, {launch_dense_0, launch_dense_1, launch_dense_2, launch_dense_3}},
-    {{2048, 32, 4, 128, 128, 8, 768, 64}, {launch_full_0, launch_full_1, launch_full_2, launch_full_3}},
+    {{1024, 16, 2, 64, 1, 1, 2048, 64}, {launch_dense_0, launch_dense_1, launch_dense_2, launch_dense_3, launch_dense_4, launch_dense_5}},
+    {{2048, 32, 4, 128, 128, 8, 768, 64}, {launch_full_0, launch_full_1, launch_full_2, launch_full_3, launch_full_4, launch_full_5}},
 };
 
 int cuda_fail(cudaError_t e, const char* what) {
@@ -373,8 +375,8 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   cudaError_t e = cudaMemsetAsync(workspace, 0, zero_bytes, st);
   if (e != cudaSuccess) return cuda_fail(e, "barrier reset");
   // the kernel build for the model's expert format and the schedule's batch
-  const int mode = m->cfg.expert_fp4 ? kModeFp4
-                   : m->cfg.expert_fp8 ? kModeFp8
+  const int mode = m->cfg.expert_fp4 ? (s->lean ? kModeFp4Lean : kModeFp4)
+                   : m->cfg.expert_fp8 ? (s->lean ? kModeFp8Lean : kModeFp8)
                    : s->max_batch <= kTB && s->lean ? kModeSmallBatch : kModeAnyBatch;
   const int rc = kShapes[m->shape_id].launch[mode](p, s->num_sms, st);
   if (rc != 0) return cuda_fail((cudaError_t)rc, "megakernel launch");

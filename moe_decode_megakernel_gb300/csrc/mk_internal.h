@@ -109,11 +109,23 @@ constexpr int stage_rows(int k) {
 enum KernelMode : int {
   kModeSmallBatch = 0,  // BF16 experts, max_batch <= kTB, lean schedules: fused routing and MoE
                         // combine, a warp per head in the merges, static separate claims
-  kModeAnyBatch = 1,    // BF16 experts, any batch (two-row passes above kTB)
-  kModeFp8 = 2,         // FP8 experts (max_batch <= kTB)
-  kModeFp4 = 3,         // FP4 experts (max_batch <= kTB)
-  kModeCount = 4
+  kModeAnyBatch = 1,    // BF16 experts, any batch (two-row passes above kTB), any schedule
+  kModeFp8 = 2,         // FP8 experts (max_batch <= kTB), any schedule
+  kModeFp4 = 3,         // FP4 experts (max_batch <= kTB), any schedule
+  kModeFp8Lean = 4,     // FP8 experts, lean schedules
+  kModeFp4Lean = 5,     // FP4 experts, lean schedules
+  kModeCount = 6
 };
+#if defined(__CUDACC__)
+#define MK_HOST_DEVICE __host__ __device__
+#else
+#define MK_HOST_DEVICE
+#endif
+MK_HOST_DEVICE constexpr bool mode_fp8(int m) { return m == kModeFp8 || m == kModeFp8Lean; }
+MK_HOST_DEVICE constexpr bool mode_fp4(int m) { return m == kModeFp4 || m == kModeFp4Lean; }
+MK_HOST_DEVICE constexpr bool mode_lean(int m) {
+  return m == kModeSmallBatch || m == kModeFp8Lean || m == kModeFp4Lean;
+}
 
 struct ShapeDims {
   int H, NQ, NKV, D, E, K, I, P;

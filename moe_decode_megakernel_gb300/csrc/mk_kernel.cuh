@@ -344,7 +344,7 @@ __host__ __device__ constexpr int xs_row() {
 // The MoE tile plan of a kernel mode's expert weights (BF16, FP8 or FP4 rows).
 template <class S, int M>
 __host__ __device__ constexpr MoePlan plan_of() {
-  return M == kModeFp4 ? S::mp4 : M == kModeFp8 ? S::mp8 : S::mp;
+  return mode_fp4(M) ? S::mp4 : mode_fp8(M) ? S::mp8 : S::mp;
 }
 
 template <class S>
@@ -538,8 +538,8 @@ static __device__ void controller(const Params& p, Ctx& c) {
 // ======================================================================
 template <class S, int M>
 struct Producer {
-  // the lean build (kModeSmallBatch): static claims and separate MoE drains only
-  static constexpr bool kLean = M == kModeSmallBatch;
+  // the lean builds: static claims and separate MoE drains only
+  static constexpr bool kLean = mode_lean(M);
   const Params& p;
   Ctx c;
   // weights and KV pages are read once per step: streaming them with
@@ -979,8 +979,8 @@ struct Producer {
   }
 
   __device__ __forceinline__ bool tile_stages(int l, int e, int t, bool up) {
-    if constexpr (M == kModeFp4) return tile_stages4(l, e, t, up);
-    constexpr bool fp8 = M == kModeFp8;
+    if constexpr (mode_fp4(M)) return tile_stages4(l, e, t, up);
+    constexpr bool fp8 = mode_fp8(M);
     constexpr MoePlan mp = plan_of<S, M>();
     const int64_t le = (int64_t)l * S::E + e;
     constexpr int eb = fp8 ? 1 : 2;  // bytes per weight
@@ -1129,8 +1129,8 @@ struct Producer {
 // ======================================================================
 template <class S, int M>
 struct Consumer {
-  // the lean build (kModeSmallBatch) leaves out the tasks of unfused schedules
-  static constexpr bool kLean = M == kModeSmallBatch;
+  // the lean builds leave out the tasks of unfused schedules
+  static constexpr bool kLean = mode_lean(M);
   const Params& p;
   Ctx c;
   Scratch<S>& sm;
@@ -2106,15 +2106,15 @@ struct Consumer {
     }
     consumers_sync();
     if (ct < D) {
-      float M = -INFINITY;
+      float mx = -INFINITY;
 #pragma unroll
       for (int k = 0; k < kConsumerWarps; ++k)
-        if (sm.red[k] > 0.f) M = fmaxf(M, sm.red[kConsumerWarps + k]);
+        if (sm.red[k] > 0.f) mx = fmaxf(mx, sm.red[kConsumerWarps + k]);
       float zt = 0.f, a = 0.f;
 #pragma unroll
       for (int k = 0; k < kConsumerWarps; ++k)
         if (sm.red[k] > 0.f) {
-          const float sc = exp2f(sm.red[kConsumerWarps + k] - M);
+          const float sc = exp2f(sm.red[kConsumerWarps + k] - mx);
           zt = fmaf(sc, sm.red[k], zt);
           a = fmaf(sc, red[k * D + ct], a);
         }
@@ -2131,12 +2131,12 @@ struct Consumer {
     const bool full = p.window == 0 || (l + 1) % p.full_period == 0;
     const int n = min(full ? slices_of(p, __ldg(p.seq_lens + b)) : p.n_static, p.max_slots);
     const int64_t base = ((int64_t)b * S::NKV + g) * p.max_slots;
-    float M = -INFINITY;
+    float mx = -INFINITY;
     for (int j = lane; j < n; j += 32) {
       const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((base + j) * G + h) * 2));
-      if (ml.y > 0.f) M = fmaxf(M, ml.x);
+      if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
     }
-    M = warp_max(M);
+    mx = warp_max(mx);
     float z = 0.f, acc[DPL];
 #pragma unroll
     for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
@@ -2146,7 +2146,7 @@ struct Consumer {
       if (j0 + lane < n) {
         const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((base + j0 + lane) * G + h) * 2));
         if (ml.y > 0.f) {
-          cj = exp2f(ml.x - M);
+          cj = exp2f(ml.x - mx);
           z = fmaf(cj, ml.y, z);
         }
       }
@@ -2590,10 +2590,10 @@ struct Consumer {
         else if constexpr (any_batch) gemv_item<S::G * S::D>(w, S::SR_O, w[F_A0 + 1], p.B);
         break;
       case W_UP_TILE:
-        if constexpr (M == kModeFp4) {
+        if constexpr (mode_fp4(M)) {
           if (w[F_A0 + 3] <= 1) gemv_item_fp4<S::H, 1>(w, w[F_A0 + 3]);
           else gemv_item_fp4<S::H, kTB>(w, w[F_A0 + 3]);
-        } else if constexpr (M == kModeFp8) {
+        } else if constexpr (mode_fp8(M)) {
           constexpr MoePlan m8 = S::mp8;
           if (w[F_A0 + 3] <= 1) gemv_item_fp8<S::H, 1>(w, 2 * m8.up_half, w[F_A0 + 3]);
           else gemv_item_fp8<S::H, kTB>(w, 2 * m8.up_half, w[F_A0 + 3]);
@@ -2605,10 +2605,10 @@ struct Consumer {
         }
         break;
       case W_DOWN_TILE:
-        if constexpr (M == kModeFp4) {
+        if constexpr (mode_fp4(M)) {
           if (w[F_A0 + 3] <= 1) gemv_item_fp4<S::I, 1>(w, w[F_A0 + 3]);
           else gemv_item_fp4<S::I, kTB>(w, w[F_A0 + 3]);
-        } else if constexpr (M == kModeFp8) {
+        } else if constexpr (mode_fp8(M)) {
           constexpr MoePlan m8 = S::mp8;
           if (w[F_A0 + 3] <= 1) gemv_item_fp8<S::I, 1>(w, m8.dn_rows, w[F_A0 + 3]);
           else gemv_item_fp8<S::I, kTB>(w, m8.dn_rows, w[F_A0 + 3]);
