@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--workload", default="full_bs1_8k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--trace", default="", help="write a Chrome trace of one step here")
+    ap.add_argument("--service", type=int, default=0,
+                    help="time G tokens of the host decode service (GPU step, greedy) after an "
+                         "8191-token prompt, instead of the contract line")
     return ap.parse_args()
 
 
@@ -381,8 +384,70 @@ def run_mine(args):
         dist.destroy_process_group()
 
 
+def run_service(args):
+    """The host decode service (include/mk_service.h) on the full model at batch
+    1: one sequence whose 8191-token prompt is fed one token per step, then G
+    greedy tokens timed through mk_service_run (each step: inputs copied in,
+    the megakernel, the device argmax, the token copied back, the host's
+    bookkeeping) against the megakernel alone at the same contexts."""
+    import numpy as np
+    import torch
+    import synth
+    import synth.device
+    import moe_decode_megakernel_gb300 as mk
+    from moe_decode_megakernel_gb300 import service as sv
+    G = args.service
+    sh = synth.MODELS["full"]
+    seed, P = 3, 8191
+    ctx = P + G
+    page = sh.page_size
+    max_pages = (ctx + page - 1) // page
+    weights = synth.device.device_weights(sh, seed)
+    model = mk.Model(mk.config_from(sh), mk.weights_from(weights), keepalive=weights)
+    kp, vp = synth.device.device_pools(sh, seed, max_pages)
+    sched = mk.Sched(model, 1, ctx)
+    gstep = sv.GpuStep(model, [sched], kp, vp, max_pages)
+    svc = sv.Service(max_pages, page, max_pages, 1, gstep)
+    prompt = np.random.default_rng(seed).integers(0, sh.vocab, P)
+    svc.add(1, prompt, max_new=G)
+    svc.run(max_steps=P - 1)  # the prompt but its last token
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    out = svc.run()  # the last prompt token, then G - 1 fed samples: G steps, G tokens
+    wall = time.perf_counter() - t0
+    assert len(out[1]) == G and svc.last_run_steps == G
+    # the megakernel alone over the same contexts (the pool holds the service's pages)
+    sess = mk.Session(model, sched)
+    # the only sequence of a fresh service holds pages 0, 1, ... in order
+    bt = torch.arange(max_pages, dtype=torch.int32, device="cuda")[None, :]
+    logits = torch.empty(1, sh.vocab, device="cuda")
+    tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lens = [torch.tensor([P + i + 1], dtype=torch.int32, device="cuda") for i in range(G)]
+    for i in range(3):
+        sess.step(tok, lens[0], bt, kp, vp, logits)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(G):
+        sess.step(tok, lens[i], bt, kp, vp, logits)
+    e1.record()
+    torch.cuda.synchronize()
+    sess.check()
+    kernel_ms = e0.elapsed_time(e1) / G
+    print(json.dumps({
+        "mode": "service", "metric": "host decode service tok/s (GPU step, greedy), batch 1",
+        "value": G / wall, "unit": "tok/s", "tokens": G, "context": [P + 1, P + G],
+        "ms_per_token": 1e3 * wall / G, "kernel_ms_per_step": kernel_ms,
+        "host_and_copies_ms_per_step": 1e3 * wall / G - kernel_ms,
+        "config": {"workload": "full shape, one sequence, 8191-token prompt fed token by token",
+                   "weights": "bf16 random N(0,0.02)", "data": "synthetic"}}), flush=True)
+
+
 def main():
     args = parse()
+    if args.service:
+        run_service(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
