@@ -127,8 +127,10 @@ int32_t mk_service_live(const mk_service* s); /* running + parked */
 /* ---- the step on the GPU ---- */
 
 /* Device bytes mk_gpu_step needs for its inputs and outputs at this batch
- * and block-table width (tokens, lengths, block tables, fp32 logits, next
- * tokens), 256-byte aligned parts. */
+ * and block-table width (tokens, lengths and block tables as one block; the
+ * next tokens and a copy of the step's error record; fp32 logits),
+ * 256-byte aligned parts.  The GPU step also holds pinned host copies of
+ * the input and output blocks (one copy each way per step). */
 size_t mk_gpu_step_dev_bytes(const mk_model* m, int32_t max_batch, int32_t max_pages);
 
 /* A GPU step on the caller's memory: the KV pools ([n_layers][num_pages]

@@ -383,14 +383,11 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   return MK_OK;
 }
 
-int mk_check_step(const mk_sched* s, const void* workspace, void* stream) {
-  if (!s || !workspace) return fail(MK_ERR_ARG, "null argument");
+}  // extern "C"
+
+namespace mk {
+int check_record(const mk_sched* s, const uint32_t* rec, const void* workspace, void* stream) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  uint32_t rec[8];
-  cudaError_t e = cudaMemcpyAsync(rec, static_cast<const uint8_t*>(workspace) + s->ws.off("error"), sizeof rec,
-                                  cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  if (e != cudaSuccess) return cuda_fail(e, "step");
   if (rec[0] == 0) return MK_OK;
   const std::string where = " (sm " + std::to_string(rec[1]) + ", task " + std::to_string((int32_t)rec[2]) +
                             ", op " + std::to_string((int32_t)rec[6]) + ", layer " +
@@ -403,8 +400,22 @@ int mk_check_step(const mk_sched* s, const void* workspace, void* stream) {
   if (rec[0] == 5)
     return fail(MK_ERR_DEVICE, "descriptor or work ring out of step (a stale entry was read)" + where);
   if (rec[0] == 6)
-    return fail(MK_ERR_DEVICE, "an FP8 expert tile's activation is beyond the f16 range (|x| > 65504)" + where);
+    return fail(MK_ERR_DEVICE, "an FP8 or FP4 expert tile's activation is beyond the f16 range (|x| > 65504)" + where);
   return fail(MK_ERR_DEVICE, "index out of range" + where);
+}
+}  // namespace mk
+
+extern "C" {
+
+int mk_check_step(const mk_sched* s, const void* workspace, void* stream) {
+  if (!s || !workspace) return fail(MK_ERR_ARG, "null argument");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t rec[8];
+  cudaError_t e = cudaMemcpyAsync(rec, static_cast<const uint8_t*>(workspace) + s->ws.off("error"), sizeof rec,
+                                  cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "step");
+  return mk::check_record(s, rec, workspace, stream);
 }
 
 }  // extern "C"

@@ -21,7 +21,11 @@ constexpr int kArgmaxThreads = 512;
 // (value, index) pairs meet by warp shuffles, then across warps in shared
 // memory.  Ties go to the lower index; NaN compares false, so it never wins.
 __global__ void __launch_bounds__(kArgmaxThreads) argmax_rows(const float* __restrict__ logits, int vocab,
-                                                                int32_t* __restrict__ next) {
+                                                                int32_t* __restrict__ next,
+                                                                const uint32_t* __restrict__ rec_src,
+                                                                uint32_t* __restrict__ rec_dst) {
+  // the GPU step's copy of the step's error record, beside the tokens
+  if (rec_src && blockIdx.x == 0 && threadIdx.x < 8) rec_dst[threadIdx.x] = rec_src[threadIdx.x];
   const float* row = logits + (size_t)blockIdx.x * vocab;
   float best = -FLT_MAX;
   int idx = vocab;  // "none yet": any real index is lower
@@ -63,6 +67,10 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 }  // namespace
 
 struct mk_gpu_step {
+  ~mk_gpu_step() {
+    if (h_in) cudaFreeHost(h_in);
+    if (h_out) cudaFreeHost(h_out);
+  }
   mk_model* model = nullptr;
   std::vector<mk_sched*> scheds;
   void* k_pool = nullptr;
@@ -72,12 +80,14 @@ struct mk_gpu_step {
   void* workspace = nullptr;
   size_t ws_bytes = 0;
   cudaStream_t stream = nullptr;
-  // device parts of dev_buf
-  int32_t* d_tok = nullptr;
-  int32_t* d_len = nullptr;
-  int32_t* d_bt = nullptr;
+  // device parts of dev_buf: the inputs as one block (tokens, lengths, block
+  // tables of the step's batch), the outputs (tokens, then the error record)
+  int32_t* d_in = nullptr;
+  int32_t* d_out = nullptr;
   float* d_logits = nullptr;
-  int32_t* d_next = nullptr;
+  // pinned host copies of both: one copy each way per step
+  int32_t* h_in = nullptr;
+  int32_t* h_out = nullptr;
 };
 
 extern "C" {
@@ -85,7 +95,8 @@ extern "C" {
 int mk_argmax_rows(const float* logits, int32_t rows, int32_t vocab, int32_t* next, void* stream) {
   if (!logits || !next || rows < 0 || vocab < 1) return fail(MK_ERR_ARG, "bad argmax arguments");
   if (rows == 0) return MK_OK;
-  argmax_rows<<<rows, kArgmaxThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(logits, vocab, next);
+  argmax_rows<<<rows, kArgmaxThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(logits, vocab, next, nullptr,
+                                                                                   nullptr);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MK_ERR_CUDA, std::string("argmax launch: ") + cudaGetErrorString(e));
   return MK_OK;
@@ -94,7 +105,7 @@ int mk_argmax_rows(const float* logits, int32_t rows, int32_t vocab, int32_t* ne
 size_t mk_gpu_step_dev_bytes(const mk_model* m, int32_t max_batch, int32_t max_pages) {
   if (!m || max_batch < 1 || max_pages < 1) return 0;
   const size_t B = (size_t)max_batch;
-  return 3 * align256(sizeof(int32_t) * B) + align256(sizeof(int32_t) * B * max_pages) +
+  return align256(sizeof(int32_t) * B * (2 + (size_t)max_pages)) + align256(sizeof(int32_t) * (B + 8)) +
          align256(sizeof(float) * B * m->cfg.vocab);
 }
 
@@ -128,15 +139,19 @@ int mk_gpu_step_create(mk_model* m, mk_sched* const* scheds, int32_t n_scheds, v
   g->stream = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* b = static_cast<uint8_t*>(dev_buf);
   const size_t B = (size_t)mb;
-  g->d_tok = reinterpret_cast<int32_t*>(b);
-  b += align256(sizeof(int32_t) * B);
-  g->d_len = reinterpret_cast<int32_t*>(b);
-  b += align256(sizeof(int32_t) * B);
-  g->d_next = reinterpret_cast<int32_t*>(b);
-  b += align256(sizeof(int32_t) * B);
-  g->d_bt = reinterpret_cast<int32_t*>(b);
-  b += align256(sizeof(int32_t) * B * max_pages);
+  const size_t in_words = B * (2 + (size_t)max_pages), out_words = B + 8;
+  g->d_in = reinterpret_cast<int32_t*>(b);
+  b += align256(sizeof(int32_t) * in_words);
+  g->d_out = reinterpret_cast<int32_t*>(b);
+  b += align256(sizeof(int32_t) * out_words);
   g->d_logits = reinterpret_cast<float*>(b);
+  cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&g->h_in), sizeof(int32_t) * in_words, cudaHostAllocDefault);
+  if (e == cudaSuccess)
+    e = cudaHostAlloc(reinterpret_cast<void**>(&g->h_out), sizeof(int32_t) * out_words, cudaHostAllocDefault);
+  if (e != cudaSuccess) {
+    delete g;
+    return fail(MK_ERR_CUDA, std::string("pinned staging buffers: ") + cudaGetErrorString(e));
+  }
   *out = g;
   return MK_OK;
 }
@@ -161,19 +176,30 @@ int mk_gpu_step_run(void* ctx, const int32_t* last_tokens, const int32_t* seq_le
                                       std::to_string(longest));
   cudaStream_t st = g->stream;
   const size_t B = (size_t)batch;
-  cudaError_t e = cudaMemcpyAsync(g->d_tok, last_tokens, sizeof(int32_t) * B, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(g->d_len, seq_lens, sizeof(int32_t) * B, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(g->d_bt, block_tables, sizeof(int32_t) * B * max_pages, cudaMemcpyHostToDevice, st);
+  // the inputs, packed in pinned memory: one copy in
+  std::copy(last_tokens, last_tokens + B, g->h_in);
+  std::copy(seq_lens, seq_lens + B, g->h_in + B);
+  std::copy(block_tables, block_tables + B * max_pages, g->h_in + 2 * B);
+  cudaError_t e = cudaMemcpyAsync(g->d_in, g->h_in, sizeof(int32_t) * B * (2 + (size_t)max_pages),
+                                  cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return fail(MK_ERR_CUDA, std::string("step inputs: ") + cudaGetErrorString(e));
-  int rc = mk_decode_step(g->model, s, g->d_tok, g->d_len, g->d_bt, batch, max_pages, g->k_pool, g->v_pool,
-                          g->num_pages, g->workspace, g->ws_bytes, g->d_logits, st);
+  int rc = mk_decode_step(g->model, s, g->d_in, g->d_in + B, g->d_in + 2 * B, batch, max_pages, g->k_pool,
+                          g->v_pool, g->num_pages, g->workspace, g->ws_bytes, g->d_logits, st);
   if (rc != MK_OK) return rc;
-  rc = mk_argmax_rows(g->d_logits, batch, g->model->cfg.vocab, g->d_next, st);
-  if (rc != MK_OK) return rc;
-  e = cudaMemcpyAsync(next_tokens, g->d_next, sizeof(int32_t) * B, cudaMemcpyDeviceToHost, st);
+  // the greedy tokens and the step's error record side by side: one copy out
+  const uint32_t* rec = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(g->workspace) +
+                                                          s->ws.off("error"));
+  argmax_rows<<<batch, kArgmaxThreads, 0, st>>>(g->d_logits, g->model->cfg.vocab, g->d_out, rec,
+                                                reinterpret_cast<uint32_t*>(g->d_out + B));
+  e = cudaGetLastError();
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(g->h_out, g->d_out, sizeof(int32_t) * (B + 8), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return fail(MK_ERR_CUDA, std::string("step outputs: ") + cudaGetErrorString(e));
-  return mk_check_step(s, g->workspace, st);  // waits for the stream
+  rc = mk::check_record(s, reinterpret_cast<const uint32_t*>(g->h_out + B), g->workspace, st);
+  if (rc != MK_OK) return rc;
+  std::copy(g->h_out, g->h_out + B, next_tokens);
+  return MK_OK;
 }
 
 }  // extern "C"

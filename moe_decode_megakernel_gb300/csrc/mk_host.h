@@ -86,4 +86,8 @@ int fail(int code, const std::string& msg);
 int attn_slices(const mk_sched* s, int seq_len);  // KV slices of a full-attention row
 int query_num_sms();                              // SMs of the current device, -1 without one
 bool is_full_layer(const mk_config& c, int l);
+// mk_check_step on a host copy of the step's error record (8 words at the
+// workspace's "error" offset); the workspace and stream serve the stall
+// diagnosis of a timeout
+int check_record(const mk_sched* s, const uint32_t* rec, const void* workspace, void* stream);
 }  // namespace mk
