@@ -18,7 +18,10 @@ def _rows(inp, extra):
 
 
 @pytest.mark.parametrize("workload,extra", [("batch32_ragged", [7, 19]), ("long_256k", [0]),
-                                            ("batch64_ragged", [33])])
+                                            ("batch64_ragged", [33]),
+                                            # two rows on the lean build; four rows on the any-batch
+                                            # build (every GEMV streamed once per pair of rows)
+                                            ("full_bs2_8k", [1]), ("full_bs4_8k", [2])])
 def test_large_workloads(workload, extra):
     inp = synth.make_inputs(workload)
     g = parity.run_gpu(inp)
