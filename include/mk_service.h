@@ -149,7 +149,10 @@ void mk_gpu_step_free(mk_gpu_step* g);
 /* mk_step_fn for ctx = an mk_gpu_step: copies the inputs to the device,
  * runs mk_decode_step and the argmax on the stream, copies the tokens back
  * and waits; device-side failures come back as mk_check_step's code.
- * MK_ERR_ARG when no schedule covers the batch. */
+ * MK_ERR_ARG when no schedule covers the batch.  The first step of each
+ * (schedule, batch) is captured as a CUDA graph that later steps replay with
+ * one launch; on a stream that cannot be captured (the legacy default
+ * stream) the steps are issued one by one. */
 int mk_gpu_step_run(void* ctx, const int32_t* last_tokens, const int32_t* seq_lens,
                     const int32_t* block_tables, int32_t batch, int32_t max_pages, int32_t* next_tokens);
 

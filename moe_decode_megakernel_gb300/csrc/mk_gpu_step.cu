@@ -68,9 +68,20 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct mk_gpu_step {
   ~mk_gpu_step() {
+    for (auto& gr : graphs) cudaGraphExecDestroy(gr.exec);
     if (h_in) cudaFreeHost(h_in);
     if (h_out) cudaFreeHost(h_out);
   }
+  // one captured step per (schedule, batch): the input copy, mk_decode_step,
+  // the argmax and the output copy replayed by one launch; off for good if a
+  // capture fails (the steps are then issued one by one)
+  struct Graph {
+    mk_sched* s;
+    int32_t batch;
+    cudaGraphExec_t exec;
+  };
+  std::vector<Graph> graphs;
+  bool graphs_off = false;
   mk_model* model = nullptr;
   std::vector<mk_sched*> scheds;
   void* k_pool = nullptr;
@@ -89,6 +100,30 @@ struct mk_gpu_step {
   int32_t* h_in = nullptr;
   int32_t* h_out = nullptr;
 };
+
+namespace {
+// One step on the stream: the packed inputs in (one copy), mk_decode_step,
+// the greedy tokens and the step's error record side by side, one copy out.
+int enqueue_step(mk_gpu_step* g, mk_sched* s, int32_t batch, int32_t max_pages) {
+  cudaStream_t st = g->stream;
+  const size_t B = (size_t)batch;
+  cudaError_t e = cudaMemcpyAsync(g->d_in, g->h_in, sizeof(int32_t) * B * (2 + (size_t)max_pages),
+                                  cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return fail(MK_ERR_CUDA, std::string("step inputs: ") + cudaGetErrorString(e));
+  const int rc = mk_decode_step(g->model, s, g->d_in, g->d_in + B, g->d_in + 2 * B, batch, max_pages, g->k_pool,
+                                g->v_pool, g->num_pages, g->workspace, g->ws_bytes, g->d_logits, st);
+  if (rc != MK_OK) return rc;
+  const uint32_t* rec = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(g->workspace) +
+                                                          s->ws.off("error"));
+  argmax_rows<<<batch, kArgmaxThreads, 0, st>>>(g->d_logits, g->model->cfg.vocab, g->d_out, rec,
+                                                reinterpret_cast<uint32_t*>(g->d_out + B));
+  e = cudaGetLastError();
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(g->h_out, g->d_out, sizeof(int32_t) * (B + 8), cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return fail(MK_ERR_CUDA, std::string("step outputs: ") + cudaGetErrorString(e));
+  return MK_OK;
+}
+}  // namespace
 
 extern "C" {
 
@@ -176,27 +211,38 @@ int mk_gpu_step_run(void* ctx, const int32_t* last_tokens, const int32_t* seq_le
                                       std::to_string(longest));
   cudaStream_t st = g->stream;
   const size_t B = (size_t)batch;
-  // the inputs, packed in pinned memory: one copy in
+  // the inputs, packed in pinned memory (read when the copy runs)
   std::copy(last_tokens, last_tokens + B, g->h_in);
   std::copy(seq_lens, seq_lens + B, g->h_in + B);
   std::copy(block_tables, block_tables + B * max_pages, g->h_in + 2 * B);
-  cudaError_t e = cudaMemcpyAsync(g->d_in, g->h_in, sizeof(int32_t) * B * (2 + (size_t)max_pages),
-                                  cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) return fail(MK_ERR_CUDA, std::string("step inputs: ") + cudaGetErrorString(e));
-  int rc = mk_decode_step(g->model, s, g->d_in, g->d_in + B, g->d_in + 2 * B, batch, max_pages, g->k_pool,
-                          g->v_pool, g->num_pages, g->workspace, g->ws_bytes, g->d_logits, st);
-  if (rc != MK_OK) return rc;
-  // the greedy tokens and the step's error record side by side: one copy out
-  const uint32_t* rec = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(g->workspace) +
-                                                          s->ws.off("error"));
-  argmax_rows<<<batch, kArgmaxThreads, 0, st>>>(g->d_logits, g->model->cfg.vocab, g->d_out, rec,
-                                                reinterpret_cast<uint32_t*>(g->d_out + B));
-  e = cudaGetLastError();
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(g->h_out, g->d_out, sizeof(int32_t) * (B + 8), cudaMemcpyDeviceToHost, st);
+  cudaGraphExec_t exec = nullptr;
+  for (const auto& gr : g->graphs)
+    if (gr.s == s && gr.batch == batch) exec = gr.exec;
+  if (!exec && !g->graphs_off) {
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
+    int rc = e == cudaSuccess ? enqueue_step(g, s, batch, max_pages) : MK_ERR_CUDA;
+    if (e == cudaSuccess) e = cudaStreamEndCapture(st, &graph);
+    if (rc == MK_OK && e == cudaSuccess) e = cudaGraphInstantiate(&exec, graph, 0);
+    if (graph) cudaGraphDestroy(graph);
+    if (rc != MK_OK || e != cudaSuccess) {
+      g->graphs_off = true;
+      exec = nullptr;
+      cudaGetLastError();  // the failed capture is not the step's error
+    } else {
+      g->graphs.push_back({s, batch, exec});
+    }
+  }
+  cudaError_t e = cudaSuccess;
+  if (exec) {
+    e = cudaGraphLaunch(exec, st);
+  } else {
+    const int rc = enqueue_step(g, s, batch, max_pages);
+    if (rc != MK_OK) return rc;
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return fail(MK_ERR_CUDA, std::string("step outputs: ") + cudaGetErrorString(e));
-  rc = mk::check_record(s, reinterpret_cast<const uint32_t*>(g->h_out + B), g->workspace, st);
+  const int rc = mk::check_record(s, reinterpret_cast<const uint32_t*>(g->h_out + B), g->workspace, st);
   if (rc != MK_OK) return rc;
   std::copy(g->h_out, g->h_out + B, next_tokens);
   return MK_OK;

@@ -73,7 +73,8 @@ def argmax_rows(logits, next_tokens, stream: int = 0) -> None:
 
 class GpuStep:
     """mk_gpu_step on torch-owned device memory: the schedules (uploaded
-    here), one workspace for all of them and the step's input/output buffer."""
+    here), one workspace for all of them, the step's input/output buffer and
+    a stream of its own."""
 
     def __init__(self, model: Model, scheds: list[Sched], k_pool, v_pool, max_pages: int, device="cuda"):
         import torch
@@ -90,7 +91,11 @@ class GpuStep:
         self.k_pool, self.v_pool = k_pool, v_pool
         handles = (ctypes.c_void_p * len(scheds))(*[s.handle.value for s in scheds])
         h = ctypes.c_void_p()
-        st = torch.cuda.current_stream().cuda_stream
+        # a stream of its own (steps are captured as CUDA graphs; the legacy
+        # default stream cannot be), after the work that made the weights and pools
+        torch.cuda.current_stream(device).synchronize()
+        self.stream = torch.cuda.Stream(device)
+        st = self.stream.cuda_stream
         _check(_lib().mk_gpu_step_create(model.handle, handles, len(scheds), k_pool.data_ptr(),
                                          v_pool.data_ptr(), k_pool.shape[1], max_pages, ws_ptr, ws, buf_ptr,
                                          nbytes, st, ctypes.byref(h)))
