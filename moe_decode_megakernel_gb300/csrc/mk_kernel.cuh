@@ -176,9 +176,6 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
-}
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -256,29 +253,6 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
   hi = (uint32_t)ah | ((uint32_t)bh << 16);
   lo = (uint32_t)f_bf16(a - bf16_f(ah)) | ((uint32_t)f_bf16(b - bf16_f(bh)) << 16);
 }
-__device__ __forceinline__ float dot8(uint4 w, uint4 x, float acc) {
-  acc = fmaf(bf16_lo(w.x), bf16_lo(x.x), acc);
-  acc = fmaf(bf16_hi(w.x), bf16_hi(x.x), acc);
-  acc = fmaf(bf16_lo(w.y), bf16_lo(x.y), acc);
-  acc = fmaf(bf16_hi(w.y), bf16_hi(x.y), acc);
-  acc = fmaf(bf16_lo(w.z), bf16_lo(x.z), acc);
-  acc = fmaf(bf16_hi(w.z), bf16_hi(x.z), acc);
-  acc = fmaf(bf16_lo(w.w), bf16_lo(x.w), acc);
-  acc = fmaf(bf16_hi(w.w), bf16_hi(x.w), acc);
-  return acc;
-}
-// 8 BF16 weights against 8 fp32 activations
-__device__ __forceinline__ float dot8f(uint4 w, float4 a, float4 b, float acc) {
-  acc = fmaf(bf16_lo(w.x), a.x, acc);
-  acc = fmaf(bf16_hi(w.x), a.y, acc);
-  acc = fmaf(bf16_lo(w.y), a.z, acc);
-  acc = fmaf(bf16_hi(w.y), a.w, acc);
-  acc = fmaf(bf16_lo(w.z), b.x, acc);
-  acc = fmaf(bf16_hi(w.z), b.y, acc);
-  acc = fmaf(bf16_lo(w.w), b.z, acc);
-  acc = fmaf(bf16_hi(w.w), b.w, acc);
-  return acc;
-}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(FULL, v, m);
@@ -289,35 +263,7 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, m));
   return v;
 }
-// Sums N per-lane values over the warp and leaves lane l holding the total of
-// value l / (32 / N) ("transpose reduction": N-1 + log2(32/N) shuffles instead
-// of 5N).  Each halving step keeps the half of the values selected by one lane
-// bit and adds the partner lane's copy of it.
-__device__ __forceinline__ void rs_halve(float* v, int n, int m, int lane) {
-  const bool up = (lane & m) != 0;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    if (i < n / 2) {
-      const float send = up ? v[i] : v[i + n / 2];
-      const float keep = up ? v[i + n / 2] : v[i];
-      v[i] = keep + __shfl_xor_sync(FULL, send, m);
-    }
-  }
-}
 
-template <int N>
-__device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
-  static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "power of two");
-  if constexpr (N >= 32) rs_halve(v, 32, 16, lane);
-  if constexpr (N >= 16) rs_halve(v, 16, N >= 32 ? 8 : 16, lane);
-  if constexpr (N >= 8) rs_halve(v, 8, 16 * 8 / N, lane);
-  if constexpr (N >= 4) rs_halve(v, 4, 16 * 4 / N, lane);
-  if constexpr (N >= 2) rs_halve(v, 2, 16 * 2 / N, lane);
-  float r = v[0];
-#pragma unroll
-  for (int m = 16 / N; m >= 1; m >>= 1) r += __shfl_xor_sync(FULL, r, m);
-  return r;
-}
 
 // ----------------------------------------------------- shared memory map
 struct Hdr {
@@ -1724,7 +1670,7 @@ struct Consumer {
   // the weight rows, two pairs at a time against the same activation loads,
   // and finishes each pair's epilogue itself (the RoPE pair for QKV, gate and
   // up rows for the MoE up/gate), so a stage needs no block-wide barrier.
-  // With one activation row the row lives in registers for the whole item.
+  // One activation row has its own instantiation, without the second row's work.
   template <int K>
   __device__ __forceinline__ void gemv_item_teams(const int32_t* w, int SR, int total_rows, int ntok) {
     // one activation row is the decode case: its own instantiation, without
@@ -1733,10 +1679,6 @@ struct Consumer {
     else gemv_item_teams_tb<K, kTB>(w, SR, total_rows, ntok);
   }
   static constexpr int kTeams = 4, kTeamWarps = kConsumerWarps / kTeams;
-#ifndef MK_XREGS
-#define MK_XREGS 0
-#endif
-  static constexpr bool kXRegs = MK_XREGS;
   static_assert(kConsumerWarps % kTeams == 0 && F_A0 + 8 + 2 * kTB <= F_TASK, "teams; down-tile row fields");
   template <int K, int TB>
   __device__ __forceinline__ void gemv_item_teams_tb(const int32_t* w, int SR, int total_rows, int ntok) {
@@ -1767,16 +1709,6 @@ struct Consumer {
     // x row t as [half][chunk][4]: lane's chunk c = lane + 32 j holds elements
     // 8c .. 8c+3 in half 0 and 8c+4 .. 8c+7 in half 1
     const uint32_t xs_a = smem_u32(sm.xs) + (uint32_t)lane * 16u;
-    constexpr bool XR = TB == 1 && kXRegs;
-    uint4 xr[XR ? CPL : 1][2];
-    if (XR) {
-#pragma unroll
-      for (int j = 0; j < CPL; ++j)
-        if (C % 32 == 0 || lane + 32 * j < C) {
-          xr[j][0] = lds128(xs_a + (uint32_t)((32 * j) * 16));
-          xr[j][1] = lds128(xs_a + (uint32_t)((C + 32 * j) * 16));
-        }
-    }
     for (int s = team; s < nst; s += kTeams) {
       const uint32_t gs = c.st + (uint32_t)s;
       const int slot = gs % kStages;
@@ -1815,8 +1747,8 @@ struct Consumer {
 #pragma unroll
               for (int t = 0; t < TB; ++t)
                 if (TB == 1 || t < tb) {
-                  const uint4 xa = XR ? xr[XR ? j : 0][0] : lds128(xs_a + (uint32_t)((t * 2 * C + 32 * j) * 16));
-                  const uint4 xb = XR ? xr[XR ? j : 0][1] : lds128(xs_a + (uint32_t)((t * 2 * C + C + 32 * j) * 16));
+                  const uint4 xa = lds128(xs_a + (uint32_t)((t * 2 * C + 32 * j) * 16));
+                  const uint4 xb = lds128(xs_a + (uint32_t)((t * 2 * C + C + 32 * j) * 16));
 #pragma unroll
                   for (int q = 0; q < 4; ++q) dot8_bf16(u[q], xa, xb, acc[q][t][0], acc[q][t][1]);
                 }
