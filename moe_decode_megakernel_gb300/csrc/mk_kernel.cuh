@@ -1738,7 +1738,9 @@ struct Consumer {
           for (int q = 0; q < 4; ++q)
 #pragma unroll
             for (int t = 0; t < TB; ++t) acc[q][t][0] = acc[q][t][1] = 0.f;
-#pragma unroll
+          // unrolled by 4, not fully: the smaller loop body fetches better
+          // (instruction fetch is one of this kernel's top stalls)
+#pragma unroll 4
           for (int j = 0; j < CPL; ++j) {
             if (C % 32 == 0 || lane + 32 * j < C) {
               uint4 u[4];
