@@ -93,9 +93,15 @@ typedef struct {
 typedef struct mk_model mk_model;
 typedef struct mk_sched mk_sched;
 
-/* Validates the shape against the compiled kernels and records the weight
- * pointers (the [out][in] layout is already tile-contiguous for the row
- * tiles the kernel streams, so nothing is repacked).  Host only. */
+/* Loads a model: validates the shape against the compiled kernels and
+ * records the weight pointers ("Cohere: a decode megakernel for North Mini
+ * Code", section "One ABI for every operation": every operation reads its
+ * weights through pointers fixed before the step, so the kernel takes the
+ * model as plain device addresses).  The [out][in] layout is already
+ * tile-contiguous for the row tiles the kernel streams, so nothing is
+ * repacked.  Host only: no device call, no copy.  MK_ERR_UNSUPPORTED for a
+ * shape no kernel was compiled for; MK_ERR_ARG for a null or misaligned
+ * pointer or an invalid field.  *out is freed with mk_free_model. */
 int mk_load_model(const mk_config* cfg, const mk_weights* w, mk_model** out);
 void mk_free_model(mk_model* m);
 
@@ -156,6 +162,12 @@ typedef struct {
                                num_sms; 1: greedy, each layer's tasks in order go to the SM
                                where a cost model (typical ready and busy time per op, a
                                claimer's static unit count) says they finish first */
+  int32_t trace_queue;      /* 1: keep every layer's MoE work queue in the workspace
+                               ("queue_trace", see mk_workspace_offset) */
+  int32_t l2_lookahead;     /* N > 0: when an SM starts a task it asks L2 to prefetch the
+                               step-independent inputs (weight rows, the KV pages of static
+                               attention slices) of its next N tasks, so they stream from HBM
+                               while dependency waits hold the stage ring; 0: off */
 } mk_sched_opts;
 
 /* Fills opts with the defaults (all zero except fuse_* = 1 and moe_static = 1). */
@@ -196,6 +208,20 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens,
                    int32_t max_pages, void* k_pool, void* v_pool, int64_t num_pages,
                    void* workspace, size_t workspace_bytes, float* logits, void* stream);
 
+/* Host-side check of a step's inputs before it is launched, for a caller
+ * that holds host copies of them (the decode service does).  mk_decode_step
+ * takes its inputs as device arrays and checks their values on the device
+ * (reported by mk_check_step), so that a step never waits for the host; this
+ * call refuses the same inputs before launch instead.  Checks: batch in [1,
+ * max_batch]; every seq_len in [1, max_ctx]; every page id the step reads
+ * (logical pages 0 .. (seq_len - 1) / page_size of each row) in [0,
+ * num_pages) and within max_pages columns; with last_tokens (may be NULL)
+ * every token in [0, vocab).  Host pointers: seq_lens [batch], block_tables
+ * [batch][max_pages], last_tokens [batch].  Returns MK_OK or MK_ERR_ARG
+ * naming the first offending row (mk_last_error()). */
+int mk_check_inputs(const mk_sched* s, const int32_t* last_tokens, const int32_t* seq_lens,
+                    const int32_t* block_tables, int32_t batch, int32_t max_pages, int64_t num_pages);
+
 /* mk_decode_step with a built-in workspace, for callers that cannot allocate
  * device memory: their device memory belongs to another allocator (a host
  * framework's caching allocator, a runtime whose budget is fixed at start-up)
@@ -209,7 +235,8 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens,
  * allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress), with that device current; make that first call
- * before any stream capture.  All calls share the array and it keeps the
+ * before any stream capture.  A lookup that fails is not remembered: the
+ * next call tries again.  All calls share the array and it keeps the
  * last call's contents (each step zeroes its own counters first): calls
  * whose executions overlap on the GPU, on any streams, race on it.
  * Device-side failures (watchdog, page id out of range) are recorded in that
@@ -241,6 +268,11 @@ const char* mk_last_error(void);
  * rows, 0}; the MoE queues are (active expert, tile) in that order),
  * "moe_queue_len" int32 [2] (active experts, routed rows),
  * "perm" int32 [B*k] (last layer), "hidden_trace" fp32 [L+1][B][H],
+ * with opts.trace_queue "queue_trace" int32 [L][R], R = (5E + 1 + B*k + 2)
+ * rounded up to a multiple of 4, each layer's record being the active-expert
+ * list [E][4] ({expert, first expert-ordered row, rows, 0}; entries past the
+ * active count are stale), the row offsets [E+1], the expert-ordered rows
+ * [B*k] (entry i = b*k + j) and {active experts, routed rows},
  * "error" uint32 [8], "barriers" uint32, with opts.trace "trace" uint64
  * [num_sms][cap][4] (popped, waits done, end in ns of %globaltimer; op |
  * layer << 8 | task << 16 | first argument << 40; unused records zero) and

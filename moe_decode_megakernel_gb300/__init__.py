@@ -53,7 +53,7 @@ class MkSchedOpts(ctypes.Structure):
                                               "fuse_moe_combine", "explicit_gather",
                                               "trace_hidden", "watchdog_ms", "trace", "moe_queue", "moe_static",
                                               "fuse_routing", "fuse_norm_qkv", "attn_static", "moe_balance",
-                                              "combine_per_head", "placement")]
+                                              "combine_per_head", "placement", "trace_queue", "l2_lookahead")]
 
 
 _lib = None
@@ -82,6 +82,7 @@ def lib():
             "mk_decode_step": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, vp, vp, i64, vp, sz, vp,
                                               vp]),
             "mk_check_step": (ctypes.c_int, [vp, vp, vp]),
+            "mk_check_inputs": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, i64]),
             "mk_decode_step_static_ws": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, vp, vp, i64, vp,
                                                         vp]),
             "mk_last_error": (ctypes.c_char_p, []),
@@ -201,6 +202,16 @@ class Sched:
 
     def validate(self) -> None:
         _check(lib().mk_sched_validate(self.handle))
+
+    def check_inputs(self, tokens, seq_lens, block_tables, num_pages: int) -> None:
+        """mk_check_inputs on host arrays (tokens may be None): raises MkError
+        (MK_ERR_ARG) for inputs the step would refuse, before any launch."""
+        import numpy as np
+        sl, slp = _i32p(seq_lens)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        tp = _i32p(tokens)[1] if tokens is not None else None
+        _check(lib().mk_check_inputs(self.handle, tp, slp, bt.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                     sl.size, bt.shape[1], num_pages))
 
     def simulate(self, seq_lens, routing=None, seed: int = 0) -> None:
         sl, slp = _i32p(seq_lens)

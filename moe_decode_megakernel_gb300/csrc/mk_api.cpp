@@ -258,6 +258,35 @@ int mk_sched_upload(mk_sched* s, void* dev, size_t bytes, void* stream) {
   return MK_OK;
 }
 
+int mk_check_inputs(const mk_sched* s, const int32_t* last_tokens, const int32_t* seq_lens,
+                    const int32_t* block_tables, int32_t batch, int32_t max_pages, int64_t num_pages) {
+  if (!s || !seq_lens || !block_tables) return fail(MK_ERR_ARG, "null argument");
+  if (batch < 1 || batch > s->max_batch)
+    return fail(MK_ERR_ARG, "batch " + std::to_string(batch) + " outside [1, " + std::to_string(s->max_batch) + "]");
+  if (max_pages < 1 || num_pages < 1) return fail(MK_ERR_ARG, "max_pages and num_pages must be positive");
+  const int P = s->dims.P;
+  for (int32_t b = 0; b < batch; ++b) {
+    const int32_t len = seq_lens[b];
+    if (len < 1 || len > s->max_ctx)
+      return fail(MK_ERR_ARG, "row " + std::to_string(b) + ": seq_len " + std::to_string(len) + " outside [1, " +
+                                  std::to_string(s->max_ctx) + "] (the schedule's max_ctx)");
+    const int32_t pages = (len + P - 1) / P;
+    if (pages > max_pages)
+      return fail(MK_ERR_ARG, "row " + std::to_string(b) + ": seq_len " + std::to_string(len) + " needs " +
+                                  std::to_string(pages) + " pages, the block table has " + std::to_string(max_pages));
+    for (int32_t j = 0; j < pages; ++j) {
+      const int32_t pg = block_tables[(size_t)b * max_pages + j];
+      if (pg < 0 || pg >= num_pages)
+        return fail(MK_ERR_ARG, "row " + std::to_string(b) + ": page " + std::to_string(pg) + " at logical page " +
+                                    std::to_string(j) + " outside [0, " + std::to_string(num_pages) + ")");
+    }
+    if (last_tokens && (last_tokens[b] < 0 || last_tokens[b] >= s->cfg.vocab))
+      return fail(MK_ERR_ARG, "row " + std::to_string(b) + ": token " + std::to_string(last_tokens[b]) +
+                                  " outside [0, " + std::to_string(s->cfg.vocab) + ")");
+  }
+  return MK_OK;
+}
+
 int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const int32_t* seq_lens,
                    const int32_t* block_tables, int32_t batch, int32_t max_pages, void* k_pool,
                    void* v_pool, int64_t num_pages, void* workspace, size_t workspace_bytes,
@@ -345,6 +374,7 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   p.y = reinterpret_cast<float*>(at("y"));
   p.moe_out = reinterpret_cast<float*>(at("moe_out"));
   p.htrace = reinterpret_cast<float*>(at("hidden_trace"));
+  p.qtrace = reinterpret_cast<int32_t*>(at("queue_trace"));
   p.trace = reinterpret_cast<uint64_t*>(at("trace"));
   p.trace_cap = s->trace_cap;
   p.stats = reinterpret_cast<uint64_t*>(at("stats"));
@@ -352,6 +382,7 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   p.n_static = s->n_static;
   p.max_slots = s->max_slots;
   p.explicit_gather = s->opts.explicit_gather;
+  p.l2_lookahead = s->opts.l2_lookahead;
   p.watchdog_ns = s->watchdog_ns;
   (void)D;
 

@@ -209,6 +209,9 @@ int mk_gpu_step_run(void* ctx, const int32_t* last_tokens, const int32_t* seq_le
     }
   if (!s) return fail(MK_ERR_ARG, "no schedule covers batch " + std::to_string(batch) + " at context " +
                                       std::to_string(longest));
+  // the host holds the inputs: refuse bad ones before anything is launched
+  const int chk = mk_check_inputs(s, last_tokens, seq_lens, block_tables, batch, max_pages, g->num_pages);
+  if (chk != MK_OK) return chk;
   cudaStream_t st = g->stream;
   const size_t B = (size_t)batch;
   // the inputs, packed in pinned memory (read when the copy runs)

@@ -204,6 +204,13 @@ constexpr MoePlan moe_plan4(ShapeDims s) {
   return p;
 }
 
+// One layer's record of the MoE queue trace (int32): the active-expert list
+// [E][4], the row offsets [E + 1], the expert-ordered rows [n_routed_max],
+// {active experts, routed rows}; padded to a multiple of 4 (16 bytes).
+MK_HOST_DEVICE constexpr int queue_trace_stride(int E, int n_routed_max) {
+  return (4 * E + (E + 1) + n_routed_max + 2 + 3) / 4 * 4;
+}
+
 // ------------------------------------------------------ kernel parameters
 struct Params {
   // the KV pools as 2-D tensors [L*pages*n_kv*P][d] for TMA tiles of
@@ -273,6 +280,7 @@ struct Params {
   float* y;             // [MB K][H] expert outputs
   float* moe_out;       // [MB][H]
   float* htrace;        // [L + 1][MB][H] or null
+  int32_t* qtrace;      // [L][queue_trace_stride(E, MB K)] or null
 
   uint64_t* trace;      // [num_sms][trace_cap][2] per work item, or null
   int trace_cap;
@@ -282,6 +290,7 @@ struct Params {
   int n_static;         // static slices per (row, group) of a sliding layer
   int max_slots;
   int explicit_gather;
+  int l2_lookahead;     // tasks ahead whose step-independent inputs are prefetched into L2
   int64_t watchdog_ns;
 };
 

@@ -2,7 +2,7 @@
 //
 // One CTA per SM, resident for the whole decode step ("Cohere: a decode
 // megakernel for North Mini Code", section "What is a Megakernel?").  The
-// CTA has three roles, fixed per warp:
+// CTA has four roles, fixed per warp:
 //   warp 0      controller: copies the SM's task descriptors from global
 //               memory into a small shared-memory ring ("The task
 //               descriptor": the controller stays ahead of the workers);
@@ -14,10 +14,15 @@
 //               boundaries without waiting on any cross-SM barrier ("3.
 //               Weight prefetch"); only the MoE claimers wait, for the
 //               routing that decides which expert rows to stream;
-//   warps 2-9   consumers: wait on the task's cross-SM counters, compute
-//               from the staged rows, write the outputs and signal.
-// There is no storer warp: decode outputs are a few hundred bytes per task,
-// so consumers store them directly and publish them with a release add.
+//   warp 2      storer: publishes finished work items -- once the
+//               consumers have arrived on an item's done barrier it adds 1,
+//               with release semantics, to each counter the item signals
+//               ("The threadblock shape": the storer signals the output
+//               barriers), so no consumer waits on a release;
+//   warps 3-10  consumers: wait on the item's cross-SM counters, compute
+//               from the staged rows and write the outputs themselves
+//               (decode outputs are a few hundred bytes per task, so they
+//               need no store pipeline).
 //
 // Cross-SM synchronisation is a counter per dependency in global memory,
 // zeroed before each step ("Barriers"): a producer task adds 1 with release
@@ -90,6 +95,10 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(b)), "l"(policy)
       : "memory");
+}
+// Asks L2 to fetch [src, src + bytes) (16-byte aligned, a multiple of 16 bytes); no completion.
+__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
@@ -1006,13 +1015,78 @@ struct Producer {
     return push(it);
   }
 
+  // ---- far-ahead L2 prefetch ("3. Weight prefetch", a layer ahead) ----
+  // The step-independent inputs of a task that is still far down this SM's
+  // list: dense weight rows (QKV, router, LM head), the O-proj rows' columns
+  // of the task's KV group, and the KV pages of static attention slices.  The
+  // stage ring holds only the next few stages, and its stages wait behind the
+  // tasks in front of them; an L2 prefetch lets these bytes stream from HBM
+  // while the SM stalls on dependencies, and the ring's later copies hit L2.
+  // MoE tiles are not prefetched: their experts are known only after routing.
+  __device__ __noinline__ void prefetch_task(const int32_t* dg) {
+    const int op = __ldg(dg + F_OP), l = __ldg(dg + F_LAYER);
+    if (op == OP_QKV_PROJ || op == OP_ROUTER_GEMM || op == OP_LM_HEAD) {
+      const uint16_t* base = op == OP_QKV_PROJ      ? p.wqkv + (int64_t)l * S::QKV * S::H
+                             : op == OP_ROUTER_GEMM ? p.wr + (int64_t)l * S::E * S::H
+                                                    : p.wlm;
+      if (!base) return;
+      const char* src = reinterpret_cast<const char*>(base + (int64_t)__ldg(dg + F_A0) * S::H);
+      const int64_t bytes = (int64_t)__ldg(dg + F_A0 + 1) * S::H * 2;
+      for (int64_t o = 0; o < bytes; o += 65536) l2_prefetch(src + o, (uint32_t)(bytes - o < 65536 ? bytes - o : 65536));
+    } else if (op == OP_O_PROJ) {
+      const uint16_t* base = p.wo + (int64_t)l * S::H * S::NQ * S::D + (int64_t)__ldg(dg + F_A0 + 2) * S::G * S::D;
+      const int row0 = __ldg(dg + F_A0), rows = __ldg(dg + F_A0 + 1);
+      for (int r = 0; r < rows; ++r) l2_prefetch(base + (int64_t)(row0 + r) * S::NQ * S::D, S::G * S::D * 2);
+    } else if (op == OP_ATTN_DECODE) {
+      const int b = __ldg(dg + F_A0), g = __ldg(dg + F_A0 + 1), j = __ldg(dg + F_A0 + 2);
+      if (b >= p.B) return;
+      const int s = __ldg(p.seq_lens + b);
+      const bool full = p.window == 0 || (l + 1) % p.full_period == 0;
+      const int lo = full ? 0 : max(0, s - p.window);
+      const int jj = lo / p.split_len + j;
+      prefetch_pages(l, b, g, max(lo, jj * p.split_len), min(s, (jj + 1) * p.split_len));
+    } else if (op == OP_ATTN_DRAIN && __ldg(dg + F_A0 + 4) >= 0) {  // static claims: entries ci, ci + n, ...
+      const uint32_t n_cl = (uint32_t)__ldg(dg + F_A0 + 5);
+      for (uint32_t i = (uint32_t)__ldg(dg + F_A0 + 4);; i += n_cl) {
+        uint32_t acc = 0;
+        int b = 0, n = 0, s = 0;
+        for (; b < p.B; ++b) {
+          s = __ldg(p.seq_lens + b);
+          n = slices_of(p, s) * S::NKV;
+          if (i < acc + (uint32_t)n) break;
+          acc += (uint32_t)n;
+        }
+        if (b >= p.B || n_cl == 0) break;
+        const int r = (int)(i - acc), per = n / S::NKV;
+        const int t0 = (r - (r / per) * per) * p.split_len;
+        prefetch_pages(l, b, r / per, t0, min(s, t0 + p.split_len));
+      }
+    }
+  }
+  // K and V pages of positions [t0, t1) of row b, KV group g, layer l.
+  __device__ __forceinline__ void prefetch_pages(int l, int b, int g, int t0, int t1) {
+    if (t1 <= t0 || t0 < 0) return;
+    constexpr uint32_t kPage = S::P * S::D * 2;
+    for (int lp = t0 / S::P; lp <= (t1 - 1) / S::P && lp < p.max_pages; ++lp) {
+      const int page = __ldg(p.block_tables + (int64_t)b * p.max_pages + lp);
+      if (page < 0 || page >= p.num_pages) return;  // the ring's copy reports it
+      const int64_t off = (((int64_t)l * p.num_pages + page) * S::NKV + g) * S::P * S::D;
+      l2_prefetch(p.kpool + off, kPage);
+      l2_prefetch(p.vpool + off, kPage);
+    }
+  }
+
   __device__ __forceinline__ void run() {
     if ((threadIdx.x & 31) != 0) return;
     stream_policy = l2_evict_first_policy();
     const int n = p.sched[2 * c.sm + 1];
+    const int32_t* list = p.sched + p.sched[2 * c.sm];
+    int pf_next = 1;  // the next task whose inputs are prefetched into L2
     Hdr* H = c.hdr;
     bool ok = true;
     for (int i = 0; i < n && ok; ++i) {
+      if (p.l2_lookahead > 0)
+        for (const int hi = min(n - 1, i + p.l2_lookahead); pf_next <= hi; ++pf_next) prefetch_task(list + 32 * pf_next);
       const int slot = i % kDescRing;
       if (!mbar_wait(p, c, &H->dfull[slot], (i / kDescRing) & 1)) {
         ok = false;
@@ -2360,6 +2434,7 @@ struct Consumer {
     const float v0 = key_value(sm.tk_key[0][0]);
     const float ej = lane < K ? expf(key_value(sm.tk_key[0][lane < K ? lane : 0]) - v0) : 0.f;
     const float z = warp_sum(ej);
+    int32_t* qt = queue_trace(l);
     if (lane < K) {
       p.topk_ids[(int64_t)l * p.MB * K + lane] = my;
       p.topk_w[(int64_t)l * p.MB * K + lane] = ej / z;
@@ -2367,8 +2442,16 @@ struct Consumer {
       p.perm[rank] = lane;
       p.inv[lane] = rank;
       sm.ids[lane] = my;
+      if (qt) {
+        reinterpret_cast<int4*>(qt)[rank] = make_int4(my, rank, 1, 0);
+        qt[5 * E + 1 + rank] = lane;
+      }
     }
     if (lane == 0) *reinterpret_cast<int2*>(p.qlen) = make_int2(K, K);  // active experts, routed rows
+    if (lane == 0 && qt) {
+      qt[5 * E + 1 + p.MB * K] = K;
+      qt[5 * E + 1 + p.MB * K + 1] = K;
+    }
     __syncwarp();
     if (lane == 0 && sig) red_release_add(sig, 1u);
     // per-expert counts and offsets (outputs; nothing downstream waits on them)
@@ -2385,9 +2468,16 @@ struct Consumer {
       if (e < E) {
         p.ecount[(int64_t)l * E + e] = chosen;
         p.eoff[e] = below;
+        if (qt) qt[4 * E + e] = below;
       }
     }
     if (lane == 0) p.eoff[E] = K;
+    if (lane == 0 && qt) qt[5 * E] = K;
+  }
+
+  // This layer's record of the MoE queue trace, or null (see queue_trace_stride).
+  __device__ __forceinline__ int32_t* queue_trace(int l) const {
+    return p.qtrace ? p.qtrace + (int64_t)l * queue_trace_stride(S::E, p.MB * S::K) : nullptr;
   }
 
   // Per-expert counts and offsets, the expert-ordered row list (rows of an
@@ -2441,6 +2531,7 @@ struct Consumer {
       }
     }
     int ro = ri - rs, ao = ai - as;
+    int32_t* qt = queue_trace(l);
 #pragma unroll
     for (int k = 0; k < PL; ++k) {
       const int e = lane * PL + k;
@@ -2450,6 +2541,10 @@ struct Consumer {
         p.ecount[(int64_t)l * E + e] = cnt[k];
         p.eoff[e] = ro;
         if (a[k]) reinterpret_cast<int4*>(p.act)[ao] = make_int4(e, ro, cnt[k], 0);
+        if (qt) {
+          qt[4 * E + e] = ro;
+          if (a[k]) reinterpret_cast<int4*>(qt)[ao] = make_int4(e, ro, cnt[k], 0);
+        }
       }
       ro += cnt[k];
       ao += a[k];
@@ -2458,6 +2553,11 @@ struct Consumer {
       p.eoff[E] = ri;
       p.qlen[0] = ai;  // active experts
       p.qlen[1] = ri;  // routed rows
+      if (qt) {
+        qt[5 * E] = ri;
+        qt[5 * E + 1 + p.MB * K] = ai;
+        qt[5 * E + 1 + p.MB * K + 1] = ri;
+      }
     }
     __syncwarp();
     for (int i = lane; i < n; i += 32) {
@@ -2468,6 +2568,7 @@ struct Consumer {
       const int row = sm.off[e] + rank;
       p.perm[row] = i;
       p.inv[i] = row;
+      if (qt) qt[5 * E + 1 + row] = i;
     }
   }
 

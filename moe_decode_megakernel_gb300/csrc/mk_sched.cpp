@@ -682,6 +682,7 @@ static void layout_workspace(mk_sched* s) {
   w.add("y", sizeof(float) * (size_t)MB * D.K * D.H);
   w.add("moe_out", sizeof(float) * (size_t)MB * D.H);
   if (s->opts.trace_hidden) w.add("hidden_trace", sizeof(float) * (size_t)(L + 1) * MB * D.H);
+  if (s->opts.trace_queue) w.add("queue_trace", sizeof(int32_t) * (size_t)L * queue_trace_stride(D.E, MB * D.K));
   if (s->opts.trace) {
     size_t most = 0;
     for (const auto& l : s->per_sm) most = std::max(most, l.size());
@@ -1031,6 +1032,10 @@ int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const 
   if (s->opts.placement < 0 || s->opts.placement > 1) {
     delete s;
     return fail(MK_ERR_ARG, "unknown placement");
+  }
+  if (s->opts.l2_lookahead < 0 || s->opts.l2_lookahead > 64) {
+    delete s;
+    return fail(MK_ERR_ARG, "l2_lookahead must be in [0, 64]");
   }
   s->watchdog_ns = (int64_t)(s->opts.watchdog_ms > 0 ? s->opts.watchdog_ms : 2000) * 1000000;
   int rc = build(s);

@@ -26,17 +26,26 @@ constexpr size_t kStaticWorkspaceBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_ws_ptr[kMaxDevices];
-cudaError_t g_ws_err[kMaxDevices];
-std::once_flag g_ws_once[kMaxDevices];
+std::mutex g_ws_mutex[kMaxDevices];
+void* g_ws_ptr[kMaxDevices];  // the array's device address on each device, once found
 
-// Run once per device, with that device current: the host-side name of the
-// array is only a stand-in, the kernel needs its device address.
-void resolve_workspace(int dev) {
-  void* ptr = nullptr;
-  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_workspace);
-  g_ws_err[dev] = e;
-  g_ws_ptr[dev] = e == cudaSuccess ? ptr : nullptr;
+// The array's device address on `dev` (current): the host-side name of the
+// array is only a stand-in, the kernel needs its device address.  Only a
+// successful lookup is kept, so a lookup that failed (for example during a
+// stream capture) is tried again on the next call.
+cudaError_t resolve_workspace(int dev, void** out) {
+  std::lock_guard<std::mutex> lock(g_ws_mutex[dev]);
+  if (!g_ws_ptr[dev]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_workspace);
+    if (e != cudaSuccess) {
+      cudaGetLastError();  // do not leave the error for the caller's next CUDA call
+      return e;
+    }
+    g_ws_ptr[dev] = ptr;
+  }
+  *out = g_ws_ptr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -56,10 +65,11 @@ extern "C" int mk_decode_step_static_ws(mk_model* m, mk_sched* s, const int32_t*
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return mk::fail(MK_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return mk::fail(MK_ERR_ARG, "device ordinal beyond the supported range");
-  std::call_once(g_ws_once[dev], resolve_workspace, dev);
-  if (g_ws_err[dev] != cudaSuccess)
+  void* ws = nullptr;
+  e = resolve_workspace(dev, &ws);
+  if (e != cudaSuccess)
     return mk::fail(MK_ERR_CUDA, std::string("cudaGetSymbolAddress of the built-in workspace: ") +
-                                     cudaGetErrorString(g_ws_err[dev]));
+                                     cudaGetErrorString(e));
   return mk_decode_step(m, s, last_tokens, seq_lens, block_tables, batch, max_pages, k_pool, v_pool, num_pages,
-                        g_ws_ptr[dev], kStaticWorkspaceBytes, logits, stream);
+                        ws, kStaticWorkspaceBytes, logits, stream);
 }

@@ -43,7 +43,9 @@ class OrcDense(ctypes.Structure):
 class OrcStepIn(ctypes.Structure):
     _fields_ = [("seed", ctypes.c_uint64), ("batch", c_int), ("tokens", P_I), ("seq_lens", P_I),
                 ("block_tables", P_I), ("max_pages", c_int), ("router_bias", P_F),
-                ("force_ids", P_I), ("n_rows", c_int), ("rows", P_I)]
+                ("force_ids", P_I), ("n_rows", c_int), ("rows", P_I), ("norm_gamma", P_D),
+                ("final_gamma", P_D), ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int64)]
 
 
 class OrcStepOut(ctypes.Structure):
@@ -86,6 +88,8 @@ def lib():
         L.orc_kv_slot.restype = c_int
         L.orc_pool_vec.argtypes = [ctypes.POINTER(OrcConfig), ctypes.c_uint64, c_int, c_int, c_int,
                                    c_int, c_int, P_D]
+        L.orc_route_queue.argtypes = [c_int, c_int, c_int, P_I, P_I, P_I, P_I, P_I]
+        L.orc_route_queue.restype = c_int
         L.orc_decode_step.argtypes = [ctypes.POINTER(OrcConfig), ctypes.POINTER(OrcStepIn),
                                       ctypes.POINTER(OrcStepOut)]
         L.orc_decode_step.restype = c_int
@@ -263,6 +267,28 @@ def pool_vec(shape, seed, is_v, layer, page, head, slot):
     return out
 
 
+@dataclass
+class RouteQueue:
+    counts: np.ndarray   # [E] rows routed to each expert
+    offsets: np.ndarray  # [E + 1] exclusive prefix sum
+    rows: np.ndarray     # [B * k] expert-ordered list of b * k + j
+    active: np.ndarray   # [n_active, 3] {expert, offset, count}, experts ascending
+
+
+def route_queue(ids, n_experts: int) -> RouteQueue:
+    """The canonical MoE work queue of one layer from its routing ids [B][k]."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    B, k = ids.shape
+    counts = np.empty(n_experts, np.int32)
+    offsets = np.empty(n_experts + 1, np.int32)
+    rows = np.empty(B * k, np.int32)
+    active = np.empty((n_experts, 3), np.int32)
+    n = lib().orc_route_queue(B, k, n_experts, _i(ids), _i(counts), _i(offsets), _i(rows), _i(active))
+    if n < 0:
+        raise ValueError("expert id out of range")
+    return RouteQueue(counts, offsets, rows, active[:n].copy())
+
+
 # ------------------------------------------------------------- the full step
 
 @dataclass
@@ -280,8 +306,25 @@ class StepResult:
 
 
 def decode_step(shape, seed, tokens, seq_lens, block_tables, router_bias=None, rows=None,
-                force_ids=None, want_hidden=False, want_kv=False, want_attn=False) -> StepResult:
+                force_ids=None, want_hidden=False, want_kv=False, want_attn=False, gains=None,
+                pools=None) -> StepResult:
+    """One decode step of the given rows.  gains: (layer gains [L][H], final
+    gain [H]) or None for ones.  pools: (K pool, V pool) as writable uint16
+    arrays [L][pages][n_kv][P][d] of BF16 bits, read through the block table
+    and updated with the new K/V, or None for the generator's pool."""
     cfg = config_from_shape(shape)
+    ng = fg = kp = vp = None
+    if gains is not None:
+        ng = np.ascontiguousarray(gains[0], np.float64)
+        fg = np.ascontiguousarray(gains[1], np.float64)
+        assert ng.shape == (shape.n_layers, shape.hidden) and fg.shape == (shape.hidden,)
+    if pools is not None:
+        kp, vp = pools
+        for a in (kp, vp):
+            assert a.dtype == np.uint16 and a.flags.c_contiguous and a.flags.writeable
+            assert a.shape[0] == shape.n_layers and a.shape[2:] == (shape.n_kv, shape.page_size,
+                                                                    shape.head_dim)
+        assert kp.shape == vp.shape
     tokens = np.ascontiguousarray(tokens, dtype=np.int32)
     seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
     bt = np.ascontiguousarray(block_tables, dtype=np.int32)
@@ -299,7 +342,10 @@ def decode_step(shape, seed, tokens, seq_lens, block_tables, router_bias=None, r
                      np.empty((L, R, shape.n_q * shape.head_dim)) if want_attn else None, rows)
     sin = OrcStepIn(seed, B, _i(tokens), _i(seq_lens), _i(bt), bt.shape[1],
                     _f(bias) if bias is not None else None,
-                    _i(force) if force is not None else None, R, _i(rows))
+                    _i(force) if force is not None else None, R, _i(rows),
+                    _d(ng) if ng is not None else None, _d(fg) if fg is not None else None,
+                    kp.ctypes.data if kp is not None else None, vp.ctypes.data if vp is not None else None,
+                    kp.shape[1] if kp is not None else 0)
     sout = OrcStepOut(_d(res.logits), _i(res.ids), _d(res.weights), _i(res.own_ids),
                       _f(res.margin), _f(res.router_logits),
                       _d(res.hidden) if want_hidden else None,

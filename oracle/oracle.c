@@ -357,8 +357,45 @@ static int config_ok(const orc_config* c) {
  * [lo, seq_len) ([tiny-vllm] "The decode loop": the length includes the
  * token; its K/V is written before the attention call).  lo = 0 for a full
  * layer, max(0, seq_len - window) for a sliding one. */
+/* The canonical MoE queue of one layer (see oracle.h).  Counting and the
+ * prefix sum are written out; the list is filled by walking the routed
+ * entries (b, j) in row-major order, each landing at its expert's next free
+ * place, which gives rows by b ascending then j ascending within an expert. */
+int orc_route_queue(int batch, int k, int n_experts, const int32_t* ids, int32_t* counts, int32_t* offsets,
+                    int32_t* rows, int32_t* active) {
+  const int n = batch * k;
+  for (int e = 0; e < n_experts; ++e) counts[e] = 0;
+  for (int i = 0; i < n; ++i) {
+    if (ids[i] < 0 || ids[i] >= n_experts) return -1;
+    ++counts[ids[i]];
+  }
+  offsets[0] = 0;
+  for (int e = 0; e < n_experts; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  int32_t* next = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n_experts > 0 ? n_experts : 1));
+  for (int e = 0; e < n_experts; ++e) next[e] = offsets[e];
+  for (int i = 0; i < n; ++i) rows[next[ids[i]]++] = i;
+  free(next);
+  int n_active = 0;
+  for (int e = 0; e < n_experts; ++e)
+    if (counts[e] > 0) {
+      active[3 * n_active + 0] = e;
+      active[3 * n_active + 1] = offsets[e];
+      active[3 * n_active + 2] = counts[e];
+      ++n_active;
+    }
+  return n_active;
+}
+
+/* Element offset of (layer, page, head, slot) in a pool [L][pages][n_kv][P][d]. */
+static size_t pool_off(const orc_config* cfg, int64_t num_pages, int layer, int page, int head, int slot) {
+  return ((((size_t)layer * (size_t)num_pages + (size_t)page) * (size_t)cfg->n_kv + (size_t)head) *
+              (size_t)cfg->page_size + (size_t)slot) * (size_t)cfg->head_dim;
+}
+
 int orc_decode_step(const orc_config* cfg, const orc_step_in* in, orc_step_out* out) {
   if (!config_ok(cfg) || !in || !out || in->batch <= 0 || in->n_rows < 0) return -1;
+  if ((in->k_pool == NULL) != (in->v_pool == NULL)) return -1;
+  if (in->k_pool && in->num_pages < 1) return -1;
   const int L = cfg->n_layers, H = cfg->hidden, nq = cfg->n_q, nkv = cfg->n_kv;
   const int d = cfg->head_dim, E = cfg->n_experts, k = cfg->top_k, V = cfg->vocab;
   const int G = nq / nkv, P = cfg->page_size, R = in->n_rows;
@@ -370,6 +407,11 @@ int orc_decode_step(const orc_config* cfg, const orc_step_in* in, orc_step_out* 
     const int s = in->seq_lens[b];
     if (s < 1 || (s + P - 1) / P > in->max_pages) return -1;
     if (in->tokens[b] < 0 || in->tokens[b] >= V) return -1;
+    if (in->k_pool) /* every page the row reads must be in the explicit pool */
+      for (int j = 0; j < (s + P - 1) / P; ++j) {
+        const int32_t pg = in->block_tables[(size_t)b * in->max_pages + j];
+        if (pg < 0 || pg >= in->num_pages) return -1;
+      }
   }
 
   double* h = (double*)malloc(sizeof(double) * (size_t)H);
@@ -402,7 +444,7 @@ int orc_decode_step(const orc_config* cfg, const orc_step_in* in, orc_step_out* 
 
     for (int l = 0; l < L; ++l) {
       if (out->hidden) memcpy(out->hidden + ((size_t)l * R + r) * H, h, sizeof(double) * H);
-      orc_rmsnorm(H, h, NULL, cfg->eps, x);
+      orc_rmsnorm(H, h, in->norm_gamma ? in->norm_gamma + (size_t)l * H : NULL, cfg->eps, x);
 
       /* attention branch */
       orc_matrix wqkv = orc_synth_matrix(cfg, in->seed, SYNTH_WQKV, l, 0, &st);
@@ -413,6 +455,17 @@ int orc_decode_step(const orc_config* cfg, const orc_step_in* in, orc_step_out* 
                sizeof(double) * 2 * nkv * d);
       /* the new entry as the BF16 pool holds it */
       for (int i = nq * d; i < QKV; ++i) qkv[i] = round_bf16(qkv[i]);
+      if (in->k_pool) { /* stored at position pos before attention reads the pool */
+        int32_t page = 0, off = 0;
+        orc_kv_slot(pos, P, brow, in->max_pages, &page, &off);
+        for (int g = 0; g < nkv; ++g) {
+          const size_t o = pool_off(cfg, in->num_pages, l, page, g, off);
+          for (int i = 0; i < d; ++i) {
+            in->k_pool[o + i] = synth_f32_to_bf16_rne((float)qkv[(size_t)(nq + g) * d + i]);
+            in->v_pool[o + i] = synth_f32_to_bf16_rne((float)qkv[(size_t)(nq + nkv + g) * d + i]);
+          }
+        }
+      }
 
       const int full = cfg->window == 0 || (l + 1) % cfg->full_period == 0;
       const int64_t lo = full ? 0 : (s - cfg->window > 0 ? s - cfg->window : 0);
@@ -423,7 +476,15 @@ int orc_decode_step(const orc_config* cfg, const orc_step_in* in, orc_step_out* 
 #pragma omp parallel for schedule(static)
         for (int t = 0; t < n; ++t) {
           const int64_t p = lo + t;
-          if (p == pos) {
+          if (in->k_pool) {
+            int32_t page = 0, off = 0;
+            orc_kv_slot(p, P, brow, in->max_pages, &page, &off);
+            const size_t o = pool_off(cfg, in->num_pages, l, page, g, off);
+            for (int i = 0; i < d; ++i) {
+              K[(size_t)t * d + i] = (double)synth_bf16_to_f32(in->k_pool[o + i]);
+              Vv[(size_t)t * d + i] = (double)synth_bf16_to_f32(in->v_pool[o + i]);
+            }
+          } else if (p == pos) {
             memcpy(K + (size_t)t * d, qkv + (size_t)(nq + g) * d, sizeof(double) * d);
             memcpy(Vv + (size_t)t * d, qkv + (size_t)(nq + nkv + g) * d, sizeof(double) * d);
           } else {
@@ -476,7 +537,7 @@ int orc_decode_step(const orc_config* cfg, const orc_step_in* in, orc_step_out* 
     if (out->hidden) memcpy(out->hidden + ((size_t)L * R + r) * H, h, sizeof(double) * H);
 
     /* final RMSNorm and LM head */
-    orc_rmsnorm(H, h, NULL, cfg->eps, x);
+    orc_rmsnorm(H, h, in->final_gamma, cfg->eps, x);
     orc_matrix wlm = orc_synth_matrix(cfg, in->seed, SYNTH_WLM, 0, 0, &st);
     if (out->logits) orc_matvec(&wlm, x, out->logits + (size_t)r * V);
   }

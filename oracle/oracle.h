@@ -116,6 +116,16 @@ typedef struct {
   const int32_t* force_ids;    /* [L][B][k] routing to follow, or NULL (see orc_decode_step) */
   int n_rows;
   const int32_t* rows;         /* the batch rows b to evaluate */
+  const double* norm_gamma;    /* [L][H] gain of each layer's input RMSNorm, or NULL (all ones) */
+  const double* final_gamma;   /* [H] gain of the final RMSNorm, or NULL (all ones) */
+  /* Optional explicit KV pools, BF16 bit patterns [L][num_pages][n_kv][P][d]
+   * (K and V).  NULL: the generator's pool, never written.  Given: attention
+   * reads every key and value from them through the block table, and the
+   * step first stores the new token's K and V (rounded to BF16) in the slot
+   * of position seq_len - 1, so that a later call sees what this one wrote. */
+  uint16_t* k_pool;
+  uint16_t* v_pool;
+  int64_t num_pages;
 } orc_step_in;
 
 typedef struct {
@@ -129,6 +139,20 @@ typedef struct {
   double* kv_new;       /* optional [L][n_rows][2][n_kv][d]: new K (after RoPE) and V, before BF16 */
   double* attn;         /* optional [L][n_rows][n_q d]: attention output */
 } orc_step_out;
+
+/* The MoE work queue of one layer, as ROUTE_FINALIZE builds it ("Cohere: a
+ * decode megakernel for North Mini Code", section "Tasks": the routing
+ * becomes per-expert row counts and offsets and the expert-ordered list of
+ * routed rows that the MoE GEMM tiles drain).  ids [batch][k] are the experts
+ * of each row.  Canonical order: experts ascending; within an expert, routed
+ * entries by row b ascending, then choice j ascending.
+ *   counts  [n_experts]      rows routed to each expert
+ *   offsets [n_experts + 1]  exclusive prefix sum of counts (offsets[E] = batch * k)
+ *   rows    [batch * k]      entry i of the expert-ordered list is b * k + j
+ *   active  [n_experts][3]   the experts with rows, ascending: {expert, offset, count}
+ * Returns the number of active experts, or -1 on an expert id out of range. */
+int orc_route_queue(int batch, int k, int n_experts, const int32_t* ids, int32_t* counts, int32_t* offsets,
+                    int32_t* rows, int32_t* active);
 
 /* Returns 0, or -1 on an invalid argument.  With force_ids, layer l of row
  * b uses the forced experts instead of its own top-k; the caller is the one

@@ -19,7 +19,7 @@ from .workloads import (MODELS, WORKLOADS, ModelShape, Workload, StepInputs, mak
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libsynth.so")
 
-EMB, WQKV, WO, WR, WG, WU, WD, WLM, KPOOL, VPOOL, SG, SU, SD, BG, BU, BD = range(1, 17)
+EMB, WQKV, WO, WR, WG, WU, WD, WLM, KPOOL, VPOOL, SG, SU, SD, BG, BU, BD, GAMMA = range(1, 18)
 
 _lib = None
 
@@ -69,6 +69,10 @@ def lib():
         L.synth_fp4_base_of.argtypes = [ctypes.c_double]
         L.synth_e2m1.restype = ctypes.c_uint8
         L.synth_e2m1.argtypes = [ctypes.c_float]
+        L.synth_fill_gains_device.restype = ctypes.c_int
+        L.synth_fill_gains_device.argtypes = [ctypes.c_void_p, u64, u64, u64, u32, ctypes.c_void_p]
+        L.synth_fill_gains_host.restype = None
+        L.synth_fill_gains_host.argtypes = [ctypes.c_void_p, u64, u64, u64, u32]
         _lib = L
     return _lib
 
@@ -183,6 +187,27 @@ def fill_scales4_device(ptr: int, n_streams: int, rows: int, seed: int, kind: in
                                              int(vary_layer), fp4_base(sigma), stream)
     if rc != 0:
         raise RuntimeError(f"synth_fill_scales_base_device failed with CUDA error {rc}")
+
+
+def fill_gains_host(n_layers: int, per_layer: int, seed: int, layer0: int = 0) -> np.ndarray:
+    """float32 RMSNorm gains [n_layers][per_layer] of layers layer0 .. (stream (GAMMA, l, 0))."""
+    out = np.empty((n_layers, per_layer), dtype=np.float32)
+    lib().synth_fill_gains_host(out.ctypes.data, n_layers, per_layer, seed, layer0)
+    return out
+
+
+def gains_host(shape, seed: int):
+    """The seeded gains of a model: (layer norms [L][H], final norm [H]), float32;
+    the final norm's stream is layer n_layers."""
+    return (fill_gains_host(shape.n_layers, shape.hidden, seed),
+            fill_gains_host(1, shape.hidden, seed, layer0=shape.n_layers)[0])
+
+
+def fill_gains_device(ptr: int, n_layers: int, per_layer: int, seed: int, layer0: int = 0,
+                      stream: int = 0) -> None:
+    rc = lib().synth_fill_gains_device(ptr, n_layers, per_layer, seed, layer0, stream)
+    if rc != 0:
+        raise RuntimeError(f"synth_fill_gains_device failed with CUDA error {rc}")
 
 
 def raw(key: int, idx: int) -> int:

@@ -10,7 +10,7 @@ import torch
 
 from . import (EMB, WQKV, WO, WR, WG, WU, WD, WLM, KPOOL, VPOOL, SG, SU, SD, BG, BU, BD, fill_device,
                fill_fp4_device, fill_bscales_device, fill_scales4_device, fill_fp8_device,
-               fill_scales_device)
+               fill_scales_device, fill_gains_device)
 from .workloads import ModelShape
 
 
@@ -21,10 +21,12 @@ def _fill(t: torch.Tensor, n_streams: int, per: int, seed: int, kind: int, layer
     fill_device(t.data_ptr(), n_streams, per, seed, kind, layer0, expert0, vary_layer, sigma, stream)
 
 
-def device_weights(shape: ModelShape, seed: int, device="cuda", router_bias=None) -> dict:
+def device_weights(shape: ModelShape, seed: int, device="cuda", router_bias=None, gains=False) -> dict:
     """All weights of the model as torch tensors (BF16 stored as uint16; with
     expert_fp8 the expert matrices as uint8 E4M3 codes plus fp32 row scales; with
-    expert_fp4 packed E2M1 codes, E4M3 block scales and fp32 row scales)."""
+    expert_fp4 packed E2M1 codes, E4M3 block scales and fp32 row scales).  The
+    RMSNorm gains are ones, or with `gains` the generator's seeded gains in
+    [0.5, 2) (synth.h, "RMSNorm gains")."""
     st = torch.cuda.current_stream(device).cuda_stream
     L, H, E, I, V = shape.n_layers, shape.hidden, shape.n_experts, shape.inter, shape.vocab
     QKV, NQD = shape.qkv_rows(), shape.n_q * shape.head_dim
@@ -41,6 +43,9 @@ def device_weights(shape: ModelShape, seed: int, device="cuda", router_bias=None
         "router_bias": (torch.as_tensor(router_bias, dtype=torch.float32).to(device)
                         if router_bias is not None else None),
     }
+    if gains:
+        fill_gains_device(w["norm_gamma"].data_ptr(), L, H, seed, stream=st)
+        fill_gains_device(w["final_gamma"].data_ptr(), 1, H, seed, layer0=L, stream=st)
     _fill(w["embedding"], 1, V * H, seed, EMB, sigma=sg, stream=st)
     _fill(w["w_qkv"], L, QKV * H, seed, WQKV, vary_layer=True, sigma=sg, stream=st)
     _fill(w["w_o"], L, H * NQD, seed, WO, vary_layer=True, sigma=sg, stream=st)

@@ -82,7 +82,9 @@ enum {
   SYNTH_SD = 13,   /* FP8 / FP4 expert down row scales [H]      */
   SYNTH_BG = 14,   /* FP4 expert gate block scales [I][H/16]    */
   SYNTH_BU = 15,   /* FP4 expert up block scales [I][H/16]      */
-  SYNTH_BD = 16    /* FP4 expert down block scales [H][I/16]    */
+  SYNTH_BD = 16,   /* FP4 expert down block scales [H][I/16]    */
+  SYNTH_GAMMA = 17 /* RMSNorm gains [H]: layer l's input norm is stream
+                      (GAMMA, l, 0), the final norm (GAMMA, n_layers, 0) */
 };
 
 SYNTH_FN uint64_t synth_mix64(uint64_t z) {
@@ -137,6 +139,23 @@ SYNTH_FN float synth_bf16_to_f32(uint16_t b) {
   f = __uint_as_float(u);
 #else
   memcpy(&f, &u, sizeof f);
+#endif
+  return f;
+}
+
+/* ---- RMSNorm gains ---- */
+
+/* Gain idx of stream key: the binary32 with exponent 2^-1 or 2^0 (top bit of
+ * the draw) and the draw's low 23 bits as its mantissa, so gains are spread
+ * over [0.5, 2) and are built from integer bits only (no rounding). */
+SYNTH_FN float synth_gain(uint64_t key, uint64_t idx) {
+  const uint64_t r = synth_draw(key, idx);
+  const uint32_t bits = ((126u + (uint32_t)(r >> 63)) << 23) | (uint32_t)(r & 0x7fffffu);
+  float f;
+#if defined(__CUDA_ARCH__)
+  f = __uint_as_float(bits);
+#else
+  memcpy(&f, &bits, sizeof f);
 #endif
   return f;
 }

@@ -126,6 +126,18 @@ __global__ void fill_block_scales(uint8_t* __restrict__ dst, uint64_t n_streams,
   }
 }
 
+// RMSNorm gains: element i of sub-stream j (layer layer0 + j).
+__global__ void fill_gains(float* __restrict__ dst, uint64_t n_streams, uint64_t per_stream, uint64_t seed,
+                           uint32_t layer0) {
+  const uint64_t total = n_streams * per_stream;
+  for (uint64_t g = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+       g += (uint64_t)gridDim.x * blockDim.x) {
+    const uint64_t j = g / per_stream, i = g - j * per_stream;
+    const uint64_t key = synth_key(seed, synth_stream(SYNTH_GAMMA, layer0 + (uint32_t)j, 0));
+    dst[g] = synth_gain(key, i);
+  }
+}
+
 int launch_blocks() {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -210,6 +222,23 @@ extern "C" void synth_fill_scales_base_host(float* dst, uint64_t rows, uint64_t 
 }
 
 extern "C" float synth_fp4_base_of(double sigma) { return synth_fp4_base(sigma); }
+
+// RMSNorm gains on the device: `per_stream` gains of layers layer0 .. layer0 + n_streams - 1.
+extern "C" int synth_fill_gains_device(float* dst, uint64_t n_streams, uint64_t per_stream, uint64_t seed,
+                                       uint32_t layer0, void* stream) {
+  if (dst == nullptr || n_streams == 0 || per_stream == 0) return (int)cudaErrorInvalidValue;
+  fill_gains<<<launch_blocks(), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(dst, n_streams, per_stream,
+                                                                                  seed, layer0);
+  return (int)cudaGetLastError();
+}
+
+extern "C" void synth_fill_gains_host(float* dst, uint64_t n_streams, uint64_t per_stream, uint64_t seed,
+                                      uint32_t layer0) {
+  for (uint64_t j = 0; j < n_streams; ++j) {
+    const uint64_t key = synth_key(seed, synth_stream(SYNTH_GAMMA, layer0 + (uint32_t)j, 0));
+    for (uint64_t i = 0; i < per_stream; ++i) dst[j * per_stream + i] = synth_gain(key, i);
+  }
+}
 extern "C" uint8_t synth_e2m1(float f) { return synth_f32_to_e2m1_rne(f); }
 
 extern "C" void synth_fill_fp8_host(uint8_t* dst, uint64_t n, uint64_t seed, uint32_t kind, uint32_t layer,

@@ -111,6 +111,7 @@ class Workload:
     zipf: float | None = None
     desc: str = ""
     shape_override: ModelShape | None = None
+    gains: bool = False  # seeded RMSNorm gains in [0.5, 2) instead of ones
 
     @property
     def shape(self) -> ModelShape:
@@ -151,6 +152,13 @@ WORKLOADS = {
                              desc="small shape with FP4 experts: 8 layers, B=2, seq_lens U[1,1024]"),
     "full_fp4_bs1_8k": Workload("full_fp4_bs1_8k", "full_fp4", 1, ("fixed", 8192), 3,
                                 desc="full shape with FP4 experts, B=1, context 8192"),
+    # seeded, non-unit RMSNorm gains (every layer's and the final norm's)
+    "tiny_gains": Workload("tiny_gains", "tiny", 1, ("fixed", 64), 31, gains=True,
+                           desc="tiny with seeded RMSNorm gains in [0.5, 2)"),
+    "small_gains": Workload("small_gains", "small", 1, ("fixed", 1024), 32, gains=True,
+                            desc="small with seeded RMSNorm gains in [0.5, 2)"),
+    "full_gains_bs1_8k": Workload("full_gains_bs1_8k", "full", 1, ("fixed", 8192), 33, gains=True,
+                                  desc="full shape, B=1, context 8192, seeded RMSNorm gains"),
     "prof_l2_8k": Workload("prof_l2_8k", "full_l2", 1, ("fixed", 8192), 7,
                            desc="full-shape layers, 2 of them, B=1, context 8192 (profiling case)"),
 }

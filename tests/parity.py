@@ -22,17 +22,20 @@ import moe_decode_megakernel_gb300 as mk
 
 LOGIT_TOL = 2e-2      # max |gpu - oracle| / max |oracle| per row
 MARGIN_TOL = 1e-3     # router-logit gap below which a top-k swap is a tie
+# Router logits: a quarter of the tie margin, so that no decision whose
+# margin exceeds MARGIN_TOL can flip through the router's own error.
+ROUTER_TOL = MARGIN_TOL / 4
 
 _cache: dict = {}
 
 
-def _device_model(shape, seed, bias):
-    key = (shape, seed, None if bias is None else bias.tobytes())
+def _device_model(shape, seed, bias, gains=False):
+    key = (shape, seed, None if bias is None else bias.tobytes(), gains)
     if _cache.get("key") != key:
         _cache.clear()
         gc.collect()
         torch.cuda.empty_cache()
-        w = synth.device.device_weights(shape, seed, router_bias=bias)
+        w = synth.device.device_weights(shape, seed, router_bias=bias, gains=gains)
         model = mk.Model(mk.config_from(shape), mk.weights_from(w), keepalive=w)
         _cache.update(key=key, w=w, model=model)
     return _cache["model"]
@@ -58,7 +61,7 @@ class GpuStep:
 def run_gpu(inp: synth.StepInputs, opts=None, steps: int = 1) -> GpuStep:
     w = inp.workload
     shape, B = w.shape, w.batch
-    model = _device_model(shape, w.seed, inp.router_bias)
+    model = _device_model(shape, w.seed, inp.router_bias, w.gains)
     o = opts if opts is not None else mk.default_sched_opts()
     sched = mk.Sched(model, B, int(inp.seq_lens.max()), o)
     sess = mk.Session(model, sched)
@@ -83,10 +86,41 @@ def run_gpu(inp: synth.StepInputs, opts=None, steps: int = 1) -> GpuStep:
     kk = torch.stack([kp[:, int(pages[b]), :, int(pos[b] % P), :] for b in range(B)], 1)
     vv = torch.stack([vp[:, int(pages[b]), :, int(pos[b] % P), :] for b in range(B)], 1)
     to_f = lambda t: synth.bf16_bits_to_f32(t.cpu().numpy())
+    extra = {"router_logits": rlog.cpu().numpy().copy()}
+    if o.trace_queue:
+        E = shape.n_experts
+        stride = queue_trace_stride(E, B * K)
+        extra["queue_trace"] = sess.region("queue_trace", torch.int32, L * stride).view(L, stride).cpu().numpy()
+        extra["expert_count"] = sess.region("expert_count", torch.int32, L * E).view(L, E).cpu().numpy()
     res = GpuStep(logits.cpu().numpy(), ids.cpu().numpy().copy(), wts.cpu().numpy().copy(),
-                  to_f(kk), to_f(vv), sess, {"router_logits": rlog.cpu().numpy().copy()})
+                  to_f(kk), to_f(vv), sess, extra)
     del kp, vp
     return res
+
+
+def queue_trace_stride(E: int, n_routed_max: int) -> int:
+    """Ints per layer of the "queue_trace" region (the layout mk.h states)."""
+    return (4 * E + (E + 1) + n_routed_max + 2 + 3) // 4 * 4
+
+
+def compare_queue(inp: synth.StepInputs, g: GpuStep) -> int:
+    """Every layer's MoE work queue as the GPU built it (active-expert list,
+    offsets, expert-ordered rows, counts) against the oracle's canonical queue
+    of the GPU's own routing: bit-exact.  Returns the layers checked."""
+    w = inp.workload
+    L, K, E, B = w.shape.n_layers, w.shape.top_k, w.shape.n_experts, w.batch
+    qt = g.extra["queue_trace"]
+    for l in range(L):
+        ref = oracle.route_queue(g.ids[l, :B], E)
+        rec = qt[l]
+        n_act, n_rows = int(rec[5 * E + 1 + B * K]), int(rec[5 * E + 1 + B * K + 1])
+        assert n_act == len(ref.active) and n_rows == B * K, (l, n_act, n_rows)
+        act = rec[:4 * E].reshape(E, 4)[:n_act]
+        assert np.array_equal(act[:, :3], ref.active), (l, act[:, :3], ref.active)
+        assert np.array_equal(rec[4 * E:5 * E + 1], ref.offsets), l
+        assert np.array_equal(rec[5 * E + 1:5 * E + 1 + B * K], ref.rows), l
+        assert np.array_equal(g.extra["expert_count"][l], ref.counts), l
+    return L
 
 
 def bf16_round(a):
@@ -102,8 +136,9 @@ class Report:
     exact_routing: int
     tie_routing: int
     total_routing: int
-    greedy_agree: int
+    greedy_agree: int     # argmax equal, or within the logit tolerance of a near-tie
     greedy_total: int
+    greedy_exact: int     # argmax equal
     kv_max_err: float
     router_err: np.ndarray  # per layer: max |gpu - oracle| router logit
     weight_err: float
@@ -119,8 +154,9 @@ def compare(inp: synth.StepInputs, g: GpuStep, rows=None) -> Report:
     # takes expert 0 with weight 1, which is the oracle's routing too
     dense = shape.n_experts == 1 and K == 1
     ids = np.zeros_like(g.ids) if dense else g.ids
+    gains = synth.gains_host(shape, w.seed) if w.gains else None
     ref = oracle.decode_step(shape, w.seed, inp.tokens, inp.seq_lens, inp.block_tables,
-                             inp.router_bias, rows=rows, force_ids=ids, want_kv=True)
+                             inp.router_bias, rows=rows, force_ids=ids, want_kv=True, gains=gains)
     rerr = np.zeros(L) if dense else np.array(
         [max(float(np.max(np.abs(g.extra["router_logits"][l, b] - ref.router_logits[l, r])))
              for r, b in enumerate(rows)) for l in range(L)])
@@ -150,12 +186,13 @@ def compare(inp: synth.StepInputs, g: GpuStep, rows=None) -> Report:
                                  for l in range(L) for r, b in enumerate(rows))
     # logits
     errs = []
-    agree = 0
+    agree = exact_greedy = 0
     for r, b in enumerate(rows):
         o = ref.logits[r]
         e = np.max(np.abs(g.logits[b] - o)) / np.max(np.abs(o))
         errs.append(e)
         ga, oa = int(np.argmax(g.logits[b])), int(np.argmax(o))
+        exact_greedy += ga == oa
         srt = np.sort(o)[::-1]
         if ga == oa or (o[oa] - o[ga]) <= 2 * LOGIT_TOL * np.max(np.abs(o)) and srt[0] - srt[1] < 1e-2:
             agree += 1
@@ -169,5 +206,5 @@ def compare(inp: synth.StepInputs, g: GpuStep, rows=None) -> Report:
                 got = gv[l, b]
                 scale = max(1.0, np.max(np.abs(want)))
                 kerr = max(kerr, float(np.max(np.abs(got - want)) / scale))
-    return Report(float(max(errs)), np.array(errs), exact, ties, L * len(rows), agree, len(rows), kerr,
-                  rerr, werr, bad)
+    return Report(float(max(errs)), np.array(errs), exact, ties, L * len(rows), agree, len(rows), exact_greedy,
+                  kerr, rerr, werr, bad)

@@ -244,3 +244,50 @@ def test_dense_schedules(workload):
                                           "MOE_UPGATE_ACT_DRAIN", "MOE_DOWN_DRAIN"))
     assert counts["FFN_UPGATE_ACT"] == sh.n_layers * (sh.inter // 64)
     assert counts["FFN_DOWN"] == sh.n_layers * (sh.hidden // 32)
+
+
+def test_host_input_check_refuses_before_launch():
+    """mk_check_inputs: a seq_len beyond the schedule's max_ctx, a page id
+    outside the pool, a block table too narrow for the length, a token outside
+    the vocabulary or a batch beyond max_batch is MK_ERR_ARG with the row named;
+    valid inputs pass.  Host only (no device)."""
+    sh = synth.MODELS["tiny"]
+    model = fake_model(sh)
+    opts = mk.default_sched_opts(num_sms=NUM_SMS)
+    s = mk.Sched(model, 4, 64, opts)
+    P = sh.page_size
+    sl = np.array([64, 17, 1], np.int32)
+    bt = np.array([[0, 1, 2, 3], [4, 5, -1, -1], [6, -1, -1, -1]], np.int32)
+    tok = np.array([0, 5, sh.vocab - 1], np.int32)
+    s.check_inputs(tok, sl, bt, 7)
+    s.check_inputs(None, sl, bt, 7)
+    cases = [
+        (tok, np.array([65, 17, 1], np.int32), bt, 7, "seq_len 65"),      # > max_ctx
+        (tok, np.array([64, 0, 1], np.int32), bt, 7, "seq_len 0"),
+        (tok, sl, bt, 6, "page 6"),                                        # outside the pool
+        (tok, np.array([64, 33, 1], np.int32), bt, 7, "page -1"),          # a page that is not there
+        (np.array([0, 5, sh.vocab], np.int32), sl, bt, 7, "token"),
+        (tok, sl, bt[:, :2], 7, "needs 4 pages"),
+    ]
+    for t, l, b, n, what in cases:
+        with pytest.raises(mk.MkError) as e:
+            s.check_inputs(t, l, b, n)
+        assert e.value.code == mk.MK_ERR_ARG and what in str(e.value), (what, str(e.value))
+    with pytest.raises(mk.MkError) as e:
+        s.check_inputs(np.zeros(5, np.int32), np.full(5, 8, np.int32), np.zeros((5, 1), np.int32), 7)
+    assert e.value.code == mk.MK_ERR_ARG and "batch 5" in str(e.value)
+    assert P == 16
+
+
+def test_queue_trace_region_size():
+    """The "queue_trace" region holds L records of the stride mk.h states."""
+    sh = synth.MODELS["full"]
+    model = fake_model(sh)
+    for B in (1, 32):
+        s = mk.Sched(model, B, 8192, mk.default_sched_opts(num_sms=NUM_SMS, trace_queue=1))
+        off = s.workspace_offset("queue_trace")
+        stride = (4 * sh.n_experts + sh.n_experts + 1 + B * sh.top_k + 2 + 3) // 4 * 4
+        assert off >= 0 and off % 16 == 0
+        assert s.workspace_bytes() - off >= sh.n_layers * stride * 4
+        assert s.workspace_bytes() - off < sh.n_layers * stride * 4 + 256
+        assert mk.Sched(model, B, 8192, mk.default_sched_opts(num_sms=NUM_SMS)).workspace_offset("queue_trace") == -1

@@ -24,12 +24,15 @@ def _rows(inp, extra):
                                             ("full_bs2_8k", [1]), ("full_bs4_8k", [2])])
 def test_large_workloads(workload, extra):
     inp = synth.make_inputs(workload)
-    g = parity.run_gpu(inp)
+    g = parity.run_gpu(inp, parity.mk.default_sched_opts(trace_queue=1))
+    # the MoE queue of every layer, bit-exact (Zipf-skewed routing at batch 32)
+    assert parity.compare_queue(inp, g) == inp.workload.shape.n_layers
     rows = _rows(inp, extra)
     rep = parity.compare(inp, g, rows=rows)
     print(workload, "rows", rows, f"logit rel err {rep.max_rel_err:.3e} router err {rep.router_err.max():.3e} "
           f"routing exact {rep.exact_routing}/{rep.total_routing} ties {rep.tie_routing} kv {rep.kv_max_err:.2e}")
     assert not rep.routing_violations, rep.routing_violations
+    assert rep.router_err.max() <= parity.ROUTER_TOL
     assert rep.weight_err <= 1e-4
     assert rep.max_rel_err <= parity.LOGIT_TOL
     assert rep.greedy_agree == rep.greedy_total

@@ -18,6 +18,7 @@ def check(rep, total_rows):
           f"routing exact {rep.exact_routing}/{rep.total_routing} ties {rep.tie_routing}  "
           f"kv {rep.kv_max_err:.2e}")
     assert not rep.routing_violations, rep.routing_violations
+    assert rep.router_err.max() <= parity.ROUTER_TOL, rep.router_err
     assert rep.weight_err <= 1e-4, rep.weight_err
     assert rep.max_rel_err <= parity.LOGIT_TOL, rep
     assert rep.greedy_agree == rep.greedy_total, rep
@@ -25,21 +26,27 @@ def check(rep, total_rows):
     assert rep.kv_max_err <= 2e-2, rep
 
 
-@pytest.mark.parametrize("workload", ["tiny", "small"])
+@pytest.mark.parametrize("workload", ["tiny", "small", "tiny_gains", "small_gains"])
 def test_small_configs(workload):
+    """tiny and small, with unit and with seeded non-unit RMSNorm gains (the
+    gains pin each layer's gain row and the final gain on the GPU side); the
+    MoE queue of every layer bit-exact."""
     inp = synth.make_inputs(workload)
-    g = parity.run_gpu(inp)
+    g = parity.run_gpu(inp, mk.default_sched_opts(trace_queue=1))
     rep = parity.compare(inp, g)
     print(workload, rep)
     check(rep, 1)
+    assert parity.compare_queue(inp, g) == inp.workload.shape.n_layers
 
 
-def test_full_bs1_8k():
-    inp = synth.make_inputs("full_bs1_8k")
-    g = parity.run_gpu(inp)
+@pytest.mark.parametrize("workload", ["full_bs1_8k", "full_gains_bs1_8k"])
+def test_full_bs1_8k(workload):
+    inp = synth.make_inputs(workload)
+    g = parity.run_gpu(inp, mk.default_sched_opts(trace_queue=1))
     rep = parity.compare(inp, g)
-    print("full_bs1_8k", rep)
+    print(workload, rep)
     check(rep, 1)
+    assert parity.compare_queue(inp, g) == 48
 
 
 @pytest.mark.parametrize("order", [1, 2, 3, 4, 5])
