@@ -164,10 +164,6 @@ typedef struct {
                                claimer's static unit count) says they finish first */
   int32_t trace_queue;      /* 1: keep every layer's MoE work queue in the workspace
                                ("queue_trace", see mk_workspace_offset) */
-  int32_t l2_lookahead;     /* N > 0: when an SM starts a task it asks L2 to prefetch the
-                               step-independent inputs (weight rows, the KV pages of static
-                               attention slices) of its next N tasks, so they stream from HBM
-                               while dependency waits hold the stage ring; 0: off */
 } mk_sched_opts;
 
 /* Fills opts with the defaults (all zero except fuse_* = 1 and moe_static = 1). */

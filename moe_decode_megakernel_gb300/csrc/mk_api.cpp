@@ -382,7 +382,6 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   p.n_static = s->n_static;
   p.max_slots = s->max_slots;
   p.explicit_gather = s->opts.explicit_gather;
-  p.l2_lookahead = s->opts.l2_lookahead;
   p.watchdog_ns = s->watchdog_ns;
   (void)D;
 

@@ -290,7 +290,6 @@ struct Params {
   int n_static;         // static slices per (row, group) of a sliding layer
   int max_slots;
   int explicit_gather;
-  int l2_lookahead;     // tasks ahead whose step-independent inputs are prefetched into L2
   int64_t watchdog_ns;
 };
 

@@ -96,10 +96,6 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
       "l"(src), "r"(bytes), "r"(smem_u32(b)), "l"(policy)
       : "memory");
 }
-// Asks L2 to fetch [src, src + bytes) (16-byte aligned, a multiple of 16 bytes); no completion.
-__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -1015,78 +1011,13 @@ struct Producer {
     return push(it);
   }
 
-  // ---- far-ahead L2 prefetch ("3. Weight prefetch", a layer ahead) ----
-  // The step-independent inputs of a task that is still far down this SM's
-  // list: dense weight rows (QKV, router, LM head), the O-proj rows' columns
-  // of the task's KV group, and the KV pages of static attention slices.  The
-  // stage ring holds only the next few stages, and its stages wait behind the
-  // tasks in front of them; an L2 prefetch lets these bytes stream from HBM
-  // while the SM stalls on dependencies, and the ring's later copies hit L2.
-  // MoE tiles are not prefetched: their experts are known only after routing.
-  __device__ __noinline__ void prefetch_task(const int32_t* dg) {
-    const int op = __ldg(dg + F_OP), l = __ldg(dg + F_LAYER);
-    if (op == OP_QKV_PROJ || op == OP_ROUTER_GEMM || op == OP_LM_HEAD) {
-      const uint16_t* base = op == OP_QKV_PROJ      ? p.wqkv + (int64_t)l * S::QKV * S::H
-                             : op == OP_ROUTER_GEMM ? p.wr + (int64_t)l * S::E * S::H
-                                                    : p.wlm;
-      if (!base) return;
-      const char* src = reinterpret_cast<const char*>(base + (int64_t)__ldg(dg + F_A0) * S::H);
-      const int64_t bytes = (int64_t)__ldg(dg + F_A0 + 1) * S::H * 2;
-      for (int64_t o = 0; o < bytes; o += 65536) l2_prefetch(src + o, (uint32_t)(bytes - o < 65536 ? bytes - o : 65536));
-    } else if (op == OP_O_PROJ) {
-      const uint16_t* base = p.wo + (int64_t)l * S::H * S::NQ * S::D + (int64_t)__ldg(dg + F_A0 + 2) * S::G * S::D;
-      const int row0 = __ldg(dg + F_A0), rows = __ldg(dg + F_A0 + 1);
-      for (int r = 0; r < rows; ++r) l2_prefetch(base + (int64_t)(row0 + r) * S::NQ * S::D, S::G * S::D * 2);
-    } else if (op == OP_ATTN_DECODE) {
-      const int b = __ldg(dg + F_A0), g = __ldg(dg + F_A0 + 1), j = __ldg(dg + F_A0 + 2);
-      if (b >= p.B) return;
-      const int s = __ldg(p.seq_lens + b);
-      const bool full = p.window == 0 || (l + 1) % p.full_period == 0;
-      const int lo = full ? 0 : max(0, s - p.window);
-      const int jj = lo / p.split_len + j;
-      prefetch_pages(l, b, g, max(lo, jj * p.split_len), min(s, (jj + 1) * p.split_len));
-    } else if (op == OP_ATTN_DRAIN && __ldg(dg + F_A0 + 4) >= 0) {  // static claims: entries ci, ci + n, ...
-      const uint32_t n_cl = (uint32_t)__ldg(dg + F_A0 + 5);
-      for (uint32_t i = (uint32_t)__ldg(dg + F_A0 + 4);; i += n_cl) {
-        uint32_t acc = 0;
-        int b = 0, n = 0, s = 0;
-        for (; b < p.B; ++b) {
-          s = __ldg(p.seq_lens + b);
-          n = slices_of(p, s) * S::NKV;
-          if (i < acc + (uint32_t)n) break;
-          acc += (uint32_t)n;
-        }
-        if (b >= p.B || n_cl == 0) break;
-        const int r = (int)(i - acc), per = n / S::NKV;
-        const int t0 = (r - (r / per) * per) * p.split_len;
-        prefetch_pages(l, b, r / per, t0, min(s, t0 + p.split_len));
-      }
-    }
-  }
-  // K and V pages of positions [t0, t1) of row b, KV group g, layer l.
-  __device__ __forceinline__ void prefetch_pages(int l, int b, int g, int t0, int t1) {
-    if (t1 <= t0 || t0 < 0) return;
-    constexpr uint32_t kPage = S::P * S::D * 2;
-    for (int lp = t0 / S::P; lp <= (t1 - 1) / S::P && lp < p.max_pages; ++lp) {
-      const int page = __ldg(p.block_tables + (int64_t)b * p.max_pages + lp);
-      if (page < 0 || page >= p.num_pages) return;  // the ring's copy reports it
-      const int64_t off = (((int64_t)l * p.num_pages + page) * S::NKV + g) * S::P * S::D;
-      l2_prefetch(p.kpool + off, kPage);
-      l2_prefetch(p.vpool + off, kPage);
-    }
-  }
-
   __device__ __forceinline__ void run() {
     if ((threadIdx.x & 31) != 0) return;
     stream_policy = l2_evict_first_policy();
     const int n = p.sched[2 * c.sm + 1];
-    const int32_t* list = p.sched + p.sched[2 * c.sm];
-    int pf_next = 1;  // the next task whose inputs are prefetched into L2
     Hdr* H = c.hdr;
     bool ok = true;
     for (int i = 0; i < n && ok; ++i) {
-      if (p.l2_lookahead > 0)
-        for (const int hi = min(n - 1, i + p.l2_lookahead); pf_next <= hi; ++pf_next) prefetch_task(list + 32 * pf_next);
       const int slot = i % kDescRing;
       if (!mbar_wait(p, c, &H->dfull[slot], (i / kDescRing) & 1)) {
         ok = false;
@@ -1875,6 +1806,15 @@ struct Consumer {
     // the row's new position (tabulated for the step at batch <= kTB)
     const int pos = b < p.B ? (p.B <= kTB ? sm.row_pos[b] : __ldg(p.seq_lens + b) - 1) : -1;
     const int qg = lane >> 2, qc = lane & 3;  // MMA fragment coordinates
+    // The new token's K/V (written by the QKV tiles after the pool page was
+    // read) replace its slot below; the slice that holds it loads them now,
+    // in the same round as the queries.
+    const bool has_new = pos >= t0 && pos < t1 && np > 0;
+    uint4 kvn = make_uint4(0u, 0u, 0u, 0u);
+    if (has_new && ct < 2 * D / 8) {
+      const int which = ct / (D / 8), cc = ct % (D / 8);
+      kvn = __ldcg(reinterpret_cast<const uint4*>(p.kvnew + (((int64_t)b * 2 + which) * S::NKV + g) * D) + cc);
+    }
     // the group's queries, scaled by log2(e)/sqrt(D), split into BF16 hi + lo,
     // kept while (layer, b, g) repeats
     if (np > 0 && !(sm.qtag[0] == l && sm.qtag[1] == b && sm.qtag[2] == g)) {
@@ -1913,13 +1853,12 @@ struct Consumer {
       const uint32_t kb = smem_u32(page), vb = kb + (uint32_t)(NT * P * 128);
       const int page_t0 = (pf + k) * P;
       // the new token's K/V replace its slot: the pool page may predate the write
-      if (pos >= page_t0 && pos < page_t0 + P && pos >= t0 && pos < t1) {
+      if (has_new && pos >= page_t0 && pos < page_t0 + P) {
         const int sl = pos - page_t0;
         if (ok && ct < 2 * D / 8) {
           const int which = ct / (D / 8), cc = ct % (D / 8);
-          const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p.kvnew + (((int64_t)b * 2 + which) * S::NKV + g) * D) + cc);
           const uint32_t a = kv_addr(which ? vb : kb, sl, cc);
-          *reinterpret_cast<uint4*>(page + (a - kb)) = v;
+          *reinterpret_cast<uint4*>(page + (a - kb)) = kvn;
           fence_proxy_async_smem();
         }
         consumers_sync();
@@ -2131,47 +2070,96 @@ struct Consumer {
   }
 
   // Head h of (b, g) merged over the slices, by one warp: lane holds dims
-  // [lane * DPL, lane * DPL + DPL).
+  // [lane * DPL, lane * DPL + DPL).  The merge is on the path from the last
+  // KV slice to the O projection, so its loads go out in as few rounds as
+  // registers allow: every slice's (max, sum) together with the first CB
+  // slices' partial outputs, then CB more slices per round.  The arithmetic
+  // is the plain definition in slice order: the global max over the slices,
+  // then acc = sum_j 2^(m_j - max) o_j and z = sum_j 2^(m_j - max) l_j.
   template <int DPL>
   __device__ __forceinline__ void combine_head(int l, int b, int g, int h, float (&out)[DPL]) {
-    constexpr int G = S::G, D = S::D;
+    constexpr int G = S::G, D = S::D, MAXC = 4, CB = 16;
     static_assert(DPL == D / 32, "lane dims");
     const bool full = p.window == 0 || (l + 1) % p.full_period == 0;
     const int n = min(full ? slices_of(p, __ldg(p.seq_lens + b)) : p.n_static, p.max_slots);
     const int64_t base = ((int64_t)b * S::NKV + g) * p.max_slots;
-    float mx = -INFINITY;
-    for (int j = lane; j < n; j += 32) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((base + j) * G + h) * 2));
-      if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
-    }
-    mx = warp_max(mx);
-    float z = 0.f, acc[DPL];
+    auto load_o = [&](int j, float (&o)[DPL]) {
+      const float* oj = p.part_o + ((base + j) * G + h) * D + lane * DPL;
+      if constexpr (DPL == 4) {
+        const float4 o4 = __ldcg(reinterpret_cast<const float4*>(oj));
+        o[0] = o4.x; o[1 % DPL] = o4.y; o[2 % DPL] = o4.z; o[3 % DPL] = o4.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) o[i] = __ldcg(oj + i);
+      }
+    };
+    float acc[DPL];
 #pragma unroll
     for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
-    for (int j0 = 0; j0 < n; j0 += 32) {
-      // lane jj: the coefficient of slice j0 + jj
-      float cj = 0.f;
-      if (j0 + lane < n) {
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((base + j0 + lane) * G + h) * 2));
-        if (ml.y > 0.f) {
-          cj = exp2f(ml.x - mx);
-          z = fmaf(cj, ml.y, z);
+    float z = 0.f, mx = -INFINITY;
+    if (n <= 32 * MAXC) {
+      // round 1: the (max, sum) of slices lane + 32k and the first CB slices' outputs
+      float2 ml[MAXC];
+#pragma unroll
+      for (int k = 0; k < MAXC; ++k) {
+        const int j = lane + 32 * k;
+        ml[k] = j < n ? __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((base + j) * G + h) * 2))
+                      : make_float2(0.f, 0.f);
+      }
+      float o[CB][DPL];
+#pragma unroll
+      for (int k = 0; k < CB; ++k) load_o(min(k, n - 1), o[k]);
+#pragma unroll
+      for (int k = 0; k < MAXC; ++k)
+        if (ml[k].y > 0.f) mx = fmaxf(mx, ml[k].x);
+      mx = warp_max(mx);
+      float cj[MAXC];
+#pragma unroll
+      for (int k = 0; k < MAXC; ++k) {
+        cj[k] = ml[k].y > 0.f ? exp2f(ml[k].x - mx) : 0.f;
+        z = fmaf(cj[k], ml[k].y, z);
+      }
+      static_assert(32 % CB == 0, "a round of slices lies in one register of cj");
+      for (int j0 = 0; j0 < n; j0 += CB) {
+        if (j0 > 0)  // the next round of CB slices
+#pragma unroll
+          for (int k = 0; k < CB; ++k) load_o(min(j0 + k, n - 1), o[k]);
+        // slice j's coefficient sits in lane j % 32, register j / 32
+        float cr = cj[0];
+#pragma unroll
+        for (int q = 1; q < MAXC; ++q)
+          if (q == (j0 >> 5)) cr = cj[q];
+#pragma unroll
+        for (int k = 0; k < CB; ++k) {
+          const float c = __shfl_sync(FULL, cr, (j0 + k) & 31);
+          if (j0 + k < n)
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) acc[i] = fmaf(c, o[k][i], acc[i]);
         }
       }
-      const int cnt = min(32, n - j0);
-#pragma unroll 8
-      for (int jj = 0; jj < cnt; ++jj) {
-        const float cb = __shfl_sync(FULL, cj, jj);
-        const float* oj = p.part_o + ((base + j0 + jj) * G + h) * D + lane * DPL;
-        if (DPL == 4) {
-          const float4 o4 = __ldcg(reinterpret_cast<const float4*>(oj));
-          acc[0] = fmaf(cb, o4.x, acc[0]);
-          acc[1] = fmaf(cb, o4.y, acc[1]);
-          acc[2 % DPL] = fmaf(cb, o4.z, acc[2 % DPL]);
-          acc[3 % DPL] = fmaf(cb, o4.w, acc[3 % DPL]);
-        } else {
+    } else {
+      // many slices: the max first, then the slices in order, one at a time
+      for (int j = lane; j < n; j += 32) {
+        const float2 m2 = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((base + j) * G + h) * 2));
+        if (m2.y > 0.f) mx = fmaxf(mx, m2.x);
+      }
+      mx = warp_max(mx);
+      for (int j0 = 0; j0 < n; j0 += 32) {
+        float c = 0.f;
+        if (j0 + lane < n) {
+          const float2 m2 = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((base + j0 + lane) * G + h) * 2));
+          if (m2.y > 0.f) {
+            c = exp2f(m2.x - mx);
+            z = fmaf(c, m2.y, z);
+          }
+        }
+        const int cnt = min(32, n - j0);
+        for (int jj = 0; jj < cnt; ++jj) {
+          const float cb = __shfl_sync(FULL, c, jj);
+          float o[DPL];
+          load_o(j0 + jj, o);
 #pragma unroll
-          for (int i = 0; i < DPL; ++i) acc[i] = fmaf(cb, __ldcg(oj + i), acc[i]);
+          for (int i = 0; i < DPL; ++i) acc[i] = fmaf(cb, o[i], acc[i]);
         }
       }
     }
@@ -2265,20 +2253,35 @@ struct Consumer {
     return 1.f / sqrtf(tot / (float)S::H + p.eps);
   }
 
+  // This thread's float4s of a gain row (issued before the residual parts
+  // are loaded, so that both arrive in the same round).
+  template <int PER>
+  __device__ __forceinline__ void load_gain(const float* gamma, float4 (&gm)[PER]) {
+    constexpr int H4 = S::H / 4;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int i4 = ct + k * kConsumerThreads;
+      gm[k] = (H4 % kConsumerThreads == 0 || i4 < H4) ? __ldg(reinterpret_cast<const float4*>(gamma) + i4)
+                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+
   __device__ __forceinline__ void norm(const int32_t* w) {
     constexpr int H4 = S::H / 4, PER = (H4 + kConsumerThreads - 1) / kConsumerThreads;
     const int l = w[F_LAYER], b1 = min(w[F_A0 + 1], p.B);
     const bool final_norm = w[F_A0 + 2] != 0, fused = w[F_A0 + 3] != 0;
+    // the gain row is loaded with the residual parts (one round of loads)
+    float4 gms[PER];
+    load_gain<PER>(final_norm ? p.gamma_f : p.gamma + (int64_t)l * S::H, gms);
     for (int b = w[F_A0]; b < b1; ++b) {
       float4 v[PER];
       const float inv_rms = resid_row<PER>(w, l, b, fused, v);
-      const float4* gam = reinterpret_cast<const float4*>(final_norm ? p.gamma_f : p.gamma + (int64_t)l * S::H);
       float4* hout = reinterpret_cast<float4*>(p.h + ((int64_t)(l & 1) * p.MB + b) * S::H);
 #pragma unroll
       for (int k = 0; k < PER; ++k) {
         const int i4 = ct + k * kConsumerThreads;
         if (H4 % kConsumerThreads == 0 || i4 < H4) {
-          const float4 gm = __ldg(gam + i4), a = v[k];
+          const float4 gm = gms[k], a = v[k];
           reinterpret_cast<float4*>(p.x + (int64_t)b * S::H)[i4] =
               make_float4(a.x * inv_rms * gm.x, a.y * inv_rms * gm.y, a.z * inv_rms * gm.z, a.w * inv_rms * gm.w);
           if (!final_norm) hout[i4] = a;
@@ -2297,15 +2300,16 @@ struct Consumer {
     // a previous item of this SM left the same rows (uniform, as for the combine)
     if (sm.xtag[0] == 1 && sm.xtag[1] == 0 && sm.xtag[2] == 0 && sm.xtag[3] == l) return;
     float4* xs4 = reinterpret_cast<float4*>(sm.xs);
+    float4 gms[PER];
+    load_gain<PER>(p.gamma + (int64_t)l * S::H, gms);
     for (int b = 0; b < p.B; ++b) {
       float4 v[PER];
       const float inv_rms = resid_row<PER>(w, l, b, true, v);
-      const float4* gam = reinterpret_cast<const float4*>(p.gamma + (int64_t)l * S::H);
 #pragma unroll
       for (int k = 0; k < PER; ++k) {
         const int i4 = ct + k * kConsumerThreads;
         if (H4 % kConsumerThreads == 0 || i4 < H4) {
-          const float4 gm = __ldg(gam + i4), a = v[k];
+          const float4 gm = gms[k], a = v[k];
           // float4 i4 of the row goes to [half i4 % 2][chunk i4 / 2], as load_x places it
           xs4[b * H4 + (i4 & 1) * (H4 / 2) + (i4 >> 1)] =
               make_float4(a.x * inv_rms * gm.x, a.y * inv_rms * gm.y, a.z * inv_rms * gm.z, a.w * inv_rms * gm.w);

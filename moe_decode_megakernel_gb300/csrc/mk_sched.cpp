@@ -1033,10 +1033,6 @@ int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const 
     delete s;
     return fail(MK_ERR_ARG, "unknown placement");
   }
-  if (s->opts.l2_lookahead < 0 || s->opts.l2_lookahead > 64) {
-    delete s;
-    return fail(MK_ERR_ARG, "l2_lookahead must be in [0, 64]");
-  }
   s->watchdog_ns = (int64_t)(s->opts.watchdog_ms > 0 ? s->opts.watchdog_ms : 2000) * 1000000;
   int rc = build(s);
   if (rc == MK_OK) rc = validate(s);
