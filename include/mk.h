@@ -161,7 +161,18 @@ typedef struct {
   int32_t placement;        /* 0 (default): task k of the flattened waves runs on SM k mod
                                num_sms; 1: greedy, each layer's tasks in order go to the SM
                                where a cost model (typical ready and busy time per op, a
-                               claimer's static unit count) says they finish first */
+                               claimer's static unit count) says they finish first;
+                               2: split, the attention branch (QKV, attention slices and
+                               claimers, merges, O-proj) round robin over SMs [0, attn_sms)
+                               and the MoE branch (RMSNorm, router, routing, MoE drains) over
+                               the others, so neither branch queues behind the other; the LM
+                               head over all SMs; 3: dependency affinity ("Task scheduler"),
+                               each task to the least loaded SM that ran a task it waits on,
+                               within a per-layer cap of the layer's tasks per SM (rounded
+                               up), else to the least loaded SM */
+  int32_t attn_sms;         /* placement 2: SMs of the attention branch; 0 = in proportion
+                               to the branch's bytes per layer (QKV, O-proj and KV against
+                               router and experts) */
   int32_t trace_queue;      /* 1: keep every layer's MoE work queue in the workspace
                                ("queue_trace", see mk_workspace_offset) */
 } mk_sched_opts;

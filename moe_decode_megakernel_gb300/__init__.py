@@ -53,7 +53,7 @@ class MkSchedOpts(ctypes.Structure):
                                               "fuse_moe_combine", "explicit_gather",
                                               "trace_hidden", "watchdog_ms", "trace", "moe_queue", "moe_static",
                                               "fuse_routing", "fuse_norm_qkv", "attn_static", "moe_balance",
-                                              "combine_per_head", "placement", "trace_queue")]
+                                              "combine_per_head", "placement", "attn_sms", "trace_queue")]
 
 
 _lib = None

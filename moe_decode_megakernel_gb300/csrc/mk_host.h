@@ -85,6 +85,7 @@ void set_error(const std::string& msg);
 int fail(int code, const std::string& msg);
 int attn_slices(const mk_sched* s, int seq_len);  // KV slices of a full-attention row
 int query_num_sms();                              // SMs of the current device, -1 without one
+int attn_group_sms(const mk_sched* s);            // SMs of the attention branch (split placement)
 bool is_full_layer(const mk_config& c, int l);
 // mk_check_step on a host copy of the step's error record (8 words at the
 // workspace's "error" offset); the workspace and stream serve the stall

@@ -94,7 +94,11 @@ def test_schedules_validate_and_simulate(workload, order):
                                   dict(fuse_norm_qkv=0, fuse_routing=0), dict(combine_per_head=1),
                                   dict(attn_static=0), dict(attn_static=0, attn_claimers=3),
                                   dict(moe_balance=1), dict(placement=1), dict(placement=1, wave_order=1),
-                                  dict(placement=1, moe_static=0), dict(placement=1, moe_claimers=5)])
+                                  dict(placement=1, moe_static=0), dict(placement=1, moe_claimers=5),
+                                  dict(placement=2), dict(placement=2, attn_sms=20),
+                                  dict(placement=2, wave_order=2), dict(placement=2, moe_static=0),
+                                  dict(placement=3), dict(placement=3, wave_order=1),
+                                  dict(placement=3, moe_static=0), dict(placement=3, fuse_norm_qkv=0)])
 def test_schedule_variants(opts):
     m, s, inp = sched_for("small", **opts)
     s.validate()
@@ -291,3 +295,67 @@ def test_queue_trace_region_size():
         assert s.workspace_bytes() - off >= sh.n_layers * stride * 4
         assert s.workspace_bytes() - off < sh.n_layers * stride * 4 + 256
         assert mk.Sched(model, B, 8192, mk.default_sched_opts(num_sms=NUM_SMS)).workspace_offset("queue_trace") == -1
+
+
+@pytest.mark.parametrize("workload", ["full_bs1_8k", "batch32_ragged", "long_256k"])
+def test_split_placement_keeps_branches_apart(workload):
+    """placement 2: every attention-branch task on SMs [0, attn_sms), every
+    MoE-branch task on the others, the LM head over all SMs; the lists
+    validate and simulate."""
+    w = synth.WORKLOADS[workload]
+    for attn_sms in (0, 48):
+        m, s, inp = sched_for(workload, placement=2, attn_sms=attn_sms)
+        s.validate()
+        s.simulate(inp.seq_lens, seed=2)
+        attn_ops = {2, 3, 7, 8, 9}
+        moe_ops = {1, 10, 11, 12, 13, 14, 15, 16}
+        na = None
+        lm_sms = set()
+        for sm in range(s.num_sms):
+            for i in range(s.num_tasks(sm)):
+                op, l = int(s.get_task(sm, i)[0]), int(s.get_task(sm, i)[1])
+                if op == 6:
+                    lm_sms.add(sm)
+                elif op in attn_ops:
+                    na = sm if na is None else max(na, sm)
+        assert len(lm_sms) == s.num_sms
+        na += 1
+        if attn_sms:
+            assert na == attn_sms
+        for sm in range(s.num_sms):
+            for i in range(s.num_tasks(sm)):
+                op, l = int(s.get_task(sm, i)[0]), int(s.get_task(sm, i)[1])
+                if l < w.shape.n_layers:
+                    assert (op in attn_ops) == (sm < na), (sm, op, l)
+                    assert op in attn_ops or op in moe_ops
+
+
+def test_affinity_placement_follows_producers():
+    """placement 3: an attention slice of a sliding layer runs on an SM that
+    ran one of its KV group's QKV tiles whenever that SM has room, no SM holds
+    more than the per-layer cap, and the lists validate and simulate on the
+    full shape."""
+    m, s, inp = sched_for("full_bs1_8k", placement=3)
+    s.validate()
+    s.simulate(inp.seq_lens, seed=3)
+    by_layer = {}
+    for sm in range(s.num_sms):
+        for i in range(s.num_tasks(sm)):
+            d = s.get_task(sm, i)
+            by_layer.setdefault(int(d[1]), []).append((sm, d))
+    colocated = total = 0
+    for l, items in by_layer.items():
+        cap = -(-len(items) // s.num_sms)
+        counts = np.bincount([sm for sm, _ in items], minlength=s.num_sms)
+        assert counts.max() <= cap, (l, counts.max(), cap)
+        if l >= 48 or synth.MODELS["full"].is_full_layer(l):
+            continue
+        qkv_sms = {}
+        for sm, d in items:
+            if int(d[0]) == 2:  # QKV tile: signals the group's QKV barrier
+                qkv_sms.setdefault(int(d[6]), set()).add(sm)
+        for sm, d in items:
+            if int(d[0]) == 7:  # a static slice waits on its group's QKV barrier
+                total += 1
+                colocated += sm in qkv_sms.get(int(d[2]), set())
+    assert total > 0 and colocated >= 0.9 * total, (colocated, total)

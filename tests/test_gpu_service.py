@@ -138,3 +138,100 @@ def _manual_forced(model, prompt, first, appended, n_more, pages):
             feed.append(t)
             feed += forced_after.pop(len(out), [])
     return out
+
+
+def _host_pools(shape, seed, num_pages):
+    """The generator's K and V pools as BF16 bits, the same values the device
+    pools start from."""
+    per = num_pages * shape.n_kv * shape.page_size * shape.head_dim
+    dims = (shape.n_layers, num_pages, shape.n_kv, shape.page_size, shape.head_dim)
+    k = synth.fill_host(shape.n_layers, per, seed, synth.KPOOL, vary_layer=True, sigma=shape.kv_sigma)
+    v = synth.fill_host(shape.n_layers, per, seed, synth.VPOOL, vary_layer=True, sigma=shape.kv_sigma)
+    return k.reshape(dims).copy(), v.reshape(dims).copy()
+
+
+@pytest.mark.parametrize("name,num_pages,max_pages", [("tiny", 24, 8), ("small", 12, 4)])
+def test_service_matches_oracle_over_many_steps(name, num_pages, max_pages):
+    """The GPU decode service over 40+ steps (two sequences batched, prompts
+    fed token by token, greedy samples, one sequence parked for two steps and
+    resumed with appended tokens) against the CPU oracle replaying each
+    sequence over its own KV pool: every sample equals the oracle's greedy
+    token (teacher-forced with the GPU's samples; a near-tie within the logit
+    tolerance may go either way), and the K/V the GPU wrote at every position
+    of every layer equal the oracle's: each head's vector within the logits'
+    tolerance of its largest entry (later positions depend on the history,
+    where single BF16 roundings may go the other way), most entries
+    bit-equal."""
+    import oracle
+    import parity
+    sh, seed = synth.MODELS[name], 37
+    w = synth.device.device_weights(sh, seed)
+    model = mk.Model(mk.config_from(sh), mk.weights_from(w), keepalive=w)
+    kp, vp = synth.device.device_pools(sh, seed, num_pages)
+    ctx = max_pages * sh.page_size
+    gstep = sv.GpuStep(model, [mk.Sched(model, 1, ctx), mk.Sched(model, 2, ctx)], kp, vp, max_pages)
+    svc = sv.Service(num_pages, sh.page_size, max_pages, 2, gstep)
+    rng = np.random.default_rng(11)
+    prompts = {1: rng.integers(0, sh.vocab, 9).tolist(), 2: rng.integers(0, sh.vocab, 21).tolist()}
+    appended = [7, 8]
+    svc.add(1, prompts[1], max_new=30)
+    svc.add(2, prompts[2], max_new=20)
+    pages, out, steps = {}, {1: [], 2: []}, 0
+    parked_at = None
+    while True:
+        for sid in (1, 2):
+            if svc.query(sid).state != sv.FINISHED:
+                pages[sid] = svc.pages(sid)
+        rows, toks = svc.step()
+        if rows:
+            steps += 1
+        for sid, t in toks:
+            out[sid].append(t)
+        if parked_at is None and len(out[1]) == 5:
+            svc.park(1)
+            parked_at = steps
+        elif parked_at is not None and parked_at > 0 and (steps >= parked_at + 2 or rows == 0):
+            svc.resume(1, appended)
+            parked_at = -1
+        if rows == 0 and parked_at == -1:
+            break
+    assert steps >= 32 and len(out[1]) == 30 and len(out[2]) == 20
+    torch.cuda.synchronize()
+    kg, vg = kp.cpu().numpy(), vp.cpu().numpy()
+    P = sh.page_size
+    exact = total = 0
+    kv_worst = 0.0
+    for sid in (1, 2):
+        ko, vo = _host_pools(sh, seed, num_pages)
+        bt = np.full((1, max_pages), -1, np.int32)
+        bt[0, :len(pages[sid])] = pages[sid]
+        feed, n_ctx, k = list(prompts[sid]), 0, 0
+        forced_after = {5: list(appended)} if sid == 1 else {}
+        while k < len(out[sid]):
+            tok = feed.pop(0)
+            r = oracle.decode_step(sh, seed, np.array([tok], np.int32), np.array([n_ctx + 1], np.int32), bt,
+                                   pools=(ko, vo))
+            n_ctx += 1
+            if not feed:  # this position produced sample k
+                g_tok, o = out[sid][k], r.logits[0]
+                oa = int(np.argmax(o))
+                exact += g_tok == oa
+                total += 1
+                assert g_tok == oa or o[oa] - o[g_tok] <= 2 * parity.LOGIT_TOL * np.max(np.abs(o)), (sid, k)
+                k += 1
+                feed.append(g_tok)
+                feed += forced_after.pop(k, [])
+        # what the GPU wrote at every position of this sequence
+        pos = np.arange(n_ctx)
+        pg, off = bt[0, pos // P], pos % P
+        for gpool, opool in ((kg, ko), (vg, vo)):
+            gv = synth.bf16_bits_to_f32(gpool[:, pg, :, off, :])  # [position][layer][head][d]
+            ov = synth.bf16_bits_to_f32(opool[:, pg, :, off, :])
+            # each head's vector within the logits' tolerance of its largest entry
+            err = np.max(np.abs(gv - ov), axis=-1) / np.max(np.abs(ov), axis=-1)
+            kv_worst = max(kv_worst, float(err.max()))
+            same = np.mean(gv == ov)
+            assert err.max() <= parity.LOGIT_TOL, (sid, float(err.max()))
+            assert same >= 0.9, same  # most entries round to the same BF16 value
+    print(f"{name}: {steps} service steps, greedy agreement {exact}/{total}, worst K/V error {kv_worst:.2e}")
+    assert exact >= 0.99 * total
