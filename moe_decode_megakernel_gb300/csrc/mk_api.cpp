@@ -42,7 +42,8 @@ int query_num_sms() {
   int launch_##name##_2(const Params& p, int grid, cudaStream_t s); \
   int launch_##name##_3(const Params& p, int grid, cudaStream_t s); \
   int launch_##name##_4(const Params& p, int grid, cudaStream_t s); \
-  int launch_##name##_5(const Params& p, int grid, cudaStream_t s);
+  int launch_##name##_5(const Params& p, int grid, cudaStream_t s); \
+  int launch_##name##_6(const Params& p, int grid, cudaStream_t s);
 MK_DECLARE_SHAPE(tiny)
 MK_DECLARE_SHAPE(small)
 MK_DECLARE_SHAPE(dense)
@@ -57,11 +58,11 @@ struct CompiledShape {
 };
 
 const CompiledShape kShapes[] = {
-    {{256, 4, 2, 64, 16, 4, 128, 16}, {launch_tiny_0, launch_tiny_1, launch_tiny_2, launch_tiny_3, launch_tiny_4, launch_tiny_5}},
-    {{1024, 16, 2, 64, 32, 4, 512, 64}, {launch_small_0, launch_small_1, launch_small_2, launch_small_3, launch_small_4, launch_small_5}},
+    {{256, 4, 2, 64, 16, 4, 128, 16}, {launch_tiny_0, launch_tiny_1, launch_tiny_2, launch_tiny_3, launch_tiny_4, launch_tiny_5, launch_tiny_6}},
+    {{1024, 16, 2, 64, 32, 4, 512, 64}, {launch_small_0, launch_small_1, launch_small_2, launch_small_3, launch_small_4, launch_small_5, launch_small_6}},
     // dense SwiGLU FFN (one expert, top-1)
-    {{1024, 16, 2, 64, 1, 1, 2048, 64}, {launch_dense_0, launch_dense_1, launch_dense_2, launch_dense_3, launch_dense_4, launch_dense_5}},
-    {{2048, 32, 4, 128, 128, 8, 768, 64}, {launch_full_0, launch_full_1, launch_full_2, launch_full_3, launch_full_4, launch_full_5}},
+    {{1024, 16, 2, 64, 1, 1, 2048, 64}, {launch_dense_0, launch_dense_1, launch_dense_2, launch_dense_3, launch_dense_4, launch_dense_5, launch_dense_6}},
+    {{2048, 32, 4, 128, 128, 8, 768, 64}, {launch_full_0, launch_full_1, launch_full_2, launch_full_3, launch_full_4, launch_full_5, launch_full_6}},
 };
 
 int cuda_fail(cudaError_t e, const char* what) {
@@ -103,6 +104,61 @@ int encode_pool(CUtensorMap* tm, void* pool, const mk_sched* s, int64_t num_page
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
   return MK_OK;
+}
+
+// A row-major BF16 matrix [rows][cols] as a 2-D tensor for the tcgen05
+// items: boxes of kTcK columns (128 bytes) by box_rows rows, swizzled in
+// 128-byte rows (the K-major operand layout the MMA descriptors name).
+int encode_operand(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                   const char* what) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  if (!base || rows >= (1ull << 31) || cols % kTcK != 0)
+    return fail(MK_ERR_ARG, std::string("no tcgen05 operand layout for ") + what);
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kTcK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MK_ERR_CUDA, std::string("cuTensorMapEncodeTiled failed for ") + what + " (" + std::to_string((int)r) + ")");
+  return MK_OK;
+}
+
+// The weights as tcgen05 A operands: boxes of kTcRows rows (the gate and up
+// matrices in blocks of 16 rows: an up/gate tile interleaves them; the
+// router in boxes of its tasks' kTcRouterRows rows).
+int encode_weight_maps(mk_model* m) {
+  if (m->tm_ready) return MK_OK;
+  const mk_config& c = m->cfg;
+  const ShapeDims& D = m->dims;
+  const uint64_t L = (uint64_t)c.n_layers, QKV = (uint64_t)(D.NQ + 2 * D.NKV) * D.D;
+  const mk_weights& w = m->w;
+  int rc = encode_operand(&m->tm_w[0], w.w_qkv, L * QKV, D.H, kTcRows, "w_qkv");
+  if (rc == MK_OK) rc = encode_operand(&m->tm_w[1], w.w_o, L * D.H, (uint64_t)D.NQ * D.D, kTcRows, "w_o");
+  if (rc == MK_OK) rc = encode_operand(&m->tm_w[2], w.w_router, L * D.E, D.H, kTcRouterRows, "w_router");
+  if (rc == MK_OK) rc = encode_operand(&m->tm_w[3], w.w_lm, (uint64_t)c.vocab, D.H, kTcRows, "w_lm");
+  if (rc == MK_OK) rc = encode_operand(&m->tm_w[4], w.w_gate, L * D.E * D.I, D.H, 16, "w_gate");
+  if (rc == MK_OK) rc = encode_operand(&m->tm_w[5], w.w_up, L * D.E * D.I, D.H, 16, "w_up");
+  if (rc == MK_OK) rc = encode_operand(&m->tm_w[6], w.w_down, L * D.E * D.H, D.I, kTcRows, "w_down");
+  if (rc == MK_OK) m->tm_ready = true;
+  return rc;
+}
+
+// The activation operands of the tcgen05 items in the workspace: boxes of
+// tc_nb rows (every activation row as a hi row and a lo row).
+int encode_act_maps(mk_sched* s, uint8_t* ws) {
+  if (s->tm_ws == ws) return MK_OK;
+  const ShapeDims& D = s->dims;
+  const uint64_t nb = (uint64_t)s->tc_nb, routed = std::max<uint64_t>(2ull * s->max_batch * D.K, nb);
+  int rc = encode_operand(&s->tm_act[0], ws + s->ws.off("xb"), nb, D.H, s->tc_nb, "xb");
+  if (rc == MK_OK) rc = encode_operand(&s->tm_act[1], ws + s->ws.off("attnb"), nb, (uint64_t)D.NQ * D.D, s->tc_nb, "attnb");
+  if (rc == MK_OK) rc = encode_operand(&s->tm_act[2], ws + s->ws.off("xgb"), routed, D.H, s->tc_nb, "xgb");
+  if (rc == MK_OK) rc = encode_operand(&s->tm_act[3], ws + s->ws.off("ub"), routed, D.I, s->tc_nb, "ub");
+  s->tm_ws = rc == MK_OK ? ws : nullptr;
+  return rc;
 }
 
 // After a timeout: the counters as the step left them, against the schedule.
@@ -398,6 +454,19 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   }
   p.tm_k = s->tm_k;
   p.tm_v = s->tm_v;
+  if (s->tc) {
+    int rc = encode_weight_maps(m);
+    if (rc == MK_OK) rc = encode_act_maps(s, ws);
+    if (rc != MK_OK) return rc;
+    p.tm_wqkv = m->tm_w[0]; p.tm_wo = m->tm_w[1]; p.tm_wr = m->tm_w[2]; p.tm_wlm = m->tm_w[3];
+    p.tm_wg = m->tm_w[4]; p.tm_wu = m->tm_w[5]; p.tm_wd = m->tm_w[6];
+    p.tm_xb = s->tm_act[0]; p.tm_attnb = s->tm_act[1]; p.tm_xgb = s->tm_act[2]; p.tm_ub = s->tm_act[3];
+    p.xb = reinterpret_cast<uint16_t*>(at("xb"));
+    p.attnb = reinterpret_cast<uint16_t*>(at("attnb"));
+    p.xgb = reinterpret_cast<uint16_t*>(at("xgb"));
+    p.ub = reinterpret_cast<uint16_t*>(at("ub"));
+    p.tc_nb = s->tc_nb;
+  }
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // "Barriers": the counters are zeroed before each step (with the error record)
@@ -405,7 +474,8 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   cudaError_t e = cudaMemsetAsync(workspace, 0, zero_bytes, st);
   if (e != cudaSuccess) return cuda_fail(e, "barrier reset");
   // the kernel build for the model's expert format and the schedule's batch
-  const int mode = m->cfg.expert_fp4 ? (s->lean ? kModeFp4Lean : kModeFp4)
+  const int mode = s->tc               ? kModeTc
+                   : m->cfg.expert_fp4 ? (s->lean ? kModeFp4Lean : kModeFp4)
                    : m->cfg.expert_fp8 ? (s->lean ? kModeFp8Lean : kModeFp8)
                    : s->max_batch <= kTB && s->lean ? kModeSmallBatch : kModeAnyBatch;
   const int rc = kShapes[m->shape_id].launch[mode](p, s->num_sms, st);

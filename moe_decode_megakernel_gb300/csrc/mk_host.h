@@ -14,6 +14,9 @@ struct mk_model {
   int shape_id;  // index into the compiled shapes
   mk::ShapeDims dims;
   mk::MoePlan plan;
+  // tensor maps of the weights for tcgen05 items (made at the first step that needs them)
+  bool tm_ready = false;
+  CUtensorMap tm_w[7];  // w_qkv, w_o, w_router, w_lm, w_gate, w_up, w_down
 };
 
 namespace mk {
@@ -62,6 +65,13 @@ struct mk_sched {
   // the lean kernel build runs it: fused routing and MoE combine, merges a
   // warp per head, static separate claims (no task the lean build leaves out)
   bool lean = false;
+  // tcgen05 GEMM items (kModeTc): BF16 experts of an MoE model at max_batch >
+  // kTB; 128-row weight tiles, explicit gather, the BF16 hi/lo operand rows
+  bool tc = false;
+  int tc_nb = 0;  // rows of an activation operand box (2 max_batch, rounded up to 16)
+  // tensor maps of the activation operands, for the workspace they were made for
+  const void* tm_ws = nullptr;
+  CUtensorMap tm_act[4];
   int split_len = 0, n_static = 0, max_slots = 0, max_attn_entries = 0;
   int lm_bar = -1;
   int trace_cap = 0;

@@ -114,7 +114,8 @@ enum KernelMode : int {
   kModeFp4 = 3,         // FP4 experts (max_batch <= kTB), any schedule
   kModeFp8Lean = 4,     // FP8 experts, lean schedules
   kModeFp4Lean = 5,     // FP4 experts, lean schedules
-  kModeCount = 6
+  kModeTc = 6,          // BF16 experts, max_batch > kTB: GEMM items on the tcgen05 tensor cores
+  kModeCount = 7
 };
 #if defined(__CUDACC__)
 #define MK_HOST_DEVICE __host__ __device__
@@ -211,6 +212,43 @@ MK_HOST_DEVICE constexpr int queue_trace_stride(int E, int n_routed_max) {
   return (4 * E + (E + 1) + n_routed_max + 2 + 3) / 4 * 4;
 }
 
+// tcgen05 GEMM items (kModeTc): an item is one tile of kTcRows weight rows
+// (the M side of the MMA) over the whole K, streamed as k-blocks of kTcK
+// elements; a stage holds one k-block of the weight tile (kTcRows x kTcK
+// BF16, 16 KB) and of the activation operand (up to kTcMaxN rows: every
+// activation row as a BF16 hi row and lo row).
+constexpr int kTcRows = 128;
+constexpr int kTcK = 64;
+constexpr int kTcABytes = kTcRows * kTcK * 2;
+constexpr int kTcMaxN = (kStageBytes - kTcABytes) / (kTcK * 2);
+constexpr int kTcRouterRows = 16;  // rows of a router task (its weight box; the MMA's other rows unused)
+// k-blocks per stage of a tcgen05 item whose weight box holds a_bytes per
+// k-block: one for full tiles, up to 8 for a router task's small boxes (the
+// activation boxes of those k-blocks must fit the stage's second half).
+MK_HOST_DEVICE constexpr int tc_kblocks_per_stage(uint32_t a_bytes, int tc_nb) {
+  int k = a_bytes >= (uint32_t)kTcABytes ? 1 : (int)((uint32_t)kTcABytes / a_bytes);
+  const int kb_fit = (kStageBytes - kTcABytes) / (tc_nb * kTcK * 2);
+  k = k < kb_fit ? k : kb_fit;
+  return k < 1 ? 1 : (k > 8 ? 8 : k);
+}
+static_assert(kTcMaxN >= 2 * kMaxBatch, "hi/lo rows of the largest batch fit a stage");
+
+// The MoE plan of tcgen05 items: up/gate tiles of 64 gate rows and the same
+// 64 up rows (one M = 128 tile), down tiles of 128 rows; "stages" count
+// k-blocks.
+constexpr MoePlan moe_plan_tc(ShapeDims s) {
+  MoePlan p{};
+  p.up_half = kTcRows / 2;
+  p.up_stages = s.H / kTcK;
+  p.up_tile = kTcRows / 2;
+  p.up_tiles = s.I / p.up_tile;
+  p.dn_rows = kTcRows;
+  p.dn_stages = s.I / kTcK;
+  p.dn_tile = kTcRows;
+  p.dn_tiles = s.H / p.dn_tile;
+  return p;
+}
+
 // ------------------------------------------------------ kernel parameters
 struct Params {
   // the KV pools as 2-D tensors [L*pages*n_kv*P][d] for TMA tiles of
@@ -285,6 +323,19 @@ struct Params {
   uint64_t* trace;      // [num_sms][trace_cap][2] per work item, or null
   int trace_cap;
   uint64_t* stats;      // [num_sms][kStats] stall counters, or null
+
+  // tcgen05 items (kModeTc): 2-D tensor maps of the weights (boxes of kTcK
+  // columns by kTcRows rows, or kTcRows / 2 rows for the gate and up
+  // matrices, 128-byte swizzle) and of the activation operands (boxes of kTcK
+  // columns by tc_nb rows), and the operands themselves: every activation row
+  // r as BF16 rows 2r (hi = bf16(x)) and 2r + 1 (lo = bf16(x - hi))
+  CUtensorMap tm_wqkv, tm_wo, tm_wr, tm_wlm, tm_wg, tm_wu, tm_wd;
+  CUtensorMap tm_xb, tm_attnb, tm_xgb, tm_ub;
+  uint16_t* xb;         // [MB][2][H]      the layer input x (written by the RMSNorm)
+  uint16_t* attnb;      // [MB][2][NQ D]   the attention output (written by the merges)
+  uint16_t* xgb;        // [MB K][2][H]    the routed rows in expert order (written by MOE_GATHER)
+  uint16_t* ub;         // [MB K][2][I]    the SwiGLU activations (written by the up/gate tiles)
+  int tc_nb;            // rows of an activation box: 2 MB rounded up to 16 (the MMA's N)
 
   int split_len;        // tokens per KV slice
   int n_static;         // static slices per (row, group) of a sliding layer

@@ -176,6 +176,75 @@ __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* tm, int x, 
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(b)), "l"(policy)
       : "memory");
 }
+// ---- tcgen05: 5th-generation tensor cores with accumulators in tensor memory
+// TMEM columns of this CTA's accumulator (power of two, >= 32), allocated by
+// one warp; the TMEM address is written to shared memory.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T: BF16 operands (both K-major), fp32 accumulator.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// One arrival on `b` once every tcgen05 operation this thread issued before has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* b) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(b))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 16 consecutive fp32 columns of this thread's TMEM lane (the warp's quarter
+// of the lanes, as the warp's index in the CTA modulo 4 selects).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// Shared-memory matrix descriptor of a K-major operand tile written by TMA
+// with the 128-byte swizzle: rows of 128 bytes (64 BF16 of K) in atoms of 8
+// rows, 1024 bytes from one atom to the next along M/N; the tile starts on a
+// 1024-byte boundary.  Moving along K within the 128-byte row adds the byte
+// offset to the start address.
+__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4)   // start address, 16-byte units
+         | ((uint64_t)1 << 16)                 // leading-dimension offset (unused when swizzled)
+         | ((uint64_t)(1024 >> 4) << 32)       // stride-dimension offset: one 8-row atom
+         | ((uint64_t)1 << 46)                 // descriptor version
+         | ((uint64_t)2 << 61);                // 128-byte swizzle
+}
+// Instruction descriptor of kind::f16: fp32 D, BF16 A and B, both K-major, M x N.
+__host__ __device__ constexpr uint32_t tc_idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_2d_plain(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* b) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(b))
+      : "memory");
+}
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -258,6 +327,15 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
   hi = (uint32_t)ah | ((uint32_t)bh << 16);
   lo = (uint32_t)f_bf16(a - bf16_f(ah)) | ((uint32_t)f_bf16(b - bf16_f(bh)) << 16);
 }
+// Four consecutive activations as BF16 hi values (at hi) and lo values (at
+// lo): the operand rows of the tcgen05 items (8-byte stores).
+__device__ __forceinline__ void store_hilo4(uint16_t* hi, uint16_t* lo, float4 v) {
+  uint32_t h0, l0, h1, l1;
+  split_bf16x2(v.x, v.y, h0, l0);
+  split_bf16x2(v.z, v.w, h1, l1);
+  *reinterpret_cast<uint2*>(hi) = make_uint2(h0, h1);
+  *reinterpret_cast<uint2*>(lo) = make_uint2(l0, l1);
+}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(FULL, v, m);
@@ -281,8 +359,12 @@ struct Hdr {
   // FP8 expert stages: the fp32 scales of the stage's rows, copied with the
   // rows (same full barrier); up/gate stages hold gate scales then up scales
   alignas(16) float scl[kStages][kMaxStageRows];
+  // tcgen05 items: the accumulator is complete / every MMA has finished; the
+  // TMEM address of the accumulator
+  uint64_t acc_full, tc_drain;
+  uint32_t tmem_addr;
   volatile int32_t abort;
-  int32_t pad[31];
+  int32_t pad[28];
 };
 
 // the longest activation row a GEMV reads: hidden, intermediate (down
@@ -295,7 +377,7 @@ __host__ __device__ constexpr int xs_row() {
 // The MoE tile plan of a kernel mode's expert weights (BF16, FP8 or FP4 rows).
 template <class S, int M>
 __host__ __device__ constexpr MoePlan plan_of() {
-  return mode_fp4(M) ? S::mp4 : mode_fp8(M) ? S::mp8 : S::mp;
+  return M == kModeTc ? S::mptc : mode_fp4(M) ? S::mp4 : mode_fp8(M) ? S::mp8 : S::mp;
 }
 
 template <class S>
@@ -326,6 +408,7 @@ template <class S>
 constexpr size_t smem_bytes() {
   return (size_t)kStages * kStageBytes + sizeof(Hdr) + sizeof(Scratch<S>);
 }
+constexpr size_t kMaxSmemPerCta = 232448;  // 227 KB of dynamic shared memory per CTA
 
 // ---------------------------------------------------------------- shapes
 template <int H_, int NQ_, int NKV_, int D_, int E_, int K_, int I_, int P_>
@@ -337,6 +420,7 @@ struct Shape {
   static constexpr MoePlan mp = moe_plan(dims);
   static constexpr MoePlan mp8 = moe_plan8(dims);  // FP8 expert rows
   static constexpr MoePlan mp4 = moe_plan4(dims);  // FP4 expert rows
+  static constexpr MoePlan mptc = moe_plan_tc(dims);  // tcgen05 GEMM tiles
   static constexpr int SR_H = stage_rows(H), SR_O = stage_rows(G * D), SR_I = stage_rows(I);
   static_assert(H % 256 == 0 && (G * D) % 8 == 0 && I % 8 == 0, "row chunks");
   static_assert(D % 32 == 0 && 32 % G == 0 && (G * D) % 4 == 0, "attention lane maps");
@@ -570,7 +654,99 @@ struct Producer {
     return ntok > kTB ? (ntok + kTB - 1) / kTB : 1;
   }
 
+  // ---- tcgen05 items (kModeTc) ----
+  // The k-blocks of one item: per stage the weight box(es) of the item's
+  // kTcRows rows (a, at column ax + kTcK kb and row ay; an up/gate tile takes
+  // its 64 gate and 64 up rows in blocks of 16, gate block j then up block j,
+  // so that gate row i and up row i meet in one warp's TMEM lanes) and the
+  // activation box (b, rows by .. by + tc_nb).  The weight boxes need no
+  // input: they go out at once, as far as the ring reaches.  The activation
+  // rows are written by other SMs, so their boxes are copied only after the
+  // item's input counters are complete (then a proxy fence: the rows were
+  // written by ordinary stores, the copy reads through the async proxy).
+  // With a weight box of a_bytes < kTcABytes (a router task's rows), a stage
+  // takes kps = tc_kblocks_per_stage(a_bytes) k-blocks: weight box j at
+  // j * a_bytes, activation box j at kTcABytes + j * (its bytes).
+  __device__ __forceinline__ bool tc_stages(const int32_t* it, const CUtensorMap* ta, int ax, int ay, bool updown,
+                                            const CUtensorMap* tb, int bx, int by, int nkb,
+                                            uint32_t a_bytes = kTcABytes) {
+    const uint32_t bbytes = (uint32_t)p.tc_nb * kTcK * 2;
+    const int kps = tc_kblocks_per_stage(a_bytes, p.tc_nb);
+    const int nst = (nkb + kps - 1) / kps;
+    const uint32_t first = c.st;
+    bool ready = false;
+    auto issue_b = [&](uint32_t gs, int st) {
+      for (int j = 0; j < kps && st * kps + j < nkb; ++j) {
+        uint8_t* dst = stage(gs % kStages) + kTcABytes + j * bbytes;
+        tma_2d_plain(dst, tb, bx + (st * kps + j) * kTcK, by, &c.hdr->full[gs % kStages]);
+      }
+    };
+    auto wait_inputs = [&]() -> bool {
+      const int64_t t0 = p.stats ? gtimer() : 0;
+      const bool ok = wait_counters(p, c, it[F_WAIT0], (uint32_t)it[F_TGT0], it[F_WAIT1], (uint32_t)it[F_TGT1],
+                                    where_of(it));
+      if (p.stats) c.stat[1] += gtimer() - t0;
+      if (!ok) return false;
+      fence_proxy_async_global();
+      for (uint32_t gs = first; gs < c.st; ++gs) issue_b(gs, (int)(gs - first));
+      return true;
+    };
+    for (int st = 0; st < nst; ++st) {
+      // the next slot would be one of this item's own stages, still without its activations
+      if (!ready && c.st - first >= (uint32_t)kStages) {
+        if (!wait_inputs()) return false;
+        ready = true;
+      }
+      int slot;
+      if (!acquire_stage(slot)) return false;
+      uint64_t* fb = &c.hdr->full[slot];
+      uint8_t* dst = stage(slot);
+      const int nk = min(kps, nkb - st * kps);
+      mbar_expect_tx(fb, (uint32_t)nk * (a_bytes + bbytes));
+      for (int j = 0; j < nk; ++j) {
+        const int x = ax + (st * kps + j) * kTcK;
+        if (updown) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            tma_2d(dst + (2 * q) * (kTcABytes / 8), &p.tm_wg, x, ay + 16 * q, fb, stream_policy);
+            tma_2d(dst + (2 * q + 1) * (kTcABytes / 8), &p.tm_wu, x, ay + 16 * q, fb, stream_policy);
+          }
+        } else {
+          tma_2d(dst + j * a_bytes, ta, x, ay, fb, stream_policy);
+        }
+      }
+      if (ready) issue_b(c.st, st);
+      ++c.st;
+    }
+    return ready || wait_inputs();
+  }
+
+  // A dense GEMM task as one tcgen05 item: its rows (<= kTcRows) of the
+  // weight matrix against every activation row of the step.
+  __device__ __forceinline__ bool tc_dense(const int32_t* d) {
+    int32_t it[32];
+    for (int i = 0; i < 32; ++i) it[i] = d[i];
+    const int op = d[F_OP], l = d[F_LAYER], row0 = d[F_A0];
+    const CUtensorMap* ta;
+    const CUtensorMap* tb = &p.tm_xb;
+    int ax = 0, ay, bx = 0, nkb = S::H / kTcK;
+    uint32_t a_bytes = kTcABytes;  // a router task copies only its own rows (the MMA's other rows are unused)
+    switch (op) {
+      case OP_QKV_PROJ: ta = &p.tm_wqkv; ay = l * S::QKV + row0; break;
+      case OP_ROUTER_GEMM: ta = &p.tm_wr; ay = l * S::E + row0; a_bytes = kTcRouterRows * kTcK * 2; break;
+      case OP_LM_HEAD: ta = &p.tm_wlm; ay = row0; break;
+      default:  // OP_O_PROJ: the columns of KV group g
+        ta = &p.tm_wo; ay = l * S::H + row0; ax = bx = d[F_A0 + 2] * S::G * S::D; tb = &p.tm_attnb;
+        nkb = S::G * S::D / kTcK; break;
+    }
+    it[F_NSTAGE] = (nkb + tc_kblocks_per_stage(a_bytes, p.tc_nb) - 1) / tc_kblocks_per_stage(a_bytes, p.tc_nb);
+    it[F_A0 + 13] = nkb;
+    if (!push(it)) return false;
+    return tc_stages(it, ta, ax, ay, false, tb, bx, 0, nkb, a_bytes);
+  }
+
   __device__ __forceinline__ bool dense(const int32_t* d) {
+    if constexpr (M == kModeTc) return tc_dense(d);
     int32_t it[32];
     for (int i = 0; i < 32; ++i) it[i] = d[i];
     const int op = d[F_OP], l = d[F_LAYER], row0 = d[F_A0], rows = d[F_A0 + 1];
@@ -871,9 +1047,26 @@ struct Producer {
           carried = true;
         }
       }
-      if (!push(it)) return false;
-      for (int ps = gemv_passes(nrows); ps > 0; --ps)
-        if (!tile_stages(l, e, t, up)) return false;
+      if constexpr (M == kModeTc) {
+        // one item of nkb k-blocks: the expert's gate/up or down rows against
+        // its routed rows (their hi/lo rows start at row 2 row0)
+        const int64_t le = (int64_t)l * S::E + e;
+        it[F_NSTAGE] = up ? S::H / kTcK : S::I / kTcK;
+        it[F_A0 + 13] = it[F_NSTAGE];
+        if (!push(it)) return false;
+        if (up) {
+          if (!tc_stages(it, nullptr, 0, (int)(le * S::I + t * mp.up_tile), true, &p.tm_xgb, 0, 2 * row0,
+                         S::H / kTcK))
+            return false;
+        } else if (!tc_stages(it, &p.tm_wd, 0, (int)(le * S::H + t * mp.dn_tile), false, &p.tm_ub, 0, 2 * row0,
+                              S::I / kTcK)) {
+          return false;
+        }
+      } else {
+        if (!push(it)) return false;
+        for (int ps = gemv_passes(nrows); ps > 0; --ps)
+          if (!tile_stages(l, e, t, up)) return false;
+      }
       cur = nxt;
       if (cur < total) {
         if (stat) {
@@ -1086,6 +1279,8 @@ struct Consumer {
   Ctx c;
   Scratch<S>& sm;
   int ct, cw, lane;
+  uint32_t tmem = 0;       // kModeTc: TMEM address of the accumulator
+  uint32_t acc_phase = 0;  // kModeTc: parity of the accumulator's next completion
 
   // --- the stage ring
   __device__ __forceinline__ bool stage_wait(int& slot) {
@@ -1099,8 +1294,13 @@ struct Consumer {
   // Every read of a stage is an explicit shared-memory load (ld.shared,
   // ldmatrix), which the release orders before the arrival.
   __device__ __forceinline__ void stage_release(int slot) {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&c.hdr->empty[slot]);
+    if constexpr (M == kModeTc) {  // one arrival, after every consumer warp's reads
+      consumers_sync();
+      if (ct == 0) mbar_arrive(&c.hdr->empty[slot]);
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.hdr->empty[slot]);
+    }
     ++c.st;
   }
   __device__ __forceinline__ const uint8_t* stage(int slot) const { return c.stages + (size_t)slot * kStageBytes; }
@@ -1983,9 +2183,21 @@ struct Consumer {
     if (b >= p.B || cw >= G) return;
     float o[DPL];
     combine_head(l, b, g, cw, o);
-    float* dst = p.attn_out + (int64_t)b * S::NQ * D + (int64_t)(g * G + cw) * D + lane * DPL;
+    const int64_t col = (int64_t)(g * G + cw) * D + lane * DPL;
+    float* dst = p.attn_out + (int64_t)b * S::NQ * D + col;
 #pragma unroll
     for (int i = 0; i < DPL; ++i) dst[i] = o[i];
+    if constexpr (M == kModeTc && DPL == 4) {
+      store_hilo4(p.attnb + (int64_t)(2 * b) * S::NQ * D + col, p.attnb + (int64_t)(2 * b + 1) * S::NQ * D + col,
+                  make_float4(o[0], o[1 % DPL], o[2 % DPL], o[3 % DPL]));
+    } else if constexpr (M == kModeTc) {
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) {
+        const uint16_t hi = f_bf16(o[i]);
+        p.attnb[(int64_t)(2 * b) * S::NQ * D + col + i] = hi;
+        p.attnb[(int64_t)(2 * b + 1) * S::NQ * D + col + i] = f_bf16(o[i] - bf16_f(hi));
+      }
+    }
   }
 
   // Head h of (b, g) by the whole block (few rows: the merge is on the path
@@ -2065,7 +2277,14 @@ struct Consumer {
           zt = fmaf(sc, sm.red[k], zt);
           a = fmaf(sc, red[k * D + ct], a);
         }
-      p.attn_out[(int64_t)b * S::NQ * D + (int64_t)(g * G + h) * D + ct] = a / zt;
+      const float o = a / zt;
+      const int64_t col = (int64_t)(g * G + h) * D + ct;
+      p.attn_out[(int64_t)b * S::NQ * D + col] = o;
+      if constexpr (M == kModeTc) {
+        const uint16_t hi = f_bf16(o);
+        p.attnb[(int64_t)(2 * b) * S::NQ * D + col] = hi;
+        p.attnb[(int64_t)(2 * b + 1) * S::NQ * D + col] = f_bf16(o - bf16_f(hi));
+      }
     }
   }
 
@@ -2282,8 +2501,11 @@ struct Consumer {
         const int i4 = ct + k * kConsumerThreads;
         if (H4 % kConsumerThreads == 0 || i4 < H4) {
           const float4 gm = gms[k], a = v[k];
-          reinterpret_cast<float4*>(p.x + (int64_t)b * S::H)[i4] =
+          const float4 xv =
               make_float4(a.x * inv_rms * gm.x, a.y * inv_rms * gm.y, a.z * inv_rms * gm.z, a.w * inv_rms * gm.w);
+          reinterpret_cast<float4*>(p.x + (int64_t)b * S::H)[i4] = xv;
+          if constexpr (M == kModeTc)
+            store_hilo4(p.xb + (int64_t)(2 * b) * S::H + 4 * i4, p.xb + (int64_t)(2 * b + 1) * S::H + 4 * i4, xv);
           if (!final_norm) hout[i4] = a;
           if (p.htrace) reinterpret_cast<float4*>(p.htrace + ((int64_t)l * p.MB + b) * S::H)[i4] = a;
         }
@@ -2576,17 +2798,39 @@ struct Consumer {
     }
   }
 
-  // expert-ordered copy of the routed rows ("Tasks": MOE_GATHER)
+  // expert-ordered copy of the routed rows ("Tasks": MOE_GATHER): a warp per
+  // row, the warp's row indices read in one round, then each row in one
+  // round of 16-byte loads
   __device__ __forceinline__ void gather(const int32_t* w) {
-    constexpr int C = S::H / 4;
+    constexpr int C = S::H / 4, PL = (C + 31) / 32, RW = 4;  // float4 per lane, rows per warp and round
     const int r0 = w[F_A0], r1 = min(r0 + w[F_A0 + 1], p.B * S::K);
-    for (int i = ct; i < (r1 - r0) * C; i += kConsumerThreads) {
-      const int r = r0 + i / C, cc = i % C;
-      int pr = __ldcg(p.perm + r);
-      int b = pr / S::K;
-      if (pr < 0 || b >= p.B) b = 0;
-      reinterpret_cast<float4*>(p.xg + (int64_t)r * S::H)[cc] =
-          __ldcg(reinterpret_cast<const float4*>(p.x + (int64_t)b * S::H) + cc);
+    for (int rb = r0 + cw; rb < r1; rb += RW * kConsumerWarps) {
+      int src[RW];
+#pragma unroll
+      for (int k = 0; k < RW; ++k) {
+        const int r = rb + k * kConsumerWarps;
+        const int pr = r < r1 ? __ldcg(p.perm + r) : 0;
+        src[k] = (pr < 0 || pr / S::K >= p.B) ? 0 : pr / S::K;
+      }
+#pragma unroll 1
+      for (int k = 0; k < RW; ++k) {
+        const int r = rb + k * kConsumerWarps;
+        if (r >= r1) break;
+        const float4* x4 = reinterpret_cast<const float4*>(p.x + (int64_t)src[k] * S::H);
+        float4 xv[PL];
+#pragma unroll
+        for (int q = 0; q < PL; ++q)
+          if (C % 32 == 0 || lane + 32 * q < C) xv[q] = __ldcg(x4 + lane + 32 * q);
+#pragma unroll
+        for (int q = 0; q < PL; ++q) {
+          const int cc = lane + 32 * q;
+          if (C % 32 != 0 && cc >= C) continue;
+          if constexpr (M == kModeTc)  // the tcgen05 items read only the BF16 operand rows
+            store_hilo4(p.xgb + (int64_t)(2 * r) * S::H + 4 * cc, p.xgb + (int64_t)(2 * r + 1) * S::H + 4 * cc, xv[q]);
+          else
+            reinterpret_cast<float4*>(p.xg + (int64_t)r * S::H)[cc] = xv[q];
+        }
+      }
     }
   }
 
@@ -2607,7 +2851,211 @@ struct Consumer {
     }
   }
 
+  // ------------------------------------------------- tcgen05 GEMM items
+  // An item of kModeTc: its kTcRows weight rows (M) against the activation
+  // operand's tc_nb rows (N: every activation row as a hi row and a lo row),
+  // K in k-blocks of kTcK, one stage each.  One thread issues the MMAs of a
+  // stage as soon as its copies land, accumulating in TMEM (fp32), and hands
+  // the stage back through tcgen05.commit (the stage's empty barrier counts
+  // kConsumerWarps arrivals: one commit each).  A last commit marks the
+  // accumulator complete; then every consumer warp reads its quarter of the
+  // TMEM lanes (lane = weight row of the tile) for a share of the activation
+  // rows (columns 2t and 2t + 1 hold hi and lo: their sum is row t's value)
+  // and writes the outputs.  The next item's MMAs start after every warp has
+  // read the accumulator (a block barrier between tcgen05 fences).
+  __device__ __forceinline__ void tc_item(const int32_t* w) {
+    const int op = w[F_OP];
+    const int nst = w[F_NSTAGE], nkb = w[F_A0 + 13];
+    // a router task's stages hold several k-blocks of its small weight box
+    const uint32_t a_bytes = op == OP_ROUTER_GEMM ? kTcRouterRows * kTcK * 2 : kTcABytes;
+    const int kps = tc_kblocks_per_stage(a_bytes, p.tc_nb);
+    const uint32_t bbytes = (uint32_t)p.tc_nb * kTcK * 2;
+    if (ct == 0) {
+      tc_fence_after();
+      constexpr uint32_t kDescK = 16 * 2 / 16;  // one MMA's K (16 BF16 = 32 bytes) in descriptor units
+      const uint32_t idesc = tc_idesc_bf16(kTcRows, p.tc_nb);
+      for (int st = 0; st < nst; ++st) {
+        const uint32_t gs = c.st + (uint32_t)st;
+        const int slot = (int)(gs % kStages);
+        if (!mbar_wait(p, c, &c.hdr->full[slot], (gs / kStages) & 1)) break;
+        const uint32_t a = smem_u32(stage(slot));
+        for (int j = 0; j < kps && st * kps + j < nkb; ++j) {
+          const uint64_t ad = tc_desc_sw128(a + j * a_bytes), bd = tc_desc_sw128(a + kTcABytes + j * bbytes);
+#pragma unroll
+          for (int k = 0; k < kTcK / 16; ++k)
+            tc_mma_bf16(tmem, ad + (uint64_t)(kDescK * k), bd + (uint64_t)(kDescK * k), idesc, (st | j | k) != 0);
+        }
+        // the stage goes back to the producer once these MMAs have read it (in
+        // this build a stage's empty barrier takes one arrival)
+        tc_commit(&c.hdr->empty[slot]);
+      }
+      tc_commit(&c.hdr->acc_full);
+    }
+    c.st += (uint32_t)nst;
+    const bool ok = mbar_wait(p, c, &c.hdr->acc_full, acc_phase);
+    acc_phase ^= 1u;
+    tc_fence_after();
+    if (__all_sync(FULL, ok && !aborted(c))) tc_epilogue(w, op);
+    tc_fence_before();
+    consumers_sync();
+  }
+
+  // The accumulator of a tcgen05 item to its outputs: this warp's TMEM lanes
+  // (weight rows 32 q .. 32 q + 31 of the tile, q = the warp's index in the
+  // CTA modulo 4) for every other chunk of 8 activation rows (the two warps of
+  // a quarter take alternate chunks).
+  __device__ __forceinline__ void tc_epilogue(const int32_t* w, int op) {
+    const int l = w[F_LAYER];
+    const int q = (int)((threadIdx.x >> 5) & 3), half = cw >> 2;
+    const int r = 32 * q + lane;  // this thread's row of the tile
+    const bool moe = op == W_UP_TILE || op == W_DOWN_TILE;
+    const int ntok = moe ? w[F_A0 + 3] : p.B;
+    const int nrows = moe ? kTcRows : w[F_A0 + 1];
+    constexpr MoePlan mp = S::mptc;
+    for (int j = half; 8 * j < ntok; j += 2) {
+      float c16[16];
+      tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(16 * j), c16);
+      float v[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) v[t] = c16[2 * t] + c16[2 * t + 1];
+      switch (op) {
+        case OP_QKV_PROJ: {
+          // rows (2i, 2i + 1) sit in neighbouring lanes: the even lane rotates the pair
+          float vp[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) vp[t] = __shfl_xor_sync(FULL, v[t], 1);
+          // the chunk's positions, then their pages: two rounds of loads for 8 rows
+          int pos[8], page[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) pos[t] = 8 * j + t < ntok ? __ldg(p.seq_lens + 8 * j + t) - 1 : -1;
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const int lp = pos[t] / S::P;
+            page[t] = pos[t] >= 0 && lp < p.max_pages ? __ldg(p.block_tables + (int64_t)(8 * j + t) * p.max_pages + lp) : -1;
+          }
+          if ((lane & 1) == 0 && r < nrows) {
+            const int row = w[F_A0] + r;
+            const int head = row / S::D, dd = row - head * S::D;
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              if (8 * j + t < ntok) qkv_out(w, l, 8 * j + t, pos[t], page[t], head, dd, v[t], vp[t]);
+          }
+          break;
+        }
+        case OP_ROUTER_GEMM:
+          if (r < nrows) {
+            const int e = w[F_A0] + r;
+            const float bias = p.rbias ? p.rbias[e] : 0.f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              if (8 * j + t < ntok) p.rlog[((int64_t)l * p.MB + 8 * j + t) * S::E + e] = v[t] + bias;
+          }
+          break;
+        case OP_LM_HEAD:
+          if (r < nrows)
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              if (8 * j + t < ntok) p.logits[(int64_t)(8 * j + t) * p.V + w[F_A0] + r] = v[t];
+          break;
+        case OP_O_PROJ:
+          if (r < nrows)
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              if (8 * j + t < ntok)
+                p.opart[(((int64_t)(l & 1) * S::NKV + w[F_A0 + 2]) * p.MB + 8 * j + t) * S::H + w[F_A0] + r] = v[t];
+          break;
+        case W_UP_TILE: {
+          // lanes 0-15 of the warp hold gate rows 16 q .. 16 q + 15, lanes 16-31 the
+          // same up rows: SiLU(gate) * up ("Tasks": the SiLU-and-multiply epilogue)
+          float up[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) up[t] = __shfl_down_sync(FULL, v[t], 16);
+          if (lane < 16) {
+            const int col = w[F_A0 + 1] * mp.up_tile + 16 * q + lane;
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              if (8 * j + t < ntok) {
+                const int row = w[F_A0 + 2] + 8 * j + t;  // expert-ordered routed row
+                const float act = v[t] / (1.f + expf(-v[t])) * up[t];
+                p.u[(int64_t)row * S::I + col] = act;
+                const uint16_t hi = f_bf16(act);
+                p.ub[((int64_t)2 * row) * S::I + col] = hi;
+                p.ub[((int64_t)2 * row + 1) * S::I + col] = f_bf16(act - bf16_f(hi));
+              }
+          }
+          break;
+        }
+        case W_DOWN_TILE: {
+          // weighted, into the (row b, slot j) the routed row belongs to: the
+          // chunk's slots, then their weights (two rounds of loads for 8 rows)
+          const int n = w[F_A0 + 1] * mp.dn_tile + r;
+          int slot[8];
+          float wt[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            slot[t] = 8 * j + t < ntok ? __ldcg(p.perm + w[F_A0 + 2] + 8 * j + t) : 0;
+            if (slot[t] < 0 || slot[t] >= p.B * S::K) slot[t] = 0;  // only after a failed step
+          }
+#pragma unroll
+          for (int t = 0; t < 8; ++t) wt[t] = __ldcg(p.topk_w + (int64_t)l * p.MB * S::K + slot[t]);
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            if (8 * j + t < ntok) p.y[(int64_t)slot[t] * S::H + n] = wt[t] * v[t];
+          break;
+        }
+        default: break;
+      }
+    }
+  }
+
+  // One QKV rotation pair (rows dd, dd + 1 of head `head`) of activation row
+  // b: RoPE by pos * base^(-dd/D) (angle reduced modulo 2 pi in double,
+  // then sin/cos in float) on q and k; q to its buffer, k and v to the pool.
+  __device__ __forceinline__ void qkv_out(const int32_t* w, int l, int b, int pos, int page, int head, int dd, float v0,
+                                          float v1) {
+    if (head < S::NQ + S::NKV) {
+      const double ang = (double)pos * sm.rope_theta[dd / 2];
+      const double red = ang - 6.283185307179586 * rint(ang * 0.15915494309189535);
+      float s0, c0;
+      sincosf((float)red, &s0, &c0);
+      const float r0 = v0 * c0 - v1 * s0, r1 = v0 * s0 + v1 * c0;
+      v0 = r0;
+      v1 = r1;
+    }
+    if (head < S::NQ) {
+      *reinterpret_cast<float2*>(p.q + ((int64_t)b * S::NQ + head) * S::D + dd) = make_float2(v0, v1);
+    } else if (pos >= 0) {
+      const bool is_v = head >= S::NQ + S::NKV;
+      const int g = head - S::NQ - (is_v ? S::NKV : 0);
+      const uint32_t packed = (uint32_t)f_bf16(v0) | ((uint32_t)f_bf16(v1) << 16);
+      *reinterpret_cast<uint32_t*>(p.kvnew + (((int64_t)b * 2 + (is_v ? 1 : 0)) * S::NKV + g) * S::D + dd) = packed;
+      if (page < 0 || page >= p.num_pages) {
+        record_error(p, ERR_PAGE, c.sm, where_of(w), pos / S::P, (uint32_t)page, (uint32_t)p.num_pages);
+      } else {
+        uint16_t* pool = is_v ? p.vpool : p.kpool;
+        const int64_t o = ((((int64_t)l * p.num_pages + page) * S::NKV + g) * S::P + pos % S::P) * S::D + dd;
+        *reinterpret_cast<uint32_t*>(pool + o) = packed;
+      }
+    }
+  }
+
   __device__ __forceinline__ void execute(const int32_t* w) {
+    if constexpr (M == kModeTc) {
+      switch (w[F_OP]) {
+        case OP_QKV_PROJ:
+        case OP_LM_HEAD:
+        case OP_O_PROJ:
+        case W_UP_TILE:
+        case W_DOWN_TILE:
+          tc_item(w);
+          return;
+        case OP_ROUTER_GEMM:
+          tc_item(w);
+          if (w[F_A0 + 5]) route_if_last(w);
+          return;
+        default: break;
+      }
+    }
     // above kTB rows (any-batch mode only) the two-row GEMV; FP8 / FP4
     // experts take their tensor-core GEMVs
     constexpr bool any_batch = M == kModeAnyBatch;
@@ -2668,12 +3116,42 @@ struct Consumer {
     }
   }
 
+  // kModeTc: TMEM columns of the accumulator (the MMA's N is at most kTcMaxN)
+  static constexpr uint32_t kTcCols = 128;
+  static_assert(kTcMaxN <= (int)kTcCols, "the accumulator's columns");
+
+  // kModeTc, after the last item: every MMA this CTA issued has completed
+  // (one more commit, waited for with the usual time limit), then the TMEM
+  // goes back -- also after a failed step, so the SM's TMEM is free again.
+  __device__ __forceinline__ void tc_release() {
+    if (ct == 0) {
+      tc_commit(&c.hdr->tc_drain);
+      const int64_t t0 = gtimer();
+      while (!mbar_try_wait(&c.hdr->tc_drain, 0) && gtimer() - t0 < p.watchdog_ns) {
+      }
+    }
+    tc_fence_before();
+    consumers_sync();
+    if (cw == 0) {
+      tc_fence_after();
+      tmem_dealloc(tmem, kTcCols);
+    }
+  }
+
   __device__ __forceinline__ void run() {
     // per-CTA set-up: the RoPE frequencies and empty activation caches
     for (int i = ct; i < S::D / 2; i += kConsumerThreads)
       sm.rope_theta[i] = pow((double)p.rope_base, -(double)(2 * i) / (double)S::D);
     if (ct < 4) sm.xtag[ct] = sm.qtag[ct] = -1;
+    if constexpr (M == kModeTc) {
+      if (cw == 0) tmem_alloc(&c.hdr->tmem_addr, kTcCols);
+      tc_fence_before();
+    }
     consumers_sync();
+    if constexpr (M == kModeTc) {
+      tc_fence_after();
+      tmem = c.hdr->tmem_addr;
+    }
     // at batch <= kTB the rows' rotations and KV pages hold for every layer:
     // computed once here, as the QKV epilogue would (angle reduced modulo
     // 2 pi in double, then sin/cos in float)
@@ -2837,7 +3315,9 @@ __global__ void __launch_bounds__(kThreads, 1) mk_persistent(const __grid_consta
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&hdr->full[i], 1);
-      mbar_init(&hdr->empty[i], kConsumerWarps);
+      // the tcgen05 build hands a stage back with one arrival (a commit of the
+      // MMAs that read it, or one thread after the block's last read)
+      mbar_init(&hdr->empty[i], M == kModeTc ? 1 : kConsumerWarps);
     }
     for (int i = 0; i < kDescRing; ++i) {
       mbar_init(&hdr->dfull[i], 1);
@@ -2848,6 +3328,8 @@ __global__ void __launch_bounds__(kThreads, 1) mk_persistent(const __grid_consta
       mbar_init(&hdr->wempty[i], 1);
       mbar_init(&hdr->done[i], kConsumerThreads);
     }
+    mbar_init(&hdr->acc_full, 1);
+    mbar_init(&hdr->tc_drain, 1);
     hdr->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -2865,6 +3347,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_persistent(const __grid_consta
     const int ct = threadIdx.x - 96;
     Consumer<S, M> cs{p, c, *scr, ct, ct / 32, ct & 31};
     cs.run();
+    if constexpr (M == kModeTc) cs.tc_release();
   }
 }
 

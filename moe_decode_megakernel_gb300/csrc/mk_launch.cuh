@@ -11,7 +11,8 @@ namespace mk {
 template <class S, int M>
 int launch_shape(const Params& p, int grid, cudaStream_t stream) {
   const void* fn = reinterpret_cast<const void*>(&dev::mk_persistent<S, M>);
-  const size_t smem = dev::smem_bytes<S>();
+  constexpr size_t smem = dev::smem_bytes<S>();
+  static_assert(smem <= dev::kMaxSmemPerCta, "shared memory of one CTA");
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
   void* args[] = {const_cast<Params*>(&p)};

@@ -399,18 +399,19 @@ static int build(mk_sched* s) {
   const int qkv_tile = o.qkv_tile_rows > 0 ? round_to(o.qkv_tile_rows, sr_h) : sr_h;
   if (D.D % qkv_tile != 0 || qkv_tile % sr_h != 0 || D.D % sr_h != 0)
     return fail(MK_ERR_ARG, "qkv_tile_rows must divide head_dim and be a multiple of the stage rows");
-  const int o_tile = o.o_tile_rows > 0 ? round_to(o.o_tile_rows, sr_o) : round_to(64, sr_o);
+  const int o_tile = s->tc ? kTcRows : o.o_tile_rows > 0 ? round_to(o.o_tile_rows, sr_o) : round_to(64, sr_o);
   // LM head: one tile per SM by default (the vocabulary split evenly in stage rows), so the
   // last wave of the step has no tail of SMs with one tile more than the others
   const int lm_even = ((c.vocab + s->num_sms - 1) / s->num_sms + sr_h - 1) / sr_h * sr_h;
-  const int lm_tile = o.lm_tile_rows > 0 ? round_to(o.lm_tile_rows, sr_h) : std::max(sr_h, lm_even);
-  const int router_tile = sr_h * std::max(1, 16 / sr_h);
+  const int lm_tile = s->tc ? kTcRows : o.lm_tile_rows > 0 ? round_to(o.lm_tile_rows, sr_h) : std::max(sr_h, lm_even);
+  const int router_tile = s->tc ? std::min(kTcRouterRows, D.E) : sr_h * std::max(1, 16 / sr_h);
   // SMs of each branch: all of them, or the split of placement 2
   const int n_attn_sms = attn_group_sms(s), n_moe_sms = s->opts.placement == 2 ? s->num_sms - n_attn_sms : s->num_sms;
   const int n_moe = o.moe_claimers > 0 ? o.moe_claimers : n_moe_sms;
   const int attn_claim_default = std::min(n_attn_sms, std::max(1, MB * NKV * full_slices));
   const int n_attn = o.attn_claimers > 0 ? o.attn_claimers : attn_claim_default;
-  const int norm_rows = 4;
+  // RMSNorm tasks: a row each for tcgen05 schedules (their rows run in parallel), else up to 4
+  const int norm_rows = s->tc ? 1 : 4;
 
   B.alloc_layer_bars();
   std::vector<Desc> all;
@@ -444,7 +445,16 @@ static int build(mk_sched* s) {
       lb.n_qkv_g[g]++;
       w_qkv.push_back(d);
     };
-    if (o.qkv_tile_rows > 0) {
+    if (s->tc) {
+      // tcgen05 items: tiles of at most kTcRows rows within each KV group's
+      // query-head, K-head and V-head segments
+      for (int g = 0; g < NKV; ++g) {
+        const int seg_r0[3] = {g * G * D.D, (D.NQ + g) * D.D, (D.NQ + NKV + g) * D.D};
+        const int seg_rows[3] = {G * D.D, D.D, D.D};
+        for (int k = 0; k < 3; ++k)
+          for (int r = 0; r < seg_rows[k]; r += kTcRows) add_qkv(seg_r0[k] + r, std::min(kTcRows, seg_rows[k] - r), g);
+      }
+    } else if (o.qkv_tile_rows > 0) {
       for (int r0 = 0; r0 < QKVROWS; r0 += qkv_tile) {
         const int head = r0 / D.D;
         add_qkv(r0, qkv_tile, head < D.NQ ? head / G : (head < D.NQ + NKV ? head - D.NQ : head - D.NQ - NKV));
@@ -547,7 +557,7 @@ static int build(mk_sched* s) {
 
     std::vector<Desc> w_gather;
     if (o.explicit_gather && !dense) {
-      const int rows = MB * D.K, per = 64;
+      const int rows = MB * D.K, per = s->tc ? 8 : 32;  // tcgen05 schedules: more, smaller gathers
       for (int r0 = 0; r0 < rows; r0 += per) {
         Desc d = blank(OP_MOE_GATHER, l);
         d[F_A0] = r0;
@@ -781,6 +791,12 @@ static void layout_workspace(mk_sched* s) {
   w.add("u", sizeof(float) * MB * D.K * D.I);
   w.add("y", sizeof(float) * (size_t)MB * D.K * D.H);
   w.add("moe_out", sizeof(float) * (size_t)MB * D.H);
+  if (s->tc) {  // the BF16 hi/lo operand rows of the tcgen05 items (at least one box of rows each)
+    w.add("xb", 2ull * s->tc_nb * D.H);
+    w.add("attnb", 2ull * s->tc_nb * D.NQ * D.D);
+    w.add("xgb", 2ull * std::max(2 * MB * D.K, s->tc_nb) * D.H);
+    w.add("ub", 2ull * std::max(2 * MB * D.K, s->tc_nb) * D.I);
+  }
   if (s->opts.trace_hidden) w.add("hidden_trace", sizeof(float) * (size_t)(L + 1) * MB * D.H);
   if (s->opts.trace_queue) w.add("queue_trace", sizeof(int32_t) * (size_t)L * queue_trace_stride(D.E, MB * D.K));
   if (s->opts.trace) {
@@ -1117,6 +1133,14 @@ int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const 
   else mk_default_sched_opts(&s->opts);
   s->max_batch = max_batch;
   s->max_ctx = max_ctx;
+  // batches beyond the GEMV's kTB rows: the weight tiles are real contractions,
+  // run on the tcgen05 tensor cores (BF16 experts of an MoE model)
+  s->tc = max_batch > kTB && !m->cfg.expert_fp8 && !m->cfg.expert_fp4 && !(m->dims.E == 1 && m->dims.K == 1);
+  if (s->tc) {
+    s->plan = moe_plan_tc(m->dims);
+    s->tc_nb = (2 * max_batch + 15) / 16 * 16;
+    s->opts.explicit_gather = 1;  // the up/gate tiles take their rows in expert order
+  }
   s->num_sms = s->opts.num_sms;
   if (s->num_sms <= 0) {
     s->num_sms = query_num_sms();
