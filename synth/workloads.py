@@ -159,6 +159,9 @@ WORKLOADS = {
                             desc="small with seeded RMSNorm gains in [0.5, 2)"),
     "full_gains_bs1_8k": Workload("full_gains_bs1_8k", "full", 1, ("fixed", 8192), 33, gains=True,
                                   desc="full shape, B=1, context 8192, seeded RMSNorm gains"),
+    "prof_l2_b32": Workload("prof_l2_b32", "full_l2", 32, ("uniform", 512, 8192), 8, zipf=1.1,
+                            desc="full-shape layers, 2 of them, B=32 ragged U[512,8192], Zipf(1.1) routing "
+                                 "(profiling case of the tensor-core build)"),
     "prof_l2_8k": Workload("prof_l2_8k", "full_l2", 1, ("fixed", 8192), 7,
                            desc="full-shape layers, 2 of them, B=1, context 8192 (profiling case)"),
 }
