@@ -137,9 +137,10 @@ typedef struct {
   int32_t trace;            /* 1: record every work item's timestamps ("trace", "stats") */
   int32_t moe_queue;        /* 0: separate up/gate and down drains; 1: one MoE queue with each
                                expert's down tiles one expert behind its up/gate tiles */
-  int32_t moe_static;       /* 1 (default): claimer c takes MoE units c, c + n, c + 2n, ... of
-                               the queue (n claimers), no atomics; 0: the first unit so and the
-                               rest from a claim counter */
+  int32_t moe_static;       /* 1: claimer c takes MoE units c, c + n, c + 2n, ... of the queue
+                               (n claimers), no atomics; 0: the first unit so and the rest from
+                               a claim counter; -1 (default): 1 for max_batch <= 2, 0 for the
+                               tensor-core schedules (max_batch > 2, BF16 experts) */
   int32_t fuse_routing;     /* 1 (default): the last router task to finish runs the top-k and
                                builds the MoE queue (no separate top-k task), and at batch <= 2
                                each router task computes the layer's RMSNorm itself instead of
@@ -177,7 +178,8 @@ typedef struct {
                                ("queue_trace", see mk_workspace_offset) */
 } mk_sched_opts;
 
-/* Fills opts with the defaults (all zero except fuse_* = 1 and moe_static = 1). */
+/* Fills opts with the defaults (all zero except fuse_* = 1, attn_static = 1 and
+ * moe_static = -1). */
 void mk_default_sched_opts(mk_sched_opts* opts);
 
 /* Builds and validates the per-SM task lists for steps with batch <=

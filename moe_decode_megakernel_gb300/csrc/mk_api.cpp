@@ -127,22 +127,23 @@ int encode_operand(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t co
   return MK_OK;
 }
 
-// The weights as tcgen05 A operands: boxes of kTcRows rows (the gate and up
-// matrices in blocks of 16 rows: an up/gate tile interleaves them; the
-// router in boxes of its tasks' kTcRouterRows rows).
+// The weights as tcgen05 A operands: boxes of the rows one item copies --
+// kTcDenseRows for QKV, O-proj and LM-head tiles, kTcRouterRows for router
+// tasks, kTcMoeRows for down tiles, blocks of 16 rows of the gate and up
+// matrices (an up/gate tile interleaves them).
 int encode_weight_maps(mk_model* m) {
   if (m->tm_ready) return MK_OK;
   const mk_config& c = m->cfg;
   const ShapeDims& D = m->dims;
   const uint64_t L = (uint64_t)c.n_layers, QKV = (uint64_t)(D.NQ + 2 * D.NKV) * D.D;
   const mk_weights& w = m->w;
-  int rc = encode_operand(&m->tm_w[0], w.w_qkv, L * QKV, D.H, kTcRows, "w_qkv");
-  if (rc == MK_OK) rc = encode_operand(&m->tm_w[1], w.w_o, L * D.H, (uint64_t)D.NQ * D.D, kTcRows, "w_o");
+  int rc = encode_operand(&m->tm_w[0], w.w_qkv, L * QKV, D.H, kTcDenseRows, "w_qkv");
+  if (rc == MK_OK) rc = encode_operand(&m->tm_w[1], w.w_o, L * D.H, (uint64_t)D.NQ * D.D, kTcDenseRows, "w_o");
   if (rc == MK_OK) rc = encode_operand(&m->tm_w[2], w.w_router, L * D.E, D.H, kTcRouterRows, "w_router");
-  if (rc == MK_OK) rc = encode_operand(&m->tm_w[3], w.w_lm, (uint64_t)c.vocab, D.H, kTcRows, "w_lm");
+  if (rc == MK_OK) rc = encode_operand(&m->tm_w[3], w.w_lm, (uint64_t)c.vocab, D.H, kTcDenseRows, "w_lm");
   if (rc == MK_OK) rc = encode_operand(&m->tm_w[4], w.w_gate, L * D.E * D.I, D.H, 16, "w_gate");
   if (rc == MK_OK) rc = encode_operand(&m->tm_w[5], w.w_up, L * D.E * D.I, D.H, 16, "w_up");
-  if (rc == MK_OK) rc = encode_operand(&m->tm_w[6], w.w_down, L * D.E * D.H, D.I, kTcRows, "w_down");
+  if (rc == MK_OK) rc = encode_operand(&m->tm_w[6], w.w_down, L * D.E * D.H, D.I, kTcMoeRows, "w_down");
   if (rc == MK_OK) m->tm_ready = true;
   return rc;
 }

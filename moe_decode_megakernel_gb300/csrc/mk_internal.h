@@ -222,6 +222,8 @@ constexpr int kTcK = 64;
 constexpr int kTcABytes = kTcRows * kTcK * 2;
 constexpr int kTcMaxN = (kStageBytes - kTcABytes) / (kTcK * 2);
 constexpr int kTcRouterRows = 16;  // rows of a router task (its weight box; the MMA's other rows unused)
+constexpr int kTcDenseRows = 64;   // rows of a QKV, O-proj or LM-head tile (the MMA's other rows unused)
+constexpr int kTcMoeRows = 128;    // weight rows of an expert tile: 64 gate + 64 up rows, or 128 down rows
 // k-blocks per stage of a tcgen05 item whose weight box holds a_bytes per
 // k-block: one for full tiles, up to 8 for a router task's small boxes (the
 // activation boxes of those k-blocks must fit the stage's second half).
@@ -233,18 +235,18 @@ MK_HOST_DEVICE constexpr int tc_kblocks_per_stage(uint32_t a_bytes, int tc_nb) {
 }
 static_assert(kTcMaxN >= 2 * kMaxBatch, "hi/lo rows of the largest batch fit a stage");
 
-// The MoE plan of tcgen05 items: up/gate tiles of 64 gate rows and the same
-// 64 up rows (one M = 128 tile), down tiles of 128 rows; "stages" count
-// k-blocks.
+// The MoE plan of tcgen05 items: up/gate tiles of kTcMoeRows / 2 gate rows
+// and the same up rows, down tiles of kTcMoeRows rows (the MMA's M = 128 has
+// the rest unused); "stages" count k-blocks.
 constexpr MoePlan moe_plan_tc(ShapeDims s) {
   MoePlan p{};
-  p.up_half = kTcRows / 2;
+  p.up_half = kTcMoeRows / 2;
   p.up_stages = s.H / kTcK;
-  p.up_tile = kTcRows / 2;
+  p.up_tile = kTcMoeRows / 2;
   p.up_tiles = s.I / p.up_tile;
-  p.dn_rows = kTcRows;
+  p.dn_rows = kTcMoeRows;
   p.dn_stages = s.I / kTcK;
-  p.dn_tile = kTcRows;
+  p.dn_tile = kTcMoeRows;
   p.dn_tiles = s.H / p.dn_tile;
   return p;
 }

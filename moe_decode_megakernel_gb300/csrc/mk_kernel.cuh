@@ -705,11 +705,11 @@ struct Producer {
       mbar_expect_tx(fb, (uint32_t)nk * (a_bytes + bbytes));
       for (int j = 0; j < nk; ++j) {
         const int x = ax + (st * kps + j) * kTcK;
-        if (updown) {
+        if (updown) {  // 16-row blocks: gate block q, then up block q
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            tma_2d(dst + (2 * q) * (kTcABytes / 8), &p.tm_wg, x, ay + 16 * q, fb, stream_policy);
-            tma_2d(dst + (2 * q + 1) * (kTcABytes / 8), &p.tm_wu, x, ay + 16 * q, fb, stream_policy);
+          for (int q = 0; q < kTcMoeRows / 32; ++q) {
+            tma_2d(dst + j * a_bytes + (2 * q) * 2048, &p.tm_wg, x, ay + 16 * q, fb, stream_policy);
+            tma_2d(dst + j * a_bytes + (2 * q + 1) * 2048, &p.tm_wu, x, ay + 16 * q, fb, stream_policy);
           }
         } else {
           tma_2d(dst + j * a_bytes, ta, x, ay, fb, stream_policy);
@@ -730,7 +730,9 @@ struct Producer {
     const CUtensorMap* ta;
     const CUtensorMap* tb = &p.tm_xb;
     int ax = 0, ay, bx = 0, nkb = S::H / kTcK;
-    uint32_t a_bytes = kTcABytes;  // a router task copies only its own rows (the MMA's other rows are unused)
+    // dense tiles copy only their own rows (the MMA's other rows are unused),
+    // several k-blocks per stage
+    uint32_t a_bytes = kTcDenseRows * kTcK * 2;
     switch (op) {
       case OP_QKV_PROJ: ta = &p.tm_wqkv; ay = l * S::QKV + row0; break;
       case OP_ROUTER_GEMM: ta = &p.tm_wr; ay = l * S::E + row0; a_bytes = kTcRouterRows * kTcK * 2; break;
@@ -1051,15 +1053,16 @@ struct Producer {
         // one item of nkb k-blocks: the expert's gate/up or down rows against
         // its routed rows (their hi/lo rows start at row 2 row0)
         const int64_t le = (int64_t)l * S::E + e;
-        it[F_NSTAGE] = up ? S::H / kTcK : S::I / kTcK;
-        it[F_A0 + 13] = it[F_NSTAGE];
+        constexpr uint32_t ab = kTcMoeRows * kTcK * 2;
+        const int nkb = up ? S::H / kTcK : S::I / kTcK, kps = tc_kblocks_per_stage(ab, p.tc_nb);
+        it[F_NSTAGE] = (nkb + kps - 1) / kps;
+        it[F_A0 + 13] = nkb;
         if (!push(it)) return false;
         if (up) {
-          if (!tc_stages(it, nullptr, 0, (int)(le * S::I + t * mp.up_tile), true, &p.tm_xgb, 0, 2 * row0,
-                         S::H / kTcK))
+          if (!tc_stages(it, nullptr, 0, (int)(le * S::I + t * mp.up_tile), true, &p.tm_xgb, 0, 2 * row0, nkb, ab))
             return false;
-        } else if (!tc_stages(it, &p.tm_wd, 0, (int)(le * S::H + t * mp.dn_tile), false, &p.tm_ub, 0, 2 * row0,
-                              S::I / kTcK)) {
+        } else if (!tc_stages(it, &p.tm_wd, 0, (int)(le * S::H + t * mp.dn_tile), false, &p.tm_ub, 0, 2 * row0, nkb,
+                              ab)) {
           return false;
         }
       } else {
@@ -2866,8 +2869,10 @@ struct Consumer {
   __device__ __forceinline__ void tc_item(const int32_t* w) {
     const int op = w[F_OP];
     const int nst = w[F_NSTAGE], nkb = w[F_A0 + 13];
-    // a router task's stages hold several k-blocks of its small weight box
-    const uint32_t a_bytes = op == OP_ROUTER_GEMM ? kTcRouterRows * kTcK * 2 : kTcABytes;
+    // dense tiles' stages hold several k-blocks of their smaller weight boxes
+    const uint32_t a_bytes = op == OP_ROUTER_GEMM                      ? kTcRouterRows * kTcK * 2
+                             : (op == W_UP_TILE || op == W_DOWN_TILE) ? kTcMoeRows * kTcK * 2
+                                                                      : kTcDenseRows * kTcK * 2;
     const int kps = tc_kblocks_per_stage(a_bytes, p.tc_nb);
     const uint32_t bbytes = (uint32_t)p.tc_nb * kTcK * 2;
     if (ct == 0) {
@@ -2910,7 +2915,8 @@ struct Consumer {
     const int r = 32 * q + lane;  // this thread's row of the tile
     const bool moe = op == W_UP_TILE || op == W_DOWN_TILE;
     const int ntok = moe ? w[F_A0 + 3] : p.B;
-    const int nrows = moe ? kTcRows : w[F_A0 + 1];
+    const int nrows = moe ? kTcMoeRows : w[F_A0 + 1];
+    if (r >= ((nrows + 31) & ~31)) return;  // a warp quarter of unused MMA rows (uniform per warp)
     constexpr MoePlan mp = S::mptc;
     for (int j = half; 8 * j < ntok; j += 2) {
       float c16[16];
@@ -2970,7 +2976,7 @@ struct Consumer {
           float up[8];
 #pragma unroll
           for (int t = 0; t < 8; ++t) up[t] = __shfl_down_sync(FULL, v[t], 16);
-          if (lane < 16) {
+          if (lane < 16 && r < nrows) {
             const int col = w[F_A0 + 1] * mp.up_tile + 16 * q + lane;
 #pragma unroll
             for (int t = 0; t < 8; ++t)

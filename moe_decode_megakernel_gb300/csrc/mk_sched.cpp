@@ -399,11 +399,11 @@ static int build(mk_sched* s) {
   const int qkv_tile = o.qkv_tile_rows > 0 ? round_to(o.qkv_tile_rows, sr_h) : sr_h;
   if (D.D % qkv_tile != 0 || qkv_tile % sr_h != 0 || D.D % sr_h != 0)
     return fail(MK_ERR_ARG, "qkv_tile_rows must divide head_dim and be a multiple of the stage rows");
-  const int o_tile = s->tc ? kTcRows : o.o_tile_rows > 0 ? round_to(o.o_tile_rows, sr_o) : round_to(64, sr_o);
+  const int o_tile = s->tc ? kTcDenseRows : o.o_tile_rows > 0 ? round_to(o.o_tile_rows, sr_o) : round_to(64, sr_o);
   // LM head: one tile per SM by default (the vocabulary split evenly in stage rows), so the
   // last wave of the step has no tail of SMs with one tile more than the others
   const int lm_even = ((c.vocab + s->num_sms - 1) / s->num_sms + sr_h - 1) / sr_h * sr_h;
-  const int lm_tile = s->tc ? kTcRows : o.lm_tile_rows > 0 ? round_to(o.lm_tile_rows, sr_h) : std::max(sr_h, lm_even);
+  const int lm_tile = s->tc ? kTcDenseRows : o.lm_tile_rows > 0 ? round_to(o.lm_tile_rows, sr_h) : std::max(sr_h, lm_even);
   const int router_tile = s->tc ? std::min(kTcRouterRows, D.E) : sr_h * std::max(1, 16 / sr_h);
   // SMs of each branch: all of them, or the split of placement 2
   const int n_attn_sms = attn_group_sms(s), n_moe_sms = s->opts.placement == 2 ? s->num_sms - n_attn_sms : s->num_sms;
@@ -446,13 +446,14 @@ static int build(mk_sched* s) {
       w_qkv.push_back(d);
     };
     if (s->tc) {
-      // tcgen05 items: tiles of at most kTcRows rows within each KV group's
-      // query-head, K-head and V-head segments
+      // tcgen05 items: tiles of at most kTcDenseRows rows within each KV
+      // group's query-head, K-head and V-head segments
       for (int g = 0; g < NKV; ++g) {
         const int seg_r0[3] = {g * G * D.D, (D.NQ + g) * D.D, (D.NQ + NKV + g) * D.D};
         const int seg_rows[3] = {G * D.D, D.D, D.D};
         for (int k = 0; k < 3; ++k)
-          for (int r = 0; r < seg_rows[k]; r += kTcRows) add_qkv(seg_r0[k] + r, std::min(kTcRows, seg_rows[k] - r), g);
+          for (int r = 0; r < seg_rows[k]; r += kTcDenseRows)
+            add_qkv(seg_r0[k] + r, std::min(kTcDenseRows, seg_rows[k] - r), g);
       }
     } else if (o.qkv_tile_rows > 0) {
       for (int r0 = 0; r0 < QKVROWS; r0 += qkv_tile) {
@@ -1108,7 +1109,7 @@ void mk_default_sched_opts(mk_sched_opts* o) {
   std::memset(o, 0, sizeof(*o));
   o->fuse_finalize = 1;
   o->fuse_moe_combine = 1;
-  o->moe_static = 1;
+  o->moe_static = -1;
   o->fuse_routing = 1;
   o->fuse_norm_qkv = 1;
   o->attn_static = 1;
@@ -1141,6 +1142,10 @@ int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const 
     s->tc_nb = (2 * max_batch + 15) / 16 * 16;
     s->opts.explicit_gather = 1;  // the up/gate tiles take their rows in expert order
   }
+  // MoE claims: static for the GEMV builds (their tiles are short and equal),
+  // dynamic for tensor-core schedules (long tiles whose count rarely divides
+  // the claimers: the SMs that finish first take the rest)
+  if (s->opts.moe_static < 0) s->opts.moe_static = s->tc ? 0 : 1;
   s->num_sms = s->opts.num_sms;
   if (s->num_sms <= 0) {
     s->num_sms = query_num_sms();
