@@ -170,7 +170,9 @@ typedef struct {
                                head over all SMs; 3: dependency affinity ("Task scheduler"),
                                each task to the least loaded SM that ran a task it waits on,
                                within a per-layer cap of the layer's tasks per SM (rounded
-                               up), else to the least loaded SM */
+                               up), else to the least loaded SM; 4: round robin, but each
+                               layer's static attention slices go first (at most 3 each) to the
+                               SMs whose static up/gate claimer gets no tile */
   int32_t attn_sms;         /* placement 2: SMs of the attention branch; 0 = in proportion
                                to the branch's bytes per layer (QKV, O-proj and KV against
                                router and experts) */

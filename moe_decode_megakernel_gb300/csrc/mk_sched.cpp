@@ -349,6 +349,33 @@ std::vector<int> place_affinity(const mk_sched* s, const std::vector<Desc>& all,
   return sm_of;
 }
 
+// Slices where there are no up/gate tiles: round robin, except that the
+// static attention slices of each layer go first to the SMs whose up/gate
+// claimer gets no unit (at batch 1 the routed experts' up/gate tiles are
+// fewer than the claimers), at most `cap` each, so that no slice delays an
+// SM's up/gate tile.  Applies where the claims are static.
+std::vector<int> place_slices_free(const mk_sched* s, const std::vector<Desc>& all,
+                                   const std::vector<size_t>& layer_begin, int MB, int cap) {
+  const int n = s->num_sms;
+  std::vector<int> sm_of(all.size());
+  for (size_t k = 0; k < all.size(); ++k) sm_of[k] = (int)(k % (size_t)n);
+  const int64_t up_units = (int64_t)std::min(s->dims.E, MB * s->dims.K) * s->plan.up_tiles;
+  for (size_t li = 0; li + 1 < layer_begin.size(); ++li) {
+    const size_t b = layer_begin[li], e = layer_begin[li + 1];
+    std::vector<int> free_sms;
+    for (size_t k = b; k < e; ++k) {
+      const Desc& d = all[k];
+      if (d[F_OP] == OP_MOE_UPGATE_ACT_DRAIN && d[F_A0 + 7] == 1 && d[F_A0 + 4] >= up_units)
+        free_sms.push_back(sm_of[k]);
+    }
+    if (free_sms.empty()) continue;
+    size_t given = 0;
+    for (size_t k = b; k < e && given < free_sms.size() * (size_t)cap; ++k)
+      if (all[k][F_OP] == OP_ATTN_DECODE) sm_of[k] = free_sms[given++ % free_sms.size()];
+  }
+  return sm_of;
+}
+
 }  // namespace
 
 // SMs of the attention branch under the split placement (all SMs otherwise):
@@ -753,6 +780,7 @@ static int build(mk_sched* s) {
   const std::vector<int> sm_of = o.placement == 1   ? place_greedy(s, all, layer_begin, MB)
                                  : o.placement == 2 ? place_split(s, all, layer_begin, n_attn_sms)
                                  : o.placement == 3 ? place_affinity(s, all, layer_begin)
+                                 : o.placement == 4 ? place_slices_free(s, all, layer_begin, MB, 3)
                                                     : std::vector<int>();
   s->tasks = std::move(all);
   s->per_sm.assign(s->num_sms, {});
@@ -1158,7 +1186,7 @@ int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const 
     delete s;
     return fail(MK_ERR_ARG, "unknown wave order");
   }
-  if (s->opts.placement < 0 || s->opts.placement > 3) {
+  if (s->opts.placement < 0 || s->opts.placement > 4) {
     delete s;
     return fail(MK_ERR_ARG, "unknown placement");
   }

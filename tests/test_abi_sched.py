@@ -98,7 +98,8 @@ def test_schedules_validate_and_simulate(workload, order):
                                   dict(placement=2), dict(placement=2, attn_sms=20),
                                   dict(placement=2, wave_order=2), dict(placement=2, moe_static=0),
                                   dict(placement=3), dict(placement=3, wave_order=1),
-                                  dict(placement=3, moe_static=0), dict(placement=3, fuse_norm_qkv=0)])
+                                  dict(placement=3, moe_static=0), dict(placement=3, fuse_norm_qkv=0),
+                                  dict(placement=4)])
 def test_schedule_variants(opts):
     m, s, inp = sched_for("small", **opts)
     s.validate()
