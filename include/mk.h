@@ -55,7 +55,10 @@ typedef struct {
   int32_t expert_fp8;  /* 1: w_gate, w_up, w_down hold OCP FP8 E4M3 codes (1 byte each,
                           same [L][E][rows][cols] layout) and each output row has one
                           fp32 scale (w_*_scale): weight = e4m3 value * row scale.
-                          Schedules for it need max_batch <= 2 */
+                          Schedules for it need max_batch <= 32; above 2 the expert
+                          tiles run on FP8 tensor-core MMAs (E4M3 weights against the
+                          activations as four E5M2 terms each), which needs hidden and
+                          inter multiples of 128 and activations below 57344 in magnitude */
   int32_t expert_fp4;  /* 1 (not with expert_fp8): w_gate, w_up, w_down hold FP4 E2M1 codes,
                           two per byte (element 2j in the low nibble of byte j), the same
                           [L][E][rows][cols] layout at half a byte per weight; each run of 16

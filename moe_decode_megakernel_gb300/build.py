@@ -17,7 +17,7 @@ SOURCES = ["mk_api.cpp", "mk_sched.cpp", "mk_static_ws.cu", "mk_service.cpp", "m
 # mk_shape.cu is compiled once per pair
 SHAPES = {"tiny": "256,4,2,64,16,4,128,16", "small": "1024,16,2,64,32,4,512,64",
           "dense": "1024,16,2,64,1,1,2048,64", "full": "2048,32,4,128,128,8,768,64"}
-MODES = 7
+MODES = 8
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

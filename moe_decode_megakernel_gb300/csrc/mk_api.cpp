@@ -43,7 +43,8 @@ int query_num_sms() {
   int launch_##name##_3(const Params& p, int grid, cudaStream_t s); \
   int launch_##name##_4(const Params& p, int grid, cudaStream_t s); \
   int launch_##name##_5(const Params& p, int grid, cudaStream_t s); \
-  int launch_##name##_6(const Params& p, int grid, cudaStream_t s);
+  int launch_##name##_6(const Params& p, int grid, cudaStream_t s); \
+  int launch_##name##_7(const Params& p, int grid, cudaStream_t s);
 MK_DECLARE_SHAPE(tiny)
 MK_DECLARE_SHAPE(small)
 MK_DECLARE_SHAPE(dense)
@@ -58,11 +59,11 @@ struct CompiledShape {
 };
 
 const CompiledShape kShapes[] = {
-    {{256, 4, 2, 64, 16, 4, 128, 16}, {launch_tiny_0, launch_tiny_1, launch_tiny_2, launch_tiny_3, launch_tiny_4, launch_tiny_5, launch_tiny_6}},
-    {{1024, 16, 2, 64, 32, 4, 512, 64}, {launch_small_0, launch_small_1, launch_small_2, launch_small_3, launch_small_4, launch_small_5, launch_small_6}},
+    {{256, 4, 2, 64, 16, 4, 128, 16}, {launch_tiny_0, launch_tiny_1, launch_tiny_2, launch_tiny_3, launch_tiny_4, launch_tiny_5, launch_tiny_6, launch_tiny_7}},
+    {{1024, 16, 2, 64, 32, 4, 512, 64}, {launch_small_0, launch_small_1, launch_small_2, launch_small_3, launch_small_4, launch_small_5, launch_small_6, launch_small_7}},
     // dense SwiGLU FFN (one expert, top-1)
-    {{1024, 16, 2, 64, 1, 1, 2048, 64}, {launch_dense_0, launch_dense_1, launch_dense_2, launch_dense_3, launch_dense_4, launch_dense_5, launch_dense_6}},
-    {{2048, 32, 4, 128, 128, 8, 768, 64}, {launch_full_0, launch_full_1, launch_full_2, launch_full_3, launch_full_4, launch_full_5, launch_full_6}},
+    {{1024, 16, 2, 64, 1, 1, 2048, 64}, {launch_dense_0, launch_dense_1, launch_dense_2, launch_dense_3, launch_dense_4, launch_dense_5, launch_dense_6, launch_dense_7}},
+    {{2048, 32, 4, 128, 128, 8, 768, 64}, {launch_full_0, launch_full_1, launch_full_2, launch_full_3, launch_full_4, launch_full_5, launch_full_6, launch_full_7}},
 };
 
 int cuda_fail(cudaError_t e, const char* what) {
@@ -106,20 +107,23 @@ int encode_pool(CUtensorMap* tm, void* pool, const mk_sched* s, int64_t num_page
   return MK_OK;
 }
 
-// A row-major BF16 matrix [rows][cols] as a 2-D tensor for the tcgen05
-// items: boxes of kTcK columns (128 bytes) by box_rows rows, swizzled in
-// 128-byte rows (the K-major operand layout the MMA descriptors name).
+// A row-major matrix [rows][cols] of BF16 (elem_bytes 2) or 8-bit codes
+// (elem_bytes 1) as a 2-D tensor for the tcgen05 items: boxes of 128 bytes
+// of a row (kTcK BF16 or kTcK8 codes) by box_rows rows, swizzled in 128-byte
+// rows (the K-major operand layout the MMA descriptors name).
 int encode_operand(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
-                   const char* what) {
+                   const char* what, int elem_bytes = 2) {
   EncodeTiledFn fn = encode_tiled();
   if (!fn) return fail(MK_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-  if (!base || rows >= (1ull << 31) || cols % kTcK != 0)
+  const uint32_t box_cols = 128u / (uint32_t)elem_bytes;
+  if (!base || rows >= (1ull << 31) || cols % box_cols != 0)
     return fail(MK_ERR_ARG, std::string("no tcgen05 operand layout for ") + what);
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kTcK, box_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * elem_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  const CUresult r = fn(tm, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
@@ -130,7 +134,8 @@ int encode_operand(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t co
 // The weights as tcgen05 A operands: boxes of the rows one item copies --
 // kTcDenseRows for QKV, O-proj and LM-head tiles, kTcRouterRows for router
 // tasks, kTcMoeRows for down tiles, blocks of 16 rows of the gate and up
-// matrices (an up/gate tile interleaves them).
+// matrices (an up/gate tile interleaves them).  FP8 experts: the expert
+// matrices as E4M3 bytes.
 int encode_weight_maps(mk_model* m) {
   if (m->tm_ready) return MK_OK;
   const mk_config& c = m->cfg;
@@ -141,23 +146,32 @@ int encode_weight_maps(mk_model* m) {
   if (rc == MK_OK) rc = encode_operand(&m->tm_w[1], w.w_o, L * D.H, (uint64_t)D.NQ * D.D, kTcDenseRows, "w_o");
   if (rc == MK_OK) rc = encode_operand(&m->tm_w[2], w.w_router, L * D.E, D.H, kTcRouterRows, "w_router");
   if (rc == MK_OK) rc = encode_operand(&m->tm_w[3], w.w_lm, (uint64_t)c.vocab, D.H, kTcDenseRows, "w_lm");
-  if (rc == MK_OK) rc = encode_operand(&m->tm_w[4], w.w_gate, L * D.E * D.I, D.H, 16, "w_gate");
-  if (rc == MK_OK) rc = encode_operand(&m->tm_w[5], w.w_up, L * D.E * D.I, D.H, 16, "w_up");
-  if (rc == MK_OK) rc = encode_operand(&m->tm_w[6], w.w_down, L * D.E * D.H, D.I, kTcMoeRows, "w_down");
+  const int eb = c.expert_fp8 ? 1 : 2;
+  if (rc == MK_OK) rc = encode_operand(&m->tm_w[4], w.w_gate, L * D.E * D.I, D.H, 16, "w_gate", eb);
+  if (rc == MK_OK) rc = encode_operand(&m->tm_w[5], w.w_up, L * D.E * D.I, D.H, 16, "w_up", eb);
+  if (rc == MK_OK) rc = encode_operand(&m->tm_w[6], w.w_down, L * D.E * D.H, D.I, kTcMoeRows, "w_down", eb);
   if (rc == MK_OK) m->tm_ready = true;
   return rc;
 }
 
 // The activation operands of the tcgen05 items in the workspace: boxes of
-// tc_nb rows (every activation row as a hi row and a lo row).
+// tc_nb rows (every activation row as a hi row and a lo row); with FP8
+// experts the expert tiles' operands are E5M2 term rows in boxes of tc_nb8.
 int encode_act_maps(mk_sched* s, uint8_t* ws) {
   if (s->tm_ws == ws) return MK_OK;
   const ShapeDims& D = s->dims;
-  const uint64_t nb = (uint64_t)s->tc_nb, routed = std::max<uint64_t>(2ull * s->max_batch * D.K, nb);
+  const uint64_t nb = (uint64_t)s->tc_nb;
   int rc = encode_operand(&s->tm_act[0], ws + s->ws.off("xb"), nb, D.H, s->tc_nb, "xb");
   if (rc == MK_OK) rc = encode_operand(&s->tm_act[1], ws + s->ws.off("attnb"), nb, (uint64_t)D.NQ * D.D, s->tc_nb, "attnb");
-  if (rc == MK_OK) rc = encode_operand(&s->tm_act[2], ws + s->ws.off("xgb"), routed, D.H, s->tc_nb, "xgb");
-  if (rc == MK_OK) rc = encode_operand(&s->tm_act[3], ws + s->ws.off("ub"), routed, D.I, s->tc_nb, "ub");
+  if (s->tc_fp8) {
+    const uint64_t routed = std::max<uint64_t>((uint64_t)kTcF8Terms * s->max_batch * D.K, (uint64_t)s->tc_nb8);
+    if (rc == MK_OK) rc = encode_operand(&s->tm_act[2], ws + s->ws.off("xg8"), routed, D.H, s->tc_nb8, "xg8", 1);
+    if (rc == MK_OK) rc = encode_operand(&s->tm_act[3], ws + s->ws.off("u8"), routed, D.I, s->tc_nb8, "u8", 1);
+  } else {
+    const uint64_t routed = std::max<uint64_t>(2ull * s->max_batch * D.K, nb);
+    if (rc == MK_OK) rc = encode_operand(&s->tm_act[2], ws + s->ws.off("xgb"), routed, D.H, s->tc_nb, "xgb");
+    if (rc == MK_OK) rc = encode_operand(&s->tm_act[3], ws + s->ws.off("ub"), routed, D.I, s->tc_nb, "ub");
+  }
   s->tm_ws = rc == MK_OK ? ws : nullptr;
   return rc;
 }
@@ -461,12 +475,20 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
     if (rc != MK_OK) return rc;
     p.tm_wqkv = m->tm_w[0]; p.tm_wo = m->tm_w[1]; p.tm_wr = m->tm_w[2]; p.tm_wlm = m->tm_w[3];
     p.tm_wg = m->tm_w[4]; p.tm_wu = m->tm_w[5]; p.tm_wd = m->tm_w[6];
-    p.tm_xb = s->tm_act[0]; p.tm_attnb = s->tm_act[1]; p.tm_xgb = s->tm_act[2]; p.tm_ub = s->tm_act[3];
+    p.tm_xb = s->tm_act[0]; p.tm_attnb = s->tm_act[1];
     p.xb = reinterpret_cast<uint16_t*>(at("xb"));
     p.attnb = reinterpret_cast<uint16_t*>(at("attnb"));
-    p.xgb = reinterpret_cast<uint16_t*>(at("xgb"));
-    p.ub = reinterpret_cast<uint16_t*>(at("ub"));
     p.tc_nb = s->tc_nb;
+    if (s->tc_fp8) {
+      p.tm_xg8 = s->tm_act[2]; p.tm_u8 = s->tm_act[3];
+      p.xg8 = at("xg8");
+      p.u8 = at("u8");
+      p.tc_nb8 = s->tc_nb8;
+    } else {
+      p.tm_xgb = s->tm_act[2]; p.tm_ub = s->tm_act[3];
+      p.xgb = reinterpret_cast<uint16_t*>(at("xgb"));
+      p.ub = reinterpret_cast<uint16_t*>(at("ub"));
+    }
   }
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -475,7 +497,7 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
   cudaError_t e = cudaMemsetAsync(workspace, 0, zero_bytes, st);
   if (e != cudaSuccess) return cuda_fail(e, "barrier reset");
   // the kernel build for the model's expert format and the schedule's batch
-  const int mode = s->tc               ? kModeTc
+  const int mode = s->tc               ? (s->tc_fp8 ? kModeTcFp8 : kModeTc)
                    : m->cfg.expert_fp4 ? (s->lean ? kModeFp4Lean : kModeFp4)
                    : m->cfg.expert_fp8 ? (s->lean ? kModeFp8Lean : kModeFp8)
                    : s->max_batch <= kTB && s->lean ? kModeSmallBatch : kModeAnyBatch;

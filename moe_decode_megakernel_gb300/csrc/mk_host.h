@@ -69,6 +69,10 @@ struct mk_sched {
   // kTB; 128-row weight tiles, explicit gather, the BF16 hi/lo operand rows
   bool tc = false;
   int tc_nb = 0;  // rows of an activation operand box (2 max_batch, rounded up to 16)
+  // FP8 experts (kModeTcFp8): the expert tiles on FP8 MMAs, their activation
+  // operands as E5M2 term rows (boxes of kTcF8Terms max_batch, rounded up to 16)
+  bool tc_fp8 = false;
+  int tc_nb8 = 0;
   // tensor maps of the activation operands, for the workspace they were made for
   const void* tm_ws = nullptr;
   CUtensorMap tm_act[4];

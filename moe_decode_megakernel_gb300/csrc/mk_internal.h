@@ -115,7 +115,8 @@ enum KernelMode : int {
   kModeFp8Lean = 4,     // FP8 experts, lean schedules
   kModeFp4Lean = 5,     // FP4 experts, lean schedules
   kModeTc = 6,          // BF16 experts, max_batch > kTB: GEMM items on the tcgen05 tensor cores
-  kModeCount = 7
+  kModeTcFp8 = 7,       // FP8 experts, max_batch > kTB: kModeTc with the expert tiles on FP8 MMAs
+  kModeCount = 8
 };
 #if defined(__CUDACC__)
 #define MK_HOST_DEVICE __host__ __device__
@@ -124,6 +125,7 @@ enum KernelMode : int {
 #endif
 MK_HOST_DEVICE constexpr bool mode_fp8(int m) { return m == kModeFp8 || m == kModeFp8Lean; }
 MK_HOST_DEVICE constexpr bool mode_fp4(int m) { return m == kModeFp4 || m == kModeFp4Lean; }
+MK_HOST_DEVICE constexpr bool mode_tc(int m) { return m == kModeTc || m == kModeTcFp8; }
 MK_HOST_DEVICE constexpr bool mode_lean(int m) {
   return m == kModeSmallBatch || m == kModeFp8Lean || m == kModeFp4Lean;
 }
@@ -235,6 +237,17 @@ MK_HOST_DEVICE constexpr int tc_kblocks_per_stage(uint32_t a_bytes, int tc_nb) {
 }
 static_assert(kTcMaxN >= 2 * kMaxBatch, "hi/lo rows of the largest batch fit a stage");
 
+// FP8 expert tiles of kModeTcFp8: a k-block is 128 E4M3 weights (128 bytes,
+// the same 16 KB box of kTcRows rows).  The activation operand holds every
+// routed row as kTcF8Terms E5M2 rows whose values, scaled by 8^-j for row j,
+// sum to the activation within 2^-12 of it (E5M2 keeps 3 significant bits:
+// each term leaves at most 1/8 of the rest), so the MMA's N is kTcF8Terms
+// per routed row, at most kTcMaxN: batches of at most kTcF8MaxBatch rows.
+constexpr int kTcK8 = 128;
+constexpr int kTcF8Terms = 4;
+constexpr int kTcF8MaxBatch = kTcMaxN / kTcF8Terms;
+static_assert(kTcF8MaxBatch >= 32, "FP8 expert tiles up to batch 32");
+
 // The MoE plan of tcgen05 items: up/gate tiles of kTcMoeRows / 2 gate rows
 // and the same up rows, down tiles of kTcMoeRows rows (the MMA's M = 128 has
 // the rest unused); "stages" count k-blocks.
@@ -248,6 +261,13 @@ constexpr MoePlan moe_plan_tc(ShapeDims s) {
   p.dn_stages = s.I / kTcK;
   p.dn_tile = kTcMoeRows;
   p.dn_tiles = s.H / p.dn_tile;
+  return p;
+}
+// the same tiles over FP8 expert rows: k-blocks of kTcK8
+constexpr MoePlan moe_plan_tc8(ShapeDims s) {
+  MoePlan p = moe_plan_tc(s);
+  p.up_stages = s.H / kTcK8;
+  p.dn_stages = s.I / kTcK8;
   return p;
 }
 
@@ -338,6 +358,13 @@ struct Params {
   uint16_t* xgb;        // [MB K][2][H]    the routed rows in expert order (written by MOE_GATHER)
   uint16_t* ub;         // [MB K][2][I]    the SwiGLU activations (written by the up/gate tiles)
   int tc_nb;            // rows of an activation box: 2 MB rounded up to 16 (the MMA's N)
+  // kModeTcFp8: the expert tiles' activation operands as E5M2 term rows
+  // (row kTcF8Terms r + j holds term j of routed row r), boxes of kTcK8
+  // columns by tc_nb8 rows; the weight maps tm_wg, tm_wu, tm_wd hold E4M3 bytes
+  CUtensorMap tm_xg8, tm_u8;
+  uint8_t* xg8;         // [MB K][kTcF8Terms][H] the routed rows in expert order (MOE_GATHER)
+  uint8_t* u8;          // [MB K][kTcF8Terms][I] the SwiGLU activations (the up/gate tiles)
+  int tc_nb8;           // kTcF8Terms MB rounded up to 16 (the expert tiles' N)
 
   int split_len;        // tokens per KV slice
   int n_static;         // static slices per (row, group) of a sliding layer

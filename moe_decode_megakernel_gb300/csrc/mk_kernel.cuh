@@ -196,6 +196,17 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[smem] * B[smem]^T: 8-bit operands (kind::f8f6f4, the formats
+// named by the instruction descriptor; one MMA takes K = 32, 32 bytes of each
+// K-major row), fp32 accumulator.
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // One arrival on `b` once every tcgen05 operation this thread issued before has completed.
 __device__ __forceinline__ void tc_commit(uint64_t* b) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(b))
@@ -233,6 +244,11 @@ __device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr) {
 // Instruction descriptor of kind::f16: fp32 D, BF16 A and B, both K-major, M x N.
 __host__ __device__ constexpr uint32_t tc_idesc_bf16(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+// Instruction descriptor of kind::f8f6f4: fp32 D, E4M3 A (format 0), E5M2 B
+// (format 1), both K-major, M x N.
+__host__ __device__ constexpr uint32_t tc_idesc_e4m3_e5m2(int m, int n) {
+  return (1u << 4) | (0u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -336,6 +352,35 @@ __device__ __forceinline__ void store_hilo4(uint16_t* hi, uint16_t* lo, float4 v
   *reinterpret_cast<uint2*>(hi) = make_uint2(h0, h1);
   *reinterpret_cast<uint2*>(lo) = make_uint2(l0, l1);
 }
+// E5M2 codes (1 sign, 5 exponent, 2 mantissa bits: the upper byte of an IEEE
+// half).  f_e5m2x2 rounds two floats to nearest even, saturating at +-57344,
+// a's code in the low byte; e5m2_f is exact.
+__device__ __forceinline__ uint32_t f_e5m2x2(float a, float b) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+  return r;
+}
+__device__ __forceinline__ float e5m2_f(uint32_t code) {
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"((unsigned short)((code & 0xffu) << 8)));
+  return f;
+}
+// The FP8 tensor-core operand of four consecutive activations: kTcF8Terms
+// E5M2 words, term j at row0 + j * term_stride.  Term j codes the remainder
+// the earlier terms leave, times 8^j: x = sum_j code_j 8^-j to within 2^-12 |x|
+// (exact differences: each code is within a factor of two of its input).
+__device__ __forceinline__ void store_e5m2_terms4(uint8_t* row0, int64_t term_stride, float4 v) {
+  float r0 = v.x, r1 = v.y, r2 = v.z, r3 = v.w;
+#pragma unroll
+  for (int j = 0; j < kTcF8Terms; ++j) {
+    const uint32_t word = f_e5m2x2(r0, r1) | (f_e5m2x2(r2, r3) << 16);
+    *reinterpret_cast<uint32_t*>(row0 + j * term_stride) = word;
+    r0 = (r0 - e5m2_f(word)) * 8.f;
+    r1 = (r1 - e5m2_f(word >> 8)) * 8.f;
+    r2 = (r2 - e5m2_f(word >> 16)) * 8.f;
+    r3 = (r3 - e5m2_f(word >> 24)) * 8.f;
+  }
+}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(FULL, v, m);
@@ -377,7 +422,7 @@ __host__ __device__ constexpr int xs_row() {
 // The MoE tile plan of a kernel mode's expert weights (BF16, FP8 or FP4 rows).
 template <class S, int M>
 __host__ __device__ constexpr MoePlan plan_of() {
-  return M == kModeTc ? S::mptc : mode_fp4(M) ? S::mp4 : mode_fp8(M) ? S::mp8 : S::mp;
+  return M == kModeTcFp8 ? S::mptc8 : mode_tc(M) ? S::mptc : mode_fp4(M) ? S::mp4 : mode_fp8(M) ? S::mp8 : S::mp;
 }
 
 template <class S>
@@ -421,6 +466,7 @@ struct Shape {
   static constexpr MoePlan mp8 = moe_plan8(dims);  // FP8 expert rows
   static constexpr MoePlan mp4 = moe_plan4(dims);  // FP4 expert rows
   static constexpr MoePlan mptc = moe_plan_tc(dims);  // tcgen05 GEMM tiles
+  static constexpr MoePlan mptc8 = moe_plan_tc8(dims);  // the same over FP8 expert rows
   static constexpr int SR_H = stage_rows(H), SR_O = stage_rows(G * D), SR_I = stage_rows(I);
   static_assert(H % 256 == 0 && (G * D) % 8 == 0 && I % 8 == 0, "row chunks");
   static_assert(D % 32 == 0 && 32 % G == 0 && (G * D) % 4 == 0, "attention lane maps");
@@ -667,18 +713,22 @@ struct Producer {
   // With a weight box of a_bytes < kTcABytes (a router task's rows), a stage
   // takes kps = tc_kblocks_per_stage(a_bytes) k-blocks: weight box j at
   // j * a_bytes, activation box j at kTcABytes + j * (its bytes).
+  // FP8 expert tiles (kModeTcFp8) take k-blocks of kk = kTcK8 one-byte
+  // weights and activation boxes of nb = tc_nb8 term rows: 128-byte rows as
+  // for BF16, so the stage layout is the same.
   __device__ __forceinline__ bool tc_stages(const int32_t* it, const CUtensorMap* ta, int ax, int ay, bool updown,
                                             const CUtensorMap* tb, int bx, int by, int nkb,
-                                            uint32_t a_bytes = kTcABytes) {
-    const uint32_t bbytes = (uint32_t)p.tc_nb * kTcK * 2;
-    const int kps = tc_kblocks_per_stage(a_bytes, p.tc_nb);
+                                            uint32_t a_bytes = kTcABytes, int kk = kTcK, int nb = 0) {
+    if (nb == 0) nb = p.tc_nb;
+    const uint32_t bbytes = (uint32_t)nb * kTcK * 2;
+    const int kps = tc_kblocks_per_stage(a_bytes, nb);
     const int nst = (nkb + kps - 1) / kps;
     const uint32_t first = c.st;
     bool ready = false;
     auto issue_b = [&](uint32_t gs, int st) {
       for (int j = 0; j < kps && st * kps + j < nkb; ++j) {
         uint8_t* dst = stage(gs % kStages) + kTcABytes + j * bbytes;
-        tma_2d_plain(dst, tb, bx + (st * kps + j) * kTcK, by, &c.hdr->full[gs % kStages]);
+        tma_2d_plain(dst, tb, bx + (st * kps + j) * kk, by, &c.hdr->full[gs % kStages]);
       }
     };
     auto wait_inputs = [&]() -> bool {
@@ -704,7 +754,7 @@ struct Producer {
       const int nk = min(kps, nkb - st * kps);
       mbar_expect_tx(fb, (uint32_t)nk * (a_bytes + bbytes));
       for (int j = 0; j < nk; ++j) {
-        const int x = ax + (st * kps + j) * kTcK;
+        const int x = ax + (st * kps + j) * kk;
         if (updown) {  // 16-row blocks: gate block q, then up block q
 #pragma unroll
           for (int q = 0; q < kTcMoeRows / 32; ++q) {
@@ -748,7 +798,7 @@ struct Producer {
   }
 
   __device__ __forceinline__ bool dense(const int32_t* d) {
-    if constexpr (M == kModeTc) return tc_dense(d);
+    if constexpr (mode_tc(M)) return tc_dense(d);
     int32_t it[32];
     for (int i = 0; i < 32; ++i) it[i] = d[i];
     const int op = d[F_OP], l = d[F_LAYER], row0 = d[F_A0], rows = d[F_A0 + 1];
@@ -1049,20 +1099,25 @@ struct Producer {
           carried = true;
         }
       }
-      if constexpr (M == kModeTc) {
+      if constexpr (mode_tc(M)) {
         // one item of nkb k-blocks: the expert's gate/up or down rows against
-        // its routed rows (their hi/lo rows start at row 2 row0)
+        // its routed rows (their hi/lo rows start at row 2 row0; FP8 experts:
+        // their E5M2 term rows at row kTcF8Terms row0)
+        constexpr bool f8 = M == kModeTcFp8;
+        constexpr int kk = f8 ? kTcK8 : kTcK, nt = f8 ? kTcF8Terms : 2;
+        const int nb = f8 ? p.tc_nb8 : p.tc_nb;
         const int64_t le = (int64_t)l * S::E + e;
-        constexpr uint32_t ab = kTcMoeRows * kTcK * 2;
-        const int nkb = up ? S::H / kTcK : S::I / kTcK, kps = tc_kblocks_per_stage(ab, p.tc_nb);
+        constexpr uint32_t ab = kTcMoeRows * kTcK * 2;  // 128 rows of 128 bytes (BF16 or FP8)
+        const int nkb = up ? S::H / kk : S::I / kk, kps = tc_kblocks_per_stage(ab, nb);
         it[F_NSTAGE] = (nkb + kps - 1) / kps;
         it[F_A0 + 13] = nkb;
         if (!push(it)) return false;
         if (up) {
-          if (!tc_stages(it, nullptr, 0, (int)(le * S::I + t * mp.up_tile), true, &p.tm_xgb, 0, 2 * row0, nkb, ab))
+          if (!tc_stages(it, nullptr, 0, (int)(le * S::I + t * mp.up_tile), true, f8 ? &p.tm_xg8 : &p.tm_xgb, 0,
+                         nt * row0, nkb, ab, kk, nb))
             return false;
-        } else if (!tc_stages(it, &p.tm_wd, 0, (int)(le * S::H + t * mp.dn_tile), false, &p.tm_ub, 0, 2 * row0, nkb,
-                              ab)) {
+        } else if (!tc_stages(it, &p.tm_wd, 0, (int)(le * S::H + t * mp.dn_tile), false, f8 ? &p.tm_u8 : &p.tm_ub, 0,
+                              nt * row0, nkb, ab, kk, nb)) {
           return false;
         }
       } else {
@@ -1297,7 +1352,7 @@ struct Consumer {
   // Every read of a stage is an explicit shared-memory load (ld.shared,
   // ldmatrix), which the release orders before the arrival.
   __device__ __forceinline__ void stage_release(int slot) {
-    if constexpr (M == kModeTc) {  // one arrival, after every consumer warp's reads
+    if constexpr (mode_tc(M)) {  // one arrival, after every consumer warp's reads
       consumers_sync();
       if (ct == 0) mbar_arrive(&c.hdr->empty[slot]);
     } else {
@@ -2190,10 +2245,10 @@ struct Consumer {
     float* dst = p.attn_out + (int64_t)b * S::NQ * D + col;
 #pragma unroll
     for (int i = 0; i < DPL; ++i) dst[i] = o[i];
-    if constexpr (M == kModeTc && DPL == 4) {
+    if constexpr (mode_tc(M) && DPL == 4) {
       store_hilo4(p.attnb + (int64_t)(2 * b) * S::NQ * D + col, p.attnb + (int64_t)(2 * b + 1) * S::NQ * D + col,
                   make_float4(o[0], o[1 % DPL], o[2 % DPL], o[3 % DPL]));
-    } else if constexpr (M == kModeTc) {
+    } else if constexpr (mode_tc(M)) {
 #pragma unroll
       for (int i = 0; i < DPL; ++i) {
         const uint16_t hi = f_bf16(o[i]);
@@ -2283,7 +2338,7 @@ struct Consumer {
       const float o = a / zt;
       const int64_t col = (int64_t)(g * G + h) * D + ct;
       p.attn_out[(int64_t)b * S::NQ * D + col] = o;
-      if constexpr (M == kModeTc) {
+      if constexpr (mode_tc(M)) {
         const uint16_t hi = f_bf16(o);
         p.attnb[(int64_t)(2 * b) * S::NQ * D + col] = hi;
         p.attnb[(int64_t)(2 * b + 1) * S::NQ * D + col] = f_bf16(o - bf16_f(hi));
@@ -2507,7 +2562,7 @@ struct Consumer {
           const float4 xv =
               make_float4(a.x * inv_rms * gm.x, a.y * inv_rms * gm.y, a.z * inv_rms * gm.z, a.w * inv_rms * gm.w);
           reinterpret_cast<float4*>(p.x + (int64_t)b * S::H)[i4] = xv;
-          if constexpr (M == kModeTc)
+          if constexpr (mode_tc(M))
             store_hilo4(p.xb + (int64_t)(2 * b) * S::H + 4 * i4, p.xb + (int64_t)(2 * b + 1) * S::H + 4 * i4, xv);
           if (!final_norm) hout[i4] = a;
           if (p.htrace) reinterpret_cast<float4*>(p.htrace + ((int64_t)l * p.MB + b) * S::H)[i4] = a;
@@ -2828,7 +2883,9 @@ struct Consumer {
         for (int q = 0; q < PL; ++q) {
           const int cc = lane + 32 * q;
           if (C % 32 != 0 && cc >= C) continue;
-          if constexpr (M == kModeTc)  // the tcgen05 items read only the BF16 operand rows
+          if constexpr (M == kModeTcFp8)  // the FP8 expert tiles read the E5M2 term rows
+            store_e5m2_terms4(p.xg8 + (int64_t)kTcF8Terms * r * S::H + 4 * cc, S::H, xv[q]);
+          else if constexpr (M == kModeTc)  // the tcgen05 items read only the BF16 operand rows
             store_hilo4(p.xgb + (int64_t)(2 * r) * S::H + 4 * cc, p.xgb + (int64_t)(2 * r + 1) * S::H + 4 * cc, xv[q]);
           else
             reinterpret_cast<float4*>(p.xg + (int64_t)r * S::H)[cc] = xv[q];
@@ -2873,12 +2930,17 @@ struct Consumer {
     const uint32_t a_bytes = op == OP_ROUTER_GEMM                      ? kTcRouterRows * kTcK * 2
                              : (op == W_UP_TILE || op == W_DOWN_TILE) ? kTcMoeRows * kTcK * 2
                                                                       : kTcDenseRows * kTcK * 2;
-    const int kps = tc_kblocks_per_stage(a_bytes, p.tc_nb);
-    const uint32_t bbytes = (uint32_t)p.tc_nb * kTcK * 2;
+    // FP8 expert tiles: E4M3 weights against the E5M2 term rows
+    const bool f8 = M == kModeTcFp8 && (op == W_UP_TILE || op == W_DOWN_TILE);
+    const int nb = f8 ? p.tc_nb8 : p.tc_nb;
+    const int kps = tc_kblocks_per_stage(a_bytes, nb);
+    const uint32_t bbytes = (uint32_t)nb * kTcK * 2;
     if (ct == 0) {
       tc_fence_after();
-      constexpr uint32_t kDescK = 16 * 2 / 16;  // one MMA's K (16 BF16 = 32 bytes) in descriptor units
-      const uint32_t idesc = tc_idesc_bf16(kTcRows, p.tc_nb);
+      // one MMA's K in descriptor units: 32 bytes (16 BF16 or 32 FP8 values),
+      // four MMAs per 128-byte k-block
+      constexpr uint32_t kDescK = 32 / 16;
+      const uint32_t idesc = f8 ? tc_idesc_e4m3_e5m2(kTcRows, nb) : tc_idesc_bf16(kTcRows, nb);
       for (int st = 0; st < nst; ++st) {
         const uint32_t gs = c.st + (uint32_t)st;
         const int slot = (int)(gs % kStages);
@@ -2886,9 +2948,15 @@ struct Consumer {
         const uint32_t a = smem_u32(stage(slot));
         for (int j = 0; j < kps && st * kps + j < nkb; ++j) {
           const uint64_t ad = tc_desc_sw128(a + j * a_bytes), bd = tc_desc_sw128(a + kTcABytes + j * bbytes);
+          if (M == kModeTcFp8 && f8) {
 #pragma unroll
-          for (int k = 0; k < kTcK / 16; ++k)
-            tc_mma_bf16(tmem, ad + (uint64_t)(kDescK * k), bd + (uint64_t)(kDescK * k), idesc, (st | j | k) != 0);
+            for (int k = 0; k < 4; ++k)
+              tc_mma_f8(tmem, ad + (uint64_t)(kDescK * k), bd + (uint64_t)(kDescK * k), idesc, (st | j | k) != 0);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tc_mma_bf16(tmem, ad + (uint64_t)(kDescK * k), bd + (uint64_t)(kDescK * k), idesc, (st | j | k) != 0);
+          }
         }
         // the stage goes back to the producer once these MMAs have read it (in
         // this build a stage's empty barrier takes one arrival)
@@ -2917,6 +2985,12 @@ struct Consumer {
     const int ntok = moe ? w[F_A0 + 3] : p.B;
     const int nrows = moe ? kTcMoeRows : w[F_A0 + 1];
     if (r >= ((nrows + 31) & ~31)) return;  // a warp quarter of unused MMA rows (uniform per warp)
+    if constexpr (M == kModeTcFp8) {
+      if (moe) {
+        tc_epilogue_f8(w, op, l, q, half, r, ntok);
+        return;
+      }
+    }
     constexpr MoePlan mp = S::mptc;
     for (int j = half; 8 * j < ntok; j += 2) {
       float c16[16];
@@ -3014,6 +3088,66 @@ struct Consumer {
     }
   }
 
+  // The accumulator of an FP8 expert tile (kModeTcFp8): columns
+  // kTcF8Terms t + j hold the products with term j of routed row t, so row t's
+  // value is their sum scaled by 8^-j, times the weight row's scale (E4M3 code
+  // times the row scale is the weight).  Chunks of 4 routed rows (16 columns),
+  // the two warps of a lane quarter taking alternate chunks.  The up/gate
+  // epilogue writes the SwiGLU activations as the down tiles' E5M2 term rows.
+  __device__ __forceinline__ void tc_epilogue_f8(const int32_t* w, int op, int l, int q, int half, int r, int ntok) {
+    constexpr MoePlan mp = S::mptc8;
+    static_assert(kTcF8Terms == 4, "four term columns per routed row: 4 rows per 16-column load");
+    const int64_t le = (int64_t)l * S::E + w[F_A0];
+    const bool up_tile = op == W_UP_TILE;
+    // this lane's weight row: gate row 16 q + lane (lanes 0-15) or the same up
+    // row (lanes 16-31) of an up/gate tile; down row r of a down tile
+    const int col = w[F_A0 + 1] * mp.up_tile + 16 * q + (lane & 15);
+    const int n = w[F_A0 + 1] * mp.dn_tile + r;
+    const float scale = up_tile ? __ldg((lane < 16 ? p.sg : p.su) + le * S::I + col) : __ldg(p.sd + le * S::H + n);
+    for (int j = half; 4 * j < ntok; j += 2) {
+      float c16[16];
+      tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(16 * j), c16);
+      float v[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        v[t] = scale * (c16[4 * t] + 0.125f * (c16[4 * t + 1] + 0.125f * (c16[4 * t + 2] + 0.125f * c16[4 * t + 3])));
+      if (up_tile) {
+        float upv[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) upv[t] = __shfl_down_sync(FULL, v[t], 16);
+        if (lane < 16) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            if (4 * j + t < ntok) {
+              const int row = w[F_A0 + 2] + 4 * j + t;  // expert-ordered routed row
+              float act = v[t] / (1.f + expf(-v[t])) * upv[t];
+              p.u[(int64_t)row * S::I + col] = act;
+              uint8_t* dst = p.u8 + (int64_t)kTcF8Terms * row * S::I + col;
+#pragma unroll
+              for (int k = 0; k < kTcF8Terms; ++k) {
+                const uint32_t code = f_e5m2x2(act, 0.f) & 0xffu;
+                dst[(int64_t)k * S::I] = (uint8_t)code;
+                act = (act - e5m2_f(code)) * 8.f;
+              }
+            }
+        }
+      } else {
+        int slot[4];
+        float wt[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          slot[t] = 4 * j + t < ntok ? __ldcg(p.perm + w[F_A0 + 2] + 4 * j + t) : 0;
+          if (slot[t] < 0 || slot[t] >= p.B * S::K) slot[t] = 0;  // only after a failed step
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) wt[t] = __ldcg(p.topk_w + (int64_t)l * p.MB * S::K + slot[t]);
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          if (4 * j + t < ntok) p.y[(int64_t)slot[t] * S::H + n] = wt[t] * v[t];
+      }
+    }
+  }
+
   // One QKV rotation pair (rows dd, dd + 1 of head `head`) of activation row
   // b: RoPE by pos * base^(-dd/D) (angle reduced modulo 2 pi in double,
   // then sin/cos in float) on q and k; q to its buffer, k and v to the pool.
@@ -3046,7 +3180,7 @@ struct Consumer {
   }
 
   __device__ __forceinline__ void execute(const int32_t* w) {
-    if constexpr (M == kModeTc) {
+    if constexpr (mode_tc(M)) {
       switch (w[F_OP]) {
         case OP_QKV_PROJ:
         case OP_LM_HEAD:
@@ -3149,12 +3283,12 @@ struct Consumer {
     for (int i = ct; i < S::D / 2; i += kConsumerThreads)
       sm.rope_theta[i] = pow((double)p.rope_base, -(double)(2 * i) / (double)S::D);
     if (ct < 4) sm.xtag[ct] = sm.qtag[ct] = -1;
-    if constexpr (M == kModeTc) {
+    if constexpr (mode_tc(M)) {
       if (cw == 0) tmem_alloc(&c.hdr->tmem_addr, kTcCols);
       tc_fence_before();
     }
     consumers_sync();
-    if constexpr (M == kModeTc) {
+    if constexpr (mode_tc(M)) {
       tc_fence_after();
       tmem = c.hdr->tmem_addr;
     }
@@ -3323,7 +3457,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_persistent(const __grid_consta
       mbar_init(&hdr->full[i], 1);
       // the tcgen05 build hands a stage back with one arrival (a commit of the
       // MMAs that read it, or one thread after the block's last read)
-      mbar_init(&hdr->empty[i], M == kModeTc ? 1 : kConsumerWarps);
+      mbar_init(&hdr->empty[i], mode_tc(M) ? 1 : kConsumerWarps);
     }
     for (int i = 0; i < kDescRing; ++i) {
       mbar_init(&hdr->dfull[i], 1);
@@ -3353,7 +3487,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_persistent(const __grid_consta
     const int ct = threadIdx.x - 96;
     Consumer<S, M> cs{p, c, *scr, ct, ct / 32, ct & 31};
     cs.run();
-    if constexpr (M == kModeTc) cs.tc_release();
+    if constexpr (mode_tc(M)) cs.tc_release();
   }
 }
 

@@ -823,8 +823,13 @@ static void layout_workspace(mk_sched* s) {
   if (s->tc) {  // the BF16 hi/lo operand rows of the tcgen05 items (at least one box of rows each)
     w.add("xb", 2ull * s->tc_nb * D.H);
     w.add("attnb", 2ull * s->tc_nb * D.NQ * D.D);
-    w.add("xgb", 2ull * std::max(2 * MB * D.K, s->tc_nb) * D.H);
-    w.add("ub", 2ull * std::max(2 * MB * D.K, s->tc_nb) * D.I);
+    if (s->tc_fp8) {  // FP8 expert tiles: E5M2 term rows, one byte each
+      w.add("xg8", 1ull * std::max(kTcF8Terms * MB * D.K, s->tc_nb8) * D.H);
+      w.add("u8", 1ull * std::max(kTcF8Terms * MB * D.K, s->tc_nb8) * D.I);
+    } else {
+      w.add("xgb", 2ull * std::max(2 * MB * D.K, s->tc_nb) * D.H);
+      w.add("ub", 2ull * std::max(2 * MB * D.K, s->tc_nb) * D.I);
+    }
   }
   if (s->opts.trace_hidden) w.add("hidden_trace", sizeof(float) * (size_t)(L + 1) * MB * D.H);
   if (s->opts.trace_queue) w.add("queue_trace", sizeof(int32_t) * (size_t)L * queue_trace_stride(D.E, MB * D.K));
@@ -1152,8 +1157,12 @@ int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const 
   *out = nullptr;
   if (max_batch < 1 || max_batch > kMaxBatch) return fail(MK_ERR_ARG, "max_batch must be in [1, 64]");
   if (max_ctx < 1) return fail(MK_ERR_ARG, "max_ctx must be >= 1");
-  if ((m->cfg.expert_fp8 || m->cfg.expert_fp4) && max_batch > kTB)
-    return fail(MK_ERR_UNSUPPORTED, "FP8 and FP4 experts are compiled for max_batch <= 2");
+  if (m->cfg.expert_fp4 && max_batch > kTB) return fail(MK_ERR_UNSUPPORTED, "FP4 experts are compiled for max_batch <= 2");
+  if (m->cfg.expert_fp8 && max_batch > kTcF8MaxBatch)
+    return fail(MK_ERR_UNSUPPORTED, "FP8 experts are compiled for max_batch <= " + std::to_string(kTcF8MaxBatch) +
+                                        " (the MMA's N holds four E5M2 term rows per routed row)");
+  if (m->cfg.expert_fp8 && max_batch > kTB && (m->dims.H % kTcK8 || m->dims.I % kTcK8))
+    return fail(MK_ERR_UNSUPPORTED, "FP8 experts above batch 2 need hidden and inter multiples of 128");
   mk_sched* s = new mk_sched();
   s->cfg = m->cfg;
   s->dims = m->dims;
@@ -1163,11 +1172,14 @@ int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const 
   s->max_batch = max_batch;
   s->max_ctx = max_ctx;
   // batches beyond the GEMV's kTB rows: the weight tiles are real contractions,
-  // run on the tcgen05 tensor cores (BF16 experts of an MoE model)
-  s->tc = max_batch > kTB && !m->cfg.expert_fp8 && !m->cfg.expert_fp4 && !(m->dims.E == 1 && m->dims.K == 1);
+  // run on the tcgen05 tensor cores (BF16 or FP8 experts of an MoE model)
+  // (FP8 experts: the expert tiles on FP8 MMAs against E5M2 term rows)
+  s->tc = max_batch > kTB && !m->cfg.expert_fp4 && !(m->dims.E == 1 && m->dims.K == 1);
   if (s->tc) {
-    s->plan = moe_plan_tc(m->dims);
+    s->tc_fp8 = m->cfg.expert_fp8 != 0;
+    s->plan = s->tc_fp8 ? moe_plan_tc8(m->dims) : moe_plan_tc(m->dims);
     s->tc_nb = (2 * max_batch + 15) / 16 * 16;
+    s->tc_nb8 = s->tc_fp8 ? (kTcF8Terms * max_batch + 15) / 16 * 16 : 0;
     s->opts.explicit_gather = 1;  // the up/gate tiles take their rows in expert order
   }
   // MoE claims: static for the GEMV builds (their tiles are short and equal),

@@ -146,6 +146,12 @@ WORKLOADS = {
                              desc="small shape with FP8 experts: 8 layers, B=2, seq_lens U[1,1024]"),
     "full_fp8_bs1_8k": Workload("full_fp8_bs1_8k", "full_fp8", 1, ("fixed", 8192), 3,
                                 desc="full shape with FP8 experts, B=1, context 8192"),
+    # FP8 experts above batch 2: the tensor-core build's FP8 expert tiles
+    "small_fp8_b16": Workload("small_fp8_b16", "small_fp8", 16, ("uniform", 1, 1024), 18,
+                              desc="small shape with FP8 experts: 8 layers, B=16, seq_lens U[1,1024]"),
+    "batch32_fp8_ragged": Workload("batch32_fp8_ragged", "full_fp8", 32, ("uniform", 512, 32768), 4, zipf=1.1,
+                                   desc="full shape with FP8 experts, B=32, seq_lens U[512,32768], "
+                                        "Zipf(1.1) router bias"),
     "small_fp4": Workload("small_fp4", "small_fp4", 1, ("fixed", 1024), 14,
                           desc="small shape with FP4 experts: 8 layers, B=1, context 1024"),
     "small_fp4_b2": Workload("small_fp4_b2", "small_fp4", 2, ("uniform", 1, 1024), 15,

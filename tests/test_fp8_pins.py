@@ -76,7 +76,7 @@ def test_oracle_fp8_expert_rows():
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("workload", ["small_fp8", "small_fp8_b2"])
+@pytest.mark.parametrize("workload", ["small_fp8", "small_fp8_b2", "small_fp8_b16"])
 def test_fp8_schedules(workload):
     w = synth.WORKLOADS[workload]
     inp = synth.make_inputs(w)
@@ -86,8 +86,16 @@ def test_fp8_schedules(workload):
     s.simulate(inp.seq_lens, seed=4)
 
 
-def test_fp8_needs_small_batch():
+def test_fp8_batch_limit():
+    """Above two rows FP8 experts take the tensor-core build (its operand rows
+    are E5M2 terms: xg8 / u8 instead of the BF16 xgb / ub), up to 32 rows: four
+    term rows per routed row fill the MMA's 128 columns."""
     m = fake_model(synth.MODELS["small_fp8"])
+    s = mk.Sched(m, 3, 1024, mk.default_sched_opts(num_sms=NUM_SMS))
+    assert s.workspace_offset("xg8") >= 0 and s.workspace_offset("xgb") == -1
+    s = mk.Sched(m, 32, 1024, mk.default_sched_opts(num_sms=NUM_SMS))
+    assert s.workspace_offset("u8") >= 0
+    assert mk.Sched(m, 2, 1024, mk.default_sched_opts(num_sms=NUM_SMS)).workspace_offset("xg8") == -1
     with pytest.raises(mk.MkError) as e:
-        mk.Sched(m, 3, 1024, mk.default_sched_opts(num_sms=NUM_SMS))
+        mk.Sched(m, 33, 1024, mk.default_sched_opts(num_sms=NUM_SMS))
     assert e.value.code == mk.MK_ERR_UNSUPPORTED
