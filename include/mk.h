@@ -57,8 +57,11 @@ typedef struct {
                           fp32 scale (w_*_scale): weight = e4m3 value * row scale.
                           Schedules for it need max_batch <= 32; above 2 the expert
                           tiles run on FP8 tensor-core MMAs (E4M3 weights against the
-                          activations as four E5M2 terms each), which needs hidden and
-                          inter multiples of 128 and activations below 57344 in magnitude */
+                          activations as four E4M3 terms each: the gathered rows scaled
+                          by a power of two per row, the SwiGLU activations as they
+                          are), which needs hidden and inter multiples of 128; a SwiGLU
+                          activation beyond 448 in magnitude fails the step
+                          (MK_ERR_DEVICE from mk_check_step) */
   int32_t expert_fp4;  /* 1 (not with expert_fp8): w_gate, w_up, w_down hold FP4 E2M1 codes,
                           two per byte (element 2j in the low nibble of byte j), the same
                           [L][E][rows][cols] layout at half a byte per weight; each run of 16

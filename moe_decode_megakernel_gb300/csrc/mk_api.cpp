@@ -156,7 +156,7 @@ int encode_weight_maps(mk_model* m) {
 
 // The activation operands of the tcgen05 items in the workspace: boxes of
 // tc_nb rows (every activation row as a hi row and a lo row); with FP8
-// experts the expert tiles' operands are E5M2 term rows in boxes of tc_nb8.
+// experts the expert tiles' operands are E4M3 term rows in boxes of tc_nb8.
 int encode_act_maps(mk_sched* s, uint8_t* ws) {
   if (s->tm_ws == ws) return MK_OK;
   const ShapeDims& D = s->dims;
@@ -483,6 +483,7 @@ int mk_decode_step(mk_model* m, mk_sched* s, const int32_t* last_tokens, const i
       p.tm_xg8 = s->tm_act[2]; p.tm_u8 = s->tm_act[3];
       p.xg8 = at("xg8");
       p.u8 = at("u8");
+      p.xg8s = reinterpret_cast<float*>(at("xg8s"));
       p.tc_nb8 = s->tc_nb8;
     } else {
       p.tm_xgb = s->tm_act[2]; p.tm_ub = s->tm_act[3];
@@ -523,7 +524,8 @@ int check_record(const mk_sched* s, const uint32_t* rec, const void* workspace, 
   if (rec[0] == 5)
     return fail(MK_ERR_DEVICE, "descriptor or work ring out of step (a stale entry was read)" + where);
   if (rec[0] == 6)
-    return fail(MK_ERR_DEVICE, "an FP8 or FP4 expert tile's activation is beyond the f16 range (|x| > 65504)" + where);
+    return fail(MK_ERR_DEVICE, "an FP8 or FP4 expert tile's activation is beyond the range of its operand format (|x| > " +
+                                   std::to_string(rec[5]) + ")" + where);
   return fail(MK_ERR_DEVICE, "index out of range" + where);
 }
 }  // namespace mk

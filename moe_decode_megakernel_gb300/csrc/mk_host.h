@@ -70,7 +70,7 @@ struct mk_sched {
   bool tc = false;
   int tc_nb = 0;  // rows of an activation operand box (2 max_batch, rounded up to 16)
   // FP8 experts (kModeTcFp8): the expert tiles on FP8 MMAs, their activation
-  // operands as E5M2 term rows (boxes of kTcF8Terms max_batch, rounded up to 16)
+  // operands as E4M3 term rows (boxes of kTcF8Terms max_batch, rounded up to 16)
   bool tc_fp8 = false;
   int tc_nb8 = 0;
   // tensor maps of the activation operands, for the workspace they were made for

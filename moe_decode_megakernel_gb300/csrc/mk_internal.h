@@ -239,10 +239,12 @@ static_assert(kTcMaxN >= 2 * kMaxBatch, "hi/lo rows of the largest batch fit a s
 
 // FP8 expert tiles of kModeTcFp8: a k-block is 128 E4M3 weights (128 bytes,
 // the same 16 KB box of kTcRows rows).  The activation operand holds every
-// routed row as kTcF8Terms E5M2 rows whose values, scaled by 8^-j for row j,
-// sum to the activation within 2^-12 of it (E5M2 keeps 3 significant bits:
-// each term leaves at most 1/8 of the rest), so the MMA's N is kTcF8Terms
-// per routed row, at most kTcMaxN: batches of at most kTcF8MaxBatch rows.
+// routed row as kTcF8Terms E4M3 rows whose values, scaled by 16^-j for row j,
+// sum to the activation within 2^-16 of it (E4M3 keeps 4 significant bits:
+// each term leaves at most 1/16 of the rest); the gathered rows are first
+// scaled by a power of two into range, the SwiGLU activations must stay
+// within +-448.  The MMA's N is kTcF8Terms per routed row, at most kTcMaxN:
+// batches of at most kTcF8MaxBatch rows.
 constexpr int kTcK8 = 128;
 constexpr int kTcF8Terms = 4;
 constexpr int kTcF8MaxBatch = kTcMaxN / kTcF8Terms;
@@ -358,12 +360,13 @@ struct Params {
   uint16_t* xgb;        // [MB K][2][H]    the routed rows in expert order (written by MOE_GATHER)
   uint16_t* ub;         // [MB K][2][I]    the SwiGLU activations (written by the up/gate tiles)
   int tc_nb;            // rows of an activation box: 2 MB rounded up to 16 (the MMA's N)
-  // kModeTcFp8: the expert tiles' activation operands as E5M2 term rows
+  // kModeTcFp8: the expert tiles' activation operands as E4M3 term rows
   // (row kTcF8Terms r + j holds term j of routed row r), boxes of kTcK8
   // columns by tc_nb8 rows; the weight maps tm_wg, tm_wu, tm_wd hold E4M3 bytes
   CUtensorMap tm_xg8, tm_u8;
   uint8_t* xg8;         // [MB K][kTcF8Terms][H] the routed rows in expert order (MOE_GATHER)
   uint8_t* u8;          // [MB K][kTcF8Terms][I] the SwiGLU activations (the up/gate tiles)
+  float* xg8s;          // [MB K] the inverse of each gathered row's power-of-two scale
   int tc_nb8;           // kTcF8Terms MB rounded up to 16 (the expert tiles' N)
 
   int split_len;        // tokens per KV slice

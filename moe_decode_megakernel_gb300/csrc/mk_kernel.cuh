@@ -245,10 +245,10 @@ __device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t tc_idesc_bf16(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
-// Instruction descriptor of kind::f8f6f4: fp32 D, E4M3 A (format 0), E5M2 B
-// (format 1), both K-major, M x N.
-__host__ __device__ constexpr uint32_t tc_idesc_e4m3_e5m2(int m, int n) {
-  return (1u << 4) | (0u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+// Instruction descriptor of kind::f8f6f4: fp32 D, E4M3 A and B (format 0),
+// both K-major, M x N.
+__host__ __device__ constexpr uint32_t tc_idesc_e4m3(int m, int n) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -352,34 +352,47 @@ __device__ __forceinline__ void store_hilo4(uint16_t* hi, uint16_t* lo, float4 v
   *reinterpret_cast<uint2*>(hi) = make_uint2(h0, h1);
   *reinterpret_cast<uint2*>(lo) = make_uint2(l0, l1);
 }
-// E5M2 codes (1 sign, 5 exponent, 2 mantissa bits: the upper byte of an IEEE
-// half).  f_e5m2x2 rounds two floats to nearest even, saturating at +-57344,
-// a's code in the low byte; e5m2_f is exact.
-__device__ __forceinline__ uint32_t f_e5m2x2(float a, float b) {
+// E4M3 codes (1 sign, 4 exponent, 3 mantissa bits; largest finite 448).
+// f_e4m3x2 rounds two floats to nearest even, saturating at +-448, a's code
+// in the low byte; e4m3_f is exact.
+__device__ __forceinline__ uint32_t f_e4m3x2(float a, float b) {
   uint16_t r;
-  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
   return r;
 }
-__device__ __forceinline__ float e5m2_f(uint32_t code) {
+__device__ __forceinline__ float e4m3_f(uint32_t code) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)(code & 0xffu)));
   float f;
-  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"((unsigned short)((code & 0xffu) << 8)));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"((unsigned short)(h2 & 0xffffu)));
   return f;
 }
-// The FP8 tensor-core operand of four consecutive activations: kTcF8Terms
-// E5M2 words, term j at row0 + j * term_stride.  Term j codes the remainder
-// the earlier terms leave, times 8^j: x = sum_j code_j 8^-j to within 2^-12 |x|
-// (exact differences: each code is within a factor of two of its input).
-__device__ __forceinline__ void store_e5m2_terms4(uint8_t* row0, int64_t term_stride, float4 v) {
+// The FP8 tensor-core operand of four consecutive activations (|v| <= 448):
+// kTcF8Terms E4M3 words, term j at row0 + j * term_stride.  Term j codes the
+// remainder the earlier terms leave, times 16^j: v = sum_j code_j 16^-j to
+// within 2^-16 |v| where |v| >= 2^-6, 2^-22 below (E4M3 keeps 4 significant
+// bits and leaves at most 1/16 of its input; the differences are exact, since
+// a code is within a factor of two of its input).
+__device__ __forceinline__ void store_e4m3_terms4(uint8_t* row0, int64_t term_stride, float4 v) {
   float r0 = v.x, r1 = v.y, r2 = v.z, r3 = v.w;
 #pragma unroll
   for (int j = 0; j < kTcF8Terms; ++j) {
-    const uint32_t word = f_e5m2x2(r0, r1) | (f_e5m2x2(r2, r3) << 16);
+    const uint32_t word = f_e4m3x2(r0, r1) | (f_e4m3x2(r2, r3) << 16);
     *reinterpret_cast<uint32_t*>(row0 + j * term_stride) = word;
-    r0 = (r0 - e5m2_f(word)) * 8.f;
-    r1 = (r1 - e5m2_f(word >> 8)) * 8.f;
-    r2 = (r2 - e5m2_f(word >> 16)) * 8.f;
-    r3 = (r3 - e5m2_f(word >> 24)) * 8.f;
+    r0 = (r0 - e4m3_f(word)) * 16.f;
+    r1 = (r1 - e4m3_f(word >> 8)) * 16.f;
+    r2 = (r2 - e4m3_f(word >> 16)) * 16.f;
+    r3 = (r3 - e4m3_f(word >> 24)) * 16.f;
   }
+}
+// 2^k with max_abs 2^k in [64, 128) (1 for 0 or a non-finite max): the
+// power-of-two scale that brings a row into the E4M3 terms' range exactly.
+__device__ __forceinline__ int e4m3_row_exponent(float max_abs) {
+  const uint32_t bits = __float_as_uint(max_abs);
+  const int e = (int)((bits >> 23) & 0xffu) - 127;  // max_abs in [2^e, 2^(e+1)) for normal values
+  if (max_abs == 0.f || e == 128) return 0;
+  const int k = 6 - (e < -126 ? -126 : e);
+  return k > 126 ? 126 : k;
 }
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -1102,7 +1115,7 @@ struct Producer {
       if constexpr (mode_tc(M)) {
         // one item of nkb k-blocks: the expert's gate/up or down rows against
         // its routed rows (their hi/lo rows start at row 2 row0; FP8 experts:
-        // their E5M2 term rows at row kTcF8Terms row0)
+        // their E4M3 term rows at row kTcF8Terms row0)
         constexpr bool f8 = M == kModeTcFp8;
         constexpr int kk = f8 ? kTcK8 : kTcK, nt = f8 ? kTcF8Terms : 2;
         const int nb = f8 ? p.tc_nb8 : p.tc_nb;
@@ -2879,13 +2892,27 @@ struct Consumer {
 #pragma unroll
         for (int q = 0; q < PL; ++q)
           if (C % 32 == 0 || lane + 32 * q < C) xv[q] = __ldcg(x4 + lane + 32 * q);
+        [[maybe_unused]] float rs = 1.f;
+        if constexpr (M == kModeTcFp8) {
+          // the row's power-of-two scale into the E4M3 terms' range (its
+          // inverse goes to the up/gate epilogue)
+          float mx = 0.f;
+#pragma unroll
+          for (int q = 0; q < PL; ++q)
+            if (C % 32 == 0 || lane + 32 * q < C)
+              mx = fmaxf(mx, fmaxf(fmaxf(fabsf(xv[q].x), fabsf(xv[q].y)), fmaxf(fabsf(xv[q].z), fabsf(xv[q].w))));
+          const int ke = e4m3_row_exponent(warp_max(mx));
+          rs = ldexpf(1.f, ke);
+          if (lane == 0) p.xg8s[r] = ldexpf(1.f, -ke);
+        }
 #pragma unroll
         for (int q = 0; q < PL; ++q) {
           const int cc = lane + 32 * q;
           if (C % 32 != 0 && cc >= C) continue;
-          if constexpr (M == kModeTcFp8)  // the FP8 expert tiles read the E5M2 term rows
-            store_e5m2_terms4(p.xg8 + (int64_t)kTcF8Terms * r * S::H + 4 * cc, S::H, xv[q]);
-          else if constexpr (M == kModeTc)  // the tcgen05 items read only the BF16 operand rows
+          if constexpr (M == kModeTcFp8) {  // the FP8 expert tiles read the E4M3 term rows
+            const float4 v = make_float4(xv[q].x * rs, xv[q].y * rs, xv[q].z * rs, xv[q].w * rs);
+            store_e4m3_terms4(p.xg8 + (int64_t)kTcF8Terms * r * S::H + 4 * cc, S::H, v);
+          } else if constexpr (M == kModeTc)  // the tcgen05 items read only the BF16 operand rows
             store_hilo4(p.xgb + (int64_t)(2 * r) * S::H + 4 * cc, p.xgb + (int64_t)(2 * r + 1) * S::H + 4 * cc, xv[q]);
           else
             reinterpret_cast<float4*>(p.xg + (int64_t)r * S::H)[cc] = xv[q];
@@ -2930,7 +2957,7 @@ struct Consumer {
     const uint32_t a_bytes = op == OP_ROUTER_GEMM                      ? kTcRouterRows * kTcK * 2
                              : (op == W_UP_TILE || op == W_DOWN_TILE) ? kTcMoeRows * kTcK * 2
                                                                       : kTcDenseRows * kTcK * 2;
-    // FP8 expert tiles: E4M3 weights against the E5M2 term rows
+    // FP8 expert tiles: E4M3 weights against the E4M3 term rows
     const bool f8 = M == kModeTcFp8 && (op == W_UP_TILE || op == W_DOWN_TILE);
     const int nb = f8 ? p.tc_nb8 : p.tc_nb;
     const int kps = tc_kblocks_per_stage(a_bytes, nb);
@@ -2940,7 +2967,7 @@ struct Consumer {
       // one MMA's K in descriptor units: 32 bytes (16 BF16 or 32 FP8 values),
       // four MMAs per 128-byte k-block
       constexpr uint32_t kDescK = 32 / 16;
-      const uint32_t idesc = f8 ? tc_idesc_e4m3_e5m2(kTcRows, nb) : tc_idesc_bf16(kTcRows, nb);
+      const uint32_t idesc = f8 ? tc_idesc_e4m3(kTcRows, nb) : tc_idesc_bf16(kTcRows, nb);
       for (int st = 0; st < nst; ++st) {
         const uint32_t gs = c.st + (uint32_t)st;
         const int slot = (int)(gs % kStages);
@@ -3090,10 +3117,12 @@ struct Consumer {
 
   // The accumulator of an FP8 expert tile (kModeTcFp8): columns
   // kTcF8Terms t + j hold the products with term j of routed row t, so row t's
-  // value is their sum scaled by 8^-j, times the weight row's scale (E4M3 code
-  // times the row scale is the weight).  Chunks of 4 routed rows (16 columns),
-  // the two warps of a lane quarter taking alternate chunks.  The up/gate
-  // epilogue writes the SwiGLU activations as the down tiles' E5M2 term rows.
+  // value is their sum scaled by 16^-j, times the weight row's scale (E4M3 code
+  // times the row scale is the weight) and, for an up/gate tile, the inverse
+  // of the gathered row's scale.  Chunks of 4 routed rows (16 columns), the
+  // two warps of a lane quarter taking alternate chunks.  The up/gate epilogue
+  // writes the SwiGLU activations as the down tiles' E4M3 term rows (unscaled:
+  // a value beyond 448 in magnitude fails the step with ERR_RANGE).
   __device__ __forceinline__ void tc_epilogue_f8(const int32_t* w, int op, int l, int q, int half, int r, int ntok) {
     constexpr MoePlan mp = S::mptc8;
     static_assert(kTcF8Terms == 4, "four term columns per routed row: 4 rows per 16-column load");
@@ -3104,17 +3133,24 @@ struct Consumer {
     const int col = w[F_A0 + 1] * mp.up_tile + 16 * q + (lane & 15);
     const int n = w[F_A0 + 1] * mp.dn_tile + r;
     const float scale = up_tile ? __ldg((lane < 16 ? p.sg : p.su) + le * S::I + col) : __ldg(p.sd + le * S::H + n);
+    bool bad = false;
     for (int j = half; 4 * j < ntok; j += 2) {
       float c16[16];
       tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(16 * j), c16);
       float v[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t)
-        v[t] = scale * (c16[4 * t] + 0.125f * (c16[4 * t + 1] + 0.125f * (c16[4 * t + 2] + 0.125f * c16[4 * t + 3])));
+        v[t] = scale * (c16[4 * t] + 0.0625f * (c16[4 * t + 1] + 0.0625f * (c16[4 * t + 2] + 0.0625f * c16[4 * t + 3])));
       if (up_tile) {
+        float xs[4];  // the gathered rows' inverse scales
+#pragma unroll
+        for (int t = 0; t < 4; ++t) xs[t] = 4 * j + t < ntok ? __ldcg(p.xg8s + w[F_A0 + 2] + 4 * j + t) : 0.f;
         float upv[4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) upv[t] = __shfl_down_sync(FULL, v[t], 16);
+        for (int t = 0; t < 4; ++t) {
+          v[t] *= xs[t];
+          upv[t] = __shfl_down_sync(FULL, v[t], 16);
+        }
         if (lane < 16) {
 #pragma unroll
           for (int t = 0; t < 4; ++t)
@@ -3122,12 +3158,13 @@ struct Consumer {
               const int row = w[F_A0 + 2] + 4 * j + t;  // expert-ordered routed row
               float act = v[t] / (1.f + expf(-v[t])) * upv[t];
               p.u[(int64_t)row * S::I + col] = act;
+              bad |= !(fabsf(act) <= 448.f);
               uint8_t* dst = p.u8 + (int64_t)kTcF8Terms * row * S::I + col;
 #pragma unroll
               for (int k = 0; k < kTcF8Terms; ++k) {
-                const uint32_t code = f_e5m2x2(act, 0.f) & 0xffu;
+                const uint32_t code = f_e4m3x2(act, 0.f) & 0xffu;
                 dst[(int64_t)k * S::I] = (uint8_t)code;
-                act = (act - e5m2_f(code)) * 8.f;
+                act = (act - e4m3_f(code)) * 16.f;
               }
             }
         }
@@ -3146,6 +3183,7 @@ struct Consumer {
           if (4 * j + t < ntok) p.y[(int64_t)slot[t] * S::H + n] = wt[t] * v[t];
       }
     }
+    if (bad) record_error(p, ERR_RANGE, c.sm, where_of(w), col, 0u, 448u);
   }
 
   // One QKV rotation pair (rows dd, dd + 1 of head `head`) of activation row

@@ -823,8 +823,9 @@ static void layout_workspace(mk_sched* s) {
   if (s->tc) {  // the BF16 hi/lo operand rows of the tcgen05 items (at least one box of rows each)
     w.add("xb", 2ull * s->tc_nb * D.H);
     w.add("attnb", 2ull * s->tc_nb * D.NQ * D.D);
-    if (s->tc_fp8) {  // FP8 expert tiles: E5M2 term rows, one byte each
+    if (s->tc_fp8) {  // FP8 expert tiles: E4M3 term rows, one byte each, and the gathered rows' scales
       w.add("xg8", 1ull * std::max(kTcF8Terms * MB * D.K, s->tc_nb8) * D.H);
+      w.add("xg8s", sizeof(float) * MB * D.K);
       w.add("u8", 1ull * std::max(kTcF8Terms * MB * D.K, s->tc_nb8) * D.I);
     } else {
       w.add("xgb", 2ull * std::max(2 * MB * D.K, s->tc_nb) * D.H);
@@ -1160,7 +1161,7 @@ int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const 
   if (m->cfg.expert_fp4 && max_batch > kTB) return fail(MK_ERR_UNSUPPORTED, "FP4 experts are compiled for max_batch <= 2");
   if (m->cfg.expert_fp8 && max_batch > kTcF8MaxBatch)
     return fail(MK_ERR_UNSUPPORTED, "FP8 experts are compiled for max_batch <= " + std::to_string(kTcF8MaxBatch) +
-                                        " (the MMA's N holds four E5M2 term rows per routed row)");
+                                        " (the MMA's N holds four E4M3 term rows per routed row)");
   if (m->cfg.expert_fp8 && max_batch > kTB && (m->dims.H % kTcK8 || m->dims.I % kTcK8))
     return fail(MK_ERR_UNSUPPORTED, "FP8 experts above batch 2 need hidden and inter multiples of 128");
   mk_sched* s = new mk_sched();
@@ -1173,7 +1174,7 @@ int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const 
   s->max_ctx = max_ctx;
   // batches beyond the GEMV's kTB rows: the weight tiles are real contractions,
   // run on the tcgen05 tensor cores (BF16 or FP8 experts of an MoE model)
-  // (FP8 experts: the expert tiles on FP8 MMAs against E5M2 term rows)
+  // (FP8 experts: the expert tiles on FP8 MMAs against E4M3 term rows)
   s->tc = max_batch > kTB && !m->cfg.expert_fp4 && !(m->dims.E == 1 && m->dims.K == 1);
   if (s->tc) {
     s->tc_fp8 = m->cfg.expert_fp8 != 0;

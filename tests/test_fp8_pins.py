@@ -88,7 +88,7 @@ def test_fp8_schedules(workload):
 
 def test_fp8_batch_limit():
     """Above two rows FP8 experts take the tensor-core build (its operand rows
-    are E5M2 terms: xg8 / u8 instead of the BF16 xgb / ub), up to 32 rows: four
+    are E4M3 terms: xg8 / u8 instead of the BF16 xgb / ub), up to 32 rows: four
     term rows per routed row fill the MMA's 128 columns."""
     m = fake_model(synth.MODELS["small_fp8"])
     s = mk.Sched(m, 3, 1024, mk.default_sched_opts(num_sms=NUM_SMS))

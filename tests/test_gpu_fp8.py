@@ -2,7 +2,7 @@
 the C ABI against the CPU oracle, which dequantizes the same codes; the
 generator's device codes against its host codes.  Above two rows the expert
 tiles run on the tensor cores (kind::f8f6f4 MMAs: the E4M3 codes against the
-activations as four E5M2 terms, the row scale applied to the accumulator)."""
+activations as four E4M3 terms, the row scale applied to the accumulator)."""
 import numpy as np
 import pytest
 import torch
@@ -103,3 +103,33 @@ def test_fp8_full_shape_batch32():
     assert rep.greedy_agree == rep.greedy_total
     assert parity.compare_queue(inp, g) == inp.workload.shape.n_layers
     parity.release()
+
+
+def test_fp8_tensor_core_range_error():
+    """The SwiGLU activations enter the down tiles as E4M3 terms, finite up to
+    448: with layer 0's up rows scaled by 10^4 the step fails with
+    MK_ERR_DEVICE naming the limit, and the same model at batch 3 with the
+    original scales runs clean."""
+    sh = synth.MODELS["small_fp8"]
+    seed = 63
+    sl = np.array([40, 7, 300], np.int32)
+    bt, npages = synth.block_tables_for(sl, sh.page_size, seed, slack_pages=2)
+    tok = np.random.default_rng(seed).integers(0, sh.vocab, size=3).astype(np.int32)
+    w = synth.device.device_weights(sh, seed)
+    dev = "cuda"
+    for boost, ok in ((1.0, True), (1e4, False)):
+        ws = dict(w)
+        ws["w_up_scale"] = w["w_up_scale"].clone()
+        ws["w_up_scale"][0] *= boost
+        model = mk.Model(mk.config_from(sh), mk.weights_from(ws), keepalive=ws)
+        sess = mk.Session(model, mk.Sched(model, 3, 512))
+        kp, vp = synth.device.device_pools(sh, seed, npages)
+        logits = torch.empty(3, sh.vocab, device=dev)
+        sess.step(torch.as_tensor(tok, device=dev), torch.as_tensor(sl, device=dev),
+                  torch.as_tensor(bt, device=dev), kp, vp, logits)
+        if ok:
+            sess.check()
+        else:
+            with pytest.raises(mk.MkError) as e:
+                sess.check()
+            assert e.value.code == mk.MK_ERR_DEVICE and "448" in str(e.value), str(e.value)

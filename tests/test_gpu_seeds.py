@@ -7,7 +7,8 @@ routing a valid top-k); over all (config, seed, row) samples the GPU's greedy
 token must equal the oracle's in at least 99% of them.  tiny and small run
 200 seeds each; the full-shape workloads 4 seeds each, every row at batch
 <= 4 and sampled rows (the shortest, the longest and random ones) at batch 32
-and 64, where the oracle's cost per row (seconds) rules out every row."""
+and 64 (and at batch 32 with FP8 experts), where the oracle's cost per row
+(seconds) rules out every row."""
 from dataclasses import replace
 
 import numpy as np
@@ -54,7 +55,7 @@ def test_two_hundred_seeds(workload):
 
 @pytest.mark.parametrize("workload,n_rows", [("full_bs1_8k", None), ("full_bs2_8k", None),
                                              ("full_bs4_8k", None), ("batch32_ragged", 6),
-                                             ("batch64_ragged", 4)])
+                                             ("batch64_ragged", 4), ("batch32_fp8_ragged", 6)])
 def test_full_shape_four_seeds(workload, n_rows):
     exact = total = 0
     worst = 0.0
@@ -69,6 +70,8 @@ def test_full_shape_four_seeds(workload, n_rows):
             rows |= set(rng.choice(B, size=n_rows, replace=False).tolist())
             rows = sorted(rows)[:n_rows + 2]
         rep = parity.compare(inp, parity.run_gpu(inp), rows=rows)
+        print(f"{workload} seed {7000 + k}: logit rel err {rep.max_rel_err:.2e} "
+              f"router err {rep.router_err.max():.2e}")
         _check_sample(rep)
         exact += rep.greedy_exact
         total += rep.greedy_total
