@@ -353,6 +353,7 @@ def run_mine(args):
         mktrace.chrome_trace(t, args.trace)
         if rank == 0:
             print(mktrace.summary(t), file=sys.stderr)
+            print(mktrace.phases(t), file=sys.stderr)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

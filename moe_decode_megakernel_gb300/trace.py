@@ -67,6 +67,40 @@ def summary(t: dict) -> str:
     return "\n".join(lines)
 
 
+def phases(t: dict) -> str:
+    """The per-layer critical path: for each op of a layer, when its first
+    and last items start and when its last item ends, in microseconds from
+    the layer's first start, as medians over the middle layers (the first
+    two and the last are left out: start-up and the LM head), and the median
+    layer period (first start to the next layer's first start)."""
+    a = t["rec"]
+    if a.size == 0:
+        return "empty trace"
+    layers = sorted(set(a[:, 5].tolist()))
+    mid = layers[2:-2] if len(layers) > 5 else layers
+    starts = {l: a[a[:, 5] == l, 2].min() for l in layers}
+    rows: dict = {}
+    periods = []
+    for l in mid:
+        m = a[:, 5] == l
+        s0 = starts[l]
+        if l + 1 in starts:
+            periods.append((starts[l + 1] - s0) / 1e3)
+        for op in set(a[m, 4].tolist()):
+            mo = m & (a[:, 4] == op)
+            rows.setdefault(op, []).append((mo.sum(), (a[mo, 2].min() - s0) / 1e3, (a[mo, 2].max() - s0) / 1e3,
+                                            (a[mo, 3].max() - s0) / 1e3, np.median(a[mo, 3] - a[mo, 2]) / 1e3))
+    lines = [f"layer period (median over layers {mid[0]}..{mid[-1]}): {np.median(periods):.1f} us" if periods
+             else "one layer"]
+    lines.append(f"{'op':>22} {'items':>6} {'first go':>9} {'last go':>8} {'last end':>9} {'busy p50':>9}")
+    order = sorted(rows, key=lambda op: np.median([r[1] for r in rows[op]]))
+    for op in order:
+        r = np.array(rows[op], dtype=np.float64)
+        med = np.median(r, axis=0)
+        lines.append(f"{op_name(op):>22} {med[0]:6.0f} {med[1]:9.1f} {med[2]:8.1f} {med[3]:9.1f} {med[4]:9.2f}")
+    return "\n".join(lines)
+
+
 def chrome_trace(t: dict, path: str) -> None:
     a = t["rec"]
     t0 = a[:, 1].min() if a.size else 0

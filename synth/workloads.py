@@ -89,6 +89,10 @@ MODELS = {
     "full_fp8": ModelShape("full_fp8", n_layers=48, hidden=2048, n_q=32, n_kv=4, head_dim=128,
                            n_experts=128, top_k=8, inter=768, vocab=65536, page_size=64,
                            window=4096, full_period=4, expert_fp8=True),
+    # the same two full-shape layers with FP8 experts (profiling case of the FP8 tensor-core build)
+    "full_fp8_l2": ModelShape("full_fp8_l2", n_layers=2, hidden=2048, n_q=32, n_kv=4, head_dim=128,
+                              n_experts=128, top_k=8, inter=768, vocab=65536, page_size=64,
+                              window=4096, full_period=2, expert_fp8=True),
     # FP4 expert weights (E2M1 codes, E4M3 block scales, fp32 row scales)
     "small_fp4": ModelShape("small_fp4", n_layers=8, hidden=1024, n_q=16, n_kv=2, head_dim=64,
                             n_experts=32, top_k=4, inter=512, vocab=32768, page_size=64, window=0,
@@ -168,6 +172,9 @@ WORKLOADS = {
     "prof_l2_b32": Workload("prof_l2_b32", "full_l2", 32, ("uniform", 512, 8192), 8, zipf=1.1,
                             desc="full-shape layers, 2 of them, B=32 ragged U[512,8192], Zipf(1.1) routing "
                                  "(profiling case of the tensor-core build)"),
+    "prof_l2_fp8_b32": Workload("prof_l2_fp8_b32", "full_fp8_l2", 32, ("uniform", 512, 8192), 8, zipf=1.1,
+                                desc="full-shape layers with FP8 experts, 2 of them, B=32 ragged U[512,8192], "
+                                     "Zipf(1.1) routing (profiling case of the FP8 tensor-core build)"),
     "prof_l2_8k": Workload("prof_l2_8k", "full_l2", 1, ("fixed", 8192), 7,
                            desc="full-shape layers, 2 of them, B=1, context 8192 (profiling case)"),
 }
