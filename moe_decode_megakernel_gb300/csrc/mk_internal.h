@@ -227,8 +227,11 @@ constexpr int kTcRouterRows = 16;  // rows of a router task (its weight box; the
 constexpr int kTcDenseRows = 64;   // rows of a QKV, O-proj or LM-head tile (the MMA's other rows unused)
 constexpr int kTcMoeRows = 128;    // weight rows of an expert tile: 64 gate + 64 up rows, or 128 down rows
 // k-blocks per stage of a tcgen05 item whose weight box holds a_bytes per
-// k-block: one for full tiles, up to 8 for a router task's small boxes (the
-// activation boxes of those k-blocks must fit the stage's second half).
+// k-block and whose activation box holds tc_nb rows: as many pairs of boxes
+// as fill the stage (the weight boxes first, then the activation boxes; both
+// sizes are multiples of 1024 bytes, so every box starts on a swizzle atom),
+// at most 8: one for full expert tiles, up to 3 for the 64-row dense tiles
+// at small batches, up to 8 for a router task's 16-row boxes.
 MK_HOST_DEVICE constexpr int tc_kblocks_per_stage(uint32_t a_bytes, int tc_nb) {
   int k = a_bytes >= (uint32_t)kTcABytes ? 1 : (int)((uint32_t)kTcABytes / a_bytes);
   const int kb_fit = (kStageBytes - kTcABytes) / (tc_nb * kTcK * 2);
@@ -271,6 +274,31 @@ constexpr MoePlan moe_plan_tc8(ShapeDims s) {
   p.up_stages = s.H / kTcK8;
   p.dn_stages = s.I / kTcK8;
   return p;
+}
+
+// In the tensor-core builds an expert with at most kTB routed rows takes the
+// batch <= kTB GEMV instead (its tiles would fill one 16-row MMA column block
+// with one or two rows): the same tiles, streamed in GEMV stages of whole
+// rows (BF16, or FP8 with their row scales), so that a stage carries 32 KB
+// of weights where a tcgen05 item's carries 16 KB next to its activations.
+constexpr MoePlan moe_plan_tc_gemv(ShapeDims s) {
+  MoePlan p = moe_plan_tc(s);
+  p.up_half = stage_rows(s.H) / 2;
+  p.up_stages = p.up_tile / p.up_half;
+  p.dn_rows = stage_rows(s.I);
+  p.dn_stages = p.dn_tile / p.dn_rows;
+  return p;
+}
+constexpr MoePlan moe_plan_tc8_gemv(ShapeDims s) {
+  MoePlan p = moe_plan_tc8(s);
+  p.up_half = stage_rows8(s.H) / 2;
+  p.up_stages = p.up_tile / p.up_half;
+  p.dn_rows = stage_rows8(s.I);
+  p.dn_stages = p.dn_tile / p.dn_rows;
+  return p;
+}
+constexpr bool gemv_plan_fits(MoePlan p) {
+  return p.up_half > 0 && p.up_tile % p.up_half == 0 && p.dn_rows > 0 && p.dn_tile % p.dn_rows == 0;
 }
 
 // ------------------------------------------------------ kernel parameters

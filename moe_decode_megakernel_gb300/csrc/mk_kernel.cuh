@@ -437,6 +437,12 @@ template <class S, int M>
 __host__ __device__ constexpr MoePlan plan_of() {
   return M == kModeTcFp8 ? S::mptc8 : mode_tc(M) ? S::mptc : mode_fp4(M) ? S::mp4 : mode_fp8(M) ? S::mp8 : S::mp;
 }
+// the stage plan of an expert tile that runs as a GEMV: in the tensor-core
+// builds the same tiles in GEMV stages (experts with at most kTB rows)
+template <class S, int M>
+__host__ __device__ constexpr MoePlan gemv_plan_of() {
+  return M == kModeTcFp8 ? S::mptcg8 : M == kModeTc ? S::mptcg : plan_of<S, M>();
+}
 
 template <class S>
 struct Scratch {
@@ -480,6 +486,9 @@ struct Shape {
   static constexpr MoePlan mp4 = moe_plan4(dims);  // FP4 expert rows
   static constexpr MoePlan mptc = moe_plan_tc(dims);  // tcgen05 GEMM tiles
   static constexpr MoePlan mptc8 = moe_plan_tc8(dims);  // the same over FP8 expert rows
+  static constexpr MoePlan mptcg = moe_plan_tc_gemv(dims);    // those tiles as GEMV stages
+  static constexpr MoePlan mptcg8 = moe_plan_tc8_gemv(dims);
+  static_assert(gemv_plan_fits(mptcg) && gemv_plan_fits(mptcg8), "GEMV stages divide the tcgen05 tiles");
   static constexpr int SR_H = stage_rows(H), SR_O = stage_rows(G * D), SR_I = stage_rows(I);
   static_assert(H % 256 == 0 && (G * D) % 8 == 0 && I % 8 == 0, "row chunks");
   static_assert(D % 32 == 0 && 32 % G == 0 && (G * D) % 4 == 0, "attention lane maps");
@@ -723,9 +732,8 @@ struct Producer {
   // rows are written by other SMs, so their boxes are copied only after the
   // item's input counters are complete (then a proxy fence: the rows were
   // written by ordinary stores, the copy reads through the async proxy).
-  // With a weight box of a_bytes < kTcABytes (a router task's rows), a stage
-  // takes kps = tc_kblocks_per_stage(a_bytes) k-blocks: weight box j at
-  // j * a_bytes, activation box j at kTcABytes + j * (its bytes).
+  // A stage takes kps = tc_kblocks_per_stage(a_bytes, nb) k-blocks: weight
+  // box j at j * a_bytes, activation box j at kps * a_bytes + j * (its bytes).
   // FP8 expert tiles (kModeTcFp8) take k-blocks of kk = kTcK8 one-byte
   // weights and activation boxes of nb = tc_nb8 term rows: 128-byte rows as
   // for BF16, so the stage layout is the same.
@@ -981,7 +989,7 @@ struct Producer {
 
   __device__ __forceinline__ bool moe_drain(const int32_t* d, int mode) {
     const int l = d[F_LAYER];
-    constexpr MoePlan mp = plan_of<S, M>();
+    constexpr MoePlan mp = gemv_plan_of<S, M>();  // (tile counts as plan_of)
     const int U = mp.up_tiles, DN = mp.dn_tiles;
     uint32_t* claim = p.bars + d[F_A0];
     const uint32_t n_claimers = (uint32_t)d[F_A0 + 5];
@@ -1112,7 +1120,7 @@ struct Producer {
           carried = true;
         }
       }
-      if constexpr (mode_tc(M)) {
+      if (mode_tc(M) && nrows > kTB) {
         // one item of nkb k-blocks: the expert's gate/up or down rows against
         // its routed rows (their hi/lo rows start at row 2 row0; FP8 experts:
         // their E4M3 term rows at row kTcF8Terms row0)
@@ -1195,8 +1203,8 @@ struct Producer {
 
   __device__ __forceinline__ bool tile_stages(int l, int e, int t, bool up) {
     if constexpr (mode_fp4(M)) return tile_stages4(l, e, t, up);
-    constexpr bool fp8 = mode_fp8(M);
-    constexpr MoePlan mp = plan_of<S, M>();
+    constexpr bool fp8 = mode_fp8(M) || M == kModeTcFp8;
+    constexpr MoePlan mp = gemv_plan_of<S, M>();
     const int64_t le = (int64_t)l * S::E + e;
     constexpr int eb = fp8 ? 1 : 2;  // bytes per weight
     if (!up && !fp8) {
@@ -1365,9 +1373,9 @@ struct Consumer {
   // Every read of a stage is an explicit shared-memory load (ld.shared,
   // ldmatrix), which the release orders before the arrival.
   __device__ __forceinline__ void stage_release(int slot) {
-    if constexpr (mode_tc(M)) {  // one arrival, after every consumer warp's reads
+    if constexpr (mode_tc(M)) {  // the stage's two arrivals, after every consumer warp's reads
       consumers_sync();
-      if (ct == 0) mbar_arrive(&c.hdr->empty[slot]);
+      if (ct == 0) mbar_arrive_n(&c.hdr->empty[slot], 2);
     } else {
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.hdr->empty[slot]);
@@ -1442,7 +1450,8 @@ struct Consumer {
       case W_UP_TILE: {
         const int row = w[F_A0 + 2] + tok;
         if (w[F_A0 + 12]) return p.x + (int64_t)row * S::H;  // dense: the rows are the batch
-        if (p.explicit_gather) return p.xg + (int64_t)row * S::H;
+        // (the tensor-core builds' gather writes only the tcgen05 operand rows)
+        if (!mode_tc(M) && p.explicit_gather) return p.xg + (int64_t)row * S::H;
         const int pr = __ldcg(p.perm + row);
         int b = pr / S::K;
         if (pr < 0 || b >= p.B) b = 0;  // only after a failed step
@@ -1754,7 +1763,7 @@ struct Consumer {
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_n(&c.hdr->empty[slot], kConsumerWarps / kTeamWarps);
+      if (lane == 0) mbar_arrive_n(&c.hdr->empty[slot], kTeamArrivals);
     }
     c.st += (uint32_t)nst;
   }
@@ -1863,7 +1872,7 @@ struct Consumer {
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_n(&c.hdr->empty[slot], kConsumerWarps / kTeamWarps);
+      if (lane == 0) mbar_arrive_n(&c.hdr->empty[slot], kTeamArrivals);
     }
     c.st += (uint32_t)nst;
   }
@@ -1906,7 +1915,7 @@ struct Consumer {
         break;
       }
       case W_UP_TILE: {  // SiLU(gate) * up ("Tasks": the SiLU-and-multiply epilogue)
-        constexpr MoePlan mp = plan_of<S, M>();
+        constexpr MoePlan mp = gemv_plan_of<S, M>();
         const float act = v0 / (1.f + expf(-v0)) * v1;
         const int row = w[F_A0 + 2] + t;
         p.u[(int64_t)row * S::I + w[F_A0 + 1] * mp.up_tile + s * mp.up_half + r0] = act;
@@ -1931,7 +1940,7 @@ struct Consumer {
         break;
       }
       case W_DOWN_TILE: {  // weighted, into the (row b, slot j) of the output
-        constexpr MoePlan mp = plan_of<S, M>();
+        constexpr MoePlan mp = gemv_plan_of<S, M>();
         const int n = w[F_A0 + 1] * mp.dn_tile + s * mp.dn_rows + r0;
         *reinterpret_cast<float2*>(p.y + (int64_t)dslot * S::H + n) = make_float2(dwt * v0, dwt * v1);
         break;
@@ -1955,6 +1964,9 @@ struct Consumer {
     else gemv_item_teams_tb<K, kTB>(w, SR, total_rows, ntok);
   }
   static constexpr int kTeams = 4, kTeamWarps = kConsumerWarps / kTeams;
+  // each warp of a team stands for its share of the arrivals a stage expects
+  // (kConsumerWarps; two in the tensor-core builds, one per warp of the team)
+  static constexpr int kTeamArrivals = mode_tc(M) ? 1 : kConsumerWarps / kTeamWarps;
   static_assert(kConsumerWarps % kTeams == 0 && F_A0 + 8 + 2 * kTB <= F_TASK, "teams; down-tile row fields");
   template <int K, int TB>
   __device__ __forceinline__ void gemv_item_teams_tb(const int32_t* w, int SR, int total_rows, int ntok) {
@@ -2051,7 +2063,7 @@ struct Consumer {
       }
       // the team's warps stand for the eight arrivals the stage expects
       __syncwarp();
-      if (lane == 0) mbar_arrive_n(&c.hdr->empty[slot], kConsumerWarps / kTeamWarps);
+      if (lane == 0) mbar_arrive_n(&c.hdr->empty[slot], kTeamArrivals);
     }
     c.st += (uint32_t)nst;
   }
@@ -2986,7 +2998,8 @@ struct Consumer {
           }
         }
         // the stage goes back to the producer once these MMAs have read it (in
-        // this build a stage's empty barrier takes one arrival)
+        // these builds a stage's empty barrier takes two arrivals)
+        tc_commit(&c.hdr->empty[slot]);
         tc_commit(&c.hdr->empty[slot]);
       }
       tc_commit(&c.hdr->acc_full);
@@ -3220,11 +3233,14 @@ struct Consumer {
   __device__ __forceinline__ void execute(const int32_t* w) {
     if constexpr (mode_tc(M)) {
       switch (w[F_OP]) {
+        case W_UP_TILE:
+        case W_DOWN_TILE:
+          if (w[F_A0 + 3] <= kTB) break;  // an expert with one or two rows: the GEMV below
+          tc_item(w);
+          return;
         case OP_QKV_PROJ:
         case OP_LM_HEAD:
         case OP_O_PROJ:
-        case W_UP_TILE:
-        case W_DOWN_TILE:
           tc_item(w);
           return;
         case OP_ROUTER_GEMM:
@@ -3258,28 +3274,30 @@ struct Consumer {
         if constexpr (mode_fp4(M)) {
           if (w[F_A0 + 3] <= 1) gemv_item_fp4<S::H, 1>(w, w[F_A0 + 3]);
           else gemv_item_fp4<S::H, kTB>(w, w[F_A0 + 3]);
-        } else if constexpr (mode_fp8(M)) {
-          constexpr MoePlan m8 = S::mp8;
+        } else if constexpr (mode_fp8(M) || M == kModeTcFp8) {
+          constexpr MoePlan m8 = gemv_plan_of<S, M>();
           if (w[F_A0 + 3] <= 1) gemv_item_fp8<S::H, 1>(w, 2 * m8.up_half, w[F_A0 + 3]);
           else gemv_item_fp8<S::H, kTB>(w, 2 * m8.up_half, w[F_A0 + 3]);
         } else {
+          constexpr MoePlan mg = gemv_plan_of<S, M>();
           if (!any_batch || w[F_A0 + 3] <= kTB)
-            gemv_item_teams<S::H>(w, 2 * S::mp.up_half, 2 * S::mp.up_half * S::mp.up_stages, w[F_A0 + 3]);
+            gemv_item_teams<S::H>(w, 2 * mg.up_half, 2 * mg.up_half * mg.up_stages, w[F_A0 + 3]);
           else if constexpr (any_batch)
-            gemv_item<S::H>(w, 2 * S::mp.up_half, 2 * S::mp.up_half * S::mp.up_stages, w[F_A0 + 3]);
+            gemv_item<S::H>(w, 2 * mg.up_half, 2 * mg.up_half * mg.up_stages, w[F_A0 + 3]);
         }
         break;
       case W_DOWN_TILE:
         if constexpr (mode_fp4(M)) {
           if (w[F_A0 + 3] <= 1) gemv_item_fp4<S::I, 1>(w, w[F_A0 + 3]);
           else gemv_item_fp4<S::I, kTB>(w, w[F_A0 + 3]);
-        } else if constexpr (mode_fp8(M)) {
-          constexpr MoePlan m8 = S::mp8;
+        } else if constexpr (mode_fp8(M) || M == kModeTcFp8) {
+          constexpr MoePlan m8 = gemv_plan_of<S, M>();
           if (w[F_A0 + 3] <= 1) gemv_item_fp8<S::I, 1>(w, m8.dn_rows, w[F_A0 + 3]);
           else gemv_item_fp8<S::I, kTB>(w, m8.dn_rows, w[F_A0 + 3]);
         } else {
-          if (!any_batch || w[F_A0 + 3] <= kTB) gemv_item_teams<S::I>(w, S::mp.dn_rows, S::mp.dn_tile, w[F_A0 + 3]);
-          else if constexpr (any_batch) gemv_item<S::I>(w, S::mp.dn_rows, S::mp.dn_tile, w[F_A0 + 3]);
+          constexpr MoePlan mg = gemv_plan_of<S, M>();
+          if (!any_batch || w[F_A0 + 3] <= kTB) gemv_item_teams<S::I>(w, mg.dn_rows, mg.dn_tile, w[F_A0 + 3]);
+          else if constexpr (any_batch) gemv_item<S::I>(w, mg.dn_rows, mg.dn_tile, w[F_A0 + 3]);
         }
         break;
       case W_ATTN: attn(w); break;
@@ -3495,7 +3513,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_persistent(const __grid_consta
       mbar_init(&hdr->full[i], 1);
       // the tcgen05 build hands a stage back with one arrival (a commit of the
       // MMAs that read it, or one thread after the block's last read)
-      mbar_init(&hdr->empty[i], mode_tc(M) ? 1 : kConsumerWarps);
+      mbar_init(&hdr->empty[i], mode_tc(M) ? 2 : kConsumerWarps);
     }
     for (int i = 0; i < kDescRing; ++i) {
       mbar_init(&hdr->dfull[i], 1);

@@ -106,15 +106,18 @@ def test_fp8_full_shape_batch32():
 
 
 def test_fp8_tensor_core_range_error():
-    """The SwiGLU activations enter the down tiles as E4M3 terms, finite up to
-    448: with layer 0's up rows scaled by 10^4 the step fails with
-    MK_ERR_DEVICE naming the limit, and the same model at batch 3 with the
-    original scales runs clean."""
+    """The SwiGLU activations enter the tensor-core down tiles as E4M3 terms,
+    finite up to 448: with layer 0's up rows scaled by 10^4 a batch of 32
+    (about four rows per expert: tensor-core tiles; experts with one or two
+    rows take the GEMV, whose f16 operands hold 65504) fails with
+    MK_ERR_DEVICE naming the limit, and the same model with the original
+    scales runs clean."""
     sh = synth.MODELS["small_fp8"]
     seed = 63
-    sl = np.array([40, 7, 300], np.int32)
+    rng = np.random.default_rng(seed)
+    sl = rng.integers(1, 512, size=32).astype(np.int32)
     bt, npages = synth.block_tables_for(sl, sh.page_size, seed, slack_pages=2)
-    tok = np.random.default_rng(seed).integers(0, sh.vocab, size=3).astype(np.int32)
+    tok = rng.integers(0, sh.vocab, size=32).astype(np.int32)
     w = synth.device.device_weights(sh, seed)
     dev = "cuda"
     for boost, ok in ((1.0, True), (1e4, False)):
@@ -122,9 +125,9 @@ def test_fp8_tensor_core_range_error():
         ws["w_up_scale"] = w["w_up_scale"].clone()
         ws["w_up_scale"][0] *= boost
         model = mk.Model(mk.config_from(sh), mk.weights_from(ws), keepalive=ws)
-        sess = mk.Session(model, mk.Sched(model, 3, 512))
+        sess = mk.Session(model, mk.Sched(model, 32, 512))
         kp, vp = synth.device.device_pools(sh, seed, npages)
-        logits = torch.empty(3, sh.vocab, device=dev)
+        logits = torch.empty(32, sh.vocab, device=dev)
         sess.step(torch.as_tensor(tok, device=dev), torch.as_tensor(sl, device=dev),
                   torch.as_tensor(bt, device=dev), kp, vp, logits)
         if ok:
