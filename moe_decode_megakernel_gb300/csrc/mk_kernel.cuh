@@ -732,8 +732,9 @@ struct Producer {
   // rows are written by other SMs, so their boxes are copied only after the
   // item's input counters are complete (then a proxy fence: the rows were
   // written by ordinary stores, the copy reads through the async proxy).
-  // A stage takes kps = tc_kblocks_per_stage(a_bytes, nb) k-blocks: weight
-  // box j at j * a_bytes, activation box j at kps * a_bytes + j * (its bytes).
+  // With a weight box of a_bytes < kTcABytes (a router task's rows), a stage
+  // takes kps = tc_kblocks_per_stage(a_bytes) k-blocks: weight box j at
+  // j * a_bytes, activation box j at kTcABytes + j * (its bytes).
   // FP8 expert tiles (kModeTcFp8) take k-blocks of kk = kTcK8 one-byte
   // weights and activation boxes of nb = tc_nb8 term rows: 128-byte rows as
   // for BF16, so the stage layout is the same.
@@ -2003,8 +2004,11 @@ struct Consumer {
       // The slot's previous use (stage s - kStages) may belong to another
       // team (kStages is not a multiple of kTeams): wait until it is released
       // first, so the parity wait below cannot match a phase two fills back.
+      // (With stats, team 0's waits for its stages count as stage waits.)
+      const int64_t t0 = (p.stats && ct == 0) ? gtimer() : 0;
       bool ok = s < kStages || mbar_wait(p, c, &c.hdr->empty[slot], ((gs / kStages) - 1) & 1);
       ok = __all_sync(FULL, ok && mbar_wait(p, c, &c.hdr->full[slot], (gs / kStages) & 1) && !aborted(c));
+      if (p.stats && ct == 0) c.stat[1] += gtimer() - t0;
       const int rows = min(SR, total_rows - s * SR);
       const int npairs = rows / 2;
       // this warp's pairs [p0, p1): the first half of the stage's pairs, or the second

@@ -52,9 +52,10 @@ def summary(t: dict) -> str:
         lines.append(f"{op_name(op):>22} {m.sum():7d} {busy / nsm:11.2f} {wait / nsm:11.2f} "
                      f"{busy / max(1, m.sum()):13.2f}")
     c = st.astype(np.float64)
-    lines.append("per SM mean: consumer wait-on-counters %.1f us, wait-on-stages %.1f us, busy %.1f us, "
-                 "items %.0f" % (c[:, 0].mean() / 1e3, c[:, 1].mean() / 1e3, c[:, 2].mean() / 1e3,
-                                 c[:, 3].mean()))
+    # busy spans an item from its inputs' arrival to its end, stage waits included
+    lines.append("per SM mean: consumer wait-on-counters %.1f us, wait-on-stages %.1f us (within busy), "
+                 "busy %.1f us, items %.0f" % (c[:, 0].mean() / 1e3, c[:, 1].mean() / 1e3, c[:, 2].mean() / 1e3,
+                                               c[:, 3].mean()))
     lines.append("per SM mean: producer wait-on-free-stage %.1f us, wait-on-routing %.1f us, "
                  "wait-on-work-ring %.1f us, claims %.0f" % (c[:, 4].mean() / 1e3, c[:, 5].mean() / 1e3,
                                                              c[:, 6].mean() / 1e3, c[:, 7].mean()))
