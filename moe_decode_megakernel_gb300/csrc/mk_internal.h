@@ -163,10 +163,18 @@ constexpr int stage_rows8(int k) {
   return r >= 8 ? p : r;
 }
 
-// FP4 stages are one 16-row group of the tensor-core GEMV (up/gate: 8 gate
-// and 8 up rows), the rows' E2M1 codes followed by their block scales.
+// FP4 stages are 16-row groups of the tensor-core GEMV (up/gate: one group
+// of 8 gate and 8 up rows), the rows' E2M1 codes followed by their block
+// scales.  A down stage takes kFp4DownGroups groups where they fit (its rows
+// are short: at inter 768 one group is 6.75 KB of a 32 KB stage), one group
+// per consumer team; otherwise one.
 constexpr int kFp4StageRows = 16;
+constexpr int kFp4DownGroups = 4;
 constexpr int fp4_stage_bytes(int k) { return kFp4StageRows * (k / 2 + k / 16); }
+constexpr int fp4_groups_per_stage(int k) {
+  return kFp4DownGroups * fp4_stage_bytes(k) <= kStageBytes ? kFp4DownGroups : 1;
+}
+static_assert(kFp4DownGroups * kFp4StageRows <= kMaxStageRows, "row scales of a down stage fit the slot's area");
 
 constexpr MoePlan moe_plan(ShapeDims s) {
   MoePlan p{};
@@ -200,7 +208,7 @@ constexpr MoePlan moe_plan4(ShapeDims s) {
   p.up_stages = moe_stages(s.I, p.up_half, 16);
   p.up_tile = p.up_half * p.up_stages;
   p.up_tiles = s.I / p.up_tile;
-  p.dn_rows = kFp4StageRows;
+  p.dn_rows = kFp4StageRows * fp4_groups_per_stage(s.I);
   p.dn_stages = moe_stages(s.H, p.dn_rows, 32);
   p.dn_tile = p.dn_rows * p.dn_stages;
   p.dn_tiles = s.H / p.dn_tile;

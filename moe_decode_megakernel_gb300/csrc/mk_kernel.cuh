@@ -1189,9 +1189,9 @@ struct Producer {
         bulk_g2s_hint(dst + 2 * cb + bb, p.bu + r0 * (S::H / 16), bb, fb, stream_policy);
         bulk_g2s(c.hdr->scl[slot], p.sg + r0, sb, fb);
         bulk_g2s(c.hdr->scl[slot] + R / 2, p.su + r0, sb, fb);
-      } else {
-        constexpr uint32_t cb = R * S::I / 2, bb = R * S::I / 16, sb = R * 4;
-        const int64_t r0 = le * S::H + t * mp.dn_tile + s * R;  // row of [L][E][H]
+      } else {  // dn_rows rows: whole 16-row groups
+        constexpr uint32_t cb = mp.dn_rows * S::I / 2, bb = mp.dn_rows * S::I / 16, sb = mp.dn_rows * 4;
+        const int64_t r0 = le * S::H + t * mp.dn_tile + s * mp.dn_rows;  // row of [L][E][H]
         mbar_expect_tx(fb, cb + bb + sb);
         bulk_g2s_hint(dst, wd + r0 * (S::I / 2), cb, fb, stream_policy);
         bulk_g2s_hint(dst + cb, p.bd + r0 * (S::I / 16), bb, fb, stream_policy);
@@ -1769,8 +1769,9 @@ struct Consumer {
     c.st += (uint32_t)nst;
   }
 
-  // FP4 expert tiles (batch <= kTB) on the tensor cores: each 16-row stage
-  // is one group of m16n8k16 f16 MMAs.  A thread's 16-byte load of a row
+  // FP4 expert tiles (batch <= kTB) on the tensor cores: each 16-row group
+  // of a stage (one per up/gate stage, up to four per down stage) is one
+  // group of m16n8k16 f16 MMAs.  A thread's 16-byte load of a row
   // holds 32 codes (two 16-input blocks) and feeds eight MMAs; each code pair
   // is converted exactly to f16 and multiplied (exactly: at most 6
   // significant bits, within the f16 range) by its block's E4M3 scale before
@@ -1782,7 +1783,7 @@ struct Consumer {
     static_assert(K % 128 == 0, "FP4 rows in 128-input chunks");
     static_assert(kTeamWarps == 2 && kTeams * 2 * kTB * 16 <= (int)(sizeof(sm.out) / sizeof(float)),
                   "partial sums of the stages fit the stage-output buffer");
-    constexpr int R = kFp4StageRows, NKC = K / 128, CB = R * K / 2;  // codes, then block scales
+    constexpr int R = kFp4StageRows, NKC = K / 128;  // rows of a group, 128-input chunks of a row
     const int op = w[F_OP];
     const int nst = w[F_NSTAGE];
     const int tb = ntok;
@@ -1805,75 +1806,88 @@ struct Consumer {
     }
     const int team = cw / kTeamWarps, tw = cw % kTeamWarps;
     const bool up = op == W_UP_TILE;
-    const int rlo = up ? g : 2 * g, rhi = up ? R / 2 + g : 2 * g + 1;  // gate/up row g; rows 2g, 2g+1
+    // a down stage holds ng 16-row groups (codes of all its rows, then their
+    // block scales): with kFp4DownGroups of them every team takes one group of
+    // every stage (and each warp stands for one arrival), else the teams take
+    // stages in turn
+    constexpr MoePlan mp4 = S::mp4;
+    static_assert(kFp4DownGroups == kTeams, "one group of a down stage per team");
+    const int rows = up ? R : mp4.dn_rows, ng = rows / R, cbytes = rows * K / 2;
+    const bool spread = ng == kTeams;
+    const int s0 = spread ? 0 : team, ds = spread ? 1 : kTeams, g0 = spread ? team : 0, dg = spread ? kTeams : 1;
+    const int arrivals = spread ? kConsumerWarps / (kTeams * kTeamWarps) : kTeamArrivals;
     const int c0 = tw * NKC / 2, c1 = (tw + 1) * NKC / 2;
     const bool bon = g < 2 * (TB == 1 ? 1 : tb);
     const uint32_t xb_a = smem_u32(sm.xs) + (uint32_t)lane * 16u;
     float* red = &sm.out[0][0];  // [team][2][kTB][16]
     int it = 0;
-    for (int s = team; s < nst; s += kTeams, ++it) {
+    for (int s = s0; s < nst; s += ds) {
       const uint32_t gs = c.st + (uint32_t)s;
       const int slot = gs % kStages;
       bool ok = s < kStages || mbar_wait(p, c, &c.hdr->empty[slot], ((gs / kStages) - 1) & 1);
       ok = __all_sync(FULL, ok && mbar_wait(p, c, &c.hdr->full[slot], (gs / kStages) & 1) && !aborted(c));
       const uint32_t st = smem_u32(stage(slot));
-      float d[4][4];
+      for (int gi = g0; gi < ng; gi += dg, ++it) {
+        // gate/up row g and up row g (rows g, R/2 + g), or rows 2g, 2g + 1 of group gi
+        const int rlo = up ? g : R * gi + 2 * g, rhi = up ? R / 2 + g : rlo + 1;
+        float d[4][4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
-      if (ok) {
-        const uint32_t alo = st + (uint32_t)(rlo * (K / 2) + q * 16), ahi = st + (uint32_t)(rhi * (K / 2) + q * 16);
-        const uint32_t blo = st + (uint32_t)(CB + rlo * (K / 16) + q * 2);
-        const uint32_t bhi = st + (uint32_t)(CB + rhi * (K / 16) + q * 2);
-        for (int kc = c0; kc < c1; ++kc) {
-          const uint4 ul = lds128(alo + (uint32_t)(kc * 64)), uh = lds128(ahi + (uint32_t)(kc * 64));
-          // the scales of blocks 2q (MMAs 0-3) and 2q + 1 (MMAs 4-7) of the chunk
-          uint32_t sl, sh, unused;
-          e4m3x4_f16(lds_u16(blo + (uint32_t)(kc * 8)), sl, unused);
-          e4m3x4_f16(lds_u16(bhi + (uint32_t)(kc * 8)), sh, unused);
-          const uint32_t sl0 = half_bcast(sl, 0x1010u), sl1 = half_bcast(sl, 0x3232u);
-          const uint32_t sh0 = half_bcast(sh, 0x1010u), sh1 = half_bcast(sh, 0x3232u);
-          uint4 b[4];
+        for (int j = 0; j < 4; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+        if (ok) {
+          const uint32_t alo = st + (uint32_t)(rlo * (K / 2) + q * 16), ahi = st + (uint32_t)(rhi * (K / 2) + q * 16);
+          const uint32_t blo = st + (uint32_t)(cbytes + rlo * (K / 16) + q * 2);
+          const uint32_t bhi = st + (uint32_t)(cbytes + rhi * (K / 16) + q * 2);
+          for (int kc = c0; kc < c1; ++kc) {
+            const uint4 ul = lds128(alo + (uint32_t)(kc * 64)), uh = lds128(ahi + (uint32_t)(kc * 64));
+            // the scales of blocks 2q (MMAs 0-3) and 2q + 1 (MMAs 4-7) of the chunk
+            uint32_t sl, sh, unused;
+            e4m3x4_f16(lds_u16(blo + (uint32_t)(kc * 8)), sl, unused);
+            e4m3x4_f16(lds_u16(bhi + (uint32_t)(kc * 8)), sh, unused);
+            const uint32_t sl0 = half_bcast(sl, 0x1010u), sl1 = half_bcast(sl, 0x3232u);
+            const uint32_t sh0 = half_bcast(sh, 0x1010u), sh1 = half_bcast(sh, 0x3232u);
+            uint4 b[4];
 #pragma unroll
-          for (int jp = 0; jp < 4; ++jp)
-            b[jp] = bon ? lds128(xb_a + (uint32_t)((kc * 4 + jp) * 256)) : make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t wl[4] = {ul.x, ul.y, ul.z, ul.w}, wh[4] = {uh.x, uh.y, uh.z, uh.w};
+            for (int jp = 0; jp < 4; ++jp)
+              b[jp] = bon ? lds128(xb_a + (uint32_t)((kc * 4 + jp) * 256)) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t wl[4] = {ul.x, ul.y, ul.z, ul.w}, wh[4] = {uh.x, uh.y, uh.z, uh.w};
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            // MMA j: codes 4j .. 4j+3 of the thread's 32 (bytes 2j, 2j+1)
-            const uint32_t cl = (j & 1) ? wl[j >> 1] >> 16 : wl[j >> 1];
-            const uint32_t chh = (j & 1) ? wh[j >> 1] >> 16 : wh[j >> 1];
-            uint32_t a0, a1, a2, a3;
-            e2m1x4_f16(cl, a0, a2);
-            e2m1x4_f16(chh, a1, a3);
-            const uint32_t fl = j < 4 ? sl0 : sl1, fh = j < 4 ? sh0 : sh1;
-            a0 = hmul2(a0, fl);
-            a2 = hmul2(a2, fl);
-            a1 = hmul2(a1, fh);
-            a3 = hmul2(a3, fh);
-            const uint32_t b0 = (j & 1) ? b[j >> 1].z : b[j >> 1].x, b1 = (j & 1) ? b[j >> 1].w : b[j >> 1].y;
-            mma_f16(d[j & 3], a0, a1, a2, a3, b0, b1);
+            for (int j = 0; j < 8; ++j) {
+              // MMA j: codes 4j .. 4j+3 of the thread's 32 (bytes 2j, 2j+1)
+              const uint32_t cl = (j & 1) ? wl[j >> 1] >> 16 : wl[j >> 1];
+              const uint32_t chh = (j & 1) ? wh[j >> 1] >> 16 : wh[j >> 1];
+              uint32_t a0, a1, a2, a3;
+              e2m1x4_f16(cl, a0, a2);
+              e2m1x4_f16(chh, a1, a3);
+              const uint32_t fl = j < 4 ? sl0 : sl1, fh = j < 4 ? sh0 : sh1;
+              a0 = hmul2(a0, fl);
+              a2 = hmul2(a2, fl);
+              a1 = hmul2(a1, fh);
+              a3 = hmul2(a3, fh);
+              const uint32_t b0 = (j & 1) ? b[j >> 1].z : b[j >> 1].x, b1 = (j & 1) ? b[j >> 1].w : b[j >> 1].y;
+              mma_f16(d[j & 3], a0, a1, a2, a3, b0, b1);
+            }
+          }
+        }
+        // columns 2t + {0, 1} of rows g and g + 8: thread q = t holds both
+        float vlo = (d[0][0] + d[1][0]) + (d[2][0] + d[3][0]) + ((d[0][1] + d[1][1]) + (d[2][1] + d[3][1]));
+        float vhi = (d[0][2] + d[1][2]) + (d[2][2] + d[3][2]) + ((d[0][3] + d[1][3]) + (d[2][3] + d[3][3]));
+        float* rb = red + (team * 2 + (it & 1)) * kTB * 16;
+        if (tw == 1 && q < tb) {
+          rb[q * 16 + g] = vlo;
+          rb[q * 16 + 8 + g] = vhi;
+        }
+        bar_sync(kBarTeam0 + team, 2 * 32);
+        if (tw == 0 && q < tb) {
+          vlo += rb[q * 16 + g];
+          vhi += rb[q * 16 + 8 + g];
+          if (ok && !aborted(c)) {
+            const float slo = c.hdr->scl[slot][rlo], shi = c.hdr->scl[slot][rhi];
+            pair_epilogue(op, w, s, up ? g : rlo, rhi, q, vlo * slo, vhi * shi, dslot, dwt);
           }
         }
       }
-      // columns 2t + {0, 1} of rows g and g + 8: thread q = t holds both
-      float vlo = (d[0][0] + d[1][0]) + (d[2][0] + d[3][0]) + ((d[0][1] + d[1][1]) + (d[2][1] + d[3][1]));
-      float vhi = (d[0][2] + d[1][2]) + (d[2][2] + d[3][2]) + ((d[0][3] + d[1][3]) + (d[2][3] + d[3][3]));
-      float* rb = red + (team * 2 + (it & 1)) * kTB * 16;
-      if (tw == 1 && q < tb) {
-        rb[q * 16 + g] = vlo;
-        rb[q * 16 + 8 + g] = vhi;
-      }
-      bar_sync(kBarTeam0 + team, 2 * 32);
-      if (tw == 0 && q < tb) {
-        vlo += rb[q * 16 + g];
-        vhi += rb[q * 16 + 8 + g];
-        if (ok && !aborted(c)) {
-          const float slo = c.hdr->scl[slot][rlo], shi = c.hdr->scl[slot][rhi];
-          pair_epilogue(op, w, s, up ? g : rlo, rhi, q, vlo * slo, vhi * shi, dslot, dwt);
-        }
-      }
       __syncwarp();
-      if (lane == 0) mbar_arrive_n(&c.hdr->empty[slot], kTeamArrivals);
+      if (lane == 0) mbar_arrive_n(&c.hdr->empty[slot], arrivals);
     }
     c.st += (uint32_t)nst;
   }
@@ -2004,11 +2018,8 @@ struct Consumer {
       // The slot's previous use (stage s - kStages) may belong to another
       // team (kStages is not a multiple of kTeams): wait until it is released
       // first, so the parity wait below cannot match a phase two fills back.
-      // (With stats, team 0's waits for its stages count as stage waits.)
-      const int64_t t0 = (p.stats && ct == 0) ? gtimer() : 0;
       bool ok = s < kStages || mbar_wait(p, c, &c.hdr->empty[slot], ((gs / kStages) - 1) & 1);
       ok = __all_sync(FULL, ok && mbar_wait(p, c, &c.hdr->full[slot], (gs / kStages) & 1) && !aborted(c));
-      if (p.stats && ct == 0) c.stat[1] += gtimer() - t0;
       const int rows = min(SR, total_rows - s * SR);
       const int npairs = rows / 2;
       // this warp's pairs [p0, p1): the first half of the stage's pairs, or the second
