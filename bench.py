@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--workload", default="full_bs1_8k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--trace", default="", help="write a Chrome trace of one step here")
+    ap.add_argument("--opts", nargs="*", default=[], metavar="KEY=VALUE",
+                    help="schedule options (mk_sched_opts fields, e.g. wave_order=1 placement=3) for "
+                         "the timed schedule; the line's config names them")
     ap.add_argument("--service", type=int, default=0,
                     help="time G tokens of the host decode service (GPU step, greedy) after an "
                          "8191-token prompt, instead of the contract line")
@@ -265,7 +268,8 @@ def run_mine(args):
     weights = synth.device.device_weights(sh, w.seed, device=dev, router_bias=inp.router_bias)
     kp, vp = synth.device.device_pools(sh, w.seed, inp.num_pages, device=dev)
     model = mk.Model(mk.config_from(sh), mk.weights_from(weights), keepalive=weights)
-    sched = mk.Sched(model, w.batch, int(inp.seq_lens.max()))
+    sched_opts = {k: int(v) for k, v in (o.split("=", 1) for o in args.opts)}
+    sched = mk.Sched(model, w.batch, int(inp.seq_lens.max()), mk.default_sched_opts(**sched_opts))
     sess = mk.Session(model, sched, device=dev)
     stream = torch.cuda.current_stream(dev)
     tok = torch.as_tensor(inp.tokens, device=dev)
@@ -340,11 +344,12 @@ def run_mine(args):
     mean_ms = total_ms / K
     peak, peak_kind = measured_peaks()
     achieved = alg / (mean_ms / 1e3) / 1e9
-    traffic = recorded_traffic(args.workload)
+    # (the recorded traffic is the default schedule's)
+    traffic = recorded_traffic(args.workload) if not sched_opts else None
 
     if args.trace:
         from moe_decode_megakernel_gb300 import trace as mktrace
-        tsched = mk.Sched(model, w.batch, int(inp.seq_lens.max()), mk.default_sched_opts(trace=1))
+        tsched = mk.Sched(model, w.batch, int(inp.seq_lens.max()), mk.default_sched_opts(trace=1, **sched_opts))
         tsess = mk.Session(model, tsched, device=dev)
         for _ in range(3):
             tsess.step(tok, sl, bt, kp, vp, logits)
@@ -366,7 +371,7 @@ def run_mine(args):
             "ms_per_step_median": statistics.median(step_ms),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": dtype_text(sh), "data": "synthetic",
-            "config": workload_config(w, inp),
+            "config": dict(workload_config(w, inp), **({"sched_opts": sched_opts} if sched_opts else {})),
             "hbm_bytes_per_step": alg, "achieved_TBps": achieved / 1e3,
             "frac_of_sol_8TBps": achieved / 1e3 / SOL_TBPS,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
