@@ -125,10 +125,12 @@ void mk_free_model(mk_model* m);
 #define MK_WAVES_MOE_FIRST 3   /* up/gate tiles ahead of attention on each SM */
 #define MK_WAVES_MOE_FIRST_O 4 /* the same, with O-proj ahead of the down tiles */
 #define MK_WAVES_O_BEFORE_DOWN 5 /* attention, merge, up/gate, O-proj, then the down tiles */
+#define MK_WAVES_INTERLEAVED_O 6 /* attention, up/gate, merge, O-proj, then the down tiles */
 
 typedef struct {
   int32_t num_sms;          /* SMs to schedule for; 0 = the current device's count */
-  int32_t wave_order;       /* MK_WAVES_* */
+  int32_t wave_order;       /* MK_WAVES_*; -1 (default): MK_WAVES_DEFAULT for max_batch <= 2,
+                               the fastest measured order of the tensor-core build above */
   int32_t attn_split_pages; /* KV pages per attention task; 0 = choose from the context */
   int32_t attn_claimers;    /* ATTN_DRAIN claimers per full-attention layer; 0 = auto */
   int32_t moe_claimers;     /* claimers per MoE drain per layer; 0 = auto */

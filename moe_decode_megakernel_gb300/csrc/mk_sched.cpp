@@ -753,6 +753,9 @@ static int build(mk_sched* s) {
       case MK_WAVES_MOE_FIRST_O:
         add(w_up); add(w_attn); add(w_acomb); add(w_o); add(w_dn); add(w_mcomb);
         break;
+      case MK_WAVES_INTERLEAVED_O:
+        add(w_attn); add(w_up); add(w_acomb); add(w_o); add(w_dn); add(w_mcomb);
+        break;
       case MK_WAVES_O_BEFORE_DOWN:
         add(w_attn); add(w_acomb); add(w_up); add(w_o); add(w_dn); add(w_mcomb);
         break;
@@ -1137,10 +1140,17 @@ static void build_attn_queue(const mk_sched* s, int B, const int32_t* seq, std::
 
 using namespace mk;
 
+// The tensor-core schedules' default wave order: there most expert tiles
+// are GEMV or tcgen05 items that can stream while the attention slices wait
+// for their queries, so the MoE waves go right behind the slices (ragged
+// batch 32: 10.9 ms interleaved against 12.0 ms in the batch-1 order).
+constexpr int kTcWaveOrder = MK_WAVES_INTERLEAVED;
+
 extern "C" {
 
 void mk_default_sched_opts(mk_sched_opts* o) {
   std::memset(o, 0, sizeof(*o));
+  o->wave_order = -1;
   o->fuse_finalize = 1;
   o->fuse_moe_combine = 1;
   o->moe_static = -1;
@@ -1195,7 +1205,8 @@ int mk_build_tasks(const mk_model* m, int32_t max_batch, int32_t max_ctx, const 
       return fail(MK_ERR_CUDA, "cannot query the SM count (no device?); pass opts.num_sms");
     }
   }
-  if (s->opts.wave_order < 0 || s->opts.wave_order > 5) {
+  if (s->opts.wave_order == -1) s->opts.wave_order = s->tc ? kTcWaveOrder : MK_WAVES_DEFAULT;
+  if (s->opts.wave_order < 0 || s->opts.wave_order > 6) {
     delete s;
     return fail(MK_ERR_ARG, "unknown wave order");
   }

@@ -74,7 +74,7 @@ def sched_for(workload, **opts):
 
 
 @pytest.mark.parametrize("workload", ["tiny", "small", "full_bs1_8k", "batch32_ragged"])
-@pytest.mark.parametrize("order", [0, 1, 2, 3, 4, 5])
+@pytest.mark.parametrize("order", [0, 1, 2, 3, 4, 5, 6])
 def test_schedules_validate_and_simulate(workload, order):
     m, s, inp = sched_for(workload, wave_order=order)
     s.validate()

@@ -49,7 +49,7 @@ def test_full_bs1_8k(workload):
     assert parity.compare_queue(inp, g) == 48
 
 
-@pytest.mark.parametrize("order", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("order", [1, 2, 3, 4, 5, 6])
 def test_wave_orders_bit_identical(order):
     """Any schedule without a cyclic wait computes the same step ("all these
     schedules produce correct outputs"); reductions have a fixed order, so
