@@ -139,10 +139,14 @@ int auto_split_pages(const mk_sched* s) {
   if (s->opts.attn_split_pages > 0) return s->opts.attn_split_pages;
   const int P = s->cfg.page_size;
   // about one KV slice per SM for a full-attention layer at the largest batch and context
-  // (full shape, batch 1, 8K: 4 pages; 2 pages, twice the slices to merge, measured 3% slower)
+  // (full shape, batch 1, 8K: 4 pages; 2 pages, twice the slices to merge, measured 3% slower),
+  // and no slice above 1 MB of K/V: one SM streams such a slice for 15 us or more, so larger
+  // ones leave the SMs unbalanced (ragged batch 32 at up to 32K: 10.9 ms with 64-page slices,
+  // 10.0 ms with 32-page ones; ragged batch 64 at up to 64K: 24.1 and 24.4 ms)
   const double tok = (double)s->max_batch * s->cfg.n_kv * s->max_ctx / (double)s->num_sms;
+  const int most = std::max(1, std::min(64, (int)((1 << 20) / ((int64_t)P * s->cfg.head_dim * 2 * 2))));
   int pages = (int)((tok + P - 1) / P);
-  return std::max(1, std::min(pages, 64));
+  return std::max(1, std::min(pages, most));
 }
 
 // Static MoE claims by readiness: the claimer of rank r takes units r, r + n,
