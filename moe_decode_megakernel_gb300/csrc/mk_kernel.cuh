@@ -2822,20 +2822,22 @@ struct Consumer {
       }
       __syncwarp();
     }
-    unsigned long long m[PL];
-#pragma unroll
-    for (int k = 0; k < PL; ++k) m[k] = 0ull;
-    for (int i = 0; i < n; ++i) {
+    // each expert's rows as a bit mask (bit b: row b routes to it), the
+    // warp's lanes taking every 32nd routed slot
+    for (int e = lane; e < E; e += 32) sm.mask[e] = 0ull;
+    __syncwarp();
+    for (int i = lane; i < n; i += 32) {
       int e = sm.ids[i];
       if (e < 0 || e >= E) {
-        if (lane == 0) record_error(p, ERR_INDEX, c.sm, kNowhere, -1, (uint32_t)e, E);
+        record_error(p, ERR_INDEX, c.sm, kNowhere, -1, (uint32_t)e, E);
         e = 0;
       }
-      const unsigned long long bit = 1ull << (i / K);
-#pragma unroll
-      for (int k = 0; k < PL; ++k)
-        if (e == lane * PL + k) m[k] |= bit;
+      atomicOr(&sm.mask[e], 1ull << (i / K));
     }
+    __syncwarp();
+    unsigned long long m[PL];
+#pragma unroll
+    for (int k = 0; k < PL; ++k) m[k] = lane * PL + k < E ? sm.mask[lane * PL + k] : 0ull;
     int cnt[PL], a[PL];
     int rs = 0, as = 0;
 #pragma unroll
