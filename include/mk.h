@@ -130,7 +130,8 @@ void mk_free_model(mk_model* m);
 typedef struct {
   int32_t num_sms;          /* SMs to schedule for; 0 = the current device's count */
   int32_t wave_order;       /* MK_WAVES_*; -1 (default): MK_WAVES_DEFAULT for max_batch <= 2,
-                               the fastest measured order of the tensor-core build above */
+                               above it (the tensor-core build) MK_WAVES_O_BEFORE_DOWN up to 8
+                               rows and MK_WAVES_INTERLEAVED beyond: the fastest measured */
   int32_t attn_split_pages; /* KV pages per attention task; 0 = choose from the context */
   int32_t attn_claimers;    /* ATTN_DRAIN claimers per full-attention layer; 0 = auto */
   int32_t moe_claimers;     /* claimers per MoE drain per layer; 0 = auto */

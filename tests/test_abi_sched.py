@@ -367,17 +367,18 @@ def _lists(s):
 
 
 @pytest.mark.parametrize("workload,batch,order", [("small", 1, 0), ("full_bs2_8k", 2, 0),
-                                                  ("full_bs4_8k", 4, 1), ("batch32_ragged", 32, 1)])
+                                                  ("full_bs4_8k", 4, 5), ("batch32_ragged", 32, 1)])
 def test_default_wave_order_per_build(workload, batch, order):
     """wave_order -1 (the default) takes the pages' order for batch <= 2
-    schedules and the interleaved order for the tensor-core schedules: the
-    task lists equal those of the explicit order."""
+    schedules and, for the tensor-core schedules, O-proj before the down
+    tiles up to 8 rows and the interleaved order beyond: the task lists equal
+    those of the explicit order."""
     w = synth.WORKLOADS[workload]
     inp = synth.make_inputs(w)
     m = fake_model(w.shape)
     ctx = int(inp.seq_lens.max())
     auto = mk.Sched(m, batch, ctx, mk.default_sched_opts(num_sms=NUM_SMS))
     explicit = mk.Sched(m, batch, ctx, mk.default_sched_opts(num_sms=NUM_SMS, wave_order=order))
-    other = mk.Sched(m, batch, ctx, mk.default_sched_opts(num_sms=NUM_SMS, wave_order=1 - order))
+    other = mk.Sched(m, batch, ctx, mk.default_sched_opts(num_sms=NUM_SMS, wave_order=2))
     assert _lists(auto) == _lists(explicit)
     assert _lists(auto) != _lists(other)
