@@ -79,3 +79,23 @@ def test_full_shape_four_seeds(workload, n_rows):
         parity.release()
     print(f"{workload}: greedy agreement {exact}/{total}, worst logit rel err {worst:.2e}")
     assert exact / total >= GREEDY_MIN
+
+
+def test_fp8_tensor_core_fifty_seeds():
+    """FP8 experts above two rows (the tensor-core build's E4M3-term expert
+    tiles and, for experts with one or two rows, the FP8 GEMV): 50 seeds of
+    the small FP8 shape at a ragged batch of 16, every row against the oracle."""
+    exact = total = 0
+    worst = router = 0.0
+    for k in range(50):
+        inp = _reseed("small_fp8_b16", 9000 + k)
+        rep = parity.compare(inp, parity.run_gpu(inp))
+        _check_sample(rep)
+        exact += rep.greedy_exact
+        total += rep.greedy_total
+        worst = max(worst, rep.max_rel_err)
+        router = max(router, float(rep.router_err.max()))
+    print(f"small_fp8_b16: greedy agreement {exact}/{total}, worst logit rel err {worst:.2e}, "
+          f"worst router err {router:.2e}")
+    assert exact / total >= GREEDY_MIN
+    parity.release()
