@@ -235,3 +235,74 @@ def test_service_matches_oracle_over_many_steps(name, num_pages, max_pages):
             assert same >= 0.9, same  # most entries round to the same BF16 value
     print(f"{name}: {steps} service steps, greedy agreement {exact}/{total}, worst K/V error {kv_worst:.2e}")
     assert exact >= 0.99 * total
+
+
+def test_service_four_sequences_tensor_core_steps():
+    """Four sequences decoded together on the small shape (a schedule of 4
+    rows: the tensor-core build, its QKV epilogue appending every K/V; the
+    2-row schedule once two have finished) over 30+ steps.  Every step is
+    replayed by the oracle over the K/V history the GPU wrote (each position
+    is written once), so each comparison is of one step: the oracle's new K/V
+    against what the GPU wrote at that position (each head vector within the
+    logits' tolerance of its largest entry), and its greedy token against the
+    GPU's sample (teacher-forced; near-ties within the tolerance either way)."""
+    import oracle
+    import parity
+    sh, seed, num_pages, max_pages = synth.MODELS["small"], 41, 16, 3
+    w = synth.device.device_weights(sh, seed)
+    model = mk.Model(mk.config_from(sh), mk.weights_from(w), keepalive=w)
+    kp, vp = synth.device.device_pools(sh, seed, num_pages)
+    ctx = max_pages * sh.page_size
+    gstep = sv.GpuStep(model, [mk.Sched(model, 2, ctx), mk.Sched(model, 4, ctx)], kp, vp, max_pages)
+    svc = sv.Service(num_pages, sh.page_size, max_pages, 4, gstep)
+    rng = np.random.default_rng(13)
+    lens, new = {1: 3, 2: 11, 3: 6, 4: 17}, {1: 24, 2: 18, 3: 30, 4: 12}
+    prompts = {sid: rng.integers(0, sh.vocab, n).tolist() for sid, n in lens.items()}
+    for sid in prompts:
+        svc.add(sid, prompts[sid], max_new=new[sid])
+    pages, out, steps = {}, {sid: [] for sid in prompts}, 0
+    while True:
+        for sid in prompts:
+            if svc.query(sid).state != sv.FINISHED:
+                pages[sid] = svc.pages(sid)
+        rows, toks = svc.step()
+        if rows == 0:
+            break
+        steps += 1
+        for sid, t in toks:
+            out[sid].append(t)
+    assert steps >= 30 and all(len(out[sid]) == new[sid] for sid in prompts)
+    torch.cuda.synchronize()
+    kg, vg = kp.cpu().numpy(), vp.cpu().numpy()
+    P = sh.page_size
+    exact = total = 0
+    kv_worst = 0.0
+    for sid in prompts:
+        ko, vo = kg.copy(), vg.copy()  # the GPU's history; each position is compared, then restored
+        bt = np.full((1, max_pages), -1, np.int32)
+        bt[0, :len(pages[sid])] = pages[sid]
+        feed, n_ctx, k = list(prompts[sid]), 0, 0
+        while k < len(out[sid]):
+            tok = feed.pop(0)
+            r = oracle.decode_step(sh, seed, np.array([tok], np.int32), np.array([n_ctx + 1], np.int32), bt,
+                                   pools=(ko, vo))
+            pg, off = bt[0, n_ctx // P], n_ctx % P
+            for gpool, opool in ((kg, ko), (vg, vo)):
+                gv = synth.bf16_bits_to_f32(gpool[:, pg, :, off, :])  # [layer][head][d]
+                ov = synth.bf16_bits_to_f32(opool[:, pg, :, off, :])
+                err = np.max(np.abs(gv - ov), axis=-1) / np.max(np.abs(ov), axis=-1)
+                kv_worst = max(kv_worst, float(err.max()))
+                assert err.max() <= parity.LOGIT_TOL, (sid, n_ctx, float(err.max()))
+                opool[:, pg, :, off, :] = gpool[:, pg, :, off, :]
+            n_ctx += 1
+            if not feed:
+                g_tok, o = out[sid][k], r.logits[0]
+                oa = int(np.argmax(o))
+                exact += g_tok == oa
+                total += 1
+                assert g_tok == oa or o[oa] - o[g_tok] <= 2 * parity.LOGIT_TOL * np.max(np.abs(o)), (sid, k)
+                k += 1
+                feed.append(g_tok)
+    print(f"small, 4 sequences: {steps} service steps, greedy agreement {exact}/{total}, "
+          f"worst one-step K/V error {kv_worst:.2e}")
+    assert exact >= 0.99 * total
