@@ -150,6 +150,8 @@ WORKLOADS = {
                              desc="small shape with FP8 experts: 8 layers, B=2, seq_lens U[1,1024]"),
     "full_fp8_bs1_8k": Workload("full_fp8_bs1_8k", "full_fp8", 1, ("fixed", 8192), 3,
                                 desc="full shape with FP8 experts, B=1, context 8192"),
+    "full_fp8_bs2_8k": Workload("full_fp8_bs2_8k", "full_fp8", 2, ("fixed", 8192), 16,
+                                desc="full shape with FP8 experts, B=2, context 8192"),
     # FP8 experts above batch 2: the tensor-core build's FP8 expert tiles
     "small_fp8_b16": Workload("small_fp8_b16", "small_fp8", 16, ("uniform", 1, 1024), 18,
                               desc="small shape with FP8 experts: 8 layers, B=16, seq_lens U[1,1024]"),
@@ -162,6 +164,8 @@ WORKLOADS = {
                              desc="small shape with FP4 experts: 8 layers, B=2, seq_lens U[1,1024]"),
     "full_fp4_bs1_8k": Workload("full_fp4_bs1_8k", "full_fp4", 1, ("fixed", 8192), 3,
                                 desc="full shape with FP4 experts, B=1, context 8192"),
+    "full_fp4_bs2_8k": Workload("full_fp4_bs2_8k", "full_fp4", 2, ("fixed", 8192), 16,
+                                desc="full shape with FP4 experts, B=2, context 8192"),
     # seeded, non-unit RMSNorm gains (every layer's and the final norm's)
     "tiny_gains": Workload("tiny_gains", "tiny", 1, ("fixed", 64), 31, gains=True,
                            desc="tiny with seeded RMSNorm gains in [0.5, 2)"),

@@ -26,7 +26,7 @@ def test_device_codes_match_host():
     assert np.array_equal(got, synth.fill_scales4_host(sh.hidden, 14, synth.SD, 3, 5, sh.weight_sigma))
 
 
-@pytest.mark.parametrize("workload", ["small_fp4", "small_fp4_b2", "full_fp4_bs1_8k"])
+@pytest.mark.parametrize("workload", ["small_fp4", "small_fp4_b2", "full_fp4_bs1_8k", "full_fp4_bs2_8k"])
 def test_fp4_against_oracle(workload):
     inp = synth.make_inputs(workload)
     g = parity.run_gpu(inp)

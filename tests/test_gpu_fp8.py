@@ -26,7 +26,7 @@ def test_device_codes_match_host():
     assert np.array_equal(got, synth.fill_scales_host(sh.inter, 12, synth.SU, 3, 5, sh.weight_sigma))
 
 
-@pytest.mark.parametrize("workload", ["small_fp8", "small_fp8_b2", "full_fp8_bs1_8k"])
+@pytest.mark.parametrize("workload", ["small_fp8", "small_fp8_b2", "full_fp8_bs1_8k", "full_fp8_bs2_8k"])
 def test_fp8_against_oracle(workload):
     inp = synth.make_inputs(workload)
     g = parity.run_gpu(inp)
